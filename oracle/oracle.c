@@ -1,0 +1,324 @@
+/*
+ * CPU oracle for the block-quantized-weight matmul.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the GPU path computes.  Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg may load it.  It shares no code,
+ * header, table or helper with the CUDA library, and the CUDA library never
+ * calls it.
+ *
+ * Arithmetic: dequantized weights in f32 (exact by construction), products
+ * and sums in f64 in k order, one final rounding to the output type.
+ *
+ * Sources (pages of the reference material, by title and section):
+ *  - Q4 split-plane format: "oxinfer 0.0.5 src/metal.rs", shader section
+ *    "Dequantizers" (struct Q4W, nib_lo / nib_hi and load(Q4W ...)): block b
+ *    of row n is 16 bytes at n*K/2 + 16*b; byte i holds element i in its low
+ *    nibble and element 16+i in its high nibble; value = (nibble - 8) * d,
+ *    d the fp16 block scale at n*(K/32) + b.  The same order is restated by
+ *    the GGUF Q4_0 decoder on the same page (load(Q4_0W ...)).
+ *  - Q8-row format: "cortiq-engine 0.8.3 src/gpu_metal/qi21.rs", module
+ *    header (q8_row: int8 weights, row scale on the f32 result).
+ *  - GEMM reference shape (dequantize, then an f64 dot product per output):
+ *    "oxinfer 0.0.5 src/metal.rs", tests module, functions dense / matvec.
+ *  - MoE chain (per token and routed expert: gate/up, SiLU(g)*u, down, the
+ *    weighted sum): same tests module, mma_moe_matches_cpu; SiLU as
+ *    g/(1+exp(-g)) from the silu_half shader.  Expert-major grouping of the
+ *    routed rows, token order inside an expert: same page, Backend::moe.
+ *
+ * Every function is single-purpose; the only parallelism is OpenMP over
+ * independent outputs, which leaves each output's arithmetic unchanged.
+ *
+ * Pins (tests marked "not gpu"): hand-built blocks for the dequantizers,
+ * exact rational brute force and a library f64 matmul for the GEMM, closed
+ * forms and invariants for the MoE chain and the layout.  No function here
+ * is left without a pin.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- number formats, from the IEEE 754 binary16 and bfloat16 definitions ---- */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Subnormals are fraction * 2^-24; exponent 31 is inf/NaN. */
+double or_f16_to_f64(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int f = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of a binary32. */
+double or_bf16_to_f64(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* Round an f64 to bfloat16 once, to nearest with ties to even.
+ * bfloat16 keeps 8 significant bits, the smallest normal is 2^-126 and the
+ * subnormal quantum 2^-133. */
+uint16_t or_f64_to_bf16(double x) {
+    if (isnan(x)) return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7F80;
+    int e;
+    frexp(a, &e);                      /* a = m * 2^e, m in [0.5, 1) */
+    int qexp = e - 8;                  /* weight of the last kept bit */
+    if (qexp < -133) qexp = -133;
+    double r = nearbyint(ldexp(a, -qexp));   /* default mode: ties to even */
+    double v = ldexp(r, qexp);
+    if (v >= ldexp(1.0, 128)) return sign | 0x7F80;
+    float f = (float)v;                /* exact: v has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return sign | (uint16_t)(u >> 16);
+}
+
+void or_f64_to_bf16_array(const double* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; i++) out[i] = or_f64_to_bf16(x[i]);
+}
+
+void or_f64_to_f32_array(const double* x, int64_t n, float* out) {
+    for (int64_t i = 0; i < n; i++) out[i] = (float)x[i];   /* RNE in the default mode */
+}
+
+/* X as stored (fp16 or bf16 bits) -> f64, exact. */
+void or_x_to_f64(const uint16_t* x, int is_bf16, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; i++) out[i] = is_bf16 ? or_bf16_to_f64(x[i]) : or_f16_to_f64(x[i]);
+}
+
+/* ---- Q4 packing and dequantization ---- */
+
+/* codes[N][K] (0..15) -> Wq[N][K/2]: byte 16b+i of row n holds
+ * codes[n][32b+i] in its low nibble and codes[n][32b+16+i] in its high one. */
+void or_pack_q4(const uint8_t* codes, int64_t N, int64_t K, uint8_t* wq) {
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < K / 32; b++)
+            for (int i = 0; i < 16; i++) {
+                uint8_t lo = codes[n * K + 32 * b + i] & 15;
+                uint8_t hi = codes[n * K + 32 * b + 16 + i] & 15;
+                wq[n * (K / 2) + 16 * b + i] = (uint8_t)(lo | (hi << 4));
+            }
+}
+
+/* W[n][32b+i] = (lo(byte) - 8) * d, W[n][32b+16+i] = (hi(byte) - 8) * d,
+ * d = f32(fp16 scale).  The f32 product of a 4-bit integer and an 11-bit
+ * significand is exact, so W is exact (the sign of zero follows IEEE). */
+void or_dequant_q4(const uint8_t* wq, const uint16_t* ws, int64_t N, int64_t K, float* w) {
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < K / 32; b++) {
+            float d = (float)or_f16_to_f64(ws[n * (K / 32) + b]);
+            for (int i = 0; i < 16; i++) {
+                uint8_t byte = wq[n * (K / 2) + 16 * b + i];
+                w[n * K + 32 * b + i] = (float)((int)(byte & 15) - 8) * d;
+                w[n * K + 32 * b + 16 + i] = (float)((int)(byte >> 4) - 8) * d;
+            }
+        }
+}
+
+/* Q8-row as a dense f32 matrix: W[n][k] = (float)q[n][k] * rs[n] (one f32
+ * rounding).  The GEMM below uses the unscaled integers and applies rs to
+ * the f64 sum instead, which is the format's own statement (row scale on
+ * the result). */
+void or_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, int64_t K, float* w) {
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++) w[n * K + k] = (float)wq[n * K + k] * rs[n];
+}
+
+/* ---- GEMM ---- */
+
+/* Y[t][n] = sum_k W[n][k] * X[t][k] in f64, k ascending.  S[t][n] is the
+ * error-bound denominator sum_k |W[n][k] * X[t][k]|.  W[N][K] f32, X[T][K]
+ * f64 (the exact stored activations).  rowscale (nullable) multiplies each
+ * output row n's sums (Q8-row). */
+void or_gemm(const float* W, const double* X, int64_t T, int64_t N, int64_t K,
+             const float* rowscale, double* Y, double* S) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t t = 0; t < T; t++)
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0, abs_acc = 0.0;
+            const float* wr = W + n * K;
+            const double* xr = X + t * K;
+            for (int64_t k = 0; k < K; k++) {
+                double p = (double)wr[k] * xr[k];
+                acc += p;
+                abs_acc += fabs(p);
+            }
+            double r = rowscale ? (double)rowscale[n] : 1.0;
+            Y[t * N + n] = acc * r;
+            if (S) S[t * N + n] = abs_acc * fabs(r);
+        }
+}
+
+/* The same sums for a list of (t, n) output positions only. */
+void or_gemm_sampled(const float* W, const double* X, int64_t N, int64_t K,
+                     const float* rowscale, const int64_t* tn, int64_t count, double* Y, double* S) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < count; i++) {
+        int64_t t = tn[2 * i], n = tn[2 * i + 1];
+        double acc = 0.0, abs_acc = 0.0;
+        for (int64_t k = 0; k < K; k++) {
+            double p = (double)W[n * K + k] * X[t * K + k];
+            acc += p;
+            abs_acc += fabs(p);
+        }
+        double r = rowscale ? (double)rowscale[n] : 1.0;
+        (void)N;
+        Y[i] = acc * r;
+        S[i] = abs_acc * fabs(r);
+    }
+}
+
+/* Q4 GEMM on packed rows, for sampled outputs at full size: dequantizes
+ * only the rows it needs, one at a time (same arithmetic as or_dequant_q4
+ * followed by or_gemm_sampled). */
+void or_gemm_q4_sampled(const uint8_t* wq, const uint16_t* ws, const double* X, int64_t N, int64_t K,
+                        const int64_t* tn, int64_t count, double* Y, double* S) {
+#pragma omp parallel
+    {
+        float* row = (float*)malloc(sizeof(float) * (size_t)K);
+#pragma omp for schedule(static)
+        for (int64_t i = 0; i < count; i++) {
+            int64_t t = tn[2 * i], n = tn[2 * i + 1];
+            or_dequant_q4(wq + n * (K / 2), ws + n * (K / 32), 1, K, row);
+            double acc = 0.0, abs_acc = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double p = (double)row[k] * X[t * K + k];
+                acc += p;
+                abs_acc += fabs(p);
+            }
+            Y[i] = acc;
+            S[i] = abs_acc;
+        }
+        free(row);
+    }
+    (void)N;
+}
+
+void or_gemm_q8_sampled(const int8_t* wq, const float* rs, const double* X, int64_t N, int64_t K,
+                        const int64_t* tn, int64_t count, double* Y, double* S) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < count; i++) {
+        int64_t t = tn[2 * i], n = tn[2 * i + 1];
+        double acc = 0.0, abs_acc = 0.0;
+        for (int64_t k = 0; k < K; k++) {
+            double p = (double)wq[n * K + k] * X[t * K + k];
+            acc += p;
+            abs_acc += fabs(p);
+        }
+        Y[i] = acc * (double)rs[n];
+        S[i] = abs_acc * fabs((double)rs[n]);
+    }
+    (void)N;
+}
+
+/* ---- MoE expert panels ---- */
+
+/* Routed (t, j) pairs grouped by expert: seg[e] = number of pairs routed to
+ * experts below e (seg[E] = T*topk), and perm lists pair ids p = t*topk + j
+ * sorted by (expert, t, j).  Returns -1 if an index is out of range. */
+int or_moe_layout(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* perm, int32_t* seg) {
+    int64_t P = T * topk;
+    int64_t* count = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    for (int64_t p = 0; p < P; p++) {
+        if (idx[p] < 0 || idx[p] >= E) { free(count); return -1; }
+        count[idx[p]]++;
+    }
+    seg[0] = 0;
+    for (int64_t e = 0; e < E; e++) seg[e + 1] = seg[e] + (int32_t)count[e];
+    int64_t* fill = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    for (int64_t p = 0; p < P; p++) {          /* pairs in (t, j) order: stable */
+        int32_t e = idx[p];
+        perm[seg[e] + fill[e]] = (int32_t)p;
+        fill[e]++;
+    }
+    free(count);
+    free(fill);
+    return 0;
+}
+
+/* One routed pair: o = Wd[e] . (silu(Wgate[e] . x) * (Wup[e] . x)), all f64.
+ * wgu[2I][H] f32 (rows 0..I-1 gate, I..2I-1 up), wd[H][I] f32, x[H] f64.
+ * a_out[I] (nullable) receives the SwiGLU activation; o[H], sabs[H] the
+ * expert output and sum_k |Wd[n][k] * a[k]|. */
+void or_moe_pair(const float* wgu, const float* wd, const double* x, int64_t H, int64_t I,
+                 double* a_out, double* o, double* sabs) {
+    double* a = (double*)malloc(sizeof(double) * (size_t)I);
+    for (int64_t i = 0; i < I; i++) {
+        double g = 0.0, u = 0.0;
+        for (int64_t k = 0; k < H; k++) g += (double)wgu[i * H + k] * x[k];
+        for (int64_t k = 0; k < H; k++) u += (double)wgu[(I + i) * H + k] * x[k];
+        a[i] = g / (1.0 + exp(-g)) * u;
+        if (a_out) a_out[i] = a[i];
+    }
+    for (int64_t n = 0; n < H; n++) {
+        double acc = 0.0, abs_acc = 0.0;
+        for (int64_t k = 0; k < I; k++) {
+            double p = (double)wd[n * I + k] * a[k];
+            acc += p;
+            abs_acc += fabs(p);
+        }
+        o[n] = acc;
+        sabs[n] = abs_acc;
+    }
+    free(a);
+}
+
+/* Full MoE output: Y[t] = sum_j w[t][j] * o(t, j), j ascending, and the
+ * bound S[t] = sum_j |w[t][j]| * sabs(t, j).  Experts' dequantized weights
+ * are looked up per pair from the packed planes (only touched experts are
+ * decoded).  X[T][H] f64.  Returns -1 on an out-of-range index. */
+int or_moe(const double* X, int64_t T, int64_t H, int64_t E, int64_t I, int64_t topk,
+           const int32_t* idx, const float* w,
+           const uint8_t* gu_q, const uint16_t* gu_s, const uint8_t* d_q, const uint16_t* d_s,
+           double* Y, double* S) {
+    for (int64_t p = 0; p < T * topk; p++)
+        if (idx[p] < 0 || idx[p] >= E) return -1;
+    /* decode each touched expert once */
+    float** gu = (float**)calloc((size_t)E, sizeof(float*));
+    float** dn = (float**)calloc((size_t)E, sizeof(float*));
+    for (int64_t p = 0; p < T * topk; p++) {
+        int64_t e = idx[p];
+        if (gu[e]) continue;
+        gu[e] = (float*)malloc(sizeof(float) * (size_t)(2 * I * H));
+        dn[e] = (float*)malloc(sizeof(float) * (size_t)(H * I));
+        or_dequant_q4(gu_q + e * (2 * I) * (H / 2), gu_s + e * (2 * I) * (H / 32), 2 * I, H, gu[e]);
+        or_dequant_q4(d_q + e * H * (I / 2), d_s + e * H * (I / 32), H, I, dn[e]);
+    }
+    double* o = (double*)malloc(sizeof(double) * (size_t)(T * topk * H));
+    double* sa = (double*)malloc(sizeof(double) * (size_t)(T * topk * H));
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t p = 0; p < T * topk; p++) {
+        int64_t t = p / topk, e = idx[p];
+        or_moe_pair(gu[e], dn[e], X + t * H, H, I, NULL, o + p * H, sa + p * H);
+    }
+    for (int64_t t = 0; t < T; t++)
+        for (int64_t n = 0; n < H; n++) {
+            double y = 0.0, s = 0.0;
+            for (int64_t j = 0; j < topk; j++) {
+                int64_t p = t * topk + j;
+                y += (double)w[p] * o[p * H + n];
+                s += fabs((double)w[p]) * sa[p * H + n];
+            }
+            Y[t * H + n] = y;
+            S[t * H + n] = s;
+        }
+    for (int64_t e = 0; e < E; e++) { free(gu[e]); free(dn[e]); }
+    free(gu); free(dn); free(o); free(sa);
+    return 0;
+}

@@ -1,0 +1,81 @@
+"""Plausible mistakes planted in a copy of the oracle must fail the pins.
+
+Each mutant is a text edit of oracle.c compiled into a temporary library;
+the hand-built blocks and the addressing pin are then run against it.
+"""
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+from test_oracle import _golden_blocks
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oracle.c")
+
+MUTANTS = {
+    "nibbles_swapped": ("(int)(byte & 15) - 8) * d;\n                w[n * K + 32 * b + 16 + i] = (float)((int)(byte >> 4)",
+                        "(int)(byte >> 4) - 8) * d;\n                w[n * K + 32 * b + 16 + i] = (float)((int)(byte & 15)"),
+    "offset_7": ("(float)((int)(byte & 15) - 8)", "(float)((int)(byte & 15) - 7)"),
+    "scale_index_drops_row": ("ws[n * (K / 32) + b]", "ws[b]"),
+    "interleaved_elements": ("w[n * K + 32 * b + 16 + i]", "w[n * K + 32 * b + 2 * (i % 8) + 1 + 16 * (i / 8)]"),
+    "subnormal_flush": ("v = ldexp((double)f, -24);", "v = 0.0;"),
+}
+
+
+def _build_mutant(name, tmp):
+    src = open(SRC).read()
+    old, new = MUTANTS[name]
+    assert old in src, name
+    path = os.path.join(tmp, f"{name}.c")
+    open(path, "w").write(src.replace(old, new, 1))
+    so = os.path.join(tmp, f"{name}.so")
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", path, "-o", so, "-lm"])
+    return ctypes.CDLL(so)
+
+
+def _dequant(lib, wq, ws, N, K):
+    out = np.empty((N, K), np.float32)
+    lib.or_dequant_q4(ctypes.c_void_p(wq.ctypes.data), ctypes.c_void_p(ws.ctypes.data),
+                      ctypes.c_int64(N), ctypes.c_int64(K), ctypes.c_void_p(out.ctypes.data))
+    return out
+
+
+def _pins_pass(lib):
+    for name, sbits, sval, raw, m in _golden_blocks():
+        wq = np.frombuffer(raw, np.uint8).reshape(1, 16).copy()
+        ws = np.array([[sbits]], np.uint16)
+        got = _dequant(lib, wq, ws, 1, 32)[0]
+        exp = np.array([mi * sval for mi in m], np.float64).astype(np.float32)
+        if not np.array_equal(got.view(np.uint32), exp.view(np.uint32)):
+            return False
+    # two rows x two blocks with distinct scales (the addressing pin)
+    blocks = {b[0]: b for b in _golden_blocks()}
+    grid = [["ramp_one", "pos03"], ["ramp_ncent", "pos20"]]
+    wq = np.zeros((2, 32), np.uint8)
+    ws = np.zeros((2, 2), np.uint16)
+    exp = np.zeros((2, 64), np.float32)
+    for n in range(2):
+        for b in range(2):
+            _, sb, sv, raw, m = blocks[grid[n][b]]
+            wq[n, 16 * b:16 * b + 16] = np.frombuffer(raw, np.uint8)
+            ws[n, b] = sb
+            exp[n, 32 * b:32 * b + 32] = np.array([mi * sv for mi in m], np.float32)
+    return np.array_equal(_dequant(lib, wq, ws, 2, 64).view(np.uint32), exp.view(np.uint32))
+
+
+def test_unmutated_copy_passes():
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "orig.c")
+        open(path, "w").write(open(SRC).read())
+        so = os.path.join(tmp, "orig.so")
+        subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", path, "-o", so, "-lm"])
+        assert _pins_pass(ctypes.CDLL(so))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_fails_pins(name):
+    with tempfile.TemporaryDirectory() as tmp:
+        assert not _pins_pass(_build_mutant(name, tmp)), f"mutant {name} slipped through"
