@@ -1,0 +1,502 @@
+"""Benchmark of the quantized-weight GEMM path on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Default workload "prefill_projection_4096": one step = the four calls of the
+prefill projection (T=512, K=N=4096): Q4 -> f32, Q4 -> bf16, Q8-row -> f32,
+Q8-row -> bf16.  The metric is dequant-GEMM TFLOP/s (2*T*N*K per call, all
+calls of all ranks over the max-over-ranks time); weight GB/s and the
+roofline fraction of the dominant kernel ride along in the same JSON line.
+Other workloads: smallest_q4, denoiser_block, moe_panels, sweep_q4_T<T>,
+sweep_q8_T<T>.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload
+(independent problems, no collective on the data path): weak scaling.
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 2**20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# workloads: inputs on the device, a list of calls per step
+# ---------------------------------------------------------------------------
+
+class Call:
+    """One C-ABI call with its algorithmic work and the buffers it reads and writes."""
+
+    def __init__(self, name, fn, flops, weight_bytes, other_bytes, launches, h2d=(), d2h=()):
+        self.name, self.fn, self.flops = name, fn, flops
+        self.weight_bytes, self.other_bytes, self.launches = weight_bytes, other_bytes, launches
+        self.h2d, self.d2h = list(h2d), list(d2h)
+
+
+def _dev_x(x_bits, dtype, dev):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16))
+    return t.view(torch.bfloat16 if dtype == "bf16" else torch.float16).to(dev)
+
+
+def _u16(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+
+def _q4_calls(cq, case, outs, dev, tag):
+    import torch
+    from block_quantized_weight_02_gb300 import pack
+    T, K, N = case["T"], case["K"], case["N"]
+    X = _dev_x(case["x"], case["x_dtype"], dev)
+    Wq = torch.from_numpy(pack.pack_q4(case["codes"])).to(dev)
+    Ws = _u16(case["scales"], dev)
+    ws = torch.empty(cq.cq_gemm_q4_workspace_bytes(T, K), dtype=torch.uint8, device=dev)
+    calls = []
+    wbytes = N * K // 2 + N * K // 32 * 2
+    for out in outs:
+        Y = torch.empty(T, N, dtype=torch.float32 if out == "f32" else torch.bfloat16, device=dev)
+        calls.append(Call(f"{tag} q4->{out}", (lambda X=X, Wq=Wq, Ws=Ws, Y=Y, ws=ws: cq.cq_gemm_q4(X, Wq, Ws, Y, ws)),
+                          2.0 * T * N * K, wbytes, X.numel() * 2 + Y.numel() * Y.element_size(), 2,
+                          h2d=[X], d2h=[Y]))
+    return calls
+
+
+def _q8_calls(cq, case, outs, dev, tag):
+    import torch
+    T, K, N = case["T"], case["K"], case["N"]
+    X = _dev_x(case["x"], case["x_dtype"], dev)
+    Wq = torch.from_numpy(case["q"]).to(dev)
+    rs = torch.from_numpy(case["rs"]).to(dev)
+    calls = []
+    for out in outs:
+        Y = torch.empty(T, N, dtype=torch.float32 if out == "f32" else torch.bfloat16, device=dev)
+        calls.append(Call(f"{tag} q8row->{out}", (lambda X=X, Wq=Wq, rs=rs, Y=Y: cq.cq_gemm_q8row(X, Wq, rs, Y)),
+                          2.0 * T * N * K, N * K + 4 * N, X.numel() * 2 + Y.numel() * Y.element_size(), 1,
+                          h2d=[X], d2h=[Y]))
+    return calls
+
+
+def _moe_calls(cq, m, dev):
+    import torch
+    from block_quantized_weight_02_gb300 import pack
+    T, H, I, E, topk = m["T"], m["H"], m["I"], m["E"], m["topk"]
+    X = _dev_x(m["x"], m["x_dtype"], dev)
+    idx = torch.from_numpy(m["idx"]).to(dev)
+    w = torch.from_numpy(m["w"]).to(dev)
+    guq = torch.from_numpy(pack.pack_q4(m["gu_codes"])).to(dev)
+    gus = _u16(m["gu_scales"], dev)
+    dq = torch.from_numpy(pack.pack_q4(m["d_codes"])).to(dev)
+    ds = _u16(m["d_scales"], dev)
+    Y = torch.empty(T, H, dtype=torch.float32, device=dev)
+    ws = torch.empty(cq.cq_moe_workspace_bytes(T, H, I, E, topk), dtype=torch.uint8, device=dev)
+    touched = len(np.unique(m["idx"]))
+    per_expert = (2 * I * H + H * I) * 9 // 16
+    flops = T * topk * (2.0 * H * 2 * I + 2.0 * I * H)
+    return [Call("moe panels", lambda: cq.cq_moe_panels(X, idx, w, guq, gus, dq, ds, Y, ws), flops,
+                 touched * per_expert, X.numel() * 2 + Y.numel() * 4 + idx.numel() * 8, 6,
+                 h2d=[X, idx, w], d2h=[Y])], touched
+
+
+def build_workload(name, dev):
+    import block_quantized_weight_02_gb300 as cq
+    from block_quantized_weight_02_gb300 import synth
+    info = {}
+    if name == "prefill_projection_4096":
+        c4, c8 = synth.c2_q4(), synth.c2_q8()
+        make = lambda: _q4_calls(cq, c4, ["f32", "bf16"], dev, "T512") + _q8_calls(cq, c8, ["f32", "bf16"], dev, "T512")
+        info = {"T": 512, "K": 4096, "N": 4096, "formats": ["q4", "q8row"], "outputs": ["f32", "bf16"]}
+    elif name == "smallest_q4":
+        c = synth.c1()
+        make = lambda: _q4_calls(cq, c, ["f32"], dev, "T16")
+        info = {"T": 16, "K": 512, "N": 256, "formats": ["q4"], "outputs": ["f32"]}
+    elif name == "denoiser_block":
+        gu, dn = synth.c3()
+        make = lambda: _q4_calls(cq, gu, ["bf16"], dev, "gate/up") + _q4_calls(cq, dn, ["bf16"], dev, "down")
+        info = {"T": 1024, "gate_up": [3072, 24576], "down": [12288, 3072], "formats": ["q4"], "outputs": ["bf16"]}
+    elif name == "moe_panels":
+        m = synth.c4()
+        calls, touched = _moe_calls(cq, m, dev)
+        info = {"T": 32, "H": 2048, "I": 768, "E": 128, "topk": 8, "touched_experts": touched, "outputs": ["f32"]}
+        return (lambda: [calls]), info, 1
+    elif name.startswith("sweep_q4_T") or name.startswith("sweep_q8_T"):
+        T = int(name.split("_T")[1])
+        if "q4" in name:
+            c = synth.c5_q4(T)
+            make = lambda: _q4_calls(cq, c, ["bf16"], dev, f"T{T}")
+        else:
+            c = synth.c5_q8(T)
+            make = lambda: _q8_calls(cq, c, ["bf16"], dev, f"T{T}")
+        info = {"T": T, "K": 8192, "N": 8192, "outputs": ["bf16"]}
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    one = make()
+    set_bytes = sum(c.weight_bytes + c.other_bytes for c in one)
+    sets = max(1, min(16, -(-3 * L2_BYTES // max(set_bytes, 1))))
+    rot = [one] + [make() for _ in range(sets - 1)]
+    return (lambda i=[0]: rot), info, sets
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class Clocks:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 8:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The slowest rank's number (timing only; no data-path collective)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step: float, world: int, ms_per_step_max: float) -> float:
+    """Weak scaling: every rank processes `units_per_step`; the job's rate is
+    all ranks' units over the slowest rank's time."""
+    return units_per_step * world / (ms_per_step_max * 1e-3)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_quantized_weight_02_gb300 as cq
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    rot_fn, info, sets = build_workload(args.workload, dev)
+    rot = rot_fn()
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        for c in rot[i % sets]:
+            c.fn()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if cq.cq_get_device_error() != 0:
+        raise SystemExit("device error during warm-up")
+
+    clocks = Clocks(local_rank)
+    clocks.start()
+    # per-call events (dominant kernel timing) on the launching stream
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in rot[0]]
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        for j, c in enumerate(rot[i % sets]):
+            ev[i][j][0].record(stream)
+            c.fn()
+            ev[i][j][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if cq.cq_get_device_error() != 0:
+        raise SystemExit("device error during the timed region")
+    per_call_ms = [float(np.mean([ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps)]))
+                   for j in range(len(rot[0]))]
+    ms_max = max_over_ranks(ms, world)
+
+    calls = rot[0]
+    flops_step = sum(c.flops for c in calls)
+    wbytes_step = sum(c.weight_bytes for c in calls)
+    ms_step = ms_max / args.steps
+    tflops = whole_job_rate(flops_step, world, ms_step) / 1e12
+    wgbs = whole_job_rate(wbytes_step, world, ms_step) / 1e9
+
+    # e2e: host buffers (pinned), H2D of each call's inputs, the calls, D2H of the outputs
+    host_in = [[torch.empty_like(t, device="cpu").pin_memory() for t in c.h2d] for c in calls]
+    host_out = [[torch.empty_like(t, device="cpu").pin_memory() for t in c.d2h] for c in calls]
+    for j, c in enumerate(calls):
+        for h, d in zip(host_in[j], c.h2d):
+            h.copy_(d.cpu())
+    h2d_b = sum(t.numel() * t.element_size() for c in calls for t in c.h2d)
+    d2h_b = sum(t.numel() * t.element_size() for c in calls for t in c.d2h)
+
+    def e2e_step():
+        for j, c in enumerate(calls):
+            for h, d in zip(host_in[j], c.h2d):
+                d.copy_(h, non_blocking=True)
+            c.fn()
+            for h, d in zip(host_out[j], c.d2h):
+                h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, min(args.steps, 50))
+    barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, world)
+    e2e_val = whole_job_rate(flops_step, world, e_ms) / 1e12
+
+    # roofline of the dominant call (largest share of the step)
+    peaks = _peaks()
+    j = int(np.argmax(per_call_ms))
+    dom = calls[j]
+    d_ms = per_call_ms[j]
+    tensor_bound = dom.flops / max(dom.weight_bytes + dom.other_bytes, 1) > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        ach = dom.flops / (d_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / peaks["bf16_tflops"], 4)}
+    else:
+        ach = (dom.weight_bytes + dom.other_bytes) / (d_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4)}
+    roof.update({"traffic": None, "kernel": dom.name, "launch_ms": round(d_ms, 5),
+                 "peak_source": peaks["source"], "launches_in_call": dom.launches})
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload)
+
+    line = {
+        "metric": "dequant-GEMM TFLOP/s (weight GB/s and roofline fraction alongside)",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "q4:fp16xfp16->f32, q8row:bf16xbf16->f32", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, **info, "parallelism": f"replicas x{world}",
+                   "l2": f"rotating {sets} input sets ({sets * sum(c.weight_bytes + c.other_bytes for c in calls) / 2**20:.0f} MiB) > L2"},
+        "weight_gbs": round(wgbs, 1),
+        "per_call_ms": {c.name: round(t, 5) for c, t in zip(calls, per_call_ms)},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_b,
+                "d2h_bytes_per_step": d2h_b},
+        "gpu_launches": sum(c.launches for c in calls) * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (the reference arm and the cpu_baseline object)
+# ---------------------------------------------------------------------------
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _oracle_sample(workload):
+    """(make(rows) -> (fn, flops, description), max_rows): the oracle on the
+    first `rows` activation rows (tokens) of the workload, full N and K."""
+    import oracle
+    from block_quantized_weight_02_gb300 import synth
+    oracle.build()
+    if workload == "prefill_projection_4096":
+        c4, c8 = synth.c2_q4(), synth.c2_q8()
+        wq = oracle.pack_q4(c4["codes"])
+
+        def make(rows):
+            X4 = oracle.x_to_f64(c4["x"][:rows], "bf16")
+            X8 = oracle.x_to_f64(c8["x"][:rows], "bf16")
+
+            def fn():
+                oracle.gemm_q4(wq, c4["scales"], 4096, 4096, X4)
+                oracle.gemm_q8row(c8["q"], c8["rs"], X8)
+            return fn, 2 * 2.0 * rows * 4096 * 4096, f"first {rows} of 512 activation rows, Q4 and Q8-row, full N and K"
+        return make, 512
+    if workload == "moe_panels":
+        m = synth.c4()
+        guq = oracle.pack_q4(m["gu_codes"])
+        dq = oracle.pack_q4(m["d_codes"])
+
+        def make(rows):
+            X = oracle.x_to_f64(m["x"][:rows], "bf16")
+            fn = lambda: oracle.moe(X, m["idx"][:rows], m["w"][:rows], guq, m["gu_scales"], dq, m["d_scales"], 128, 768)
+            return fn, rows * 8 * 6.0 * 2048 * 768, f"first {rows} of 32 tokens, full expert chain"
+        return make, 32
+    if workload == "smallest_q4":
+        c = synth.c1()
+        wq = oracle.pack_q4(c["codes"])
+
+        def make(rows):
+            X = oracle.x_to_f64(c["x"][:rows], "f16")
+            return (lambda: oracle.gemm_q4(wq, c["scales"], 256, 512, X)), 2.0 * rows * 256 * 512, \
+                f"first {rows} of 16 activation rows"
+        return make, 16
+    if workload == "denoiser_block":
+        c, fmt = synth.c3()[0], "q4"
+    else:
+        T = int(workload.split("_T")[1])
+        fmt = "q4" if "q4" in workload else "q8"
+        c = synth.c5_q4(T) if fmt == "q4" else synth.c5_q8(T)
+    wq = oracle.pack_q4(c["codes"]) if fmt == "q4" else None
+
+    def make(rows):
+        X = oracle.x_to_f64(c["x"][:rows], "bf16")
+        if fmt == "q4":
+            fn = lambda: oracle.gemm_q4(wq, c["scales"], c["N"], c["K"], X)
+        else:
+            fn = lambda: oracle.gemm_q8row(c["q"], c["rs"], X)
+        return fn, 2.0 * rows * c["N"] * c["K"], f"first {rows} of {c['T']} activation rows, full N and K"
+    return make, c["T"]
+
+
+def _calibrated(workload, target_s):
+    make, max_rows = _oracle_sample(workload)
+    fn, flops, _ = make(1)
+    t0 = time.perf_counter()
+    fn()
+    t1 = max(time.perf_counter() - t0, 1e-4)
+    rows = int(max(1, min(max_rows, target_s / t1)))
+    return make(rows)
+
+
+def cpu_baseline(workload):
+    fn, flops, desc = _calibrated(workload, 10.0)
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+            "sample": desc, "seconds": round(dt, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    # each step is a bounded sample, sized so that the whole run takes about two minutes
+    per_step = min(20.0, 120.0 / max(1, args.steps + args.warmup))
+    fn, flops, desc = _calibrated(args.workload, per_step)
+    for _ in range(args.warmup):
+        fn()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+    dt = float(np.mean(times))
+    v = flops / dt / 1e12
+    line = {"impl": "reference", "metric": "dequant-GEMM TFLOP/s (weight GB/s and roofline fraction alongside)",
+            "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded)", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill_projection_4096")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

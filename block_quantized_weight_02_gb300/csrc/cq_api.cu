@@ -1,0 +1,329 @@
+// The C ABI: argument checks, workspace carve-up, path choice and launch
+// order.  Every step of the computation runs in the kernels of k_aux.cu,
+// k_skinny.cu and k_tc.cu; nothing here touches the data.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "cq_internal.h"
+
+namespace cq {
+
+Options& options() {
+    static Options o;
+    return o;
+}
+
+static thread_local char g_msg[512] = "";
+
+cq_status fail(cq_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    int n = snprintf(g_msg, sizeof g_msg, "decline: ");
+    vsnprintf(g_msg + n, sizeof g_msg - n, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+cq_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(CQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    if (!fn) return false;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, dt, (cuuint32_t)rank, const_cast<void*>(base), reinterpret_cast<const cuuint64_t*>(dims),
+                    reinterpret_cast<const cuuint64_t*>(strides_bytes), reinterpret_cast<const cuuint32_t*>(box),
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
+namespace {
+
+constexpr size_t ALIGN = 256;
+size_t up(size_t v) { return (v + ALIGN - 1) / ALIGN * ALIGN; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+cq_status check_arch() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) return fail(CQ_ERR_ARCH, "device %d is sm_%d%d, this library is built for sm_103a", dev, major, minor);
+    return CQ_OK;
+}
+
+cq_status check_x(int xt) {
+    if (xt != CQ_F16 && xt != CQ_BF16) return fail(CQ_ERR_DTYPE, "activations must be fp16 or bf16 (got %d)", xt);
+    return CQ_OK;
+}
+cq_status check_y(int yt) {
+    if (yt != CQ_F32 && yt != CQ_BF16) return fail(CQ_ERR_DTYPE, "output must be f32 or bf16 (got %d)", yt);
+    return CQ_OK;
+}
+
+// Workspace of the Q4 GEMM: guarded fp16 activations, then inverse scales.
+struct Q4Ws {
+    uint16_t* xh;
+    float* rsx;
+};
+size_t q4_ws_bytes(int64_t T, int64_t K) { return up((size_t)T * K * 2) + up((size_t)T * 4); }
+Q4Ws q4_ws(void* ws, int64_t T, int64_t K) {
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    return {reinterpret_cast<uint16_t*>(b), reinterpret_cast<float*>(b + up((size_t)T * K * 2))};
+}
+
+struct MoeLayout {
+    size_t status, seg, perm, inv, xh, rsx, a, ah, rsa, eo, total;
+};
+MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
+    const size_t P = (size_t)(T * topk);
+    MoeLayout l;
+    size_t o = 0;
+    l.status = o; o += up(4);
+    l.seg = o; o += up((size_t)(E + 1) * 4);
+    l.perm = o; o += up(P * 4);
+    l.inv = o; o += up(P * 4);
+    l.xh = o; o += up((size_t)T * H * 2);
+    l.rsx = o; o += up((size_t)T * 4);
+    l.a = o; o += up(P * I * 4);
+    l.ah = o; o += up(P * I * 2);
+    l.rsa = o; o += up(P * 4);
+    l.eo = o; o += up(P * H * 4);
+    l.total = o;
+    return l;
+}
+
+bool use_skinny(int64_t T) {
+    const Options& o = options();
+    if (o.force_path == 1) return true;
+    if (o.force_path == 2) return false;
+    return T <= o.small_t_max;
+}
+
+cq_status launched(cudaError_t e, const char* what) {
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return CQ_OK;
+}
+
+}  // namespace
+}  // namespace cq
+
+using namespace cq;
+
+extern "C" {
+
+int cq_version(void) { return 100; }
+
+const char* cq_last_error(void) { return g_msg; }
+
+cq_status cq_set_option(int option, int64_t value) {
+    Options& o = options();
+    switch (option) {
+        case CQ_OPT_SMALL_T_MAX:
+            if (value < 0 || value > 32) return fail(CQ_ERR_ARG, "small-T limit must be in [0, 32]");
+            o.small_t_max = value;
+            return CQ_OK;
+        case CQ_OPT_FORCE_PATH:
+            if (value < 0 || value > 2) return fail(CQ_ERR_ARG, "path must be 0, 1 or 2");
+            o.force_path = value;
+            return CQ_OK;
+        case CQ_OPT_WAIT_NS:
+            if (value < 1000000 || value > 60000000000LL) return fail(CQ_ERR_ARG, "wait limit must be in [1 ms, 60 s]");
+            o.wait_ns = value;
+            return CQ_OK;
+        case CQ_OPT_TEST_STALL:
+            if (value != 0 && value != 1) return fail(CQ_ERR_ARG, "stall must be 0 or 1");
+            o.test_stall = value;
+            return CQ_OK;
+        case CQ_OPT_TRACE:
+            o.trace = value != 0;
+            return CQ_OK;
+        default:
+            return fail(CQ_ERR_ARG, "unknown option %d", option);
+    }
+}
+
+int64_t cq_get_option(int option) {
+    const Options& o = options();
+    switch (option) {
+        case CQ_OPT_SMALL_T_MAX: return o.small_t_max;
+        case CQ_OPT_FORCE_PATH: return o.force_path;
+        case CQ_OPT_WAIT_NS: return o.wait_ns;
+        case CQ_OPT_TEST_STALL: return o.test_stall;
+        case CQ_OPT_TRACE: return o.trace;
+        default: return -1;
+    }
+}
+
+size_t cq_gemm_q4_workspace_bytes(int64_t T, int64_t K) {
+    if (T < 1 || K < 1) return 0;
+    return q4_ws_bytes(T, K);
+}
+
+cq_status cq_gemm_q4(const void* X, int xt, int64_t T, int64_t K, const uint8_t* Wq, const uint16_t* Ws, int64_t N,
+                     void* Y, int yt, void* ws, size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    if (!X || !Wq || !Ws || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q4: null pointer");
+    cq_status st;
+    if ((st = check_x(xt)) || (st = check_y(yt))) return st;
+    if (T < 1 || N < 1 || K < 256 || K % 256) return fail(CQ_ERR_SHAPE, "cq_gemm_q4: need T>=1, N>=1, K%%256==0 (T=%lld K=%lld N=%lld)", (long long)T, (long long)K, (long long)N);
+    if (T > (1LL << 31) - 1 || N > (1LL << 31) - 1) return fail(CQ_ERR_SHAPE, "cq_gemm_q4: T and N must fit in int32");
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(Y)) return fail(CQ_ERR_ALIGN, "cq_gemm_q4: pointers must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(ws) & (ALIGN - 1)) || ws_bytes < q4_ws_bytes(T, K)) return fail(CQ_ERR_WORKSPACE, "cq_gemm_q4: workspace needs %zu bytes, 256-aligned", q4_ws_bytes(T, K));
+    if ((st = check_arch())) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Q4Ws w = q4_ws(ws, T, K);
+    if ((st = launched(launch_x_half(X, xt, T, K, w.xh, w.rsx, s), "activation guard pass"))) return st;
+    if (use_skinny(T)) {
+        if (T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4: the weight-streaming path serves T <= 32");
+        SkinnyDense a = {w.xh, 0, w.rsx, nullptr, Wq, Ws, T, K, N, Y, yt};
+        return launched(launch_skinny_q4(a, s), "weight-streaming Q4 GEMM");
+    }
+    TcArgs a = {w.xh, 0, w.rsx, nullptr, Wq, Ws, T, K, N, Y, yt};
+    return launched(launch_tc_q4(a, s), "tcgen05 Q4 GEMM");
+}
+
+cq_status cq_gemm_q8row(const void* X, int xt, int64_t T, int64_t K, const int8_t* Wq, const float* rs, int64_t N,
+                        void* Y, int yt, void* stream) {
+    g_msg[0] = 0;
+    if (!X || !Wq || !rs || !Y) return fail(CQ_ERR_NULL, "cq_gemm_q8row: null pointer");
+    cq_status st;
+    if ((st = check_x(xt)) || (st = check_y(yt))) return st;
+    if (T < 1 || N < 1 || K < 128 || K % 128) return fail(CQ_ERR_SHAPE, "cq_gemm_q8row: need T>=1, N>=1, K%%128==0 (T=%lld K=%lld N=%lld)", (long long)T, (long long)K, (long long)N);
+    if (T > (1LL << 31) - 1 || N > (1LL << 31) - 1) return fail(CQ_ERR_SHAPE, "cq_gemm_q8row: T and N must fit in int32");
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(rs) || !aligned16(Y)) return fail(CQ_ERR_ALIGN, "cq_gemm_q8row: pointers must be 16-byte aligned");
+    if ((st = check_arch())) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (use_skinny(T)) {
+        if (T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q8row: the weight-streaming path serves T <= 32");
+        SkinnyDense a = {X, xt == CQ_BF16, nullptr, rs, reinterpret_cast<const uint8_t*>(Wq), nullptr, T, K, N, Y, yt};
+        return launched(launch_skinny_q8(a, s), "weight-streaming Q8-row GEMM");
+    }
+    TcArgs a = {X, xt == CQ_BF16, nullptr, rs, reinterpret_cast<const uint8_t*>(Wq), nullptr, T, K, N, Y, yt};
+    return launched(launch_tc_q8(a, s), "tcgen05 Q8-row GEMM");
+}
+
+size_t cq_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
+    if (T < 1 || H < 1 || I < 1 || E < 1 || topk < 1) return 0;
+    return moe_layout(T, H, I, E, topk).total;
+}
+
+cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E, int64_t I, int64_t topk,
+                        const int32_t* idx, const float* w, const uint8_t* Wgu_q, const uint16_t* Wgu_s,
+                        const uint8_t* Wd_q, const uint16_t* Wd_s, void* Y, int yt, void* ws, size_t ws_bytes,
+                        void* stream) {
+    g_msg[0] = 0;
+    if (!X || !idx || !w || !Wgu_q || !Wgu_s || !Wd_q || !Wd_s || !Y || !ws) return fail(CQ_ERR_NULL, "cq_moe_panels: null pointer");
+    cq_status st;
+    if ((st = check_x(xt)) || (st = check_y(yt))) return st;
+    if (T < 1 || topk < 1 || topk > 64 || E < 1 || E > 1024 || T * topk > 65536 || H < 256 || H % 256 || I < 256 ||
+        I % 256)
+        return fail(CQ_ERR_SHAPE, "cq_moe_panels: shape rules broken (T=%lld H=%lld I=%lld E=%lld topk=%lld)",
+                    (long long)T, (long long)H, (long long)I, (long long)E, (long long)topk);
+    if (!aligned16(X) || !aligned16(idx) || !aligned16(w) || !aligned16(Wgu_q) || !aligned16(Wgu_s) ||
+        !aligned16(Wd_q) || !aligned16(Wd_s) || !aligned16(Y))
+        return fail(CQ_ERR_ALIGN, "cq_moe_panels: pointers must be 16-byte aligned");
+    const MoeLayout l = moe_layout(T, H, I, E, topk);
+    if ((reinterpret_cast<uintptr_t>(ws) & (ALIGN - 1)) || ws_bytes < l.total) return fail(CQ_ERR_WORKSPACE, "cq_moe_panels: workspace needs %zu bytes, 256-aligned", l.total);
+    if ((st = check_arch())) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    int32_t* status = reinterpret_cast<int32_t*>(b + l.status);
+    SkinnyMoe m = {};
+    m.xh = reinterpret_cast<uint16_t*>(b + l.xh);
+    m.rsx = reinterpret_cast<float*>(b + l.rsx);
+    m.ah = reinterpret_cast<uint16_t*>(b + l.ah);
+    m.rsa = reinterpret_cast<float*>(b + l.rsa);
+    m.w = w;
+    m.seg = reinterpret_cast<int32_t*>(b + l.seg);
+    m.perm = reinterpret_cast<int32_t*>(b + l.perm);
+    m.status = status;
+    m.gu_q = Wgu_q;
+    m.gu_s = Wgu_s;
+    m.d_q = Wd_q;
+    m.d_s = Wd_s;
+    m.a = reinterpret_cast<float*>(b + l.a);
+    m.eo = reinterpret_cast<float*>(b + l.eo);
+    m.T = T;
+    m.H = H;
+    m.I = I;
+    m.E = E;
+    m.topk = topk;
+    int32_t* inv = reinterpret_cast<int32_t*>(b + l.inv);
+    if ((st = launched(launch_moe_route(idx, T, topk, E, const_cast<int32_t*>(m.seg), const_cast<int32_t*>(m.perm), inv, status, s), "MoE routing layout"))) return st;
+    if ((st = launched(launch_x_half(X, xt, T, H, const_cast<uint16_t*>(m.xh), const_cast<float*>(m.rsx), s), "MoE activation guard pass"))) return st;
+    if ((st = launched(launch_moe_gateup(m, s), "MoE gate/up panels"))) return st;
+    if ((st = launched(launch_a_half(m.a, T * topk, I, const_cast<uint16_t*>(m.ah), const_cast<float*>(m.rsa), status, s), "MoE SwiGLU guard pass"))) return st;
+    if ((st = launched(launch_moe_down(m, s), "MoE down panels"))) return st;
+    return launched(launch_moe_combine(m.eo, inv, T, topk, H, Y, yt, status, s), "MoE combine");
+}
+
+cq_status cq_moe_layout(const void* ws, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk, int32_t* perm_out,
+                        int32_t* seg_out, void* stream) {
+    g_msg[0] = 0;
+    if (!ws || !perm_out || !seg_out) return fail(CQ_ERR_NULL, "cq_moe_layout: null pointer");
+    if (T < 1 || topk < 1 || E < 1) return fail(CQ_ERR_SHAPE, "cq_moe_layout: bad shape");
+    const MoeLayout l = moe_layout(T, H, I, E, topk);
+    const uint8_t* b = static_cast<const uint8_t*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(perm_out, b + l.perm, (size_t)(T * topk) * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(seg_out, b + l.seg, (size_t)(E + 1) * 4, cudaMemcpyDeviceToDevice, s);
+    return launched(e, "cq_moe_layout copy");
+}
+
+cq_status cq_dequant_q4(const uint8_t* Wq, const uint16_t* Ws, int64_t N, int64_t K, float* W, void* stream) {
+    g_msg[0] = 0;
+    if (!Wq || !Ws || !W) return fail(CQ_ERR_NULL, "cq_dequant_q4: null pointer");
+    if (N < 1 || K < 32 || K % 32) return fail(CQ_ERR_SHAPE, "cq_dequant_q4: need N>=1, K%%32==0");
+    if (!aligned16(Wq) || !aligned16(W)) return fail(CQ_ERR_ALIGN, "cq_dequant_q4: Wq and W must be 16-byte aligned");
+    cq_status st;
+    if ((st = check_arch())) return st;
+    return launched(launch_dequant_q4(Wq, Ws, N, K, W, static_cast<cudaStream_t>(stream)), "dequant Q4");
+}
+
+cq_status cq_dequant_q8row(const int8_t* Wq, const float* rs, int64_t N, int64_t K, float* W, void* stream) {
+    g_msg[0] = 0;
+    if (!Wq || !rs || !W) return fail(CQ_ERR_NULL, "cq_dequant_q8row: null pointer");
+    if (N < 1 || K < 1) return fail(CQ_ERR_SHAPE, "cq_dequant_q8row: need N>=1, K>=1");
+    cq_status st;
+    if ((st = check_arch())) return st;
+    return launched(launch_dequant_q8row(Wq, rs, N, K, W, static_cast<cudaStream_t>(stream)), "dequant Q8-row");
+}
+
+cq_status cq_get_device_error(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    const int a = take_error_aux(), b = take_error_skinny(), c = take_error_tc();
+    const int v = a ? a : (b ? b : c);
+    if (v == DEV_INDEX) return fail(CQ_ERR_INDEX, "a routing index is outside [0, E)");
+    if (v == DEV_TIMEOUT) return fail(CQ_ERR_TIMEOUT, "a device pipeline wait ran past its limit");
+    return CQ_OK;
+}
+
+}  // extern "C"

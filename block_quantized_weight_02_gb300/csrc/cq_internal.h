@@ -1,0 +1,106 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstddef>
+#include <cstdio>
+
+#include "../../include/cq.h"
+
+namespace cq {
+
+// Device error word values (shared by all kernels; first writer wins).
+enum DevErr : int { DEV_OK = 0, DEV_INDEX = 1, DEV_TIMEOUT = 2 };
+
+struct Options {
+    int64_t small_t_max = 32;
+    int64_t force_path = 0;
+    int64_t wait_ns = 1000000000LL;
+    int64_t test_stall = 0;
+    int64_t trace = 0;
+};
+Options& options();
+
+// Host error reporting.
+cq_status fail(cq_status st, const char* fmt, ...);
+cq_status cuda_fail(cudaError_t e, const char* what);
+
+// Tensor map encoding (driver entry point fetched through the runtime, so
+// the library has no link-time dependency on libcuda).
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes /* rank-1 entries */, const uint32_t* box,
+                  CUtensorMapSwizzle swz);
+
+int num_sms();
+
+// ---- launchers (one translation unit each) ------------------------------
+
+// Per-TU device error words: read-and-clear (synchronous copies).
+int take_error_aux();
+int take_error_skinny();
+int take_error_tc();
+
+// aux kernels
+cudaError_t launch_dequant_q4(const uint8_t* wq, const uint16_t* ws, int64_t N, int64_t K, float* w, cudaStream_t s);
+cudaError_t launch_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, int64_t K, float* w, cudaStream_t s);
+// X rows -> fp16 with a per-row power-of-two guard; rsx = inverse scales.
+cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s);
+
+struct MoeWs;  // workspace carve-up (cq_api.cu)
+cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
+                             int32_t* inv, int32_t* status, cudaStream_t s);
+cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,
+                          cudaStream_t s);
+cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, int64_t topk, int64_t H, void* y,
+                               int yt, const int32_t* status, cudaStream_t s);
+
+// Weight-streaming (small-T) GEMM.
+struct SkinnyDense {
+    const void* x;       // activations [T][K] (fp16 for Q4 after the guard pass; fp16/bf16 for Q8)
+    int x_bf16;
+    const float* rsx;    // Q4: per-row inverse guard scale [T]; null for Q8
+    const float* rs;     // Q8: row scales [N]; null for Q4
+    const uint8_t* wq;   // Q4 nibbles / Q8 int8 bytes
+    const uint16_t* ws;  // Q4 scales
+    int64_t T, K, N;
+    void* y;
+    int yt;
+};
+cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s);
+cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s);
+
+struct SkinnyMoe {
+    const uint16_t* xh;     // [T][H] fp16 (guarded)
+    const float* rsx;       // [T]
+    const uint16_t* ah;     // [P][I] fp16 (guarded), grouped order
+    const float* rsa;       // [P]
+    const float* w;         // routing weights [T*topk] (pair id order)
+    const int32_t* seg;     // [E+1]
+    const int32_t* perm;    // [P] pair ids in grouped order
+    const int32_t* status;  // non-zero: skip
+    const uint8_t *gu_q, *d_q;
+    const uint16_t *gu_s, *d_s;
+    float* a;               // [P][I] f32 SwiGLU output, grouped order
+    float* eo;              // [P][H] f32 weighted expert outputs, grouped order
+    int64_t T, H, I, E, topk;
+};
+cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s);
+cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s);
+
+// tcgen05 (large-T) GEMM.
+struct TcArgs {
+    const void* x;       // [T][K] fp16/bf16 (Q4: guarded fp16)
+    int x_bf16;
+    const float* rsx;    // Q4
+    const float* rs;     // Q8
+    const uint8_t* wq;
+    const uint16_t* ws;
+    int64_t T, K, N;
+    void* y;
+    int yt;
+};
+cudaError_t launch_tc_q4(const TcArgs& a, cudaStream_t s);
+cudaError_t launch_tc_q8(const TcArgs& a, cudaStream_t s);
+
+}  // namespace cq

@@ -1,0 +1,274 @@
+// Small kernels around the GEMMs: the dequantization test hooks, the
+// activation guard pass (rows -> fp16 behind a power-of-two scale), the
+// MoE routing layout, the SwiGLU-activation guard pass and the combine.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "cq_internal.h"
+
+namespace cq {
+
+__device__ int g_err_aux = 0;
+
+__device__ __forceinline__ void set_err(int code) { atomicCAS(&g_err_aux, 0, code); }
+
+int take_error_aux() {
+    int v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_err_aux, sizeof(int));
+    cudaMemcpyToSymbol(g_err_aux, &z, sizeof(int));
+    return v;
+}
+
+// ---- dequantization hooks ---------------------------------------------
+// Q4 ("oxinfer 0.0.5 src/metal.rs", Dequantizers / load(Q4W ...)): one
+// thread per 32-element block; W = f32(nibble - 8) * f32(scale), one exact
+// f32 product per element.
+__global__ void k_dequant_q4(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ ws, int64_t nblocks,
+                             int64_t bpr, float* __restrict__ w) {
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= nblocks) return;
+    const int64_t n = i / bpr, b = i % bpr;
+    const float d = __half2float(__ushort_as_half(ws[i]));
+    const uint4 v = *reinterpret_cast<const uint4*>(wq + 16 * i);
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    float* out = w + n * (bpr * 32) + b * 32;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t byte = (words[j >> 2] >> (8 * (j & 3))) & 0xFF;
+        out[j] = __fmul_rn((float)((int)(byte & 15) - 8), d);
+        out[16 + j] = __fmul_rn((float)((int)(byte >> 4) - 8), d);
+    }
+}
+
+__global__ void k_dequant_q8row(const int8_t* __restrict__ wq, const float* __restrict__ rs, int64_t N, int64_t K,
+                                float* __restrict__ w) {
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= N * K) return;
+    w[i] = __fmul_rn((float)wq[i], rs[i / K]);
+}
+
+cudaError_t launch_dequant_q4(const uint8_t* wq, const uint16_t* ws, int64_t N, int64_t K, float* w, cudaStream_t s) {
+    const int64_t nb = N * (K / 32);
+    k_dequant_q4<<<(unsigned)((nb + 255) / 256), 256, 0, s>>>(wq, ws, nb, K / 32, w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, int64_t K, float* w, cudaStream_t s) {
+    const int64_t n = N * K;
+    k_dequant_q8row<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(wq, rs, N, K, w);
+    return cudaGetLastError();
+}
+
+// ---- power-of-two guard -------------------------------------------------
+// A row whose largest magnitude is m is multiplied by 2^(14 - e), where
+// m = f * 2^e with f in [0.5, 1), so that m lands in [2^13, 2^14) before
+// the fp16 rounding; the inverse factor goes to the epilogue.  ("oxinfer
+// 0.0.5 src/metal.rs", MMA_SHADER_SRC header, row_scale / x_half.)
+__device__ __forceinline__ int guard_shift(float m) {
+    if (!(m > 0.f) || !isfinite(m)) return 0;
+    int e;
+    frexpf(m, &e);
+    int sh = 14 - e;
+    return sh < -120 ? -120 : (sh > 120 ? 120 : sh);
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+__device__ __forceinline__ float block_max_256(float m, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) r = fmaxf(r, red[i]);
+    return r;
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// One CTA of 256 threads per row; K % 8 == 0.
+template <typename T>
+__global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t K, __half* __restrict__ xh,
+                                                float* __restrict__ rsx) {
+    __shared__ float red[8];
+    const int64_t row = blockIdx.x;
+    const uint4* src = reinterpret_cast<const uint4*>(x + row * K);
+    const int64_t n8 = K / 8;
+    float m = 0.f;
+    for (int64_t i = threadIdx.x; i < n8; i += 256) {
+        uint4 v = src[i];
+        const T* e = reinterpret_cast<const T*>(&v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(to_f32<T>(e[j])));
+    }
+    m = block_max_256(m, red);
+    const int sh = guard_shift(m);
+    const float sc = pow2f(sh);
+    uint4* dst = reinterpret_cast<uint4*>(xh + row * K);
+    for (int64_t i = threadIdx.x; i < n8; i += 256) {
+        uint4 v = src[i];
+        const T* e = reinterpret_cast<const T*>(&v);
+        uint4 o;
+        __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            oh[j] = __halves2half2(__float2half_rn(to_f32<T>(e[2 * j]) * sc), __float2half_rn(to_f32<T>(e[2 * j + 1]) * sc));
+        dst[i] = o;
+    }
+    if (threadIdx.x == 0) rsx[row] = pow2f(-sh);
+}
+
+cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s) {
+    if (xt == CQ_BF16)
+        k_x_half<__nv_bfloat16><<<(unsigned)T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), K,
+                                                            reinterpret_cast<__half*>(xh), rsx);
+    else
+        k_x_half<__half><<<(unsigned)T, 256, 0, s>>>(reinterpret_cast<const __half*>(x), K,
+                                                     reinterpret_cast<__half*>(xh), rsx);
+    return cudaGetLastError();
+}
+
+// ---- MoE routing layout -------------------------------------------------
+// Routed (t, j) pairs grouped by expert, token order kept inside an expert
+// ("oxinfer 0.0.5 src/metal.rs", Backend::moe: per-expert counts, segment
+// starts, gathered sources filled in token order).  One CTA.
+//   seg[e]   = number of pairs routed to experts below e  (seg[E] = P)
+//   perm[q]  = pair id (t*topk + j) at grouped position q
+//   inv[p]   = grouped position of pair p
+//   status   = 0, or 1 if an index is outside [0, E) (nothing else written)
+__global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ idx, int P, int E,
+                                                   int32_t* __restrict__ seg, int32_t* __restrict__ perm,
+                                                   int32_t* __restrict__ inv, int32_t* __restrict__ status) {
+    extern __shared__ int sh[];
+    int* cnt = sh;            // [E]
+    int* fill = sh + E;       // [E]
+    int* chunk_e = sh + 2 * E;  // [256]
+    __shared__ int bad;
+    if (threadIdx.x == 0) bad = 0;
+    for (int e = threadIdx.x; e < E; e += 256) cnt[e] = 0;
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += 256) {
+        const int e = idx[p];
+        if (e < 0 || e >= E)
+            bad = 1;
+        else
+            atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    if (bad) {
+        if (threadIdx.x == 0) {
+            *status = 1;
+            set_err(DEV_INDEX);
+        }
+        return;
+    }
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int e = 0; e < E; ++e) {
+            seg[e] = acc;
+            fill[e] = acc;
+            acc += cnt[e];
+        }
+        seg[E] = acc;
+    }
+    __syncthreads();
+    for (int base = 0; base < P; base += 256) {
+        const int p = base + threadIdx.x;
+        const int e = p < P ? idx[p] : -1;
+        chunk_e[threadIdx.x] = e;
+        __syncthreads();
+        if (e >= 0) {
+            int before = 0;
+            for (int q = 0; q < (int)threadIdx.x; ++q) before += (chunk_e[q] == e);
+            const int pos = fill[e] + before;
+            perm[pos] = p;
+            inv[p] = pos;
+        }
+        __syncthreads();
+        if (e >= 0) atomicAdd(&fill[e], 1);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *status = 0;
+}
+
+cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
+                             int32_t* inv, int32_t* status, cudaStream_t s) {
+    const size_t smem = (size_t)(2 * E + 256) * sizeof(int);
+    k_moe_route<<<1, 256, smem, s>>>(idx, (int)(T * topk), (int)E, seg, perm, inv, status);
+    return cudaGetLastError();
+}
+
+// SwiGLU activations (f32, grouped order) -> fp16 behind the same
+// power-of-two guard as the inputs ("oxinfer 0.0.5 src/metal.rs",
+// silu_half: scaled half rows and an inverse scale per row).
+__global__ void __launch_bounds__(256) k_a_half(const float* __restrict__ a, int64_t I, __half* __restrict__ ah,
+                                                float* __restrict__ rsa, const int32_t* __restrict__ status) {
+    if (*status != 0) return;
+    __shared__ float red[8];
+    const int64_t row = blockIdx.x;
+    const float4* src = reinterpret_cast<const float4*>(a + row * I);
+    const int64_t n4 = I / 4;
+    float m = 0.f;
+    for (int64_t i = threadIdx.x; i < n4; i += 256) {
+        float4 v = src[i];
+        m = fmaxf(fmaxf(fmaxf(m, fabsf(v.x)), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    }
+    m = block_max_256(m, red);
+    const int sh = guard_shift(m);
+    const float sc = pow2f(sh);
+    __half2* dst = reinterpret_cast<__half2*>(ah + row * I);
+    for (int64_t i = threadIdx.x; i < n4; i += 256) {
+        float4 v = src[i];
+        dst[2 * i] = __floats2half2_rn(v.x * sc, v.y * sc);
+        dst[2 * i + 1] = __floats2half2_rn(v.z * sc, v.w * sc);
+    }
+    if (threadIdx.x == 0) rsa[row] = pow2f(-sh);
+}
+
+cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,
+                          cudaStream_t s) {
+    k_a_half<<<(unsigned)P, 256, 0, s>>>(a, I, reinterpret_cast<__half*>(ah), rsa, status);
+    return cudaGetLastError();
+}
+
+// Y[t][n] = sum over slots j (in order) of eo[inv[t*topk + j]][n]; the
+// routing weight is already in eo ("oxinfer 0.0.5 src/metal.rs",
+// moe_combine).  f32 sums, one rounding to the output type.
+__global__ void __launch_bounds__(256) k_moe_combine(const float* __restrict__ eo, const int32_t* __restrict__ inv,
+                                                     int topk, int64_t H, void* __restrict__ y, int yt,
+                                                     const int32_t* __restrict__ status) {
+    if (*status != 0) return;
+    const int64_t t = blockIdx.y;
+    const int64_t c = ((int64_t)blockIdx.x * 256 + threadIdx.x) * 4;
+    if (c >= H) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < topk; ++j) {
+        const int64_t r = inv[t * topk + j];
+        const float4 v = *reinterpret_cast<const float4*>(eo + r * H + c);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    if (yt == CQ_F32) {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(y) + t * H + c) = acc;
+    } else {
+        __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(y) + t * H + c);
+        o[0] = __floats2bfloat162_rn(acc.x, acc.y);
+        o[1] = __floats2bfloat162_rn(acc.z, acc.w);
+    }
+}
+
+cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, int64_t topk, int64_t H, void* y,
+                               int yt, const int32_t* status, cudaStream_t s) {
+    dim3 grid((unsigned)((H / 4 + 255) / 256), (unsigned)T);
+    k_moe_combine<<<grid, 256, 0, s>>>(eo, inv, (int)topk, H, y, yt, status);
+    return cudaGetLastError();
+}
+
+}  // namespace cq

@@ -1,0 +1,407 @@
+// Large-T GEMM on the 5th-generation tensor cores (tcgen05, accumulator in
+// tensor memory), weights dequantized on the fly in shared memory.
+//
+// Y^T tile = W tile (128 weight rows, M) x X tile^T (BN activation rows, N),
+// K in stages of 64.  Warp roles in a CTA of 192 threads:
+//   warp 4      TMA producer: raw weight tile (Q4 nibbles 128 x 32 B or Q8
+//               bytes 128 x 64 B, swizzled so the decode reads are
+//               bank-conflict free) and the activation tile (BN x 64 fp16 /
+//               bf16, 128-byte swizzle = the MMA's K-major operand layout);
+//   warps 0-3   decoders, one thread per weight row: raw row -> 64 fp16/bf16
+//               values written into the A operand tile in the 128-byte
+//               swizzled K-major layout, then the epilogue;
+//   warp 5      allocates the tensor memory and issues tcgen05.mma
+//               (M = 128, N = BN, K = 16) from one thread, committing each
+//               stage back to the producer and the last to the epilogue.
+// Q4 decode: (nibble - 8) * fp16 block scale, rounded once to fp16 (the
+// scale folded into the half operand, as in mma_tile of "oxinfer 0.0.5
+// src/metal.rs"); the activations arrive as fp16 behind a per-row
+// power-of-two guard whose inverse the epilogue applies.  Q8-row decode:
+// int8 -> the activation type exactly; the row scale is applied to the f32
+// accumulator in the epilogue ("cortiq-engine 0.8.3 src/gpu_metal/qi21.rs",
+// module header on q8_row).
+// Every wait is time-bounded; on a timeout the CTA stops, lets copies in
+// flight land, frees its tensor memory and reports CQ_ERR_TIMEOUT.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "cq_internal.h"
+#include "cq_ptx.cuh"
+
+namespace cq {
+
+__device__ int g_err_tc = 0;
+
+int take_error_tc() {
+    int v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_err_tc, sizeof(int));
+    cudaMemcpyToSymbol(g_err_tc, &z, sizeof(int));
+    return v;
+}
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+
+struct Params {
+    const float* rsx;
+    const float* rs;
+    const uint16_t* ws;   // Q4 block scales [N][K/32]
+    void* y;
+    int yt;
+    int64_t T, N, K;
+    uint64_t wait_ns;
+    int stall;
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+__device__ __forceinline__ uint32_t nib2_to_h2(uint32_t v) {
+    const uint32_t h = (v & 0x000F000Fu) | 0x64006400u;
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h),
+                              __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), s);
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t w, uint32_t sel) {
+    const uint32_t h = prmt(w ^ 0x80808080u, 0x64646464u, sel);
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h),
+                              __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, int lo_byte) {
+    const float a = (float)(int)(int8_t)((w >> (8 * lo_byte)) & 0xFF);
+    const float b = (float)(int)(int8_t)((w >> (8 * (lo_byte + 1))) & 0xFF);
+    const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+template <int FMT>
+struct Raw;
+template <>
+struct Raw<0> { static constexpr int ROW = 32; };   // Q4: 64 k = 32 bytes per row
+template <>
+struct Raw<1> { static constexpr int ROW = 64; };   // Q8: 64 bytes per row
+
+template <int FMT, int BN, int XBF, int STAGES>
+struct Layout {
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int R_BYTES = BM * Raw<FMT>::ROW;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
+    static constexpr int R_OFF = B_OFF + STAGES * B_BYTES;
+    static constexpr int BAR_OFF = R_OFF + STAGES * ((R_BYTES + 1023) / 1024 * 1024);
+    static constexpr int R_STRIDE = (R_BYTES + 1023) / 1024 * 1024;
+    // full[S], dec[S], empty[S], accf, then tmem slot, abort, never
+    static constexpr int MISC = (3 * STAGES + 1) * 8 + 16;
+    static constexpr int TOTAL = BAR_OFF + MISC + 1024;  // + alignment slack
+};
+
+template <int FMT, int BN, int XBF, int STAGES>
+__global__ void __launch_bounds__(THREADS, 1)
+k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const Params p) {
+    using L = Layout<FMT, BN, XBF, STAGES>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * BM;          // first weight row
+    const int t0 = blockIdx.y * BN;          // first activation row
+    const int nk = (int)(p.K / BK);
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto dec_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    const uint32_t accf_bar = bar0 + 8u * (3 * STAGES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* never_flag = abort_flag + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(dec_bar(s), 128);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(accf_bar, 1);
+        *abort_flag = 0;
+        *never_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), BN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        atomicCAS(&g_err_tc, 0, DEV_TIMEOUT);
+    };
+
+    if (warp == 4) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmW);
+            tma_prefetch_desc(&tmX);
+            int issued = 0;
+            if (!p.stall) {
+                for (int kb = 0; kb < nk; ++kb) {
+                    const int s = kb % STAGES;
+                    const uint32_t par = (uint32_t)((kb / STAGES) & 1);
+                    if (!mbar_wait(empty_bar(s), par ^ 1u, p.wait_ns, abort_flag)) {
+                        give_up();
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::R_BYTES + L::B_BYTES));
+                    tma_load_2d(sb + L::R_OFF + s * L::R_STRIDE, &tmW, full_bar(s), kb * Raw<FMT>::ROW, m0);
+                    tma_load_2d(sb + L::B_OFF + s * L::B_BYTES, &tmX, full_bar(s), kb * BK, t0);
+                    ++issued;
+                }
+            }
+            if (*abort_flag) {
+                // copies already issued must land before the CTA can exit
+                const int first = issued > STAGES ? issued - STAGES : 0;
+                for (int kb = first; kb < issued; ++kb)
+                    mbar_wait(full_bar(kb % STAGES), (uint32_t)((kb / STAGES) & 1), p.wait_ns, never_flag);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(BM, BN, XBF);
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t par = (uint32_t)((kb / STAGES) & 1);
+                if (!mbar_wait(dec_bar(s), par, p.wait_ns, abort_flag) ||
+                    !mbar_wait(full_bar(s), par, p.wait_ns, abort_flag)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_base = sb + L::A_OFF + s * A_BYTES;
+                const uint32_t b_base = sb + L::B_OFF + s * L::B_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    tc_mma_f16(tmem, smem_desc_sw128(a_base + 32 * kk), smem_desc_sw128(b_base + 32 * kk), idesc,
+                               (kb | kk) != 0 ? 1u : 0u);
+                tc_commit(empty_bar(s));
+            }
+            tc_commit(accf_bar);   // also lets teardown know every MMA has finished
+        }
+        __syncwarp();
+    } else {
+        // ================= decoders (thread = weight row), then epilogue =================
+        const int r = threadIdx.x;           // 0..127
+        const int64_t n = (int64_t)m0 + r;
+        const bool row_ok = n < p.N;
+        const uint32_t a_row = (uint32_t)(r * 128);
+        const uint32_t xr = (uint32_t)(r & 7);
+        uint32_t sc_next = 0;
+        if (FMT == 0 && row_ok) sc_next = __ldg(reinterpret_cast<const uint32_t*>(p.ws + n * (p.K / 32)));
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t par = (uint32_t)((kb / STAGES) & 1);
+            const uint32_t sc = sc_next;
+            if (FMT == 0 && row_ok && kb + 1 < nk)
+                sc_next = __ldg(reinterpret_cast<const uint32_t*>(p.ws + n * (p.K / 32) + 2 * (kb + 1)));
+            if (!mbar_wait(full_bar(s), par, p.wait_ns, abort_flag)) {
+                give_up();
+                break;
+            }
+            const uint32_t raw = sb + L::R_OFF + s * L::R_STRIDE;
+            const uint32_t adst = sb + L::A_OFF + s * A_BYTES + a_row;
+            if (FMT == 0) {
+                // 32-byte rows, 32-byte swizzle: chunk j of row r sits at j ^ ((r >> 2) & 1)
+                const uint32_t sw = (uint32_t)((r >> 2) & 1);
+                const uint4 v0 = ld_shared_v4(raw + r * 32 + ((0u ^ sw) << 4));
+                const uint4 v1 = ld_shared_v4(raw + r * 32 + ((1u ^ sw) << 4));
+                const __half2 s0 = __halves2half2(__ushort_as_half((uint16_t)(sc & 0xFFFF)),
+                                                  __ushort_as_half((uint16_t)(sc & 0xFFFF)));
+                const __half2 s1 = __halves2half2(__ushort_as_half((uint16_t)(sc >> 16)),
+                                                  __ushort_as_half((uint16_t)(sc >> 16)));
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const uint4 v = b ? v1 : v0;
+                    const __half2 sh = b ? s1 : s0;
+                    const uint32_t px = prmt(v.x, 0u, 0x3120u), py = prmt(v.y, 0u, 0x3120u);
+                    const uint32_t pz = prmt(v.z, 0u, 0x3120u), pw = prmt(v.w, 0u, 0x3120u);
+                    // chunk 0: elements 0-7 (low nibbles of bytes 0-7)
+                    st_shared_v4(adst + (((uint32_t)(4 * b + 0) ^ xr) << 4), hmul2_u32(nib2_to_h2(px), sh),
+                                 hmul2_u32(nib2_to_h2(px >> 8), sh), hmul2_u32(nib2_to_h2(py), sh),
+                                 hmul2_u32(nib2_to_h2(py >> 8), sh));
+                    // chunk 1: elements 8-15 (low nibbles of bytes 8-15)
+                    st_shared_v4(adst + (((uint32_t)(4 * b + 1) ^ xr) << 4), hmul2_u32(nib2_to_h2(pz), sh),
+                                 hmul2_u32(nib2_to_h2(pz >> 8), sh), hmul2_u32(nib2_to_h2(pw), sh),
+                                 hmul2_u32(nib2_to_h2(pw >> 8), sh));
+                    // chunk 2: elements 16-23 (high nibbles of bytes 0-7)
+                    st_shared_v4(adst + (((uint32_t)(4 * b + 2) ^ xr) << 4), hmul2_u32(nib2_to_h2(px >> 4), sh),
+                                 hmul2_u32(nib2_to_h2(px >> 12), sh), hmul2_u32(nib2_to_h2(py >> 4), sh),
+                                 hmul2_u32(nib2_to_h2(py >> 12), sh));
+                    // chunk 3: elements 24-31 (high nibbles of bytes 8-15)
+                    st_shared_v4(adst + (((uint32_t)(4 * b + 3) ^ xr) << 4), hmul2_u32(nib2_to_h2(pz >> 4), sh),
+                                 hmul2_u32(nib2_to_h2(pz >> 12), sh), hmul2_u32(nib2_to_h2(pw >> 4), sh),
+                                 hmul2_u32(nib2_to_h2(pw >> 12), sh));
+                }
+            } else {
+                // 64-byte rows, 64-byte swizzle: chunk j of row r sits at j ^ ((r >> 1) & 3)
+                const uint32_t sw = (uint32_t)((r >> 1) & 3);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = ld_shared_v4(raw + r * 64 + (((uint32_t)q ^ sw) << 4));
+                    // bytes 16q..16q+15 = elements 16q..16q+15 = output chunks 2q, 2q+1
+                    uint32_t o[8];
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (XBF) {
+                            o[2 * i] = i8x2_to_bf2(wv[i], 0);
+                            o[2 * i + 1] = i8x2_to_bf2(wv[i], 2);
+                        } else {
+                            o[2 * i] = i8x2_to_h2(wv[i], 0x4140u);
+                            o[2 * i + 1] = i8x2_to_h2(wv[i], 0x4342u);
+                        }
+                    }
+                    st_shared_v4(adst + (((uint32_t)(2 * q) ^ xr) << 4), o[0], o[1], o[2], o[3]);
+                    st_shared_v4(adst + (((uint32_t)(2 * q + 1) ^ xr) << 4), o[4], o[5], o[6], o[7]);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(dec_bar(s));
+        }
+
+        // ---- epilogue: TMEM -> registers -> scale -> Y[t][n] ----
+        if (!*abort_flag && mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) {
+            tc_fence_after();
+            const float rsn = (FMT == 1 && row_ok) ? p.rs[n] : 0.f;
+            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(cc * 32), v);
+                tmem_ld_wait();
+                const int64_t tb = (int64_t)t0 + cc * 32;
+                float rsx_l = 0.f;
+                if (FMT == 0 && tb + lane < p.T) rsx_l = p.rsx[tb + lane];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, rsx_l, j) : rsn;
+                    const int64_t t = tb + j;
+                    if (row_ok && t < p.T) {
+                        const float val = __uint_as_float(v[j]) * sx;
+                        if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = val;
+                        else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(val);
+                    }
+                }
+            }
+        } else if (!*abort_flag) {
+            give_up();
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        if (*abort_flag && lane == 0) mbar_wait(accf_bar, 0, p.wait_ns, never_flag);  // MMAs done
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, BN);
+    }
+}
+
+template <int FMT, int BN, int XBF, int STAGES>
+cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, const Params& p, dim3 grid, cudaStream_t s) {
+    using L = Layout<FMT, BN, XBF, STAGES>;
+    auto kern = k_tc<FMT, BN, XBF, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, THREADS, L::TOTAL, s>>>(mw, mx, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
+    const int xbf = fmt == 0 ? 0 : a.x_bf16;
+    const int64_t mt = (a.N + BM - 1) / BM;
+    int bn = 256;
+    if (mt * ((a.T + 255) / 256) < num_sms()) bn = 128;
+    if (bn == 128 && mt * ((a.T + 127) / 128) < num_sms() && a.T <= 64) bn = 64;
+    CUtensorMap mw, mx;
+    {
+        const uint64_t kbytes = fmt == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+        uint64_t d[2] = {kbytes, (uint64_t)a.N};
+        uint64_t st[1] = {kbytes};
+        uint32_t box[2] = {(uint32_t)(fmt == 0 ? 32 : 64), (uint32_t)BM};
+        if (!encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.wq, d, st, box,
+                          fmt == 0 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        uint64_t d[2] = {(uint64_t)a.K, (uint64_t)a.T};
+        uint64_t st[1] = {(uint64_t)a.K * 2};
+        uint32_t box[2] = {(uint32_t)BK, (uint32_t)bn};
+        if (!encode_tiled(&mx, xbf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x, d,
+                          st, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    Params p = {};
+    p.rsx = a.rsx;
+    p.rs = a.rs;
+    p.ws = a.ws;
+    p.y = a.y;
+    p.yt = a.yt;
+    p.T = a.T;
+    p.N = a.N;
+    p.K = a.K;
+    p.wait_ns = (uint64_t)options().wait_ns;
+    p.stall = (int)options().test_stall;
+    options().test_stall = 0;
+    dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), 1);
+    if (options().trace)
+        fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d grid=(%u,%u)\n", fmt, (long long)a.T,
+                (long long)a.N, (long long)a.K, bn, grid.x, grid.y);
+    if (fmt == 0) {
+        if (bn == 256) return launch_bn<0, 256, 0, 4>(mw, mx, p, grid, s);
+        if (bn == 128) return launch_bn<0, 128, 0, 6>(mw, mx, p, grid, s);
+        return launch_bn<0, 64, 0, 8>(mw, mx, p, grid, s);
+    }
+    if (xbf) {
+        if (bn == 256) return launch_bn<1, 256, 1, 3>(mw, mx, p, grid, s);
+        if (bn == 128) return launch_bn<1, 128, 1, 5>(mw, mx, p, grid, s);
+        return launch_bn<1, 64, 1, 6>(mw, mx, p, grid, s);
+    }
+    if (bn == 256) return launch_bn<1, 256, 0, 3>(mw, mx, p, grid, s);
+    if (bn == 128) return launch_bn<1, 128, 0, 5>(mw, mx, p, grid, s);
+    return launch_bn<1, 64, 0, 6>(mw, mx, p, grid, s);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_q4(const TcArgs& a, cudaStream_t s) { return launch(0, a, s); }
+cudaError_t launch_tc_q8(const TcArgs& a, cudaStream_t s) { return launch(1, a, s); }
+
+}  // namespace cq

@@ -1,0 +1,170 @@
+/*
+ * cq — matmul against block-quantized weights, dequantized on the fly, on
+ * one GB300 (sm_103a).  C ABI of libcq.so.
+ *
+ * Weight formats
+ *  - Q4 split plane.  Wq[N][K/2] bytes plus Ws[N][K/32] fp16 block scales.
+ *    Block b of row n is the 16 bytes at n*K/2 + 16*b; byte i holds element
+ *    32b+i in its low nibble and element 32b+16+i in its high nibble; an
+ *    element decodes as (nibble - 8) * Ws[n][b].  ("oxinfer 0.0.5
+ *    src/metal.rs", shader section "Dequantizers", struct Q4W and
+ *    load(Q4W ...); restated by load(Q4_0W ...) on the same page.)
+ *  - Q8-row.  Wq[N][K] int8 plus rs[N] f32; the row scale multiplies the
+ *    f32 accumulator of each output row.  ("cortiq-engine 0.8.3
+ *    src/gpu_metal/qi21.rs", module header on q8_row weights: integer
+ *    weights exact in half precision, row scale in the epilogue.)
+ *
+ * Common conventions
+ *  - Every pointer argument is a DEVICE pointer unless it says otherwise;
+ *    `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - The caller owns every buffer.  No entry point allocates device memory
+ *    or synchronises the stream (cq_get_device_error excepted); all work is
+ *    enqueued on `stream`.  Scratch memory comes from the caller's
+ *    workspace `ws` of `ws_bytes` bytes (size it with the *_workspace_bytes
+ *    query; 256-byte aligned).
+ *  - Row-major, densely packed tensors.  All pointers 16-byte aligned.
+ *  - Errors found on the host (bad pointer, dtype, shape, alignment, short
+ *    workspace) return a status before anything is enqueued and set a
+ *    thread-local message (cq_last_error), in the style of the pages'
+ *    "decline: <reason>" (cortiq-engine src/gpu_metal/qi21.rs, decline()).
+ *    A failed launch returns CQ_ERR_CUDA.  Problems only the device can see
+ *    (a routing index out of range, a pipeline wait that exceeded its time
+ *    limit) set a device error word that cq_get_device_error reports; the
+ *    remaining kernels of that call do no work.
+ *  - Outputs are overwritten, never accumulated into.
+ */
+#ifndef CQ_H
+#define CQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CQ_OK = 0,
+    CQ_ERR_NULL = 1,        /* a required pointer is NULL */
+    CQ_ERR_DTYPE = 2,       /* unsupported activation or output type */
+    CQ_ERR_SHAPE = 3,       /* a size breaks the shape rules */
+    CQ_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+    CQ_ERR_INDEX = 5,       /* a routing index outside [0, E) (device-detected) */
+    CQ_ERR_WORKSPACE = 6,   /* workspace missing, short or misaligned */
+    CQ_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
+    CQ_ERR_TIMEOUT = 8,     /* a device pipeline wait ran past its limit */
+    CQ_ERR_ARCH = 9,        /* the current device is not sm_103 */
+    CQ_ERR_ARG = 10         /* any other invalid argument */
+} cq_status;
+
+typedef enum { CQ_F16 = 0, CQ_BF16 = 1, CQ_F32 = 2 } cq_dtype;
+
+/* ---------------------------------------------------------------------------
+ * Q4 GEMM:  Y[T][N] = X[T][K] . dequant(Wq, Ws)[N][K]^T
+ *
+ * X: fp16 or bf16 (xt), [T][K].  Wq: [N][K/2] bytes.  Ws: fp16 bits
+ * [N][K/32].  Y: f32 or bf16 (yt), [T][N], overwritten.
+ * Shape rules: T >= 1, N >= 1, K >= 256 and K % 256 == 0.
+ * Arithmetic: each activation row is scaled by a power of two that puts its
+ * largest magnitude in [2^13, 2^14) and rounded to fp16; each weight is
+ * (nibble - 8) * scale rounded once to fp16; products accumulate in f32;
+ * the output is scaled back by the inverse power of two and rounded once to
+ * yt.  (The guard follows "oxinfer 0.0.5 src/metal.rs", MMA_SHADER_SRC
+ * header and the x_half shader; the scale folded into the half operand
+ * follows mma_tile on the same page.)
+ * Workspace: cq_gemm_q4_workspace_bytes(T, K) bytes.
+ * ------------------------------------------------------------------------- */
+size_t cq_gemm_q4_workspace_bytes(int64_t T, int64_t K);
+cq_status cq_gemm_q4(const void* X, int xt, int64_t T, int64_t K,
+                     const uint8_t* Wq, const uint16_t* Ws, int64_t N,
+                     void* Y, int yt, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Q8-row GEMM:  Y[T][N] = (X[T][K] . Wq[N][K]^T) * rs[N]
+ *
+ * X: fp16 or bf16 [T][K]; the int8 weights are converted exactly to the
+ * same type, products accumulate in f32, rs[n] multiplies the accumulator
+ * of output row n, one rounding to yt (f32 or bf16).
+ * Shape rules: T >= 1, N >= 1, K >= 128 and K % 128 == 0.  No workspace.
+ * ------------------------------------------------------------------------- */
+cq_status cq_gemm_q8row(const void* X, int xt, int64_t T, int64_t K,
+                        const int8_t* Wq, const float* rs, int64_t N,
+                        void* Y, int yt, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Routed MoE expert panels (all experts Q4):
+ *   for each token t and slot j < topk, e = idx[t][j]:
+ *     g = Wgate[e] . x_t,  u = Wup[e] . x_t          (Wgu rows 0..I-1, I..2I-1)
+ *     a = g / (1 + exp(-g)) * u                       (SwiGLU)
+ *     Y[t] += w[t][j] * (Wd[e] . a)                   (Y starts at zero)
+ * ("oxinfer 0.0.5 src/metal.rs": Backend::moe and the silu_half /
+ *  moe_combine shaders; its tests module, mma_moe_matches_cpu, states the
+ *  same chain in f64.)
+ *
+ * X: fp16/bf16 [T][H].  idx: int32 [T][topk].  w: f32 [T][topk].
+ * Wgu_q: [E][2I][H/2], Wgu_s: fp16 [E][2I][H/32].
+ * Wd_q:  [E][H][I/2],  Wd_s:  fp16 [E][H][I/32].
+ * Y: f32 or bf16 [T][H], overwritten.
+ * Routed pairs are grouped by expert (ascending), token order inside an
+ * expert; each (t, j) is its own entry, so repeated experts in a row are
+ * counted twice.  The j-sum per token runs in slot order (deterministic).
+ * Shape rules: T >= 1, 1 <= topk <= 64, 1 <= E <= 1024, T*topk <= 65536,
+ * H % 256 == 0, I % 256 == 0, H >= 256, I >= 256.
+ * Workspace: cq_moe_workspace_bytes(T, H, I, E, topk) bytes.  After the
+ * call completes, cq_moe_layout reads the routing layout kept there.
+ * An index outside [0, E) sets CQ_ERR_INDEX on the device and leaves Y
+ * untouched.
+ * ------------------------------------------------------------------------- */
+size_t cq_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk);
+cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E,
+                        int64_t I, int64_t topk,
+                        const int32_t* idx, const float* w,
+                        const uint8_t* Wgu_q, const uint16_t* Wgu_s,
+                        const uint8_t* Wd_q, const uint16_t* Wd_s,
+                        void* Y, int yt, void* ws, size_t ws_bytes, void* stream);
+
+/* Copies the routing layout of the last cq_moe_panels call on `ws` into
+ * perm_out[T*topk] (pair ids t*topk + j in grouped order) and
+ * seg_out[E+1] (exclusive prefix of per-expert pair counts), both device
+ * int32 arrays, enqueued on `stream`. */
+cq_status cq_moe_layout(const void* ws, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk,
+                        int32_t* perm_out, int32_t* seg_out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Test hooks: the dequantized weights in f32 (bit-exact definitions).
+ *  cq_dequant_q4:    W[n][k] = (nibble - 8) * f32(scale)   (exact)
+ *  cq_dequant_q8row: W[n][k] = f32(q) * rs[n]              (one rounding)
+ * Shape rules: N >= 1, K >= 32, K % 32 == 0 (Q4); K >= 1 (Q8).
+ * ------------------------------------------------------------------------- */
+cq_status cq_dequant_q4(const uint8_t* Wq, const uint16_t* Ws, int64_t N, int64_t K,
+                        float* W, void* stream);
+cq_status cq_dequant_q8row(const int8_t* Wq, const float* rs, int64_t N, int64_t K,
+                           float* W, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Errors and options
+ * ------------------------------------------------------------------------- */
+/* Synchronises `stream`, then returns and clears the device error word
+ * (CQ_OK, CQ_ERR_INDEX or CQ_ERR_TIMEOUT); CQ_ERR_CUDA if the sync failed. */
+cq_status cq_get_device_error(void* stream);
+/* The calling thread's last host-side error message ("" if none). */
+const char* cq_last_error(void);
+
+typedef enum {
+    CQ_OPT_SMALL_T_MAX = 0,  /* largest T served by the weight-streaming path (default 32, max 32) */
+    CQ_OPT_FORCE_PATH = 1,   /* 0 auto, 1 weight-streaming, 2 tensor-memory (tcgen05) path */
+    CQ_OPT_WAIT_NS = 2,      /* time limit of every device pipeline wait, ns (default 1e9) */
+    CQ_OPT_TEST_STALL = 3,   /* test only: 1 makes the next tcgen05 launch's loader issue nothing */
+    CQ_OPT_TRACE = 4         /* 1 prints the chosen path and grid of each call to stderr */
+} cq_option;
+/* Process-wide; returns CQ_ERR_ARG for an unknown option or value. */
+cq_status cq_set_option(int option, int64_t value);
+int64_t cq_get_option(int option);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int cq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CQ_H */

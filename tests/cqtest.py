@@ -1,0 +1,104 @@
+"""Shared helpers of the GPU parity tests: upload seeded inputs, run the
+C-ABI entry points, compare with the CPU oracle under the acceptance bound
+|y - y_ref| <= 2e-3 * sum_k |w_k x_k| + 1e-6 per element and relative
+Frobenius error <= 1e-3 (bf16 outputs against the oracle's one RNE
+rounding of its f64 result)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import block_quantized_weight_02_gb300 as cq
+from block_quantized_weight_02_gb300 import pack
+
+DEV = "cuda:0"
+TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def to_dev_x(x_bits: np.ndarray, dtype: str) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).view(TORCH_DT[dtype]).to(DEV)
+
+
+def to_dev(a: np.ndarray) -> torch.Tensor:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(DEV)
+
+
+def y_host(Y: torch.Tensor) -> np.ndarray:
+    return Y.float().cpu().numpy().astype(np.float64)
+
+
+def check(y: np.ndarray, yref: np.ndarray, S: np.ndarray, out_dtype: str, what: str = ""):
+    yr = oracle.round_out(yref, out_dtype)
+    yr = yr.astype(np.float64) if out_dtype == "f32" else oracle.x_to_f64(yr, "bf16")
+    err = np.abs(y - yr)
+    bound = 2e-3 * S + 1e-6
+    bad = err > bound
+    fro = np.linalg.norm(y - yr) / max(np.linalg.norm(yr), 1e-300)
+    if bad.any() or not np.all(np.isfinite(y)) or fro > 1e-3:
+        i = int(np.argmax(err / bound))
+        raise AssertionError(f"{what}: {int(bad.sum())} elements over the bound (worst ratio "
+                             f"{float((err / bound).flat[i]):.3g} at {np.unravel_index(i, err.shape)}: "
+                             f"y={y.flat[i]!r} ref={yr.flat[i]!r} S={S.flat[i]!r}), rel Frobenius {fro:.3g}")
+    return float(np.max(err / bound)), float(fro)
+
+
+def run_q4(case, out_dtype="f32", Y=None):
+    T, K, N = case["T"], case["K"], case["N"]
+    wq = pack.pack_q4(case["codes"])
+    X = to_dev_x(case["x"], case["x_dtype"])
+    Wq = to_dev(wq)
+    Ws = to_dev(case["scales"])
+    if Y is None:
+        Y = torch.empty(T, N, dtype=TORCH_DT[out_dtype], device=DEV)
+    ws = torch.empty(max(cq.cq_gemm_q4_workspace_bytes(T, K), 1), dtype=torch.uint8, device=DEV)
+    cq.cq_gemm_q4(X, Wq, Ws, Y, ws)
+    st = cq.cq_get_device_error()
+    assert st == 0, cq.STATUS[st]
+    return Y, wq
+
+
+def run_q8(case, out_dtype="f32", Y=None):
+    T, K, N = case["T"], case["K"], case["N"]
+    X = to_dev_x(case["x"], case["x_dtype"])
+    if Y is None:
+        Y = torch.empty(T, N, dtype=TORCH_DT[out_dtype], device=DEV)
+    cq.cq_gemm_q8row(X, to_dev(case["q"]), to_dev(case["rs"]), Y)
+    st = cq.cq_get_device_error()
+    assert st == 0, cq.STATUS[st]
+    return Y
+
+
+def oracle_q4(case, wq):
+    X = oracle.x_to_f64(case["x"], case["x_dtype"])
+    return oracle.gemm_q4(wq, case["scales"], case["N"], case["K"], X)
+
+
+def oracle_q8(case):
+    X = oracle.x_to_f64(case["x"], case["x_dtype"])
+    return oracle.gemm_q8row(case["q"], case["rs"], X)
+
+
+def sample_positions(T, N, count, seed):
+    """Corners, edges and random (t, n) positions."""
+    rng = np.random.default_rng(seed)
+    fixed = [(0, 0), (0, N - 1), (T - 1, 0), (T - 1, N - 1), (T // 2, N // 2)]
+    rnd = np.stack([rng.integers(0, T, count), rng.integers(0, N, count)], axis=1)
+    return np.concatenate([np.array(fixed, np.int64), rnd.astype(np.int64)])
+
+
+class ForcePath:
+    """Context manager: route GEMMs through one path (1 weight-streaming, 2 tcgen05)."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        self.old = cq.cq_get_option(cq.CQ_OPT_FORCE_PATH)
+        cq.cq_set_option(cq.CQ_OPT_FORCE_PATH, self.path)
+
+    def __exit__(self, *a):
+        cq.cq_set_option(cq.CQ_OPT_FORCE_PATH, self.old)

@@ -1,0 +1,243 @@
+"""GPU parity of the Q4 / Q8-row GEMMs and the dequantization hooks against
+the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import block_quantized_weight_02_gb300 as cq
+from block_quantized_weight_02_gb300 import pack, synth
+
+from cqtest import (DEV, ForcePath, check, oracle_q4, oracle_q8, run_q4, run_q8, sample_positions, to_dev,
+                    to_dev_x, y_host)
+from test_oracle import _golden_blocks
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_dev):
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+# ---- dequantization hooks: bit-exact ------------------------------------
+
+def test_dequant_q4_golden_blocks_bit_exact():
+    blocks = _golden_blocks()
+    wq = np.stack([np.frombuffer(b[3], np.uint8) for b in blocks])            # one block per row
+    ws = np.array([[b[1]] for b in blocks], np.uint16)
+    W = torch.empty(len(blocks), 32, dtype=torch.float32, device=DEV)
+    cq.cq_dequant_q4(to_dev(wq), to_dev(ws), W)
+    ref = oracle.dequant_q4(wq, ws, len(blocks), 32)
+    assert np.array_equal(W.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_q4_random_bit_exact():
+    rng = np.random.default_rng(77)
+    N, K = 300, 1024
+    wq = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    ws = rng.integers(0, 65536, (N, K // 32), dtype=np.uint32).astype(np.uint16)
+    ws[(ws & 0x7C00) == 0x7C00] = 0x3C00        # no inf/NaN scales (IEEE propagation, unpinned)
+    ws[:4, :4] = [[0x0000, 0x8000, 0x0001, 0x8001]] * 4
+    W = torch.empty(N, K, dtype=torch.float32, device=DEV)
+    cq.cq_dequant_q4(to_dev(wq), to_dev(ws), W)
+    ref = oracle.dequant_q4(wq, ws, N, K)
+    assert np.array_equal(W.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_q8row_bit_exact():
+    rng = np.random.default_rng(78)
+    q, rs = synth.draw_q8row(rng, 129, 200)
+    q[0, :3] = [-128, 127, 0]
+    W = torch.empty(129, 200, dtype=torch.float32, device=DEV)
+    cq.cq_dequant_q8row(to_dev(q), to_dev(rs), W)
+    assert np.array_equal(W.cpu().numpy().view(np.uint32), oracle.dequant_q8row(q, rs).view(np.uint32))
+
+
+# ---- small shapes, both paths, full comparison --------------------------
+
+SMALL = [(1, 256, 64), (3, 512, 130), (8, 256, 200), (16, 768, 64), (17, 256, 96), (32, 512, 257)]
+LARGE = [(33, 256, 128), (100, 512, 300), (150, 512, 192), (257, 768, 130), (512, 256, 384)]
+
+
+@pytest.mark.parametrize("T,K,N", SMALL)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_q4_skinny_small(T, K, N, out, xdt):
+    case = synth.gemm_q4_case(1000 + T + K + N, T, K, N, x_dtype=xdt, signed=True)
+    with ForcePath(1):
+        Y, wq = run_q4(case, out)
+    yref, S = oracle_q4(case, wq)
+    check(y_host(Y), yref, S, out, f"q4 skinny T={T} K={K} N={N}")
+
+
+@pytest.mark.parametrize("T,K,N", SMALL + LARGE)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_q4_tcgen05_small(T, K, N, out, xdt):
+    case = synth.gemm_q4_case(2000 + T + K + N, T, K, N, x_dtype=xdt, signed=True)
+    with ForcePath(2):
+        Y, wq = run_q4(case, out)
+    yref, S = oracle_q4(case, wq)
+    check(y_host(Y), yref, S, out, f"q4 tcgen05 T={T} K={K} N={N}")
+
+
+@pytest.mark.parametrize("T,K,N", [(1, 128, 64), (3, 256, 130), (8, 384, 200), (16, 128, 64), (17, 256, 96),
+                                   (32, 512, 257)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_q8_skinny_small(T, K, N, out, xdt):
+    case = synth.gemm_q8_case(3000 + T + K + N, T, K, N, x_dtype=xdt)
+    with ForcePath(1):
+        Y = run_q8(case, out)
+    yref, S = oracle_q8(case)
+    check(y_host(Y), yref, S, out, f"q8 skinny T={T} K={K} N={N}")
+
+
+@pytest.mark.parametrize("T,K,N", [(1, 128, 64), (17, 256, 96), (33, 128, 128), (100, 384, 300),
+                                   (150, 512, 192), (257, 640, 130), (512, 256, 384)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_q8_tcgen05_small(T, K, N, out, xdt):
+    case = synth.gemm_q8_case(4000 + T + K + N, T, K, N, x_dtype=xdt)
+    with ForcePath(2):
+        Y = run_q8(case, out)
+    yref, S = oracle_q8(case)
+    check(y_host(Y), yref, S, out, f"q8 tcgen05 T={T} K={K} N={N}")
+
+
+def test_q4_wide_magnitude_rows_guard():
+    """Rows spanning 1e-3 .. 2e5 (beyond fp16's range), as in the pages'
+    GPU-vs-CPU test ("oxinfer 0.0.5 src/metal.rs", tests module, input())."""
+    T, K, N = 40, 512, 192
+    rng = np.random.default_rng(5)
+    mags = np.array([1e-3, 1.0, 300.0, 2e5])
+    xv = (rng.uniform(-0.5, 0.5, (T, K)) * mags[np.arange(T) % 4][:, None])
+    case = synth.gemm_q4_case(6, T, K, N)
+    case["x"] = synth.to_storage(xv, "bf16")
+    for path in (1, 2):
+        with ForcePath(path):
+            Y, wq = run_q4(case, "f32")
+        yref, S = oracle_q4(case, wq)
+        check(y_host(Y), yref, S, "f32", f"q4 wide rows path {path}")
+
+
+def test_q8_wide_magnitude_rows():
+    T, K, N = 40, 512, 192
+    rng = np.random.default_rng(6)
+    mags = np.array([1e-3, 1.0, 300.0, 2e5])
+    case = synth.gemm_q8_case(7, T, K, N)
+    case["x"] = synth.to_storage(rng.uniform(-0.5, 0.5, (T, K)) * mags[np.arange(T) % 4][:, None], "bf16")
+    for path in (1, 2):
+        with ForcePath(path):
+            Y = run_q8(case, "f32")
+        yref, S = oracle_q8(case)
+        check(y_host(Y), yref, S, "f32", f"q8 wide rows path {path}")
+
+
+def test_outputs_overwritten_and_bounds_respected():
+    """Y starts as NaN inside a larger buffer; the call fills Y exactly."""
+    T, K, N = 37, 512, 200
+    case = synth.gemm_q4_case(8, T, K, N)
+    for path in (1, 2):
+        buf = torch.full((T * N + 4096,), float("nan"), dtype=torch.float32, device=DEV)
+        Y = buf[:T * N].view(T, N)
+        with ForcePath(path):
+            run_q4(case, "f32", Y=Y)
+        assert torch.isfinite(Y).all()
+        assert torch.isnan(buf[T * N:]).all()
+
+
+def test_deterministic_repeat():
+    case = synth.gemm_q4_case(9, 24, 4096, 512)
+    case8 = synth.gemm_q8_case(9, 200, 1024, 512)
+    a, _ = run_q4(case, "f32")
+    b, _ = run_q4(case, "f32")
+    assert torch.equal(a, b)
+    c = run_q8(case8, "bf16")
+    d = run_q8(case8, "bf16")
+    assert torch.equal(c, d)
+
+
+def test_c1_smallest_q4_case():
+    case = synth.c1()
+    Y, wq = run_q4(case, "f32")
+    yref, S = oracle_q4(case, wq)
+    check(y_host(Y), yref, S, "f32", "C1")
+
+
+# ---- the configured sizes, sampled outputs ------------------------------
+
+def _sampled_q4(case, out, count=3000, seed=0):
+    Y, wq = run_q4(case, out)
+    tn = sample_positions(case["T"], case["N"], count, seed)
+    yref, S = oracle.gemm_q4_sampled(wq, case["scales"], case["N"], case["K"],
+                                     oracle.x_to_f64(case["x"], case["x_dtype"]), tn)
+    y = y_host(Y)[tn[:, 0], tn[:, 1]]
+    return check(y, yref, S, out, f"q4 T={case['T']} K={case['K']} N={case['N']} {out}")
+
+
+def _sampled_q8(case, out, count=3000, seed=0):
+    Y = run_q8(case, out)
+    tn = sample_positions(case["T"], case["N"], count, seed)
+    yref, S = oracle.gemm_q8_sampled(case["q"], case["rs"], oracle.x_to_f64(case["x"], case["x_dtype"]), tn)
+    y = y_host(Y)[tn[:, 0], tn[:, 1]]
+    return check(y, yref, S, out, f"q8 T={case['T']} K={case['K']} N={case['N']} {out}")
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_c2_prefill_projection_q4(out):
+    _sampled_q4(synth.c2_q4(), out)
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_c2_prefill_projection_q8(out):
+    _sampled_q8(synth.c2_q8(), out)
+
+
+def test_c2_full_output_q4_f32():
+    """Every output of the prefill projection (17 GFLOP of f64 on the host)."""
+    case = synth.c2_q4()
+    Y, wq = run_q4(case, "f32")
+    yref, S = oracle_q4(case, wq)
+    check(y_host(Y), yref, S, "f32", "C2 q4 full")
+
+
+def test_c3_denoiser_block():
+    gu, dn = synth.c3()
+    _sampled_q4(gu, "bf16", count=2000)
+    _sampled_q4(dn, "bf16", count=2000)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 128, 512, 2048])
+def test_c5_sweep_q4(T):
+    for out in ("bf16", "f32"):
+        _sampled_q4(synth.c5_q4(T), out, count=1500, seed=T)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 128, 512, 2048])
+def test_c5_sweep_q8(T):
+    for out in ("bf16", "f32"):
+        _sampled_q8(synth.c5_q8(T), out, count=1500, seed=T)
+
+
+# ---- failure handling without a fault -----------------------------------
+
+def test_wait_timeout_reports_status_and_context_survives():
+    case = synth.gemm_q8_case(10, 200, 256, 128)
+    old = cq.cq_get_option(cq.CQ_OPT_WAIT_NS)
+    try:
+        cq.cq_set_option(cq.CQ_OPT_WAIT_NS, 20_000_000)       # 20 ms
+        cq.cq_set_option(cq.CQ_OPT_TEST_STALL, 1)             # the next tcgen05 loader issues nothing
+        with ForcePath(2):
+            X = to_dev_x(case["x"], "bf16")
+            Y = torch.empty(200, 128, dtype=torch.float32, device=DEV)
+            cq.cq_gemm_q8row(X, to_dev(case["q"]), to_dev(case["rs"]), Y)
+        assert cq.cq_get_device_error() == 8                   # CQ_ERR_TIMEOUT
+    finally:
+        cq.cq_set_option(cq.CQ_OPT_WAIT_NS, old)
+        cq.cq_set_option(cq.CQ_OPT_TEST_STALL, 0)
+    Y = run_q8(case, "f32")                                   # the context is still usable
+    yref, S = oracle_q8(case)
+    check(y_host(Y), yref, S, "f32", "after timeout")
