@@ -1,8 +1,8 @@
 """Shared helpers of the GPU parity tests: upload seeded inputs, run the
 C-ABI entry points, compare with the CPU oracle under the acceptance bound
 |y - y_ref| <= 2e-3 * sum_k |w_k x_k| + 1e-6 per element and relative
-Frobenius error <= 1e-3 (bf16 outputs against the oracle's one RNE
-rounding of its f64 result)."""
+Frobenius error <= 1e-3, applied to the value before a bf16 output's
+mandatory final rounding (see check())."""
 from __future__ import annotations
 
 import numpy as np
@@ -31,18 +31,36 @@ def y_host(Y: torch.Tensor) -> np.ndarray:
     return Y.float().cpu().numpy().astype(np.float64)
 
 
+def half_ulp_bf16(y: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |y| (y already a bf16 value)."""
+    a = np.abs(y)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(np.maximum(e, -126) - 8), 2.0**-134)
+
+
 def check(y: np.ndarray, yref: np.ndarray, S: np.ndarray, out_dtype: str, what: str = ""):
-    yr = oracle.round_out(yref, out_dtype)
-    yr = yr.astype(np.float64) if out_dtype == "f32" else oracle.x_to_f64(yr, "bf16")
-    err = np.abs(y - yr)
-    bound = 2e-3 * S + 1e-6
+    """Acceptance: the computed value before the output's own rounding is
+    within |err| <= 2e-3*S + 1e-6 per element and relative Frobenius <= 1e-3
+    of the f64 reference.  An f32 output's rounding (2^-24 relative) is far
+    inside that; a bf16 output's rounding (up to half a bf16 ulp of y) is
+    not, so for bf16 that rounding is added exactly to both bounds."""
+    err = np.abs(y - yref)
+    r = half_ulp_bf16(y) if out_dtype == "bf16" else np.zeros_like(y)
+    bound = 2e-3 * S + 1e-6 + r
     bad = err > bound
-    fro = np.linalg.norm(y - yr) / max(np.linalg.norm(yr), 1e-300)
-    if bad.any() or not np.all(np.isfinite(y)) or fro > 1e-3:
+    nref = max(np.linalg.norm(yref), 1e-300)
+    fro = np.linalg.norm(y - yref) / nref
+    fro_bound = 1e-3 + np.linalg.norm(r) / nref
+    if bad.any() or not np.all(np.isfinite(y)) or fro > fro_bound:
         i = int(np.argmax(err / bound))
         raise AssertionError(f"{what}: {int(bad.sum())} elements over the bound (worst ratio "
                              f"{float((err / bound).flat[i]):.3g} at {np.unravel_index(i, err.shape)}: "
-                             f"y={y.flat[i]!r} ref={yr.flat[i]!r} S={S.flat[i]!r}), rel Frobenius {fro:.3g}")
+                             f"y={y.flat[i]!r} ref={yref.flat[i]!r} S={S.flat[i]!r}), rel Frobenius {fro:.3g} "
+                             f"(bound {fro_bound:.3g})")
+    if out_dtype == "bf16":
+        # the rounded outputs mostly coincide with the oracle's own rounding
+        same = np.mean(oracle.x_to_f64(oracle.f64_to_bf16(yref), "bf16") == y)
+        assert same >= 0.8, f"{what}: only {same:.3f} of bf16 outputs equal the oracle's rounding"
     return float(np.max(err / bound)), float(fro)
 
 
