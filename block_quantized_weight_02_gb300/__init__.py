@@ -27,6 +27,7 @@ _c_p, _c_i64, _c_int, _c_sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, cty
 _SIGS = {
     "cq_gemm_q4_workspace_bytes": (_c_sz, [_c_i64, _c_i64]),
     "cq_gemm_q4": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p, _c_int, _c_p, _c_sz, _c_p]),
+    "cq_gemm_q4_noalloc": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p, _c_int, _c_p]),
     "cq_gemm_q8row": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p, _c_int, _c_p]),
     "cq_moe_workspace_bytes": (_c_sz, [_c_i64] * 5),
     "cq_moe_panels": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p,
@@ -103,6 +104,18 @@ def cq_gemm_q4(X, Wq, Ws, Y, ws, stream=None, raise_on_error=True):
     N = Wq.shape[0]
     st = lib().cq_gemm_q4(_ptr(X), _xt(X), T, K, _ptr(Wq), _ptr(Ws), N, _ptr(Y), _xt(Y), _ptr(ws),
                           0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    if raise_on_error:
+        _check(st)
+    return st
+
+
+def cq_gemm_q4_noalloc(X, Wq, Ws, Y, stream=None, raise_on_error=True):
+    """cq_gemm_q4 without a caller workspace: for callers that cannot
+    allocate device memory; the scratch is a fixed array inside the library
+    (see include/cq.h for the size limit and the sharing rules)."""
+    T, K = X.shape
+    N = Wq.shape[0]
+    st = lib().cq_gemm_q4_noalloc(_ptr(X), _xt(X), T, K, _ptr(Wq), _ptr(Ws), N, _ptr(Y), _xt(Y), _stream(stream))
     if raise_on_error:
         _check(st)
     return st

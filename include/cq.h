@@ -80,6 +80,33 @@ cq_status cq_gemm_q4(const void* X, int xt, int64_t T, int64_t K,
                      void* Y, int yt, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Q4 GEMM without caller scratch:  the same result as cq_gemm_q4 (same
+ * kernels, same arithmetic), for callers that cannot allocate device memory
+ * or hand out a workspace -- for example a plugin inside a host framework
+ * that owns every device allocation, a runtime whose memory budget is fixed
+ * in advance, or a latency-critical loop that must not call cudaMalloc /
+ * cudaFree (which can synchronise the device).  The pages have no
+ * counterpart of this entry point.
+ *
+ * The guarded fp16 copy of X and its per-row scales live in one fixed array
+ * of CQ_NOALLOC_SCRATCH_BYTES inside the library; every GPU that loads the
+ * library holds it until the process exits.  Limit: round256(T*K*2) +
+ * round256(T*4) <= CQ_NOALLOC_SCRATCH_BYTES, else CQ_ERR_SHAPE (use
+ * cq_gemm_q4 with a workspace).  The entry point allocates nothing.
+ * The first call on a device looks up the array's device address for that
+ * device (with it current); make that first call before any stream capture.
+ * Nothing in the array needs to start at zero.  All calls share the array
+ * and it keeps the last call's contents, so calls that can overlap on the
+ * GPU (different streams, different host threads on one device) race: order
+ * them on one stream or serialise them.
+ * Same arguments, shape rules and errors as cq_gemm_q4, without ws/ws_bytes.
+ * ------------------------------------------------------------------------- */
+#define CQ_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+cq_status cq_gemm_q4_noalloc(const void* X, int xt, int64_t T, int64_t K,
+                             const uint8_t* Wq, const uint16_t* Ws, int64_t N,
+                             void* Y, int yt, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Q8-row GEMM:  Y[T][N] = (X[T][K] . Wq[N][K]^T) * rs[N]
  *
  * X: fp16 or bf16 [T][K]; the int8 weights are converted exactly to the
