@@ -255,19 +255,51 @@ def run_ours(args, rank, world, local_rank):
 
     clocks = Clocks(local_rank)
     clocks.start()
-    # per-call events (dominant kernel timing) on the launching stream
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in rot[0]]
-          for _ in range(args.steps)]
+    # The timed region: K steps, with an event pair around every call (on the
+    # launching stream).  By default the whole region is captured once into a
+    # CUDA graph and replayed, so host-side launch overhead does not leave the
+    # GPU idle between the short calls; --eager times direct calls instead.
+    timing = "eager"
+    graph = None
+    ev = None
+    if not args.eager:
+        try:
+            ev = [[(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in rot[0]]
+                  for _ in range(args.steps)]
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                cap = torch.cuda.current_stream()
+                for i in range(args.steps):
+                    for j, c in enumerate(rot[i % sets]):
+                        ev[i][j][0].record(cap)
+                        c.fn()
+                        ev[i][j][1].record(cap)
+            timing = "cuda-graph replay"
+        except Exception as exc:          # e.g. no external events in this torch
+            print(f"bench: graph capture unavailable ({exc!r}); timing direct calls", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
+            cq.cq_get_device_error()
+    if graph is None:
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in rot[0]]
+              for _ in range(args.steps)]
+    else:
+        graph.replay()                    # one untimed replay
+        torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(args.steps):
-        for j, c in enumerate(rot[i % sets]):
-            ev[i][j][0].record(stream)
-            c.fn()
-            ev[i][j][1].record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            for j, c in enumerate(rot[i % sets]):
+                ev[i][j][0].record(stream)
+                c.fn()
+                ev[i][j][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -345,6 +377,7 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "q4:fp16xfp16->f32, q8row:bf16xbf16->f32", "data": "synthetic (seeded)",
         "config": {"workload": args.workload, **info, "parallelism": f"replicas x{world}",
+                   "timing": timing,
                    "l2": f"rotating {sets} input sets ({sets * sum(c.weight_bytes + c.other_bytes for c in calls) / 2**20:.0f} MiB) > L2"},
         "weight_gbs": round(wgbs, 1),
         "per_call_ms": {c.name: round(t, 5) for c, t in zip(calls, per_call_ms)},
@@ -478,6 +511,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_projection_4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time direct calls instead of a captured CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

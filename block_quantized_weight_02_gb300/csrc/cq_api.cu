@@ -99,7 +99,7 @@ Q4Ws q4_ws(void* ws, int64_t T, int64_t K) {
 }
 
 struct MoeLayout {
-    size_t status, seg, perm, inv, xh, rsx, a, ah, rsa, eo, total;
+    size_t status, seg, perm, inv, act, xh, rsx, a, ah, rsa, eo, total;
 };
 MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
     const size_t P = (size_t)(T * topk);
@@ -109,8 +109,9 @@ MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
     l.seg = o; o += up((size_t)(E + 1) * 4);
     l.perm = o; o += up(P * 4);
     l.inv = o; o += up(P * 4);
-    l.xh = o; o += up((size_t)T * H * 2);
-    l.rsx = o; o += up((size_t)T * 4);
+    l.act = o; o += up((size_t)(E + 1) * 4);   // active experts, then their count
+    l.xh = o; o += up(P * H * 2);
+    l.rsx = o; o += up(P * 4);
     l.a = o; o += up(P * I * 4);
     l.ah = o; o += up(P * I * 2);
     l.rsa = o; o += up(P * 4);
@@ -164,6 +165,14 @@ cq_status cq_set_option(int option, int64_t value) {
         case CQ_OPT_TRACE:
             o.trace = value != 0;
             return CQ_OK;
+        case CQ_OPT_TC_BN:
+            if (value != 0 && value != 64 && value != 128 && value != 256) return fail(CQ_ERR_ARG, "token tile must be 0, 64, 128 or 256");
+            o.tc_bn = value;
+            return CQ_OK;
+        case CQ_OPT_TC_CLUSTER:
+            if (value != 0 && value != 1 && value != 2 && value != 4) return fail(CQ_ERR_ARG, "cluster size must be 0, 1, 2 or 4");
+            o.tc_cluster = value;
+            return CQ_OK;
         default:
             return fail(CQ_ERR_ARG, "unknown option %d", option);
     }
@@ -177,6 +186,8 @@ int64_t cq_get_option(int option) {
         case CQ_OPT_WAIT_NS: return o.wait_ns;
         case CQ_OPT_TEST_STALL: return o.test_stall;
         case CQ_OPT_TRACE: return o.trace;
+        case CQ_OPT_TC_BN: return o.tc_bn;
+        case CQ_OPT_TC_CLUSTER: return o.tc_cluster;
         default: return -1;
     }
 }
@@ -276,8 +287,11 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E, 
     m.E = E;
     m.topk = topk;
     int32_t* inv = reinterpret_cast<int32_t*>(b + l.inv);
-    if ((st = launched(launch_moe_route(idx, T, topk, E, const_cast<int32_t*>(m.seg), const_cast<int32_t*>(m.perm), inv, status, s), "MoE routing layout"))) return st;
-    if ((st = launched(launch_x_half(X, xt, T, H, const_cast<uint16_t*>(m.xh), const_cast<float*>(m.rsx), s), "MoE activation guard pass"))) return st;
+    int32_t* act = reinterpret_cast<int32_t*>(b + l.act);
+    m.act = act;
+    m.n_act = act + E;
+    if ((st = launched(launch_moe_route(idx, T, topk, E, const_cast<int32_t*>(m.seg), const_cast<int32_t*>(m.perm), inv, act, act + E, status, s), "MoE routing layout"))) return st;
+    if ((st = launched(launch_x_half_gather(X, xt, T * topk, H, const_cast<uint16_t*>(m.xh), const_cast<float*>(m.rsx), m.perm, (int)topk, status, s), "MoE activation gather + guard pass"))) return st;
     if ((st = launched(launch_moe_gateup(m, s), "MoE gate/up panels"))) return st;
     if ((st = launched(launch_a_half(m.a, T * topk, I, const_cast<uint16_t*>(m.ah), const_cast<float*>(m.rsa), status, s), "MoE SwiGLU guard pass"))) return st;
     if ((st = launched(launch_moe_down(m, s), "MoE down panels"))) return st;

@@ -19,6 +19,8 @@ struct Options {
     int64_t wait_ns = 1000000000LL;
     int64_t test_stall = 0;
     int64_t trace = 0;
+    int64_t tc_bn = 0;
+    int64_t tc_cluster = 0;
 };
 Options& options();
 
@@ -46,10 +48,14 @@ cudaError_t launch_dequant_q4(const uint8_t* wq, const uint16_t* ws, int64_t N, 
 cudaError_t launch_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, int64_t K, float* w, cudaStream_t s);
 // X rows -> fp16 with a per-row power-of-two guard; rsx = inverse scales.
 cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s);
+// The same for gathered rows: output row r <- input row gather[r] / per.
+cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K, uint16_t* xh, float* rsx,
+                                 const int32_t* gather, int per, const int32_t* status, cudaStream_t s);
 
 struct MoeWs;  // workspace carve-up (cq_api.cu)
+// Also writes the active experts (count > 0, ascending) to act[] and their number to *n_act.
 cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
-                             int32_t* inv, int32_t* status, cudaStream_t s);
+                             int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, cudaStream_t s);
 cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,
                           cudaStream_t s);
 cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, int64_t topk, int64_t H, void* y,
@@ -71,14 +77,16 @@ cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s);
 cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s);
 
 struct SkinnyMoe {
-    const uint16_t* xh;     // [T][H] fp16 (guarded)
-    const float* rsx;       // [T]
+    const uint16_t* xh;     // [P][H] fp16 (guarded), rows gathered into grouped order
+    const float* rsx;       // [P]
     const uint16_t* ah;     // [P][I] fp16 (guarded), grouped order
     const float* rsa;       // [P]
     const float* w;         // routing weights [T*topk] (pair id order)
     const int32_t* seg;     // [E+1]
     const int32_t* perm;    // [P] pair ids in grouped order
     const int32_t* status;  // non-zero: skip
+    const int32_t* act;     // [E] active experts, ascending
+    const int32_t* n_act;   // number of active experts
     const uint8_t *gu_q, *d_q;
     const uint16_t *gu_s, *d_s;
     float* a;               // [P][I] f32 SwiGLU output, grouped order

@@ -5,6 +5,7 @@
 #include <cuda_fp16.h>
 
 #include "cq_internal.h"
+#include "cq_ptx.cuh"
 
 namespace cq {
 
@@ -91,13 +92,19 @@ __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// One CTA of 256 threads per row; K % 8 == 0.
+// One CTA of 256 threads per output row; K % 8 == 0.  With a gather list,
+// output row r is source row gather[r] / per (the MoE pairs in grouped
+// order, as the pages' x_half gathers through `src`).
 template <typename T>
 __global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t K, __half* __restrict__ xh,
-                                                float* __restrict__ rsx) {
+                                                float* __restrict__ rsx, const int32_t* __restrict__ gather, int per,
+                                                const int32_t* __restrict__ status) {
+    pdl_launch_dependents();   // the GEMM after this pass may start streaming its weights
+    if (status && *status != 0) return;
     __shared__ float red[8];
     const int64_t row = blockIdx.x;
-    const uint4* src = reinterpret_cast<const uint4*>(x + row * K);
+    const int64_t src_row = gather ? (int64_t)(gather[row] / per) : row;
+    const uint4* src = reinterpret_cast<const uint4*>(x + src_row * K);
     const int64_t n8 = K / 8;
     float m = 0.f;
     for (int64_t i = threadIdx.x; i < n8; i += 256) {
@@ -124,12 +131,17 @@ __global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t
 }
 
 cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s) {
+    return launch_x_half_gather(x, xt, T, K, xh, rsx, nullptr, 1, nullptr, s);
+}
+
+cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K, uint16_t* xh, float* rsx,
+                                 const int32_t* gather, int per, const int32_t* status, cudaStream_t s) {
     if (xt == CQ_BF16)
-        k_x_half<__nv_bfloat16><<<(unsigned)T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), K,
-                                                            reinterpret_cast<__half*>(xh), rsx);
+        k_x_half<__nv_bfloat16><<<(unsigned)rows, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), K,
+                                                               reinterpret_cast<__half*>(xh), rsx, gather, per, status);
     else
-        k_x_half<__half><<<(unsigned)T, 256, 0, s>>>(reinterpret_cast<const __half*>(x), K,
-                                                     reinterpret_cast<__half*>(xh), rsx);
+        k_x_half<__half><<<(unsigned)rows, 256, 0, s>>>(reinterpret_cast<const __half*>(x), K,
+                                                        reinterpret_cast<__half*>(xh), rsx, gather, per, status);
     return cudaGetLastError();
 }
 
@@ -143,7 +155,8 @@ cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t*
 //   status   = 0, or 1 if an index is outside [0, E) (nothing else written)
 __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ idx, int P, int E,
                                                    int32_t* __restrict__ seg, int32_t* __restrict__ perm,
-                                                   int32_t* __restrict__ inv, int32_t* __restrict__ status) {
+                                                   int32_t* __restrict__ inv, int32_t* __restrict__ act,
+                                                   int32_t* __restrict__ n_act, int32_t* __restrict__ status) {
     extern __shared__ int sh[];
     int* cnt = sh;            // [E]
     int* fill = sh + E;       // [E]
@@ -168,13 +181,15 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
         return;
     }
     if (threadIdx.x == 0) {
-        int acc = 0;
+        int acc = 0, na = 0;
         for (int e = 0; e < E; ++e) {
             seg[e] = acc;
             fill[e] = acc;
             acc += cnt[e];
+            if (cnt[e] > 0) act[na++] = e;
         }
         seg[E] = acc;
+        *n_act = na;
     }
     __syncthreads();
     for (int base = 0; base < P; base += 256) {
@@ -197,9 +212,9 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
 }
 
 cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
-                             int32_t* inv, int32_t* status, cudaStream_t s) {
+                             int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, cudaStream_t s) {
     const size_t smem = (size_t)(2 * E + 256) * sizeof(int);
-    k_moe_route<<<1, 256, smem, s>>>(idx, (int)(T * topk), (int)E, seg, perm, inv, status);
+    k_moe_route<<<1, 256, smem, s>>>(idx, (int)(T * topk), (int)E, seg, perm, inv, act, n_act, status);
     return cudaGetLastError();
 }
 

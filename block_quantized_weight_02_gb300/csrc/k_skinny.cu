@@ -5,14 +5,15 @@
 // activation rows (tokens or routed pairs) in N, so a small T only narrows
 // N.  One CTA owns 64 weight rows and a contiguous range of K:
 //  - a producer warp streams the packed weights (and, for Q4, the fp16
-//    block scales) into a shared-memory ring with TMA, one stage per
+//    block scales) and the matching slice of the activations (fp16/bf16,
+//    128-byte swizzled) into a shared-memory ring with TMA, one stage per
 //    256 k (Q4) or 128 k (Q8), each stage tracked by full/empty mbarriers;
-//  - eight consumer warps take the stages round-robin, decode the weights
+//  - four consumer warps take the stages round-robin, decode the weights
 //    from shared memory straight into mma.sync A fragments (Q4:
 //    (nibble - 8) * scale rounded once to fp16; Q8: int8 converted exactly
 //    to the activation type) and multiply with activation fragments read
-//    from global memory (L1/L2 resident);
-//  - the eight partial tiles are summed in a fixed order in shared memory,
+//    from the same stage;
+//  - the four partial tiles are summed in a fixed order in shared memory,
 //    and, when K is split across a thread-block cluster, the CTAs' partial
 //    tiles are summed in rank order through distributed shared memory, so
 //    results are deterministic.
@@ -24,6 +25,7 @@
 // Prior art on the pages: the 8-row expert panels ("cortiq-engine 0.8.41
 // src/gpu_metal/clover.rs", q4tp_mul_mm_n8) and the 32-token MMA tiles for
 // short inputs ("oxinfer 0.0.5 src/metal.rs", mma_tile with TM = 32).
+#include <algorithm>
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -48,7 +50,7 @@ namespace {
 
 constexpr int RB = 64;           // weight rows per CTA (two TMA row boxes of 32)
 constexpr int MT = 4;            // m16 tiles per consumer warp
-constexpr int CONSUMERS = 8;     // consumer warps
+constexpr int CONSUMERS = 4;     // consumer warps (two CTAs share an SM)
 constexpr int THREADS = (CONSUMERS + 1) * 32;
 constexpr int BOX_BYTES = 32 * 64;  // one TMA box: 32 rows x 64 bytes
 
@@ -77,6 +79,10 @@ struct Params {
     int topk;
     int64_t I, H;
     uint64_t wait_ns;
+    int pdl;              // launched with a programmatic dependency on the previous kernel
+    const int32_t* act;   // MoE: active experts, ascending
+    const int32_t* n_act; // MoE: number of active experts
+    int rbs;              // MoE: row blocks per expert matrix
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -105,55 +111,93 @@ __device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t w, uint32_t sel) {
     const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
     return *reinterpret_cast<const uint32_t*>(&r);
 }
+// int8 pair (bytes lo_byte, lo_byte+1 of w) -> bf16x2 exactly: 0x4B0000uu is
+// the f32 2^23 + u with u = v + 128; subtracting 2^23 + 128 leaves v.
 __device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, int lo_byte) {
-    const float a = (float)(int)(int8_t)((w >> (8 * lo_byte)) & 0xFF);
-    const float b = (float)(int)(int8_t)((w >> (8 * (lo_byte + 1))) & 0xFF);
+    const uint32_t wx = w ^ 0x80808080u;
+    const float a = __uint_as_float(prmt(wx, 0x4B000000u, 0x7440u + (uint32_t)lo_byte)) - 8388736.0f;
+    const float b = __uint_as_float(prmt(wx, 0x4B000000u, 0x7441u + (uint32_t)lo_byte)) - 8388736.0f;
     const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <int FMT>
+template <int FMT, int NCOL>
 struct StageGeo;
-template <>
-struct StageGeo<0> {                       // Q4: 256 k per stage
+template <int NCOL>
+struct StageGeo<0, NCOL> {                 // Q4: 256 k per stage
     static constexpr int KSTAGE = 256;
     static constexpr int W_BYTES = 4 * BOX_BYTES;     // [kh 2][rbox 2][32][64 B]
     static constexpr int S_BYTES = 2 * 32 * 16;       // [rbox 2][32][8 fp16]
-    static constexpr int BYTES = W_BYTES + S_BYTES;
+    static constexpr int XBOXES = 4;                  // 64-k boxes of activations
+    static constexpr int X_OFF = W_BYTES + S_BYTES;   // 1024-aligned
+    static constexpr int XBOX = NCOL * 128;           // [NCOL rows][64 x 16-bit], 128-byte swizzle
+    static constexpr int BYTES = X_OFF + XBOXES * XBOX;
 };
-template <>
-struct StageGeo<1> {                       // Q8: 128 k per stage
+template <int NCOL>
+struct StageGeo<1, NCOL> {                 // Q8: 128 k per stage
     static constexpr int KSTAGE = 128;
     static constexpr int W_BYTES = 4 * BOX_BYTES;     // [kh 2][rbox 2][32][64 B]
-    static constexpr int S_BYTES = 0;
-    static constexpr int BYTES = W_BYTES;
+    static constexpr int XBOXES = 2;
+    static constexpr int X_OFF = W_BYTES;
+    static constexpr int XBOX = NCOL * 128;
+    static constexpr int BYTES = X_OFF + XBOXES * XBOX;
 };
 
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
 template <int FMT, int NT, int XBF, int MODE, int NSLOT>
-__global__ void __launch_bounds__(THREADS, 1)
-k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS, const Params p) {
-    using G = StageGeo<FMT>;
+__global__ void __launch_bounds__(THREADS, 2)
+k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
+         const __grid_constant__ CUtensorMap tmX, const Params p) {
     constexpr int NCOL = 8 * NT;
+    using G = StageGeo<FMT, NCOL>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int rb = blockIdx.y;
-    const int expert = blockIdx.z;
-
-    // ---- which columns (activation rows) this CTA serves ----
-    int64_t ncols_total;
-    int64_t col0 = 0;  // grouped-position base (MoE)
-    if (MODE == DENSE) {
-        ncols_total = p.T;
-    } else {
+    // ---- work items: (expert, row block) pairs; each may hold several column groups ----
+    // dense: one item per CTA (row block blockIdx.y, k range blockIdx.x of the cluster);
+    // MoE: a static round-robin share of (active expert x row block), so the
+    // weight stream of one CTA continues across items without refilling.
+    int nitems = 1, first = 0, stride = 1;
+    if (MODE != DENSE) {
+        pdl_wait();   // the routing layout and gathered rows come from the previous kernels
         if (*p.status != 0) return;
-        col0 = p.seg[expert];
-        ncols_total = p.seg[expert + 1] - col0;
-        if (ncols_total == 0) return;
+        nitems = *p.n_act * p.rbs;
+        first = blockIdx.x;
+        stride = gridDim.x;
+        if (first >= nitems) return;
     }
-    const int ngroups = (int)((ncols_total + NCOL - 1) / NCOL);
+    struct Item {
+        int expert, rb;
+        int64_t col0, ncols;
+        int ngroups;
+        int row_box[2];
+    };
+    auto get_item = [&](int idx) {
+        Item it;
+        if (MODE == DENSE) {
+            it.expert = 0;
+            it.rb = blockIdx.y;
+            it.col0 = 0;
+            it.ncols = p.T;
+        } else {
+            it.expert = p.act[idx / p.rbs];
+            it.rb = idx % p.rbs;
+            it.col0 = p.seg[it.expert];
+            it.ncols = p.seg[it.expert + 1] - it.col0;
+        }
+        it.ngroups = (int)((it.ncols + NCOL - 1) / NCOL);
+        if (MODE == GATEUP) {
+            it.row_box[0] = it.rb * 32;
+            it.row_box[1] = (int)p.I + it.rb * 32;
+        } else {
+            it.row_box[0] = it.rb * RB;
+            it.row_box[1] = it.rb * RB + 32;
+        }
+        return it;
+    };
 
     // ---- k range ----
     const int ks = MODE == DENSE ? (int)blockIdx.x : 0;
@@ -189,44 +233,69 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     }
     __syncthreads();
 
-    // rows of the two 32-row boxes
-    int row_box[2];
-    if (MODE == GATEUP) {
-        row_box[0] = rb * 32;
-        row_box[1] = (int)p.I + rb * 32;
-    } else {
-        row_box[0] = rb * RB;
-        row_box[1] = rb * RB + 32;
-    }
-
     if (warp == CONSUMERS) {
         // ================= producer =================
         if (lane == 0) {
             tma_prefetch_desc(&tmW);
             if (FMT == 0) tma_prefetch_desc(&tmS);
+            tma_prefetch_desc(&tmX);
             int64_t issued = 0;
             bool ok = true;
-            for (int grp = 0; grp < ngroups && ok; ++grp) {
-                for (int i = 0; i < nst; ++i) {
-                    const int64_t gi = (int64_t)grp * nst + i;
-                    const int slot = (int)(gi % NSLOT);
-                    const uint32_t par = (uint32_t)((gi / NSLOT) & 1);
-                    if (!mbar_wait(empty_bar(slot), par ^ 1u, p.wait_ns, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sbase = smem_base + (uint32_t)(slot * G::BYTES);
-                    mbar_arrive_expect_tx(full_bar(slot), (uint32_t)G::BYTES);
-                    const int st = st0 + i;
-                    for (int kh = 0; kh < 2; ++kh)
-                        for (int bx = 0; bx < 2; ++bx)
-                            tma_load_3d(sbase + (uint32_t)((kh * 2 + bx) * BOX_BYTES), &tmW, full_bar(slot),
-                                        st * 128 + kh * 64, row_box[bx], expert);
-                    if (FMT == 0)
-                        for (int bx = 0; bx < 2; ++bx)
-                            tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * 512), &tmS, full_bar(slot), st * 8,
-                                        row_box[bx], expert);
+            auto load_w = [&](const Item& it, int i, int slot) {
+                const uint32_t sbase = smem_base + (uint32_t)(slot * G::BYTES);
+                const int st = st0 + i;
+                for (int kh = 0; kh < 2; ++kh)
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_3d(sbase + (uint32_t)((kh * 2 + bx) * BOX_BYTES), &tmW, full_bar(slot),
+                                    st * 128 + kh * 64, it.row_box[bx], it.expert);
+                if (FMT == 0)
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * 512), &tmS, full_bar(slot), st * 8,
+                                    it.row_box[bx], it.expert);
+            };
+            auto load_x = [&](const Item& it, int i, int slot, int grp) {
+                const uint32_t sbase = smem_base + (uint32_t)(slot * G::BYTES);
+                const int st = st0 + i;
+                // activation rows of this column group (dense: tokens; MoE: grouped pairs)
+                const int xrow0 = (int)(it.col0 + (int64_t)grp * NCOL);
+                for (int xb = 0; xb < G::XBOXES; ++xb)
+                    tma_load_2d(sbase + (uint32_t)(G::X_OFF + xb * G::XBOX), &tmX, full_bar(slot),
+                                st * G::KSTAGE + 64 * xb, xrow0);
+            };
+            int64_t gi = 0;
+            // With a programmatic dependency (dense Q4: the activation guard pass runs just
+            // before), the weights of the first ring fill are requested before waiting for
+            // the activations; everything else follows the wait.
+            int pre = 0;
+            if (MODE == DENSE) {
+                const Item it0 = get_item(0);
+                pre = p.pdl ? (nst < NSLOT ? nst : NSLOT) : 0;
+                for (int i = 0; i < pre; ++i) {            // fresh slots: no empty wait needed
+                    mbar_arrive_expect_tx(full_bar(i), (uint32_t)G::BYTES);
+                    load_w(it0, i, i);
+                }
+                pdl_wait();
+                for (int i = 0; i < pre; ++i) {
+                    load_x(it0, i, i, 0);
                     ++issued;
+                }
+                gi = pre;
+            }
+            for (int idx = first; idx < nitems && ok; idx += stride) {
+                const Item it = get_item(idx);
+                for (int grp = 0; grp < it.ngroups && ok; ++grp) {
+                    for (int i = (idx == first && grp == 0) ? pre : 0; i < nst; ++i, ++gi) {
+                        const int slot = (int)(gi % NSLOT);
+                        const uint32_t par = (uint32_t)((gi / NSLOT) & 1);
+                        if (!mbar_wait(empty_bar(slot), par ^ 1u, p.wait_ns, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full_bar(slot), (uint32_t)G::BYTES);
+                        load_w(it, i, slot);
+                        load_x(it, i, slot, grp);
+                        ++issued;
+                    }
                 }
             }
             if (!ok) {
@@ -241,23 +310,13 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
         __syncwarp();
     } else {
         // ================= consumers =================
-        for (int grp = 0; grp < ngroups; ++grp) {
+        int64_t gbase = 0;   // global index of the first stage of the current column group
+        for (int idx = first; idx < nitems; idx += stride) {
+          const Item it = get_item(idx);
+          const int64_t col0 = it.col0, ncols_total = it.ncols;
+          const int rb = it.rb;
+          for (int grp = 0; grp < it.ngroups; ++grp, gbase += nst) {
             const int64_t cbase = (int64_t)grp * NCOL;
-            // activation row pointers for this thread's columns (col = 8*nt + g)
-            const uint16_t* xrow[NT];
-            bool xval[NT];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int64_t col = cbase + 8 * nt + g;
-                xval[nt] = col < ncols_total;
-                int64_t r = 0;
-                if (xval[nt]) {
-                    if (MODE == DENSE) r = col;
-                    else if (MODE == GATEUP) r = p.perm[col0 + col] / p.topk;
-                    else r = col0 + col;
-                }
-                xrow[nt] = p.x + r * p.K;
-            }
             float acc[MT][NT][4];
 #pragma unroll
             for (int a = 0; a < MT; ++a)
@@ -268,7 +327,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
 
             bool ok = !*abort_flag;
             for (int i = warp; i < nst && ok; i += CONSUMERS) {
-                const int64_t gi = (int64_t)grp * nst + i;
+                const int64_t gi = gbase + i;
                 const int slot = (int)(gi % NSLOT);
                 if (!mbar_wait(full_bar(slot), (uint32_t)((gi / NSLOT) & 1), p.wait_ns, abort_flag)) {
                     ok = false;
@@ -277,89 +336,83 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                     break;
                 }
                 const uint8_t* sW = smem + slot * G::BYTES;
-                const int64_t kst = (int64_t)(st0 + i) * G::KSTAGE;
+                const uint8_t* sX = sW + G::X_OFF;
                 if (FMT == 0) {
                     const __half* sS = reinterpret_cast<const __half*>(sW + G::W_BYTES);
 #pragma unroll
                     for (int kh = 0; kh < 2; ++kh) {
-                        const int64_t kc = kst + kh * 128;
-                        uint32_t bw[NT][16];
+                        // this thread's 64-byte activation span (k = 128 kh + 32 c .. +31) of each column
+                        const uint8_t* xbox = sX + (2 * kh + (c >> 1)) * G::XBOX;
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            if (xval[nt]) {
-                                const uint16_t* src = xrow[nt] + kc + 32 * c;
+                        for (int sp = 0; sp < 2; ++sp) {
+                            // words 4sp..4sp+3 (low-nibble steps 2sp, 2sp+1) and 8+4sp.. (high-nibble steps)
+                            uint4 blo[NT], bhi[NT];
 #pragma unroll
-                                for (int v = 0; v < 4; ++v) {
-                                    const uint4 q = ld_nc_v4(src + 8 * v);
-                                    bw[nt][4 * v] = q.x; bw[nt][4 * v + 1] = q.y; bw[nt][4 * v + 2] = q.z; bw[nt][4 * v + 3] = q.w;
-                                }
-                            } else {
-#pragma unroll
-                                for (int v = 0; v < 16; ++v) bw[nt][v] = 0u;
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const int row = 8 * nt + g;
+                                const uint8_t* xr = xbox + row * 128;
+                                blo[nt] = lds128(xr + (((4 * (c & 1) + sp) ^ g) << 4));
+                                bhi[nt] = lds128(xr + (((4 * (c & 1) + 2 + sp) ^ g) << 4));
                             }
-                        }
 #pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            const int bx = mt >> 1, lr = 16 * (mt & 1) + g;
-                            const uint8_t* box = sW + (kh * 2 + bx) * BOX_BYTES;
-                            const uint4 w0 = *reinterpret_cast<const uint4*>(box + lr * 64 + 16 * c);
-                            const uint4 w1 = *reinterpret_cast<const uint4*>(box + (lr + 8) * 64 + 16 * c);
-                            const __half s0 = sS[(bx * 32 + lr) * 8 + kh * 4 + c];
-                            const __half s1 = sS[(bx * 32 + lr + 8) * 8 + kh * 4 + c];
-                            const __half2 s0h = __halves2half2(s0, s0), s1h = __halves2half2(s1, s1);
-                            const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
-                            const uint32_t r1[4] = {w1.x, w1.y, w1.z, w1.w};
+                            for (int mt = 0; mt < MT; ++mt) {
+                                // (re)read this m-tile's two weight rows and scales: cheap shared loads
+                                // instead of keeping all four m-tiles live in registers
+                                const int bx = mt >> 1, lr = 16 * (mt & 1) + g;
+                                const uint8_t* box = sW + (kh * 2 + bx) * BOX_BYTES;
+                                const uint4 wa = lds128(box + lr * 64 + 16 * c);
+                                const uint4 wb = lds128(box + (lr + 8) * 64 + 16 * c);
+                                const __half s0 = sS[(bx * 32 + lr) * 8 + kh * 4 + c];
+                                const __half s1 = sS[(bx * 32 + lr + 8) * 8 + kh * 4 + c];
+                                const __half2 sa = __halves2half2(s0, s0), sb2 = __halves2half2(s1, s1);
+                                const uint32_t r0[4] = {wa.x, wa.y, wa.z, wa.w};
+                                const uint32_t r1[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-                            for (int s = 0; s < 4; ++s) {
-                                const uint32_t p0 = prmt(r0[s], 0u, 0x3120u), p1 = prmt(r1[s], 0u, 0x3120u);
-                                uint32_t alo[4], ahi[4];
-                                alo[0] = hmul2_u32(nib2_to_h2(p0), s0h);
-                                alo[1] = hmul2_u32(nib2_to_h2(p1), s1h);
-                                alo[2] = hmul2_u32(nib2_to_h2(p0 >> 8), s0h);
-                                alo[3] = hmul2_u32(nib2_to_h2(p1 >> 8), s1h);
-                                ahi[0] = hmul2_u32(nib2_to_h2(p0 >> 4), s0h);
-                                ahi[1] = hmul2_u32(nib2_to_h2(p1 >> 4), s1h);
-                                ahi[2] = hmul2_u32(nib2_to_h2(p0 >> 12), s0h);
-                                ahi[3] = hmul2_u32(nib2_to_h2(p1 >> 12), s1h);
+                                for (int u = 0; u < 2; ++u) {
+                                    const int s = 2 * sp + u;
+                                    const uint32_t p0 = prmt(r0[s], 0u, 0x3120u), p1 = prmt(r1[s], 0u, 0x3120u);
+                                    uint32_t alo[4], ahi[4];
+                                    alo[0] = hmul2_u32(nib2_to_h2(p0), sa);
+                                    alo[1] = hmul2_u32(nib2_to_h2(p1), sb2);
+                                    alo[2] = hmul2_u32(nib2_to_h2(p0 >> 8), sa);
+                                    alo[3] = hmul2_u32(nib2_to_h2(p1 >> 8), sb2);
+                                    ahi[0] = hmul2_u32(nib2_to_h2(p0 >> 4), sa);
+                                    ahi[1] = hmul2_u32(nib2_to_h2(p1 >> 4), sb2);
+                                    ahi[2] = hmul2_u32(nib2_to_h2(p0 >> 12), sa);
+                                    ahi[3] = hmul2_u32(nib2_to_h2(p1 >> 12), sb2);
 #pragma unroll
-                                for (int nt = 0; nt < NT; ++nt) {
-                                    mma_16816_f16(acc[mt][nt], alo, bw[nt][2 * s], bw[nt][2 * s + 1]);
-                                    mma_16816_f16(acc[mt][nt], ahi, bw[nt][2 * s + 8], bw[nt][2 * s + 9]);
+                                    for (int nt = 0; nt < NT; ++nt) {
+                                        const uint32_t l0 = u ? blo[nt].z : blo[nt].x, l1 = u ? blo[nt].w : blo[nt].y;
+                                        const uint32_t h0 = u ? bhi[nt].z : bhi[nt].x, h1 = u ? bhi[nt].w : bhi[nt].y;
+                                        mma_16816_f16(acc[mt][nt], alo, l0, l1);
+                                        mma_16816_f16(acc[mt][nt], ahi, h0, h1);
+                                    }
                                 }
                             }
                         }
                     }
                 } else {
-                    const int64_t kc = kst;
-                    uint32_t bw[NT][16];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (xval[nt]) {
-                            const uint16_t* src = xrow[nt] + kc + 16 * c;
-                            const uint4 q0 = ld_nc_v4(src), q1 = ld_nc_v4(src + 8);
-                            const uint4 q2 = ld_nc_v4(src + 64), q3 = ld_nc_v4(src + 72);
-                            bw[nt][0] = q0.x; bw[nt][1] = q0.y; bw[nt][2] = q0.z; bw[nt][3] = q0.w;
-                            bw[nt][4] = q1.x; bw[nt][5] = q1.y; bw[nt][6] = q1.z; bw[nt][7] = q1.w;
-                            bw[nt][8] = q2.x; bw[nt][9] = q2.y; bw[nt][10] = q2.z; bw[nt][11] = q2.w;
-                            bw[nt][12] = q3.x; bw[nt][13] = q3.y; bw[nt][14] = q3.z; bw[nt][15] = q3.w;
-                        } else {
+                    for (int kh = 0; kh < 2; ++kh) {
+                        // activations k = 64 kh + 16 c .. +15 of each column (box kh, chunks 2c, 2c+1)
+                        const uint8_t* xbox = sX + kh * G::XBOX;
+                        uint4 b0[NT], b1[NT];
 #pragma unroll
-                            for (int v = 0; v < 16; ++v) bw[nt][v] = 0u;
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const int row = 8 * nt + g;
+                            b0[nt] = lds128(xbox + row * 128 + (((2 * c) ^ g) << 4));
+                            b1[nt] = lds128(xbox + row * 128 + (((2 * c + 1) ^ g) << 4));
                         }
-                    }
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        const int bx = mt >> 1, lr = 16 * (mt & 1) + g;
-#pragma unroll
-                        for (int kh = 0; kh < 2; ++kh) {
+                        for (int mt = 0; mt < MT; ++mt) {
+                            const int bx = mt >> 1, lr = 16 * (mt & 1) + g;
                             const uint8_t* box = sW + (kh * 2 + bx) * BOX_BYTES;
-                            const uint4 w0 = *reinterpret_cast<const uint4*>(box + lr * 64 + 16 * c);
-                            const uint4 w1 = *reinterpret_cast<const uint4*>(box + (lr + 8) * 64 + 16 * c);
+                            const uint4 w0 = lds128(box + lr * 64 + 16 * c);
+                            const uint4 w1 = lds128(box + (lr + 8) * 64 + 16 * c);
                             const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
                             const uint32_t r1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                             for (int s4 = 0; s4 < 4; ++s4) {
-                                const int s = kh * 4 + s4;
                                 uint32_t a[4];
                                 if (XBF) {
                                     a[0] = i8x2_to_bf2(r0[s4], 0);
@@ -374,8 +427,11 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                                 }
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
-                                    if (XBF) mma_16816_bf16(acc[mt][nt], a, bw[nt][2 * s], bw[nt][2 * s + 1]);
-                                    else mma_16816_f16(acc[mt][nt], a, bw[nt][2 * s], bw[nt][2 * s + 1]);
+                                    // words 2 s4, 2 s4 + 1 of the 16-k run
+                                    const uint4& bb = s4 < 2 ? b0[nt] : b1[nt];
+                                    const uint32_t x0 = (s4 & 1) ? bb.z : bb.x, x1 = (s4 & 1) ? bb.w : bb.y;
+                                    if (XBF) mma_16816_bf16(acc[mt][nt], a, x0, x1);
+                                    else mma_16816_f16(acc[mt][nt], a, x0, x1);
                                 }
                             }
                         }
@@ -417,8 +473,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                         const int64_t q = cbase + col;
                         if (q >= ncols_total) continue;
                         const int64_t pos = col0 + q;
-                        const int tok = p.perm[pos] / p.topk;
-                        const float sc = p.rsx[tok];
+                        const float sc = p.rsx[pos];
                         const float gv = part[i * NCOL + col] * sc;
                         const float uv = part[(32 + i) * NCOL + col] * sc;
                         p.out[pos * p.I + (int64_t)rb * 32 + i] = gv / (1.0f + expf(-gv)) * uv;
@@ -435,10 +490,13 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 }
                 asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
             }
+          }
         }
     }
 
     if (MODE == DENSE) {
+        const int rb = blockIdx.y;
+        pdl_wait();   // outputs and guard scales only after the previous kernel has finished
         // ---- sum the cluster's partial tiles in rank order, epilogue ----
         if (p.ks > 1) {
             cg::cluster_group cluster = cg::this_cluster();
@@ -475,9 +533,9 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
 }
 
 template <int FMT, int NT, int XBF, int MODE, int NSLOT>
-size_t smem_bytes() {
-    using G = StageGeo<FMT>;
+constexpr size_t smem_bytes() {
     constexpr int NCOL = 8 * NT;
+    using G = StageGeo<FMT, NCOL>;
     constexpr int RING = NSLOT * G::BYTES;
     constexpr int RED = CONSUMERS * RB * NCOL * 4;
     constexpr int PART_OFF = (MODE == DENSE) ? (RING > RED ? RING : RED) : RING + RED;
@@ -503,34 +561,58 @@ bool make_maps(CUtensorMap* mw, CUtensorMap* ms, int fmt, const uint8_t* wq, con
     return true;
 }
 
+// Activations [rows][K] 16-bit, read in boxes of 64 k x ncol rows with the
+// 128-byte swizzle.
+bool make_xmap(CUtensorMap* mx, const void* x, int64_t rows, int64_t K, int bf16, int ncol) {
+    uint64_t d[2] = {(uint64_t)K, (uint64_t)rows};
+    uint64_t st[1] = {(uint64_t)K * 2};
+    uint32_t box[2] = {64, (uint32_t)ncol};
+    return encode_tiled(mx, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, d, st,
+                        box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 template <int FMT, int NT, int XBF, int MODE, int NSLOT>
-cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& ms, const Params& p, dim3 grid, int cluster,
-                     cudaStream_t s) {
+cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, int64_t xrows, const Params& p,
+                     dim3 grid, int cluster, cudaStream_t s) {
+    CUtensorMap mx;
+    if (!make_xmap(&mx, x, xrows, p.K, XBF, 8 * NT)) return cudaErrorInvalidValue;
     auto kern = k_skinny<FMT, NT, XBF, MODE, NSLOT>;
-    const size_t smem = smem_bytes<FMT, NT, XBF, MODE, NSLOT>();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    constexpr size_t smem = smem_bytes<FMT, NT, XBF, MODE, NSLOT>();
+    static_assert(smem <= 113 * 1024, "two CTAs per SM");
+    static int configured_device = -1;       // attributes are per device; set once per instantiation
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, mw, ms, p);
+    cfg.numAttrs = p.pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, mw, ms, mx, p);
 }
 
 template <int FMT, int XBF>
-cudaError_t launch_dense_nt(const CUtensorMap& mw, const CUtensorMap& ms, const Params& p, dim3 grid, int cluster,
-                            int64_t T, cudaStream_t s) {
-    if (T <= 8) return launch_t<FMT, 1, XBF, DENSE, 8>(mw, ms, p, grid, cluster, s);
-    if (T <= 16) return launch_t<FMT, 2, XBF, DENSE, 8>(mw, ms, p, grid, cluster, s);
-    return launch_t<FMT, 4, XBF, DENSE, 8>(mw, ms, p, grid, cluster, s);
+cudaError_t launch_dense_nt(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, const Params& p, dim3 grid,
+                            int cluster, int64_t T, cudaStream_t s) {
+    constexpr int S1 = FMT == 0 ? 8 : 10, S2 = FMT == 0 ? 6 : 8, S4 = FMT == 0 ? 4 : 6;
+    if (T <= 8) return launch_t<FMT, 1, XBF, DENSE, S1>(mw, ms, x, T, p, grid, cluster, s);
+    if (T <= 16) return launch_t<FMT, 2, XBF, DENSE, S2>(mw, ms, x, T, p, grid, cluster, s);
+    return launch_t<FMT, 4, XBF, DENSE, S4>(mw, ms, x, T, p, grid, cluster, s);
 }
 
 cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
@@ -547,9 +629,10 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     p.y = a.y;
     p.yt = a.yt;
     p.wait_ns = (uint64_t)options().wait_ns;
+    p.pdl = fmt == 0 ? 1 : 0;     // Q4: the guard pass just before touches neither weights nor Y
     const int64_t rbs = (a.N + RB - 1) / RB;
     int ks = 1;
-    const int64_t cap = 2 * (int64_t)num_sms();
+    const int64_t cap = 2 * (int64_t)num_sms();      // two CTAs fit per SM
     for (int cand : {2, 4, 8})
         if (rbs * cand <= cap && p.nst_total / cand >= 2) ks = cand;
     p.ks = ks;
@@ -557,9 +640,9 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     if (options().trace)
         fprintf(stderr, "cq: skinny fmt=%d T=%lld N=%lld K=%lld grid=(%d,%lld) cluster=%d\n", fmt, (long long)a.T,
                 (long long)a.N, (long long)a.K, ks, (long long)rbs, ks);
-    if (fmt == 0) return launch_dense_nt<0, 0>(mw, ms, p, grid, ks, a.T, s);
-    if (a.x_bf16) return launch_dense_nt<1, 1>(mw, ms, p, grid, ks, a.T, s);
-    return launch_dense_nt<1, 0>(mw, ms, p, grid, ks, a.T, s);
+    if (fmt == 0) return launch_dense_nt<0, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
+    if (a.x_bf16) return launch_dense_nt<1, 1>(mw, ms, a.x, p, grid, ks, a.T, s);
+    return launch_dense_nt<1, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
 }
 
 }  // namespace
@@ -567,6 +650,8 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
 cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s) { return launch_dense(0, a, s); }
 cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s) { return launch_dense(1, a, s); }
 
+// Gate/up panels: activations are the guarded rows already gathered into
+// grouped order ([P][H] fp16, inverse scales [P]).
 cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s) {
     CUtensorMap mw, ms;
     if (!make_maps(&mw, &ms, 0, m.gu_q, m.gu_s, 2 * m.I, m.H, m.E)) return cudaErrorInvalidValue;
@@ -586,8 +671,13 @@ cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s) {
     p.I = m.I;
     p.H = m.H;
     p.wait_ns = (uint64_t)options().wait_ns;
-    dim3 grid(1, (unsigned)(m.I / 32), (unsigned)m.E);
-    return launch_t<0, 1, 0, GATEUP, 8>(mw, ms, p, grid, 1, s);
+    p.act = m.act;
+    p.n_act = m.n_act;
+    p.rbs = (int)(m.I / 32);
+    // persistent: two CTAs per SM share the (active expert x row block) items
+    const int64_t items_max = m.E * p.rbs;
+    dim3 grid((unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items_max), 1, 1);
+    return launch_t<0, 1, 0, GATEUP, 6>(mw, ms, m.xh, m.T * m.topk, p, grid, 1, s);
 }
 
 cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s) {
@@ -609,8 +699,12 @@ cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s) {
     p.I = m.I;
     p.H = m.H;
     p.wait_ns = (uint64_t)options().wait_ns;
-    dim3 grid(1, (unsigned)(m.H / RB), (unsigned)m.E);
-    return launch_t<0, 1, 0, DOWN, 8>(mw, ms, p, grid, 1, s);
+    p.act = m.act;
+    p.n_act = m.n_act;
+    p.rbs = (int)(m.H / RB);
+    const int64_t items_max = m.E * p.rbs;
+    dim3 grid((unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items_max), 1, 1);
+    return launch_t<0, 1, 0, DOWN, 6>(mw, ms, m.ah, m.T * m.topk, p, grid, 1, s);
 }
 
 }  // namespace cq

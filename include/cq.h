@@ -182,7 +182,9 @@ typedef enum {
     CQ_OPT_FORCE_PATH = 1,   /* 0 auto, 1 weight-streaming, 2 tensor-memory (tcgen05) path */
     CQ_OPT_WAIT_NS = 2,      /* time limit of every device pipeline wait, ns (default 1e9) */
     CQ_OPT_TEST_STALL = 3,   /* test only: 1 makes the next tcgen05 launch's loader issue nothing */
-    CQ_OPT_TRACE = 4         /* 1 prints the chosen path and grid of each call to stderr */
+    CQ_OPT_TRACE = 4,        /* 1 prints the chosen path and grid of each call to stderr */
+    CQ_OPT_TC_BN = 5,        /* tcgen05 token tile: 0 auto (default), or 64, 128, 256 */
+    CQ_OPT_TC_CLUSTER = 6    /* tcgen05 CTAs sharing one activation tile by multicast: 0 auto, 1, 2, 4 */
 } cq_option;
 /* Process-wide; returns CQ_ERR_ARG for an unknown option or value. */
 cq_status cq_set_option(int option, int64_t value);

@@ -103,7 +103,7 @@ def test_workspace_sizes(L):
     assert cq.cq_gemm_q4_workspace_bytes(3, 256) == 1536 + 256
     b = cq.cq_moe_workspace_bytes(32, 2048, 768, 128, 8)
     P = 256
-    need = 256 + 768 + P * 4 * 2 + 32 * 2048 * 2 + 256 + P * 768 * 4 + P * 768 * 2 + P * 4 + P * 2048 * 4
+    need = 256 + 768 + P * 4 * 2 + 768 + P * 2048 * 2 + P * 4 + P * 768 * 4 + P * 768 * 2 + P * 4 + P * 2048 * 4
     assert b == need
 
 

@@ -241,3 +241,34 @@ def test_wait_timeout_reports_status_and_context_survives():
     Y = run_q8(case, "f32")                                   # the context is still usable
     yref, S = oracle_q8(case)
     check(y_host(Y), yref, S, "f32", "after timeout")
+
+
+class _Opt:
+    """Context manager setting one library option for the duration."""
+
+    def __init__(self, opt, value):
+        self.opt, self.value = opt, value
+
+    def __enter__(self):
+        self.old = cq.cq_get_option(self.opt)
+        cq.cq_set_option(self.opt, self.value)
+
+    def __exit__(self, *a):
+        cq.cq_set_option(self.opt, self.old)
+
+
+@pytest.mark.parametrize("cl", [1, 2, 4])
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_tcgen05_cluster_multicast_and_token_tiles(cl, bn):
+    """Every cluster size (activation tile multicast to 1, 2 or 4 CTAs) and
+    token tile, on shapes whose weight-row tiles do not fill whole clusters
+    (N=300 -> 3 tiles, padded) and whose tokens leave a ragged tile."""
+    case4 = synth.gemm_q4_case(5000 + cl + bn, 150, 512, 300, x_dtype="bf16", signed=True)
+    case8 = synth.gemm_q8_case(6000 + cl + bn, 150, 512, 300, x_dtype="bf16")
+    with ForcePath(2), _Opt(cq.CQ_OPT_TC_CLUSTER, cl), _Opt(cq.CQ_OPT_TC_BN, bn):
+        Y4, wq = run_q4(case4, "f32")
+        Y8 = run_q8(case8, "bf16")
+    yref, S = oracle_q4(case4, wq)
+    check(y_host(Y4), yref, S, "f32", f"q4 cl={cl} bn={bn}")
+    yref8, S8 = oracle_q8(case8)
+    check(y_host(Y8), yref8, S8, "bf16", f"q8 cl={cl} bn={bn}")
