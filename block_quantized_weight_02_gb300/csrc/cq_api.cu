@@ -173,6 +173,10 @@ cq_status cq_set_option(int option, int64_t value) {
             if (value != 0 && value != 1 && value != 2 && value != 4) return fail(CQ_ERR_ARG, "cluster size must be 0, 1, 2 or 4");
             o.tc_cluster = value;
             return CQ_OK;
+        case CQ_OPT_TC_AMODE:
+            if (value < 0 || value > 2) return fail(CQ_ERR_ARG, "operand mode must be 0, 1 or 2");
+            o.tc_amode = value;
+            return CQ_OK;
         default:
             return fail(CQ_ERR_ARG, "unknown option %d", option);
     }
@@ -188,6 +192,7 @@ int64_t cq_get_option(int option) {
         case CQ_OPT_TRACE: return o.trace;
         case CQ_OPT_TC_BN: return o.tc_bn;
         case CQ_OPT_TC_CLUSTER: return o.tc_cluster;
+        case CQ_OPT_TC_AMODE: return o.tc_amode;
         default: return -1;
     }
 }

@@ -96,19 +96,24 @@ struct Raw<1> { static constexpr int ROW = 64; };   // Q8: 64 bytes per row
 
 // Shared memory: a load ring of LS stages (raw weight tile + activation
 // tile, filled by TMA) and a shorter ring of AS decoded weight tiles.
-template <int FMT, int BN, int LS, int AS>
+template <int FMT, int BN, int LS, int AS, int AM>
 struct Layout {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int R_BYTES = BM * Raw<FMT>::ROW;
     static constexpr int R_STRIDE = (R_BYTES + 1023) / 1024 * 1024;
     static constexpr int A_OFF = 0;
-    static constexpr int B_OFF = A_OFF + AS * A_BYTES;
+    static constexpr int B_OFF = A_OFF + (AM == 0 ? AS * A_BYTES : 0);   // AM 1: decoded tiles in TMEM
     static constexpr int R_OFF = B_OFF + LS * B_BYTES;
     static constexpr int BAR_OFF = R_OFF + LS * R_STRIDE;
     // full[LS], empty[LS], afull[AS], aempty[AS], accf; then tmem slot, abort, never
     static constexpr int NBAR = 2 * LS + 2 * AS + 1;
     static constexpr int MISC = NBAR * 8 + 16;
     static constexpr int TOTAL = BAR_OFF + MISC + 1024;  // + alignment slack
+    // tensor memory: accumulator in columns [0, BN); AM 1 adds AS decoded A tiles of 32 columns
+    static constexpr int A_COL = BN;
+    static constexpr int NEED = AM == 0 ? BN : BN + AS * 32;
+    static constexpr int TMEM_COLS = NEED <= 32 ? 32 : NEED <= 64 ? 64 : NEED <= 128 ? 128 : NEED <= 256 ? 256 : 512;
+    static_assert(NEED <= 512, "tensor memory budget");
 };
 
 constexpr int DEC_WARPS = 8;                 // two decoder threads per weight row
@@ -125,10 +130,10 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <int FMT, int BN, int XBF, int LS, int AS, int CL>
+template <int FMT, int BN, int XBF, int LS, int AS, int CL, int AM>
 __global__ void __launch_bounds__(THREADS, 1)
 k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const Params p) {
-    using L = Layout<FMT, BN, LS, AS>;
+    using L = Layout<FMT, BN, LS, AS, AM>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
@@ -164,7 +169,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
-        tmem_alloc(smem_u32(tmem_slot), BN);
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -242,9 +247,14 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                 const uint32_t a_base = sb + L::A_OFF + a * A_BYTES;
                 const uint32_t b_base = sb + L::B_OFF + s * L::B_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    tc_mma_f16(tmem, smem_desc_sw128(a_base + 32 * kk), smem_desc_sw128(b_base + 32 * kk), idesc,
-                               (kb | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    if (AM == 0)
+                        tc_mma_f16(tmem, smem_desc_sw128(a_base + 32 * kk), smem_desc_sw128(b_base + 32 * kk),
+                                   idesc, (kb | kk) != 0 ? 1u : 0u);
+                    else   // A from tensor memory: 8 columns per K=16 step
+                        tc_mma_f16_ts(tmem, tmem + (uint32_t)(L::A_COL + a * 32 + kk * 8),
+                                      smem_desc_sw128(b_base + 32 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
+                }
                 // raw + activation slot free (decoders finished with raw earlier), in every CTA
                 // of the cluster, since the peers multicast into this slot too
                 if (CL == 1) tc_commit(empty_bar(s));
@@ -279,6 +289,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             }
             const uint32_t raw = sb + L::R_OFF + s * L::R_STRIDE;
             const uint32_t adst = sb + L::A_OFF + a * A_BYTES + a_row;
+            // this thread's 32 decoded values (k = 32h .. 32h+31 of the stage), two per word, in k order
+            uint32_t o[16];
             if (FMT == 0) {
                 // 32-byte rows, 32-byte swizzle: chunk j of row r sits at j ^ ((r >> 2) & 1)
                 const uint4 v = ld_shared_v4(raw + r * 32 + (((uint32_t)h ^ (uint32_t)((r >> 2) & 1)) << 4));
@@ -288,23 +300,26 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                 const __half2 sh = __halves2half2(__ushort_as_half(sbits), __ushort_as_half(sbits));
                 const uint32_t px = prmt(v.x, 0u, 0x3120u), py = prmt(v.y, 0u, 0x3120u);
                 const uint32_t pz = prmt(v.z, 0u, 0x3120u), pw = prmt(v.w, 0u, 0x3120u);
-                const uint32_t c0 = (uint32_t)(4 * h);
                 // elements 0-7 of the block: low nibbles of bytes 0-7
-                st_shared_v4(adst + (((c0 + 0) ^ xr) << 4), hmul2_u32(nib2_to_h2(px), sh),
-                             hmul2_u32(nib2_to_h2(px >> 8), sh), hmul2_u32(nib2_to_h2(py), sh),
-                             hmul2_u32(nib2_to_h2(py >> 8), sh));
+                o[0] = hmul2_u32(nib2_to_h2(px), sh);
+                o[1] = hmul2_u32(nib2_to_h2(px >> 8), sh);
+                o[2] = hmul2_u32(nib2_to_h2(py), sh);
+                o[3] = hmul2_u32(nib2_to_h2(py >> 8), sh);
                 // elements 8-15: low nibbles of bytes 8-15
-                st_shared_v4(adst + (((c0 + 1) ^ xr) << 4), hmul2_u32(nib2_to_h2(pz), sh),
-                             hmul2_u32(nib2_to_h2(pz >> 8), sh), hmul2_u32(nib2_to_h2(pw), sh),
-                             hmul2_u32(nib2_to_h2(pw >> 8), sh));
+                o[4] = hmul2_u32(nib2_to_h2(pz), sh);
+                o[5] = hmul2_u32(nib2_to_h2(pz >> 8), sh);
+                o[6] = hmul2_u32(nib2_to_h2(pw), sh);
+                o[7] = hmul2_u32(nib2_to_h2(pw >> 8), sh);
                 // elements 16-23: high nibbles of bytes 0-7
-                st_shared_v4(adst + (((c0 + 2) ^ xr) << 4), hmul2_u32(nib2_to_h2(px >> 4), sh),
-                             hmul2_u32(nib2_to_h2(px >> 12), sh), hmul2_u32(nib2_to_h2(py >> 4), sh),
-                             hmul2_u32(nib2_to_h2(py >> 12), sh));
+                o[8] = hmul2_u32(nib2_to_h2(px >> 4), sh);
+                o[9] = hmul2_u32(nib2_to_h2(px >> 12), sh);
+                o[10] = hmul2_u32(nib2_to_h2(py >> 4), sh);
+                o[11] = hmul2_u32(nib2_to_h2(py >> 12), sh);
                 // elements 24-31: high nibbles of bytes 8-15
-                st_shared_v4(adst + (((c0 + 3) ^ xr) << 4), hmul2_u32(nib2_to_h2(pz >> 4), sh),
-                             hmul2_u32(nib2_to_h2(pz >> 12), sh), hmul2_u32(nib2_to_h2(pw >> 4), sh),
-                             hmul2_u32(nib2_to_h2(pw >> 12), sh));
+                o[12] = hmul2_u32(nib2_to_h2(pz >> 4), sh);
+                o[13] = hmul2_u32(nib2_to_h2(pz >> 12), sh);
+                o[14] = hmul2_u32(nib2_to_h2(pw >> 4), sh);
+                o[15] = hmul2_u32(nib2_to_h2(pw >> 12), sh);
             } else {
                 // 64-byte rows, 64-byte swizzle: chunk j of row r sits at j ^ ((r >> 1) & 3)
                 const uint32_t sw = (uint32_t)((r >> 1) & 3);
@@ -312,25 +327,33 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                 for (int qq = 0; qq < 2; ++qq) {
                     const uint32_t q = (uint32_t)(2 * h + qq);
                     const uint4 v = ld_shared_v4(raw + r * 64 + ((q ^ sw) << 4));
-                    // bytes 16q..16q+15 = elements 16q..16q+15 = output chunks 2q, 2q+1
-                    uint32_t o[8];
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         if (XBF) {
                             const uint32_t wx = wv[i] ^ 0x80808080u;
-                            o[2 * i] = pack_bf2(i8_to_f32(wx, 0x7440u), i8_to_f32(wx, 0x7441u));
-                            o[2 * i + 1] = pack_bf2(i8_to_f32(wx, 0x7442u), i8_to_f32(wx, 0x7443u));
+                            o[8 * qq + 2 * i] = pack_bf2(i8_to_f32(wx, 0x7440u), i8_to_f32(wx, 0x7441u));
+                            o[8 * qq + 2 * i + 1] = pack_bf2(i8_to_f32(wx, 0x7442u), i8_to_f32(wx, 0x7443u));
                         } else {
-                            o[2 * i] = i8x2_to_h2(wv[i], 0x4140u);
-                            o[2 * i + 1] = i8x2_to_h2(wv[i], 0x4342u);
+                            o[8 * qq + 2 * i] = i8x2_to_h2(wv[i], 0x4140u);
+                            o[8 * qq + 2 * i + 1] = i8x2_to_h2(wv[i], 0x4342u);
                         }
                     }
-                    st_shared_v4(adst + (((2 * q) ^ xr) << 4), o[0], o[1], o[2], o[3]);
-                    st_shared_v4(adst + (((2 * q + 1) ^ xr) << 4), o[4], o[5], o[6], o[7]);
                 }
             }
-            fence_proxy_async_smem();
+            if (AM == 0) {
+                // shared-memory A tile, 128-byte swizzled K-major: 16-byte chunk 4h+j of row r
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    st_shared_v4(adst + ((((uint32_t)(4 * h + j)) ^ xr) << 4), o[4 * j], o[4 * j + 1], o[4 * j + 2],
+                                 o[4 * j + 3]);
+                fence_proxy_async_smem();
+            } else {
+                // tensor-memory A tile: lane r, columns A_COL + 32a + 16h .. +15
+                tmem_st_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(L::A_COL + a * 32 + 16 * h), o);
+                tmem_st_wait();
+                tc_fence_before();
+            }
             mbar_arrive(afull_bar(a));
         }
 
@@ -372,17 +395,17 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         if (*abort_flag && lane == 0) mbar_wait(accf_bar, 0, p.wait_ns, never_flag);  // MMAs done
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, BN);
+        tmem_dealloc(tmem, L::TMEM_COLS);
     }
     // no CTA leaves while a peer may still multicast into it or signal its barriers
     if (CL > 1) cluster_sync_all();
 }
 
-template <int FMT, int BN, int XBF, int LS, int AS, int CL>
+template <int FMT, int BN, int XBF, int LS, int AS, int CL, int AM>
 cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, const Params& p, dim3 grid, cudaStream_t s) {
-    using L = Layout<FMT, BN, LS, AS>;
+    using L = Layout<FMT, BN, LS, AS, AM>;
     static_assert(L::TOTAL <= 232448, "shared memory budget");
-    auto kern = k_tc<FMT, BN, XBF, LS, AS, CL>;
+    auto kern = k_tc<FMT, BN, XBF, LS, AS, CL, AM>;
     static int configured_device = -1;       // attributes are per device; set once per instantiation
     int dev = 0;
     cudaGetDevice(&dev);
@@ -465,25 +488,42 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     if (options().trace)
         fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d cluster=%d grid=(%u,%u)\n", fmt,
                 (long long)a.T, (long long)a.N, (long long)a.K, bn, cl, grid.x, grid.y);
-#define CQ_TC_CL(F, B, X, LSv, ASv)                                              \
-    do {                                                                        \
-        if (cl == 4) return launch_bn<F, B, X, LSv, ASv, 4>(mw, mx, p, grid, s); \
-        if (cl == 2) return launch_bn<F, B, X, LSv, ASv, 2>(mw, mx, p, grid, s); \
-        return launch_bn<F, B, X, LSv, ASv, 1>(mw, mx, p, grid, s);             \
+    // decoded weight operand: 1 = shared memory, 2 = tensor memory (default)
+    const int am = options().tc_amode == 1 ? 0 : 1;
+#define CQ_TC_CL(F, B, X, LSv, ASv, AMv)                                                  \
+    do {                                                                                  \
+        if (cl == 4) return launch_bn<F, B, X, LSv, ASv, 4, AMv>(mw, mx, p, grid, s);      \
+        if (cl == 2) return launch_bn<F, B, X, LSv, ASv, 2, AMv>(mw, mx, p, grid, s);      \
+        return launch_bn<F, B, X, LSv, ASv, 1, AMv>(mw, mx, p, grid, s);                  \
     } while (0)
+    if (am == 0) {
+        if (fmt == 0) {
+            if (bn == 256) CQ_TC_CL(0, 256, 0, 5, 2, 0);
+            if (bn == 128) CQ_TC_CL(0, 128, 0, 8, 3, 0);
+            CQ_TC_CL(0, 64, 0, 12, 4, 0);
+        }
+        if (xbf) {
+            if (bn == 256) CQ_TC_CL(1, 256, 1, 4, 3, 0);
+            if (bn == 128) CQ_TC_CL(1, 128, 1, 7, 3, 0);
+            CQ_TC_CL(1, 64, 1, 10, 4, 0);
+        }
+        if (bn == 256) CQ_TC_CL(1, 256, 0, 4, 3, 0);
+        if (bn == 128) CQ_TC_CL(1, 128, 0, 7, 3, 0);
+        CQ_TC_CL(1, 64, 0, 10, 4, 0);
+    }
     if (fmt == 0) {
-        if (bn == 256) CQ_TC_CL(0, 256, 0, 5, 2);
-        if (bn == 128) CQ_TC_CL(0, 128, 0, 8, 3);
-        CQ_TC_CL(0, 64, 0, 12, 4);
+        if (bn == 256) CQ_TC_CL(0, 256, 0, 6, 4, 1);
+        if (bn == 128) CQ_TC_CL(0, 128, 0, 10, 4, 1);
+        CQ_TC_CL(0, 64, 0, 16, 4, 1);
     }
     if (xbf) {
-        if (bn == 256) CQ_TC_CL(1, 256, 1, 4, 3);
-        if (bn == 128) CQ_TC_CL(1, 128, 1, 7, 3);
-        CQ_TC_CL(1, 64, 1, 10, 4);
+        if (bn == 256) CQ_TC_CL(1, 256, 1, 5, 4, 1);
+        if (bn == 128) CQ_TC_CL(1, 128, 1, 9, 4, 1);
+        CQ_TC_CL(1, 64, 1, 13, 4, 1);
     }
-    if (bn == 256) CQ_TC_CL(1, 256, 0, 4, 3);
-    if (bn == 128) CQ_TC_CL(1, 128, 0, 7, 3);
-    CQ_TC_CL(1, 64, 0, 10, 4);
+    if (bn == 256) CQ_TC_CL(1, 256, 0, 5, 4, 1);
+    if (bn == 128) CQ_TC_CL(1, 128, 0, 9, 4, 1);
+    CQ_TC_CL(1, 64, 0, 13, 4, 1);
 #undef CQ_TC_CL
 }
 
