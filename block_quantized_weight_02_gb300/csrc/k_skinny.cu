@@ -234,78 +234,79 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     __syncthreads();
 
     if (warp == CONSUMERS) {
-        // ================= producer =================
-        if (lane == 0) {
-            tma_prefetch_desc(&tmW);
-            if (FMT == 0) tma_prefetch_desc(&tmS);
-            tma_prefetch_desc(&tmX);
-            int64_t issued = 0;
+        // ================= producers =================
+        // Lane s owns ring slot s and issues every copy of the stages that land in it
+        // (stage gi goes to slot gi % NSLOT): one thread keeps only a few bulk copies
+        // outstanding, so the ring is filled from NSLOT threads.
+        if (lane < NSLOT) {
+            const int s = lane;
+            if (lane == 0) {
+                tma_prefetch_desc(&tmW);
+                if (FMT == 0) tma_prefetch_desc(&tmS);
+                tma_prefetch_desc(&tmX);
+            }
+            int64_t last_gi = -1;     // the last stage this lane issued
             bool ok = true;
-            auto load_w = [&](const Item& it, int i, int slot) {
-                const uint32_t sbase = smem_base + (uint32_t)(slot * G::BYTES);
+            auto load_w = [&](const Item& it, int i) {
+                const uint32_t sbase = smem_base + (uint32_t)(s * G::BYTES);
                 const int st = st0 + i;
                 for (int kh = 0; kh < 2; ++kh)
                     for (int bx = 0; bx < 2; ++bx)
-                        tma_load_3d(sbase + (uint32_t)((kh * 2 + bx) * BOX_BYTES), &tmW, full_bar(slot),
+                        tma_load_3d(sbase + (uint32_t)((kh * 2 + bx) * BOX_BYTES), &tmW, full_bar(s),
                                     st * 128 + kh * 64, it.row_box[bx], it.expert);
                 if (FMT == 0)
                     for (int bx = 0; bx < 2; ++bx)
-                        tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * 512), &tmS, full_bar(slot), st * 8,
+                        tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * 512), &tmS, full_bar(s), st * 8,
                                     it.row_box[bx], it.expert);
             };
-            auto load_x = [&](const Item& it, int i, int slot, int grp) {
-                const uint32_t sbase = smem_base + (uint32_t)(slot * G::BYTES);
+            auto load_x = [&](const Item& it, int i, int grp) {
+                const uint32_t sbase = smem_base + (uint32_t)(s * G::BYTES);
                 const int st = st0 + i;
                 // activation rows of this column group (dense: tokens; MoE: grouped pairs)
                 const int xrow0 = (int)(it.col0 + (int64_t)grp * NCOL);
                 for (int xb = 0; xb < G::XBOXES; ++xb)
-                    tma_load_2d(sbase + (uint32_t)(G::X_OFF + xb * G::XBOX), &tmX, full_bar(slot),
+                    tma_load_2d(sbase + (uint32_t)(G::X_OFF + xb * G::XBOX), &tmX, full_bar(s),
                                 st * G::KSTAGE + 64 * xb, xrow0);
             };
-            int64_t gi = 0;
             // With a programmatic dependency (dense Q4: the activation guard pass runs just
             // before), the weights of the first ring fill are requested before waiting for
             // the activations; everything else follows the wait.
-            int pre = 0;
+            const bool pre = MODE == DENSE && p.pdl && s < nst;
             if (MODE == DENSE) {
-                const Item it0 = get_item(0);
-                pre = p.pdl ? (nst < NSLOT ? nst : NSLOT) : 0;
-                for (int i = 0; i < pre; ++i) {            // fresh slots: no empty wait needed
-                    mbar_arrive_expect_tx(full_bar(i), (uint32_t)G::BYTES);
-                    load_w(it0, i, i);
+                if (pre) {                                   // fresh slot: no empty wait needed
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)G::BYTES);
+                    load_w(get_item(0), s);
                 }
                 pdl_wait();
-                for (int i = 0; i < pre; ++i) {
-                    load_x(it0, i, i, 0);
-                    ++issued;
+                if (pre) {
+                    load_x(get_item(0), s, 0);
+                    last_gi = s;
                 }
-                gi = pre;
             }
+            int64_t gi = 0;
             for (int idx = first; idx < nitems && ok; idx += stride) {
                 const Item it = get_item(idx);
                 for (int grp = 0; grp < it.ngroups && ok; ++grp) {
-                    for (int i = (idx == first && grp == 0) ? pre : 0; i < nst; ++i, ++gi) {
-                        const int slot = (int)(gi % NSLOT);
+                    for (int i = 0; i < nst; ++i, ++gi) {
+                        if (gi % NSLOT != s || (pre && gi == s)) continue;
                         const uint32_t par = (uint32_t)((gi / NSLOT) & 1);
-                        if (!mbar_wait(empty_bar(slot), par ^ 1u, p.wait_ns, abort_flag)) {
+                        if (!mbar_wait(empty_bar(s), par ^ 1u, p.wait_ns, abort_flag)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(full_bar(slot), (uint32_t)G::BYTES);
-                        load_w(it, i, slot);
-                        load_x(it, i, slot, grp);
-                        ++issued;
+                        mbar_arrive_expect_tx(full_bar(s), (uint32_t)G::BYTES);
+                        load_w(it, i);
+                        load_x(it, i, grp);
+                        last_gi = gi;
                     }
                 }
             }
             if (!ok) {
                 *abort_flag = 1;
                 atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
-                // let copies already in flight land before the CTA can exit
-                const int64_t first = issued > NSLOT ? issued - NSLOT : 0;
-                for (int64_t gi = first; gi < issued; ++gi)
-                    mbar_wait(full_bar((int)(gi % NSLOT)), (uint32_t)((gi / NSLOT) & 1), p.wait_ns, never_flag);
             }
+            if (*abort_flag && last_gi >= 0)   // this lane's last copy must land before the CTA can exit
+                mbar_wait(full_bar(s), (uint32_t)((last_gi / NSLOT) & 1), p.wait_ns, never_flag);
         }
         __syncwarp();
     } else {

@@ -189,12 +189,17 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     };
 
     if (warp == PRODUCER_WARP) {
-        // ================= TMA producer =================
-        if (lane == 0) {
-            tma_prefetch_desc(&tmW);
-            tma_prefetch_desc(&tmX);
-            int issued = 0;
-            auto load_x = [&](int kb, int s) {
+        // ================= TMA producers =================
+        // Lane s owns ring slot s and issues that slot's copies: one thread keeps only a
+        // few bulk copies outstanding, so the ring is filled from LS threads.
+        if (lane < LS) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tmW);
+                tma_prefetch_desc(&tmX);
+            }
+            const int s = lane;
+            int issued = 0;        // stages issued by this lane
+            auto load_x = [&](int kb) {
                 const uint32_t dst = sb + L::B_OFF + s * L::B_BYTES + rank * (XS * 128);
                 if (CL == 1) tma_load_2d(dst, &tmX, full_bar(s), kb * BK, t0);
                 else tma_load_2d_mc(dst, &tmX, full_bar(s), kb * BK, t0 + (int)rank * XS, CMASK);
@@ -202,33 +207,31 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             if (!p.stall) {
                 // With a programmatic dependency, the raw weights of the first ring fill are
                 // requested before waiting for the guarded activations.
-                const int pre = p.pdl ? (nk < LS ? nk : LS) : 0;
-                for (int kb = 0; kb < pre; ++kb) {
-                    mbar_arrive_expect_tx(full_bar(kb), (uint32_t)(L::R_BYTES + L::B_BYTES));
-                    tma_load_2d(sb + L::R_OFF + kb * L::R_STRIDE, &tmW, full_bar(kb), kb * Raw<FMT>::ROW, m0);
+                const bool pre = p.pdl && s < nk;
+                if (pre) {
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::R_BYTES + L::B_BYTES));
+                    tma_load_2d(sb + L::R_OFF + s * L::R_STRIDE, &tmW, full_bar(s), s * Raw<FMT>::ROW, m0);
                 }
                 pdl_wait();
-                for (int kb = 0; kb < pre; ++kb) {
-                    load_x(kb, kb);
+                if (pre) {
+                    load_x(s);
                     ++issued;
                 }
-                for (int kb = pre; kb < nk; ++kb) {
-                    const int s = kb % LS;
+                for (int kb = s + (pre ? LS : 0); kb < nk; kb += LS) {
                     if (!mbar_wait(empty_bar(s), (uint32_t)(((kb / LS) & 1) ^ 1), p.wait_ns, abort_flag)) {
                         give_up();
                         break;
                     }
                     mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::R_BYTES + L::B_BYTES));
                     tma_load_2d(sb + L::R_OFF + s * L::R_STRIDE, &tmW, full_bar(s), kb * Raw<FMT>::ROW, m0);
-                    load_x(kb, s);
+                    load_x(kb);
                     ++issued;
                 }
             }
-            if (*abort_flag) {
-                // copies already issued must land before the CTA can exit
-                const int first = issued > LS ? issued - LS : 0;
-                for (int kb = first; kb < issued; ++kb)
-                    mbar_wait(full_bar(kb % LS), (uint32_t)((kb / LS) & 1), p.wait_ns, never_flag);
+            if (*abort_flag && issued > 0) {
+                // this lane's last copy must land before the CTA can exit
+                const int kb_last = s + (issued - 1) * LS;
+                mbar_wait(full_bar(s), (uint32_t)((kb_last / LS) & 1), p.wait_ns, never_flag);
             }
         }
         __syncwarp();
@@ -405,6 +408,7 @@ template <int FMT, int BN, int XBF, int LS, int AS, int CL, int AM>
 cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, const Params& p, dim3 grid, cudaStream_t s) {
     using L = Layout<FMT, BN, LS, AS, AM>;
     static_assert(L::TOTAL <= 232448, "shared memory budget");
+    static_assert(LS <= 32, "one producer lane per ring slot");
     auto kern = k_tc<FMT, BN, XBF, LS, AS, CL, AM>;
     static int configured_device = -1;       // attributes are per device; set once per instantiation
     int dev = 0;
