@@ -95,7 +95,8 @@ template <>
 struct Raw<1> { static constexpr int ROW = 64; };   // Q8: 64 bytes per row
 
 // Shared memory: a load ring of LS stages (raw weight tile + activation
-// tile, filled by TMA) and a shorter ring of AS decoded weight tiles.
+// tile, filled by TMA) and (AM 0) a shorter ring of AS decoded weight tiles;
+// with AM 1 the decoded tiles are AS == LS slots of tensor memory.
 template <int FMT, int BN, int LS, int AS, int AM>
 struct Layout {
     static constexpr int B_BYTES = BN * BK * 2;
@@ -237,16 +238,20 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ================= MMA issuer =================
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(BM, BN, XBF);
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % LS, a = kb % AS;
-                if (!mbar_wait(afull_bar(a), (uint32_t)((kb / AS) & 1), p.wait_ns, abort_flag) ||
-                    !mbar_wait(full_bar(s), (uint32_t)((kb / LS) & 1), p.wait_ns, abort_flag)) {
-                    give_up();
-                    break;
-                }
-                tc_fence_after();
+        // The whole warp runs the loop (converged); one lane issues the tensor-core work.
+        // With the decoded tiles in tensor memory (AM 1) there is one decoded slot per load
+        // slot, so one commit frees both and the only wait is the decoders' hand-off.
+        constexpr uint32_t idesc = idesc_f16(BM, BN, XBF);
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % LS, a = kb % AS;
+            bool ok = mbar_wait(afull_bar(a), (uint32_t)((kb / AS) & 1), p.wait_ns, abort_flag);
+            if (AM == 0 && ok) ok = mbar_wait(full_bar(s), (uint32_t)((kb / LS) & 1), p.wait_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) give_up();
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
                 const uint32_t a_base = sb + L::A_OFF + a * A_BYTES;
                 const uint32_t b_base = sb + L::B_OFF + s * L::B_BYTES;
 #pragma unroll
@@ -258,14 +263,15 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                         tc_mma_f16_ts(tmem, tmem + (uint32_t)(L::A_COL + a * 32 + kk * 8),
                                       smem_desc_sw128(b_base + 32 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
-                // raw + activation slot free (decoders finished with raw earlier), in every CTA
-                // of the cluster, since the peers multicast into this slot too
+                // raw + activation slot (and, AM 1, its decoded tile) free once these MMAs are
+                // done, in every CTA of the cluster, since the peers multicast into this slot too
                 if (CL == 1) tc_commit(empty_bar(s));
                 else tc_commit_mc(empty_bar(s), CMASK);
-                tc_commit(aempty_bar(a));   // decoded slot free
+                if (AM == 0) tc_commit(aempty_bar(a));   // decoded slot free
             }
-            tc_commit(accf_bar);   // also lets teardown know every MMA has finished
+            __syncwarp();
         }
+        if (lane == 0) tc_commit(accf_bar);   // also lets teardown know every MMA has finished
         __syncwarp();
     } else {
         // ================= decoders (two threads per weight row), then epilogue =================
@@ -285,8 +291,9 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                 sc_cur = sc_next;
                 if (row_ok && kb + 4 < nk) sc_next = __ldg(reinterpret_cast<const uint4*>(srow + 2 * (kb + 4)));
             }
+            // AM 1: decoded slot a == load slot s, free once the slot was refilled
             if (!mbar_wait(full_bar(s), (uint32_t)((kb / LS) & 1), p.wait_ns, abort_flag) ||
-                !mbar_wait(aempty_bar(a), (uint32_t)(((kb / AS) & 1) ^ 1), p.wait_ns, abort_flag)) {
+                (AM == 0 && !mbar_wait(aempty_bar(a), (uint32_t)(((kb / AS) & 1) ^ 1), p.wait_ns, abort_flag))) {
                 give_up();
                 break;
             }
@@ -409,6 +416,7 @@ cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, const Params
     using L = Layout<FMT, BN, LS, AS, AM>;
     static_assert(L::TOTAL <= 232448, "shared memory budget");
     static_assert(LS <= 32, "one producer lane per ring slot");
+    static_assert(AM == 0 || AS == LS, "tensor-memory decoded slots pair with load slots");
     auto kern = k_tc<FMT, BN, XBF, LS, AS, CL, AM>;
     static int configured_device = -1;       // attributes are per device; set once per instantiation
     int dev = 0;
@@ -515,19 +523,20 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         if (bn == 128) CQ_TC_CL(1, 128, 0, 7, 3, 0);
         CQ_TC_CL(1, 64, 0, 10, 4, 0);
     }
+    // AM 1: one tensor-memory decoded slot per load slot (AS == LS)
     if (fmt == 0) {
-        if (bn == 256) CQ_TC_CL(0, 256, 0, 6, 4, 1);
-        if (bn == 128) CQ_TC_CL(0, 128, 0, 10, 4, 1);
-        CQ_TC_CL(0, 64, 0, 16, 4, 1);
+        if (bn == 256) CQ_TC_CL(0, 256, 0, 6, 6, 1);
+        if (bn == 128) CQ_TC_CL(0, 128, 0, 10, 10, 1);
+        CQ_TC_CL(0, 64, 0, 14, 14, 1);
     }
     if (xbf) {
-        if (bn == 256) CQ_TC_CL(1, 256, 1, 5, 4, 1);
-        if (bn == 128) CQ_TC_CL(1, 128, 1, 9, 4, 1);
-        CQ_TC_CL(1, 64, 1, 13, 4, 1);
+        if (bn == 256) CQ_TC_CL(1, 256, 1, 5, 5, 1);
+        if (bn == 128) CQ_TC_CL(1, 128, 1, 9, 9, 1);
+        CQ_TC_CL(1, 64, 1, 13, 13, 1);
     }
-    if (bn == 256) CQ_TC_CL(1, 256, 0, 5, 4, 1);
-    if (bn == 128) CQ_TC_CL(1, 128, 0, 9, 4, 1);
-    CQ_TC_CL(1, 64, 0, 13, 4, 1);
+    if (bn == 256) CQ_TC_CL(1, 256, 0, 5, 5, 1);
+    if (bn == 128) CQ_TC_CL(1, 128, 0, 9, 9, 1);
+    CQ_TC_CL(1, 64, 0, 13, 13, 1);
 #undef CQ_TC_CL
 }
 
