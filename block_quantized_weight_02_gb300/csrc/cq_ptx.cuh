@@ -46,15 +46,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of global time, or as soon as *abort becomes non-zero (another
-// thread of the CTA already gave up); returns false then.
+// thread of the CTA already gave up); returns false then.  Between polls the
+// thread sleeps (32 ns, doubling to 256 ns) so that waiting warps leave the
+// issue slots of their scheduler to the warps that do the work.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           const volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    uint32_t sleep_ns = 32;
     while (true) {
+        __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (global_timer_ns() - t0 > limit_ns) return false;
+        if (sleep_ns < 256) sleep_ns <<= 1;
     }
 }
 

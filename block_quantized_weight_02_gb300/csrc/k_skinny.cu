@@ -17,10 +17,10 @@
 //    and, when K is split across a thread-block cluster, the CTAs' partial
 //    tiles are summed in rank order through distributed shared memory, so
 //    results are deterministic.
-// Inside a 128-k chunk the contraction order is permuted (the same way for
-// weights and activations): each thread of a quad owns one 32-k block (Q4)
-// or two 16-k runs (Q8), which makes every shared-memory read a
-// conflict-free 16-byte load.  The sum is unchanged.
+// Inside a stage the contraction order is permuted (the same way for weights
+// and activations): thread c of a quad owns 32-k blocks 2c and 2c+1 (Q4) or
+// 16-k runs 2c and 2c+1 (Q8), which with the 128-byte swizzles makes every
+// shared-memory read a conflict-free 16-byte load.  The sum is unchanged.
 //
 // Prior art on the pages: the 8-row expert panels ("cortiq-engine 0.8.41
 // src/gpu_metal/clover.rs", q4tp_mul_mm_n8) and the 32-token MMA tiles for
@@ -52,7 +52,6 @@ constexpr int RB = 64;           // weight rows per CTA (two TMA row boxes of 32
 constexpr int MT = 4;            // m16 tiles per consumer warp
 constexpr int CONSUMERS = 4;     // consumer warps (two CTAs share an SM)
 constexpr int THREADS = (CONSUMERS + 1) * 32;
-constexpr int BOX_BYTES = 32 * 64;  // one TMA box: 32 rows x 64 bytes
 
 enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
 
@@ -121,26 +120,21 @@ __device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, int lo_byte) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// One stage in shared memory, filled by three TMA copies (five for gate/up):
+//  W  [64 rows][128 B], 128-byte swizzle: 16-byte chunk j of row r at j ^ (r % 8)
+//     (Q4: 256 k = eight 32-k blocks; Q8: 128 k = eight 16-k runs)
+//  S  [64 rows][8 fp16] block scales (Q4 only)
+//  X  [NCOL rows][XSL slabs of 64 k][128 B], 128-byte swizzle over the 3-D
+//     view {64 elements, K/64 slabs, rows} of the activations.
 template <int FMT, int NCOL>
-struct StageGeo;
-template <int NCOL>
-struct StageGeo<0, NCOL> {                 // Q4: 256 k per stage
-    static constexpr int KSTAGE = 256;
-    static constexpr int W_BYTES = 4 * BOX_BYTES;     // [kh 2][rbox 2][32][64 B]
-    static constexpr int S_BYTES = 2 * 32 * 16;       // [rbox 2][32][8 fp16]
-    static constexpr int XBOXES = 4;                  // 64-k boxes of activations
-    static constexpr int X_OFF = W_BYTES + S_BYTES;   // 1024-aligned
-    static constexpr int XBOX = NCOL * 128;           // [NCOL rows][64 x 16-bit], 128-byte swizzle
-    static constexpr int BYTES = X_OFF + XBOXES * XBOX;
-};
-template <int NCOL>
-struct StageGeo<1, NCOL> {                 // Q8: 128 k per stage
-    static constexpr int KSTAGE = 128;
-    static constexpr int W_BYTES = 4 * BOX_BYTES;     // [kh 2][rbox 2][32][64 B]
-    static constexpr int XBOXES = 2;
-    static constexpr int X_OFF = W_BYTES;
-    static constexpr int XBOX = NCOL * 128;
-    static constexpr int BYTES = X_OFF + XBOXES * XBOX;
+struct StageGeo {
+    static constexpr int KSTAGE = FMT == 0 ? 256 : 128;
+    static constexpr int W_BYTES = RB * 128;
+    static constexpr int S_BYTES = FMT == 0 ? RB * 16 : 0;
+    static constexpr int XSL = KSTAGE / 64;            // 64-k slabs per stage
+    static constexpr int X_OFF = W_BYTES + S_BYTES;    // 1024-aligned
+    static constexpr int X_BYTES = NCOL * XSL * 128;
+    static constexpr int BYTES = X_OFF + X_BYTES;
 };
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
@@ -250,23 +244,24 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
             auto load_w = [&](const Item& it, int i) {
                 const uint32_t sbase = smem_base + (uint32_t)(s * G::BYTES);
                 const int st = st0 + i;
-                for (int kh = 0; kh < 2; ++kh)
-                    for (int bx = 0; bx < 2; ++bx)
-                        tma_load_3d(sbase + (uint32_t)((kh * 2 + bx) * BOX_BYTES), &tmW, full_bar(s),
-                                    st * 128 + kh * 64, it.row_box[bx], it.expert);
-                if (FMT == 0)
-                    for (int bx = 0; bx < 2; ++bx)
-                        tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * 512), &tmS, full_bar(s), st * 8,
+                if (MODE == GATEUP) {      // gate rows and up rows are 32-row boxes apart in the matrix
+                    for (int bx = 0; bx < 2; ++bx) {
+                        tma_load_3d(sbase + (uint32_t)(bx * 32 * 128), &tmW, full_bar(s), st * 128, it.row_box[bx],
+                                    it.expert);
+                        tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * 32 * 16), &tmS, full_bar(s), st * 8,
                                     it.row_box[bx], it.expert);
+                    }
+                } else {
+                    tma_load_3d(sbase, &tmW, full_bar(s), st * 128, it.row_box[0], it.expert);
+                    if (FMT == 0) tma_load_3d(sbase + (uint32_t)G::W_BYTES, &tmS, full_bar(s), st * 8, it.row_box[0], it.expert);
+                }
             };
             auto load_x = [&](const Item& it, int i, int grp) {
                 const uint32_t sbase = smem_base + (uint32_t)(s * G::BYTES);
                 const int st = st0 + i;
                 // activation rows of this column group (dense: tokens; MoE: grouped pairs)
                 const int xrow0 = (int)(it.col0 + (int64_t)grp * NCOL);
-                for (int xb = 0; xb < G::XBOXES; ++xb)
-                    tma_load_2d(sbase + (uint32_t)(G::X_OFF + xb * G::XBOX), &tmX, full_bar(s),
-                                st * G::KSTAGE + 64 * xb, xrow0);
+                tma_load_3d(sbase + (uint32_t)G::X_OFF, &tmX, full_bar(s), 0, st * G::XSL, xrow0);
             };
             // With a programmatic dependency (dense Q4: the activation guard pass runs just
             // before), the weights of the first ring fill are requested before waiting for
@@ -327,7 +322,10 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                     for (int q = 0; q < 4; ++q) acc[a][b][q] = 0.f;
 
             bool ok = !*abort_flag;
-            for (int i = warp; i < nst && ok; i += CONSUMERS) {
+            // Stage gi goes to warp gi % CONSUMERS and slot gi % NSLOT; NSLOT is a multiple of
+            // CONSUMERS, so each slot always belongs to one warp, which then waits for the
+            // slot's rounds in order (a parity wait cannot tell round r+1 from round r-1).
+            for (int i = (int)((warp - gbase % CONSUMERS + CONSUMERS) % CONSUMERS); i < nst && ok; i += CONSUMERS) {
                 const int64_t gi = gbase + i;
                 const int slot = (int)(gi % NSLOT);
                 if (!mbar_wait(full_bar(slot), (uint32_t)((gi / NSLOT) & 1), p.wait_ns, abort_flag)) {
@@ -342,8 +340,9 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                     const __half* sS = reinterpret_cast<const __half*>(sW + G::W_BYTES);
 #pragma unroll
                     for (int kh = 0; kh < 2; ++kh) {
-                        // this thread's 64-byte activation span (k = 128 kh + 32 c .. +31) of each column
-                        const uint8_t* xbox = sX + (2 * kh + (c >> 1)) * G::XBOX;
+                        // this thread's 32-k block j = 2c + kh: weight chunk j of each row, and
+                        // activations k = 32 j .. 32 j + 31 = slab c, bytes 64 kh .. 64 kh + 63
+                        const int j = 2 * c + kh;
 #pragma unroll
                         for (int sp = 0; sp < 2; ++sp) {
                             // words 4sp..4sp+3 (low-nibble steps 2sp, 2sp+1) and 8+4sp.. (high-nibble steps)
@@ -351,27 +350,25 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 const int row = 8 * nt + g;
-                                const uint8_t* xr = xbox + row * 128;
-                                blo[nt] = lds128(xr + (((4 * (c & 1) + sp) ^ g) << 4));
-                                bhi[nt] = lds128(xr + (((4 * (c & 1) + 2 + sp) ^ g) << 4));
+                                const uint8_t* xr = sX + row * (G::XSL * 128) + c * 128;
+                                const int sw = (G::XSL * row + c) & 7;
+                                blo[nt] = lds128(xr + (((4 * kh + sp) ^ sw) << 4));
+                                bhi[nt] = lds128(xr + (((4 * kh + 2 + sp) ^ sw) << 4));
                             }
 #pragma unroll
                             for (int mt = 0; mt < MT; ++mt) {
-                                // (re)read this m-tile's two weight rows and scales: cheap shared loads
-                                // instead of keeping all four m-tiles live in registers
-                                const int bx = mt >> 1, lr = 16 * (mt & 1) + g;
-                                const uint8_t* box = sW + (kh * 2 + bx) * BOX_BYTES;
-                                const uint4 wa = lds128(box + lr * 64 + 16 * c);
-                                const uint4 wb = lds128(box + (lr + 8) * 64 + 16 * c);
-                                const __half s0 = sS[(bx * 32 + lr) * 8 + kh * 4 + c];
-                                const __half s1 = sS[(bx * 32 + lr + 8) * 8 + kh * 4 + c];
+                                const int lr = 16 * mt + g;
+                                const uint4 wa = lds128(sW + lr * 128 + ((j ^ (lr & 7)) << 4));
+                                const uint4 wb = lds128(sW + (lr + 8) * 128 + ((j ^ ((lr + 8) & 7)) << 4));
+                                const __half s0 = sS[lr * 8 + j];
+                                const __half s1 = sS[(lr + 8) * 8 + j];
                                 const __half2 sa = __halves2half2(s0, s0), sb2 = __halves2half2(s1, s1);
                                 const uint32_t r0[4] = {wa.x, wa.y, wa.z, wa.w};
                                 const uint32_t r1[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
                                 for (int u = 0; u < 2; ++u) {
-                                    const int s = 2 * sp + u;
-                                    const uint32_t p0 = prmt(r0[s], 0u, 0x3120u), p1 = prmt(r1[s], 0u, 0x3120u);
+                                    const int st4 = 2 * sp + u;
+                                    const uint32_t p0 = prmt(r0[st4], 0u, 0x3120u), p1 = prmt(r1[st4], 0u, 0x3120u);
                                     uint32_t alo[4], ahi[4];
                                     alo[0] = hmul2_u32(nib2_to_h2(p0), sa);
                                     alo[1] = hmul2_u32(nib2_to_h2(p1), sb2);
@@ -395,21 +392,24 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 } else {
 #pragma unroll
                     for (int kh = 0; kh < 2; ++kh) {
-                        // activations k = 64 kh + 16 c .. +15 of each column (box kh, chunks 2c, 2c+1)
-                        const uint8_t* xbox = sX + kh * G::XBOX;
+                        // this thread's 16-k run j = 2c + kh: weight chunk j of each row, and
+                        // activations k = 16 j .. 16 j + 15 = slab j / 4, 32 bytes at 32 (j % 4)
+                        const int j = 2 * c + kh;
+                        const int slab = j >> 2;
                         uint4 b0[NT], b1[NT];
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             const int row = 8 * nt + g;
-                            b0[nt] = lds128(xbox + row * 128 + (((2 * c) ^ g) << 4));
-                            b1[nt] = lds128(xbox + row * 128 + (((2 * c + 1) ^ g) << 4));
+                            const uint8_t* xr = sX + row * (G::XSL * 128) + slab * 128;
+                            const int sw = (G::XSL * row + slab) & 7;
+                            b0[nt] = lds128(xr + (((2 * (j & 3)) ^ sw) << 4));
+                            b1[nt] = lds128(xr + (((2 * (j & 3) + 1) ^ sw) << 4));
                         }
 #pragma unroll
                         for (int mt = 0; mt < MT; ++mt) {
-                            const int bx = mt >> 1, lr = 16 * (mt & 1) + g;
-                            const uint8_t* box = sW + (kh * 2 + bx) * BOX_BYTES;
-                            const uint4 w0 = lds128(box + lr * 64 + 16 * c);
-                            const uint4 w1 = lds128(box + (lr + 8) * 64 + 16 * c);
+                            const int lr = 16 * mt + g;
+                            const uint4 w0 = lds128(sW + lr * 128 + ((j ^ (lr & 7)) << 4));
+                            const uint4 w1 = lds128(sW + (lr + 8) * 128 + ((j ^ ((lr + 8) & 7)) << 4));
                             const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
                             const uint32_t r1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
@@ -543,17 +543,18 @@ constexpr size_t smem_bytes() {
     return (size_t)PART_OFF + RB * NCOL * 4 + 2 * NSLOT * 8 + 16 + 1024;
 }
 
+// Weights [E][R][K bytes] and scales [E][R][K/32], boxes of rows_box rows.
 bool make_maps(CUtensorMap* mw, CUtensorMap* ms, int fmt, const uint8_t* wq, const uint16_t* ws, int64_t R,
-               int64_t K, int64_t E) {
+               int64_t K, int64_t E, int rows_box) {
     const uint64_t kbytes = fmt == 0 ? (uint64_t)K / 2 : (uint64_t)K;
     uint64_t dw[3] = {kbytes, (uint64_t)R, (uint64_t)E};
     uint64_t sw[2] = {kbytes, kbytes * (uint64_t)R};
-    uint32_t bw[3] = {64, 32, 1};
-    if (!encode_tiled(mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, wq, dw, sw, bw, CU_TENSOR_MAP_SWIZZLE_NONE)) return false;
+    uint32_t bw[3] = {128, (uint32_t)rows_box, 1};
+    if (!encode_tiled(mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, wq, dw, sw, bw, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
     if (fmt == 0) {
         uint64_t ds[3] = {(uint64_t)K / 32, (uint64_t)R, (uint64_t)E};
         uint64_t ss[2] = {(uint64_t)K / 32 * 2, (uint64_t)K / 32 * 2 * (uint64_t)R};
-        uint32_t bs[3] = {8, 32, 1};
+        uint32_t bs[3] = {8, (uint32_t)rows_box, 1};
         if (!encode_tiled(ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, ws, ds, ss, bs, CU_TENSOR_MAP_SWIZZLE_NONE))
             return false;
     } else {
@@ -562,13 +563,13 @@ bool make_maps(CUtensorMap* mw, CUtensorMap* ms, int fmt, const uint8_t* wq, con
     return true;
 }
 
-// Activations [rows][K] 16-bit, read in boxes of 64 k x ncol rows with the
-// 128-byte swizzle.
-bool make_xmap(CUtensorMap* mx, const void* x, int64_t rows, int64_t K, int bf16, int ncol) {
-    uint64_t d[2] = {(uint64_t)K, (uint64_t)rows};
-    uint64_t st[1] = {(uint64_t)K * 2};
-    uint32_t box[2] = {64, (uint32_t)ncol};
-    return encode_tiled(mx, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, d, st,
+// Activations [rows][K] 16-bit seen as {64 elements, K/64 slabs, rows}; one box
+// is xsl slabs of ncol rows, stored [row][slab][128 B] with the 128-byte swizzle.
+bool make_xmap(CUtensorMap* mx, const void* x, int64_t rows, int64_t K, int bf16, int ncol, int xsl) {
+    uint64_t d[3] = {64, (uint64_t)K / 64, (uint64_t)rows};
+    uint64_t st[2] = {128, (uint64_t)K * 2};
+    uint32_t box[3] = {64, (uint32_t)xsl, (uint32_t)ncol};
+    return encode_tiled(mx, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x, d, st,
                         box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -576,10 +577,11 @@ template <int FMT, int NT, int XBF, int MODE, int NSLOT>
 cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, int64_t xrows, const Params& p,
                      dim3 grid, int cluster, cudaStream_t s) {
     CUtensorMap mx;
-    if (!make_xmap(&mx, x, xrows, p.K, XBF, 8 * NT)) return cudaErrorInvalidValue;
+    if (!make_xmap(&mx, x, xrows, p.K, XBF, 8 * NT, StageGeo<FMT, 8 * NT>::XSL)) return cudaErrorInvalidValue;
     auto kern = k_skinny<FMT, NT, XBF, MODE, NSLOT>;
     constexpr size_t smem = smem_bytes<FMT, NT, XBF, MODE, NSLOT>();
     static_assert(smem <= 113 * 1024, "two CTAs per SM");
+    static_assert(NSLOT % CONSUMERS == 0, "each ring slot is consumed by one warp");
     static int configured_device = -1;       // attributes are per device; set once per instantiation
     int dev = 0;
     cudaGetDevice(&dev);
@@ -610,7 +612,7 @@ cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& ms, const void* x
 template <int FMT, int XBF>
 cudaError_t launch_dense_nt(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, const Params& p, dim3 grid,
                             int cluster, int64_t T, cudaStream_t s) {
-    constexpr int S1 = FMT == 0 ? 8 : 10, S2 = FMT == 0 ? 6 : 8, S4 = FMT == 0 ? 4 : 6;
+    constexpr int S1 = 8, S2 = FMT == 0 ? 4 : 8, S4 = 4;
     if (T <= 8) return launch_t<FMT, 1, XBF, DENSE, S1>(mw, ms, x, T, p, grid, cluster, s);
     if (T <= 16) return launch_t<FMT, 2, XBF, DENSE, S2>(mw, ms, x, T, p, grid, cluster, s);
     return launch_t<FMT, 4, XBF, DENSE, S4>(mw, ms, x, T, p, grid, cluster, s);
@@ -618,7 +620,7 @@ cudaError_t launch_dense_nt(const CUtensorMap& mw, const CUtensorMap& ms, const 
 
 cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     CUtensorMap mw, ms;
-    if (!make_maps(&mw, &ms, fmt, a.wq, a.ws, a.N, a.K, 1)) return cudaErrorInvalidValue;
+    if (!make_maps(&mw, &ms, fmt, a.wq, a.ws, a.N, a.K, 1, RB)) return cudaErrorInvalidValue;
     Params p = {};
     p.K = a.K;
     p.nst_total = (int)(a.K / (fmt == 0 ? 256 : 128));
@@ -655,7 +657,7 @@ cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s) { return laun
 // grouped order ([P][H] fp16, inverse scales [P]).
 cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s) {
     CUtensorMap mw, ms;
-    if (!make_maps(&mw, &ms, 0, m.gu_q, m.gu_s, 2 * m.I, m.H, m.E)) return cudaErrorInvalidValue;
+    if (!make_maps(&mw, &ms, 0, m.gu_q, m.gu_s, 2 * m.I, m.H, m.E, 32)) return cudaErrorInvalidValue;
     Params p = {};
     p.K = m.H;
     p.nst_total = (int)(m.H / 256);
@@ -678,12 +680,12 @@ cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s) {
     // persistent: two CTAs per SM share the (active expert x row block) items
     const int64_t items_max = m.E * p.rbs;
     dim3 grid((unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items_max), 1, 1);
-    return launch_t<0, 1, 0, GATEUP, 6>(mw, ms, m.xh, m.T * m.topk, p, grid, 1, s);
+    return launch_t<0, 1, 0, GATEUP, 4>(mw, ms, m.xh, m.T * m.topk, p, grid, 1, s);
 }
 
 cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s) {
     CUtensorMap mw, ms;
-    if (!make_maps(&mw, &ms, 0, m.d_q, m.d_s, m.H, m.I, m.E)) return cudaErrorInvalidValue;
+    if (!make_maps(&mw, &ms, 0, m.d_q, m.d_s, m.H, m.I, m.E, RB)) return cudaErrorInvalidValue;
     Params p = {};
     p.K = m.I;
     p.nst_total = (int)(m.I / 256);
@@ -705,7 +707,7 @@ cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s) {
     p.rbs = (int)(m.H / RB);
     const int64_t items_max = m.E * p.rbs;
     dim3 grid((unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items_max), 1, 1);
-    return launch_t<0, 1, 0, DOWN, 6>(mw, ms, m.ah, m.T * m.topk, p, grid, 1, s);
+    return launch_t<0, 1, 0, DOWN, 4>(mw, ms, m.ah, m.T * m.topk, p, grid, 1, s);
 }
 
 }  // namespace cq

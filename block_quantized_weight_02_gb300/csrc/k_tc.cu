@@ -358,13 +358,23 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                     st_shared_v4(adst + ((((uint32_t)(4 * h + j)) ^ xr) << 4), o[4 * j], o[4 * j + 1], o[4 * j + 2],
                                  o[4 * j + 3]);
                 fence_proxy_async_smem();
+                mbar_arrive(afull_bar(a));
             } else {
-                // tensor-memory A tile: lane r, columns A_COL + 32a + 16h .. +15
+                // tensor-memory A tile: lane r, columns A_COL + 32a + 16h .. +15.  The store
+                // of this stage is handed to the MMA one stage later, so its latency overlaps
+                // the next stage's wait and decode.
+                if (kb > 0) {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(afull_bar((kb - 1) % AS));
+                }
                 tmem_st_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(L::A_COL + a * 32 + 16 * h), o);
-                tmem_st_wait();
-                tc_fence_before();
+                if (kb + 1 == nk) {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(afull_bar(a));
+                }
             }
-            mbar_arrive(afull_bar(a));
         }
 
         // ---- epilogue: TMEM -> registers -> scale -> Y[t][n] ----
