@@ -79,7 +79,8 @@ def _q4_calls(cq, case, outs, dev, tag):
     for out in outs:
         Y = torch.empty(T, N, dtype=torch.float32 if out == "f32" else torch.bfloat16, device=dev)
         calls.append(Call(f"{tag} q4->{out}", (lambda X=X, Wq=Wq, Ws=Ws, Y=Y, ws=ws: cq.cq_gemm_q4(X, Wq, Ws, Y, ws)),
-                          2.0 * T * N * K, wbytes, X.numel() * 2 + Y.numel() * Y.element_size(), 2,
+                          2.0 * T * N * K, wbytes, X.numel() * 2 + Y.numel() * Y.element_size(),
+                          1 if T <= 32 else 2,   # weight-streaming path: one kernel; tcgen05: guard pass + GEMM
                           h2d=[X], d2h=[Y]))
     return calls
 
@@ -255,36 +256,27 @@ def run_ours(args, rank, world, local_rank):
 
     clocks = Clocks(local_rank)
     clocks.start()
-    # The timed region: K steps, with an event pair around every call (on the
-    # launching stream).  By default the whole region is captured once into a
-    # CUDA graph and replayed, so host-side launch overhead does not leave the
-    # GPU idle between the short calls; --eager times direct calls instead.
+    # The timed region: K steps of the workload's calls, back to back on one
+    # stream.  By default it is captured once into a CUDA graph and replayed,
+    # so host-side launch overhead does not leave the GPU idle between the
+    # short calls and consecutive kernels overlap through their programmatic
+    # dependencies; --eager times direct calls instead.
     timing = "eager"
     graph = None
-    ev = None
     if not args.eager:
         try:
-            ev = [[(torch.cuda.Event(enable_timing=True, external=True),
-                    torch.cuda.Event(enable_timing=True, external=True)) for _ in rot[0]]
-                  for _ in range(args.steps)]
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
-                cap = torch.cuda.current_stream()
                 for i in range(args.steps):
-                    for j, c in enumerate(rot[i % sets]):
-                        ev[i][j][0].record(cap)
+                    for c in rot[i % sets]:
                         c.fn()
-                        ev[i][j][1].record(cap)
             timing = "cuda-graph replay"
-        except Exception as exc:          # e.g. no external events in this torch
+        except Exception as exc:
             print(f"bench: graph capture unavailable ({exc!r}); timing direct calls", file=sys.stderr)
             graph = None
             torch.cuda.synchronize()
             cq.cq_get_device_error()
-    if graph is None:
-        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in rot[0]]
-              for _ in range(args.steps)]
-    else:
+    if graph is not None:
         graph.replay()                    # one untimed replay
         torch.cuda.synchronize()
     barrier()
@@ -296,10 +288,8 @@ def run_ours(args, rank, world, local_rank):
         graph.replay()
     else:
         for i in range(args.steps):
-            for j, c in enumerate(rot[i % sets]):
-                ev[i][j][0].record(stream)
+            for c in rot[i % sets]:
                 c.fn()
-                ev[i][j][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -307,9 +297,35 @@ def run_ours(args, rank, world, local_rank):
     ms = t0.elapsed_time(t1)
     if cq.cq_get_device_error() != 0:
         raise SystemExit("device error during the timed region")
-    per_call_ms = [float(np.mean([ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps)]))
-                   for j in range(len(rot[0]))]
     ms_max = max_over_ranks(ms, world)
+
+    # Per-call duration (for the roofline of the dominant call): each call of
+    # the step alone, repeated back to back over the rotating input sets, timed
+    # with CUDA events on the launching stream; the average call time there.
+    reps = max(3, min(args.steps, 50))
+    per_call_ms = []
+    for j in range(len(rot[0])):
+        g = None
+        if graph is not None:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(reps):
+                    rot[i % sets][j].fn()
+            g.replay()
+            torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        if g is not None:
+            g.replay()
+        else:
+            for i in range(reps):
+                rot[i % sets][j].fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per_call_ms.append(a.elapsed_time(b) / reps)
+        del g
+    if cq.cq_get_device_error() != 0:
+        raise SystemExit("device error while timing the calls")
 
     calls = rot[0]
     flops_step = sum(c.flops for c in calls)

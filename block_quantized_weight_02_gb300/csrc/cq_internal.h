@@ -48,15 +48,21 @@ int take_error_tc();
 cudaError_t launch_dequant_q4(const uint8_t* wq, const uint16_t* ws, int64_t N, int64_t K, float* w, cudaStream_t s);
 cudaError_t launch_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, int64_t K, float* w, cudaStream_t s);
 // X rows -> fp16 with a per-row power-of-two guard; rsx = inverse scales.
-cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s);
+// stream_order: inside each 32-k block, write the order the weight-streaming
+// GEMM reads (position 8 wi + t <- k = 4 wi + {0,2,16,18,1,3,17,19}[t]);
+// otherwise k order (the tcgen05 GEMM).
+cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, int stream_order,
+                          cudaStream_t s);
 // The same for gathered rows: output row r <- input row gather[r] / per.
 cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K, uint16_t* xh, float* rsx,
-                                 const int32_t* gather, int per, const int32_t* status, cudaStream_t s);
+                                 const int32_t* gather, int per, const int32_t* status, int stream_order,
+                                 cudaStream_t s);
 
 struct MoeWs;  // workspace carve-up (cq_api.cu)
 // Also writes the active experts (count > 0, ascending) to act[] and their number to *n_act.
 cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
                              int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, cudaStream_t s);
+// Writes the weight-streaming order (the down panels read it).
 cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,
                           cudaStream_t s);
 cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, int64_t topk, int64_t H, void* y,
@@ -64,10 +70,10 @@ cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, i
 
 // Weight-streaming (small-T) GEMM.
 struct SkinnyDense {
-    const void* x;       // activations [T][K] (fp16 for Q4 after the guard pass; fp16/bf16 for Q8)
+    const void* x;       // Q4: guarded fp16 [T][K] in the streaming order; Q8: fp16/bf16 [T][K] as given
     int x_bf16;
-    const float* rsx;    // Q4: per-row inverse guard scale [T]; null for Q8
-    const float* rs;     // Q8: row scales [N]; null for Q4
+    const float* rsx;    // Q4: per-row inverse guard scale [T]
+    const float* rs;     // Q8: row scales [N]
     const uint8_t* wq;   // Q4 nibbles / Q8 int8 bytes
     const uint16_t* ws;  // Q4 scales
     int64_t T, K, N;
@@ -78,9 +84,9 @@ cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s);
 cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s);
 
 struct SkinnyMoe {
-    const uint16_t* xh;     // [P][H] fp16 (guarded), rows gathered into grouped order
+    const uint16_t* xh;     // [P][H] fp16 (guarded, streaming order), rows gathered into grouped order
     const float* rsx;       // [P]
-    const uint16_t* ah;     // [P][I] fp16 (guarded), grouped order
+    const uint16_t* ah;     // [P][I] fp16 (guarded, streaming order), grouped order
     const float* rsa;       // [P]
     const float* w;         // routing weights [T*topk] (pair id order)
     const int32_t* seg;     // [E+1]

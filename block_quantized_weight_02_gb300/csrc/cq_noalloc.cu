@@ -81,12 +81,12 @@ extern "C" cq_status cq_gemm_q4_noalloc(const void* X, int xt, int64_t T, int64_
     uint16_t* xh = static_cast<uint16_t*>(scratch);
     float* rsx = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + xh_bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = launch_x_half(X, xt, T, K, xh, rsx, s);
-    if (e != cudaSuccess) return cuda_fail(e, "activation guard pass");
     const Options& o = options();
     const bool skinny = o.force_path == 1 || (o.force_path == 0 && T <= o.small_t_max);
+    if (skinny && T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4_noalloc: the weight-streaming path serves T <= 32");
+    e = launch_x_half(X, xt, T, K, xh, rsx, skinny ? 1 : 0, s);
+    if (e != cudaSuccess) return cuda_fail(e, "activation guard pass");
     if (skinny) {
-        if (T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4_noalloc: the weight-streaming path serves T <= 32");
         SkinnyDense a = {xh, 0, rsx, nullptr, Wq, Ws, T, K, N, Y, yt};
         e = launch_skinny_q4(a, s);
         return e == cudaSuccess ? CQ_OK : cuda_fail(e, "weight-streaming Q4 GEMM");

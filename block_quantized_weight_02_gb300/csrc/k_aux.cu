@@ -11,6 +11,24 @@ namespace cq {
 
 __device__ int g_err_aux = 0;
 
+// Launch with a programmatic dependency on the previous kernel in the
+// stream: the kernel may be scheduled while that one finishes, and waits for
+// it (griddepcontrol.wait) before touching anything.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ void set_err(int code) { atomicCAS(&g_err_aux, 0, code); }
 
 int take_error_aux() {
@@ -92,14 +110,38 @@ __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// One CTA of 256 threads per output row; K % 8 == 0.  With a gather list,
-// output row r is source row gather[r] / per (the MoE pairs in grouped
-// order, as the pages' x_half gathers through `src`).
+// Order of the 16-bit activations inside each 32-k block for the
+// weight-streaming GEMM: position 8 wi + t holds k = 4 wi + TAU[t], TAU =
+// {0, 2, 16, 18, 1, 3, 17, 19}.  Byte 4 wi + b of a packed Q4 block carries
+// elements 4 wi + b (low nibble) and 16 + 4 wi + b (high nibble); masking a
+// 32-bit word of four such bytes yields the pairs (b0, b2) and (b1, b3) of
+// each nibble plane, and this order puts the matching activations of one
+// word side by side, so one 16-byte shared-memory load feeds two MMAs.  The
+// contraction is the same sum in another order.
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+// v: 32 scaled values of one block in k order -> four 16-byte chunks in stream order.
+__device__ __forceinline__ void store_block_stream_order(const float* v, uint4* dst) {
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        const int b = 4 * wi;
+        dst[wi] = make_uint4(pack_h2(v[b], v[b + 2]), pack_h2(v[16 + b], v[18 + b]), pack_h2(v[b + 1], v[b + 3]),
+                             pack_h2(v[17 + b], v[19 + b]));
+    }
+}
+
+// One CTA of 256 threads per output row; K % 8 == 0 (K % 32 == 0 with
+// stream_order).  With a gather list, output row r is source row
+// gather[r] / per (the MoE pairs in grouped order, as the pages' x_half
+// gathers through `src`).
 template <typename T>
 __global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t K, __half* __restrict__ xh,
                                                 float* __restrict__ rsx, const int32_t* __restrict__ gather, int per,
-                                                const int32_t* __restrict__ status) {
-    pdl_launch_dependents();   // the GEMM after this pass may start streaming its weights
+                                                const int32_t* __restrict__ status, int stream_order) {
+    pdl_launch_dependents();   // the GEMM after this pass may start streaming its weights now
+    pdl_wait();                // inputs ready and the previous readers of xh done
     if (status && *status != 0) return;
     __shared__ float red[8];
     const int64_t row = blockIdx.x;
@@ -117,32 +159,48 @@ __global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t
     const int sh = guard_shift(m);
     const float sc = pow2f(sh);
     uint4* dst = reinterpret_cast<uint4*>(xh + row * K);
-    for (int64_t i = threadIdx.x; i < n8; i += 256) {
-        uint4 v = src[i];
-        const T* e = reinterpret_cast<const T*>(&v);
-        uint4 o;
-        __half2* oh = reinterpret_cast<__half2*>(&o);
+    if (stream_order) {
+        for (int64_t blk = threadIdx.x; blk < K / 32; blk += 256) {
+            float v[32];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            oh[j] = __halves2half2(__float2half_rn(to_f32<T>(e[2 * j]) * sc), __float2half_rn(to_f32<T>(e[2 * j + 1]) * sc));
-        dst[i] = o;
+            for (int q = 0; q < 4; ++q) {
+                uint4 u = src[4 * blk + q];
+                const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[8 * q + j] = to_f32<T>(e[j]) * sc;
+            }
+            store_block_stream_order(v, dst + 4 * blk);
+        }
+    } else {
+        for (int64_t i = threadIdx.x; i < n8; i += 256) {
+            uint4 v = src[i];
+            const T* e = reinterpret_cast<const T*>(&v);
+            uint4 o;
+            __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                oh[j] = __halves2half2(__float2half_rn(to_f32<T>(e[2 * j]) * sc),
+                                       __float2half_rn(to_f32<T>(e[2 * j + 1]) * sc));
+            dst[i] = o;
+        }
     }
     if (threadIdx.x == 0) rsx[row] = pow2f(-sh);
 }
 
-cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s) {
-    return launch_x_half_gather(x, xt, T, K, xh, rsx, nullptr, 1, nullptr, s);
+cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, int stream_order,
+                          cudaStream_t s) {
+    return launch_x_half_gather(x, xt, T, K, xh, rsx, nullptr, 1, nullptr, stream_order, s);
 }
 
 cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K, uint16_t* xh, float* rsx,
-                                 const int32_t* gather, int per, const int32_t* status, cudaStream_t s) {
+                                 const int32_t* gather, int per, const int32_t* status, int stream_order,
+                                 cudaStream_t s) {
     if (xt == CQ_BF16)
-        k_x_half<__nv_bfloat16><<<(unsigned)rows, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), K,
-                                                               reinterpret_cast<__half*>(xh), rsx, gather, per, status);
-    else
-        k_x_half<__half><<<(unsigned)rows, 256, 0, s>>>(reinterpret_cast<const __half*>(x), K,
-                                                        reinterpret_cast<__half*>(xh), rsx, gather, per, status);
-    return cudaGetLastError();
+        return launch_pdl(k_x_half<__nv_bfloat16>, dim3((unsigned)rows), dim3(256), 0, s,
+                          reinterpret_cast<const __nv_bfloat16*>(x), K, reinterpret_cast<__half*>(xh), rsx, gather, per,
+                          status, stream_order);
+    return launch_pdl(k_x_half<__half>, dim3((unsigned)rows), dim3(256), 0, s, reinterpret_cast<const __half*>(x), K,
+                      reinterpret_cast<__half*>(xh), rsx, gather, per, status, stream_order);
 }
 
 // ---- MoE routing layout -------------------------------------------------
@@ -157,6 +215,8 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
                                                    int32_t* __restrict__ seg, int32_t* __restrict__ perm,
                                                    int32_t* __restrict__ inv, int32_t* __restrict__ act,
                                                    int32_t* __restrict__ n_act, int32_t* __restrict__ status) {
+    pdl_wait();               // idx may come from the previous kernel; the previous call's readers are done
+    pdl_launch_dependents();
     extern __shared__ int sh[];
     int* cnt = sh;            // [E]
     int* fill = sh + E;       // [E]
@@ -214,15 +274,17 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
 cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
                              int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, cudaStream_t s) {
     const size_t smem = (size_t)(2 * E + 256) * sizeof(int);
-    k_moe_route<<<1, 256, smem, s>>>(idx, (int)(T * topk), (int)E, seg, perm, inv, act, n_act, status);
-    return cudaGetLastError();
+    return launch_pdl(k_moe_route, dim3(1), dim3(256), smem, s, idx, (int)(T * topk), (int)E, seg, perm, inv, act, n_act,
+                      status);
 }
 
 // SwiGLU activations (f32, grouped order) -> fp16 behind the same
-// power-of-two guard as the inputs ("oxinfer 0.0.5 src/metal.rs",
+// power-of-two guard as the inputs, in the weight-streaming order ("oxinfer 0.0.5 src/metal.rs",
 // silu_half: scaled half rows and an inverse scale per row).
 __global__ void __launch_bounds__(256) k_a_half(const float* __restrict__ a, int64_t I, __half* __restrict__ ah,
                                                 float* __restrict__ rsa, const int32_t* __restrict__ status) {
+    pdl_launch_dependents();
+    pdl_wait();
     if (*status != 0) return;
     __shared__ float red[8];
     const int64_t row = blockIdx.x;
@@ -236,19 +298,26 @@ __global__ void __launch_bounds__(256) k_a_half(const float* __restrict__ a, int
     m = block_max_256(m, red);
     const int sh = guard_shift(m);
     const float sc = pow2f(sh);
-    __half2* dst = reinterpret_cast<__half2*>(ah + row * I);
-    for (int64_t i = threadIdx.x; i < n4; i += 256) {
-        float4 v = src[i];
-        dst[2 * i] = __floats2half2_rn(v.x * sc, v.y * sc);
-        dst[2 * i + 1] = __floats2half2_rn(v.z * sc, v.w * sc);
+    // written in the weight-streaming GEMM's order inside each 32-k block (I % 32 == 0)
+    uint4* dst = reinterpret_cast<uint4*>(ah + row * I);
+    for (int64_t blk = threadIdx.x; blk < I / 32; blk += 256) {
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 u = src[8 * blk + q];
+            v[4 * q] = u.x * sc;
+            v[4 * q + 1] = u.y * sc;
+            v[4 * q + 2] = u.z * sc;
+            v[4 * q + 3] = u.w * sc;
+        }
+        store_block_stream_order(v, dst + 4 * blk);
     }
     if (threadIdx.x == 0) rsa[row] = pow2f(-sh);
 }
 
 cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,
                           cudaStream_t s) {
-    k_a_half<<<(unsigned)P, 256, 0, s>>>(a, I, reinterpret_cast<__half*>(ah), rsa, status);
-    return cudaGetLastError();
+    return launch_pdl(k_a_half, dim3((unsigned)P), dim3(256), 0, s, a, I, reinterpret_cast<__half*>(ah), rsa, status);
 }
 
 // Y[t][n] = sum over slots j (in order) of eo[inv[t*topk + j]][n]; the
@@ -257,6 +326,8 @@ cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, fl
 __global__ void __launch_bounds__(256) k_moe_combine(const float* __restrict__ eo, const int32_t* __restrict__ inv,
                                                      int topk, int64_t H, void* __restrict__ y, int yt,
                                                      const int32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_launch_dependents();
     if (*status != 0) return;
     const int64_t t = blockIdx.y;
     const int64_t c = ((int64_t)blockIdx.x * 256 + threadIdx.x) * 4;
@@ -282,8 +353,7 @@ __global__ void __launch_bounds__(256) k_moe_combine(const float* __restrict__ e
 cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, int64_t topk, int64_t H, void* y,
                                int yt, const int32_t* status, cudaStream_t s) {
     dim3 grid((unsigned)((H / 4 + 255) / 256), (unsigned)T);
-    k_moe_combine<<<grid, 256, 0, s>>>(eo, inv, (int)topk, H, y, yt, status);
-    return cudaGetLastError();
+    return launch_pdl(k_moe_combine, grid, dim3(256), 0, s, eo, inv, (int)topk, H, y, yt, status);
 }
 
 }  // namespace cq

@@ -3,24 +3,42 @@
 //
 // Y^T = W . X^T with the weight rows in the MMA's M dimension and the
 // activation rows (tokens or routed pairs) in N, so a small T only narrows
-// N.  One CTA owns 64 weight rows and a contiguous range of K:
+// N.  One CTA owns RB weight rows and a contiguous range of K:
 //  - a producer warp streams the packed weights (and, for Q4, the fp16
-//    block scales) and the matching slice of the activations (fp16/bf16,
-//    128-byte swizzled) into a shared-memory ring with TMA, one stage per
-//    256 k (Q4) or 128 k (Q8), each stage tracked by full/empty mbarriers;
-//  - four consumer warps take the stages round-robin, decode the weights
-//    from shared memory straight into mma.sync A fragments (Q4:
-//    (nibble - 8) * scale rounded once to fp16; Q8: int8 converted exactly
-//    to the activation type) and multiply with activation fragments read
-//    from the same stage;
-//  - the four partial tiles are summed in a fixed order in shared memory,
-//    and, when K is split across a thread-block cluster, the CTAs' partial
-//    tiles are summed in rank order through distributed shared memory, so
-//    results are deterministic.
-// Inside a stage the contraction order is permuted (the same way for weights
-// and activations): thread c of a quad owns 32-k blocks 2c and 2c+1 (Q4) or
-// 16-k runs 2c and 2c+1 (Q8), which with the 128-byte swizzles makes every
-// shared-memory read a conflict-free 16-byte load.  The sum is unchanged.
+//    block scales) and the matching slice of the activations into a
+//    shared-memory ring with TMA, one stage per 256 k (Q4) or 128 k (Q8),
+//    each stage tracked by full/empty mbarriers; producer lane s issues
+//    every copy of ring slot s;
+//  - eight consumer warps take part in every stage.  With up to 16
+//    activation columns each warp owns 16 weight rows and the whole stage
+//    (RB = 128); with 32 columns each warp owns 16 rows and half of the
+//    stage's k (RB = 64; the halves are summed in a fixed order at the
+//    end), which halves each warp's activation reads from shared memory.
+// Decoding goes straight from shared memory into mma.sync A fragments:
+//  - Q4 (activations: the guarded fp16 rows, written by the guard pass in
+//    the order below): lane c of a quad decodes word c (bytes 4c .. 4c + 3)
+//    of one 32-k block for its two rows.  Masking the word (and the word
+//    shifted by 8) gives the fp16 pairs 1024 + n (low nibbles) and
+//    1024 + 16 n (high nibbles) of bytes (b0, b2) and (b1, b3); one
+//    subtraction, or one fused multiply-add by 1/16, turns each pair into
+//    n - 8 exactly.  Inside each block the guard pass stores the
+//    activations so that the eight partners of one word are one 16-byte
+//    chunk.  The two MMAs of one block take all 32 k of that block, so
+//    their f32 result is multiplied by the block scale (exact in f32) into
+//    the running sum: the scale is folded per 32-k block.
+//  - Q8 (activations fp16 or bf16 as given): int8 pairs become fp16
+//    exactly ((v ^ 0x80) | 0x6400 is 1024 + v + 128) or bf16 exactly (low
+//    seven bits and the sign bit go to two bf16 numbers whose difference is
+//    v); the row scale is applied in the epilogue.
+// When K is split across a thread-block cluster, the CTAs' partial tiles
+// are summed in rank order through distributed shared memory, so results
+// are deterministic.
+// Launches overlap through programmatic dependent launch: every CTA lets
+// the next kernel in the stream start as soon as it runs, and the
+// producer requests the weights of its first ring fill before it waits for
+// the previous kernel (weights are never written by this library); the
+// activations, the expert layout and the outputs are touched only after
+// that wait.
 //
 // Prior art on the pages: the 8-row expert panels ("cortiq-engine 0.8.41
 // src/gpu_metal/clover.rs", q4tp_mul_mm_n8) and the 32-token MMA tiles for
@@ -48,21 +66,16 @@ int take_error_skinny() {
 
 namespace {
 
-constexpr int RB = 64;           // weight rows per CTA (two TMA row boxes of 32)
-constexpr int MT = 4;            // m16 tiles per consumer warp
-constexpr int CONSUMERS = 4;     // consumer warps (two CTAs share an SM)
+constexpr int CONSUMERS = 8;     // consumer warps, all of them in every stage
 constexpr int THREADS = (CONSUMERS + 1) * 32;
 
 enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
 
 struct Params {
-    // weights: tensor maps over [E][R][Kbytes] (bytes) and [E][R][K/32] (fp16)
     int64_t K;
     int nst_total;        // stages over the whole K
     int ks;               // K split (cluster size)
     int64_t N;            // DENSE: output rows; MoE: rows of one expert matrix
-    // activations
-    const uint16_t* x;    // 16-bit activations, row stride K
     int64_t T;            // DENSE: activation rows
     const float* rsx;     // Q4 guard inverse scales per activation row (DENSE / GATEUP)
     const float* rs;      // Q8 row scales
@@ -75,10 +88,9 @@ struct Params {
     const float* w;       // routing weights by pair id
     const float* rsa;     // DOWN: guard inverse scale per grouped pair
     float* out;           // GATEUP: a [P][I]; DOWN: eo [P][H]
-    int topk;
     int64_t I, H;
     uint64_t wait_ns;
-    int pdl;              // launched with a programmatic dependency on the previous kernel
+    int pdl;              // launch with a programmatic dependency on the previous kernel
     const int32_t* act;   // MoE: active experts, ascending
     const int32_t* n_act; // MoE: number of active experts
     int rbs;              // MoE: row blocks per expert matrix
@@ -89,44 +101,69 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
     return r;
 }
-
-// Two nibbles at bits 0-3 and 16-19 -> half2 (nibble - 8), exact:
-// 0x6400 | n is the fp16 value 1024 + n; subtracting 1032 leaves n - 8.
-__device__ __forceinline__ uint32_t nib2_to_h2(uint32_t v) {
-    const uint32_t h = (v & 0x000F000Fu) | 0x64006400u;
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
-    return *reinterpret_cast<const uint32_t*>(&r);
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<const __half2*>(&v); }
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128a(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
 }
 
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
-    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), s);
-    return *reinterpret_cast<const uint32_t*>(&r);
+// Eight nibbles (bytes b0..b3 of w, one 32-bit word of a Q4 block) -> four
+// fp16 pairs holding n - 8 exactly:
+// d[0] = low nibbles of (b0, b2), d[1] = high nibbles of (b0, b2),
+// d[2] = low nibbles of (b1, b3), d[3] = high nibbles of (b1, b3).
+// 0x6400 | n is 1024 + n and 0x6400 | (n << 4) is 1024 + 16 n; 1024 + n - 1032
+// and (1024 + 16 n) / 16 - 72 are both n - 8 with no rounding.
+__device__ __forceinline__ void decode_q4_word(uint32_t w, uint32_t d[4]) {
+    const __half2 k1032 = u32_as_h2(0x64086408u);               // 1032
+    const __half2 k16th = u32_as_h2(0x2C002C00u);               // 1/16
+    const __half2 km72 = u32_as_h2(0xD480D480u);                // -72
+    const uint32_t w8 = w >> 8;
+    d[0] = h2_as_u32(__hsub2(u32_as_h2((w & 0x000F000Fu) | 0x64006400u), k1032));
+    d[1] = h2_as_u32(__hfma2(u32_as_h2((w & 0x00F000F0u) | 0x64006400u), k16th, km72));
+    d[2] = h2_as_u32(__hsub2(u32_as_h2((w8 & 0x000F000Fu) | 0x64006400u), k1032));
+    d[3] = h2_as_u32(__hfma2(u32_as_h2((w8 & 0x00F000F0u) | 0x64006400u), k16th, km72));
 }
 
-// int8 pair (bytes sel0, sel1 of w) -> half2 exactly: (v ^ 0x80) | 0x6400
-// is 1024 + v + 128; subtracting 1152 leaves v.
-__device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t w, uint32_t sel) {
-    const uint32_t h = prmt(w ^ 0x80808080u, 0x64646464u, sel);
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
-    return *reinterpret_cast<const uint32_t*>(&r);
+// int8 pair (bytes sel of w) -> half2 exactly: (v ^ 0x80) | 0x6400 is
+// 1024 + v + 128; subtracting 1152 leaves v.
+__device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t wx /* w ^ 0x80808080 */, uint32_t sel) {
+    const uint32_t h = prmt(wx, 0x64646464u, sel);
+    return h2_as_u32(__hsub2(u32_as_h2(h), u32_as_h2(0x64806480u)));
 }
-// int8 pair (bytes lo_byte, lo_byte+1 of w) -> bf16x2 exactly: 0x4B0000uu is
-// the f32 2^23 + u with u = v + 128; subtracting 2^23 + 128 leaves v.
-__device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, int lo_byte) {
-    const uint32_t wx = w ^ 0x80808080u;
-    const float a = __uint_as_float(prmt(wx, 0x4B000000u, 0x7440u + (uint32_t)lo_byte)) - 8388736.0f;
-    const float b = __uint_as_float(prmt(wx, 0x4B000000u, 0x7441u + (uint32_t)lo_byte)) - 8388736.0f;
-    const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+// int8 pair (bytes sel of w) -> bf16x2 exactly: with 0x43 as the high byte,
+// the low seven bits of v give 128 + (v & 127) and the sign bit gives 128 or
+// 256 (0x4300 / 0x4380); their difference is v, an integer bf16 holds exactly.
+__device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
+    const uint32_t t = prmt(w, 0x43434343u, sel);
+    const uint32_t lo = t & 0xFF7FFF7Fu, hi = t & 0xFF80FF80u;
+    const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&lo),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&hi));
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // One stage in shared memory, filled by three TMA copies (five for gate/up):
-//  W  [64 rows][128 B], 128-byte swizzle: 16-byte chunk j of row r at j ^ (r % 8)
+//  W  [RB rows][128 B], 128-byte swizzle: 16-byte chunk j of row r at j ^ (r % 8)
 //     (Q4: 256 k = eight 32-k blocks; Q8: 128 k = eight 16-k runs)
-//  S  [64 rows][8 fp16] block scales (Q4 only)
+//  S  [RB rows][8 fp16] block scales (Q4 only)
 //  X  [NCOL rows][XSL slabs of 64 k][128 B], 128-byte swizzle over the 3-D
-//     view {64 elements, K/64 slabs, rows} of the activations.
-template <int FMT, int NCOL>
+//     view {64 elements, K/64 slabs, rows} of the activations; a row's chunk
+//     c of slab s sits at c ^ ((XSL row + s) % 8).
+// Weight rows per stage for MT m16 tiles per warp and KW warp groups along k.
+__host__ __device__ constexpr int rows_per_stage(int MT, int KW) { return CONSUMERS / KW * MT * 16; }
+
+template <int FMT, int NCOL, int RB>
 struct StageGeo {
     static constexpr int KSTAGE = FMT == 0 ? 256 : 128;
     static constexpr int W_BYTES = RB * 128;
@@ -139,17 +176,26 @@ struct StageGeo {
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
-template <int FMT, int NT, int XBF, int MODE, int NSLOT>
+// MT: m16 tiles per consumer warp; KW: warp groups along k (the stage's
+// eight 32-k blocks, or 16-k runs, are split over them), so 8 / KW warps
+// cover the stage's RB = 8 / KW * MT * 16 rows.
+template <int FMT, int NT, int MT, int KW, int XBF, int MODE, int NSLOT>
 __global__ void __launch_bounds__(THREADS, 2)
 k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
          const __grid_constant__ CUtensorMap tmX, const Params p) {
     constexpr int NCOL = 8 * NT;
-    using G = StageGeo<FMT, NCOL>;
+    constexpr int RG = CONSUMERS / KW;        // warps along rows
+    constexpr int RB = rows_per_stage(MT, KW);
+    static_assert(KW == 1 || KW == 2, "k split over one or two warp groups");
+    static_assert(FMT == 1 || (MT == 1 && XBF == 0), "Q4 stages: one m16 tile per warp, guarded fp16 activations");
+    static_assert(MODE == DENSE || RB == 128, "expert panels use 128-row stages");
+    using G = StageGeo<FMT, NCOL, RB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
+    pdl_launch_dependents();   // the next kernel in the stream may be scheduled now
     // ---- work items: (expert, row block) pairs; each may hold several column groups ----
     // dense: one item per CTA (row block blockIdx.y, k range blockIdx.x of the cluster);
     // MoE: a static round-robin share of (active expert x row block), so the
@@ -183,12 +229,12 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
             it.ncols = p.seg[it.expert + 1] - it.col0;
         }
         it.ngroups = (int)((it.ncols + NCOL - 1) / NCOL);
-        if (MODE == GATEUP) {
-            it.row_box[0] = it.rb * 32;
-            it.row_box[1] = (int)p.I + it.rb * 32;
+        if (MODE == GATEUP) {     // 64 gate rows, then the 64 matching up rows
+            it.row_box[0] = it.rb * (RB / 2);
+            it.row_box[1] = (int)p.I + it.rb * (RB / 2);
         } else {
             it.row_box[0] = it.rb * RB;
-            it.row_box[1] = it.rb * RB + 32;
+            it.row_box[1] = 0;
         }
         return it;
     };
@@ -200,12 +246,12 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     const int nst = st1 - st0;
 
     // ---- shared memory carve-up ----
+    // part [RB][NCOL] f32: the CTA's partial tile (dense: aliases the ring, which
+    // is idle once every stage has been consumed)
     constexpr int RING = NSLOT * G::BYTES;
-    constexpr int RED = CONSUMERS * RB * NCOL * 4;
-    constexpr int RED_OFF = (MODE == DENSE) ? 0 : RING;
-    constexpr int PART_OFF = (MODE == DENSE) ? (RING > RED ? RING : RED) : RING + RED;
-    constexpr int BAR_OFF = PART_OFF + RB * NCOL * 4;
-    float* red = reinterpret_cast<float*>(smem + RED_OFF);
+    constexpr int PART_OFF = (MODE == DENSE) ? 0 : RING;
+    constexpr int PART_BYTES = RB * NCOL * 4;
+    constexpr int BAR_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
     float* part = reinterpret_cast<float*>(smem + PART_OFF);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // full[NSLOT], empty[NSLOT]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NSLOT);
@@ -219,7 +265,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), CONSUMERS);
         }
         *abort_flag = 0;
         *never_flag = 0;
@@ -239,16 +285,17 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 if (FMT == 0) tma_prefetch_desc(&tmS);
                 tma_prefetch_desc(&tmX);
             }
-            int64_t last_gi = -1;     // the last stage this lane issued
+            int last_gi = -1;         // the last stage this lane issued
+            uint32_t last_phase = 0;  // and the phase of its round
             bool ok = true;
             auto load_w = [&](const Item& it, int i) {
                 const uint32_t sbase = smem_base + (uint32_t)(s * G::BYTES);
                 const int st = st0 + i;
-                if (MODE == GATEUP) {      // gate rows and up rows are 32-row boxes apart in the matrix
+                if (MODE == GATEUP) {      // gate rows and up rows are two 64-row boxes
                     for (int bx = 0; bx < 2; ++bx) {
-                        tma_load_3d(sbase + (uint32_t)(bx * 32 * 128), &tmW, full_bar(s), st * 128, it.row_box[bx],
-                                    it.expert);
-                        tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * 32 * 16), &tmS, full_bar(s), st * 8,
+                        tma_load_3d(sbase + (uint32_t)(bx * (RB / 2) * 128), &tmW, full_bar(s), st * 128,
+                                    it.row_box[bx], it.expert);
+                        tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * (RB / 2) * 16), &tmS, full_bar(s), st * 8,
                                     it.row_box[bx], it.expert);
                     }
                 } else {
@@ -263,10 +310,9 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 const int xrow0 = (int)(it.col0 + (int64_t)grp * NCOL);
                 tma_load_3d(sbase + (uint32_t)G::X_OFF, &tmX, full_bar(s), 0, st * G::XSL, xrow0);
             };
-            // With a programmatic dependency (dense Q4: the activation guard pass runs just
-            // before), the weights of the first ring fill are requested before waiting for
-            // the activations; everything else follows the wait.
-            const bool pre = MODE == DENSE && p.pdl && s < nst;
+            // The weights of the first ring fill are requested before waiting for the
+            // previous kernel in the stream; the activations follow the wait.
+            const bool pre = MODE == DENSE && s < nst;
             if (MODE == DENSE) {
                 if (pre) {                                   // fresh slot: no empty wait needed
                     mbar_arrive_expect_tx(full_bar(s), (uint32_t)G::BYTES);
@@ -276,16 +322,25 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 if (pre) {
                     load_x(get_item(0), s, 0);
                     last_gi = s;
+                    last_phase = 0;   // round 0
                 }
             }
-            int64_t gi = 0;
+            // walk every stage in order; this lane issues the ones that land in slot s
+            int gi = 0, slot = 0;
+            uint32_t phase = 0;
             for (int idx = first; idx < nitems && ok; idx += stride) {
                 const Item it = get_item(idx);
                 for (int grp = 0; grp < it.ngroups && ok; ++grp) {
                     for (int i = 0; i < nst; ++i, ++gi) {
-                        if (gi % NSLOT != s || (pre && gi == s)) continue;
-                        const uint32_t par = (uint32_t)((gi / NSLOT) & 1);
-                        if (!mbar_wait(empty_bar(s), par ^ 1u, p.wait_ns, abort_flag)) {
+                        const int my = slot == s && !(pre && gi == s);
+                        const uint32_t ph = phase;
+                        if (++slot == NSLOT) {
+                            slot = 0;
+                            phase ^= 1u;
+                        }
+                        if (!my) continue;
+                        // round r of the slot waits for the consumers' release of round r - 1
+                        if (!mbar_wait(empty_bar(s), ph ^ 1u, p.wait_ns, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -293,6 +348,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                         load_w(it, i);
                         load_x(it, i, grp);
                         last_gi = gi;
+                        last_phase = ph;
                     }
                 }
             }
@@ -301,17 +357,28 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
             }
             if (*abort_flag && last_gi >= 0)   // this lane's last copy must land before the CTA can exit
-                mbar_wait(full_bar(s), (uint32_t)((last_gi / NSLOT) & 1), p.wait_ns, never_flag);
+                mbar_wait(full_bar(s), last_phase, p.wait_ns, never_flag);
         }
         __syncwarp();
     } else {
         // ================= consumers =================
-        int64_t gbase = 0;   // global index of the first stage of the current column group
+        const int rg = warp % RG, kq = warp / RG;
+        const int row0 = rg * (16 * MT) + g;      // this lane's first row in the stage (row0 % 8 == g)
+        const uint32_t kqv = KW == 1 ? 0u : (uint32_t)kq;
+        // Lane-constant parts of the shared-memory addresses.  Stage bases are
+        // 1024-aligned and these offsets leave bits 4..6 to the swizzle terms, so
+        // the per-block 16-byte chunk choice is one XOR with a compile-time value.
+        //  W: row row0, chunk (j ^ g), word c; row row0 + 8 is 1024 bytes further.
+        const uint32_t w_lane = ((uint32_t)(row0 * 128 + 4 * c) ^ ((uint32_t)g << 4)) ^ (kqv << 4);
+        //  X (Q4): row 8 nt + g, slab j / 2, chunk 4 (j % 2) + c, swizzled by the
+        //  line (4 row + slab) % 8 = (4 (g % 2)) ^ (j / 2).
+        const uint32_t x_lane = (uint32_t)(512 * g) | ((((uint32_t)c) ^ (4u * (uint32_t)(g & 1)) ^ (4u * kqv)) << 4);
+        uint32_t slot = 0, phase = 0;             // ring position of the next stage (same walk as the producers)
         for (int idx = first; idx < nitems; idx += stride) {
           const Item it = get_item(idx);
           const int64_t col0 = it.col0, ncols_total = it.ncols;
           const int rb = it.rb;
-          for (int grp = 0; grp < it.ngroups; ++grp, gbase += nst) {
+          for (int grp = 0; grp < it.ngroups; ++grp) {
             const int64_t cbase = (int64_t)grp * NCOL;
             float acc[MT][NT][4];
 #pragma unroll
@@ -322,109 +389,101 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                     for (int q = 0; q < 4; ++q) acc[a][b][q] = 0.f;
 
             bool ok = !*abort_flag;
-            // Stage gi goes to warp gi % CONSUMERS and slot gi % NSLOT; NSLOT is a multiple of
-            // CONSUMERS, so each slot always belongs to one warp, which then waits for the
-            // slot's rounds in order (a parity wait cannot tell round r+1 from round r-1).
-            for (int i = (int)((warp - gbase % CONSUMERS + CONSUMERS) % CONSUMERS); i < nst && ok; i += CONSUMERS) {
-                const int64_t gi = gbase + i;
-                const int slot = (int)(gi % NSLOT);
-                if (!mbar_wait(full_bar(slot), (uint32_t)((gi / NSLOT) & 1), p.wait_ns, abort_flag)) {
+            for (int i = 0; i < nst && ok; ++i) {
+                if (!mbar_wait(full_bar((int)slot), phase, p.wait_ns, abort_flag)) {
                     ok = false;
                     *abort_flag = 1;
                     atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
                     break;
                 }
-                const uint8_t* sW = smem + slot * G::BYTES;
-                const uint8_t* sX = sW + G::X_OFF;
+                const uint32_t sW = smem_base + slot * (uint32_t)G::BYTES;
+                const uint32_t sX = sW + (uint32_t)G::X_OFF;
                 if (FMT == 0) {
-                    const __half* sS = reinterpret_cast<const __half*>(sW + G::W_BYTES);
+                    // Block j = jf + kq: the two MMAs over its 32 k see one scale per row, so
+                    // their f32 result is scaled once into the sum.
+                    const uint32_t wS = sW + w_lane, xS = sX + x_lane;
+                    const uint32_t sS = sW + (uint32_t)G::W_BYTES + (uint32_t)(row0 * 16) + 2u * kqv;
+                    uint4 sc0 = make_uint4(0, 0, 0, 0), sc1 = make_uint4(0, 0, 0, 0);
+                    if (KW == 1) {                      // all eight block scales of both rows
+                        sc0 = lds128a(sS);
+                        sc1 = lds128a(sS + 128);
+                    }
+#pragma unroll(KW == 1 ? 8 : 2)
+                    for (int jj = 0; jj < 8 / KW; ++jj) {
+                        const int jf = KW == 1 ? jj : 2 * jj;     // the block index without this warp's k half
+                        const uint32_t wad = wS ^ ((uint32_t)jf << 4);
+                        const uint32_t wa = lds32(wad), wb = lds32(wad + 1024);
+                        const uint32_t jx = (4u * (uint32_t)(jf & 1)) ^ (uint32_t)(jf >> 1);
+                        const uint32_t xad = (xS ^ (jx << 4)) + 128u * (uint32_t)(jf >> 1);
+                        uint4 bx[NT];
 #pragma unroll
-                    for (int kh = 0; kh < 2; ++kh) {
-                        // this thread's 32-k block j = 2c + kh: weight chunk j of each row, and
-                        // activations k = 32 j .. 32 j + 31 = slab c, bytes 64 kh .. 64 kh + 63
-                        const int j = 2 * c + kh;
+                        for (int nt = 0; nt < NT; ++nt) bx[nt] = lds128a(xad + 4096u * nt);
+                        float sa, sb;
+                        if (KW == 1) {
+                            const uint32_t wsa = (jf >> 1) == 0 ? sc0.x : (jf >> 1) == 1 ? sc0.y : (jf >> 1) == 2 ? sc0.z : sc0.w;
+                            const uint32_t wsb = (jf >> 1) == 0 ? sc1.x : (jf >> 1) == 1 ? sc1.y : (jf >> 1) == 2 ? sc1.z : sc1.w;
+                            sa = __half2float(__ushort_as_half((unsigned short)((jf & 1) ? (wsa >> 16) : (wsa & 0xFFFFu))));
+                            sb = __half2float(__ushort_as_half((unsigned short)((jf & 1) ? (wsb >> 16) : (wsb & 0xFFFFu))));
+                        } else {
+                            sa = __half2float(__ushort_as_half((unsigned short)lds16(sS + 2u * jf)));
+                            sb = __half2float(__ushort_as_half((unsigned short)lds16(sS + 128u + 2u * jf)));
+                        }
+                        uint32_t d[4], e[4];
+                        decode_q4_word(wa, d);
+                        decode_q4_word(wb, e);
+                        const uint32_t a1[4] = {d[0], e[0], d[1], e[1]};
+                        const uint32_t a2[4] = {d[2], e[2], d[3], e[3]};
 #pragma unroll
-                        for (int sp = 0; sp < 2; ++sp) {
-                            // words 4sp..4sp+3 (low-nibble steps 2sp, 2sp+1) and 8+4sp.. (high-nibble steps)
-                            uint4 blo[NT], bhi[NT];
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                const int row = 8 * nt + g;
-                                const uint8_t* xr = sX + row * (G::XSL * 128) + c * 128;
-                                const int sw = (G::XSL * row + c) & 7;
-                                blo[nt] = lds128(xr + (((4 * kh + sp) ^ sw) << 4));
-                                bhi[nt] = lds128(xr + (((4 * kh + 2 + sp) ^ sw) << 4));
-                            }
-#pragma unroll
-                            for (int mt = 0; mt < MT; ++mt) {
-                                const int lr = 16 * mt + g;
-                                const uint4 wa = lds128(sW + lr * 128 + ((j ^ (lr & 7)) << 4));
-                                const uint4 wb = lds128(sW + (lr + 8) * 128 + ((j ^ ((lr + 8) & 7)) << 4));
-                                const __half s0 = sS[lr * 8 + j];
-                                const __half s1 = sS[(lr + 8) * 8 + j];
-                                const __half2 sa = __halves2half2(s0, s0), sb2 = __halves2half2(s1, s1);
-                                const uint32_t r0[4] = {wa.x, wa.y, wa.z, wa.w};
-                                const uint32_t r1[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-                                for (int u = 0; u < 2; ++u) {
-                                    const int st4 = 2 * sp + u;
-                                    const uint32_t p0 = prmt(r0[st4], 0u, 0x3120u), p1 = prmt(r1[st4], 0u, 0x3120u);
-                                    uint32_t alo[4], ahi[4];
-                                    alo[0] = hmul2_u32(nib2_to_h2(p0), sa);
-                                    alo[1] = hmul2_u32(nib2_to_h2(p1), sb2);
-                                    alo[2] = hmul2_u32(nib2_to_h2(p0 >> 8), sa);
-                                    alo[3] = hmul2_u32(nib2_to_h2(p1 >> 8), sb2);
-                                    ahi[0] = hmul2_u32(nib2_to_h2(p0 >> 4), sa);
-                                    ahi[1] = hmul2_u32(nib2_to_h2(p1 >> 4), sb2);
-                                    ahi[2] = hmul2_u32(nib2_to_h2(p0 >> 12), sa);
-                                    ahi[3] = hmul2_u32(nib2_to_h2(p1 >> 12), sb2);
-#pragma unroll
-                                    for (int nt = 0; nt < NT; ++nt) {
-                                        const uint32_t l0 = u ? blo[nt].z : blo[nt].x, l1 = u ? blo[nt].w : blo[nt].y;
-                                        const uint32_t h0 = u ? bhi[nt].z : bhi[nt].x, h1 = u ? bhi[nt].w : bhi[nt].y;
-                                        mma_16816_f16(acc[mt][nt], alo, l0, l1);
-                                        mma_16816_f16(acc[mt][nt], ahi, h0, h1);
-                                    }
-                                }
-                            }
+                        for (int nt = 0; nt < NT; ++nt) {
+                            float pb[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_16816_f16(pb, a1, bx[nt].x, bx[nt].y);
+                            mma_16816_f16(pb, a2, bx[nt].z, bx[nt].w);
+                            acc[0][nt][0] = fmaf(sa, pb[0], acc[0][nt][0]);
+                            acc[0][nt][1] = fmaf(sa, pb[1], acc[0][nt][1]);
+                            acc[0][nt][2] = fmaf(sb, pb[2], acc[0][nt][2]);
+                            acc[0][nt][3] = fmaf(sb, pb[3], acc[0][nt][3]);
                         }
                     }
                 } else {
+                    const uint8_t* pW = smem + slot * G::BYTES;
+                    const uint8_t* pX = pW + G::X_OFF;
 #pragma unroll
-                    for (int kh = 0; kh < 2; ++kh) {
-                        // this thread's 16-k run j = 2c + kh: weight chunk j of each row, and
+                    for (int kk = 0; kk < 2 / KW; ++kk) {
+                        // this lane's 16-k run j = 2c + kh: chunk j of each of its rows, and
                         // activations k = 16 j .. 16 j + 15 = slab j / 4, 32 bytes at 32 (j % 4)
+                        const int kh = KW == 1 ? kk : kq;
                         const int j = 2 * c + kh;
                         const int slab = j >> 2;
                         uint4 b0[NT], b1[NT];
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const int row = 8 * nt + g;
-                            const uint8_t* xr = sX + row * (G::XSL * 128) + slab * 128;
-                            const int sw = (G::XSL * row + slab) & 7;
+                            const int xrow = 8 * nt + g;
+                            const uint8_t* xr = pX + xrow * (G::XSL * 128) + slab * 128;
+                            const int sw = (G::XSL * xrow + slab) & 7;
                             b0[nt] = lds128(xr + (((2 * (j & 3)) ^ sw) << 4));
                             b1[nt] = lds128(xr + (((2 * (j & 3) + 1) ^ sw) << 4));
                         }
 #pragma unroll
                         for (int mt = 0; mt < MT; ++mt) {
-                            const int lr = 16 * mt + g;
-                            const uint4 w0 = lds128(sW + lr * 128 + ((j ^ (lr & 7)) << 4));
-                            const uint4 w1 = lds128(sW + (lr + 8) * 128 + ((j ^ ((lr + 8) & 7)) << 4));
-                            const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
-                            const uint32_t r1[4] = {w1.x, w1.y, w1.z, w1.w};
+                            const int r0 = row0 + 16 * mt;
+                            const uint4 w0 = lds128(pW + r0 * 128 + ((j ^ g) << 4));
+                            const uint4 w1 = lds128(pW + (r0 + 8) * 128 + ((j ^ g) << 4));
+                            const uint32_t q0[4] = {w0.x, w0.y, w0.z, w0.w};
+                            const uint32_t q1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                             for (int s4 = 0; s4 < 4; ++s4) {
                                 uint32_t a[4];
                                 if (XBF) {
-                                    a[0] = i8x2_to_bf2(r0[s4], 0);
-                                    a[1] = i8x2_to_bf2(r1[s4], 0);
-                                    a[2] = i8x2_to_bf2(r0[s4], 2);
-                                    a[3] = i8x2_to_bf2(r1[s4], 2);
+                                    a[0] = i8x2_to_bf2(q0[s4], 0x4140u);
+                                    a[1] = i8x2_to_bf2(q1[s4], 0x4140u);
+                                    a[2] = i8x2_to_bf2(q0[s4], 0x4342u);
+                                    a[3] = i8x2_to_bf2(q1[s4], 0x4342u);
                                 } else {
-                                    a[0] = i8x2_to_h2(r0[s4], 0x4140u);
-                                    a[1] = i8x2_to_h2(r1[s4], 0x4140u);
-                                    a[2] = i8x2_to_h2(r0[s4], 0x4342u);
-                                    a[3] = i8x2_to_h2(r1[s4], 0x4342u);
+                                    const uint32_t x0w = q0[s4] ^ 0x80808080u, x1w = q1[s4] ^ 0x80808080u;
+                                    a[0] = i8x2_to_h2(x0w, 0x4140u);
+                                    a[1] = i8x2_to_h2(x1w, 0x4140u);
+                                    a[2] = i8x2_to_h2(x0w, 0x4342u);
+                                    a[3] = i8x2_to_h2(x1w, 0x4342u);
                                 }
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
@@ -439,45 +498,55 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(slot));
+                if (lane == 0) mbar_arrive(empty_bar((int)slot));
+                if (++slot == (uint32_t)NSLOT) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
             }
 
-            // ---- deterministic reduction over the consumer warps ----
-            // (dense: red aliases the ring, so every warp must be done with it)
+            // ---- the CTA's partial tile ----
+            // (dense: part aliases the ring, so every warp must be done with it; the k
+            // halves of KW == 2 are added in a fixed order)
             if (MODE == DENSE) asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int h = 0; h < KW; ++h) {
+                if (kq == h) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int r = 16 * mt + g, col = 8 * nt + 2 * c;
-                    float* base = red + ((size_t)warp * RB) * NCOL;
-                    base[r * NCOL + col] = acc[mt][nt][0];
-                    base[r * NCOL + col + 1] = acc[mt][nt][1];
-                    base[(r + 8) * NCOL + col] = acc[mt][nt][2];
-                    base[(r + 8) * NCOL + col + 1] = acc[mt][nt][3];
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const int r = row0 + 16 * mt, col = 8 * nt + 2 * c;
+                            float2* p0 = reinterpret_cast<float2*>(part + r * NCOL + col);
+                            float2* p1 = reinterpret_cast<float2*>(part + (r + 8) * NCOL + col);
+                            if (h == 0) {
+                                *p0 = make_float2(acc[mt][nt][0], acc[mt][nt][1]);
+                                *p1 = make_float2(acc[mt][nt][2], acc[mt][nt][3]);
+                            } else {
+                                const float2 u0 = *p0, u1 = *p1;
+                                *p0 = make_float2(u0.x + acc[mt][nt][0], u0.y + acc[mt][nt][1]);
+                                *p1 = make_float2(u1.x + acc[mt][nt][2], u1.y + acc[mt][nt][3]);
+                            }
+                        }
                 }
-            asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
-            for (int e = threadIdx.x; e < RB * NCOL; e += CONSUMERS * 32) {
-                float s = 0.f;
-#pragma unroll
-                for (int w = 0; w < CONSUMERS; ++w) s += red[(size_t)w * RB * NCOL + e];
-                part[e] = s;
+                asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
             }
-            asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
 
-            if (MODE != DENSE && !*abort_flag) {
-                // MoE epilogues (single CTA per k range)
+            if (MODE != DENSE) {
+              // MoE epilogues (single CTA per k range).  The barrier after them is taken by
+              // every consumer warp whatever the abort flag says, so the counts always match.
+              if (!*abort_flag) {
                 if (MODE == GATEUP) {
-                    // element (i, col): gate at local row i, up at local row 32 + i
-                    for (int e = threadIdx.x; e < 32 * NCOL; e += CONSUMERS * 32) {
-                        const int i = e & 31, col = e >> 5;
+                    // element (i, col): gate at local row i, up at local row 64 + i
+                    for (int e = threadIdx.x; e < (RB / 2) * NCOL; e += CONSUMERS * 32) {
+                        const int i = e & (RB / 2 - 1), col = e / (RB / 2);
                         const int64_t q = cbase + col;
                         if (q >= ncols_total) continue;
                         const int64_t pos = col0 + q;
                         const float sc = p.rsx[pos];
                         const float gv = part[i * NCOL + col] * sc;
-                        const float uv = part[(32 + i) * NCOL + col] * sc;
-                        p.out[pos * p.I + (int64_t)rb * 32 + i] = gv / (1.0f + expf(-gv)) * uv;
+                        const float uv = part[(RB / 2 + i) * NCOL + col] * sc;
+                        p.out[pos * p.I + (int64_t)rb * (RB / 2) + i] = gv / (1.0f + expf(-gv)) * uv;
                     }
                 } else {
                     for (int e = threadIdx.x; e < RB * NCOL; e += CONSUMERS * 32) {
@@ -489,7 +558,8 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                         p.out[pos * p.H + (int64_t)rb * RB + r] = v;
                     }
                 }
-                asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
+              }
+              asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
             }
           }
         }
@@ -533,14 +603,14 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     }
 }
 
-template <int FMT, int NT, int XBF, int MODE, int NSLOT>
+template <int FMT, int NT, int RB, int MODE, int NSLOT>
 constexpr size_t smem_bytes() {
     constexpr int NCOL = 8 * NT;
-    using G = StageGeo<FMT, NCOL>;
+    using G = StageGeo<FMT, NCOL, RB>;
     constexpr int RING = NSLOT * G::BYTES;
-    constexpr int RED = CONSUMERS * RB * NCOL * 4;
-    constexpr int PART_OFF = (MODE == DENSE) ? (RING > RED ? RING : RED) : RING + RED;
-    return (size_t)PART_OFF + RB * NCOL * 4 + 2 * NSLOT * 8 + 16 + 1024;
+    constexpr int PART_BYTES = RB * NCOL * 4;
+    constexpr int BAR_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
+    return (size_t)BAR_OFF + 2 * NSLOT * 8 + 16 + 1024;
 }
 
 // Weights [E][R][K bytes] and scales [E][R][K/32], boxes of rows_box rows.
@@ -573,15 +643,15 @@ bool make_xmap(CUtensorMap* mx, const void* x, int64_t rows, int64_t K, int bf16
                         box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int FMT, int NT, int XBF, int MODE, int NSLOT>
+template <int FMT, int NT, int MT, int KW, int XBF, int MODE, int NSLOT>
 cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, int64_t xrows, const Params& p,
                      dim3 grid, int cluster, cudaStream_t s) {
+    constexpr int RB = rows_per_stage(MT, KW);
     CUtensorMap mx;
-    if (!make_xmap(&mx, x, xrows, p.K, XBF, 8 * NT, StageGeo<FMT, 8 * NT>::XSL)) return cudaErrorInvalidValue;
-    auto kern = k_skinny<FMT, NT, XBF, MODE, NSLOT>;
-    constexpr size_t smem = smem_bytes<FMT, NT, XBF, MODE, NSLOT>();
+    if (!make_xmap(&mx, x, xrows, p.K, XBF, 8 * NT, StageGeo<FMT, 8 * NT, RB>::XSL)) return cudaErrorInvalidValue;
+    auto kern = k_skinny<FMT, NT, MT, KW, XBF, MODE, NSLOT>;
+    constexpr size_t smem = smem_bytes<FMT, NT, RB, MODE, NSLOT>();
     static_assert(smem <= 113 * 1024, "two CTAs per SM");
-    static_assert(NSLOT % CONSUMERS == 0, "each ring slot is consumed by one warp");
     static int configured_device = -1;       // attributes are per device; set once per instantiation
     int dev = 0;
     cudaGetDevice(&dev);
@@ -609,31 +679,43 @@ cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& ms, const void* x
     return cudaLaunchKernelEx(&cfg, kern, mw, ms, mx, p);
 }
 
+// Layout and ring depth per column count (as many stages as fit two CTAs
+// per SM): up to 16 columns, 128-row stages with every warp on the whole
+// stage; 32 columns, 64-row stages with the k blocks split over two warp
+// groups, so each warp reads half of the activations.
+struct DenseCfg {
+    int nt, mt, kw, rb;
+};
+DenseCfg dense_cfg(int64_t T) {
+    if (T <= 8) return {1, 1, 1, rows_per_stage(1, 1)};
+    if (T <= 16) return {2, 1, 1, rows_per_stage(1, 1)};
+    return {4, 1, 2, rows_per_stage(1, 2)};
+}
+
 template <int FMT, int XBF>
 cudaError_t launch_dense_nt(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, const Params& p, dim3 grid,
                             int cluster, int64_t T, cudaStream_t s) {
-    constexpr int S1 = 8, S2 = FMT == 0 ? 4 : 8, S4 = 4;
-    if (T <= 8) return launch_t<FMT, 1, XBF, DENSE, S1>(mw, ms, x, T, p, grid, cluster, s);
-    if (T <= 16) return launch_t<FMT, 2, XBF, DENSE, S2>(mw, ms, x, T, p, grid, cluster, s);
-    return launch_t<FMT, 4, XBF, DENSE, S4>(mw, ms, x, T, p, grid, cluster, s);
+    if (T <= 8) return launch_t<FMT, 1, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 6>(mw, ms, x, T, p, grid, cluster, s);
+    if (T <= 16) return launch_t<FMT, 2, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 5>(mw, ms, x, T, p, grid, cluster, s);
+    return launch_t<FMT, 4, 1, 2, XBF, DENSE, FMT == 0 ? 4 : 6>(mw, ms, x, T, p, grid, cluster, s);
 }
 
 cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
+    const DenseCfg cf = dense_cfg(a.T);
     CUtensorMap mw, ms;
-    if (!make_maps(&mw, &ms, fmt, a.wq, a.ws, a.N, a.K, 1, RB)) return cudaErrorInvalidValue;
+    if (!make_maps(&mw, &ms, fmt, a.wq, a.ws, a.N, a.K, 1, cf.rb)) return cudaErrorInvalidValue;
     Params p = {};
     p.K = a.K;
     p.nst_total = (int)(a.K / (fmt == 0 ? 256 : 128));
     p.N = a.N;
-    p.x = reinterpret_cast<const uint16_t*>(a.x);
     p.T = a.T;
     p.rsx = a.rsx;
     p.rs = a.rs;
     p.y = a.y;
     p.yt = a.yt;
     p.wait_ns = (uint64_t)options().wait_ns;
-    p.pdl = fmt == 0 ? 1 : 0;     // Q4: the guard pass just before touches neither weights nor Y
-    const int64_t rbs = (a.N + RB - 1) / RB;
+    p.pdl = 1;
+    const int64_t rbs = (a.N + cf.rb - 1) / cf.rb;
     int ks = 1;
     const int64_t cap = 2 * (int64_t)num_sms();      // two CTAs fit per SM
     for (int cand : {2, 4, 8})
@@ -641,11 +723,11 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     p.ks = ks;
     dim3 grid((unsigned)ks, (unsigned)rbs, 1);
     if (options().trace)
-        fprintf(stderr, "cq: skinny fmt=%d T=%lld N=%lld K=%lld grid=(%d,%lld) cluster=%d\n", fmt, (long long)a.T,
-                (long long)a.N, (long long)a.K, ks, (long long)rbs, ks);
+        fprintf(stderr, "cq: skinny fmt=%d T=%lld N=%lld K=%lld rows/stage=%d grid=(%d,%lld) cluster=%d\n", fmt,
+                (long long)a.T, (long long)a.N, (long long)a.K, cf.rb, ks, (long long)rbs, ks);
     if (fmt == 0) return launch_dense_nt<0, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
-    if (a.x_bf16) return launch_dense_nt<1, 1>(mw, ms, a.x, p, grid, ks, a.T, s);
-    return launch_dense_nt<1, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
+    return a.x_bf16 ? launch_dense_nt<1, 1>(mw, ms, a.x, p, grid, ks, a.T, s)
+                    : launch_dense_nt<1, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
 }
 
 }  // namespace
@@ -654,60 +736,61 @@ cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s) { return laun
 cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s) { return launch_dense(1, a, s); }
 
 // Gate/up panels: activations are the guarded rows already gathered into
-// grouped order ([P][H] fp16, inverse scales [P]).
+// grouped order ([P][H] fp16, inverse scales [P]).  One item is 64 gate rows
+// and the 64 matching up rows of one expert.
 cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s) {
     CUtensorMap mw, ms;
-    if (!make_maps(&mw, &ms, 0, m.gu_q, m.gu_s, 2 * m.I, m.H, m.E, 32)) return cudaErrorInvalidValue;
+    constexpr int RB = rows_per_stage(1, 1);
+    if (!make_maps(&mw, &ms, 0, m.gu_q, m.gu_s, 2 * m.I, m.H, m.E, RB / 2)) return cudaErrorInvalidValue;
     Params p = {};
     p.K = m.H;
     p.nst_total = (int)(m.H / 256);
     p.ks = 1;
     p.N = 2 * m.I;
-    p.x = m.xh;
     p.rsx = m.rsx;
     p.seg = m.seg;
     p.perm = m.perm;
     p.status = m.status;
     p.w = m.w;
     p.out = m.a;
-    p.topk = (int)m.topk;
     p.I = m.I;
     p.H = m.H;
     p.wait_ns = (uint64_t)options().wait_ns;
     p.act = m.act;
     p.n_act = m.n_act;
-    p.rbs = (int)(m.I / 32);
+    p.pdl = 1;
+    p.rbs = (int)(m.I / (RB / 2));
     // persistent: two CTAs per SM share the (active expert x row block) items
     const int64_t items_max = m.E * p.rbs;
     dim3 grid((unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items_max), 1, 1);
-    return launch_t<0, 1, 0, GATEUP, 4>(mw, ms, m.xh, m.T * m.topk, p, grid, 1, s);
+    return launch_t<0, 1, 1, 1, 0, GATEUP, 4>(mw, ms, m.xh, m.T * m.topk, p, grid, 1, s);
 }
 
 cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s) {
     CUtensorMap mw, ms;
+    constexpr int RB = rows_per_stage(1, 1);
     if (!make_maps(&mw, &ms, 0, m.d_q, m.d_s, m.H, m.I, m.E, RB)) return cudaErrorInvalidValue;
     Params p = {};
     p.K = m.I;
     p.nst_total = (int)(m.I / 256);
     p.ks = 1;
     p.N = m.H;
-    p.x = m.ah;
     p.rsa = m.rsa;
     p.seg = m.seg;
     p.perm = m.perm;
     p.status = m.status;
     p.w = m.w;
     p.out = m.eo;
-    p.topk = (int)m.topk;
     p.I = m.I;
     p.H = m.H;
     p.wait_ns = (uint64_t)options().wait_ns;
     p.act = m.act;
     p.n_act = m.n_act;
+    p.pdl = 1;
     p.rbs = (int)(m.H / RB);
     const int64_t items_max = m.E * p.rbs;
     dim3 grid((unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items_max), 1, 1);
-    return launch_t<0, 1, 0, DOWN, 4>(mw, ms, m.ah, m.T * m.topk, p, grid, 1, s);
+    return launch_t<0, 1, 1, 1, 0, DOWN, 4>(mw, ms, m.ah, m.T * m.topk, p, grid, 1, s);
 }
 
 }  // namespace cq

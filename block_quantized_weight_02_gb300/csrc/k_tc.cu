@@ -228,6 +228,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                     load_x(kb);
                     ++issued;
                 }
+            } else {
+                pdl_wait();   // every path waits once, so kernels later in the stream stay ordered
             }
             if (*abort_flag && issued > 0) {
                 // this lane's last copy must land before the CTA can exit

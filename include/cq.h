@@ -65,13 +65,18 @@ typedef enum { CQ_F16 = 0, CQ_BF16 = 1, CQ_F32 = 2 } cq_dtype;
  * X: fp16 or bf16 (xt), [T][K].  Wq: [N][K/2] bytes.  Ws: fp16 bits
  * [N][K/32].  Y: f32 or bf16 (yt), [T][N], overwritten.
  * Shape rules: T >= 1, N >= 1, K >= 256 and K % 256 == 0.
- * Arithmetic: each activation row is scaled by a power of two that puts its
- * largest magnitude in [2^13, 2^14) and rounded to fp16; each weight is
- * (nibble - 8) * scale rounded once to fp16; products accumulate in f32;
- * the output is scaled back by the inverse power of two and rounded once to
- * yt.  (The guard follows "oxinfer 0.0.5 src/metal.rs", MMA_SHADER_SRC
- * header and the x_half shader; the scale folded into the half operand
- * follows mma_tile on the same page.)
+ * Arithmetic, T > 32 (tcgen05 path): each activation row is scaled by a
+ * power of two that puts its largest magnitude in [2^13, 2^14) and rounded
+ * to fp16; each weight is (nibble - 8) * scale rounded once to fp16;
+ * products accumulate in f32; the output is scaled back by the inverse
+ * power of two and rounded once to yt.  (The guard follows "oxinfer 0.0.5
+ * src/metal.rs", MMA_SHADER_SRC header and the x_half shader; the scale
+ * folded into the half operand follows mma_tile on the same page.)
+ * Arithmetic, T <= 32 (weight-streaming path): the same guarded fp16
+ * activations; nibble - 8 is exact in fp16; the products of one 32-k block
+ * accumulate in f32 and are multiplied by the block scale (exact in f32)
+ * into an f32 sum, which the inverse power of two scales back before the
+ * one rounding to yt.
  * Workspace: cq_gemm_q4_workspace_bytes(T, K) bytes.
  * ------------------------------------------------------------------------- */
 size_t cq_gemm_q4_workspace_bytes(int64_t T, int64_t K);
