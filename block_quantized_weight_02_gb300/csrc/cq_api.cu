@@ -217,7 +217,7 @@ cq_status cq_gemm_q4(const void* X, int xt, int64_t T, int64_t K, const uint8_t*
     const Q4Ws w = q4_ws(ws, T, K);
     const bool skinny = use_skinny(T);
     if (skinny && T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4: the weight-streaming path serves T <= 32");
-    if ((st = launched(launch_x_half(X, xt, T, K, w.xh, w.rsx, skinny ? 1 : 0, s), "activation guard pass"))) return st;
+    if ((st = launched(launch_x_half(X, xt, T, K, w.xh, w.rsx, s), "activation guard pass"))) return st;
     if (skinny) {
         SkinnyDense a = {w.xh, 0, w.rsx, nullptr, Wq, Ws, T, K, N, Y, yt};
         return launched(launch_skinny_q4(a, s), "weight-streaming Q4 GEMM");
@@ -297,7 +297,7 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E, 
     m.act = act;
     m.n_act = act + E;
     if ((st = launched(launch_moe_route(idx, T, topk, E, const_cast<int32_t*>(m.seg), const_cast<int32_t*>(m.perm), inv, act, act + E, status, s), "MoE routing layout"))) return st;
-    if ((st = launched(launch_x_half_gather(X, xt, T * topk, H, const_cast<uint16_t*>(m.xh), const_cast<float*>(m.rsx), m.perm, (int)topk, status, 1, s), "MoE activation gather + guard pass"))) return st;
+    if ((st = launched(launch_x_half_gather(X, xt, T * topk, H, const_cast<uint16_t*>(m.xh), const_cast<float*>(m.rsx), m.perm, (int)topk, status, s), "MoE activation gather + guard pass"))) return st;
     if ((st = launched(launch_moe_gateup(m, s), "MoE gate/up panels"))) return st;
     if ((st = launched(launch_a_half(m.a, T * topk, I, const_cast<uint16_t*>(m.ah), const_cast<float*>(m.rsa), status, s), "MoE SwiGLU guard pass"))) return st;
     if ((st = launched(launch_moe_down(m, s), "MoE down panels"))) return st;

@@ -48,15 +48,12 @@ int take_error_tc();
 cudaError_t launch_dequant_q4(const uint8_t* wq, const uint16_t* ws, int64_t N, int64_t K, float* w, cudaStream_t s);
 cudaError_t launch_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, int64_t K, float* w, cudaStream_t s);
 // X rows -> fp16 with a per-row power-of-two guard; rsx = inverse scales.
-// stream_order: inside each 32-k block, write the order the weight-streaming
-// GEMM reads (position 8 wi + t <- k = 4 wi + {0,2,16,18,1,3,17,19}[t]);
-// otherwise k order (the tcgen05 GEMM).
-cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, int stream_order,
-                          cudaStream_t s);
+// Inside each 32-k block the output is in the Q4 streaming order (position
+// 8 wi + t <- k = 4 wi + {0,2,16,18,1,3,17,19}[t]) that both Q4 GEMMs read.
+cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s);
 // The same for gathered rows: output row r <- input row gather[r] / per.
 cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K, uint16_t* xh, float* rsx,
-                                 const int32_t* gather, int per, const int32_t* status, int stream_order,
-                                 cudaStream_t s);
+                                 const int32_t* gather, int per, const int32_t* status, cudaStream_t s);
 
 struct MoeWs;  // workspace carve-up (cq_api.cu)
 // Also writes the active experts (count > 0, ascending) to act[] and their number to *n_act.
@@ -105,7 +102,7 @@ cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s);
 
 // tcgen05 (large-T) GEMM.
 struct TcArgs {
-    const void* x;       // [T][K] fp16/bf16 (Q4: guarded fp16)
+    const void* x;       // [T][K] fp16/bf16 (Q4: guarded fp16 in the streaming order)
     int x_bf16;
     const float* rsx;    // Q4
     const float* rs;     // Q8

@@ -84,7 +84,7 @@ extern "C" cq_status cq_gemm_q4_noalloc(const void* X, int xt, int64_t T, int64_
     const Options& o = options();
     const bool skinny = o.force_path == 1 || (o.force_path == 0 && T <= o.small_t_max);
     if (skinny && T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4_noalloc: the weight-streaming path serves T <= 32");
-    e = launch_x_half(X, xt, T, K, xh, rsx, skinny ? 1 : 0, s);
+    e = launch_x_half(X, xt, T, K, xh, rsx, s);
     if (e != cudaSuccess) return cuda_fail(e, "activation guard pass");
     if (skinny) {
         SkinnyDense a = {xh, 0, rsx, nullptr, Wq, Ws, T, K, N, Y, yt};

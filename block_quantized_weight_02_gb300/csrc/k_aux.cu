@@ -110,14 +110,15 @@ __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// Order of the 16-bit activations inside each 32-k block for the
-// weight-streaming GEMM: position 8 wi + t holds k = 4 wi + TAU[t], TAU =
+// Order of the 16-bit activations inside each 32-k block for the Q4 GEMMs
+// (both paths): position 8 wi + t holds k = 4 wi + TAU[t], TAU =
 // {0, 2, 16, 18, 1, 3, 17, 19}.  Byte 4 wi + b of a packed Q4 block carries
 // elements 4 wi + b (low nibble) and 16 + 4 wi + b (high nibble); masking a
 // 32-bit word of four such bytes yields the pairs (b0, b2) and (b1, b3) of
 // each nibble plane, and this order puts the matching activations of one
-// word side by side, so one 16-byte shared-memory load feeds two MMAs.  The
-// contraction is the same sum in another order.
+// word side by side (one 16-byte shared-memory load feeds two MMAs of the
+// weight-streaming path; the tcgen05 path stores its decoded weights in the
+// same order).  The contraction is the same sum in another order.
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -132,14 +133,14 @@ __device__ __forceinline__ void store_block_stream_order(const float* v, uint4* 
     }
 }
 
-// One CTA of 256 threads per output row; K % 8 == 0 (K % 32 == 0 with
-// stream_order).  With a gather list, output row r is source row
+// One CTA of 256 threads per output row; K % 32 == 0; the output is in the
+// streaming order above.  With a gather list, output row r is source row
 // gather[r] / per (the MoE pairs in grouped order, as the pages' x_half
 // gathers through `src`).
 template <typename T>
 __global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t K, __half* __restrict__ xh,
                                                 float* __restrict__ rsx, const int32_t* __restrict__ gather, int per,
-                                                const int32_t* __restrict__ status, int stream_order) {
+                                                const int32_t* __restrict__ status) {
     pdl_launch_dependents();   // the GEMM after this pass may start streaming its weights now
     pdl_wait();                // inputs ready and the previous readers of xh done
     if (status && *status != 0) return;
@@ -159,48 +160,32 @@ __global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t
     const int sh = guard_shift(m);
     const float sc = pow2f(sh);
     uint4* dst = reinterpret_cast<uint4*>(xh + row * K);
-    if (stream_order) {
-        for (int64_t blk = threadIdx.x; blk < K / 32; blk += 256) {
-            float v[32];
+    for (int64_t blk = threadIdx.x; blk < K / 32; blk += 256) {
+        float v[32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 u = src[4 * blk + q];
-                const T* e = reinterpret_cast<const T*>(&u);
+        for (int q = 0; q < 4; ++q) {
+            uint4 u = src[4 * blk + q];
+            const T* e = reinterpret_cast<const T*>(&u);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) v[8 * q + j] = to_f32<T>(e[j]) * sc;
-            }
-            store_block_stream_order(v, dst + 4 * blk);
+            for (int j = 0; j < 8; ++j) v[8 * q + j] = to_f32<T>(e[j]) * sc;
         }
-    } else {
-        for (int64_t i = threadIdx.x; i < n8; i += 256) {
-            uint4 v = src[i];
-            const T* e = reinterpret_cast<const T*>(&v);
-            uint4 o;
-            __half2* oh = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                oh[j] = __halves2half2(__float2half_rn(to_f32<T>(e[2 * j]) * sc),
-                                       __float2half_rn(to_f32<T>(e[2 * j + 1]) * sc));
-            dst[i] = o;
-        }
+        store_block_stream_order(v, dst + 4 * blk);
     }
     if (threadIdx.x == 0) rsx[row] = pow2f(-sh);
 }
 
-cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, int stream_order,
-                          cudaStream_t s) {
-    return launch_x_half_gather(x, xt, T, K, xh, rsx, nullptr, 1, nullptr, stream_order, s);
+cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s) {
+    return launch_x_half_gather(x, xt, T, K, xh, rsx, nullptr, 1, nullptr, s);
 }
 
 cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K, uint16_t* xh, float* rsx,
-                                 const int32_t* gather, int per, const int32_t* status, int stream_order,
-                                 cudaStream_t s) {
+                                 const int32_t* gather, int per, const int32_t* status, cudaStream_t s) {
     if (xt == CQ_BF16)
         return launch_pdl(k_x_half<__nv_bfloat16>, dim3((unsigned)rows), dim3(256), 0, s,
                           reinterpret_cast<const __nv_bfloat16*>(x), K, reinterpret_cast<__half*>(xh), rsx, gather, per,
-                          status, stream_order);
+                          status);
     return launch_pdl(k_x_half<__half>, dim3((unsigned)rows), dim3(256), 0, s, reinterpret_cast<const __half*>(x), K,
-                      reinterpret_cast<__half*>(xh), rsx, gather, per, status, stream_order);
+                      reinterpret_cast<__half*>(xh), rsx, gather, per, status);
 }
 
 // ---- MoE routing layout -------------------------------------------------

@@ -2,26 +2,35 @@
 // tensor memory), weights dequantized on the fly in shared memory.
 //
 // Y^T tile = W tile (128 weight rows, M) x X tile^T (BN activation rows, N),
-// K in stages of 64.  Warp roles in a CTA of 192 threads:
-//   warp 4      TMA producer: raw weight tile (Q4 nibbles 128 x 32 B or Q8
-//               bytes 128 x 64 B, swizzled so the decode reads are
-//               bank-conflict free) and the activation tile (BN x 64 fp16 /
-//               bf16, 128-byte swizzle = the MMA's K-major operand layout);
-//   warps 0-3   decoders, one thread per weight row: raw row -> 64 fp16/bf16
-//               values written into the A operand tile in the 128-byte
-//               swizzled K-major layout, then the epilogue;
-//   warp 5      allocates the tensor memory and issues tcgen05.mma
+// K in stages of 64, loaded in super-stages of G stages (one weight box of
+// G * 32 or G * 64 bytes per row and one activation box of G 64-k chunks:
+// a TMA box costs nearly the same whatever its size, so fewer, larger boxes
+// keep the copies ahead of the tensor core).  Warp roles in a CTA of 576
+// threads:
+//   warp 16     TMA producers: lane s issues the weight box of super-slot s,
+//               lane LSS + s its activation box;
+//   warps 0-15  decoders: group w / 4 takes every fourth stage, warp w
+//               rows 32 (w % 4) .. +31 of it (one 64-k row per thread),
+//               decoded into the A operand (tensor memory by default, else
+//               the 128-byte swizzled K-major tile in shared memory); four
+//               stages are in decode at once.  Then the epilogue;
+//   warp 17     allocates the tensor memory and issues tcgen05.mma
 //               (M = 128, N = BN, K = 16) from one thread, committing each
-//               stage back to the producer and the last to the epilogue.
+//               stage's decoded slot and each super-stage's load slot back,
+//               and the last stage to the epilogue.
 // Q4 decode: (nibble - 8) * fp16 block scale, rounded once to fp16 (the
 // scale folded into the half operand, as in mma_tile of "oxinfer 0.0.5
 // src/metal.rs"); the activations arrive as fp16 behind a per-row
-// power-of-two guard whose inverse the epilogue applies.  Q8-row decode:
+// power-of-two guard whose inverse the epilogue applies, stored by the
+// guard pass in the streaming order inside each 32-k block, the order in
+// which two masks per word yield the nibble pairs; the decoded weights are
+// written in that same order, so the contraction is unchanged.  Q8-row decode:
 // int8 -> the activation type exactly; the row scale is applied to the f32
 // accumulator in the epilogue ("cortiq-engine 0.8.3 src/gpu_metal/qi21.rs",
 // module header on q8_row).
 // Every wait is time-bounded; on a timeout the CTA stops, lets copies in
 // flight land, frees its tensor memory and reports CQ_ERR_TIMEOUT.
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -62,16 +71,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
     return r;
 }
-__device__ __forceinline__ uint32_t nib2_to_h2(uint32_t v) {
-    const uint32_t h = (v & 0x000F000Fu) | 0x64006400u;
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h),
-                              __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
-    return *reinterpret_cast<const uint32_t*>(&r);
-}
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
-    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), s);
-    return *reinterpret_cast<const uint32_t*>(&r);
-}
 __device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t w, uint32_t sel) {
     const uint32_t h = prmt(w ^ 0x80808080u, 0x64646464u, sel);
     const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h),
@@ -87,27 +86,62 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+// Eight nibbles (bytes b0..b3 of w) -> four fp16 pairs (n - 8) * scale, each
+// rounded once, in the activations' streaming order: (low b0, low b2),
+// (high b0, high b2), (low b1, low b3), (high b1, high b3).  0x6400 | n is
+// 1024 + n and 0x6400 | (n << 4) is 1024 + 16 n; 1024 + n - 1032 and
+// (1024 + 16 n) / 16 - 72 are n - 8 exactly.
+__device__ __forceinline__ void decode_q4_word_scaled(uint32_t w, __half2 sc, uint32_t* o) {
+    const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+    const __half2 km72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));
+    const uint32_t w8 = w >> 8;
+    const uint32_t l02 = (w & 0x000F000Fu) | 0x64006400u, h02 = (w & 0x00F000F0u) | 0x64006400u;
+    const uint32_t l13 = (w8 & 0x000F000Fu) | 0x64006400u, h13 = (w8 & 0x00F000F0u) | 0x64006400u;
+    const __half2 d0 = __hsub2(*reinterpret_cast<const __half2*>(&l02), k1032);
+    const __half2 d1 = __hfma2(*reinterpret_cast<const __half2*>(&h02), k16th, km72);
+    const __half2 d2 = __hsub2(*reinterpret_cast<const __half2*>(&l13), k1032);
+    const __half2 d3 = __hfma2(*reinterpret_cast<const __half2*>(&h13), k16th, km72);
+    const __half2 r0 = __hmul2(d0, sc), r1 = __hmul2(d1, sc), r2 = __hmul2(d2, sc), r3 = __hmul2(d3, sc);
+    o[0] = *reinterpret_cast<const uint32_t*>(&r0);
+    o[1] = *reinterpret_cast<const uint32_t*>(&r1);
+    o[2] = *reinterpret_cast<const uint32_t*>(&r2);
+    o[3] = *reinterpret_cast<const uint32_t*>(&r3);
+}
+
 template <int FMT>
 struct Raw;
 template <>
-struct Raw<0> { static constexpr int ROW = 32; };   // Q4: 64 k = 32 bytes per row
+struct Raw<0> { static constexpr int ROW = 32; };   // Q4: 64 k = 32 bytes per row and stage
 template <>
-struct Raw<1> { static constexpr int ROW = 64; };   // Q8: 64 bytes per row
+struct Raw<1> { static constexpr int ROW = 64; };   // Q8: 64 bytes per row and stage
 
-// Shared memory: a load ring of LS stages (raw weight tile + activation
-// tile, filled by TMA) and (AM 0) a shorter ring of AS decoded weight tiles;
-// with AM 1 the decoded tiles are AS == LS slots of tensor memory.
-template <int FMT, int BN, int LS, int AS, int AM>
+// Loads come in super-stages of G stages (G x 64 k), two TMA boxes each: a TMA
+// box costs about the same however few bytes it holds, so the weight rows are
+// fetched G stages at a time (G * ROW bytes per row) and the activation tile as
+// one 3-D box of G 64-k chunks.
+// Shared memory per super-slot: X [G][BN rows][128 B] (each chunk one
+// 128-byte-swizzled K-major operand tile), then W [128 rows][G * ROW B]
+// (128- or 64-byte swizzle).  AM 0 adds AS decoded tiles [128][128 B] in
+// front; AM 1 keeps the decoded tiles in tensor memory.
+template <int FMT, int BN, int G, int LSS, int AS, int AM>
 struct Layout {
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int R_BYTES = BM * Raw<FMT>::ROW;
-    static constexpr int R_STRIDE = (R_BYTES + 1023) / 1024 * 1024;
+    static constexpr int WROW = G * Raw<FMT>::ROW;            // 64 or 128 bytes
+    static constexpr int X_CHUNK = BN * 128;
+    static constexpr int X_BYTES = G * X_CHUNK;
+    static constexpr int W_BYTES = BM * WROW;
+    static constexpr int SLOT = X_BYTES + W_BYTES;             // multiple of 1024
     static constexpr int A_OFF = 0;
-    static constexpr int B_OFF = A_OFF + (AM == 0 ? AS * A_BYTES : 0);   // AM 1: decoded tiles in TMEM
-    static constexpr int R_OFF = B_OFF + LS * B_BYTES;
-    static constexpr int BAR_OFF = R_OFF + LS * R_STRIDE;
-    // full[LS], empty[LS], afull[AS], aempty[AS], accf; then tmem slot, abort, never
-    static constexpr int NBAR = 2 * LS + 2 * AS + 1;
+    static constexpr int S_OFF = AM == 0 ? AS * A_BYTES : 0;
+    static constexpr int BAR_OFF = S_OFF + LSS * SLOT;
+    // full[LSS], empty[LSS], afull[AS], aempty[AS / 2] (one per pair of decoded slots), accf;
+    // then tmem slot, abort, never
+    static constexpr int NBAR = 2 * LSS + AS + AS / 2 + 1;
     static constexpr int MISC = NBAR * 8 + 16;
     static constexpr int TOTAL = BAR_OFF + MISC + 1024;  // + alignment slack
     // tensor memory: accumulator in columns [0, BN); AM 1 adds AS decoded A tiles of 32 columns
@@ -115,26 +149,30 @@ struct Layout {
     static constexpr int NEED = AM == 0 ? BN : BN + AS * 32;
     static constexpr int TMEM_COLS = NEED <= 32 ? 32 : NEED <= 64 ? 64 : NEED <= 128 ? 128 : NEED <= 256 ? 256 : 512;
     static_assert(NEED <= 512, "tensor memory budget");
+    static_assert(SLOT % 1024 == 0 && X_CHUNK % 1024 == 0, "1024-byte aligned swizzled tiles");
+    static_assert(WROW == 32 || WROW == 64 || WROW == 128, "weight rows of 32, 64 or 128 bytes");
 };
 
-constexpr int DEC_WARPS = 8;                 // two decoder threads per weight row
+constexpr int DEC_WARPS = 16;                // 4 groups (stages kb % 4) x 4 row quarters
 constexpr int THREADS = (DEC_WARPS + 2) * 32;
 constexpr int PRODUCER_WARP = DEC_WARPS;
 constexpr int MMA_WARP = DEC_WARPS + 1;
 
-// int8 byte i of w -> f32 exactly: 0x4B0000uu is 2^23 + u with u = v + 128.
-__device__ __forceinline__ float i8_to_f32(uint32_t wx /* w ^ 0x80808080 */, uint32_t sel) {
-    return __uint_as_float(prmt(wx, 0x4B000000u, sel)) - 8388736.0f;
-}
-__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
-    const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+// int8 pair (bytes sel of w) -> bf16x2 exactly: with 0x43 as the high byte, the
+// low seven bits of v give 128 + (v & 127) and the sign bit gives 128 or 256
+// (0x4300 / 0x4380); their difference is v, an integer bf16 holds exactly.
+__device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
+    const uint32_t t = prmt(w, 0x43434343u, sel);
+    const uint32_t lo = t & 0xFF7FFF7Fu, hi = t & 0xFF80FF80u;
+    const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&lo),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&hi));
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <int FMT, int BN, int XBF, int LS, int AS, int CL, int AM>
+template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM>
 __global__ void __launch_bounds__(THREADS, 1)
 k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const Params p) {
-    using L = Layout<FMT, BN, LS, AS, AM>;
+    using L = Layout<FMT, BN, G, LSS, AS, AM>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
@@ -142,28 +180,28 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BM;          // first weight row
     const int t0 = blockIdx.y * BN;          // first activation row
-    const int nk = (int)(p.K / BK);
+    const int nk = (int)(p.K / BK);          // stages
+    const int ns = nk / G;                   // super-stages
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (LS + s); };
-    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * LS + a); };
-    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * LS + AS + a); };
-    const uint32_t accf_bar = bar0 + 8u * (2 * LS + 2 * AS);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (LSS + s); };
+    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * LSS + a); };
+    auto aempty_bar = [&](int pr) { return bar0 + 8u * (2 * LSS + AS + pr); };   // decoded slots 2pr, 2pr + 1
+    const uint32_t accf_bar = bar0 + 8u * (2 * LSS + AS + AS / 2);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never_flag = abort_flag + 1;
+    auto slot_base = [&](int s) { return sb + (uint32_t)(L::S_OFF + s * L::SLOT); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < LS; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), CL);   // a slot is free once every CTA of the cluster has consumed it
+        for (int s = 0; s < LSS; ++s) {
+            mbar_init(full_bar(s), 1);   // the weight lane's arrival + both boxes' bytes
+            mbar_init(empty_bar(s), 1);  // the MMA's commit after the super-stage's last stage
         }
-        for (int a = 0; a < AS; ++a) {
-            mbar_init(afull_bar(a), DEC_WARPS * 32);
-            mbar_init(aempty_bar(a), 1);
-        }
+        for (int a = 0; a < AS; ++a) mbar_init(afull_bar(a), 4);       // one arrival per warp of the decoding group
+        for (int pr = 0; pr < AS / 2; ++pr) mbar_init(aempty_bar(pr), 1);  // the MMA's commit of the stage pair
         mbar_init(accf_bar, 1);
         *abort_flag = 0;
         *never_flag = 0;
@@ -177,12 +215,6 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // cluster of CL CTAs along the weight rows: CTA `rank` loads rows
-    // [rank*BN/CL, (rank+1)*BN/CL) of each activation tile and multicasts them
-    constexpr int XS = BN / CL;
-    constexpr uint16_t CMASK = (uint16_t)((1u << CL) - 1u);
-    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
-    if (CL > 1) cluster_sync_all();   // every CTA's barriers are initialised before any multicast
 
     auto give_up = [&]() {
         *abort_flag = 1;
@@ -191,215 +223,232 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
 
     if (warp == PRODUCER_WARP) {
         // ================= TMA producers =================
-        // Lane s owns ring slot s and issues that slot's copies: one thread keeps only a
-        // few bulk copies outstanding, so the ring is filled from LS threads.
-        if (lane < LS) {
+        // Lane s < LSS issues the weight box of super-slot s (and posts the bytes of
+        // both boxes), lane LSS + s its activation box: a thread keeps only a few bulk
+        // copies in flight, so the boxes come from 2 LSS threads.
+        const int s = lane % LSS;
+        const bool wl = lane < LSS, xl = lane >= LSS && lane < 2 * LSS;
+        if (wl || xl) {
             if (lane == 0) {
                 tma_prefetch_desc(&tmW);
                 tma_prefetch_desc(&tmX);
             }
-            const int s = lane;
-            int issued = 0;        // stages issued by this lane
-            auto load_x = [&](int kb) {
-                const uint32_t dst = sb + L::B_OFF + s * L::B_BYTES + rank * (XS * 128);
-                if (CL == 1) tma_load_2d(dst, &tmX, full_bar(s), kb * BK, t0);
-                else tma_load_2d_mc(dst, &tmX, full_bar(s), kb * BK, t0 + (int)rank * XS, CMASK);
+            const uint32_t base = slot_base(s);
+            int issued = 0;        // super-stages issued by this lane
+            auto issue = [&](int j) {
+                if (wl) {
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::X_BYTES + L::W_BYTES));
+                    tma_load_2d(base + L::X_BYTES, &tmW, full_bar(s), j * L::WROW, m0);
+                } else {
+                    tma_load_3d(base, &tmX, full_bar(s), 0, t0, j * G);
+                }
             };
             if (!p.stall) {
-                // With a programmatic dependency, the raw weights of the first ring fill are
-                // requested before waiting for the guarded activations.
-                const bool pre = p.pdl && s < nk;
-                if (pre) {
-                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::R_BYTES + L::B_BYTES));
-                    tma_load_2d(sb + L::R_OFF + s * L::R_STRIDE, &tmW, full_bar(s), s * Raw<FMT>::ROW, m0);
-                }
+                // With a programmatic dependency the weights of the first ring fill are
+                // requested before waiting for the previous kernel (the guard pass);
+                // the activations only after it.
+                const bool pre = s < ns;
+                if (pre && wl) issue(s);
                 pdl_wait();
                 if (pre) {
-                    load_x(s);
+                    if (xl) issue(s);
                     ++issued;
                 }
-                for (int kb = s + (pre ? LS : 0); kb < nk; kb += LS) {
-                    if (!mbar_wait(empty_bar(s), (uint32_t)(((kb / LS) & 1) ^ 1), p.wait_ns, abort_flag)) {
+                uint32_t ph = pre ? 1u : 0u;     // phase of this slot's round for super-stage j
+                for (int j = s + (pre ? LSS : 0); j < ns; j += LSS, ph ^= 1u) {
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, p.wait_ns, abort_flag)) {
                         give_up();
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::R_BYTES + L::B_BYTES));
-                    tma_load_2d(sb + L::R_OFF + s * L::R_STRIDE, &tmW, full_bar(s), kb * Raw<FMT>::ROW, m0);
-                    load_x(kb);
+                    issue(j);
                     ++issued;
                 }
             } else {
                 pdl_wait();   // every path waits once, so kernels later in the stream stay ordered
             }
             if (*abort_flag && issued > 0) {
-                // this lane's last copy must land before the CTA can exit
-                const int kb_last = s + (issued - 1) * LS;
-                mbar_wait(full_bar(s), (uint32_t)((kb_last / LS) & 1), p.wait_ns, never_flag);
+                // this lane's last copy must land before the CTA can exit (round issued - 1)
+                mbar_wait(full_bar(s), (uint32_t)((issued - 1) & 1), p.wait_ns, never_flag);
             }
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ================= MMA issuer =================
-        // The whole warp runs the loop (converged); one lane issues the tensor-core work.
-        // With the decoded tiles in tensor memory (AM 1) there is one decoded slot per load
-        // slot, so one commit frees both and the only wait is the decoders' hand-off.
-        constexpr uint32_t idesc = idesc_f16(BM, BN, XBF);
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % LS, a = kb % AS;
-            bool ok = mbar_wait(afull_bar(a), (uint32_t)((kb / AS) & 1), p.wait_ns, abort_flag);
-            if (AM == 0 && ok) ok = mbar_wait(full_bar(s), (uint32_t)((kb / LS) & 1), p.wait_ns, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0) give_up();
-                break;
-            }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t a_base = sb + L::A_OFF + a * A_BYTES;
-                const uint32_t b_base = sb + L::B_OFF + s * L::B_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    if (AM == 0)
-                        tc_mma_f16(tmem, smem_desc_sw128(a_base + 32 * kk), smem_desc_sw128(b_base + 32 * kk),
-                                   idesc, (kb | kk) != 0 ? 1u : 0u);
-                    else   // A from tensor memory: 8 columns per K=16 step
-                        tc_mma_f16_ts(tmem, tmem + (uint32_t)(L::A_COL + a * 32 + kk * 8),
-                                      smem_desc_sw128(b_base + 32 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
+        // One thread issues the tensor-core work, two stages per round: wait for both
+        // decoded slots (their groups had waited for the super-slot, so the activations are
+        // in too), eight MMAs, one commit that frees the pair of decoded slots and, at the end
+        // of a super-stage, one that frees the super-slot.  Descriptors advance by adding.
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(BM, BN, XBF);
+            int a = 0, s = 0, u = 0;          // decoded slot, super-slot and chunk of stage kb
+            uint32_t aph = 0;
+            for (int kb = 0; kb < nk; kb += 2) {
+                if (!mbar_wait(afull_bar(a), aph, p.wait_ns, abort_flag) ||
+                    !mbar_wait(afull_bar(a + 1), aph, p.wait_ns, abort_flag)) {
+                    give_up();
+                    break;
                 }
-                // raw + activation slot (and, AM 1, its decoded tile) free once these MMAs are
-                // done, in every CTA of the cluster, since the peers multicast into this slot too
-                if (CL == 1) tc_commit(empty_bar(s));
-                else tc_commit_mc(empty_bar(s), CMASK);
-                if (AM == 0) tc_commit(aempty_bar(a));   // decoded slot free
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint64_t bd = smem_desc_sw128(slot_base(s) + (uint32_t)(u * L::X_CHUNK));
+                    const uint64_t ad = AM == 0 ? smem_desc_sw128(sb + L::A_OFF + (a + h) * A_BYTES) : 0;
+                    const uint32_t at = tmem + (uint32_t)(L::A_COL + (a + h) * 32);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint32_t acc = (kb + h + kk) != 0 ? 1u : 0u;
+                        // +32 bytes of K = +2 in the descriptor's 16-byte address units
+                        if (AM == 0) tc_mma_f16(tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
+                        else tc_mma_f16_ts(tmem, at + 8u * kk, bd + 2u * kk, idesc, acc);
+                    }
+                    if (++u == G) {
+                        u = 0;
+                        tc_commit(empty_bar(s));                // super-slot free after its last stage
+                        if (++s == LSS) s = 0;
+                    }
+                }
+                tc_commit(aempty_bar(a >> 1));                  // decoded slots a, a + 1 free
+                a += 2;
+                if (a == AS) { a = 0; aph ^= 1u; }
             }
-            __syncwarp();
+            tc_commit(accf_bar);   // also lets teardown know every MMA has finished
         }
-        if (lane == 0) tc_commit(accf_bar);   // also lets teardown know every MMA has finished
         __syncwarp();
     } else {
-        // ================= decoders (two threads per weight row), then epilogue =================
-        const int r = threadIdx.x & (BM - 1);      // weight row within the tile
-        const int h = threadIdx.x >> 7;            // which 32-k half of the 64-k stage
+        // ================= decoders, then epilogue =================
+        // Four groups of four warps; group g = w / 4 decodes stages g, g + 4, g + 8, ...
+        // and in each of them warp w covers rows 32 (w % 4) .. +31 (its tensor-memory lane
+        // quarter), one whole 64-k row per thread.  Four stages are decoded at once, so the
+        // per-stage chain (wait, load, decode, store, hand-off) of one warp overlaps the
+        // others' instead of setting the pace.
+        const int q4w = warp & 3, grp = warp >> 2;
+        const int r = 32 * q4w + lane;             // weight row within the tile
         const int64_t n = (int64_t)m0 + r;
         const bool row_ok = n < p.N;
-        const uint32_t a_row = (uint32_t)(r * 128);
         const uint32_t xr = (uint32_t)(r & 7);
-        // Q4 scales: 8 fp16 (4 stages x 2 blocks) per 16-byte load, one group ahead
-        uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_next = make_uint4(0, 0, 0, 0);
-        const uint16_t* srow = p.ws + n * (p.K / 32);
-        if (FMT == 0 && row_ok) sc_next = __ldg(reinterpret_cast<const uint4*>(srow));
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % LS, a = kb % AS;
-            if (FMT == 0 && (kb & 3) == 0) {
-                sc_cur = sc_next;
-                if (row_ok && kb + 4 < nk) sc_next = __ldg(reinterpret_cast<const uint4*>(srow + 2 * (kb + 4)));
-            }
-            // AM 1: decoded slot a == load slot s, free once the slot was refilled
-            if (!mbar_wait(full_bar(s), (uint32_t)((kb / LS) & 1), p.wait_ns, abort_flag) ||
-                (AM == 0 && !mbar_wait(aempty_bar(a), (uint32_t)(((kb / AS) & 1) ^ 1), p.wait_ns, abort_flag))) {
+        const uint32_t t_lane = (uint32_t)(32 * q4w) << 16;
+        // weight rows of G * ROW bytes: 128-byte swizzle (chunk c at c ^ (r % 8)), 64-byte
+        // swizzle (chunk c at c ^ ((r / 2) % 4)) or 32-byte swizzle (chunk c at c ^ ((r / 4) % 2))
+        const uint32_t wsw = L::WROW == 128 ? (uint32_t)(r & 7)
+                           : L::WROW == 64  ? (uint32_t)((r >> 1) & 3)
+                                            : (uint32_t)((r >> 2) & 1);
+        // Q4 scales of this row: the two fp16 of stage kb (blocks 2 kb, 2 kb + 1), loaded two
+        // of this group's stages ahead
+        const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.ws + n * (p.K / 32));
+        uint32_t sc0 = 0, sc1 = 0;
+        if (FMT == 0 && row_ok) {
+            if (grp < nk) sc0 = __ldg(srow + grp);
+            if (grp + 4 < nk) sc1 = __ldg(srow + grp + 4);
+        }
+        // Every group waits for every super-stage in order (decoding only its own stages
+        // in it), so each round of each super-slot is waited for in order and a parity
+        // wait never mistakes round r for round r - 2, whatever LSS is.
+        int s = 0;
+        uint32_t ph = 0;
+        bool stop = false;
+        for (int j = 0; j < ns && !stop; ++j) {
+          if (!mbar_wait(full_bar(s), ph, p.wait_ns, abort_flag)) {
+              give_up();
+              break;
+          }
+#pragma unroll
+          for (int u = 0; u < G; ++u) {
+            const int kb = j * G + u;
+            if ((kb & 3) != grp) continue;
+            const int a = kb % AS;                             // decoded slot
+            const uint32_t aph = (uint32_t)((kb / AS) & 1);
+            uint32_t sc_next = 0;
+            if (FMT == 0 && row_ok && kb + 8 < nk) sc_next = __ldg(srow + kb + 8);
+            if (!mbar_wait(aempty_bar(a >> 1), aph ^ 1u, p.wait_ns, abort_flag)) {
                 give_up();
+                stop = true;
                 break;
             }
-            const uint32_t raw = sb + L::R_OFF + s * L::R_STRIDE;
-            const uint32_t adst = sb + L::A_OFF + a * A_BYTES + a_row;
-            // this thread's 32 decoded values (k = 32h .. 32h+31 of the stage), two per word, in k order
-            uint32_t o[16];
+            const uint32_t wrow = slot_base(s) + (uint32_t)(L::X_BYTES + r * L::WROW);
+            // this thread's 64 decoded values (the whole stage for row r), two per word
+            uint32_t o[32];
             if (FMT == 0) {
-                // 32-byte rows, 32-byte swizzle: chunk j of row r sits at j ^ ((r >> 2) & 1)
-                const uint4 v = ld_shared_v4(raw + r * 32 + (((uint32_t)h ^ (uint32_t)((r >> 2) & 1)) << 4));
-                const uint32_t kq = (uint32_t)(kb & 3);
-                const uint32_t w2 = kq == 0 ? sc_cur.x : kq == 1 ? sc_cur.y : kq == 2 ? sc_cur.z : sc_cur.w;
-                const uint16_t sbits = (uint16_t)(h ? (w2 >> 16) : (w2 & 0xFFFF));
-                const __half2 sh = __halves2half2(__ushort_as_half(sbits), __ushort_as_half(sbits));
-                const uint32_t px = prmt(v.x, 0u, 0x3120u), py = prmt(v.y, 0u, 0x3120u);
-                const uint32_t pz = prmt(v.z, 0u, 0x3120u), pw = prmt(v.w, 0u, 0x3120u);
-                // elements 0-7 of the block: low nibbles of bytes 0-7
-                o[0] = hmul2_u32(nib2_to_h2(px), sh);
-                o[1] = hmul2_u32(nib2_to_h2(px >> 8), sh);
-                o[2] = hmul2_u32(nib2_to_h2(py), sh);
-                o[3] = hmul2_u32(nib2_to_h2(py >> 8), sh);
-                // elements 8-15: low nibbles of bytes 8-15
-                o[4] = hmul2_u32(nib2_to_h2(pz), sh);
-                o[5] = hmul2_u32(nib2_to_h2(pz >> 8), sh);
-                o[6] = hmul2_u32(nib2_to_h2(pw), sh);
-                o[7] = hmul2_u32(nib2_to_h2(pw >> 8), sh);
-                // elements 16-23: high nibbles of bytes 0-7
-                o[8] = hmul2_u32(nib2_to_h2(px >> 4), sh);
-                o[9] = hmul2_u32(nib2_to_h2(px >> 12), sh);
-                o[10] = hmul2_u32(nib2_to_h2(py >> 4), sh);
-                o[11] = hmul2_u32(nib2_to_h2(py >> 12), sh);
-                // elements 24-31: high nibbles of bytes 8-15
-                o[12] = hmul2_u32(nib2_to_h2(pz >> 4), sh);
-                o[13] = hmul2_u32(nib2_to_h2(pz >> 12), sh);
-                o[14] = hmul2_u32(nib2_to_h2(pw >> 4), sh);
-                o[15] = hmul2_u32(nib2_to_h2(pw >> 12), sh);
+                // stage u = chunks 2u, 2u + 1 (one 32-k block each) of the row.  Each block is
+                // decoded in the activations' streaming order (the guard pass wrote them in
+                // that order): columns 16 b .. 16 b + 15 for block b.
+                const uint4 v0 = ld_shared_v4(wrow + (((uint32_t)(2 * u) ^ wsw) << 4));
+                const uint4 v1 = ld_shared_v4(wrow + (((uint32_t)(2 * u + 1) ^ wsw) << 4));
+                const __half2 s0 = __halves2half2(__ushort_as_half((uint16_t)(sc0 & 0xFFFF)),
+                                                  __ushort_as_half((uint16_t)(sc0 & 0xFFFF)));
+                const __half2 s1 = __halves2half2(__ushort_as_half((uint16_t)(sc0 >> 16)),
+                                                  __ushort_as_half((uint16_t)(sc0 >> 16)));
+                decode_q4_word_scaled(v0.x, s0, o);
+                decode_q4_word_scaled(v0.y, s0, o + 4);
+                decode_q4_word_scaled(v0.z, s0, o + 8);
+                decode_q4_word_scaled(v0.w, s0, o + 12);
+                decode_q4_word_scaled(v1.x, s1, o + 16);
+                decode_q4_word_scaled(v1.y, s1, o + 20);
+                decode_q4_word_scaled(v1.z, s1, o + 24);
+                decode_q4_word_scaled(v1.w, s1, o + 28);
             } else {
-                // 64-byte rows, 64-byte swizzle: chunk j of row r sits at j ^ ((r >> 1) & 3)
-                const uint32_t sw = (uint32_t)((r >> 1) & 3);
+                // stage u = chunks 4u .. 4u + 3 of the row, in k order
 #pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    const uint32_t q = (uint32_t)(2 * h + qq);
-                    const uint4 v = ld_shared_v4(raw + r * 64 + ((q ^ sw) << 4));
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 v = ld_shared_v4(wrow + (((uint32_t)(4 * u + c) ^ wsw) << 4));
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         if (XBF) {
-                            const uint32_t wx = wv[i] ^ 0x80808080u;
-                            o[8 * qq + 2 * i] = pack_bf2(i8_to_f32(wx, 0x7440u), i8_to_f32(wx, 0x7441u));
-                            o[8 * qq + 2 * i + 1] = pack_bf2(i8_to_f32(wx, 0x7442u), i8_to_f32(wx, 0x7443u));
+                            o[8 * c + 2 * i] = i8x2_to_bf2(wv[i], 0x4140u);
+                            o[8 * c + 2 * i + 1] = i8x2_to_bf2(wv[i], 0x4342u);
                         } else {
-                            o[8 * qq + 2 * i] = i8x2_to_h2(wv[i], 0x4140u);
-                            o[8 * qq + 2 * i + 1] = i8x2_to_h2(wv[i], 0x4342u);
+                            o[8 * c + 2 * i] = i8x2_to_h2(wv[i], 0x4140u);
+                            o[8 * c + 2 * i + 1] = i8x2_to_h2(wv[i], 0x4342u);
                         }
                     }
                 }
             }
             if (AM == 0) {
-                // shared-memory A tile, 128-byte swizzled K-major: 16-byte chunk 4h+j of row r
+                // shared-memory A tile, 128-byte swizzled K-major: the 8 chunks of row r
+                const uint32_t adst = sb + L::A_OFF + a * A_BYTES + (uint32_t)(r * 128);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    st_shared_v4(adst + ((((uint32_t)(4 * h + j)) ^ xr) << 4), o[4 * j], o[4 * j + 1], o[4 * j + 2],
-                                 o[4 * j + 3]);
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(adst + ((((uint32_t)c) ^ xr) << 4), o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
                 fence_proxy_async_smem();
-                mbar_arrive(afull_bar(a));
             } else {
-                // tensor-memory A tile: lane r, columns A_COL + 32a + 16h .. +15.  The store
-                // of this stage is handed to the MMA one stage later, so its latency overlaps
-                // the next stage's wait and decode.
-                if (kb > 0) {
-                    tmem_st_wait();
-                    tc_fence_before();
-                    mbar_arrive(afull_bar((kb - 1) % AS));
-                }
-                tmem_st_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(L::A_COL + a * 32 + 16 * h), o);
-                if (kb + 1 == nk) {
-                    tmem_st_wait();
-                    tc_fence_before();
-                    mbar_arrive(afull_bar(a));
-                }
+                // tensor-memory A tile: lane r, columns A_COL + 32 a .. +31
+                tmem_st_32x32b_x32(tmem + t_lane + (uint32_t)(L::A_COL + a * 32), o);
+                tmem_st_wait();
+                tc_fence_before();
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull_bar(a));
+            sc0 = sc1;
+            sc1 = sc_next;
+          }
+          if (++s == LSS) {
+              s = 0;
+              ph ^= 1u;
+          }
         }
 
         // ---- epilogue: TMEM -> registers -> scale -> Y[t][n] ----
-        // warp w reads TMEM lanes 32*(w % 4).. and the columns of half w / 4
+        // warp w reads TMEM lanes 32 (w % 4).. and the accumulator columns
+        // [g BN/4, (g + 1) BN/4) of its group g = w / 4, 16 at a time
         if (!*abort_flag && mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) {
             tc_fence_after();
             pdl_wait();   // outputs and guard scales only after the previous kernel has finished
             const float rsn = (FMT == 1 && row_ok) ? p.rs[n] : 0.f;
-            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            constexpr int CW = BN / 4;
 #pragma unroll 1
-            for (int cc = h * (BN / 64); cc < (h + 1) * (BN / 64); ++cc) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(cc * 32), v);
+            for (int cc = grp * CW; cc < (grp + 1) * CW; cc += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)cc, v);
                 tmem_ld_wait();
-                const int64_t tb = (int64_t)t0 + cc * 32;
+                const int64_t tb = (int64_t)t0 + cc;
                 float rsx_l = 0.f;
-                if (FMT == 0 && tb + lane < p.T) rsx_l = p.rsx[tb + lane];
+                if (FMT == 0 && lane < 16 && tb + lane < p.T) rsx_l = p.rsx[tb + lane];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, rsx_l, j) : rsn;
-                    const int64_t t = tb + j;
+                for (int jj = 0; jj < 16; ++jj) {
+                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, rsx_l, jj) : rsn;
+                    const int64_t t = tb + jj;
                     if (row_ok && t < p.T) {
-                        const float val = __uint_as_float(v[j]) * sx;
+                        const float val = __uint_as_float(v[jj]) * sx;
                         if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = val;
                         else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(val);
                     }
@@ -419,17 +468,39 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         tc_fence_after();
         tmem_dealloc(tmem, L::TMEM_COLS);
     }
-    // no CTA leaves while a peer may still multicast into it or signal its barriers
-    if (CL > 1) cluster_sync_all();
 }
 
-template <int FMT, int BN, int XBF, int LS, int AS, int CL, int AM>
-cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, const Params& p, dim3 grid, cudaStream_t s) {
-    using L = Layout<FMT, BN, LS, AS, AM>;
+template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM>
+cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t s) {
+    using L = Layout<FMT, BN, G, LSS, AS, AM>;
     static_assert(L::TOTAL <= 232448, "shared memory budget");
-    static_assert(LS <= 32, "one producer lane per ring slot");
-    static_assert(AM == 0 || AS == LS, "tensor-memory decoded slots pair with load slots");
-    auto kern = k_tc<FMT, BN, XBF, LS, AS, CL, AM>;
+    static_assert(2 * LSS <= 32, "two producer lanes per super-slot");
+    // Group g decodes the stages kb % 4 == g: with AS a multiple of 4 each decoded slot
+    // (and pair of slots) belongs to fixed groups that wait for its rounds in order.
+    static_assert(AS % 4 == 0 && (G == 1 || G == 2 || G == 4), "decoded slots owned by fixed decoder groups");
+    // weights: rows of G stages (G * ROW bytes) per box
+    CUtensorMap mw, mx;
+    {
+        const uint64_t kbytes = FMT == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+        uint64_t d[2] = {kbytes, (uint64_t)a.N};
+        uint64_t st[1] = {kbytes};
+        uint32_t box[2] = {(uint32_t)L::WROW, (uint32_t)BM};
+        if (!encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.wq, d, st, box,
+                          L::WROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : L::WROW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B))
+            return cudaErrorInvalidValue;
+    }
+    // activations seen as {64 elements, T rows, K/64 chunks} (strides K*2 B, 128 B): one
+    // box of G chunks of BN rows lands as [chunk][row][128 B], G operand tiles
+    {
+        uint64_t d[3] = {64, (uint64_t)a.T, (uint64_t)a.K / 64};
+        uint64_t st[2] = {(uint64_t)a.K * 2, 128};
+        uint32_t box[3] = {64, (uint32_t)BN, (uint32_t)G};
+        if (!encode_tiled(&mx, XBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, d,
+                          st, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    auto kern = k_tc<FMT, BN, XBF, G, LSS, AS, AM>;
     static int configured_device = -1;       // attributes are per device; set once per instantiation
     int dev = 0;
     cudaGetDevice(&dev);
@@ -443,20 +514,11 @@ cudaError_t launch_bn(const CUtensorMap& mw, const CUtensorMap& mx, const Params
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = L::TOTAL;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = CL;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-    if (p.pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = na;
+    cfg.numAttrs = p.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, mw, mx, p);
 }
 
@@ -465,33 +527,21 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     const int64_t mt = (a.N + BM - 1) / BM;
     int bn = (int)options().tc_bn;
     if (bn != 64 && bn != 128 && bn != 256) {
-        bn = 256;
-        if (mt * ((a.T + 255) / 256) < num_sms()) bn = 128;
-        if (bn == 128 && mt * ((a.T + 127) / 128) < num_sms() && a.T <= 64) bn = 64;
-    }
-    // cluster size along the weight rows (the activation tile is multicast)
-    int cl = (int)options().tc_cluster;
-    if (cl != 1 && cl != 2 && cl != 4) {
-        const int64_t ctas = mt * ((a.T + bn - 1) / bn);
-        cl = (mt >= 4 && ctas <= 128) ? 4 : (mt >= 2 ? 2 : 1);
-    }
-    CUtensorMap mw, mx;
-    {
-        const uint64_t kbytes = fmt == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
-        uint64_t d[2] = {kbytes, (uint64_t)a.N};
-        uint64_t st[1] = {kbytes};
-        uint32_t box[2] = {(uint32_t)(fmt == 0 ? 32 : 64), (uint32_t)BM};
-        if (!encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.wq, d, st, box,
-                          fmt == 0 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
-            return cudaErrorInvalidValue;
-    }
-    {
-        uint64_t d[2] = {(uint64_t)a.K, (uint64_t)a.T};
-        uint64_t st[1] = {(uint64_t)a.K * 2};
-        uint32_t box[2] = {(uint32_t)BK, (uint32_t)(bn / cl)};
-        if (!encode_tiled(&mx, xbf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x, d,
-                          st, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
+        // One CTA per SM; a CTA's time per 64-k stage is about max(decode and loads, MMA):
+        // the former does not depend on BN, the MMA grows with BN (about 320 cycles at
+        // BN = 128 on one SM).  Pick the width with the least waves x per-CTA time (ties:
+        // the wider tile, which decodes each weight fewer times).
+        const double dec = 450.0;
+        double best = 0.0;
+        for (int cand : {256, 128, 64}) {
+            const int64_t ctas = mt * ((a.T + cand - 1) / cand);
+            const int64_t waves = (ctas + num_sms() - 1) / num_sms();
+            const double cost = (double)waves * std::max(dec, 320.0 * cand / 128.0);
+            if (best == 0.0 || cost < best - 1e-9) {
+                best = cost;
+                bn = cand;
+            }
+        }
     }
     Params p = {};
     p.rsx = a.rsx;
@@ -505,51 +555,43 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     p.wait_ns = (uint64_t)options().wait_ns;
     p.stall = (int)options().test_stall;
     options().test_stall = 0;
-    p.pdl = fmt == 0 ? 1 : 0;     // Q4: the guard pass just before touches neither weights nor Y
-    // grid x padded to whole clusters: extra CTAs see only zero-filled weight rows and store nothing
-    const int64_t gx = (mt + cl - 1) / cl * cl;
-    dim3 grid((unsigned)gx, (unsigned)((a.T + bn - 1) / bn), 1);
+    p.pdl = 1;   // the guard pass (Q4) or the previous kernel touches neither the weights nor anything before the wait
+    dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), 1);
     if (options().trace)
-        fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d cluster=%d grid=(%u,%u)\n", fmt,
-                (long long)a.T, (long long)a.N, (long long)a.K, bn, cl, grid.x, grid.y);
+        fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d grid=(%u,%u)\n", fmt, (long long)a.T,
+                (long long)a.N, (long long)a.K, bn, grid.x, grid.y);
     // decoded weight operand: 1 = shared memory, 2 = tensor memory (default)
     const int am = options().tc_amode == 1 ? 0 : 1;
-#define CQ_TC_CL(F, B, X, LSv, ASv, AMv)                                                  \
-    do {                                                                                  \
-        if (cl == 4) return launch_bn<F, B, X, LSv, ASv, 4, AMv>(mw, mx, p, grid, s);      \
-        if (cl == 2) return launch_bn<F, B, X, LSv, ASv, 2, AMv>(mw, mx, p, grid, s);      \
-        return launch_bn<F, B, X, LSv, ASv, 1, AMv>(mw, mx, p, grid, s);                  \
-    } while (0)
+    // <FMT, BN, XBF, G, LSS, AS, AM>: super-stages of G stages (weight rows of 64 or 128
+    // bytes per box), as many super-slots as fit next to the decoded slots
     if (am == 0) {
         if (fmt == 0) {
-            if (bn == 256) CQ_TC_CL(0, 256, 0, 5, 2, 0);
-            if (bn == 128) CQ_TC_CL(0, 128, 0, 8, 3, 0);
-            CQ_TC_CL(0, 64, 0, 12, 4, 0);
+            if (bn == 256) return launch_bn<0, 256, 0, 2, 2, 4, 0>(a, p, grid, s);
+            if (bn == 128) return launch_bn<0, 128, 0, 2, 4, 4, 0>(a, p, grid, s);
+            return launch_bn<0, 64, 0, 4, 3, 4, 0>(a, p, grid, s);
         }
         if (xbf) {
-            if (bn == 256) CQ_TC_CL(1, 256, 1, 4, 3, 0);
-            if (bn == 128) CQ_TC_CL(1, 128, 1, 7, 3, 0);
-            CQ_TC_CL(1, 64, 1, 10, 4, 0);
+            if (bn == 256) return launch_bn<1, 256, 1, 2, 2, 4, 0>(a, p, grid, s);
+            if (bn == 128) return launch_bn<1, 128, 1, 2, 3, 4, 0>(a, p, grid, s);
+            return launch_bn<1, 64, 1, 2, 4, 4, 0>(a, p, grid, s);
         }
-        if (bn == 256) CQ_TC_CL(1, 256, 0, 4, 3, 0);
-        if (bn == 128) CQ_TC_CL(1, 128, 0, 7, 3, 0);
-        CQ_TC_CL(1, 64, 0, 10, 4, 0);
+        if (bn == 256) return launch_bn<1, 256, 0, 2, 2, 4, 0>(a, p, grid, s);
+        if (bn == 128) return launch_bn<1, 128, 0, 2, 3, 4, 0>(a, p, grid, s);
+        return launch_bn<1, 64, 0, 2, 4, 4, 0>(a, p, grid, s);
     }
-    // AM 1: one tensor-memory decoded slot per load slot (AS == LS)
     if (fmt == 0) {
-        if (bn == 256) CQ_TC_CL(0, 256, 0, 6, 6, 1);
-        if (bn == 128) CQ_TC_CL(0, 128, 0, 10, 10, 1);
-        CQ_TC_CL(0, 64, 0, 14, 14, 1);
+        if (bn == 256) return launch_bn<0, 256, 0, 2, 3, 8, 1>(a, p, grid, s);
+        if (bn == 128) return launch_bn<0, 128, 0, 2, 5, 8, 1>(a, p, grid, s);
+        return launch_bn<0, 64, 0, 4, 4, 8, 1>(a, p, grid, s);
     }
     if (xbf) {
-        if (bn == 256) CQ_TC_CL(1, 256, 1, 5, 5, 1);
-        if (bn == 128) CQ_TC_CL(1, 128, 1, 9, 9, 1);
-        CQ_TC_CL(1, 64, 1, 13, 13, 1);
+        if (bn == 256) return launch_bn<1, 256, 1, 1, 5, 8, 1>(a, p, grid, s);
+        if (bn == 128) return launch_bn<1, 128, 1, 2, 4, 8, 1>(a, p, grid, s);
+        return launch_bn<1, 64, 1, 2, 6, 8, 1>(a, p, grid, s);
     }
-    if (bn == 256) CQ_TC_CL(1, 256, 0, 5, 5, 1);
-    if (bn == 128) CQ_TC_CL(1, 128, 0, 9, 9, 1);
-    CQ_TC_CL(1, 64, 0, 13, 13, 1);
-#undef CQ_TC_CL
+    if (bn == 256) return launch_bn<1, 256, 0, 1, 5, 8, 1>(a, p, grid, s);
+    if (bn == 128) return launch_bn<1, 128, 0, 2, 4, 8, 1>(a, p, grid, s);
+    return launch_bn<1, 64, 0, 2, 6, 8, 1>(a, p, grid, s);
 }
 
 }  // namespace
