@@ -169,9 +169,9 @@ cq_status cq_set_option(int option, int64_t value) {
             if (value != 0 && value != 64 && value != 128 && value != 256) return fail(CQ_ERR_ARG, "token tile must be 0, 64, 128 or 256");
             o.tc_bn = value;
             return CQ_OK;
-        case CQ_OPT_TC_CLUSTER:
-            if (value != 0 && value != 1 && value != 2 && value != 4) return fail(CQ_ERR_ARG, "cluster size must be 0, 1, 2 or 4");
-            o.tc_cluster = value;
+        case CQ_OPT_TC_KSPLIT:
+            if (value != 0 && value != 1 && value != 2) return fail(CQ_ERR_ARG, "K split must be 0, 1 or 2");
+            o.tc_ksplit = value;
             return CQ_OK;
         case CQ_OPT_TC_AMODE:
             if (value < 0 || value > 2) return fail(CQ_ERR_ARG, "operand mode must be 0, 1 or 2");
@@ -191,7 +191,7 @@ int64_t cq_get_option(int option) {
         case CQ_OPT_TEST_STALL: return o.test_stall;
         case CQ_OPT_TRACE: return o.trace;
         case CQ_OPT_TC_BN: return o.tc_bn;
-        case CQ_OPT_TC_CLUSTER: return o.tc_cluster;
+        case CQ_OPT_TC_KSPLIT: return o.tc_ksplit;
         case CQ_OPT_TC_AMODE: return o.tc_amode;
         default: return -1;
     }

@@ -20,7 +20,7 @@ struct Options {
     int64_t test_stall = 0;
     int64_t trace = 0;
     int64_t tc_bn = 0;
-    int64_t tc_cluster = 0;
+    int64_t tc_ksplit = 0;
     int64_t tc_amode = 0;
 };
 Options& options();

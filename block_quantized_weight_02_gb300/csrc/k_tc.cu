@@ -169,7 +169,10 @@ __device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM>
+// KS: K split over a cluster of KS CTAs along z (1 or 2); the two partial
+// accumulators are exchanged through distributed shared memory and each CTA
+// finishes half of the tile's columns.
+template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS>
 __global__ void __launch_bounds__(THREADS, 1)
 k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const Params p) {
     using L = Layout<FMT, BN, G, LSS, AS, AM>;
@@ -180,8 +183,11 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BM;          // first weight row
     const int t0 = blockIdx.y * BN;          // first activation row
-    const int nk = (int)(p.K / BK);          // stages
+    const int kz = KS > 1 ? (int)blockIdx.z : 0;
+    const int nk = (int)(p.K / BK) / KS;     // stages of this CTA's k range
+    const int k0 = kz * nk;                  // its first stage
     const int ns = nk / G;                   // super-stages
+    const int j0 = k0 / G;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
     const uint32_t bar0 = smem_u32(bars);
@@ -238,9 +244,9 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             auto issue = [&](int j) {
                 if (wl) {
                     mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::X_BYTES + L::W_BYTES));
-                    tma_load_2d(base + L::X_BYTES, &tmW, full_bar(s), j * L::WROW, m0);
+                    tma_load_2d(base + L::X_BYTES, &tmW, full_bar(s), (j0 + j) * L::WROW, m0);
                 } else {
-                    tma_load_3d(base, &tmX, full_bar(s), 0, t0, j * G);
+                    tma_load_3d(base, &tmX, full_bar(s), 0, t0, (j0 + j) * G);
                 }
             };
             if (!p.stall) {
@@ -334,7 +340,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                                             : (uint32_t)((r >> 2) & 1);
         // Q4 scales of this row: the two fp16 of stage kb (blocks 2 kb, 2 kb + 1), loaded two
         // of this group's stages ahead
-        const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.ws + n * (p.K / 32));
+        const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.ws + n * (p.K / 32)) + k0;
         uint32_t sc0 = 0, sc1 = 0;
         if (FMT == 0 && row_ok) {
             if (grp < nk) sc0 = __ldg(srow + grp);
@@ -430,7 +436,11 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         // ---- epilogue: TMEM -> registers -> scale -> Y[t][n] ----
         // warp w reads TMEM lanes 32 (w % 4).. and the accumulator columns
         // [g BN/4, (g + 1) BN/4) of its group g = w / 4, 16 at a time
-        if (!*abort_flag && mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) {
+        if (KS > 1) {
+            // split K: wait for this CTA's MMAs; the exchange follows below
+            if (!*abort_flag && !mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) give_up();
+            tc_fence_after();
+        } else if (!*abort_flag && mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) {
             tc_fence_after();
             pdl_wait();   // outputs and guard scales only after the previous kernel has finished
             const float rsn = (FMT == 1 && row_ok) ? p.rs[n] : 0.f;
@@ -459,6 +469,78 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         }
     }
 
+    if (KS > 1) {
+        // ---- split-K exchange: every thread of both CTAs passes both cluster barriers ----
+        // After the first, both CTAs' MMAs are done and their rings idle.  Rank r finishes
+        // columns [r BN/2, (r + 1) BN/2): it sends the other half of its accumulator into
+        // the partner's ring memory, then, after the second barrier, adds the partner's
+        // half to its own (a + b, the same in both orders).  Buffer: [128 rows][BN/2] f32,
+        // 16-byte chunk c of row r stored at chunk c ^ (r % CH) (CH chunks per row), so
+        // both the remote 16-byte stores and the local 16-byte loads of a warp's 32 rows
+        // spread over the banks.
+        constexpr int HALF = BN / 2;
+        const uint32_t rank = cluster_ctarank(), partner = rank ^ 1u;
+        cluster_sync_all();
+        const bool dec = warp < DEC_WARPS;
+        const int q4w = warp & 3, grp = warp >> 2;
+        const int r = 32 * q4w + lane;
+        const uint32_t t_lane = (uint32_t)(32 * q4w) << 16;
+        constexpr int CW = HALF / 4;              // columns per decoder group
+        constexpr int CH = HALF / 4;              // 16-byte chunks per buffer row
+        const uint32_t row_off = (uint32_t)(r * HALF * 4);
+        const uint32_t csw = (uint32_t)(r % CH);
+        if (dec && !*abort_flag) {
+            const uint32_t dst = mapa_shared(sb, partner) + row_off;
+            const int hb = (int)partner * HALF;
+#pragma unroll 1
+            for (int cc = grp * CW; cc < (grp + 1) * CW; cc += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)(hb + cc), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st_cluster_v4(dst + (((uint32_t)(cc / 4 + q) ^ csw) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                  v[4 * q + 3]);
+            }
+        }
+        cluster_sync_all();
+        if (dec && !*abort_flag) {
+            pdl_wait();   // outputs and guard scales only after the previous kernel has finished
+            const int64_t n = (int64_t)m0 + r;
+            const bool row_ok = n < p.N;
+            const float rsn = (FMT == 1 && row_ok) ? p.rs[n] : 0.f;
+            const int hb = (int)rank * HALF;
+#pragma unroll 1
+            for (int cc = grp * CW; cc < (grp + 1) * CW; cc += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)(hb + cc), v);
+                tmem_ld_wait();
+                float pr[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w = ld_shared_v4(sb + row_off + (((uint32_t)(cc / 4 + q) ^ csw) << 4));
+                    pr[4 * q] = __uint_as_float(w.x);
+                    pr[4 * q + 1] = __uint_as_float(w.y);
+                    pr[4 * q + 2] = __uint_as_float(w.z);
+                    pr[4 * q + 3] = __uint_as_float(w.w);
+                }
+                const int64_t tb = (int64_t)t0 + hb + cc;
+                float rsx_l = 0.f;
+                if (FMT == 0 && lane < 16 && tb + lane < p.T) rsx_l = p.rsx[tb + lane];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, rsx_l, jj) : rsn;
+                    const int64_t t = tb + jj;
+                    if (row_ok && t < p.T) {
+                        const float val = (__uint_as_float(v[jj]) + pr[jj]) * sx;
+                        if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = val;
+                        else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(val);
+                    }
+                }
+            }
+        }
+    }
+
     // ---- teardown ----
     tc_fence_before();
     __syncthreads();
@@ -470,10 +552,12 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     }
 }
 
-template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM>
+template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS = 1>
 cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t s) {
     using L = Layout<FMT, BN, G, LSS, AS, AM>;
     static_assert(L::TOTAL <= 232448, "shared memory budget");
+    static_assert(KS == 1 || (KS == 2 && L::S_OFF + LSS * L::SLOT >= (BN / 2) * 128 * 4),
+                  "the partner's half accumulator fits in the ring memory");
     static_assert(2 * LSS <= 32, "two producer lanes per super-slot");
     // Group g decodes the stages kb % 4 == g: with AS a multiple of 4 each decoded slot
     // (and pair of slots) belongs to fixed groups that wait for its rounds in order.
@@ -500,7 +584,7 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
                           st, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
-    auto kern = k_tc<FMT, BN, XBF, G, LSS, AS, AM>;
+    auto kern = k_tc<FMT, BN, XBF, G, LSS, AS, AM, KS>;
     static int configured_device = -1;       // attributes are per device; set once per instantiation
     int dev = 0;
     cudaGetDevice(&dev);
@@ -514,34 +598,63 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = L::TOTAL;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (KS > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = KS;
+        ++na;
+    }
+    if (p.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = p.pdl ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, mw, mx, p);
 }
 
 cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     const int xbf = fmt == 0 ? 0 : a.x_bf16;
     const int64_t mt = (a.N + BM - 1) / BM;
+    const int64_t nk = a.K / BK;
+    // One CTA per SM.  Time of a CTA ~ its stages x the measured cost of a 64-k stage
+    // (about 800 / 830 / 940 cycles at BN = 64 / 128 / 256: the MMA issue path and the
+    // loads, not the MMA itself, set it below BN = 256), plus about 6000 cycles for the
+    // exchange when K is split over two CTAs; times the waves.  The cheapest candidate
+    // wins (ties: the earlier, wider one).
     int bn = (int)options().tc_bn;
-    if (bn != 64 && bn != 128 && bn != 256) {
-        // One CTA per SM; a CTA's time per 64-k stage is about max(decode and loads, MMA):
-        // the former does not depend on BN, the MMA grows with BN (about 320 cycles at
-        // BN = 128 on one SM).  Pick the width with the least waves x per-CTA time (ties:
-        // the wider tile, which decodes each weight fewer times).
-        const double dec = 450.0;
-        double best = 0.0;
-        for (int cand : {256, 128, 64}) {
-            const int64_t ctas = mt * ((a.T + cand - 1) / cand);
+    int ks = (int)options().tc_ksplit;
+    const bool ks2_ok = nk % 8 == 0;
+    {
+        struct Cand { int bn, ks; };
+        const Cand cands[] = {{256, 1}, {256, 2}, {128, 1}, {128, 2}, {64, 1}};
+        double best = -1.0;
+        int bbn = 128, bks = 1;
+        for (const Cand& c : cands) {
+            if (bn != 0 && c.bn != bn) continue;
+            if (ks != 0 && c.ks != ks) continue;
+            // split only to fill the GPU: when the unsplit tiles leave a quarter of the SMs idle
+            if (c.ks == 2 && (!ks2_ok || (ks == 0 && mt * ((a.T + c.bn - 1) / c.bn) * 4 > 3 * num_sms()))) continue;
+            const double stage = c.bn == 256 ? 940.0 : c.bn == 128 ? 830.0 : 800.0;
+            const int64_t ctas = mt * ((a.T + c.bn - 1) / c.bn) * c.ks;
             const int64_t waves = (ctas + num_sms() - 1) / num_sms();
-            const double cost = (double)waves * std::max(dec, 320.0 * cand / 128.0);
-            if (best == 0.0 || cost < best - 1e-9) {
+            const double cost = (double)waves * ((double)(nk / c.ks) * stage + (c.ks > 1 ? 6000.0 : 0.0));
+            if (best < 0.0 || cost < best - 1e-9) {
                 best = cost;
-                bn = cand;
+                bbn = c.bn;
+                bks = c.ks;
             }
         }
+        if (best < 0.0) {   // a forced combination that cannot run: fall back to no split
+            bbn = bn != 0 ? bn : 128;
+            bks = 1;
+        }
+        bn = bbn;
+        ks = bks;
     }
     Params p = {};
     p.rsx = a.rsx;
@@ -556,41 +669,41 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     p.stall = (int)options().test_stall;
     options().test_stall = 0;
     p.pdl = 1;   // the guard pass (Q4) or the previous kernel touches neither the weights nor anything before the wait
-    dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), 1);
+    dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), (unsigned)ks);
     if (options().trace)
-        fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d grid=(%u,%u)\n", fmt, (long long)a.T,
-                (long long)a.N, (long long)a.K, bn, grid.x, grid.y);
+        fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d ksplit=%d grid=(%u,%u,%u)\n", fmt,
+                (long long)a.T, (long long)a.N, (long long)a.K, bn, ks, grid.x, grid.y, grid.z);
     // decoded weight operand: 1 = shared memory, 2 = tensor memory (default)
     const int am = options().tc_amode == 1 ? 0 : 1;
     // <FMT, BN, XBF, G, LSS, AS, AM>: super-stages of G stages (weight rows of 64 or 128
     // bytes per box), as many super-slots as fit next to the decoded slots
     if (am == 0) {
         if (fmt == 0) {
-            if (bn == 256) return launch_bn<0, 256, 0, 2, 2, 4, 0>(a, p, grid, s);
-            if (bn == 128) return launch_bn<0, 128, 0, 2, 4, 4, 0>(a, p, grid, s);
+            if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 2, 2, 4, 0, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 2, 2, 4, 0, 1>(a, p, grid, s);
+            if (bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 2, 4, 4, 0, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 2, 4, 4, 0, 1>(a, p, grid, s);
             return launch_bn<0, 64, 0, 4, 3, 4, 0>(a, p, grid, s);
         }
         if (xbf) {
-            if (bn == 256) return launch_bn<1, 256, 1, 2, 2, 4, 0>(a, p, grid, s);
-            if (bn == 128) return launch_bn<1, 128, 1, 2, 3, 4, 0>(a, p, grid, s);
+            if (bn == 256) return ks == 2 ? launch_bn<1, 256, 1, 2, 2, 4, 0, 2>(a, p, grid, s) : launch_bn<1, 256, 1, 2, 2, 4, 0, 1>(a, p, grid, s);
+            if (bn == 128) return ks == 2 ? launch_bn<1, 128, 1, 2, 3, 4, 0, 2>(a, p, grid, s) : launch_bn<1, 128, 1, 2, 3, 4, 0, 1>(a, p, grid, s);
             return launch_bn<1, 64, 1, 2, 4, 4, 0>(a, p, grid, s);
         }
-        if (bn == 256) return launch_bn<1, 256, 0, 2, 2, 4, 0>(a, p, grid, s);
-        if (bn == 128) return launch_bn<1, 128, 0, 2, 3, 4, 0>(a, p, grid, s);
+        if (bn == 256) return ks == 2 ? launch_bn<1, 256, 0, 2, 2, 4, 0, 2>(a, p, grid, s) : launch_bn<1, 256, 0, 2, 2, 4, 0, 1>(a, p, grid, s);
+        if (bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 3, 4, 0, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 3, 4, 0, 1>(a, p, grid, s);
         return launch_bn<1, 64, 0, 2, 4, 4, 0>(a, p, grid, s);
     }
     if (fmt == 0) {
-        if (bn == 256) return launch_bn<0, 256, 0, 2, 3, 8, 1>(a, p, grid, s);
-        if (bn == 128) return launch_bn<0, 128, 0, 2, 5, 8, 1>(a, p, grid, s);
+        if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 2, 3, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 2, 3, 8, 1, 1>(a, p, grid, s);
+        if (bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 2, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 2, 5, 8, 1, 1>(a, p, grid, s);
         return launch_bn<0, 64, 0, 4, 4, 8, 1>(a, p, grid, s);
     }
     if (xbf) {
-        if (bn == 256) return launch_bn<1, 256, 1, 1, 5, 8, 1>(a, p, grid, s);
-        if (bn == 128) return launch_bn<1, 128, 1, 2, 4, 8, 1>(a, p, grid, s);
+        if (bn == 256) return ks == 2 ? launch_bn<1, 256, 1, 1, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 256, 1, 1, 5, 8, 1, 1>(a, p, grid, s);
+        if (bn == 128) return ks == 2 ? launch_bn<1, 128, 1, 2, 4, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 1, 2, 4, 8, 1, 1>(a, p, grid, s);
         return launch_bn<1, 64, 1, 2, 6, 8, 1>(a, p, grid, s);
     }
-    if (bn == 256) return launch_bn<1, 256, 0, 1, 5, 8, 1>(a, p, grid, s);
-    if (bn == 128) return launch_bn<1, 128, 0, 2, 4, 8, 1>(a, p, grid, s);
+    if (bn == 256) return ks == 2 ? launch_bn<1, 256, 0, 1, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 256, 0, 1, 5, 8, 1, 1>(a, p, grid, s);
+    if (bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 4, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 4, 8, 1, 1>(a, p, grid, s);
     return launch_bn<1, 64, 0, 2, 6, 8, 1>(a, p, grid, s);
 }
 

@@ -258,19 +258,19 @@ class _Opt:
 
 
 @pytest.mark.parametrize("am", [1, 2])
-@pytest.mark.parametrize("cl", [1, 2, 4])
+@pytest.mark.parametrize("ks", [1, 2])
 @pytest.mark.parametrize("bn", [64, 128, 256])
-def test_tcgen05_cluster_multicast_and_token_tiles(cl, bn, am):
-    """Every cluster size (activation tile multicast to 1, 2 or 4 CTAs), token
-    tile and placement of the decoded weight operand (1 shared memory,
-    2 tensor memory), on shapes whose weight-row tiles do not fill whole
-    clusters (N=300 -> 3 tiles, padded) and whose tokens leave a ragged tile."""
-    case4 = synth.gemm_q4_case(5000 + cl + bn, 150, 512, 300, x_dtype="bf16", signed=True)
-    case8 = synth.gemm_q8_case(6000 + cl + bn, 150, 512, 300, x_dtype="bf16")
-    with ForcePath(2), _Opt(cq.CQ_OPT_TC_CLUSTER, cl), _Opt(cq.CQ_OPT_TC_BN, bn), _Opt(cq.CQ_OPT_TC_AMODE, am):
+def test_tcgen05_ksplit_token_tiles_and_operand_modes(ks, bn, am):
+    """Every token tile, K split (one CTA, or two CTAs of a cluster whose
+    partial sums are exchanged in shared memory) and placement of the decoded
+    weight operand (1 shared memory, 2 tensor memory), on shapes with a
+    ragged weight-row tile (N=300) and a ragged token tile."""
+    case4 = synth.gemm_q4_case(5000 + ks + bn, 150, 512, 300, x_dtype="bf16", signed=True)
+    case8 = synth.gemm_q8_case(6000 + ks + bn, 150, 512, 300, x_dtype="bf16")
+    with ForcePath(2), _Opt(cq.CQ_OPT_TC_KSPLIT, ks), _Opt(cq.CQ_OPT_TC_BN, bn), _Opt(cq.CQ_OPT_TC_AMODE, am):
         Y4, wq = run_q4(case4, "f32")
         Y8 = run_q8(case8, "bf16")
     yref, S = oracle_q4(case4, wq)
-    check(y_host(Y4), yref, S, "f32", f"q4 cl={cl} bn={bn} am={am}")
+    check(y_host(Y4), yref, S, "f32", f"q4 ks={ks} bn={bn} am={am}")
     yref8, S8 = oracle_q8(case8)
-    check(y_host(Y8), yref8, S8, "bf16", f"q8 cl={cl} bn={bn} am={am}")
+    check(y_host(Y8), yref8, S8, "bf16", f"q8 ks={ks} bn={bn} am={am}")
