@@ -148,28 +148,68 @@ __global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t
     const int64_t row = blockIdx.x;
     const int64_t src_row = gather ? (int64_t)(gather[row] / per) : row;
     const uint4* src = reinterpret_cast<const uint4*>(x + src_row * K);
-    const int64_t n8 = K / 8;
-    float m = 0.f;
-    for (int64_t i = threadIdx.x; i < n8; i += 256) {
-        uint4 v = src[i];
-        const T* e = reinterpret_cast<const T*>(&v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(to_f32<T>(e[j])));
-    }
-    m = block_max_256(m, red);
-    const int sh = guard_shift(m);
-    const float sc = pow2f(sh);
     uint4* dst = reinterpret_cast<uint4*>(xh + row * K);
-    for (int64_t blk = threadIdx.x; blk < K / 32; blk += 256) {
-        float v[32];
+    const int64_t nblk = K / 32;
+    const int tid = threadIdx.x;
+    int sh;
+    if (nblk <= 2 * 256) {
+        // up to two 32-element blocks per thread: read once, kept in registers
+        uint4 c[2][4];
+        float m = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 u = src[4 * blk + q];
-            const T* e = reinterpret_cast<const T*>(&u);
+        for (int i = 0; i < 2; ++i) {
+            const int64_t blk = tid + 256 * i;
+            if (blk < nblk) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[8 * q + j] = to_f32<T>(e[j]) * sc;
+                for (int q = 0; q < 4; ++q) {
+                    c[i][q] = src[4 * blk + q];
+                    const T* e = reinterpret_cast<const T*>(&c[i][q]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(to_f32<T>(e[j])));
+                }
+            }
         }
-        store_block_stream_order(v, dst + 4 * blk);
+        m = block_max_256(m, red);
+        sh = guard_shift(m);
+        const float sc = pow2f(sh);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int64_t blk = tid + 256 * i;
+            if (blk < nblk) {
+                float v[32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const T* e = reinterpret_cast<const T*>(&c[i][q]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[8 * q + j] = to_f32<T>(e[j]) * sc;
+                }
+                store_block_stream_order(v, dst + 4 * blk);
+            }
+        }
+    } else {
+        // longer rows: one pass for the maximum, one for the conversion
+        const int64_t n8 = K / 8;
+        float m = 0.f;
+        for (int64_t i = tid; i < n8; i += 256) {
+            uint4 v = src[i];
+            const T* e = reinterpret_cast<const T*>(&v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(to_f32<T>(e[j])));
+        }
+        m = block_max_256(m, red);
+        sh = guard_shift(m);
+        const float sc = pow2f(sh);
+        for (int64_t blk = tid; blk < nblk; blk += 256) {
+            float v[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 u = src[4 * blk + q];
+                const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[8 * q + j] = to_f32<T>(e[j]) * sc;
+            }
+            store_block_stream_order(v, dst + 4 * blk);
+        }
     }
     if (threadIdx.x == 0) rsx[row] = pow2f(-sh);
 }
@@ -191,7 +231,9 @@ cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K,
 // ---- MoE routing layout -------------------------------------------------
 // Routed (t, j) pairs grouped by expert, token order kept inside an expert
 // ("oxinfer 0.0.5 src/metal.rs", Backend::moe: per-expert counts, segment
-// starts, gathered sources filled in token order).  One CTA.
+// starts, gathered sources filled in token order).  One CTA: shared-memory
+// counts, a block scan for the segment starts and the active experts, and a
+// stable rank inside each expert from a warp match on the expert index.
 //   seg[e]   = number of pairs routed to experts below e  (seg[E] = P)
 //   perm[q]  = pair id (t*topk + j) at grouped position q
 //   inv[p]   = grouped position of pair p
@@ -200,17 +242,18 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
                                                    int32_t* __restrict__ seg, int32_t* __restrict__ perm,
                                                    int32_t* __restrict__ inv, int32_t* __restrict__ act,
                                                    int32_t* __restrict__ n_act, int32_t* __restrict__ status) {
+    pdl_launch_dependents();  // the gather pass after this one may be scheduled now
     pdl_wait();               // idx may come from the previous kernel; the previous call's readers are done
-    pdl_launch_dependents();
     extern __shared__ int sh[];
-    int* cnt = sh;            // [E]
-    int* fill = sh + E;       // [E]
-    int* chunk_e = sh + 2 * E;  // [256]
+    int* cnt = sh;            // [E] pairs per expert
+    int* fill = sh + E;       // [E] next free grouped position of each expert
     __shared__ int bad;
-    if (threadIdx.x == 0) bad = 0;
-    for (int e = threadIdx.x; e < E; e += 256) cnt[e] = 0;
+    __shared__ int wsum[2][8];  // per-warp totals of the block scan (counts, active flags)
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) bad = 0;
+    for (int e = tid; e < E; e += 256) cnt[e] = 0;
     __syncthreads();
-    for (int p = threadIdx.x; p < P; p += 256) {
+    for (int p = tid; p < P; p += 256) {
         const int e = idx[p];
         if (e < 0 || e >= E)
             bad = 1;
@@ -219,46 +262,84 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
     }
     __syncthreads();
     if (bad) {
-        if (threadIdx.x == 0) {
+        if (tid == 0) {
             *status = 1;
             set_err(DEV_INDEX);
         }
         return;
     }
-    if (threadIdx.x == 0) {
-        int acc = 0, na = 0;
-        for (int e = 0; e < E; ++e) {
-            seg[e] = acc;
-            fill[e] = acc;
-            acc += cnt[e];
-            if (cnt[e] > 0) act[na++] = e;
+    // exclusive scans of cnt[e] and of [cnt[e] > 0] over the experts: thread tid owns the
+    // contiguous experts [tid * per, (tid + 1) * per)
+    const int per = (E + 255) / 256;
+    const int e0 = tid * per;
+    int lc = 0, la = 0;
+    for (int i = 0; i < per; ++i) {
+        const int e = e0 + i;
+        if (e < E) {
+            lc += cnt[e];
+            la += cnt[e] > 0;
         }
-        seg[E] = acc;
+    }
+    int xc = lc, xa = la;      // inclusive warp scans
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yc = __shfl_up_sync(0xffffffffu, xc, o), ya = __shfl_up_sync(0xffffffffu, xa, o);
+        if (lane >= o) {
+            xc += yc;
+            xa += ya;
+        }
+    }
+    if (lane == 31) {
+        wsum[0][warp] = xc;
+        wsum[1][warp] = xa;
+    }
+    __syncthreads();
+    int bc = 0, ba = 0;
+    for (int w = 0; w < warp; ++w) {
+        bc += wsum[0][w];
+        ba += wsum[1][w];
+    }
+    int c = bc + xc - lc, na = ba + xa - la;   // exclusive prefixes at e0
+    for (int i = 0; i < per; ++i) {
+        const int e = e0 + i;
+        if (e < E) {
+            seg[e] = c;
+            fill[e] = c;
+            if (cnt[e] > 0) act[na++] = e;
+            c += cnt[e];
+        }
+    }
+    if (tid == 255) {
+        seg[E] = c;      // = P
         *n_act = na;
     }
     __syncthreads();
+    // stable positions: pairs in id order (t ascending, then j), 256 per chunk; inside a
+    // chunk the warps take turns, and a warp ranks its lanes with a match on the expert
     for (int base = 0; base < P; base += 256) {
-        const int p = base + threadIdx.x;
+        const int p = base + tid;
         const int e = p < P ? idx[p] : -1;
-        chunk_e[threadIdx.x] = e;
-        __syncthreads();
-        if (e >= 0) {
-            int before = 0;
-            for (int q = 0; q < (int)threadIdx.x; ++q) before += (chunk_e[q] == e);
-            const int pos = fill[e] + before;
-            perm[pos] = p;
-            inv[p] = pos;
+        for (int w = 0; w < 8; ++w) {
+            if (warp == w) {
+                const unsigned peers = __match_any_sync(0xffffffffu, e);
+                if (e >= 0) {
+                    const int rank = __popc(peers & ((1u << lane) - 1u));
+                    const int pos = fill[e] + rank;
+                    perm[pos] = p;
+                    inv[p] = pos;
+                }
+                __syncwarp();
+                if (e >= 0 && (peers & ((1u << lane) - 1u)) == 0u) fill[e] += __popc(peers);
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        if (e >= 0) atomicAdd(&fill[e], 1);
-        __syncthreads();
     }
-    if (threadIdx.x == 0) *status = 0;
+    if (tid == 0) *status = 0;
 }
 
 cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
                              int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, cudaStream_t s) {
-    const size_t smem = (size_t)(2 * E + 256) * sizeof(int);
+    const size_t smem = (size_t)(2 * E) * sizeof(int);
     return launch_pdl(k_moe_route, dim3(1), dim3(256), smem, s, idx, (int)(T * topk), (int)E, seg, perm, inv, act, n_act,
                       status);
 }
