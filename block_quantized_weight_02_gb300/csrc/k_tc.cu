@@ -64,6 +64,7 @@ struct Params {
     uint64_t wait_ns;
     int stall;
     int pdl;   // launched with a programmatic dependency on the guard pass
+    int y_tma; // Y row pitch is a multiple of 16 bytes: tiles leave through a TMA store
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -139,9 +140,14 @@ struct Layout {
     static constexpr int A_OFF = 0;
     static constexpr int S_OFF = AM == 0 ? AS * A_BYTES : 0;
     static constexpr int BAR_OFF = S_OFF + LSS * SLOT;
-    // full[LSS], empty[LSS], afull[AS], aempty[AS / 2] (one per pair of decoded slots), accf;
+    // Decoded slots are handed over in rounds of RS stages, NRB rounds in flight: four stages
+    // when the ring holds many stages (BN < 256 with tensor-memory slots), else two, so
+    // that a round never waits for ring slots its own MMAs free.
+    static constexpr int RS = (AM == 1 && BN < 256) ? 4 : 2;
+    static constexpr int NRB = AS / RS;
+    // full[LSS], empty[LSS], afull[NRB], aempty[NRB] (one per round in flight), accf, xchg;
     // then tmem slot, abort, never
-    static constexpr int NBAR = 2 * LSS + AS + AS / 2 + 1;
+    static constexpr int NBAR = 2 * LSS + 2 * NRB + 2;
     static constexpr int MISC = NBAR * 8 + 16;
     static constexpr int TOTAL = BAR_OFF + MISC + 1024;  // + alignment slack
     // tensor memory: accumulator in columns [0, BN); AM 1 adds AS decoded A tiles of 32 columns
@@ -152,6 +158,19 @@ struct Layout {
     static_assert(SLOT % 1024 == 0 && X_CHUNK % 1024 == 0, "1024-byte aligned swizzled tiles");
     static_assert(WROW == 32 || WROW == 64 || WROW == 128, "weight rows of 32, 64 or 128 bytes");
 };
+
+// Epilogue geometry: a CTA finishes NC columns of its tile (all BN, or its half under a
+// K split); decoder group g owns NC / 4 of them and handles them CH at a time (one
+// tensor-memory load, one output box, one exchange copy per chunk).
+constexpr int ep_cols(int BN, int KS) { return KS > 1 ? BN / 2 : BN; }
+constexpr int ep_chunk(int BN, int KS) { return ep_cols(BN, KS) / 4 < 32 ? ep_cols(BN, KS) / 4 : 32; }
+
+template <int CH>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[CH]) {
+    static_assert(CH == 16 || CH == 32, "16 or 32 columns per load");
+    if constexpr (CH == 32) tmem_ld_32x32b_x32(taddr, v);
+    else tmem_ld_32x32b_x16(taddr, v);
+}
 
 constexpr int DEC_WARPS = 16;                // 4 groups (stages kb % 4) x 4 row quarters
 constexpr int THREADS = (DEC_WARPS + 2) * 32;
@@ -174,7 +193,8 @@ __device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
 // finishes half of the tile's columns.
 template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS>
 __global__ void __launch_bounds__(THREADS, 1)
-k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const Params p) {
+k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+     const __grid_constant__ CUtensorMap tmY, const Params p) {
     using L = Layout<FMT, BN, G, LSS, AS, AM>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -184,6 +204,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     const int m0 = blockIdx.x * BM;          // first weight row
     const int t0 = blockIdx.y * BN;          // first activation row
     const int kz = KS > 1 ? (int)blockIdx.z : 0;
+    const uint32_t crank = KS > 1 ? cluster_ctarank() : 0u;   // rank in the K-split cluster
     const int nk = (int)(p.K / BK) / KS;     // stages of this CTA's k range
     const int k0 = kz * nk;                  // its first stage
     const int ns = nk / G;                   // super-stages
@@ -193,9 +214,14 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (LSS + s); };
-    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * LSS + a); };
-    auto aempty_bar = [&](int pr) { return bar0 + 8u * (2 * LSS + AS + pr); };   // decoded slots 2pr, 2pr + 1
-    const uint32_t accf_bar = bar0 + 8u * (2 * LSS + AS + AS / 2);
+    // Decoded slots come in rounds of RS stages (stages r RS .. r RS + RS - 1 in slots
+    // (r % NRB) RS ..): per round in flight one barrier says the round is decoded, one
+    // that its MMAs are done.
+    constexpr int RS = L::RS, NRB = L::NRB;
+    auto afull_bar = [&](int rb) { return bar0 + 8u * (2 * LSS + rb); };
+    auto aempty_bar = [&](int rb) { return bar0 + 8u * (2 * LSS + NRB + rb); };
+    const uint32_t accf_bar = bar0 + 8u * (2 * LSS + 2 * NRB);
+    const uint32_t xchg_bar = accf_bar + 8u;   // split K: the partner's half has arrived
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never_flag = abort_flag + 1;
@@ -206,9 +232,12 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             mbar_init(full_bar(s), 1);   // the weight lane's arrival + both boxes' bytes
             mbar_init(empty_bar(s), 1);  // the MMA's commit after the super-stage's last stage
         }
-        for (int a = 0; a < AS; ++a) mbar_init(afull_bar(a), 4);       // one arrival per warp of the decoding group
-        for (int pr = 0; pr < AS / 2; ++pr) mbar_init(aempty_bar(pr), 1);  // the MMA's commit of the stage pair
+        for (int rb = 0; rb < NRB; ++rb) {
+            mbar_init(afull_bar(rb), 4 * RS);   // one arrival per warp of each of the round's RS stages
+            mbar_init(aempty_bar(rb), 1);       // the MMA's commit of the round
+        }
         mbar_init(accf_bar, 1);
+        mbar_init(xchg_bar, 1);
         *abort_flag = 0;
         *never_flag = 0;
         fence_mbar_init();
@@ -226,6 +255,16 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         *abort_flag = 1;
         atomicCAS(&g_err_tc, 0, DEV_TIMEOUT);
     };
+    // The next kernel in the stream may be scheduled on idle SMs now; it waits for this
+    // grid to finish before it touches memory.
+    pdl_launch_dependents();
+
+    constexpr int NC = ep_cols(BN, KS);      // epilogue: columns this CTA finishes
+    constexpr int CW = NC / 4;               //           columns per decoder group
+    constexpr int CH = ep_chunk(BN, KS);     //           columns per chunk
+    static_assert(CW % 16 == 0 && CW % CH == 0 && CW <= 64, "epilogue chunks");
+    const int cbase = kz * NC;               // first column finished here
+    float esc0 = 0.f, esc1 = 0.f;            // epilogue scales, loaded before the last MMAs end
 
     if (warp == PRODUCER_WARP) {
         // ================= TMA producers =================
@@ -284,38 +323,42 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         // decoded slots (their groups had waited for the super-slot, so the activations are
         // in too), eight MMAs, one commit that frees the pair of decoded slots and, at the end
         // of a super-stage, one that frees the super-slot.  Descriptors advance by adding.
+        // A super-slot's release is committed only when a later super-stage waits for it.
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(BM, BN, XBF);
-            int a = 0, s = 0, u = 0;          // decoded slot, super-slot and chunk of stage kb
-            uint32_t aph = 0;
-            for (int kb = 0; kb < nk; kb += 2) {
-                if (!mbar_wait(afull_bar(a), aph, p.wait_ns, abort_flag) ||
-                    !mbar_wait(afull_bar(a + 1), aph, p.wait_ns, abort_flag)) {
+            const int nr = (nk + RS - 1) / RS;     // rounds (the last one may be short)
+            int s = 0, u = 0, js = 0;             // super-slot, chunk and super-stage of the next stage
+            for (int r = 0; r < nr; ++r) {
+                const int rb = r % NRB;
+                if (!mbar_wait(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag)) {
                     give_up();
                     break;
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint64_t bd = smem_desc_sw128(slot_base(s) + (uint32_t)(u * L::X_CHUNK));
-                    const uint64_t ad = AM == 0 ? smem_desc_sw128(sb + L::A_OFF + (a + h) * A_BYTES) : 0;
-                    const uint32_t at = tmem + (uint32_t)(L::A_COL + (a + h) * 32);
+                for (int i = 0; i < RS; ++i) {
+                    const int kb = r * RS + i;
+                    if (kb < nk) {
+                        const int a = rb * RS + i;
+                        const uint64_t bd = smem_desc_sw128(slot_base(s) + (uint32_t)(u * L::X_CHUNK));
+                        const uint64_t ad = AM == 0 ? smem_desc_sw128(sb + L::A_OFF + a * A_BYTES) : 0;
+                        const uint32_t at = tmem + (uint32_t)(L::A_COL + a * 32);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint32_t acc = (kb + h + kk) != 0 ? 1u : 0u;
-                        // +32 bytes of K = +2 in the descriptor's 16-byte address units
-                        if (AM == 0) tc_mma_f16(tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
-                        else tc_mma_f16_ts(tmem, at + 8u * kk, bd + 2u * kk, idesc, acc);
-                    }
-                    if (++u == G) {
-                        u = 0;
-                        tc_commit(empty_bar(s));                // super-slot free after its last stage
-                        if (++s == LSS) s = 0;
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint32_t acc = (kb + kk) != 0 ? 1u : 0u;
+                            // +32 bytes of K = +2 in the descriptor's 16-byte address units
+                            if (AM == 0) tc_mma_f16(tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
+                            else tc_mma_f16_ts(tmem, at + 8u * kk, bd + 2u * kk, idesc, acc);
+                        }
+                        if (++u == G) {
+                            u = 0;
+                            if (js + LSS < ns) tc_commit(empty_bar(s));   // super-slot free
+                            ++js;
+                            if (++s == LSS) s = 0;
+                        }
                     }
                 }
-                tc_commit(aempty_bar(a >> 1));                  // decoded slots a, a + 1 free
-                a += 2;
-                if (a == AS) { a = 0; aph ^= 1u; }
+                tc_commit(aempty_bar(rb));                     // the round's decoded slots free
             }
             tc_commit(accf_bar);   // also lets teardown know every MMA has finished
         }
@@ -362,10 +405,11 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             const int kb = j * G + u;
             if ((kb & 3) != grp) continue;
             const int a = kb % AS;                             // decoded slot
-            const uint32_t aph = (uint32_t)((kb / AS) & 1);
+            const int rb = (kb / RS) % NRB;                    // its round's barriers
+            const uint32_t rph = (uint32_t)((kb / AS) & 1);    // and their phase
             uint32_t sc_next = 0;
             if (FMT == 0 && row_ok && kb + 8 < nk) sc_next = __ldg(srow + kb + 8);
-            if (!mbar_wait(aempty_bar(a >> 1), aph ^ 1u, p.wait_ns, abort_flag)) {
+            if (!mbar_wait(aempty_bar(rb), rph ^ 1u, p.wait_ns, abort_flag)) {
                 give_up();
                 stop = true;
                 break;
@@ -423,7 +467,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                 tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(a));
+            if (lane == 0) mbar_arrive(afull_bar(rb));
             sc0 = sc1;
             sc1 = sc_next;
           }
@@ -432,113 +476,130 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
               ph ^= 1u;
           }
         }
-
-        // ---- epilogue: TMEM -> registers -> scale -> Y[t][n] ----
-        // warp w reads TMEM lanes 32 (w % 4).. and the accumulator columns
-        // [g BN/4, (g + 1) BN/4) of its group g = w / 4, 16 at a time
-        if (KS > 1) {
-            // split K: wait for this CTA's MMAs; the exchange follows below
-            if (!*abort_flag && !mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) give_up();
-            tc_fence_after();
-        } else if (!*abort_flag && mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) {
-            tc_fence_after();
-            pdl_wait();   // outputs and guard scales only after the previous kernel has finished
-            const float rsn = (FMT == 1 && row_ok) ? p.rs[n] : 0.f;
-            constexpr int CW = BN / 4;
-#pragma unroll 1
-            for (int cc = grp * CW; cc < (grp + 1) * CW; cc += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)cc, v);
-                tmem_ld_wait();
-                const int64_t tb = (int64_t)t0 + cc;
-                float rsx_l = 0.f;
-                if (FMT == 0 && lane < 16 && tb + lane < p.T) rsx_l = p.rsx[tb + lane];
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, rsx_l, jj) : rsn;
-                    const int64_t t = tb + jj;
-                    if (row_ok && t < p.T) {
-                        const float val = __uint_as_float(v[jj]) * sx;
-                        if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = val;
-                        else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(val);
-                    }
-                }
+        // A short last round: the groups without a stage in it still arrive (after the
+        // round NRB back has freed the barrier), so the MMA thread's wait completes.
+        for (int kb = nk; kb < (nk + RS - 1) / RS * RS && !stop && !*abort_flag; ++kb) {
+            if ((kb & 3) != grp) continue;
+            const int rb = (kb / RS) % NRB;
+            if (!mbar_wait(aempty_bar(rb), (uint32_t)(((kb / AS) & 1) ^ 1), p.wait_ns, abort_flag)) {
+                give_up();
+                break;
             }
-        } else if (!*abort_flag) {
-            give_up();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull_bar(rb));
         }
+
+        // Output scales of the epilogue (Q4: the guard inverse of each token this thread's
+        // group finishes, lane l holding columns l and 32 + l; Q8: the row scale), read
+        // while the last MMAs run.  Outputs and guard scales only after the previous
+        // kernel has finished.
+        pdl_wait();
+        if (FMT == 0) {
+            const int64_t tb = (int64_t)t0 + cbase + grp * CW;
+            if (lane < CW && tb + lane < p.T) esc0 = p.rsx[tb + lane];
+            if (CW > 32 && tb + 32 + lane < p.T) esc1 = p.rsx[tb + 32 + lane];
+        } else if (row_ok) {
+            esc0 = p.rs[n];
+        }
+        // the accumulator is complete once the MMA thread's last commit arrives
+        if (!*abort_flag && !mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) give_up();
+        tc_fence_after();
     }
 
-    if (KS > 1) {
-        // ---- split-K exchange: every thread of both CTAs passes both cluster barriers ----
-        // After the first, both CTAs' MMAs are done and their rings idle.  Rank r finishes
-        // columns [r BN/2, (r + 1) BN/2): it sends the other half of its accumulator into
-        // the partner's ring memory, then, after the second barrier, adds the partner's
-        // half to its own (a + b, the same in both orders).  Buffer: [128 rows][BN/2] f32,
-        // 16-byte chunk c of row r stored at chunk c ^ (r % CH) (CH chunks per row), so
-        // both the remote 16-byte stores and the local 16-byte loads of a warp's 32 rows
-        // spread over the banks.
+    // ================= epilogue (every thread reaches it) =================
+    // The decoder warps read the accumulator (warp w: TMEM lanes 32 (w % 4).., the CW
+    // columns of its group g = w / 4, CH at a time), scale it and stage each chunk in the
+    // idle ring memory as [token][128 rows] in the output type; after a barrier of the
+    // group's four warps its first thread stores the chunk with TMA (rows and tokens
+    // outside Y are clipped), so the stores overlap the staging of later chunks.  When
+    // Y's row pitch is not a multiple of 16 bytes the decoders store element by element.
+    // Split K: after a first cluster barrier both CTAs' MMAs are done and their rings
+    // idle; the CTA of k half z finishes columns [z BN/2, (z + 1) BN/2).  Each stages the other half of
+    // its accumulator ([column][128 rows] f32) chunk by chunk, and the group's first
+    // thread copies each chunk in bulk into the partner, completing on the partner's
+    // exchange barrier.  The sum is own + partner (a + b, the same in both orders).  A
+    // CTA arrives on a second cluster barrier once the partner's half is in and waits on
+    // it before exiting, so no copy still reads the memory of a CTA that has left.
+    // Barriers are taken by every decoder warp whatever the abort flag; only the copies
+    // and stores are skipped after a timeout.
+    {
         constexpr int HALF = BN / 2;
-        const uint32_t rank = cluster_ctarank(), partner = rank ^ 1u;
-        cluster_sync_all();
+        constexpr uint32_t SEND_OFF = 0;              // split K: outgoing half
+        constexpr uint32_t RECV_OFF = HALF * 128 * 4; //          incoming half
+        constexpr uint32_t YST_OFF = KS > 1 ? 2 * HALF * 128 * 4 : 0;   // staged output tile
         const bool dec = warp < DEC_WARPS;
         const int q4w = warp & 3, grp = warp >> 2;
         const int r = 32 * q4w + lane;
         const uint32_t t_lane = (uint32_t)(32 * q4w) << 16;
-        constexpr int CW = HALF / 4;              // columns per decoder group
-        constexpr int CH = HALF / 4;              // 16-byte chunks per buffer row
-        const uint32_t row_off = (uint32_t)(r * HALF * 4);
-        const uint32_t csw = (uint32_t)(r % CH);
-        if (dec && !*abort_flag) {
-            const uint32_t dst = mapa_shared(sb, partner) + row_off;
-            const int hb = (int)partner * HALF;
+        const bool lead = q4w == 0 && lane == 0;     // issues the group's copies and stores
+        const int gbar = 2 + grp;                    // the group's named barrier (1 is all decoders)
+        if (KS > 1) {
+            const uint32_t partner = crank ^ 1u;
+            cluster_sync_all();
+            if (threadIdx.x == 0) mbar_arrive_expect_tx(xchg_bar, (uint32_t)(HALF * 128 * 4));
+            if (dec) {
+                const int hb = (int)partner * HALF;
+                uint32_t* st = reinterpret_cast<uint32_t*>(smem + SEND_OFF);
 #pragma unroll 1
-            for (int cc = grp * CW; cc < (grp + 1) * CW; cc += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)(hb + cc), v);
-                tmem_ld_wait();
+                for (int cc = grp * CW; cc < (grp + 1) * CW; cc += CH) {
+                    uint32_t v[CH];
+                    tmem_ld_cols<CH>(tmem + t_lane + (uint32_t)(hb + cc), v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st_cluster_v4(dst + (((uint32_t)(cc / 4 + q) ^ csw) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2],
-                                  v[4 * q + 3]);
+                    for (int jj = 0; jj < CH; ++jj) st[(cc + jj) * 128 + r] = v[jj];
+                    fence_proxy_async_smem();
+                    named_bar_sync(gbar, 128);
+                    if (lead && !*abort_flag)
+                        bulk_copy_to_cluster(mapa_shared(sb + RECV_OFF + (uint32_t)(cc * 512), partner),
+                                             sb + SEND_OFF + (uint32_t)(cc * 512), (uint32_t)(CH * 512),
+                                             mapa_shared(xchg_bar, partner));
+                }
+                if (!*abort_flag && !mbar_wait(xchg_bar, 0, p.wait_ns, abort_flag)) give_up();
             }
+            cluster_arrive_release();
         }
-        cluster_sync_all();
-        if (dec && !*abort_flag) {
-            pdl_wait();   // outputs and guard scales only after the previous kernel has finished
+        if (dec) {
             const int64_t n = (int64_t)m0 + r;
             const bool row_ok = n < p.N;
-            const float rsn = (FMT == 1 && row_ok) ? p.rs[n] : 0.f;
-            const int hb = (int)rank * HALF;
+            const float* recv = reinterpret_cast<const float*>(smem + RECV_OFF);
+            const bool f32 = p.yt == CQ_F32;
+            const int esz = f32 ? 4 : 2;
 #pragma unroll 1
-            for (int cc = grp * CW; cc < (grp + 1) * CW; cc += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)(hb + cc), v);
+            for (int ci = 0; ci < CW / CH; ++ci) {
+                const int cc = grp * CW + ci * CH;
+                uint32_t v[CH];
+                tmem_ld_cols<CH>(tmem + t_lane + (uint32_t)(cbase + cc), v);
                 tmem_ld_wait();
-                float pr[16];
+                const int64_t tb = (int64_t)t0 + cbase + cc;
+                const float escq = ci == 0 ? esc0 : esc1;
+                const bool skip = *abort_flag != 0;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 w = ld_shared_v4(sb + row_off + (((uint32_t)(cc / 4 + q) ^ csw) << 4));
-                    pr[4 * q] = __uint_as_float(w.x);
-                    pr[4 * q + 1] = __uint_as_float(w.y);
-                    pr[4 * q + 2] = __uint_as_float(w.z);
-                    pr[4 * q + 3] = __uint_as_float(w.w);
-                }
-                const int64_t tb = (int64_t)t0 + hb + cc;
-                float rsx_l = 0.f;
-                if (FMT == 0 && lane < 16 && tb + lane < p.T) rsx_l = p.rsx[tb + lane];
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, rsx_l, jj) : rsn;
+                for (int jj = 0; jj < CH; ++jj) {
+                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, escq, jj) : esc0;
+                    float acc = __uint_as_float(v[jj]);
+                    if (KS > 1) acc += recv[(cc + jj) * 128 + r];
+                    const float val = acc * sx;
                     const int64_t t = tb + jj;
-                    if (row_ok && t < p.T) {
-                        const float val = (__uint_as_float(v[jj]) + pr[jj]) * sx;
-                        if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = val;
+                    if (p.y_tma) {
+                        if (f32) reinterpret_cast<float*>(smem + YST_OFF)[(cc + jj) * 128 + r] = val;
+                        else reinterpret_cast<__nv_bfloat16*>(smem + YST_OFF)[(cc + jj) * 128 + r] = __float2bfloat16_rn(val);
+                    } else if (!skip && row_ok && t < p.T) {
+                        if (f32) reinterpret_cast<float*>(p.y)[t * p.N + n] = val;
                         else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(val);
                     }
                 }
+                if (p.y_tma) {
+                    fence_proxy_async_smem();
+                    named_bar_sync(gbar, 128);
+                    if (lead && !*abort_flag) {
+                        tma_store_2d(&tmY, sb + YST_OFF + (uint32_t)(cc * 128 * esz), m0, (int)tb);
+                        bulk_commit();
+                    }
+                }
             }
+            if (lead) bulk_wait_read0();   // the staging memory must stay valid until TMA has read it
         }
+        if (KS > 1) cluster_wait_acquire();
     }
 
     // ---- teardown ----
@@ -556,12 +617,14 @@ template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS = 1>
 cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t s) {
     using L = Layout<FMT, BN, G, LSS, AS, AM>;
     static_assert(L::TOTAL <= 232448, "shared memory budget");
-    static_assert(KS == 1 || (KS == 2 && L::S_OFF + LSS * L::SLOT >= (BN / 2) * 128 * 4),
-                  "the partner's half accumulator fits in the ring memory");
+    // epilogue staging (f32 at most) below the barriers: split K needs the outgoing and the
+    // incoming half and the staged output half; otherwise the staged output tile
+    static_assert(L::S_OFF + LSS * L::SLOT >= (KS > 1 ? 3 * (BN / 2) * 128 * 4 : BN * 128 * 4),
+                  "epilogue staging fits in the ring memory");
     static_assert(2 * LSS <= 32, "two producer lanes per super-slot");
-    // Group g decodes the stages kb % 4 == g: with AS a multiple of 4 each decoded slot
-    // (and pair of slots) belongs to fixed groups that wait for its rounds in order.
-    static_assert(AS % 4 == 0 && (G == 1 || G == 2 || G == 4), "decoded slots owned by fixed decoder groups");
+    // Group g decodes the stages kb % 4 == g, in rounds of 2 or 4 stages with AS 4 or 8
+    // slots: each round barrier is waited for by fixed groups, every one of its rounds in order.
+    static_assert((AS == 4 || AS == 8) && (G == 1 || G == 2 || G == 4), "decoded slots owned by fixed decoder groups");
     // weights: rows of G stages (G * ROW bytes) per box
     CUtensorMap mw, mx;
     {
@@ -582,6 +645,17 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
         uint32_t box[3] = {64, (uint32_t)BN, (uint32_t)G};
         if (!encode_tiled(&mx, XBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, d,
                           st, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    // output tiles: Y [T][N] seen as {N, T}; a box is 128 rows x one epilogue chunk of columns
+    CUtensorMap my = mx;
+    if (p.y_tma) {
+        const uint64_t es = a.yt == CQ_F32 ? 4 : 2;
+        uint64_t d[2] = {(uint64_t)a.N, (uint64_t)a.T};
+        uint64_t st[1] = {(uint64_t)a.N * es};
+        uint32_t box[2] = {(uint32_t)BM, (uint32_t)ep_chunk(BN, KS)};
+        if (!encode_tiled(&my, a.yt == CQ_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          a.y, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
     auto kern = k_tc<FMT, BN, XBF, G, LSS, AS, AM, KS>;
@@ -614,7 +688,7 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, mw, mx, p);
+    return cudaLaunchKernelEx(&cfg, kern, mw, mx, my, p);
 }
 
 cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
@@ -669,6 +743,7 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     p.stall = (int)options().test_stall;
     options().test_stall = 0;
     p.pdl = 1;   // the guard pass (Q4) or the previous kernel touches neither the weights nor anything before the wait
+    p.y_tma = ((a.N * (a.yt == CQ_F32 ? 4 : 2)) % 16 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0) ? 1 : 0;
     dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), (unsigned)ks);
     if (options().trace)
         fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d ksplit=%d grid=(%u,%u,%u)\n", fmt,
@@ -693,7 +768,7 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         return launch_bn<1, 64, 0, 2, 4, 4, 0>(a, p, grid, s);
     }
     if (fmt == 0) {
-        if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 2, 3, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 2, 3, 8, 1, 1>(a, p, grid, s);
+        if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 1, 6, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 1, 6, 8, 1, 1>(a, p, grid, s);
         if (bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 2, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 2, 5, 8, 1, 1>(a, p, grid, s);
         return launch_bn<0, 64, 0, 4, 4, 8, 1>(a, p, grid, s);
     }

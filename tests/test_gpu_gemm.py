@@ -274,3 +274,16 @@ def test_tcgen05_ksplit_token_tiles_and_operand_modes(ks, bn, am):
     check(y_host(Y4), yref, S, "f32", f"q4 ks={ks} bn={bn} am={am}")
     yref8, S8 = oracle_q8(case8)
     check(y_host(Y8), yref8, S8, "bf16", f"q8 ks={ks} bn={bn} am={am}")
+
+
+@pytest.mark.parametrize("K", [128, 384, 640])
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_tcgen05_q8_short_last_round(K, bn):
+    """Q8-row K (a multiple of 128) whose 64-k stages do not fill the last
+    round of decoded slots handed to the MMA thread: the decoder groups without
+    a stage in it still complete the round."""
+    case8 = synth.gemm_q8_case(7300 + K + bn, 200, K, 256, x_dtype="bf16")
+    with ForcePath(2), _Opt(cq.CQ_OPT_TC_BN, bn), _Opt(cq.CQ_OPT_TC_KSPLIT, 1):
+        Y8 = run_q8(case8, "f32")
+    yref8, S8 = oracle_q8(case8)
+    check(y_host(Y8), yref8, S8, "f32", f"q8 K={K} bn={bn}")
