@@ -177,6 +177,10 @@ cq_status cq_set_option(int option, int64_t value) {
             if (value < 0 || value > 2) return fail(CQ_ERR_ARG, "operand mode must be 0, 1 or 2");
             o.tc_amode = value;
             return CQ_OK;
+        case CQ_OPT_TC_PAIR:
+            if (value < 0 || value > 2) return fail(CQ_ERR_ARG, "CTA pair mode must be 0, 1 or 2");
+            o.tc_pair = value;
+            return CQ_OK;
         default:
             return fail(CQ_ERR_ARG, "unknown option %d", option);
     }
@@ -193,6 +197,7 @@ int64_t cq_get_option(int option) {
         case CQ_OPT_TC_BN: return o.tc_bn;
         case CQ_OPT_TC_KSPLIT: return o.tc_ksplit;
         case CQ_OPT_TC_AMODE: return o.tc_amode;
+        case CQ_OPT_TC_PAIR: return o.tc_pair;
         default: return -1;
     }
 }

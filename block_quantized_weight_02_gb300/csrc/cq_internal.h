@@ -22,6 +22,7 @@ struct Options {
     int64_t tc_bn = 0;
     int64_t tc_ksplit = 0;
     int64_t tc_amode = 0;
+    int64_t tc_pair = 0;
 };
 Options& options();
 

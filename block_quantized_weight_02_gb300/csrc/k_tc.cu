@@ -129,11 +129,12 @@ struct Raw<1> { static constexpr int ROW = 64; };   // Q8: 64 bytes per row and 
 // Shared memory per super-slot: X [G][BN rows][128 B] (each chunk one
 // 128-byte-swizzled K-major operand tile), then W [128 rows][G * ROW B]
 // (128- or 64-byte swizzle).  AM 0 adds AS decoded tiles [128][128 B] in
-// front; AM 1 keeps the decoded tiles in tensor memory.
-template <int FMT, int BN, int G, int LSS, int AS, int AM>
+// front; AM 1 keeps the decoded tiles in tensor memory.  With CTA pairs (CG 2)
+// each CTA holds half of the activation rows (its half of the MMA's B operand).
+template <int FMT, int BN, int G, int LSS, int AS, int AM, int CG = 1>
 struct Layout {
     static constexpr int WROW = G * Raw<FMT>::ROW;            // 64 or 128 bytes
-    static constexpr int X_CHUNK = BN * 128;
+    static constexpr int X_CHUNK = (BN / CG) * 128;
     static constexpr int X_BYTES = G * X_CHUNK;
     static constexpr int W_BYTES = BM * WROW;
     static constexpr int SLOT = X_BYTES + W_BYTES;             // multiple of 1024
@@ -141,9 +142,10 @@ struct Layout {
     static constexpr int S_OFF = AM == 0 ? AS * A_BYTES : 0;
     static constexpr int BAR_OFF = S_OFF + LSS * SLOT;
     // Decoded slots are handed over in rounds of RS stages, NRB rounds in flight: four stages
-    // when the ring holds many stages (BN < 256 with tensor-memory slots), else two, so
-    // that a round never waits for ring slots its own MMAs free.
-    static constexpr int RS = (AM == 1 && BN < 256) ? 4 : 2;
+    // when the ring holds many stages (tensor-memory slots with BN < 256, or a CTA pair,
+    // whose half activation tiles leave room for more), else two, so that a round never
+    // waits for ring slots its own MMAs free.
+    static constexpr int RS = (AM == 1 && (BN < 256 || CG == 2)) ? 4 : 2;
     static constexpr int NRB = AS / RS;
     // full[LSS], empty[LSS], afull[NRB], aempty[NRB] (one per round in flight), accf, xchg;
     // then tmem slot, abort, never
@@ -191,11 +193,18 @@ __device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
 // KS: K split over a cluster of KS CTAs along z (1 or 2); the two partial
 // accumulators are exchanged through distributed shared memory and each CTA
 // finishes half of the tile's columns.
-template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS>
+// CG: CTA pairs along x (1 or 2).  With 2, two neighbouring weight-row tiles share
+// one 256-row MMA (cta_group::2): each CTA decodes its 128 rows into its own tensor
+// memory and loads half of the activation rows; the even CTA's MMA thread issues
+// for both once both CTAs' decoders have arrived on its barrier, and every release
+// it commits reaches both CTAs.  Each CTA's accumulator holds its rows x all BN
+// columns, so the epilogue is unchanged.  Cluster ranks run x fastest: the pair
+// peer is rank ^ 1, the K-split partner rank ^ CG.
+template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS, int CG>
 __global__ void __launch_bounds__(THREADS, 1)
 k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
      const __grid_constant__ CUtensorMap tmY, const Params p) {
-    using L = Layout<FMT, BN, G, LSS, AS, AM>;
+    using L = Layout<FMT, BN, G, LSS, AS, AM, CG>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
@@ -204,7 +213,10 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     const int m0 = blockIdx.x * BM;          // first weight row
     const int t0 = blockIdx.y * BN;          // first activation row
     const int kz = KS > 1 ? (int)blockIdx.z : 0;
-    const uint32_t crank = KS > 1 ? cluster_ctarank() : 0u;   // rank in the K-split cluster
+    const uint32_t crank = (KS > 1 || CG > 1) ? cluster_ctarank() : 0u;   // rank in the cluster
+    const int cx = CG > 1 ? (int)(crank & 1u) : 0;                // position in the CTA pair
+    const bool leader = cx == 0;                                   // issues the pair's MMAs
+    const uint16_t pair_mask = (uint16_t)(3u << (crank - (uint32_t)cx));
     const int nk = (int)(p.K / BK) / KS;     // stages of this CTA's k range
     const int k0 = kz * nk;                  // its first stage
     const int ns = nk / G;                   // super-stages
@@ -233,7 +245,9 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             mbar_init(empty_bar(s), 1);  // the MMA's commit after the super-stage's last stage
         }
         for (int rb = 0; rb < NRB; ++rb) {
-            mbar_init(afull_bar(rb), 4 * RS);   // one arrival per warp of each of the round's RS stages
+            // one arrival per warp of each of the round's RS stages; in a pair the even CTA's
+            // barrier also takes the odd CTA's relayed arrival
+            mbar_init(afull_bar(rb), 4 * RS + (CG > 1 && leader ? 1 : 0));
             mbar_init(aempty_bar(rb), 1);       // the MMA's commit of the round
         }
         mbar_init(accf_bar, 1);
@@ -243,11 +257,17 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
-        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
-        tmem_relinquish();
+        if (CG > 1) {
+            tmem_alloc_pair(smem_u32(tmem_slot), L::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (CG > 1) cluster_sync_all();   // the peer's barriers and tensor memory exist before any use
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -285,7 +305,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                     mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::X_BYTES + L::W_BYTES));
                     tma_load_2d(base + L::X_BYTES, &tmW, full_bar(s), (j0 + j) * L::WROW, m0);
                 } else {
-                    tma_load_3d(base, &tmX, full_bar(s), 0, t0, (j0 + j) * G);
+                    tma_load_3d(base, &tmX, full_bar(s), 0, t0 + cx * (BN / CG), (j0 + j) * G);
                 }
             };
             if (!p.stall) {
@@ -323,14 +343,17 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         // decoded slots (their groups had waited for the super-slot, so the activations are
         // in too), eight MMAs, one commit that frees the pair of decoded slots and, at the end
         // of a super-stage, one that frees the super-slot.  Descriptors advance by adding.
-        // A super-slot's release is committed only when a later super-stage waits for it.
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(BM, BN, XBF);
+        // A super-slot's (decoded round's) release is committed only when a later load
+        // (decode) waits for it.  In a CTA pair only the even CTA's thread issues.
+        if (lane == 0 && (CG == 1 || leader)) {
+            constexpr uint32_t idesc = idesc_f16(BM * CG, BN, XBF);
             const int nr = (nk + RS - 1) / RS;     // rounds (the last one may be short)
             int s = 0, u = 0, js = 0;             // super-slot, chunk and super-stage of the next stage
             for (int r = 0; r < nr; ++r) {
                 const int rb = r % NRB;
-                if (!mbar_wait(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag)) {
+                const bool got = CG > 1 ? mbar_wait_cluster_spin(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag)
+                                        : mbar_wait_spin(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag);
+                if (!got) {
                     give_up();
                     break;
                 }
@@ -348,19 +371,41 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                             const uint32_t acc = (kb + kk) != 0 ? 1u : 0u;
                             // +32 bytes of K = +2 in the descriptor's 16-byte address units
                             if (AM == 0) tc_mma_f16(tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
+                            else if (CG > 1) tc_mma_f16_ts_pair(tmem, at + 8u * kk, bd + 2u * kk, idesc, acc);
                             else tc_mma_f16_ts(tmem, at + 8u * kk, bd + 2u * kk, idesc, acc);
                         }
                         if (++u == G) {
                             u = 0;
-                            if (js + LSS < ns) tc_commit(empty_bar(s));   // super-slot free
+                            if (js + LSS < ns) {                         // super-slot free
+                                if (CG > 1) tc_commit_pair_mc(empty_bar(s), pair_mask);
+                                else tc_commit(empty_bar(s));
+                            }
                             ++js;
                             if (++s == LSS) s = 0;
                         }
                     }
                 }
-                tc_commit(aempty_bar(rb));                     // the round's decoded slots free
+                if (r + NRB < nr) {                             // the round's decoded slots free
+                    if (CG > 1) tc_commit_pair_mc(aempty_bar(rb), pair_mask);
+                    else tc_commit(aempty_bar(rb));
+                }
             }
-            tc_commit(accf_bar);   // also lets teardown know every MMA has finished
+            // also lets teardown know every MMA has finished
+            if (CG > 1) tc_commit_pair_mc(accf_bar, pair_mask);
+            else tc_commit(accf_bar);
+        } else if (CG > 1 && lane == 0) {
+            // The odd CTA of a pair relays each round: once its own decoders have arrived,
+            // one arrival (release at cluster scope) on the even CTA's barrier.
+            const int nr = (nk + RS - 1) / RS;
+            const uint32_t peer_afull = mapa_shared(afull_bar(0), crank ^ 1u);
+            for (int r = 0; r < nr; ++r) {
+                const int rb = r % NRB;
+                if (!mbar_wait_spin(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag)) {
+                    give_up();
+                    break;
+                }
+                mbar_arrive_remote(peer_afull + 8u * (uint32_t)rb);
+            }
         }
         __syncwarp();
     } else {
@@ -396,7 +441,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         uint32_t ph = 0;
         bool stop = false;
         for (int j = 0; j < ns && !stop; ++j) {
-          if (!mbar_wait(full_bar(s), ph, p.wait_ns, abort_flag)) {
+          if (!mbar_wait_spin(full_bar(s), ph, p.wait_ns, abort_flag)) {
               give_up();
               break;
           }
@@ -409,11 +454,12 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             const uint32_t rph = (uint32_t)((kb / AS) & 1);    // and their phase
             uint32_t sc_next = 0;
             if (FMT == 0 && row_ok && kb + 8 < nk) sc_next = __ldg(srow + kb + 8);
-            if (!mbar_wait(aempty_bar(rb), rph ^ 1u, p.wait_ns, abort_flag)) {
+            if (!mbar_wait_spin(aempty_bar(rb), rph ^ 1u, p.wait_ns, abort_flag)) {
                 give_up();
                 stop = true;
                 break;
             }
+            tc_fence_after();   // the slot's earlier MMAs (committed by this or the pair's CTA) are done
             const uint32_t wrow = slot_base(s) + (uint32_t)(L::X_BYTES + r * L::WROW);
             // this thread's 64 decoded values (the whole stage for row r), two per word
             uint32_t o[32];
@@ -534,11 +580,11 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         const bool lead = q4w == 0 && lane == 0;     // issues the group's copies and stores
         const int gbar = 2 + grp;                    // the group's named barrier (1 is all decoders)
         if (KS > 1) {
-            const uint32_t partner = crank ^ 1u;
+            const uint32_t partner = crank ^ (uint32_t)CG;
             cluster_sync_all();
             if (threadIdx.x == 0) mbar_arrive_expect_tx(xchg_bar, (uint32_t)(HALF * 128 * 4));
             if (dec) {
-                const int hb = (int)partner * HALF;
+                const int hb = (kz ^ 1) * HALF;         // the columns the partner finishes
                 uint32_t* st = reinterpret_cast<uint32_t*>(smem + SEND_OFF);
 #pragma unroll 1
                 for (int cc = grp * CW; cc < (grp + 1) * CW; cc += CH) {
@@ -557,6 +603,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                 if (!*abort_flag && !mbar_wait(xchg_bar, 0, p.wait_ns, abort_flag)) give_up();
             }
             cluster_arrive_release();
+        } else if (CG > 1) {
+            cluster_arrive_release();   // neither CTA of a pair leaves while the other may still use it
         }
         if (dec) {
             const int64_t n = (int64_t)m0 + r;
@@ -599,7 +647,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             }
             if (lead) bulk_wait_read0();   // the staging memory must stay valid until TMA has read it
         }
-        if (KS > 1) cluster_wait_acquire();
+        if (KS > 1 || CG > 1) cluster_wait_acquire();
     }
 
     // ---- teardown ----
@@ -609,13 +657,15 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         if (*abort_flag && lane == 0) mbar_wait(accf_bar, 0, p.wait_ns, never_flag);  // MMAs done
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, L::TMEM_COLS);
+        if (CG > 1) tmem_dealloc_pair(tmem, L::TMEM_COLS);
+        else tmem_dealloc(tmem, L::TMEM_COLS);
     }
 }
 
-template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS = 1>
+template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS = 1, int CG = 1>
 cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t s) {
-    using L = Layout<FMT, BN, G, LSS, AS, AM>;
+    using L = Layout<FMT, BN, G, LSS, AS, AM, CG>;
+    static_assert(CG == 1 || (CG == 2 && AM == 1 && BN == 256), "CTA pairs: decoded weights in tensor memory, 256 columns");
     static_assert(L::TOTAL <= 232448, "shared memory budget");
     // epilogue staging (f32 at most) below the barriers: split K needs the outgoing and the
     // incoming half and the staged output half; otherwise the staged output tile
@@ -638,11 +688,11 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
             return cudaErrorInvalidValue;
     }
     // activations seen as {64 elements, T rows, K/64 chunks} (strides K*2 B, 128 B): one
-    // box of G chunks of BN rows lands as [chunk][row][128 B], G operand tiles
+    // box of G chunks of BN / CG rows lands as [chunk][row][128 B], G operand tiles
     {
         uint64_t d[3] = {64, (uint64_t)a.T, (uint64_t)a.K / 64};
         uint64_t st[2] = {(uint64_t)a.K * 2, 128};
-        uint32_t box[3] = {64, (uint32_t)BN, (uint32_t)G};
+        uint32_t box[3] = {64, (uint32_t)(BN / CG), (uint32_t)G};
         if (!encode_tiled(&mx, XBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, d,
                           st, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
@@ -658,7 +708,7 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
                           a.y, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
-    auto kern = k_tc<FMT, BN, XBF, G, LSS, AS, AM, KS>;
+    auto kern = k_tc<FMT, BN, XBF, G, LSS, AS, AM, KS, CG>;
     static int configured_device = -1;       // attributes are per device; set once per instantiation
     int dev = 0;
     cudaGetDevice(&dev);
@@ -674,9 +724,10 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (KS > 1) {
+    if (KS > 1 || CG > 1) {
+        if (grid.x % CG != 0) return cudaErrorInvalidValue;
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.x = CG;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = KS;
         ++na;
@@ -696,13 +747,17 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     const int64_t mt = (a.N + BM - 1) / BM;
     const int64_t nk = a.K / BK;
     // One CTA per SM.  Time of a CTA ~ its stages x the measured cost of a 64-k stage
-    // (about 800 / 830 / 940 cycles at BN = 64 / 128 / 256: the MMA issue path and the
-    // loads, not the MMA itself, set it below BN = 256), plus about 6000 cycles for the
-    // exchange when K is split over two CTAs; times the waves.  The cheapest candidate
-    // wins (ties: the earlier, wider one).
+    // (about 800 / 830 cycles at BN = 64 / 128, set by the MMA issue path and the loads;
+    // at BN = 256 about 940 alone and 620 in CTA pairs, whose half activation tiles relieve
+    // the loads), plus about 6000 cycles for the exchange when K is split over two CTAs;
+    // times the waves.  Tiles at least twice as wide as the tokens are not considered.
+    // The cheapest candidate wins (ties: the earlier, wider one).
     int bn = (int)options().tc_bn;
     int ks = (int)options().tc_ksplit;
     const bool ks2_ok = nk % 8 == 0;
+    // 256-column tiles in CTA pairs (one 256-row MMA over two neighbouring row tiles):
+    // an even number of row tiles and decoded weights in tensor memory
+    const bool pair_ok = mt % 2 == 0 && options().tc_amode != 1 && options().tc_pair != 1;
     {
         struct Cand { int bn, ks; };
         const Cand cands[] = {{256, 1}, {256, 2}, {128, 1}, {128, 2}, {64, 1}};
@@ -711,9 +766,10 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         for (const Cand& c : cands) {
             if (bn != 0 && c.bn != bn) continue;
             if (ks != 0 && c.ks != ks) continue;
+            if (bn == 0 && 2 * a.T <= c.bn) continue;   // at least half of every tile's columns unused
             // split only to fill the GPU: when the unsplit tiles leave a quarter of the SMs idle
             if (c.ks == 2 && (!ks2_ok || (ks == 0 && mt * ((a.T + c.bn - 1) / c.bn) * 4 > 3 * num_sms()))) continue;
-            const double stage = c.bn == 256 ? 940.0 : c.bn == 128 ? 830.0 : 800.0;
+            const double stage = c.bn == 256 ? (pair_ok ? 620.0 : 940.0) : c.bn == 128 ? 830.0 : 800.0;
             const int64_t ctas = mt * ((a.T + c.bn - 1) / c.bn) * c.ks;
             const int64_t waves = (ctas + num_sms() - 1) / num_sms();
             const double cost = (double)waves * ((double)(nk / c.ks) * stage + (c.ks > 1 ? 6000.0 : 0.0));
@@ -746,8 +802,9 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     p.y_tma = ((a.N * (a.yt == CQ_F32 ? 4 : 2)) % 16 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0) ? 1 : 0;
     dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), (unsigned)ks);
     if (options().trace)
-        fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d ksplit=%d grid=(%u,%u,%u)\n", fmt,
-                (long long)a.T, (long long)a.N, (long long)a.K, bn, ks, grid.x, grid.y, grid.z);
+        fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d ksplit=%d pair=%d grid=(%u,%u,%u)\n", fmt,
+                (long long)a.T, (long long)a.N, (long long)a.K, bn, ks, (int)(bn == 256 && pair_ok), grid.x, grid.y,
+                grid.z);
     // decoded weight operand: 1 = shared memory, 2 = tensor memory (default)
     const int am = options().tc_amode == 1 ? 0 : 1;
     // <FMT, BN, XBF, G, LSS, AS, AM>: super-stages of G stages (weight rows of 64 or 128
@@ -767,16 +824,20 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         if (bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 3, 4, 0, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 3, 4, 0, 1>(a, p, grid, s);
         return launch_bn<1, 64, 0, 2, 4, 4, 0>(a, p, grid, s);
     }
+    const bool pair = bn == 256 && pair_ok;
     if (fmt == 0) {
+        if (pair) return ks == 2 ? launch_bn<0, 256, 0, 2, 5, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 2, 5, 8, 1, 1, 2>(a, p, grid, s);
         if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 1, 6, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 1, 6, 8, 1, 1>(a, p, grid, s);
         if (bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 2, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 2, 5, 8, 1, 1>(a, p, grid, s);
         return launch_bn<0, 64, 0, 4, 4, 8, 1>(a, p, grid, s);
     }
     if (xbf) {
+        if (pair) return ks == 2 ? launch_bn<1, 256, 1, 2, 4, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 256, 1, 2, 4, 8, 1, 1, 2>(a, p, grid, s);
         if (bn == 256) return ks == 2 ? launch_bn<1, 256, 1, 1, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 256, 1, 1, 5, 8, 1, 1>(a, p, grid, s);
         if (bn == 128) return ks == 2 ? launch_bn<1, 128, 1, 2, 4, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 1, 2, 4, 8, 1, 1>(a, p, grid, s);
         return launch_bn<1, 64, 1, 2, 6, 8, 1>(a, p, grid, s);
     }
+    if (pair) return ks == 2 ? launch_bn<1, 256, 0, 2, 4, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 256, 0, 2, 4, 8, 1, 1, 2>(a, p, grid, s);
     if (bn == 256) return ks == 2 ? launch_bn<1, 256, 0, 1, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 256, 0, 1, 5, 8, 1, 1>(a, p, grid, s);
     if (bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 4, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 4, 8, 1, 1>(a, p, grid, s);
     return launch_bn<1, 64, 0, 2, 6, 8, 1>(a, p, grid, s);

@@ -190,7 +190,10 @@ typedef enum {
     CQ_OPT_TRACE = 4,        /* 1 prints the chosen path and grid of each call to stderr */
     CQ_OPT_TC_BN = 5,        /* tcgen05 token tile: 0 auto (default), or 64, 128, 256 */
     CQ_OPT_TC_KSPLIT = 6,    /* tcgen05 K split over a 2-CTA cluster (partials exchanged in shared memory): 0 auto, 1, 2 */
-    CQ_OPT_TC_AMODE = 7      /* decoded weight operand of the tcgen05 MMA: 0 auto (tensor memory), 1 shared, 2 tensor memory */
+    CQ_OPT_TC_AMODE = 7,     /* decoded weight operand of the tcgen05 MMA: 0 auto (tensor memory), 1 shared, 2 tensor memory */
+    CQ_OPT_TC_PAIR = 8       /* tcgen05, 256-column tiles with decoded weights in tensor memory: 0 auto / 2 on
+                                (neighbouring weight-row tiles share one 256-row MMA on a CTA pair, each CTA
+                                loading half of the activation tile; needs an even number of row tiles), 1 off */
 } cq_option;
 /* Process-wide; returns CQ_ERR_ARG for an unknown option or value. */
 cq_status cq_set_option(int option, int64_t value);

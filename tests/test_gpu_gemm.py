@@ -287,3 +287,26 @@ def test_tcgen05_q8_short_last_round(K, bn):
         Y8 = run_q8(case8, "f32")
     yref8, S8 = oracle_q8(case8)
     check(y_host(Y8), yref8, S8, "f32", f"q8 K={K} bn={bn}")
+
+
+@pytest.mark.parametrize("ks", [1, 2])
+@pytest.mark.parametrize("pair", [1, 2])
+def test_tcgen05_cta_pairs(ks, pair):
+    """256-column tiles with neighbouring weight-row tiles sharing one 256-row
+    MMA on a CTA pair (each CTA decoding its rows into its own tensor memory and
+    loading half of the activation rows) against the unpaired kernel and the
+    oracle: an even number of row tiles with a ragged last one (N=468), a
+    ragged token tile, both weight formats and both activation types."""
+    case4 = synth.gemm_q4_case(7100 + ks, 300, 512, 468, x_dtype="bf16", signed=True)
+    case8 = synth.gemm_q8_case(7200 + ks, 300, 512, 468, x_dtype="f16")
+    case8b = synth.gemm_q8_case(7250 + ks, 300, 512, 468, x_dtype="bf16")
+    with ForcePath(2), _Opt(cq.CQ_OPT_TC_KSPLIT, ks), _Opt(cq.CQ_OPT_TC_BN, 256), _Opt(cq.CQ_OPT_TC_PAIR, pair):
+        Y4, wq = run_q4(case4, "f32")
+        Y8 = run_q8(case8, "bf16")
+        Y8b = run_q8(case8b, "f32")
+    yref, S = oracle_q4(case4, wq)
+    check(y_host(Y4), yref, S, "f32", f"q4 ks={ks} pair={pair}")
+    yref8, S8 = oracle_q8(case8)
+    check(y_host(Y8), yref8, S8, "bf16", f"q8 f16 ks={ks} pair={pair}")
+    yref8b, S8b = oracle_q8(case8b)
+    check(y_host(Y8b), yref8b, S8b, "f32", f"q8 bf16 ks={ks} pair={pair}")
