@@ -145,8 +145,12 @@ struct Layout {
     // when the ring holds many stages (tensor-memory slots with BN < 256, or a CTA pair,
     // whose half activation tiles leave room for more), else two, so that a round never
     // waits for ring slots its own MMAs free.
-    static constexpr int RS = (AM == 1 && (BN < 256 || CG == 2)) ? 4 : 2;
+    static constexpr int RS = (AM == 1 && BN < 256) ? 4 : 2;
     static constexpr int NRB = AS / RS;
+    // When a round is one super-stage, the super-slot's release (committed after the
+    // round's MMAs) also frees the round's decoded slots: the decoders wait on it and no
+    // separate release is committed.  With LSS >= NRB no wait can fall two phases behind.
+    static constexpr bool MERGE = RS == G && LSS >= NRB;
     // full[LSS], empty[LSS], afull[NRB], aempty[NRB] (one per round in flight), accf, xchg;
     // then tmem slot, abort, never
     static constexpr int NBAR = 2 * LSS + 2 * NRB + 2;
@@ -230,6 +234,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     // (r % NRB) RS ..): per round in flight one barrier says the round is decoded, one
     // that its MMAs are done.
     constexpr int RS = L::RS, NRB = L::NRB;
+    constexpr bool MERGE = L::MERGE;
     auto afull_bar = [&](int rb) { return bar0 + 8u * (2 * LSS + rb); };
     auto aempty_bar = [&](int rb) { return bar0 + 8u * (2 * LSS + NRB + rb); };
     const uint32_t accf_bar = bar0 + 8u * (2 * LSS + 2 * NRB);
@@ -376,7 +381,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                         }
                         if (++u == G) {
                             u = 0;
-                            if (js + LSS < ns) {                         // super-slot free
+                            // super-slot free (and, merged, the round's decoded slots)
+                            if (js + (MERGE && NRB < LSS ? NRB : LSS) < ns) {
                                 if (CG > 1) tc_commit_pair_mc(empty_bar(s), pair_mask);
                                 else tc_commit(empty_bar(s));
                             }
@@ -385,7 +391,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                         }
                     }
                 }
-                if (r + NRB < nr) {                             // the round's decoded slots free
+                if (!MERGE && r + NRB < nr) {                   // the round's decoded slots free
                     if (CG > 1) tc_commit_pair_mc(aempty_bar(rb), pair_mask);
                     else tc_commit(aempty_bar(rb));
                 }
@@ -454,7 +460,11 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             const uint32_t rph = (uint32_t)((kb / AS) & 1);    // and their phase
             uint32_t sc_next = 0;
             if (FMT == 0 && row_ok && kb + 8 < nk) sc_next = __ldg(srow + kb + 8);
-            if (!mbar_wait_spin(aempty_bar(rb), rph ^ 1u, p.wait_ns, abort_flag)) {
+            // the slot's previous round (NRB back) must have been consumed
+            const int rp = kb / RS - NRB;
+            const bool freed = MERGE ? (rp < 0 || mbar_wait_spin(empty_bar(rp % LSS), (uint32_t)((rp / LSS) & 1), p.wait_ns, abort_flag))
+                                     : mbar_wait_spin(aempty_bar(rb), rph ^ 1u, p.wait_ns, abort_flag);
+            if (!freed) {
                 give_up();
                 stop = true;
                 break;
@@ -527,7 +537,10 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         for (int kb = nk; kb < (nk + RS - 1) / RS * RS && !stop && !*abort_flag; ++kb) {
             if ((kb & 3) != grp) continue;
             const int rb = (kb / RS) % NRB;
-            if (!mbar_wait(aempty_bar(rb), (uint32_t)(((kb / AS) & 1) ^ 1), p.wait_ns, abort_flag)) {
+            const int rp = kb / RS - NRB;
+            const bool freed = MERGE ? (rp < 0 || mbar_wait(empty_bar(rp % LSS), (uint32_t)((rp / LSS) & 1), p.wait_ns, abort_flag))
+                                     : mbar_wait(aempty_bar(rb), (uint32_t)(((kb / AS) & 1) ^ 1), p.wait_ns, abort_flag);
+            if (!freed) {
                 give_up();
                 break;
             }
