@@ -222,11 +222,11 @@ cq_status cq_gemm_q4(const void* X, int xt, int64_t T, int64_t K, const uint8_t*
     const Q4Ws w = q4_ws(ws, T, K);
     const bool skinny = use_skinny(T);
     if (skinny && T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4: the weight-streaming path serves T <= 32");
-    if ((st = launched(launch_x_half(X, xt, T, K, w.xh, w.rsx, s), "activation guard pass"))) return st;
-    if (skinny) {
-        SkinnyDense a = {w.xh, 0, w.rsx, nullptr, Wq, Ws, T, K, N, Y, yt};
+    if (skinny) {   // the activations as given: no guard pass
+        SkinnyDense a = {X, xt == CQ_BF16 ? 1 : 0, nullptr, nullptr, Wq, Ws, T, K, N, Y, yt};
         return launched(launch_skinny_q4(a, s), "weight-streaming Q4 GEMM");
     }
+    if ((st = launched(launch_x_half(X, xt, T, K, w.xh, w.rsx, s), "activation guard pass"))) return st;
     TcArgs a = {w.xh, 0, w.rsx, nullptr, Wq, Ws, T, K, N, Y, yt};
     return launched(launch_tc_q4(a, s), "tcgen05 Q4 GEMM");
 }

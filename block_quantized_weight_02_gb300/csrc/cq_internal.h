@@ -68,9 +68,9 @@ cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, i
 
 // Weight-streaming (small-T) GEMM.
 struct SkinnyDense {
-    const void* x;       // Q4: guarded fp16 [T][K] in the streaming order; Q8: fp16/bf16 [T][K] as given
+    const void* x;       // fp16/bf16 [T][K] as given (k order)
     int x_bf16;
-    const float* rsx;    // Q4: per-row inverse guard scale [T]
+    const float* rsx;    // unused (no guard on this path)
     const float* rs;     // Q8: row scales [N]
     const uint8_t* wq;   // Q4 nibbles / Q8 int8 bytes
     const uint16_t* ws;  // Q4 scales

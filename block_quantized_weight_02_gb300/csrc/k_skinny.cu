@@ -67,7 +67,9 @@ int take_error_skinny() {
 namespace {
 
 constexpr int CONSUMERS = 8;     // consumer warps, all of them in every stage
-constexpr int THREADS = (CONSUMERS + 1) * 32;
+constexpr int PRODUCER = CONSUMERS;
+constexpr int PERMUTER = CONSUMERS + 1;   // puts activations given in k order into the streaming order
+constexpr int THREADS = (CONSUMERS + 2) * 32;
 
 enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
 
@@ -103,6 +105,11 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<const __half2*>(&v); }
+__device__ __forceinline__ uint32_t bf2_as_u32(__nv_bfloat162 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+__device__ __forceinline__ __nv_bfloat162 u32_as_bf2(uint32_t v) { return *reinterpret_cast<const __nv_bfloat162*>(&v); }
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
@@ -134,6 +141,17 @@ __device__ __forceinline__ void decode_q4_word(uint32_t w, uint32_t d[4]) {
     d[1] = h2_as_u32(__hfma2(u32_as_h2((w & 0x00F000F0u) | 0x64006400u), k16th, km72));
     d[2] = h2_as_u32(__hsub2(u32_as_h2((w8 & 0x000F000Fu) | 0x64006400u), k1032));
     d[3] = h2_as_u32(__hfma2(u32_as_h2((w8 & 0x00F000F0u) | 0x64006400u), k16th, km72));
+}
+
+// The same four pairs as bf16 (for bf16 activations): 0x4300 | n is 128 + n,
+// and 128 + n - 136 is n - 8 with no rounding; the high nibbles are shifted down
+// first (a bf16 has only seven stored mantissa bits).
+__device__ __forceinline__ void decode_q4_word_bf16(uint32_t w, uint32_t d[4]) {
+    const __nv_bfloat162 k136 = u32_as_bf2(0x43084308u);                  // 136
+    d[0] = bf2_as_u32(__hsub2(u32_as_bf2((w & 0x000F000Fu) | 0x43004300u), k136));
+    d[1] = bf2_as_u32(__hsub2(u32_as_bf2(((w >> 4) & 0x000F000Fu) | 0x43004300u), k136));
+    d[2] = bf2_as_u32(__hsub2(u32_as_bf2(((w >> 8) & 0x000F000Fu) | 0x43004300u), k136));
+    d[3] = bf2_as_u32(__hsub2(u32_as_bf2(((w >> 12) & 0x000F000Fu) | 0x43004300u), k136));
 }
 
 // int8 pair (bytes sel of w) -> half2 exactly: (v ^ 0x80) | 0x6400 is
@@ -179,7 +197,10 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_
 // MT: m16 tiles per consumer warp; KW: warp groups along k (the stage's
 // eight 32-k blocks, or 16-k runs, are split over them), so 8 / KW warps
 // cover the stage's RB = 8 / KW * MT * 16 rows.
-template <int FMT, int NT, int MT, int KW, int XBF, int MODE, int NSLOT>
+// RAW: the activations are the caller's rows as given (fp16 or bf16, k order);
+// the permuter warp puts each staged tile into the streaming order in place and
+// no guard scale applies (Q4 dense only).
+template <int FMT, int NT, int MT, int KW, int XBF, int MODE, int NSLOT, int RAW>
 __global__ void __launch_bounds__(THREADS, 2)
 k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
          const __grid_constant__ CUtensorMap tmX, const Params p) {
@@ -187,7 +208,8 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     constexpr int RG = CONSUMERS / KW;        // warps along rows
     constexpr int RB = rows_per_stage(MT, KW);
     static_assert(KW == 1 || KW == 2, "k split over one or two warp groups");
-    static_assert(FMT == 1 || (MT == 1 && XBF == 0), "Q4 stages: one m16 tile per warp, guarded fp16 activations");
+    static_assert(FMT == 1 || (MT == 1 && (XBF == 0 || RAW)), "Q4 stages: one m16 tile per warp; bf16 activations as given");
+    static_assert(RAW == 0 || (FMT == 0 && MODE == DENSE), "activations as given: dense Q4");
     static_assert(MODE == DENSE || RB == 128, "expert panels use 128-row stages");
     using G = StageGeo<FMT, NCOL, RB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -253,19 +275,25 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     constexpr int PART_BYTES = RB * NCOL * 4;
     constexpr int BAR_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
     float* part = reinterpret_cast<float*>(smem + PART_OFF);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // full[NSLOT], empty[NSLOT]
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NSLOT);
+    // full[NSLOT], empty[NSLOT], xfull[NSLOT] (RAW: activation box landed), xready[NSLOT]
+    // (RAW: activations in the streaming order)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * NSLOT);
     volatile int* never_flag = abort_flag + 1;  // stays 0: waits that must not be cut short
 
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t bar_base = smem_u32(bars);
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (NSLOT + s); };
+    auto xfull_bar = [&](int s) { return bar_base + 8u * (2 * NSLOT + s); };
+    auto xready_bar = [&](int s) { return bar_base + 8u * (3 * NSLOT + s); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), CONSUMERS);
+            mbar_init(xfull_bar(s), 1);
+            mbar_init(xready_bar(s), 1);
         }
         *abort_flag = 0;
         *never_flag = 0;
@@ -273,7 +301,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     }
     __syncthreads();
 
-    if (warp == CONSUMERS) {
+    if (warp == PRODUCER) {
         // ================= producers =================
         // Lane s owns ring slot s and issues every copy of the stages that land in it
         // (stage gi goes to slot gi % NSLOT): one thread keeps only a few bulk copies
@@ -308,14 +336,17 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 const int st = st0 + i;
                 // activation rows of this column group (dense: tokens; MoE: grouped pairs)
                 const int xrow0 = (int)(it.col0 + (int64_t)grp * NCOL);
-                tma_load_3d(sbase + (uint32_t)G::X_OFF, &tmX, full_bar(s), 0, st * G::XSL, xrow0);
+                if (RAW) mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)G::X_BYTES);
+                tma_load_3d(sbase + (uint32_t)G::X_OFF, &tmX, RAW ? xfull_bar(s) : full_bar(s), 0, st * G::XSL, xrow0);
             };
+            // bytes of a stage that land on the full barrier (RAW: the activations have their own)
+            constexpr uint32_t FULL_BYTES = RAW ? (uint32_t)G::X_OFF : (uint32_t)G::BYTES;
             // The weights of the first ring fill are requested before waiting for the
             // previous kernel in the stream; the activations follow the wait.
             const bool pre = MODE == DENSE && s < nst;
             if (MODE == DENSE) {
                 if (pre) {                                   // fresh slot: no empty wait needed
-                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)G::BYTES);
+                    mbar_arrive_expect_tx(full_bar(s), FULL_BYTES);
                     load_w(get_item(0), s);
                 }
                 pdl_wait();
@@ -344,7 +375,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(full_bar(s), (uint32_t)G::BYTES);
+                        mbar_arrive_expect_tx(full_bar(s), FULL_BYTES);
                         load_w(it, i);
                         load_x(it, i, grp);
                         last_gi = gi;
@@ -356,8 +387,60 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 *abort_flag = 1;
                 atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
             }
-            if (*abort_flag && last_gi >= 0)   // this lane's last copy must land before the CTA can exit
+            if (*abort_flag && last_gi >= 0) {  // this lane's last copies must land before the CTA can exit
                 mbar_wait(full_bar(s), last_phase, p.wait_ns, never_flag);
+                if (RAW) mbar_wait(xfull_bar(s), last_phase, p.wait_ns, never_flag);
+            }
+        }
+        __syncwarp();
+    } else if (warp == PERMUTER) {
+        // ================= activations into the streaming order (RAW) =================
+        // Inside each 32-element block, chunk wi of the streaming order holds the pairs
+        // (k, k + 2) for k = 4 wi, 16 + 4 wi, 4 wi + 1, 17 + 4 wi.  The staged tile is
+        // [row][64-k slab][128 B] with the 128-byte swizzle (chunk q of line L at q ^ (L % 8));
+        // each lane reads the four chunks of a block and writes the four reordered ones
+        // back to the same places.  The walk over stages is the consumers'.
+        if (RAW) {
+            constexpr int BLOCKS = NCOL * G::XSL * 2;      // 32-element blocks per stage
+            static_assert(BLOCKS % 32 == 0, "whole blocks per lane");
+            uint32_t slot = 0, phase = 0;
+            bool ok = true;
+            for (int i = 0; i < nst && ok; ++i) {
+                if (!mbar_wait_spin(xfull_bar((int)slot), phase, p.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sX = smem_base + slot * (uint32_t)G::BYTES + (uint32_t)G::X_OFF;
+#pragma unroll
+                for (int b = lane; b < BLOCKS; b += 32) {
+                    const uint32_t line = (uint32_t)(b >> 1), h = (uint32_t)(b & 1), sw = line & 7u;
+                    const uint32_t base = sX + line * 128u;
+                    uint4 v[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[q] = lds128a(base + (((4u * h + (uint32_t)q) ^ sw) << 4));
+                    const uint32_t wv[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                                             v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const uint32_t a0 = wv[2 * wi], a1 = wv[2 * wi + 1], b0 = wv[8 + 2 * wi], b1 = wv[9 + 2 * wi];
+                        sts128(base + (((4u * h + (uint32_t)wi) ^ sw) << 4),
+                               make_uint4(prmt(a0, a1, 0x5410u), prmt(b0, b1, 0x5410u), prmt(a0, a1, 0x7632u),
+                                          prmt(b0, b1, 0x7632u)));
+                    }
+                }
+                // the next activation box of this slot is written by TMA (the async proxy)
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xready_bar((int)slot));
+                if (++slot == (uint32_t)NSLOT) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
+            }
         }
         __syncwarp();
     } else {
@@ -390,7 +473,8 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
 
             bool ok = !*abort_flag;
             for (int i = 0; i < nst && ok; ++i) {
-                if (!mbar_wait(full_bar((int)slot), phase, p.wait_ns, abort_flag)) {
+                if (!mbar_wait(full_bar((int)slot), phase, p.wait_ns, abort_flag) ||
+                    (RAW && !mbar_wait_spin(xready_bar((int)slot), phase, p.wait_ns, abort_flag))) {
                     ok = false;
                     *abort_flag = 1;
                     atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
@@ -429,15 +513,25 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                             sb = __half2float(__ushort_as_half((unsigned short)lds16(sS + 128u + 2u * jf)));
                         }
                         uint32_t d[4], e[4];
-                        decode_q4_word(wa, d);
-                        decode_q4_word(wb, e);
+                        if (XBF) {
+                            decode_q4_word_bf16(wa, d);
+                            decode_q4_word_bf16(wb, e);
+                        } else {
+                            decode_q4_word(wa, d);
+                            decode_q4_word(wb, e);
+                        }
                         const uint32_t a1[4] = {d[0], e[0], d[1], e[1]};
                         const uint32_t a2[4] = {d[2], e[2], d[3], e[3]};
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             float pb[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma_16816_f16(pb, a1, bx[nt].x, bx[nt].y);
-                            mma_16816_f16(pb, a2, bx[nt].z, bx[nt].w);
+                            if (XBF) {
+                                mma_16816_bf16(pb, a1, bx[nt].x, bx[nt].y);
+                                mma_16816_bf16(pb, a2, bx[nt].z, bx[nt].w);
+                            } else {
+                                mma_16816_f16(pb, a1, bx[nt].x, bx[nt].y);
+                                mma_16816_f16(pb, a2, bx[nt].z, bx[nt].w);
+                            }
                             acc[0][nt][0] = fmaf(sa, pb[0], acc[0][nt][0]);
                             acc[0][nt][1] = fmaf(sa, pb[1], acc[0][nt][1]);
                             acc[0][nt][2] = fmaf(sb, pb[2], acc[0][nt][2]);
@@ -578,11 +672,17 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 const int lo = rank * per, hi = min(RB * NCOL, lo + per);
                 for (int e = lo + threadIdx.x; e < hi; e += CONSUMERS * 32) {
                     const int r = e & (RB - 1), col = e / RB;
+                    // all ranks' values requested at once, then added in rank order
+                    float v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = q < p.ks ? cluster.map_shared_rank(part, q)[r * NCOL + col] : 0.f;
                     float s = 0.f;
-                    for (int q = 0; q < p.ks; ++q) s += cluster.map_shared_rank(part, q)[r * NCOL + col];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (q < p.ks) s += v[q];
                     const int64_t n = (int64_t)rb * RB + r, t = col;
                     if (n < p.N && t < p.T) {
-                        const float v = s * (FMT == 0 ? p.rsx[t] : p.rs[n]);
+                        const float v = s * (FMT == 0 ? (RAW ? 1.f : p.rsx[t]) : p.rs[n]);
                         if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = v;
                         else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(v);
                     }
@@ -594,7 +694,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 const int r = e & (RB - 1), col = e / RB;
                 const int64_t n = (int64_t)rb * RB + r, t = col;
                 if (n < p.N && t < p.T) {
-                    const float v = part[r * NCOL + col] * (FMT == 0 ? p.rsx[t] : p.rs[n]);
+                    const float v = part[r * NCOL + col] * (FMT == 0 ? (RAW ? 1.f : p.rsx[t]) : p.rs[n]);
                     if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = v;
                     else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(v);
                 }
@@ -610,7 +710,7 @@ constexpr size_t smem_bytes() {
     constexpr int RING = NSLOT * G::BYTES;
     constexpr int PART_BYTES = RB * NCOL * 4;
     constexpr int BAR_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
-    return (size_t)BAR_OFF + 2 * NSLOT * 8 + 16 + 1024;
+    return (size_t)BAR_OFF + 4 * NSLOT * 8 + 16 + 1024;
 }
 
 // Weights [E][R][K bytes] and scales [E][R][K/32], boxes of rows_box rows.
@@ -643,13 +743,13 @@ bool make_xmap(CUtensorMap* mx, const void* x, int64_t rows, int64_t K, int bf16
                         box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int FMT, int NT, int MT, int KW, int XBF, int MODE, int NSLOT>
+template <int FMT, int NT, int MT, int KW, int XBF, int MODE, int NSLOT, int RAW = 0>
 cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, int64_t xrows, const Params& p,
                      dim3 grid, int cluster, cudaStream_t s) {
     constexpr int RB = rows_per_stage(MT, KW);
     CUtensorMap mx;
     if (!make_xmap(&mx, x, xrows, p.K, XBF, 8 * NT, StageGeo<FMT, 8 * NT, RB>::XSL)) return cudaErrorInvalidValue;
-    auto kern = k_skinny<FMT, NT, MT, KW, XBF, MODE, NSLOT>;
+    auto kern = k_skinny<FMT, NT, MT, KW, XBF, MODE, NSLOT, RAW>;
     constexpr size_t smem = smem_bytes<FMT, NT, RB, MODE, NSLOT>();
     static_assert(smem <= 113 * 1024, "two CTAs per SM");
     static int configured_device = -1;       // attributes are per device; set once per instantiation
@@ -692,12 +792,14 @@ DenseCfg dense_cfg(int64_t T) {
     return {4, 1, 2, rows_per_stage(1, 2)};
 }
 
+// Q4 takes the activations as given (RAW): the permuter warp orders them.
 template <int FMT, int XBF>
 cudaError_t launch_dense_nt(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, const Params& p, dim3 grid,
                             int cluster, int64_t T, cudaStream_t s) {
-    if (T <= 8) return launch_t<FMT, 1, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 6>(mw, ms, x, T, p, grid, cluster, s);
-    if (T <= 16) return launch_t<FMT, 2, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 5>(mw, ms, x, T, p, grid, cluster, s);
-    return launch_t<FMT, 4, 1, 2, XBF, DENSE, FMT == 0 ? 4 : 6>(mw, ms, x, T, p, grid, cluster, s);
+    constexpr int RAW = FMT == 0 ? 1 : 0;
+    if (T <= 8) return launch_t<FMT, 1, 1, 1, XBF, DENSE, FMT == 0 ? 5 : 6, RAW>(mw, ms, x, T, p, grid, cluster, s);
+    if (T <= 16) return launch_t<FMT, 2, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 5, RAW>(mw, ms, x, T, p, grid, cluster, s);
+    return launch_t<FMT, 4, 1, 2, XBF, DENSE, FMT == 0 ? 4 : 6, RAW>(mw, ms, x, T, p, grid, cluster, s);
 }
 
 cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
@@ -715,9 +817,11 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     p.yt = a.yt;
     p.wait_ns = (uint64_t)options().wait_ns;
     p.pdl = 1;
+    // K split (cluster size): as many CTAs as fit two per SM (a CTA alone keeps too few
+    // bytes in flight to draw its share of the bandwidth), at least two stages each.
     const int64_t rbs = (a.N + cf.rb - 1) / cf.rb;
     int ks = 1;
-    const int64_t cap = 2 * (int64_t)num_sms();      // two CTAs fit per SM
+    const int64_t cap = 2 * (int64_t)num_sms();
     for (int cand : {2, 4, 8})
         if (rbs * cand <= cap && p.nst_total / cand >= 2) ks = cand;
     p.ks = ks;
@@ -725,7 +829,9 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     if (options().trace)
         fprintf(stderr, "cq: skinny fmt=%d T=%lld N=%lld K=%lld rows/stage=%d grid=(%d,%lld) cluster=%d\n", fmt,
                 (long long)a.T, (long long)a.N, (long long)a.K, cf.rb, ks, (long long)rbs, ks);
-    if (fmt == 0) return launch_dense_nt<0, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
+    if (fmt == 0)
+        return a.x_bf16 ? launch_dense_nt<0, 1>(mw, ms, a.x, p, grid, ks, a.T, s)
+                        : launch_dense_nt<0, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
     return a.x_bf16 ? launch_dense_nt<1, 1>(mw, ms, a.x, p, grid, ks, a.T, s)
                     : launch_dense_nt<1, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
 }

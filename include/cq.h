@@ -72,11 +72,11 @@ typedef enum { CQ_F16 = 0, CQ_BF16 = 1, CQ_F32 = 2 } cq_dtype;
  * power of two and rounded once to yt.  (The guard follows "oxinfer 0.0.5
  * src/metal.rs", MMA_SHADER_SRC header and the x_half shader; the scale
  * folded into the half operand follows mma_tile on the same page.)
- * Arithmetic, T <= 32 (weight-streaming path): the same guarded fp16
- * activations; nibble - 8 is exact in fp16; the products of one 32-k block
- * accumulate in f32 and are multiplied by the block scale (exact in f32)
- * into an f32 sum, which the inverse power of two scales back before the
- * one rounding to yt.
+ * Arithmetic, T <= 32 (weight-streaming path): the activations as given
+ * (fp16 or bf16, no guard); nibble - 8 is exact in either type, so every
+ * product is exact in f32; the products of one 32-k block accumulate in f32
+ * and are multiplied by the block scale into an f32 sum, rounded once to yt.
+ * This path uses no workspace (the argument is still checked).
  * Workspace: cq_gemm_q4_workspace_bytes(T, K) bytes.
  * ------------------------------------------------------------------------- */
 size_t cq_gemm_q4_workspace_bytes(int64_t T, int64_t K);
