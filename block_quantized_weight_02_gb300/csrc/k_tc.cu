@@ -678,16 +678,19 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
 template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS = 1, int CG = 1>
 cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t s) {
     using L = Layout<FMT, BN, G, LSS, AS, AM, CG>;
-    static_assert(CG == 1 || (CG == 2 && AM == 1 && BN == 256), "CTA pairs: decoded weights in tensor memory, 256 columns");
+    static_assert(CG == 1 || (CG == 2 && AM == 1 && BN >= 128), "CTA pairs: decoded weights in tensor memory, 128 or 256 columns");
     static_assert(L::TOTAL <= 232448, "shared memory budget");
     // epilogue staging (f32 at most) below the barriers: split K needs the outgoing and the
     // incoming half and the staged output half; otherwise the staged output tile
     static_assert(L::S_OFF + LSS * L::SLOT >= (KS > 1 ? 3 * (BN / 2) * 128 * 4 : BN * 128 * 4),
                   "epilogue staging fits in the ring memory");
     static_assert(2 * LSS <= 32, "two producer lanes per super-slot");
-    // Group g decodes the stages kb % 4 == g, in rounds of 2 or 4 stages with AS 4 or 8
-    // slots: each round barrier is waited for by fixed groups, every one of its rounds in order.
-    static_assert((AS == 4 || AS == 8) && (G == 1 || G == 2 || G == 4), "decoded slots owned by fixed decoder groups");
+    // Group g decodes the stages kb % 4 == g, in rounds of RS = 2 or 4 stages, NRB = AS / RS
+    // rounds in flight: with RS = 4 every group is in every round; with RS = 2 groups 0, 1
+    // take the even rounds and 2, 3 the odd ones, so NRB must be even.  Either way each
+    // round barrier is waited for by fixed groups, every one of its rounds in order.
+    static_assert(AS % L::RS == 0 && (L::RS == 4 || L::NRB % 2 == 0) && (G == 1 || G == 2 || G == 4),
+                  "decoded slots owned by fixed decoder groups");
     // weights: rows of G stages (G * ROW bytes) per box
     CUtensorMap mw, mx;
     {
@@ -760,11 +763,10 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     const int64_t mt = (a.N + BM - 1) / BM;
     const int64_t nk = a.K / BK;
     // One CTA per SM.  Time of a CTA ~ its stages x the measured cost of a 64-k stage
-    // (about 800 / 830 cycles at BN = 64 / 128, set by the MMA issue path and the loads;
-    // at BN = 256 about 940 alone and 620 in CTA pairs, whose half activation tiles relieve
-    // the loads), plus about 6000 cycles for the exchange when K is split over two CTAs;
-    // times the waves.  Tiles at least twice as wide as the tokens are not considered.
-    // The cheapest candidate wins (ties: the earlier, wider one).
+    // (clock stamps in the kernel: about 520 cycles at BN = 64, 570 at 128 and 800 at 256,
+    // 515 and 690 in CTA pairs), plus about 6000 cycles for the exchange when K is split
+    // over two CTAs; times the waves.  Tiles at least twice as wide as the tokens are not
+    // considered.  The cheapest candidate wins (ties: the earlier, wider one).
     int bn = (int)options().tc_bn;
     int ks = (int)options().tc_ksplit;
     const bool ks2_ok = nk % 8 == 0;
@@ -782,7 +784,7 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
             if (bn == 0 && 2 * a.T <= c.bn) continue;   // at least half of every tile's columns unused
             // split only to fill the GPU: when the unsplit tiles leave a quarter of the SMs idle
             if (c.ks == 2 && (!ks2_ok || (ks == 0 && mt * ((a.T + c.bn - 1) / c.bn) * 4 > 3 * num_sms()))) continue;
-            const double stage = c.bn == 256 ? (pair_ok ? 620.0 : 940.0) : c.bn == 128 ? 830.0 : 800.0;
+            const double stage = c.bn == 256 ? (pair_ok ? 690.0 : 800.0) : c.bn == 128 ? (pair_ok ? 515.0 : 570.0) : 520.0;
             const int64_t ctas = mt * ((a.T + c.bn - 1) / c.bn) * c.ks;
             const int64_t waves = (ctas + num_sms() - 1) / num_sms();
             const double cost = (double)waves * ((double)(nk / c.ks) * stage + (c.ks > 1 ? 6000.0 : 0.0));
@@ -816,7 +818,7 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), (unsigned)ks);
     if (options().trace)
         fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d ksplit=%d pair=%d grid=(%u,%u,%u)\n", fmt,
-                (long long)a.T, (long long)a.N, (long long)a.K, bn, ks, (int)(bn == 256 && pair_ok), grid.x, grid.y,
+                (long long)a.T, (long long)a.N, (long long)a.K, bn, ks, (int)(bn >= 128 && pair_ok), grid.x, grid.y,
                 grid.z);
     // decoded weight operand: 1 = shared memory, 2 = tensor memory (default)
     const int am = options().tc_amode == 1 ? 0 : 1;
@@ -837,23 +839,26 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         if (bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 3, 4, 0, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 3, 4, 0, 1>(a, p, grid, s);
         return launch_bn<1, 64, 0, 2, 4, 4, 0>(a, p, grid, s);
     }
-    const bool pair = bn == 256 && pair_ok;
+    const bool pair = bn >= 128 && pair_ok;
     if (fmt == 0) {
+        if (pair && bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 4, 4, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 4, 4, 12, 1, 1, 2>(a, p, grid, s);
         if (pair) return ks == 2 ? launch_bn<0, 256, 0, 2, 5, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 2, 5, 8, 1, 1, 2>(a, p, grid, s);
         if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 1, 6, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 1, 6, 8, 1, 1>(a, p, grid, s);
-        if (bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 2, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 2, 5, 8, 1, 1>(a, p, grid, s);
-        return launch_bn<0, 64, 0, 4, 4, 8, 1>(a, p, grid, s);
+        if (bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 2, 5, 12, 1, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 2, 5, 12, 1, 1>(a, p, grid, s);
+        return launch_bn<0, 64, 0, 4, 4, 12, 1>(a, p, grid, s);
     }
     if (xbf) {
+        if (pair && bn == 128) return ks == 2 ? launch_bn<1, 128, 1, 2, 6, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 128, 1, 2, 6, 12, 1, 1, 2>(a, p, grid, s);
         if (pair) return ks == 2 ? launch_bn<1, 256, 1, 2, 4, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 256, 1, 2, 4, 8, 1, 1, 2>(a, p, grid, s);
         if (bn == 256) return ks == 2 ? launch_bn<1, 256, 1, 1, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 256, 1, 1, 5, 8, 1, 1>(a, p, grid, s);
-        if (bn == 128) return ks == 2 ? launch_bn<1, 128, 1, 2, 4, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 1, 2, 4, 8, 1, 1>(a, p, grid, s);
-        return launch_bn<1, 64, 1, 2, 6, 8, 1>(a, p, grid, s);
+        if (bn == 128) return ks == 2 ? launch_bn<1, 128, 1, 2, 4, 12, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 1, 2, 4, 12, 1, 1>(a, p, grid, s);
+        return launch_bn<1, 64, 1, 2, 6, 12, 1>(a, p, grid, s);
     }
+    if (pair && bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 6, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 6, 12, 1, 1, 2>(a, p, grid, s);
     if (pair) return ks == 2 ? launch_bn<1, 256, 0, 2, 4, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 256, 0, 2, 4, 8, 1, 1, 2>(a, p, grid, s);
     if (bn == 256) return ks == 2 ? launch_bn<1, 256, 0, 1, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 256, 0, 1, 5, 8, 1, 1>(a, p, grid, s);
-    if (bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 4, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 4, 8, 1, 1>(a, p, grid, s);
-    return launch_bn<1, 64, 0, 2, 6, 8, 1>(a, p, grid, s);
+    if (bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 4, 12, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 4, 12, 1, 1>(a, p, grid, s);
+    return launch_bn<1, 64, 0, 2, 6, 12, 1>(a, p, grid, s);
 }
 
 }  // namespace
