@@ -352,8 +352,17 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         // (decode) waits for it.  In a CTA pair only the even CTA's thread issues.
         if (lane == 0 && (CG == 1 || leader)) {
             constexpr uint32_t idesc = idesc_f16(BM * CG, BN, XBF);
+            // One thread's serial address arithmetic sits between MMAs, so the operand
+            // addresses advance by adding constants: the descriptors' address field is the
+            // shared-memory address in 16-byte units (no carry: addresses stay below 256 KB).
+            const uint64_t bd0 = smem_desc_sw128(slot_base(0));
+            const uint64_t ad0 = AM == 0 ? smem_desc_sw128(sb + L::A_OFF) : 0;
+            const uint32_t at0 = tmem + (uint32_t)L::A_COL;
+            constexpr uint32_t X_STEP = (uint32_t)(L::X_CHUNK >> 4);                      // next chunk
+            constexpr uint32_t S_STEP = (uint32_t)((L::SLOT - (G - 1) * L::X_CHUNK) >> 4); // next super-slot
             const int nr = (nk + RS - 1) / RS;     // rounds (the last one may be short)
             int s = 0, u = 0, js = 0;             // super-slot, chunk and super-stage of the next stage
+            uint32_t boff = 0;                    // its activation tile, 16-byte units from super-slot 0
             for (int r = 0; r < nr; ++r) {
                 const int rb = r % NRB;
                 const bool got = CG > 1 ? mbar_wait_cluster_spin(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag)
@@ -363,14 +372,14 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                     break;
                 }
                 tc_fence_after();
+                const uint32_t a_r = (uint32_t)(rb * RS);   // the round's first decoded slot
 #pragma unroll
                 for (int i = 0; i < RS; ++i) {
                     const int kb = r * RS + i;
                     if (kb < nk) {
-                        const int a = rb * RS + i;
-                        const uint64_t bd = smem_desc_sw128(slot_base(s) + (uint32_t)(u * L::X_CHUNK));
-                        const uint64_t ad = AM == 0 ? smem_desc_sw128(sb + L::A_OFF + a * A_BYTES) : 0;
-                        const uint32_t at = tmem + (uint32_t)(L::A_COL + a * 32);
+                        const uint64_t bd = bd0 + boff;
+                        const uint64_t ad = AM == 0 ? ad0 + (uint64_t)((a_r + (uint32_t)i) * (uint32_t)(A_BYTES >> 4)) : 0;
+                        const uint32_t at = at0 + (a_r + (uint32_t)i) * 32u;
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint32_t acc = (kb + kk) != 0 ? 1u : 0u;
@@ -387,7 +396,14 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                                 else tc_commit(empty_bar(s));
                             }
                             ++js;
-                            if (++s == LSS) s = 0;
+                            if (++s == LSS) {
+                                s = 0;
+                                boff = 0;
+                            } else {
+                                boff += S_STEP;
+                            }
+                        } else {
+                            boff += X_STEP;
                         }
                     }
                 }
