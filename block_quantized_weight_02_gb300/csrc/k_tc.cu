@@ -166,10 +166,14 @@ struct Layout {
 };
 
 // Epilogue geometry: a CTA finishes NC columns of its tile (all BN, or its half under a
-// K split); decoder group g owns NC / 4 of them and handles them CH at a time (one
-// tensor-memory load, one output box, one exchange copy per chunk).
+// K split); each of the first NG decoder groups (all four from 64 columns, else group 0)
+// owns NC / NG of them and handles them CH at a time (one tensor-memory load, one
+// output box, one exchange copy per chunk).
 constexpr int ep_cols(int BN, int KS) { return KS > 1 ? BN / 2 : BN; }
-constexpr int ep_chunk(int BN, int KS) { return ep_cols(BN, KS) / 4 < 32 ? ep_cols(BN, KS) / 4 : 32; }
+constexpr int ep_groups(int BN, int KS) { return ep_cols(BN, KS) >= 64 ? 4 : 1; }
+constexpr int ep_chunk(int BN, int KS) {
+    return ep_cols(BN, KS) / ep_groups(BN, KS) < 32 ? ep_cols(BN, KS) / ep_groups(BN, KS) : 32;
+}
 
 template <int CH>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[CH]) {
@@ -285,7 +289,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     pdl_launch_dependents();
 
     constexpr int NC = ep_cols(BN, KS);      // epilogue: columns this CTA finishes
-    constexpr int CW = NC / 4;               //           columns per decoder group
+    constexpr int NG = ep_groups(BN, KS);    //           decoder groups that take part
+    constexpr int CW = NC / NG;              //           columns per such group
     constexpr int CH = ep_chunk(BN, KS);     //           columns per chunk
     static_assert(CW % 16 == 0 && CW % CH == 0 && CW <= 64, "epilogue chunks");
     const int cbase = kz * NC;               // first column finished here
@@ -571,8 +576,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         pdl_wait();
         if (FMT == 0) {
             const int64_t tb = (int64_t)t0 + cbase + grp * CW;
-            if (lane < CW && tb + lane < p.T) esc0 = p.rsx[tb + lane];
-            if (CW > 32 && tb + 32 + lane < p.T) esc1 = p.rsx[tb + 32 + lane];
+            if (grp < NG && lane < CW && tb + lane < p.T) esc0 = p.rsx[tb + lane];
+            if (grp < NG && CW > 32 && tb + 32 + lane < p.T) esc1 = p.rsx[tb + 32 + lane];
         } else if (row_ok) {
             esc0 = p.rs[n];
         }
@@ -612,7 +617,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             const uint32_t partner = crank ^ (uint32_t)CG;
             cluster_sync_all();
             if (threadIdx.x == 0) mbar_arrive_expect_tx(xchg_bar, (uint32_t)(HALF * 128 * 4));
-            if (dec) {
+            if (dec && grp < NG) {
                 const int hb = (kz ^ 1) * HALF;         // the columns the partner finishes
                 uint32_t* st = reinterpret_cast<uint32_t*>(smem + SEND_OFF);
 #pragma unroll 1
@@ -629,13 +634,13 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                                              sb + SEND_OFF + (uint32_t)(cc * 512), (uint32_t)(CH * 512),
                                              mapa_shared(xchg_bar, partner));
                 }
-                if (!*abort_flag && !mbar_wait(xchg_bar, 0, p.wait_ns, abort_flag)) give_up();
             }
+            if (dec && !*abort_flag && !mbar_wait(xchg_bar, 0, p.wait_ns, abort_flag)) give_up();
             cluster_arrive_release();
         } else if (CG > 1) {
             cluster_arrive_release();   // neither CTA of a pair leaves while the other may still use it
         }
-        if (dec) {
+        if (dec && grp < NG) {
             const int64_t n = (int64_t)m0 + r;
             const bool row_ok = n < p.N;
             const float* recv = reinterpret_cast<const float*>(smem + RECV_OFF);
@@ -694,7 +699,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
 template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS = 1, int CG = 1>
 cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t s) {
     using L = Layout<FMT, BN, G, LSS, AS, AM, CG>;
-    static_assert(CG == 1 || (CG == 2 && AM == 1 && BN >= 128), "CTA pairs: decoded weights in tensor memory, 128 or 256 columns");
+    static_assert(CG == 1 || (CG == 2 && AM == 1 && BN >= 32), "CTA pairs: decoded weights in tensor memory");
     static_assert(L::TOTAL <= 232448, "shared memory budget");
     // epilogue staging (f32 at most) below the barriers: split K needs the outgoing and the
     // incoming half and the staged output half; otherwise the staged output tile
@@ -785,22 +790,25 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     // considered.  The cheapest candidate wins (ties: the earlier, wider one).
     int bn = (int)options().tc_bn;
     int ks = (int)options().tc_ksplit;
+    if (bn == 32 && options().tc_amode == 1) bn = 64;   // 32-column tiles keep decoded weights in tensor memory
     const bool ks2_ok = nk % 8 == 0;
     // 256-column tiles in CTA pairs (one 256-row MMA over two neighbouring row tiles):
     // an even number of row tiles and decoded weights in tensor memory
     const bool pair_ok = mt % 2 == 0 && options().tc_amode != 1 && options().tc_pair != 1;
     {
         struct Cand { int bn, ks; };
-        const Cand cands[] = {{256, 1}, {256, 2}, {128, 1}, {128, 2}, {64, 1}};
+        const Cand cands[] = {{256, 1}, {256, 2}, {128, 1}, {128, 2}, {64, 1}, {32, 1}, {32, 2}};
         double best = -1.0;
         int bbn = 128, bks = 1;
         for (const Cand& c : cands) {
             if (bn != 0 && c.bn != bn) continue;
             if (ks != 0 && c.ks != ks) continue;
-            if (bn == 0 && 2 * a.T <= c.bn) continue;   // at least half of every tile's columns unused
+            if (bn == 0 && 2 * a.T <= c.bn && c.bn > 32) continue;   // at least half of every tile's columns unused
+            if (c.bn == 32 && options().tc_amode == 1) continue;
             // split only to fill the GPU: when the unsplit tiles leave a quarter of the SMs idle
             if (c.ks == 2 && (!ks2_ok || (ks == 0 && mt * ((a.T + c.bn - 1) / c.bn) * 4 > 3 * num_sms()))) continue;
-            const double stage = c.bn == 256 ? (pair_ok ? 690.0 : 800.0) : c.bn == 128 ? (pair_ok ? 515.0 : 570.0) : 520.0;
+            const double stage = c.bn == 256 ? (pair_ok ? 690.0 : 800.0) : c.bn == 128 ? (pair_ok ? 515.0 : 570.0)
+                               : c.bn == 64 ? 520.0 : (pair_ok ? 300.0 : 520.0);
             const int64_t ctas = mt * ((a.T + c.bn - 1) / c.bn) * c.ks;
             const int64_t waves = (ctas + num_sms() - 1) / num_sms();
             const double cost = (double)waves * ((double)(nk / c.ks) * stage + (c.ks > 1 ? 6000.0 : 0.0));
@@ -834,7 +842,7 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), (unsigned)ks);
     if (options().trace)
         fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d ksplit=%d pair=%d grid=(%u,%u,%u)\n", fmt,
-                (long long)a.T, (long long)a.N, (long long)a.K, bn, ks, (int)(bn >= 128 && pair_ok), grid.x, grid.y,
+                (long long)a.T, (long long)a.N, (long long)a.K, bn, ks, (int)((bn >= 128 || bn == 32) && pair_ok), grid.x, grid.y,
                 grid.z);
     // decoded weight operand: 1 = shared memory, 2 = tensor memory (default)
     const int am = options().tc_amode == 1 ? 0 : 1;
@@ -855,8 +863,12 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         if (bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 3, 4, 0, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 3, 4, 0, 1>(a, p, grid, s);
         return launch_bn<1, 64, 0, 2, 4, 4, 0>(a, p, grid, s);
     }
-    const bool pair = bn >= 128 && pair_ok;
+    const bool pair = (bn >= 128 || bn == 32) && pair_ok;
     if (fmt == 0) {
+        if (bn == 32) {
+            if (pair) return ks == 2 ? launch_bn<0, 32, 0, 4, 8, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 32, 0, 4, 8, 12, 1, 1, 2>(a, p, grid, s);
+            return ks == 2 ? launch_bn<0, 32, 0, 4, 6, 12, 1, 2>(a, p, grid, s) : launch_bn<0, 32, 0, 4, 6, 12, 1, 1>(a, p, grid, s);
+        }
         if (pair && bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 4, 4, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 4, 4, 12, 1, 1, 2>(a, p, grid, s);
         if (pair) return ks == 2 ? launch_bn<0, 256, 0, 2, 5, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 2, 5, 8, 1, 1, 2>(a, p, grid, s);
         if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 1, 6, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 1, 6, 8, 1, 1>(a, p, grid, s);
@@ -864,11 +876,19 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         return launch_bn<0, 64, 0, 4, 4, 12, 1>(a, p, grid, s);
     }
     if (xbf) {
+        if (bn == 32) {
+            if (pair) return ks == 2 ? launch_bn<1, 32, 1, 2, 10, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 32, 1, 2, 10, 12, 1, 1, 2>(a, p, grid, s);
+            return ks == 2 ? launch_bn<1, 32, 1, 2, 8, 12, 1, 2>(a, p, grid, s) : launch_bn<1, 32, 1, 2, 8, 12, 1, 1>(a, p, grid, s);
+        }
         if (pair && bn == 128) return ks == 2 ? launch_bn<1, 128, 1, 2, 6, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 128, 1, 2, 6, 12, 1, 1, 2>(a, p, grid, s);
         if (pair) return ks == 2 ? launch_bn<1, 256, 1, 2, 4, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 256, 1, 2, 4, 8, 1, 1, 2>(a, p, grid, s);
         if (bn == 256) return ks == 2 ? launch_bn<1, 256, 1, 1, 5, 8, 1, 2>(a, p, grid, s) : launch_bn<1, 256, 1, 1, 5, 8, 1, 1>(a, p, grid, s);
         if (bn == 128) return ks == 2 ? launch_bn<1, 128, 1, 2, 4, 12, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 1, 2, 4, 12, 1, 1>(a, p, grid, s);
         return launch_bn<1, 64, 1, 2, 6, 12, 1>(a, p, grid, s);
+    }
+    if (bn == 32) {
+        if (pair) return ks == 2 ? launch_bn<1, 32, 0, 2, 10, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 32, 0, 2, 10, 12, 1, 1, 2>(a, p, grid, s);
+        return ks == 2 ? launch_bn<1, 32, 0, 2, 8, 12, 1, 2>(a, p, grid, s) : launch_bn<1, 32, 0, 2, 8, 12, 1, 1>(a, p, grid, s);
     }
     if (pair && bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 6, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 6, 12, 1, 1, 2>(a, p, grid, s);
     if (pair) return ks == 2 ? launch_bn<1, 256, 0, 2, 4, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 256, 0, 2, 4, 8, 1, 1, 2>(a, p, grid, s);

@@ -259,7 +259,7 @@ class _Opt:
 
 @pytest.mark.parametrize("am", [1, 2])
 @pytest.mark.parametrize("ks", [1, 2])
-@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("bn", [32, 64, 128, 256])
 def test_tcgen05_ksplit_token_tiles_and_operand_modes(ks, bn, am):
     """Every token tile, K split (one CTA, or two CTAs of a cluster whose
     partial sums are exchanged in shared memory) and placement of the decoded
@@ -277,7 +277,7 @@ def test_tcgen05_ksplit_token_tiles_and_operand_modes(ks, bn, am):
 
 
 @pytest.mark.parametrize("K", [128, 384, 640])
-@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("bn", [32, 64, 128, 256])
 def test_tcgen05_q8_short_last_round(K, bn):
     """Q8-row K (a multiple of 128) whose 64-k stages do not fill the last
     round of decoded slots handed to the MMA thread: the decoder groups without
@@ -289,24 +289,25 @@ def test_tcgen05_q8_short_last_round(K, bn):
     check(y_host(Y8), yref8, S8, "f32", f"q8 K={K} bn={bn}")
 
 
+@pytest.mark.parametrize("bn", [32, 128, 256])
 @pytest.mark.parametrize("ks", [1, 2])
 @pytest.mark.parametrize("pair", [1, 2])
-def test_tcgen05_cta_pairs(ks, pair):
-    """256-column tiles with neighbouring weight-row tiles sharing one 256-row
-    MMA on a CTA pair (each CTA decoding its rows into its own tensor memory and
+def test_tcgen05_cta_pairs(ks, pair, bn):
+    """32-, 128- and 256-column tiles with neighbouring weight-row tiles sharing
+    one 256-row MMA on a CTA pair (each CTA decoding its rows into its own tensor memory and
     loading half of the activation rows) against the unpaired kernel and the
     oracle: an even number of row tiles with a ragged last one (N=468), a
     ragged token tile, both weight formats and both activation types."""
     case4 = synth.gemm_q4_case(7100 + ks, 300, 512, 468, x_dtype="bf16", signed=True)
     case8 = synth.gemm_q8_case(7200 + ks, 300, 512, 468, x_dtype="f16")
     case8b = synth.gemm_q8_case(7250 + ks, 300, 512, 468, x_dtype="bf16")
-    with ForcePath(2), _Opt(cq.CQ_OPT_TC_KSPLIT, ks), _Opt(cq.CQ_OPT_TC_BN, 256), _Opt(cq.CQ_OPT_TC_PAIR, pair):
+    with ForcePath(2), _Opt(cq.CQ_OPT_TC_KSPLIT, ks), _Opt(cq.CQ_OPT_TC_BN, bn), _Opt(cq.CQ_OPT_TC_PAIR, pair):
         Y4, wq = run_q4(case4, "f32")
         Y8 = run_q8(case8, "bf16")
         Y8b = run_q8(case8b, "f32")
     yref, S = oracle_q4(case4, wq)
-    check(y_host(Y4), yref, S, "f32", f"q4 ks={ks} pair={pair}")
+    check(y_host(Y4), yref, S, "f32", f"q4 ks={ks} pair={pair} bn={bn}")
     yref8, S8 = oracle_q8(case8)
-    check(y_host(Y8), yref8, S8, "bf16", f"q8 f16 ks={ks} pair={pair}")
+    check(y_host(Y8), yref8, S8, "bf16", f"q8 f16 ks={ks} pair={pair} bn={bn}")
     yref8b, S8b = oracle_q8(case8b)
-    check(y_host(Y8b), yref8b, S8b, "f32", f"q8 bf16 ks={ks} pair={pair}")
+    check(y_host(Y8b), yref8b, S8b, "f32", f"q8 bf16 ks={ks} pair={pair} bn={bn}")
