@@ -121,6 +121,25 @@ def _moe_calls(cq, m, dev):
                  h2d=[X, idx, w], d2h=[Y])], touched
 
 
+def _dtype_of(name, info):
+    """The arithmetic each call of the workload runs in: the tcgen05 path (T > 32)
+    multiplies guarded fp16 activations by fp16 weights; the weight-streaming path
+    (T <= 32) multiplies the activations as given (bf16 here, fp16 for the smallest
+    case) by the exact nibble - 8 and scales each 32-k block in f32; Q8-row is
+    bf16 x bf16 (int8 exact); all accumulate in f32."""
+    if name == "moe_panels":
+        return "q4:fp16xfp16->f32"
+    if name == "smallest_q4":
+        return "q4:fp16xfp16->f32"
+    T = info.get("T", 0)
+    q4 = "q4:bf16xbf16->f32" if T <= 32 else "q4:fp16xfp16->f32"
+    if name == "prefill_projection_4096":
+        return q4 + ", q8row:bf16xbf16->f32"
+    if name.startswith("sweep_q8"):
+        return "q8row:bf16xbf16->f32"
+    return q4
+
+
 def build_workload(name, dev):
     import block_quantized_weight_02_gb300 as cq
     from block_quantized_weight_02_gb300 import synth
@@ -391,7 +410,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": "dequant-GEMM TFLOP/s (weight GB/s and roofline fraction alongside)",
         "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "q4:fp16xfp16->f32, q8row:bf16xbf16->f32", "data": "synthetic (seeded)",
+        "vs_baseline": None, "dtype": _dtype_of(args.workload, info), "data": "synthetic (seeded)",
         "config": {"workload": args.workload, **info, "parallelism": f"replicas x{world}",
                    "timing": timing,
                    "l2": f"rotating {sets} input sets ({sets * sum(c.weight_bytes + c.other_bytes for c in calls) / 2**20:.0f} MiB) > L2"},
