@@ -273,8 +273,13 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     constexpr int RING = NSLOT * G::BYTES;
     constexpr int PART_OFF = (MODE == DENSE) ? 0 : RING;
     constexpr int PART_BYTES = RB * NCOL * 4;
-    constexpr int BAR_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
+    // dense: recv [ks][slice] f32, the partial sums the cluster's ranks push to this rank
+    // (a region of its own, so ranks still streaming are never written into)
+    constexpr int RECV_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
+    constexpr int RECV_BYTES = (MODE == DENSE) ? PART_BYTES : 0;
+    constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
     float* part = reinterpret_cast<float*>(smem + PART_OFF);
+    float* recv = reinterpret_cast<float*>(smem + RECV_OFF);
     // full[NSLOT], empty[NSLOT], xfull[NSLOT] (RAW: activation box landed), xready[NSLOT]
     // (RAW: activations in the streaming order)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
@@ -663,23 +668,27 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
         const int rb = blockIdx.y;
         pdl_wait();   // outputs and guard scales only after the previous kernel has finished
         // ---- sum the cluster's partial tiles in rank order, epilogue ----
+        // Rank q finishes slice q of the tile.  Every rank pushes its partial values of
+        // slice q into rank q's recv[rank][.]; after one cluster barrier each rank adds
+        // its slice locally in rank order.
         if (p.ks > 1) {
             cg::cluster_group cluster = cg::this_cluster();
-            cluster.sync();
             const int rank = (int)cluster.block_rank();
+            const int per = (RB * NCOL + p.ks - 1) / p.ks;
             if (warp < CONSUMERS && !*abort_flag) {
-                const int per = (RB * NCOL + p.ks - 1) / p.ks;
+                // element e is (row e % RB, column e / RB), as in the sums below
+                for (int e = threadIdx.x; e < RB * NCOL; e += CONSUMERS * 32) {
+                    const int q = e / per;
+                    cluster.map_shared_rank(recv, q)[rank * per + (e - q * per)] = part[(e & (RB - 1)) * NCOL + e / RB];
+                }
+            }
+            cluster.sync();
+            if (warp < CONSUMERS && !*abort_flag) {
                 const int lo = rank * per, hi = min(RB * NCOL, lo + per);
                 for (int e = lo + threadIdx.x; e < hi; e += CONSUMERS * 32) {
                     const int r = e & (RB - 1), col = e / RB;
-                    // all ranks' values requested at once, then added in rank order
-                    float v[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) v[q] = q < p.ks ? cluster.map_shared_rank(part, q)[r * NCOL + col] : 0.f;
                     float s = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        if (q < p.ks) s += v[q];
+                    for (int q = 0; q < p.ks; ++q) s += recv[q * per + (e - lo)];
                     const int64_t n = (int64_t)rb * RB + r, t = col;
                     if (n < p.N && t < p.T) {
                         const float v = s * (FMT == 0 ? (RAW ? 1.f : p.rsx[t]) : p.rs[n]);
@@ -688,7 +697,6 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                     }
                 }
             }
-            cluster.sync();
         } else if (warp < CONSUMERS && !*abort_flag) {
             for (int e = threadIdx.x; e < RB * NCOL; e += CONSUMERS * 32) {
                 const int r = e & (RB - 1), col = e / RB;
@@ -709,7 +717,8 @@ constexpr size_t smem_bytes() {
     using G = StageGeo<FMT, NCOL, RB>;
     constexpr int RING = NSLOT * G::BYTES;
     constexpr int PART_BYTES = RB * NCOL * 4;
-    constexpr int BAR_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
+    constexpr int RECV_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
+    constexpr int BAR_OFF = RECV_OFF + ((MODE == DENSE) ? PART_BYTES : 0);
     return (size_t)BAR_OFF + 4 * NSLOT * 8 + 16 + 1024;
 }
 
@@ -797,8 +806,8 @@ template <int FMT, int XBF>
 cudaError_t launch_dense_nt(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, const Params& p, dim3 grid,
                             int cluster, int64_t T, cudaStream_t s) {
     constexpr int RAW = FMT == 0 ? 1 : 0;
-    if (T <= 8) return launch_t<FMT, 1, 1, 1, XBF, DENSE, FMT == 0 ? 5 : 6, RAW>(mw, ms, x, T, p, grid, cluster, s);
-    if (T <= 16) return launch_t<FMT, 2, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 5, RAW>(mw, ms, x, T, p, grid, cluster, s);
+    if (T <= 8) return launch_t<FMT, 1, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 5, RAW>(mw, ms, x, T, p, grid, cluster, s);
+    if (T <= 16) return launch_t<FMT, 2, 1, 1, XBF, DENSE, FMT == 0 ? 3 : 5, RAW>(mw, ms, x, T, p, grid, cluster, s);
     return launch_t<FMT, 4, 1, 2, XBF, DENSE, FMT == 0 ? 4 : 6, RAW>(mw, ms, x, T, p, grid, cluster, s);
 }
 
