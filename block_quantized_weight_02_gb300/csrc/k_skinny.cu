@@ -9,30 +9,35 @@
 //    shared-memory ring with TMA, one stage per 256 k (Q4) or 128 k (Q8),
 //    each stage tracked by full/empty mbarriers; producer lane s issues
 //    every copy of ring slot s;
+//  - dense Q4 takes the caller's activations as given (fp16 or bf16, k
+//    order): their box lands on a barrier of its own and a permuter warp
+//    rewrites each 32-element block in place into the order below before
+//    the consumers read it;
 //  - eight consumer warps take part in every stage.  With up to 16
 //    activation columns each warp owns 16 weight rows and the whole stage
 //    (RB = 128); with 32 columns each warp owns 16 rows and half of the
 //    stage's k (RB = 64; the halves are summed in a fixed order at the
 //    end), which halves each warp's activation reads from shared memory.
 // Decoding goes straight from shared memory into mma.sync A fragments:
-//  - Q4 (activations: the guarded fp16 rows, written by the guard pass in
-//    the order below): lane c of a quad decodes word c (bytes 4c .. 4c + 3)
-//    of one 32-k block for its two rows.  Masking the word (and the word
-//    shifted by 8) gives the fp16 pairs 1024 + n (low nibbles) and
-//    1024 + 16 n (high nibbles) of bytes (b0, b2) and (b1, b3); one
-//    subtraction, or one fused multiply-add by 1/16, turns each pair into
-//    n - 8 exactly.  Inside each block the guard pass stores the
-//    activations so that the eight partners of one word are one 16-byte
-//    chunk.  The two MMAs of one block take all 32 k of that block, so
+//  - Q4 (dense: the activations as given, in the activation type; MoE: the
+//    guarded fp16 rows written by the guard passes): lane c of a quad
+//    decodes word c (bytes 4c .. 4c + 3) of one 32-k block for its two rows.
+//    Masking the word (and the word shifted by 8) gives the fp16 pairs
+//    1024 + n (low nibbles) and 1024 + 16 n (high nibbles) of bytes (b0, b2)
+//    and (b1, b3); one subtraction, or one fused multiply-add by 1/16, turns
+//    each pair into n - 8 exactly (bf16: 128 + n from the shifted nibbles,
+//    minus 136).  Inside each block the activations sit so that the eight
+//    partners of one word are one 16-byte chunk (the guard pass or the
+//    permuter warp writes them so).  The two MMAs of one block take all 32 k of that block, so
 //    their f32 result is multiplied by the block scale (exact in f32) into
 //    the running sum: the scale is folded per 32-k block.
 //  - Q8 (activations fp16 or bf16 as given): int8 pairs become fp16
 //    exactly ((v ^ 0x80) | 0x6400 is 1024 + v + 128) or bf16 exactly (low
 //    seven bits and the sign bit go to two bf16 numbers whose difference is
 //    v); the row scale is applied in the epilogue.
-// When K is split across a thread-block cluster, the CTAs' partial tiles
-// are summed in rank order through distributed shared memory, so results
-// are deterministic.
+// When K is split across a thread-block cluster, each rank pushes its
+// partial values into the receive buffer of the rank that finishes them and
+// the sums are taken in rank order, so results are deterministic.
 // Launches overlap through programmatic dependent launch: every CTA lets
 // the next kernel in the stream start as soon as it runs, and the
 // producer requests the weights of its first ring fill before it waits for
@@ -79,7 +84,7 @@ struct Params {
     int ks;               // K split (cluster size)
     int64_t N;            // DENSE: output rows; MoE: rows of one expert matrix
     int64_t T;            // DENSE: activation rows
-    const float* rsx;     // Q4 guard inverse scales per activation row (DENSE / GATEUP)
+    const float* rsx;     // Q4 guard inverse scales per activation row (GATEUP; unused by dense Q4)
     const float* rs;      // Q8 row scales
     void* y;
     int yt;
@@ -666,7 +671,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
 
     if (MODE == DENSE) {
         const int rb = blockIdx.y;
-        pdl_wait();   // outputs and guard scales only after the previous kernel has finished
+        pdl_wait();   // outputs only after the previous kernel has finished
         // ---- sum the cluster's partial tiles in rank order, epilogue ----
         // Rank q finishes slice q of the tile.  Every rank pushes its partial values of
         // slice q into rank q's recv[rank][.]; after one cluster barrier each rank adds
