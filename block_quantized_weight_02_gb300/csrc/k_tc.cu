@@ -15,9 +15,16 @@
 //               the 128-byte swizzled K-major tile in shared memory); four
 //               stages are in decode at once.  Then the epilogue;
 //   warp 17     allocates the tensor memory and issues tcgen05.mma
-//               (M = 128, N = BN, K = 16) from one thread, committing each
-//               stage's decoded slot and each super-stage's load slot back,
-//               and the last stage to the epilogue.
+//               (M = 128, N = BN, K = 16) from one thread, a round of 2 or 4
+//               stages at a time, committing each round's decoded slots and
+//               each super-stage's load slot back, and the last round to the
+//               epilogue.
+// CTA pairs (cta_group::2): two neighbouring weight-row tiles share one MMA
+// of M = 256; each CTA decodes its own rows into its own tensor memory and
+// loads half of the activation rows; the even CTA issues.  K split: two CTAs
+// of a cluster take the two halves of K and exchange half of their f32
+// accumulators through distributed shared memory.  Epilogue: scaled,
+// staged in shared memory and stored with TMA per decoder group and chunk.
 // Q4 decode: (nibble - 8) * fp16 block scale, rounded once to fp16 (the
 // scale folded into the half operand, as in mma_tile of "oxinfer 0.0.5
 // src/metal.rs"); the activations arrive as fp16 behind a per-row
