@@ -116,6 +116,18 @@ def test_options(L):
     cq.cq_set_option(cq.CQ_OPT_SMALL_T_MAX, 16)
     assert cq.cq_get_option(cq.CQ_OPT_SMALL_T_MAX) == 16
     cq.cq_set_option(cq.CQ_OPT_SMALL_T_MAX, old)
+    # tcgen05 tiles, K split, operand placement and CTA pairs
+    for opt, good, bad in [(cq.CQ_OPT_TC_BN, [0, 32, 64, 128, 256], [16, 48, 512]),
+                           (cq.CQ_OPT_TC_KSPLIT, [0, 1, 2], [3, -1]),
+                           (cq.CQ_OPT_TC_AMODE, [0, 1, 2], [3]),
+                           (cq.CQ_OPT_TC_PAIR, [0, 1, 2], [3, -1])]:
+        before = cq.cq_get_option(opt)
+        for v in good:
+            assert cq.lib().cq_set_option(opt, v) == 0, (opt, v)
+            assert cq.cq_get_option(opt) == v
+        for v in bad:
+            assert cq.lib().cq_set_option(opt, v) == 10, (opt, v)
+        cq.cq_set_option(opt, before)
 
 
 def test_packer_matches_oracle_packer():

@@ -311,3 +311,22 @@ def test_tcgen05_cta_pairs(ks, pair, bn):
     check(y_host(Y8), yref8, S8, "bf16", f"q8 f16 ks={ks} pair={pair} bn={bn}")
     yref8b, S8b = oracle_q8(case8b)
     check(y_host(Y8b), yref8b, S8b, "f32", f"q8 bf16 ks={ks} pair={pair} bn={bn}")
+
+
+@pytest.mark.parametrize("T", [1, 8, 17, 32])
+def test_q4_weight_streaming_fp16_activations_at_the_range_edges(T):
+    """The weight-streaming path multiplies the caller's fp16 activations as
+    given (no guard): values near the fp16 maximum, subnormals and zeros,
+    with exact nibble - 8 weights, every product exact in f32."""
+    K, N = 512, 192
+    rng = np.random.default_rng(40 + T)
+    xv = rng.uniform(-1.0, 1.0, (T, K))
+    xv[:, 0::7] *= 60000.0           # near the fp16 maximum (65504)
+    xv[:, 3::11] *= 2.0 ** -20       # fp16 subnormals
+    xv[:, 5::13] = 0.0
+    case = synth.gemm_q4_case(9, T, K, N, x_dtype="f16", signed=True)
+    case["x"] = synth.to_storage(xv, "f16")
+    with ForcePath(1):
+        Y, wq = run_q4(case, "f32")
+    yref, S = oracle_q4(case, wq)
+    check(y_host(Y), yref, S, "f32", f"q4 streaming fp16 edges T={T}")
