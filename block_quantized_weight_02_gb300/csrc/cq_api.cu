@@ -166,7 +166,7 @@ cq_status cq_set_option(int option, int64_t value) {
             o.trace = value != 0;
             return CQ_OK;
         case CQ_OPT_TC_BN:
-            if (value != 0 && value != 32 && value != 64 && value != 128 && value != 256) return fail(CQ_ERR_ARG, "token tile must be 0, 32, 64, 128 or 256");
+            if (value != 0 && value != 32 && value != 64 && value != 128 && value != 192 && value != 256) return fail(CQ_ERR_ARG, "token tile must be 0, 32, 64, 128, 192 or 256");
             o.tc_bn = value;
             return CQ_OK;
         case CQ_OPT_TC_KSPLIT:

@@ -152,7 +152,7 @@ struct Layout {
     // when the ring holds many stages (tensor-memory slots with BN < 256, or a CTA pair,
     // whose half activation tiles leave room for more), else two, so that a round never
     // waits for ring slots its own MMAs free.
-    static constexpr int RS = (AM == 1 && BN < 256) ? 4 : 2;
+    static constexpr int RS = (AM == 1 && BN <= 128) ? 4 : 2;
     static constexpr int NRB = AS / RS;
     // When a round is one super-stage, the super-slot's release (committed after the
     // round's MMAs) also frees the round's decoded slots: the decoders wait on it and no
@@ -179,7 +179,7 @@ struct Layout {
 constexpr int ep_cols(int BN, int KS) { return KS > 1 ? BN / 2 : BN; }
 constexpr int ep_groups(int BN, int KS) { return ep_cols(BN, KS) >= 64 ? 4 : 1; }
 constexpr int ep_chunk(int BN, int KS) {
-    return ep_cols(BN, KS) / ep_groups(BN, KS) < 32 ? ep_cols(BN, KS) / ep_groups(BN, KS) : 32;
+    return (ep_cols(BN, KS) / ep_groups(BN, KS)) % 32 == 0 ? 32 : 16;
 }
 
 template <int CH>
@@ -660,11 +660,13 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                 tmem_ld_cols<CH>(tmem + t_lane + (uint32_t)(cbase + cc), v);
                 tmem_ld_wait();
                 const int64_t tb = (int64_t)t0 + cbase + cc;
-                const float escq = ci == 0 ? esc0 : esc1;
                 const bool skip = *abort_flag != 0;
 #pragma unroll
                 for (int jj = 0; jj < CH; ++jj) {
-                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, escq, jj) : esc0;
+                    // column ci CH + jj of the group: its scale sits in lane (column % 32) of esc0
+                    // (columns 0..31) or esc1 (32..63)
+                    const int gc = ci * CH + jj;
+                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, gc < 32 ? esc0 : esc1, gc & 31) : esc0;
                     float acc = __uint_as_float(v[jj]);
                     if (KS > 1) acc += recv[(cc + jj) * 128 + r];
                     const float val = acc * sx;
@@ -792,19 +794,22 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     const int64_t nk = a.K / BK;
     // One CTA per SM.  Time of a CTA ~ its stages x the measured cost of a 64-k stage
     // (clock stamps in the kernel: about 520 cycles at BN = 64, 570 at 128 and 800 at 256,
-    // 515 and 690 in CTA pairs), plus about 6000 cycles for the exchange when K is split
+    // 515, 680 and 690 in CTA pairs at 128, 192 and 256; 192-column pairs fill the SMs
+    // where 256-column tiles leave a third idle), plus about 6000 cycles for the exchange when K is split
     // over two CTAs; times the waves.  Tiles at least twice as wide as the tokens are not
     // considered.  The cheapest candidate wins (ties: the earlier, wider one).
     int bn = (int)options().tc_bn;
     int ks = (int)options().tc_ksplit;
     if (bn == 32 && options().tc_amode == 1) bn = 64;   // 32-column tiles keep decoded weights in tensor memory
+    if (bn == 192 && !(mt % 2 == 0 && options().tc_amode != 1 && options().tc_pair != 1)) bn = 256;   // pairs only
+    if (bn == 192 && options().tc_ksplit == 2) ks = 1;                                                 // no K split
     const bool ks2_ok = nk % 8 == 0;
     // 256-column tiles in CTA pairs (one 256-row MMA over two neighbouring row tiles):
     // an even number of row tiles and decoded weights in tensor memory
     const bool pair_ok = mt % 2 == 0 && options().tc_amode != 1 && options().tc_pair != 1;
     {
         struct Cand { int bn, ks; };
-        const Cand cands[] = {{256, 1}, {256, 2}, {128, 1}, {128, 2}, {64, 1}, {32, 1}, {32, 2}};
+        const Cand cands[] = {{256, 1}, {256, 2}, {192, 1}, {128, 1}, {128, 2}, {64, 1}, {32, 1}, {32, 2}};
         double best = -1.0;
         int bbn = 128, bks = 1;
         for (const Cand& c : cands) {
@@ -814,8 +819,10 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
             if (c.bn == 32 && options().tc_amode == 1) continue;
             // split only to fill the GPU: when the unsplit tiles leave a quarter of the SMs idle
             if (c.ks == 2 && (!ks2_ok || (ks == 0 && mt * ((a.T + c.bn - 1) / c.bn) * 4 > 3 * num_sms()))) continue;
-            const double stage = c.bn == 256 ? (pair_ok ? 690.0 : 800.0) : c.bn == 128 ? (pair_ok ? 515.0 : 570.0)
-                               : c.bn == 64 ? 520.0 : (pair_ok ? 300.0 : 520.0);
+            if (c.bn == 192 && c.ks != 1) continue;
+            if (c.bn == 192 && !pair_ok) continue;   // 192-column tiles only in CTA pairs
+            const double stage = c.bn == 256 ? (pair_ok ? 690.0 : 800.0) : c.bn == 192 ? 680.0
+                               : c.bn == 128 ? (pair_ok ? 515.0 : 570.0) : c.bn == 64 ? 520.0 : (pair_ok ? 300.0 : 520.0);
             const int64_t ctas = mt * ((a.T + c.bn - 1) / c.bn) * c.ks;
             const int64_t waves = (ctas + num_sms() - 1) / num_sms();
             const double cost = (double)waves * ((double)(nk / c.ks) * stage + (c.ks > 1 ? 6000.0 : 0.0));
@@ -872,6 +879,7 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     }
     const bool pair = (bn >= 128 || bn == 32) && pair_ok;
     if (fmt == 0) {
+        if (bn == 192) return launch_bn<0, 192, 0, 2, 6, 8, 1, 1, 2>(a, p, grid, s);
         if (bn == 32) {
             if (pair) return ks == 2 ? launch_bn<0, 32, 0, 4, 8, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 32, 0, 4, 8, 12, 1, 1, 2>(a, p, grid, s);
             return ks == 2 ? launch_bn<0, 32, 0, 4, 6, 12, 1, 2>(a, p, grid, s) : launch_bn<0, 32, 0, 4, 6, 12, 1, 1>(a, p, grid, s);
@@ -883,6 +891,7 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         return launch_bn<0, 64, 0, 4, 4, 12, 1>(a, p, grid, s);
     }
     if (xbf) {
+        if (bn == 192) return launch_bn<1, 192, 1, 2, 5, 8, 1, 1, 2>(a, p, grid, s);
         if (bn == 32) {
             if (pair) return ks == 2 ? launch_bn<1, 32, 1, 2, 10, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 32, 1, 2, 10, 12, 1, 1, 2>(a, p, grid, s);
             return ks == 2 ? launch_bn<1, 32, 1, 2, 8, 12, 1, 2>(a, p, grid, s) : launch_bn<1, 32, 1, 2, 8, 12, 1, 1>(a, p, grid, s);
@@ -893,6 +902,7 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         if (bn == 128) return ks == 2 ? launch_bn<1, 128, 1, 2, 4, 12, 1, 2>(a, p, grid, s) : launch_bn<1, 128, 1, 2, 4, 12, 1, 1>(a, p, grid, s);
         return launch_bn<1, 64, 1, 2, 6, 12, 1>(a, p, grid, s);
     }
+    if (bn == 192) return launch_bn<1, 192, 0, 2, 5, 8, 1, 1, 2>(a, p, grid, s);
     if (bn == 32) {
         if (pair) return ks == 2 ? launch_bn<1, 32, 0, 2, 10, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<1, 32, 0, 2, 10, 12, 1, 1, 2>(a, p, grid, s);
         return ks == 2 ? launch_bn<1, 32, 0, 2, 8, 12, 1, 2>(a, p, grid, s) : launch_bn<1, 32, 0, 2, 8, 12, 1, 1>(a, p, grid, s);

@@ -188,7 +188,7 @@ typedef enum {
     CQ_OPT_WAIT_NS = 2,      /* time limit of every device pipeline wait, ns (default 1e9) */
     CQ_OPT_TEST_STALL = 3,   /* test only: 1 makes the next tcgen05 launch's loader issue nothing */
     CQ_OPT_TRACE = 4,        /* 1 prints the chosen path and grid of each call to stderr */
-    CQ_OPT_TC_BN = 5,        /* tcgen05 token tile: 0 auto (default), or 32, 64, 128, 256 */
+    CQ_OPT_TC_BN = 5,        /* tcgen05 token tile: 0 auto (default), or 32, 64, 128, 192 (CTA pairs only, no K split), 256 */
     CQ_OPT_TC_KSPLIT = 6,    /* tcgen05 K split over a 2-CTA cluster (partials exchanged in shared memory): 0 auto, 1, 2 */
     CQ_OPT_TC_AMODE = 7,     /* decoded weight operand of the tcgen05 MMA: 0 auto (tensor memory), 1 shared, 2 tensor memory */
     CQ_OPT_TC_PAIR = 8       /* tcgen05, 256-column tiles with decoded weights in tensor memory: 0 auto / 2 on

@@ -117,7 +117,7 @@ def test_options(L):
     assert cq.cq_get_option(cq.CQ_OPT_SMALL_T_MAX) == 16
     cq.cq_set_option(cq.CQ_OPT_SMALL_T_MAX, old)
     # tcgen05 tiles, K split, operand placement and CTA pairs
-    for opt, good, bad in [(cq.CQ_OPT_TC_BN, [0, 32, 64, 128, 256], [16, 48, 512]),
+    for opt, good, bad in [(cq.CQ_OPT_TC_BN, [0, 32, 64, 128, 192, 256], [16, 48, 512]),
                            (cq.CQ_OPT_TC_KSPLIT, [0, 1, 2], [3, -1]),
                            (cq.CQ_OPT_TC_AMODE, [0, 1, 2], [3]),
                            (cq.CQ_OPT_TC_PAIR, [0, 1, 2], [3, -1])]:

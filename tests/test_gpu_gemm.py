@@ -289,12 +289,12 @@ def test_tcgen05_q8_short_last_round(K, bn):
     check(y_host(Y8), yref8, S8, "f32", f"q8 K={K} bn={bn}")
 
 
-@pytest.mark.parametrize("bn", [32, 128, 256])
+@pytest.mark.parametrize("bn", [32, 128, 192, 256])
 @pytest.mark.parametrize("ks", [1, 2])
 @pytest.mark.parametrize("pair", [1, 2])
 def test_tcgen05_cta_pairs(ks, pair, bn):
-    """32-, 128- and 256-column tiles with neighbouring weight-row tiles sharing
-    one 256-row MMA on a CTA pair (each CTA decoding its rows into its own tensor memory and
+    """32-, 128-, 192- and 256-column tiles with neighbouring weight-row tiles
+    sharing one 256-row MMA on a CTA pair (192 columns: pairs only, no K split) (each CTA decoding its rows into its own tensor memory and
     loading half of the activation rows) against the unpaired kernel and the
     oracle: an even number of row tiles with a ragged last one (N=468), a
     ragged token tile, both weight formats and both activation types."""
