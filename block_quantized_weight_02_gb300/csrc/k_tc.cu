@@ -158,9 +158,9 @@ struct Layout {
     // round's MMAs) also frees the round's decoded slots: the decoders wait on it and no
     // separate release is committed.  With LSS >= NRB no wait can fall two phases behind.
     static constexpr bool MERGE = RS == G && LSS >= NRB;
-    // full[LSS], empty[LSS], afull[NRB], aempty[NRB] (one per round in flight), accf, xchg;
-    // then tmem slot, abort, never
-    static constexpr int NBAR = 2 * LSS + 2 * NRB + 2;
+    // full[LSS], empty[LSS], afull[NRB], aempty[NRB] (one per round in flight), accf,
+    // xchg[4] (split K: one per decoder group); then tmem slot, abort, never
+    static constexpr int NBAR = 2 * LSS + 2 * NRB + 5;
     static constexpr int MISC = NBAR * 8 + 16;
     static constexpr int TOTAL = BAR_OFF + MISC + 1024;  // + alignment slack
     // tensor memory: accumulator in columns [0, BN); AM 1 adds AS decoded A tiles of 32 columns
@@ -249,7 +249,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     auto afull_bar = [&](int rb) { return bar0 + 8u * (2 * LSS + rb); };
     auto aempty_bar = [&](int rb) { return bar0 + 8u * (2 * LSS + NRB + rb); };
     const uint32_t accf_bar = bar0 + 8u * (2 * LSS + 2 * NRB);
-    const uint32_t xchg_bar = accf_bar + 8u;   // split K: the partner's half has arrived
+    // split K: the partner's columns of decoder group g have arrived
+    auto xchg_bar = [&](int g) { return accf_bar + 8u + 8u * (uint32_t)g; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never_flag = abort_flag + 1;
@@ -267,7 +268,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
             mbar_init(aempty_bar(rb), 1);       // the MMA's commit of the round
         }
         mbar_init(accf_bar, 1);
-        mbar_init(xchg_bar, 1);
+        for (int g = 0; g < 4; ++g) mbar_init(xchg_bar(g), 1);
         *abort_flag = 0;
         *never_flag = 0;
         fence_mbar_init();
@@ -604,9 +605,10 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     // idle; the CTA of k half z finishes columns [z BN/2, (z + 1) BN/2).  Each stages the other half of
     // its accumulator ([column][128 rows] f32) chunk by chunk, and the group's first
     // thread copies each chunk in bulk into the partner, completing on the partner's
-    // exchange barrier.  The sum is own + partner (a + b, the same in both orders).  A
-    // CTA arrives on a second cluster barrier once the partner's half is in and waits on
-    // it before exiting, so no copy still reads the memory of a CTA that has left.
+    // exchange barrier of the same group, so each group finishes as soon as its own
+    // columns are in.  The sum is own + partner (a + b, the same in both orders).  A
+    // thread arrives on a second cluster barrier once its group's columns are in and
+    // waits on it before exiting, so no copy still reads the memory of a CTA that has left.
     // Barriers are taken by every decoder warp whatever the abort flag; only the copies
     // and stores are skipped after a timeout.
     {
@@ -623,7 +625,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         if (KS > 1) {
             const uint32_t partner = crank ^ (uint32_t)CG;
             cluster_sync_all();
-            if (threadIdx.x == 0) mbar_arrive_expect_tx(xchg_bar, (uint32_t)(HALF * 128 * 4));
+            // each group receives the partner's values of its own CW columns
+            if (dec && grp < NG && lead) mbar_arrive_expect_tx(xchg_bar(grp), (uint32_t)(CW * 128 * 4));
             if (dec && grp < NG) {
                 const int hb = (kz ^ 1) * HALF;         // the columns the partner finishes
                 uint32_t* st = reinterpret_cast<uint32_t*>(smem + SEND_OFF);
@@ -639,10 +642,10 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                     if (lead && !*abort_flag)
                         bulk_copy_to_cluster(mapa_shared(sb + RECV_OFF + (uint32_t)(cc * 512), partner),
                                              sb + SEND_OFF + (uint32_t)(cc * 512), (uint32_t)(CH * 512),
-                                             mapa_shared(xchg_bar, partner));
+                                             mapa_shared(xchg_bar(grp), partner));
                 }
+                if (!*abort_flag && !mbar_wait(xchg_bar(grp), 0, p.wait_ns, abort_flag)) give_up();
             }
-            if (dec && !*abort_flag && !mbar_wait(xchg_bar, 0, p.wait_ns, abort_flag)) give_up();
             cluster_arrive_release();
         } else if (CG > 1) {
             cluster_arrive_release();   // neither CTA of a pair leaves while the other may still use it
