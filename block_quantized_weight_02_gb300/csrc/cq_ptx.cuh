@@ -383,6 +383,52 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_bf16) {
            | ((uint32_t)(M >> 4) << 24);              // M / 16
 }
 
+// ---- packed 16-bit conversions ------------------------------------------
+// Written as single PTX instructions: the same expressions in C++ (a shift, an
+// AND and an OR of constants, the half / bfloat16 intrinsics) compile to more
+// instructions, and the weight decoders issue these for every weight.
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+// (a & MASK) | c in one lop3 (truth table 0xEA = (x & y) | z).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "n"(MASK), "r"(c));
+    return r;
+}
+// a & MASK in one lop3 (truth table 0xC0 = x & y).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_mask(uint32_t a) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, 0, 0xC0;" : "=r"(r) : "r"(a), "n"(MASK));
+    return r;
+}
+// Round-to-nearest packed arithmetic on two fp16 / bf16 values per register.
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t fma_f16x2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // ---- legacy warp MMA (weight-streaming path) ----------------------------
 // A pure function of its registers: not volatile, so the compiler may move
 // it among the (volatile) shared-memory loads of the next step.

@@ -103,15 +103,6 @@ struct Params {
     int rbs;              // MoE: row blocks per expert matrix
 };
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
-__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<const __half2*>(&v); }
-__device__ __forceinline__ uint32_t bf2_as_u32(__nv_bfloat162 h) { return *reinterpret_cast<const uint32_t*>(&h); }
-__device__ __forceinline__ __nv_bfloat162 u32_as_bf2(uint32_t v) { return *reinterpret_cast<const __nv_bfloat162*>(&v); }
 __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
@@ -138,42 +129,36 @@ __device__ __forceinline__ uint32_t lds16(uint32_t a) {
 // 0x6400 | n is 1024 + n and 0x6400 | (n << 4) is 1024 + 16 n; 1024 + n - 1032
 // and (1024 + 16 n) / 16 - 72 are both n - 8 with no rounding.
 __device__ __forceinline__ void decode_q4_word(uint32_t w, uint32_t d[4]) {
-    const __half2 k1032 = u32_as_h2(0x64086408u);               // 1032
-    const __half2 k16th = u32_as_h2(0x2C002C00u);               // 1/16
-    const __half2 km72 = u32_as_h2(0xD480D480u);                // -72
+    const uint32_t c6400 = 0x64006400u, k1032 = 0x64086408u, k16th = 0x2C002C00u, km72 = 0xD480D480u;
     const uint32_t w8 = w >> 8;
-    d[0] = h2_as_u32(__hsub2(u32_as_h2((w & 0x000F000Fu) | 0x64006400u), k1032));
-    d[1] = h2_as_u32(__hfma2(u32_as_h2((w & 0x00F000F0u) | 0x64006400u), k16th, km72));
-    d[2] = h2_as_u32(__hsub2(u32_as_h2((w8 & 0x000F000Fu) | 0x64006400u), k1032));
-    d[3] = h2_as_u32(__hfma2(u32_as_h2((w8 & 0x00F000F0u) | 0x64006400u), k16th, km72));
+    d[0] = sub_f16x2(and_or<0x000F000Fu>(w, c6400), k1032);
+    d[1] = fma_f16x2(and_or<0x00F000F0u>(w, c6400), k16th, km72);
+    d[2] = sub_f16x2(and_or<0x000F000Fu>(w8, c6400), k1032);
+    d[3] = fma_f16x2(and_or<0x00F000F0u>(w8, c6400), k16th, km72);
 }
 
 // The same four pairs as bf16 (for bf16 activations): 0x4300 | n is 128 + n,
 // and 128 + n - 136 is n - 8 with no rounding; the high nibbles are shifted down
 // first (a bf16 has only seven stored mantissa bits).
 __device__ __forceinline__ void decode_q4_word_bf16(uint32_t w, uint32_t d[4]) {
-    const __nv_bfloat162 k136 = u32_as_bf2(0x43084308u);                  // 136
-    d[0] = bf2_as_u32(__hsub2(u32_as_bf2((w & 0x000F000Fu) | 0x43004300u), k136));
-    d[1] = bf2_as_u32(__hsub2(u32_as_bf2(((w >> 4) & 0x000F000Fu) | 0x43004300u), k136));
-    d[2] = bf2_as_u32(__hsub2(u32_as_bf2(((w >> 8) & 0x000F000Fu) | 0x43004300u), k136));
-    d[3] = bf2_as_u32(__hsub2(u32_as_bf2(((w >> 12) & 0x000F000Fu) | 0x43004300u), k136));
+    const uint32_t c4300 = 0x43004300u, k136 = 0x43084308u;
+    d[0] = sub_bf16x2(and_or<0x000F000Fu>(w, c4300), k136);
+    d[1] = sub_bf16x2(and_or<0x000F000Fu>(w >> 4, c4300), k136);
+    d[2] = sub_bf16x2(and_or<0x000F000Fu>(w >> 8, c4300), k136);
+    d[3] = sub_bf16x2(and_or<0x000F000Fu>(w >> 12, c4300), k136);
 }
 
 // int8 pair (bytes sel of w) -> half2 exactly: (v ^ 0x80) | 0x6400 is
 // 1024 + v + 128; subtracting 1152 leaves v.
 __device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t wx /* w ^ 0x80808080 */, uint32_t sel) {
-    const uint32_t h = prmt(wx, 0x64646464u, sel);
-    return h2_as_u32(__hsub2(u32_as_h2(h), u32_as_h2(0x64806480u)));
+    return sub_f16x2(prmt(wx, 0x64646464u, sel), 0x64806480u);
 }
 // int8 pair (bytes sel of w) -> bf16x2 exactly: with 0x43 as the high byte,
 // the low seven bits of v give 128 + (v & 127) and the sign bit gives 128 or
 // 256 (0x4300 / 0x4380); their difference is v, an integer bf16 holds exactly.
 __device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
     const uint32_t t = prmt(w, 0x43434343u, sel);
-    const uint32_t lo = t & 0xFF7FFF7Fu, hi = t & 0xFF80FF80u;
-    const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&lo),
-                                     *reinterpret_cast<const __nv_bfloat162*>(&hi));
-    return *reinterpret_cast<const uint32_t*>(&r);
+    return sub_bf16x2(and_mask<0xFF7FFF7Fu>(t), and_mask<0xFF80FF80u>(t));
 }
 
 // One stage in shared memory, filled by three TMA copies (five for gate/up):

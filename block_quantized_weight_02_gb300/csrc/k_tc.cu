@@ -74,16 +74,8 @@ struct Params {
     int y_tma; // Y row pitch is a multiple of 16 bytes: tiles leave through a TMA store
 };
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
 __device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t w, uint32_t sel) {
-    const uint32_t h = prmt(w ^ 0x80808080u, 0x64646464u, sel);
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h),
-                              __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
-    return *reinterpret_cast<const uint32_t*>(&r);
+    return sub_f16x2(prmt(w ^ 0x80808080u, 0x64646464u, sel), 0x64806480u);
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -94,32 +86,18 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
-    uint2 v;
-    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-    return v;
-}
 // Eight nibbles (bytes b0..b3 of w) -> four fp16 pairs (n - 8) * scale, each
 // rounded once, in the activations' streaming order: (low b0, low b2),
 // (high b0, high b2), (low b1, low b3), (high b1, high b3).  0x6400 | n is
 // 1024 + n and 0x6400 | (n << 4) is 1024 + 16 n; 1024 + n - 1032 and
 // (1024 + 16 n) / 16 - 72 are n - 8 exactly.
-__device__ __forceinline__ void decode_q4_word_scaled(uint32_t w, __half2 sc, uint32_t* o) {
-    const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
-    const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
-    const __half2 km72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));
+__device__ __forceinline__ void decode_q4_word_scaled(uint32_t w, uint32_t sc, uint32_t* o) {
+    const uint32_t c6400 = 0x64006400u, k1032 = 0x64086408u, k16th = 0x2C002C00u, km72 = 0xD480D480u;
     const uint32_t w8 = w >> 8;
-    const uint32_t l02 = (w & 0x000F000Fu) | 0x64006400u, h02 = (w & 0x00F000F0u) | 0x64006400u;
-    const uint32_t l13 = (w8 & 0x000F000Fu) | 0x64006400u, h13 = (w8 & 0x00F000F0u) | 0x64006400u;
-    const __half2 d0 = __hsub2(*reinterpret_cast<const __half2*>(&l02), k1032);
-    const __half2 d1 = __hfma2(*reinterpret_cast<const __half2*>(&h02), k16th, km72);
-    const __half2 d2 = __hsub2(*reinterpret_cast<const __half2*>(&l13), k1032);
-    const __half2 d3 = __hfma2(*reinterpret_cast<const __half2*>(&h13), k16th, km72);
-    const __half2 r0 = __hmul2(d0, sc), r1 = __hmul2(d1, sc), r2 = __hmul2(d2, sc), r3 = __hmul2(d3, sc);
-    o[0] = *reinterpret_cast<const uint32_t*>(&r0);
-    o[1] = *reinterpret_cast<const uint32_t*>(&r1);
-    o[2] = *reinterpret_cast<const uint32_t*>(&r2);
-    o[3] = *reinterpret_cast<const uint32_t*>(&r3);
+    o[0] = mul_f16x2(sub_f16x2(and_or<0x000F000Fu>(w, c6400), k1032), sc);
+    o[1] = mul_f16x2(fma_f16x2(and_or<0x00F000F0u>(w, c6400), k16th, km72), sc);
+    o[2] = mul_f16x2(sub_f16x2(and_or<0x000F000Fu>(w8, c6400), k1032), sc);
+    o[3] = mul_f16x2(fma_f16x2(and_or<0x00F000F0u>(w8, c6400), k16th, km72), sc);
 }
 
 template <int FMT>
@@ -199,10 +177,7 @@ constexpr int MMA_WARP = DEC_WARPS + 1;
 // (0x4300 / 0x4380); their difference is v, an integer bf16 holds exactly.
 __device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
     const uint32_t t = prmt(w, 0x43434343u, sel);
-    const uint32_t lo = t & 0xFF7FFF7Fu, hi = t & 0xFF80FF80u;
-    const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&lo),
-                                     *reinterpret_cast<const __nv_bfloat162*>(&hi));
-    return *reinterpret_cast<const uint32_t*>(&r);
+    return sub_bf16x2(and_mask<0xFF7FFF7Fu>(t), and_mask<0xFF80FF80u>(t));
 }
 
 // KS: K split over a cluster of KS CTAs along z (1 or 2); the two partial
@@ -508,10 +483,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                 // that order): columns 16 b .. 16 b + 15 for block b.
                 const uint4 v0 = ld_shared_v4(wrow + (((uint32_t)(2 * u) ^ wsw) << 4));
                 const uint4 v1 = ld_shared_v4(wrow + (((uint32_t)(2 * u + 1) ^ wsw) << 4));
-                const __half2 s0 = __halves2half2(__ushort_as_half((uint16_t)(sc0 & 0xFFFF)),
-                                                  __ushort_as_half((uint16_t)(sc0 & 0xFFFF)));
-                const __half2 s1 = __halves2half2(__ushort_as_half((uint16_t)(sc0 >> 16)),
-                                                  __ushort_as_half((uint16_t)(sc0 >> 16)));
+                // the block scales, each in both halves of a register
+                const uint32_t s0 = prmt(sc0, sc0, 0x1010u), s1 = prmt(sc0, sc0, 0x3232u);
                 decode_q4_word_scaled(v0.x, s0, o);
                 decode_q4_word_scaled(v0.y, s0, o + 4);
                 decode_q4_word_scaled(v0.z, s0, o + 8);
