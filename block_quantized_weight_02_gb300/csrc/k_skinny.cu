@@ -10,27 +10,27 @@
 //    each stage tracked by full/empty mbarriers; producer lane s issues
 //    every copy of ring slot s;
 //  - dense Q4 takes the caller's activations as given (fp16 or bf16, k
-//    order): their box lands on a barrier of its own and a permuter warp
-//    rewrites each 32-element block in place into the order below before
-//    the consumers read it;
+//    order) and decodes the weights into pairs of adjacent k to match them;
 //  - eight consumer warps take part in every stage.  With up to 16
 //    activation columns each warp owns 16 weight rows and the whole stage
 //    (RB = 128); with 32 columns each warp owns 16 rows and half of the
 //    stage's k (RB = 64; the halves are summed in a fixed order at the
 //    end), which halves each warp's activation reads from shared memory.
 // Decoding goes straight from shared memory into mma.sync A fragments:
-//  - Q4 (dense: the activations as given, in the activation type; MoE: the
-//    guarded fp16 rows written by the guard passes): lane c of a quad
-//    decodes word c (bytes 4c .. 4c + 3) of one 32-k block for its two rows.
-//    Masking the word (and the word shifted by 8) gives the fp16 pairs
-//    1024 + n (low nibbles) and 1024 + 16 n (high nibbles) of bytes (b0, b2)
-//    and (b1, b3); one subtraction, or one fused multiply-add by 1/16, turns
-//    each pair into n - 8 exactly (bf16: 128 + n from the shifted nibbles,
-//    minus 136).  Inside each block the activations sit so that the eight
-//    partners of one word are one 16-byte chunk (the guard pass or the
-//    permuter warp writes them so).  The two MMAs of one block take all 32 k of that block, so
-//    their f32 result is multiplied by the block scale (exact in f32) into
-//    the running sum: the scale is folded per 32-k block.
+//  - Q4: lane c of a quad decodes word c (bytes 4c .. 4c + 3, that is
+//    k = 4c .. 4c + 3 in the low nibbles and k = 4c + 16 .. 4c + 19 in the
+//    high ones) of one 32-k block for its two rows.  Dense (the activations
+//    as given, in the activation type): the nibbles of adjacent bytes are
+//    paired, (b0, b1) and (b2, b3), so each pair is two adjacent k and the
+//    MMA's activation operand is two 8-byte runs of the row in k order.
+//    MoE (the guarded fp16 rows, written by the gather pass so that the
+//    eight partners of one word are one 16-byte chunk): the nibbles of
+//    bytes (b0, b2) and (b1, b3) are paired.  Either way a pair becomes
+//    128 + n (bf16) or 1024 + n (fp16) by masking and byte moves, and one
+//    subtraction (or a fused multiply-add by 1/16 for 1024 + 16 n) leaves
+//    n - 8 exactly.  The two MMAs of one block take all 32 k of that block,
+//    so their f32 result is multiplied by the block scale (exact in f32)
+//    into the running sum: the scale is folded per 32-k block.
 //  - Q8 (activations fp16 or bf16 as given): int8 pairs become fp16
 //    exactly ((v ^ 0x80) | 0x6400 is 1024 + v + 128) or bf16 exactly (low
 //    seven bits and the sign bit go to two bf16 numbers whose difference is
@@ -73,8 +73,7 @@ namespace {
 
 constexpr int CONSUMERS = 8;     // consumer warps, all of them in every stage
 constexpr int PRODUCER = CONSUMERS;
-constexpr int PERMUTER = CONSUMERS + 1;   // puts activations given in k order into the streaming order
-constexpr int THREADS = (CONSUMERS + 2) * 32;
+constexpr int THREADS = (CONSUMERS + 1) * 32;
 
 enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
 
@@ -111,6 +110,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
 }
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
 __device__ __forceinline__ uint4 lds128a(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
@@ -137,15 +141,30 @@ __device__ __forceinline__ void decode_q4_word(uint32_t w, uint32_t d[4]) {
     d[3] = fma_f16x2(and_or<0x00F000F0u>(w8, c6400), k16th, km72);
 }
 
-// The same four pairs as bf16 (for bf16 activations): 0x4300 | n is 128 + n,
-// and 128 + n - 136 is n - 8 with no rounding; the high nibbles are shifted down
-// first (a bf16 has only seven stored mantissa bits).
-__device__ __forceinline__ void decode_q4_word_bf16(uint32_t w, uint32_t d[4]) {
-    const uint32_t c4300 = 0x43004300u, k136 = 0x43084308u;
-    d[0] = sub_bf16x2(and_or<0x000F000Fu>(w, c4300), k136);
-    d[1] = sub_bf16x2(and_or<0x000F000Fu>(w >> 4, c4300), k136);
-    d[2] = sub_bf16x2(and_or<0x000F000Fu>(w >> 8, c4300), k136);
-    d[3] = sub_bf16x2(and_or<0x000F000Fu>(w >> 12, c4300), k136);
+// The same nibbles paired by adjacent bytes (dense path, activations in k
+// order): bytes b0..b3 of w hold k = j .. j + 3 (low nibbles) and j + 16 ..
+// j + 19 (high nibbles), and
+// d[0] = k (j, j + 1), d[1] = (j + 2, j + 3), d[2] = (j + 16, j + 17),
+// d[3] = (j + 18, j + 19).  The masked nibbles are moved next to a constant
+// high byte by one byte permutation per pair.  bf16 (seven stored mantissa
+// bits): the high nibbles are shifted down first; 0x4300 | n is 128 + n, and
+// 128 + n - 136 is n - 8 exactly.  fp16: 1024 + n and 1024 + 16 n as in the
+// streaming-order decode above.
+__device__ __forceinline__ void decode_q4_word_adj_bf16(uint32_t w, uint32_t d[4]) {
+    const uint32_t c43 = 0x43434343u, k136 = 0x43084308u;
+    const uint32_t lo = and_mask<0x0F0F0F0Fu>(w), hi = and_mask<0x0F0F0F0Fu>(w >> 4);
+    d[0] = sub_bf16x2(prmt(lo, c43, 0x4140u), k136);
+    d[1] = sub_bf16x2(prmt(lo, c43, 0x4342u), k136);
+    d[2] = sub_bf16x2(prmt(hi, c43, 0x4140u), k136);
+    d[3] = sub_bf16x2(prmt(hi, c43, 0x4342u), k136);
+}
+__device__ __forceinline__ void decode_q4_word_adj(uint32_t w, uint32_t d[4]) {
+    const uint32_t c64 = 0x64646464u, k1032 = 0x64086408u, k16th = 0x2C002C00u, km72 = 0xD480D480u;
+    const uint32_t lo = and_mask<0x0F0F0F0Fu>(w), hi = and_mask<0xF0F0F0F0u>(w);
+    d[0] = sub_f16x2(prmt(lo, c64, 0x4140u), k1032);
+    d[1] = sub_f16x2(prmt(lo, c64, 0x4342u), k1032);
+    d[2] = fma_f16x2(prmt(hi, c64, 0x4140u), k16th, km72);
+    d[3] = fma_f16x2(prmt(hi, c64, 0x4342u), k16th, km72);
 }
 
 // int8 pair (bytes sel of w) -> half2 exactly: (v ^ 0x80) | 0x6400 is
@@ -187,9 +206,8 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_
 // MT: m16 tiles per consumer warp; KW: warp groups along k (the stage's
 // eight 32-k blocks, or 16-k runs, are split over them), so 8 / KW warps
 // cover the stage's RB = 8 / KW * MT * 16 rows.
-// RAW: the activations are the caller's rows as given (fp16 or bf16, k order);
-// the permuter warp puts each staged tile into the streaming order in place and
-// no guard scale applies (Q4 dense only).
+// RAW: the activations are the caller's rows as given (fp16 or bf16, k order),
+// matched by the adjacent-k decode; no guard scale applies (Q4 dense only).
 template <int FMT, int NT, int MT, int KW, int XBF, int MODE, int NSLOT, int RAW>
 __global__ void __launch_bounds__(THREADS, 2)
 k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
@@ -270,25 +288,20 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
     float* part = reinterpret_cast<float*>(smem + PART_OFF);
     float* recv = reinterpret_cast<float*>(smem + RECV_OFF);
-    // full[NSLOT], empty[NSLOT], xfull[NSLOT] (RAW: activation box landed), xready[NSLOT]
-    // (RAW: activations in the streaming order)
+    // full[NSLOT], empty[NSLOT]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * NSLOT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NSLOT);
     volatile int* never_flag = abort_flag + 1;  // stays 0: waits that must not be cut short
 
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t bar_base = smem_u32(bars);
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (NSLOT + s); };
-    auto xfull_bar = [&](int s) { return bar_base + 8u * (2 * NSLOT + s); };
-    auto xready_bar = [&](int s) { return bar_base + 8u * (3 * NSLOT + s); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), CONSUMERS);
-            mbar_init(xfull_bar(s), 1);
-            mbar_init(xready_bar(s), 1);
         }
         *abort_flag = 0;
         *never_flag = 0;
@@ -331,11 +344,9 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 const int st = st0 + i;
                 // activation rows of this column group (dense: tokens; MoE: grouped pairs)
                 const int xrow0 = (int)(it.col0 + (int64_t)grp * NCOL);
-                if (RAW) mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)G::X_BYTES);
-                tma_load_3d(sbase + (uint32_t)G::X_OFF, &tmX, RAW ? xfull_bar(s) : full_bar(s), 0, st * G::XSL, xrow0);
+                tma_load_3d(sbase + (uint32_t)G::X_OFF, &tmX, full_bar(s), 0, st * G::XSL, xrow0);
             };
-            // bytes of a stage that land on the full barrier (RAW: the activations have their own)
-            constexpr uint32_t FULL_BYTES = RAW ? (uint32_t)G::X_OFF : (uint32_t)G::BYTES;
+            constexpr uint32_t FULL_BYTES = (uint32_t)G::BYTES;   // bytes of a stage
             // The weights of the first ring fill are requested before waiting for the
             // previous kernel in the stream; the activations follow the wait.
             const bool pre = MODE == DENSE && s < nst;
@@ -384,57 +395,6 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
             }
             if (*abort_flag && last_gi >= 0) {  // this lane's last copies must land before the CTA can exit
                 mbar_wait(full_bar(s), last_phase, p.wait_ns, never_flag);
-                if (RAW) mbar_wait(xfull_bar(s), last_phase, p.wait_ns, never_flag);
-            }
-        }
-        __syncwarp();
-    } else if (warp == PERMUTER) {
-        // ================= activations into the streaming order (RAW) =================
-        // Inside each 32-element block, chunk wi of the streaming order holds the pairs
-        // (k, k + 2) for k = 4 wi, 16 + 4 wi, 4 wi + 1, 17 + 4 wi.  The staged tile is
-        // [row][64-k slab][128 B] with the 128-byte swizzle (chunk q of line L at q ^ (L % 8));
-        // each lane reads the four chunks of a block and writes the four reordered ones
-        // back to the same places.  The walk over stages is the consumers'.
-        if (RAW) {
-            constexpr int BLOCKS = NCOL * G::XSL * 2;      // 32-element blocks per stage
-            static_assert(BLOCKS % 32 == 0, "whole blocks per lane");
-            uint32_t slot = 0, phase = 0;
-            bool ok = true;
-            for (int i = 0; i < nst && ok; ++i) {
-                if (!mbar_wait_spin(xfull_bar((int)slot), phase, p.wait_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t sX = smem_base + slot * (uint32_t)G::BYTES + (uint32_t)G::X_OFF;
-#pragma unroll
-                for (int b = lane; b < BLOCKS; b += 32) {
-                    const uint32_t line = (uint32_t)(b >> 1), h = (uint32_t)(b & 1), sw = line & 7u;
-                    const uint32_t base = sX + line * 128u;
-                    uint4 v[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = lds128a(base + (((4u * h + (uint32_t)q) ^ sw) << 4));
-                    const uint32_t wv[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
-                                             v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
-#pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        const uint32_t a0 = wv[2 * wi], a1 = wv[2 * wi + 1], b0 = wv[8 + 2 * wi], b1 = wv[9 + 2 * wi];
-                        sts128(base + (((4u * h + (uint32_t)wi) ^ sw) << 4),
-                               make_uint4(prmt(a0, a1, 0x5410u), prmt(b0, b1, 0x5410u), prmt(a0, a1, 0x7632u),
-                                          prmt(b0, b1, 0x7632u)));
-                    }
-                }
-                // the next activation box of this slot is written by TMA (the async proxy)
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xready_bar((int)slot));
-                if (++slot == (uint32_t)NSLOT) {
-                    slot = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
             }
         }
         __syncwarp();
@@ -448,9 +408,13 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
         // the per-block 16-byte chunk choice is one XOR with a compile-time value.
         //  W: row row0, chunk (j ^ g), word c; row row0 + 8 is 1024 bytes further.
         const uint32_t w_lane = ((uint32_t)(row0 * 128 + 4 * c) ^ ((uint32_t)g << 4)) ^ (kqv << 4);
-        //  X (Q4): row 8 nt + g, slab j / 2, chunk 4 (j % 2) + c, swizzled by the
-        //  line (4 row + slab) % 8 = (4 (g % 2)) ^ (j / 2).
-        const uint32_t x_lane = (uint32_t)(512 * g) | ((((uint32_t)c) ^ (4u * (uint32_t)(g & 1)) ^ (4u * kqv)) << 4);
+        //  X (Q4): row 8 nt + g, slab j / 2, swizzled by the line (4 row + slab) % 8 =
+        //  (4 (g % 2)) ^ (j / 2).  Streaming order (MoE): chunk 4 (j % 2) + c.  k order
+        //  (dense): elements 4c .. 4c + 3 of block j, byte 8 (c % 2) of chunk
+        //  4 (j % 2) + c / 2, and elements 4c + 16 .. 4c + 19 two chunks further.
+        const uint32_t x_lane = RAW ? (uint32_t)(512 * g + 8 * (c & 1)) |
+                                          (((((uint32_t)c >> 1)) ^ (4u * (uint32_t)(g & 1)) ^ (4u * kqv)) << 4)
+                                    : (uint32_t)(512 * g) | ((((uint32_t)c) ^ (4u * (uint32_t)(g & 1)) ^ (4u * kqv)) << 4);
         uint32_t slot = 0, phase = 0;             // ring position of the next stage (same walk as the producers)
         for (int idx = first; idx < nitems; idx += stride) {
           const Item it = get_item(idx);
@@ -468,8 +432,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
 
             bool ok = !*abort_flag;
             for (int i = 0; i < nst && ok; ++i) {
-                if (!mbar_wait(full_bar((int)slot), phase, p.wait_ns, abort_flag) ||
-                    (RAW && !mbar_wait_spin(xready_bar((int)slot), phase, p.wait_ns, abort_flag))) {
+                if (!mbar_wait(full_bar((int)slot), phase, p.wait_ns, abort_flag)) {
                     ok = false;
                     *abort_flag = 1;
                     atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
@@ -496,7 +459,14 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                         const uint32_t xad = (xS ^ (jx << 4)) + 128u * (uint32_t)(jf >> 1);
                         uint4 bx[NT];
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) bx[nt] = lds128a(xad + 4096u * nt);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            if (RAW) {   // the two 8-byte runs, k order
+                                const uint2 lo = lds64(xad + 4096u * nt), hi = lds64((xad + 4096u * nt) ^ 32u);
+                                bx[nt] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                            } else {
+                                bx[nt] = lds128a(xad + 4096u * nt);
+                            }
+                        }
                         float sa, sb;
                         if (KW == 1) {
                             const uint32_t wsa = (jf >> 1) == 0 ? sc0.x : (jf >> 1) == 1 ? sc0.y : (jf >> 1) == 2 ? sc0.z : sc0.w;
@@ -508,9 +478,12 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                             sb = __half2float(__ushort_as_half((unsigned short)lds16(sS + 128u + 2u * jf)));
                         }
                         uint32_t d[4], e[4];
-                        if (XBF) {
-                            decode_q4_word_bf16(wa, d);
-                            decode_q4_word_bf16(wb, e);
+                        if (RAW && XBF) {
+                            decode_q4_word_adj_bf16(wa, d);
+                            decode_q4_word_adj_bf16(wb, e);
+                        } else if (RAW) {
+                            decode_q4_word_adj(wa, d);
+                            decode_q4_word_adj(wb, e);
                         } else {
                             decode_q4_word(wa, d);
                             decode_q4_word(wb, e);
@@ -709,7 +682,7 @@ constexpr size_t smem_bytes() {
     constexpr int PART_BYTES = RB * NCOL * 4;
     constexpr int RECV_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
     constexpr int BAR_OFF = RECV_OFF + ((MODE == DENSE) ? PART_BYTES : 0);
-    return (size_t)BAR_OFF + 4 * NSLOT * 8 + 16 + 1024;
+    return (size_t)BAR_OFF + 2 * NSLOT * 8 + 16 + 1024;
 }
 
 // Weights [E][R][K bytes] and scales [E][R][K/32], boxes of rows_box rows.
@@ -791,7 +764,7 @@ DenseCfg dense_cfg(int64_t T) {
     return {4, 1, 2, rows_per_stage(1, 2)};
 }
 
-// Q4 takes the activations as given (RAW): the permuter warp orders them.
+// Q4 takes the activations as given (RAW), in k order.
 template <int FMT, int XBF>
 cudaError_t launch_dense_nt(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, const Params& p, dim3 grid,
                             int cluster, int64_t T, cudaStream_t s) {
