@@ -330,3 +330,63 @@ def test_q4_weight_streaming_fp16_activations_at_the_range_edges(T):
         Y, wq = run_q4(case, "f32")
     yref, S = oracle_q4(case, wq)
     check(y_host(Y), yref, S, "f32", f"q4 streaming fp16 edges T={T}")
+
+
+# ---- weight-streaming Q4: partition shapes, workspace contents, graph replay ----
+
+@pytest.mark.parametrize("T,K,N", [(1, 8192, 130), (8, 4096, 64), (8, 256, 1000), (16, 2048, 600),
+                                   (32, 1024, 777), (5, 768, 129), (1, 256, 40000)])
+def test_q4_streaming_partition_shapes(T, K, N):
+    """Shapes that split a row block's K over a cluster (few rows, long K), leave a
+    ragged last row block, give a CTA a single stage (K = 256), or make row blocks
+    outnumber two CTAs per SM (no K split); the result is compared element by
+    element with the oracle."""
+    case = synth.gemm_q4_case(2000 + T + K + N, T, K, N, x_dtype="bf16", signed=True)
+    with ForcePath(1):
+        Y, wq = run_q4(case, "f32")
+    yref, S = oracle_q4(case, wq)
+    check(y_host(Y), yref, S, "f32", f"q4 streaming T={T} K={K} N={N}")
+
+
+def test_q4_streaming_workspace_contents_and_graph_replay():
+    """The workspace may hold anything: filled with 0xFF bytes, with random bytes,
+    or with the guard copy a T > 32 call leaves in it, the weight-streaming result
+    is the same bit for bit; so is every replay of a captured CUDA graph."""
+    T, K, N = 8, 2048, 520
+    case = synth.gemm_q4_case(77, T, K, N, x_dtype="bf16", signed=True)
+    wq = pack.pack_q4(case["codes"])
+    X = to_dev_x(case["x"], "bf16")
+    Wq, Ws = to_dev(wq), to_dev(case["scales"])
+    big = synth.gemm_q4_case(78, 64, K, N, x_dtype="bf16", signed=True)
+    Xb = to_dev_x(big["x"], "bf16")
+    Yb = torch.empty(64, N, dtype=torch.float32, device=DEV)
+    nbytes = max(cq.cq_gemm_q4_workspace_bytes(T, K), cq.cq_gemm_q4_workspace_bytes(64, K))
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)
+    Y = torch.empty(T, N, dtype=torch.float32, device=DEV)
+    with ForcePath(0):
+        cq.cq_gemm_q4(X, Wq, Ws, Y, ws)
+        ref = Y.clone()
+        yref, S = oracle_q4(case, wq)
+        check(y_host(ref), yref, S, "f32", "q4 streaming, workspace of 0xFF bytes")
+        ws.copy_(torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=DEV))
+        Y.zero_()
+        cq.cq_gemm_q4(X, Wq, Ws, Y, ws)
+        assert torch.equal(Y, ref)
+        cq.cq_gemm_q4(Xb, Wq, Ws, Yb, ws)          # the guard pass writes over the workspace
+        Y.zero_()
+        cq.cq_gemm_q4(X, Wq, Ws, Y, ws)
+        assert torch.equal(Y, ref)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            cq.cq_gemm_q4(X, Wq, Ws, Y, ws)          # warm up on the capture stream
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cq.cq_gemm_q4(X, Wq, Ws, Y, ws)
+        for _ in range(3):
+            Y.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert cq.cq_get_device_error() == 0
+            assert torch.equal(Y, ref)
