@@ -1,19 +1,35 @@
 """Benchmark of the quantized-weight GEMM path on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                [--no-per-config] [--no-cpu-baseline] [--eager] [--traffic-pass]
 
-Default workload "prefill_projection_4096": one step = the four calls of the
-prefill projection (T=512, K=N=4096): Q4 -> f32, Q4 -> bf16, Q8-row -> f32,
-Q8-row -> bf16.  The metric is dequant-GEMM TFLOP/s (2*T*N*K per call, all
-calls of all ranks over the max-over-ranks time); weight GB/s and the
-roofline fraction of the dominant kernel ride along in the same JSON line.
-Other workloads: smallest_q4, denoiser_block, moe_panels, sweep_q4_T<T>,
-sweep_q8_T<T>.
+Default workload "denoiser_block" (the largest configuration): one step = the
+two Q4 GEMMs of the denoiser block at 1024 target rows, gate/up (T=1024,
+K=3072, N=2x12288) then down (T=1024, K=12288, N=3072), bf16 outputs.  The
+metric is dequant-GEMM TFLOP/s (2*T*N*K per call, all calls of all ranks over
+the max-over-ranks time); weight GB/s and the roofline fraction of the
+dominant call ride along in the same JSON line.
+
+Beside it, "per_config" times every call of the other configurations alone,
+each in a back-to-back chain of its own over input sets larger than L2: the
+smallest Q4 case, the prefill projection (Q4 and Q8-row, f32 and bf16), the
+MoE expert panels and the decode-to-prefill sweep (Q4 and Q8-row at
+T = 1, 8, 32, 128, 512, 2048).  Each entry gives microseconds per call,
+TFLOP/s, weight GB/s, the fractions of the measured tensor and HBM peaks, the
+bound (whichever roofline is lower for the call's arithmetic intensity) and
+the DRAM traffic per call from the committed ncu summary
+(profiles/traffic_per_call.md), or null once the kernel sources have changed
+since it was taken.
+
+Other workloads for the headline: smallest_q4, prefill_projection_4096,
+moe_panels, sweep_q4_T<T>, sweep_q8_T<T>.
 
 Under torchrun (N > 1) every rank runs its own copy of the workload
 (independent problems, no collective on the data path): weak scaling.
 --impl reference times the CPU oracle on a bounded sample of the same
-workload (rank 0 only).
+workload (rank 0 only).  --traffic-pass runs every call of every
+configuration once, after one warm-up call each, and exits (the command the
+ncu traffic summary is taken over).
 """
 from __future__ import annotations
 
@@ -140,7 +156,7 @@ def _dtype_of(name, info):
     return q4
 
 
-def build_workload(name, dev):
+def build_workload(name, dev, max_sets=16):
     import block_quantized_weight_02_gb300 as cq
     from block_quantized_weight_02_gb300 import synth
     info = {}
@@ -174,7 +190,7 @@ def build_workload(name, dev):
         raise SystemExit(f"unknown workload {name}")
     one = make()
     set_bytes = sum(c.weight_bytes + c.other_bytes for c in one)
-    sets = max(1, min(16, -(-3 * L2_BYTES // max(set_bytes, 1))))
+    sets = max(1, min(max_sets, -(-3 * L2_BYTES // max(set_bytes, 1))))
     rot = [one] + [make() for _ in range(sets - 1)]
     return (lambda i=[0]: rot), info, sets
 
@@ -246,6 +262,115 @@ def whole_job_rate(units_per_step: float, world: int, ms_per_step_max: float) ->
     return units_per_step * world / (ms_per_step_max * 1e-3)
 
 
+PER_CONFIG = (["smallest_q4", "prefill_projection_4096", "moe_panels"]
+              + [f"sweep_{f}_T{t}" for f in ("q4", "q8") for t in (1, 8, 32, 128, 512, 2048)])
+
+TRAFFIC_MD = os.path.join(ROOT, "profiles", "traffic_per_call.md")
+
+
+def kernel_sources_hash() -> str:
+    """Hash of the library's kernel sources and header: the DRAM traffic taken
+    with ncu belongs to the kernels built from exactly these files."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantized_weight_02_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "cq.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(path=TRAFFIC_MD):
+    """{(workload, call): DRAM bytes per call} from the committed ncu summary
+    (rows `| workload | call | launches | DRAM bytes per call | ...`), empty when
+    the summary was taken on other kernel sources."""
+    if not os.path.exists(path):
+        return {}
+    txt = open(path).read()
+    import re
+    m = re.search(r"kernel sources `([0-9a-f]{16})`", txt)
+    if not m or m.group(1) != kernel_sources_hash():
+        return {}
+    out = {}
+    for line in txt.splitlines():
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and (cells[0] in PER_CONFIG or cells[0] == "denoiser_block"):
+            try:
+                out[(cells[0], cells[1])] = int(cells[3].replace(",", ""))
+            except ValueError:
+                pass
+    return out
+
+
+def roofline_entry(call, ms, peaks, traffic):
+    """Throughput of one call and its fractions of the measured peaks.  The
+    bound is the roofline the call's arithmetic intensity (FLOPs over its
+    algorithmic bytes: weights + activations + outputs) puts it under."""
+    s = ms * 1e-3
+    alg = call.weight_bytes + call.other_bytes
+    tf = call.flops / s / 1e12
+    gbs = alg / s / 1e9
+    ft, fh = tf / peaks["bf16_tflops"], gbs / peaks["hbm_gbs"]
+    tensor = call.flops / max(alg, 1) > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return {"us": round(ms * 1e3, 3), "tflops": round(tf, 2), "weight_gbs": round(call.weight_bytes / s / 1e9, 1),
+            "bytes_gbs": round(gbs, 1), "bound": "tensor" if tensor else "hbm",
+            "frac": round(ft if tensor else fh, 4), "frac_tensor": round(ft, 4), "frac_hbm": round(fh, 4),
+            "algorithmic_bytes": int(alg), "traffic": traffic, "launches": call.launches}
+
+
+def time_calls(rot, sets, reps, stream, use_graph):
+    """Average duration (ms) of each call of the step alone: the call repeated
+    back to back over the rotating input sets, captured in a CUDA graph and
+    replayed once untimed, then timed with CUDA events on the launching stream."""
+    import torch
+    out = []
+    for j in range(len(rot[0])):
+        g = None
+        if use_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(reps):
+                    rot[i % sets][j].fn()
+            g.replay()
+            torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        if g is not None:
+            g.replay()
+        else:
+            for i in range(reps):
+                rot[i % sets][j].fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b) / reps)
+        del g
+    return out
+
+
+def traffic_pass(args, dev):
+    """Every call of every configuration once after one warm-up call each, one
+    input set, nothing timed: the launches an ncu DRAM-traffic capture reads.
+    Prints the launch order (workload, call, launches) to stdout."""
+    import torch
+    import block_quantized_weight_02_gb300 as cq
+    names = ["denoiser_block"] + PER_CONFIG if args.configs == "all" else args.configs.split(",")
+    for name in names:
+        rot_fn, info, sets = build_workload(name, dev, max_sets=1)
+        calls = rot_fn()[0]
+        for c in calls:
+            c.fn()
+            torch.cuda.synchronize()
+            c.fn()
+            torch.cuda.synchronize()
+            print(f"traffic-pass\t{name}\t{c.name}\t{c.launches}", flush=True)
+        if cq.cq_get_device_error() != 0:
+            raise SystemExit(f"device error in {name}")
+        del calls, rot_fn
+        torch.cuda.empty_cache()
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -255,6 +380,11 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    if args.traffic_pass:
+        traffic_pass(args, dev)
+        return
+    peaks = _peaks()
+    traffic = load_traffic()
     rot_fn, info, sets = build_workload(args.workload, dev)
     rot = rot_fn()
     stream = torch.cuda.current_stream()
@@ -267,14 +397,16 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
+    # Clocks are sampled from the warm-up to the end of the per-call timings
+    # (the K timed steps alone last milliseconds, shorter than a sample).
+    clocks = Clocks(local_rank)
+    clocks.start()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     if cq.cq_get_device_error() != 0:
         raise SystemExit("device error during warm-up")
 
-    clocks = Clocks(local_rank)
-    clocks.start()
     # The timed region: K steps of the workload's calls, back to back on one
     # stream.  By default it is captured once into a CUDA graph and replayed,
     # so host-side launch overhead does not leave the GPU idle between the
@@ -312,37 +444,14 @@ def run_ours(args, rank, world, local_rank):
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    clk = clocks.stop()
     ms = t0.elapsed_time(t1)
     if cq.cq_get_device_error() != 0:
         raise SystemExit("device error during the timed region")
     ms_max = max_over_ranks(ms, world)
 
-    # Per-call duration (for the roofline of the dominant call): each call of
-    # the step alone, repeated back to back over the rotating input sets, timed
-    # with CUDA events on the launching stream; the average call time there.
+    # Per-call duration (for the roofline of the dominant call).
     reps = max(3, min(args.steps, 50))
-    per_call_ms = []
-    for j in range(len(rot[0])):
-        g = None
-        if graph is not None:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                for i in range(reps):
-                    rot[i % sets][j].fn()
-            g.replay()
-            torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        if g is not None:
-            g.replay()
-        else:
-            for i in range(reps):
-                rot[i % sets][j].fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        per_call_ms.append(a.elapsed_time(b) / reps)
-        del g
+    per_call_ms = time_calls(rot, sets, reps, stream, graph is not None)
     if cq.cq_get_device_error() != 0:
         raise SystemExit("device error while timing the calls")
 
@@ -386,21 +495,37 @@ def run_ours(args, rank, world, local_rank):
     e2e_val = whole_job_rate(flops_step, world, e_ms) / 1e12
 
     # roofline of the dominant call (largest share of the step)
-    peaks = _peaks()
     j = int(np.argmax(per_call_ms))
     dom = calls[j]
-    d_ms = per_call_ms[j]
-    tensor_bound = dom.flops / max(dom.weight_bytes + dom.other_bytes, 1) > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if tensor_bound:
-        ach = dom.flops / (d_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(ach / peaks["bf16_tflops"], 4)}
-    else:
-        ach = (dom.weight_bytes + dom.other_bytes) / (d_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4)}
-    roof.update({"traffic": None, "kernel": dom.name, "launch_ms": round(d_ms, 5),
-                 "peak_source": peaks["source"], "launches_in_call": dom.launches})
+    ent = roofline_entry(dom, per_call_ms[j], peaks, traffic.get((args.workload, dom.name)))
+    roof = {"bound": ent["bound"], "achieved": ent["tflops"] if ent["bound"] == "tensor" else ent["bytes_gbs"],
+            "peak": peaks["bf16_tflops"] if ent["bound"] == "tensor" else peaks["hbm_gbs"],
+            "unit": "TFLOP/s" if ent["bound"] == "tensor" else "GB/s", "frac": ent["frac"],
+            "traffic": ent["traffic"], "algorithmic_bytes": ent["algorithmic_bytes"], "kernel": dom.name,
+            "launch_ms": round(per_call_ms[j], 5), "peak_source": peaks["source"],
+            "launches_in_call": dom.launches}
+
+    # every call of the other configurations, each alone in its own chain
+    per_config = {args.workload: {c.name: roofline_entry(c, t, peaks, traffic.get((args.workload, c.name)))
+                                  for c, t in zip(calls, per_call_ms)}}
+    if not args.no_per_config:
+        del rot, rot_fn, graph
+        torch.cuda.empty_cache()
+        for name in PER_CONFIG:
+            if name == args.workload:
+                continue
+            r_fn, _, n_sets = build_workload(name, dev)
+            r = r_fn()
+            r[0][0].fn()                  # warm-up
+            torch.cuda.synchronize()
+            t_ms = time_calls(r, n_sets, 20 if name.endswith("T2048") else 50, stream, not args.eager)
+            if cq.cq_get_device_error() != 0:
+                raise SystemExit(f"device error while timing {name}")
+            per_config[name] = {c.name: roofline_entry(c, t, peaks, traffic.get((name, c.name)))
+                                for c, t in zip(r[0], t_ms)}
+            del r, r_fn
+            torch.cuda.empty_cache()
+    clk = clocks.stop()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -422,6 +547,9 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": sum(c.launches for c in calls) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "per_config": per_config,
+        "peaks": {"tensor_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peaks["source"]},
+        "traffic_source": "profiles/traffic_per_call.md" if traffic else None,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -477,7 +605,19 @@ def _oracle_sample(workload):
                 f"first {rows} of 16 activation rows"
         return make, 16
     if workload == "denoiser_block":
-        c, fmt = synth.c3()[0], "q4"
+        gu, dn = synth.c3()
+        wgu, wdn = oracle.pack_q4(gu["codes"]), oracle.pack_q4(dn["codes"])
+
+        def make(rows):
+            Xg = oracle.x_to_f64(gu["x"][:rows], "bf16")
+            Xd = oracle.x_to_f64(dn["x"][:rows], "bf16")
+
+            def fn():
+                oracle.gemm_q4(wgu, gu["scales"], gu["N"], gu["K"], Xg)
+                oracle.gemm_q4(wdn, dn["scales"], dn["N"], dn["K"], Xd)
+            return fn, 2.0 * rows * (gu["N"] * gu["K"] + dn["N"] * dn["K"]), \
+                f"first {rows} of 1024 activation rows of both GEMMs (gate/up and down), full N and K"
+        return make, 1024
     else:
         T = int(workload.split("_T")[1])
         fmt = "q4" if "q4" in workload else "q8"
@@ -544,7 +684,11 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="prefill_projection_4096")
+    ap.add_argument("--workload", default="denoiser_block")
+    ap.add_argument("--no-per-config", action="store_true", help="time only the headline workload")
+    ap.add_argument("--traffic-pass", action="store_true",
+                    help="run every call of the configurations in --configs once (after a warm-up call) and exit")
+    ap.add_argument("--configs", default="all", help="comma-separated workloads for --traffic-pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time direct calls instead of a captured CUDA graph")
     args = ap.parse_args()

@@ -28,6 +28,8 @@ cq_status fail(cq_status st, const char* fmt, ...) {
     return st;
 }
 
+void clear_last_error() { g_msg[0] = 0; }
+
 cq_status cuda_fail(cudaError_t e, const char* what) {
     return fail(CQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }

@@ -26,8 +26,9 @@ struct Options {
 };
 Options& options();
 
-// Host error reporting.
+// Host error reporting (a thread-local "decline: ..." message).
 cq_status fail(cq_status st, const char* fmt, ...);
+void clear_last_error();
 cq_status cuda_fail(cudaError_t e, const char* what);
 
 // Tensor map encoding (driver entry point fetched through the runtime, so

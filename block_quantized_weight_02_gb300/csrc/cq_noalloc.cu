@@ -53,6 +53,7 @@ using namespace cq;
 
 extern "C" cq_status cq_gemm_q4_noalloc(const void* X, int xt, int64_t T, int64_t K, const uint8_t* Wq,
                                          const uint16_t* Ws, int64_t N, void* Y, int yt, void* stream) {
+    clear_last_error();
     if (!X || !Wq || !Ws || !Y) return fail(CQ_ERR_NULL, "cq_gemm_q4_noalloc: null pointer");
     if (xt != CQ_F16 && xt != CQ_BF16) return fail(CQ_ERR_DTYPE, "cq_gemm_q4_noalloc: activations must be fp16 or bf16");
     if (yt != CQ_F32 && yt != CQ_BF16) return fail(CQ_ERR_DTYPE, "cq_gemm_q4_noalloc: output must be f32 or bf16");

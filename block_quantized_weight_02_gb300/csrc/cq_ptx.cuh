@@ -105,17 +105,6 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src,
                  ::"r"(dst), "r"(src), "r"(bytes), "r"(mbar) : "memory");
 }
 
-// The same tile delivered to the same shared-memory offset of every CTA in
-// cta_mask (this GPU's own memory); each destination's mbarrier at `bar`'s
-// offset receives the bytes written into that CTA.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1,
-                                               uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask) : "memory");
-}
-
 // Address of the same shared-memory offset in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     uint32_t r;
@@ -324,12 +313,6 @@ __device__ __forceinline__ bool mbar_wait_cluster_spin(uint32_t bar, uint32_t pa
             if (global_timer_ns() - t0 > limit_ns) return false;
         }
     }
-}
-
-// As tc_commit, arriving on the mbarrier at the same offset in every CTA of cta_mask.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-                 ::"r"(bar), "h"(cta_mask) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane

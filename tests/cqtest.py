@@ -41,27 +41,40 @@ def half_ulp_bf16(y: np.ndarray) -> np.ndarray:
 def check(y: np.ndarray, yref: np.ndarray, S: np.ndarray, out_dtype: str, what: str = ""):
     """Acceptance: the computed value before the output's own rounding is
     within |err| <= 2e-3*S + 1e-6 per element and relative Frobenius <= 1e-3
-    of the f64 reference.  An f32 output's rounding (2^-24 relative) is far
-    inside that; a bf16 output's rounding (up to half a bf16 ulp of y) is
-    not, so for bf16 that rounding is added exactly to both bounds."""
-    err = np.abs(y - yref)
-    r = half_ulp_bf16(y) if out_dtype == "bf16" else np.zeros_like(y)
-    bound = 2e-3 * S + 1e-6 + r
-    bad = err > bound
+    of the f64 reference.
+
+    An f32 output's rounding (2^-24 relative) is far inside that, so y itself
+    is tested.  A bf16 output y stands for every value in its rounding box
+    [y - r, y + r] (r = half a bf16 ulp at y), and the bound holds for the
+    unrounded value exactly when some value in that box meets it: the test
+    takes d = max(|y - yref| - r, 0), the distance from yref to the box, and
+    requires d <= 2e-3*S + 1e-6 per element and ||d|| <= 1e-3 ||yref||.
+
+    For bf16 it also compares y with RNE_bf16(yref), the oracle's own
+    rounding: a value v within b of yref rounds to a bf16 number at most
+    b + r + r' from it (r' the half ulp at RNE_bf16(yref)), so wherever the
+    element bound b is below half an ulp the two are equal or adjacent bf16
+    numbers.  "One ulp everywhere" is not implied by the bound: where |y| is
+    small against S (cancellation) b spans many ulps of y."""
+    bound = 2e-3 * S + 1e-6
     nref = max(np.linalg.norm(yref), 1e-300)
-    fro = np.linalg.norm(y - yref) / nref
-    fro_bound = 1e-3 + np.linalg.norm(r) / nref
-    if bad.any() or not np.all(np.isfinite(y)) or fro > fro_bound:
-        i = int(np.argmax(err / bound))
-        raise AssertionError(f"{what}: {int(bad.sum())} elements over the bound (worst ratio "
-                             f"{float((err / bound).flat[i]):.3g} at {np.unravel_index(i, err.shape)}: "
-                             f"y={y.flat[i]!r} ref={yref.flat[i]!r} S={S.flat[i]!r}), rel Frobenius {fro:.3g} "
-                             f"(bound {fro_bound:.3g})")
     if out_dtype == "bf16":
-        # the rounded outputs mostly coincide with the oracle's own rounding
-        same = np.mean(oracle.x_to_f64(oracle.f64_to_bf16(yref), "bf16") == y)
-        assert same >= 0.8, f"{what}: only {same:.3f} of bf16 outputs equal the oracle's rounding"
-    return float(np.max(err / bound)), float(fro)
+        r = half_ulp_bf16(y)
+        d = np.maximum(np.abs(y - yref) - r, 0.0)
+        z = oracle.x_to_f64(oracle.f64_to_bf16(yref), "bf16")
+        co = np.abs(y - z) <= bound + r + half_ulp_bf16(z)
+    else:
+        d = np.abs(y - yref)
+        co = np.ones(y.shape, bool)
+    bad = d > bound
+    fro = np.linalg.norm(d) / nref
+    if bad.any() or not np.all(np.isfinite(y)) or fro > 1e-3 or not co.all():
+        i = int(np.argmax(d / bound))
+        raise AssertionError(f"{what}: {int(bad.sum())} elements over the bound (worst ratio "
+                             f"{float((d / bound).flat[i]):.3g} at {np.unravel_index(i, d.shape)}: "
+                             f"y={y.flat[i]!r} ref={yref.flat[i]!r} S={S.flat[i]!r}), rel Frobenius {fro:.3g} "
+                             f"(bound 1e-3), {int((~co).sum())} bf16 outputs away from the oracle's rounding")
+    return float(np.max(d / bound)), float(fro)
 
 
 def run_q4(case, out_dtype="f32", Y=None):

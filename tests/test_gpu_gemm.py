@@ -390,3 +390,116 @@ def test_q4_streaming_workspace_contents_and_graph_replay():
             torch.cuda.synchronize()
             assert cq.cq_get_device_error() == 0
             assert torch.equal(Y, ref)
+
+
+# ---- the GEMMs' own decoders, bit-exact through identity activations ----
+# Row t of X is the unit vector at column k_t, so output (t, n) is the single
+# product W[n][k_t] * 1 plus exact zeros.  On the weight-streaming path every
+# product is exact and the block scale multiplies the f32 result of its
+# block, so Y[t][n] is the oracle's dequantized weight itself (one exact f32
+# product).  On the tcgen05 path the decoder rounds (q - 8) * scale once to
+# fp16, the guard scales the unit row to 2^13 and back, so Y[t][n] is the
+# fp16 rounding (RNE) of the oracle's weight.  The only freedom is the sign
+# of a zero result, which a sum does not carry, so values are compared with
+# == (+0 == -0) and every nonzero value is then equal bit for bit.
+
+_SPECIAL_SCALES = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x03FF, 0x83FF, 0x0400, 0x3C00, 0xBC00, 0x2E66],
+                           np.uint16)
+
+
+def _decoder_case(seed, N, K, big_scales):
+    """Codes over 0..15 with nibble 8 (zero) on every 7th column, signed fp16
+    block scales with +-0, subnormal, smallest normal and unit scales mixed in
+    (and, where no fp16 rounding of the weight follows, the largest finite)."""
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, (N, K), dtype=np.uint8)
+    codes[:, ::7] = 8
+    mag = rng.uniform(0.005, 0.02, (N, K // 32)) * np.where(rng.integers(0, 2, (N, K // 32)) == 1, -1.0, 1.0)
+    scales = mag.astype(np.float16).view(np.uint16)
+    specials = np.concatenate([_SPECIAL_SCALES, np.array([0x7BFF, 0xFBFF], np.uint16)]) if big_scales \
+        else _SPECIAL_SCALES
+    m = rng.random(scales.shape) < 0.25
+    scales[m] = rng.choice(specials, int(m.sum()))
+    return codes, scales
+
+
+def _unit_rows(T, K, xdt, shift):
+    """X[t] = e_{k_t}: block (5 t + shift) mod K/32, position (13 t + shift) mod 32
+    (every position of a 32-k block once per 32 rows)."""
+    nb = K // 32
+    kt = 32 * ((5 * np.arange(T) + shift) % nb) + (13 * np.arange(T) + shift) % 32
+    x = np.zeros((T, K))
+    x[np.arange(T), kt] = 1.0
+    return synth.to_storage(x, xdt), kt
+
+
+def _assert_values_equal(Y, E, what):
+    y = Y.cpu().numpy()
+    eq = y == E
+    assert eq.all(), (f"{what}: {int((~eq).sum())} of {eq.size} outputs differ, first at "
+                      f"{np.argwhere(~eq)[0]}: {y[tuple(np.argwhere(~eq)[0])]!r} vs {E[tuple(np.argwhere(~eq)[0])]!r}")
+    nz = E != 0
+    assert np.array_equal(y[nz].view(np.uint32), E[nz].astype(np.float32).view(np.uint32))
+
+
+@pytest.mark.parametrize("T", [1, 8, 16, 32])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_q4_streaming_decoder_bit_exact_identity(T, xdt):
+    N, K = 300, 1024
+    codes, scales = _decoder_case(8100 + T, N, K, big_scales=True)
+    wq = pack.pack_q4(codes)
+    W = oracle.dequant_q4(wq, scales, N, K)
+    for shift in (0, 7):
+        x, kt = _unit_rows(T, K, xdt, shift)
+        Y = torch.empty(T, N, dtype=torch.float32, device=DEV)
+        with ForcePath(1):
+            cq.cq_gemm_q4(to_dev_x(x, xdt), to_dev(wq), to_dev(scales), Y,
+                          torch.empty(cq.cq_gemm_q4_workspace_bytes(T, K), dtype=torch.uint8, device=DEV))
+        assert cq.cq_get_device_error() == 0
+        _assert_values_equal(Y, W[:, kt].T, f"q4 streaming decode T={T} {xdt} shift={shift}")
+
+
+@pytest.mark.parametrize("T,bn,ks", [(40, 0, 0), (64, 64, 1), (150, 128, 2), (300, 256, 1), (300, 256, 2),
+                                     (256, 192, 1)])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_q4_tcgen05_decoder_bit_exact_identity(T, bn, ks, xdt):
+    N, K = 512, 512
+    codes, scales = _decoder_case(8200 + T + bn, N, K, big_scales=False)
+    wq = pack.pack_q4(codes)
+    W16 = oracle.dequant_q4(wq, scales, N, K).astype(np.float16).astype(np.float32)   # numpy RNE to fp16
+    x, kt = _unit_rows(T, K, xdt, 3)
+    Y = torch.empty(T, N, dtype=torch.float32, device=DEV)
+    with ForcePath(2), _Opt(cq.CQ_OPT_TC_BN, bn), _Opt(cq.CQ_OPT_TC_KSPLIT, ks):
+        cq.cq_gemm_q4(to_dev_x(x, xdt), to_dev(wq), to_dev(scales), Y,
+                      torch.empty(cq.cq_gemm_q4_workspace_bytes(T, K), dtype=torch.uint8, device=DEV))
+    assert cq.cq_get_device_error() == 0
+    _assert_values_equal(Y, W16[:, kt].T, f"q4 tcgen05 decode T={T} bn={bn} ks={ks} {xdt}")
+
+
+@pytest.mark.parametrize("path,T,bn,ks", [(1, 8, 0, 0), (1, 32, 0, 0), (2, 64, 64, 1), (2, 300, 256, 2),
+                                          (2, 200, 128, 1)])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_q8_decoders_bit_exact_identity(path, T, bn, ks, xdt):
+    """Q8-row: int8 -> the activation type exactly, the row scale on the f32
+    sum: Y[t][n] = RNE_f32(q[n][k_t] * rs[n]), the oracle's dequantized weight."""
+    N, K = 260, 512
+    rng = np.random.default_rng(8300 + T)
+    q, rs = synth.draw_q8row(rng, N, K)
+    q[0, :] = -128
+    q[1, :] = 127
+    q[2, ::3] = 0
+    W = oracle.dequant_q8row(q, rs)
+    x, kt = _unit_rows(T, K, xdt, 11)
+    Y = torch.empty(T, N, dtype=torch.float32, device=DEV)
+    with ForcePath(path), _Opt(cq.CQ_OPT_TC_BN, bn), _Opt(cq.CQ_OPT_TC_KSPLIT, ks):
+        cq.cq_gemm_q8row(to_dev_x(x, xdt), to_dev(q), to_dev(rs), Y)
+    assert cq.cq_get_device_error() == 0
+    _assert_values_equal(Y, W[:, kt].T, f"q8 decode path={path} T={T} bn={bn} ks={ks} {xdt}")
+
+
+# ---- C3 with f32 outputs: the strict bound on the largest shapes ---------
+
+def test_c3_denoiser_block_f32():
+    gu, dn = synth.c3()
+    _sampled_q4(gu, "f32", count=2000, seed=3)
+    _sampled_q4(dn, "f32", count=2000, seed=4)
