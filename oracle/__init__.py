@@ -214,3 +214,24 @@ def moe(X, idx, w, gu_q, gu_s, d_q, d_s, E, I):
     if rc != 0:
         raise ValueError("routing index out of range")
     return Y, S
+
+
+# ---- dense FFN chain -------------------------------------------------------
+
+def ffn(X, gu_q, gu_s, d_q, d_s, I, want_a=False):
+    """(Y, S[, A]) f64 for the dense gate/up -> SwiGLU -> down chain over every
+    token of X [T][H] (f64): gu_q/gu_s the Q4 gate|up rows [2I][H/2], [2I][H/32];
+    d_q/d_s the Q4 down rows [H][I/2], [H][I/32]."""
+    X = _c(X, np.float64)
+    T, H = X.shape
+    gu_q = _c(gu_q, np.uint8)
+    gu_s = _c(gu_s, np.uint16)
+    d_q = _c(d_q, np.uint8)
+    d_s = _c(d_s, np.uint16)
+    assert gu_q.size == 2 * I * H // 2 and d_q.size == H * I // 2
+    Y = np.empty((T, H), np.float64)
+    S = np.empty((T, H), np.float64)
+    A = np.empty((T, I), np.float64) if want_a else None
+    _load().or_ffn(_p(X), _i(T), _i(H), _i(I), _p(gu_q), _p(gu_s), _p(d_q), _p(d_s), _p(Y), _p(S),
+                   _p(A) if want_a else None)
+    return (Y, S, A) if want_a else (Y, S)

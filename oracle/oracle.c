@@ -25,13 +25,17 @@
  *    weighted sum): same tests module, mma_moe_matches_cpu; SiLU as
  *    g/(1+exp(-g)) from the silu_half shader.  Expert-major grouping of the
  *    routed rows, token order inside an expert: same page, Backend::moe.
+ *  - Dense FFN chain (gate/up, SwiGLU, down for every token): "cortiq-engine
+ *    0.8.3 src/gpu_metal/qi21.rs", fn blocks (gemm(TG, TU) -> swiglu ->
+ *    gemm(TD)) and its module header.
  *
  * Every function is single-purpose; the only parallelism is OpenMP over
  * independent outputs, which leaves each output's arithmetic unchanged.
  *
  * Pins (tests marked "not gpu"): hand-built blocks for the dequantizers,
  * exact rational brute force and a library f64 matmul for the GEMM, closed
- * forms and invariants for the MoE chain and the layout.  No function here
+ * forms and invariants for the MoE chain and the layout, a one-hot closed
+ * form, library matmuls and the one-expert MoE chain for the dense FFN.  No function here
  * is left without a pin.
  */
 #include <math.h>
@@ -321,4 +325,52 @@ int or_moe(const double* X, int64_t T, int64_t H, int64_t E, int64_t I, int64_t 
     for (int64_t e = 0; e < E; e++) { free(gu[e]); free(dn[e]); }
     free(gu); free(dn); free(o); free(sa);
     return 0;
+}
+
+/* ---- dense FFN chain (gate/up -> SwiGLU -> down) ---- */
+
+/* For every token t of X[T][H] (f64):
+ *   g_i = sum_k Wg[i][k] x_k,  u_i = sum_k Wu[i][k] x_k       (i < I; f64, k ascending)
+ *   a_i = g_i / (1 + exp(-g_i)) * u_i                          (f64)
+ *   Y[t][n] = sum_i Wd[n][i] a_i,  S[t][n] = sum_i |Wd[n][i] a_i|
+ * with Wgu[2I][H] the dequantized gate|up rows (gate 0..I-1, up I..2I-1) and
+ * Wd[H][I], both Q4.  This is one routed pair of the MoE chain with weight 1
+ * applied to every token: the denoiser block's GEMM chain gemm(TG, TU) ->
+ * swiglu -> gemm(TD) ("cortiq-engine 0.8.3 src/gpu_metal/qi21.rs", fn blocks
+ * and its module header).  A_out (nullable, [T][I]) receives a. */
+void or_ffn(const double* X, int64_t T, int64_t H, int64_t I,
+            const uint8_t* gu_q, const uint16_t* gu_s, const uint8_t* d_q, const uint16_t* d_s,
+            double* Y, double* S, double* A_out) {
+    float* wgu = (float*)malloc(sizeof(float) * (size_t)(2 * I * H));
+    float* wd = (float*)malloc(sizeof(float) * (size_t)(H * I));
+    or_dequant_q4(gu_q, gu_s, 2 * I, H, wgu);
+    or_dequant_q4(d_q, d_s, H, I, wd);
+#pragma omp parallel
+    {
+        double* a = (double*)malloc(sizeof(double) * (size_t)I);
+#pragma omp for schedule(dynamic)
+        for (int64_t t = 0; t < T; t++) {
+            const double* x = X + t * H;
+            for (int64_t i = 0; i < I; i++) {
+                double g = 0.0, u = 0.0;
+                for (int64_t k = 0; k < H; k++) g += (double)wgu[i * H + k] * x[k];
+                for (int64_t k = 0; k < H; k++) u += (double)wgu[(I + i) * H + k] * x[k];
+                a[i] = g / (1.0 + exp(-g)) * u;
+                if (A_out) A_out[t * I + i] = a[i];
+            }
+            for (int64_t n = 0; n < H; n++) {
+                double acc = 0.0, abs_acc = 0.0;
+                for (int64_t i = 0; i < I; i++) {
+                    double p = (double)wd[n * I + i] * a[i];
+                    acc += p;
+                    abs_acc += fabs(p);
+                }
+                Y[t * H + n] = acc;
+                S[t * H + n] = abs_acc;
+            }
+        }
+        free(a);
+    }
+    free(wgu);
+    free(wd);
 }

@@ -427,3 +427,78 @@ def test_routing_ties_prefer_lower_index_and_renormalise():
     assert abs(float(w.sum()) - 1.0) < 1e-6
     p = np.exp(np.array([2.0, 2.0, 2.0, 0.5]) - 2.0)
     assert np.allclose(w[0], p / p.sum(), rtol=1e-6)
+
+
+# ---- dense FFN chain -------------------------------------------------------
+
+def _dense_ffn_weights(seed, H, I):
+    rng = np.random.default_rng(seed)
+    gc, gs = synth.draw_q4(rng, 2 * I, H, signed=True)
+    dc, ds = synth.draw_q4(rng, H, I, signed=True)
+    return oracle.pack_q4(gc), gs, oracle.pack_q4(dc), ds
+
+
+def test_ffn_closed_form_one_hot_rows():
+    """Token t = unit vector e_{k_t}: g_i = gate[i][k_t], u_i = up[i][k_t]
+    exactly, a_i = silu(g_i) u_i, then y = Wd . a; a and y written out with
+    math.exp and exact sums (fsum)."""
+    H, I = 64, 32
+    rng = np.random.default_rng(61)
+    gc = np.full((2 * I, H), 8, np.uint8)
+    gc[:, :] = rng.integers(0, 16, (2 * I, H))
+    guq = oracle.pack_q4(gc)
+    gus = np.full((2 * I, H // 32), 0x3C00, np.uint16)          # scale 1: weights are nibble - 8
+    dc = rng.integers(0, 16, (H, I), dtype=np.uint8)
+    ds = rng.uniform(0.005, 0.02, (H, I // 32)).astype(np.float16).view(np.uint16)
+    dq = oracle.pack_q4(dc)
+    ks = [3, 17, 40, 63]
+    X = np.zeros((len(ks), H))
+    X[np.arange(len(ks)), ks] = 1.0
+    Y, S, A = oracle.ffn(X, guq, gus, dq, ds, I, want_a=True)
+    wd = (dc.astype(np.float64) - 8) * ds.view(np.float16).astype(np.float64).repeat(32, axis=1)
+    for t, k in enumerate(ks):
+        g = gc[:I, k].astype(np.float64) - 8
+        u = gc[I:, k].astype(np.float64) - 8
+        a = np.array([gi / (1 + math.exp(-gi)) * ui for gi, ui in zip(g, u)])
+        assert np.allclose(A[t], a, rtol=1e-15, atol=0)
+        y = np.array([math.fsum(wd[n] * a) for n in range(H)])
+        assert np.allclose(Y[t], y, rtol=1e-12, atol=1e-12)
+        assert np.allclose(S[t], np.abs(wd) @ np.abs(a), rtol=1e-12)
+
+
+def test_ffn_equals_one_expert_moe_with_unit_weight():
+    """The dense chain is the routed chain with one expert and weight 1 for
+    every token: equal to oracle.moe (E=1, top-1) bit for bit, and each row
+    equal to moe_pair on that token."""
+    H, I, T = 128, 64, 5
+    guq, gus, dq, ds = _dense_ffn_weights(62, H, I)
+    rng = np.random.default_rng(63)
+    X = oracle.x_to_f64(synth.draw_x(rng, T, H), "bf16")
+    Y, S = oracle.ffn(X, guq, gus, dq, ds, I)
+    Ym, Sm = oracle.moe(X, np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32), guq[None], gus[None],
+                        dq[None], ds[None], 1, I)
+    assert np.array_equal(Y, Ym) and np.array_equal(S, Sm)
+    wgu = oracle.dequant_q4(guq, gus, 2 * I, H)
+    wd = oracle.dequant_q4(dq, ds, H, I)
+    for t in range(T):
+        _, o, s = oracle.moe_pair(wgu, wd, X[t])
+        assert np.array_equal(Y[t], o) and np.array_equal(S[t], s)
+
+
+def test_ffn_matches_library_matmuls():
+    """g, u and y through torch's f64 matmul on the oracle's dequantized
+    weights, SiLU from torch: equal within f64 rounding of the sums."""
+    H, I, T = 256, 96, 7
+    guq, gus, dq, ds = _dense_ffn_weights(64, H, I)
+    rng = np.random.default_rng(65)
+    X = oracle.x_to_f64(synth.draw_x(rng, T, H, 0.5), "bf16")
+    Y, S, A = oracle.ffn(X, guq, gus, dq, ds, I, want_a=True)
+    wgu = torch.from_numpy(oracle.dequant_q4(guq, gus, 2 * I, H).astype(np.float64))
+    wd = torch.from_numpy(oracle.dequant_q4(dq, ds, H, I).astype(np.float64))
+    x = torch.from_numpy(X)
+    G = x @ wgu[:I].T
+    U = x @ wgu[I:].T
+    At = torch.nn.functional.silu(G) * U
+    Yt = At @ wd.T
+    assert np.allclose(A, At.numpy(), rtol=1e-12, atol=1e-13)
+    assert np.all(np.abs(Y - Yt.numpy()) <= 1e-12 * S + 1e-15)

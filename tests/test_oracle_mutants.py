@@ -79,3 +79,64 @@ def test_unmutated_copy_passes():
 def test_mutant_fails_pins(name):
     with tempfile.TemporaryDirectory() as tmp:
         assert not _pins_pass(_build_mutant(name, tmp)), f"mutant {name} slipped through"
+
+
+# ---- the dense FFN chain: mutants against its one-hot closed form ----------
+
+FFN_MUTANTS = {
+    "ffn_gate_up_swapped": ("g += (double)wgu[i * H + k] * x[k];\n                for (int64_t k = 0; k < H; k++) u += (double)wgu[(I + i) * H + k] * x[k];",
+                            "u += (double)wgu[i * H + k] * x[k];\n                for (int64_t k = 0; k < H; k++) g += (double)wgu[(I + i) * H + k] * x[k];"),
+    "ffn_silu_sign": ("                a[i] = g / (1.0 + exp(-g)) * u;\n                if (A_out)",
+                      "                a[i] = g / (1.0 + exp(g)) * u;\n                if (A_out)"),
+    "ffn_down_transposed": ("wd[n * I + i]", "wd[i * H + n]"),
+    "ffn_down_skips_last": ("for (int64_t i = 0; i < I; i++) {\n                    double p", "for (int64_t i = 0; i + 1 < I; i++) {\n                    double p"),
+}
+
+
+def _ffn_closed_form_passes(lib):
+    import math
+    H = I = 64
+    rng = np.random.default_rng(71)
+    gc = rng.integers(0, 16, (2 * I, H), dtype=np.uint8)
+    dc = rng.integers(0, 16, (H, I), dtype=np.uint8)
+    pack = lambda c: (c.reshape(c.shape[0], -1, 2, 16)[:, :, 0, :] | (c.reshape(c.shape[0], -1, 2, 16)[:, :, 1, :] << 4)).reshape(c.shape[0], -1).astype(np.uint8)
+    guq, dq = pack(gc), pack(dc)
+    gus = np.full((2 * I, H // 32), 0x3C00, np.uint16)
+    ds = np.full((H, I // 32), 0x3C00, np.uint16)
+    ks = [5, 30]
+    X = np.zeros((2, H))
+    X[[0, 1], ks] = 1.0
+    Y = np.empty((2, H))
+    S = np.empty((2, H))
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)
+    i64 = ctypes.c_int64
+    lib.or_ffn(p(X), i64(2), i64(H), i64(I), p(guq), p(gus), p(dq), p(ds), p(Y), p(S), None)
+    wd = dc.astype(np.float64) - 8
+    for t, k in enumerate(ks):
+        a = [(g - 8) / (1 + math.exp(-(g - 8))) * (u - 8) for g, u in zip(gc[:I, k].astype(float), gc[I:, k].astype(float))]
+        y = np.array([math.fsum(wd[n] * a) for n in range(H)])
+        if not np.allclose(Y[t], y, rtol=1e-12, atol=1e-12):
+            return False
+    return True
+
+
+def test_unmutated_ffn_passes():
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "orig.c")
+        open(path, "w").write(open(SRC).read())
+        so = os.path.join(tmp, "orig.so")
+        subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", path, "-o", so, "-lm"])
+        assert _ffn_closed_form_passes(ctypes.CDLL(so))
+
+
+@pytest.mark.parametrize("name", sorted(FFN_MUTANTS))
+def test_ffn_mutant_fails_closed_form(name):
+    src = open(SRC).read()
+    old, new = FFN_MUTANTS[name]
+    assert src.count(old) == 1, name
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, f"{name}.c")
+        open(path, "w").write(src.replace(old, new))
+        so = os.path.join(tmp, f"{name}.so")
+        subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", path, "-o", so, "-lm"])
+        assert not _ffn_closed_form_passes(ctypes.CDLL(so)), f"mutant {name} slipped through"
