@@ -137,6 +137,25 @@ def _moe_calls(cq, m, dev):
                  h2d=[X, idx, w], d2h=[Y])], touched
 
 
+def _ffn_calls(cq, gu, dn, dev):
+    """The denoiser block as one chained call: gate/up GEMM with SwiGLU in its
+    epilogue, then the down GEMM, on the configured weights and the gate/up X."""
+    import torch
+    from block_quantized_weight_02_gb300 import pack
+    T, H, I = gu["T"], gu["K"], gu["N"] // 2
+    X = _dev_x(gu["x"], gu["x_dtype"], dev)
+    guq = torch.from_numpy(pack.pack_q4(gu["codes"])).to(dev)
+    gus = _u16(gu["scales"], dev)
+    dq = torch.from_numpy(pack.pack_q4(dn["codes"])).to(dev)
+    ds = _u16(dn["scales"], dev)
+    Y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(cq.cq_ffn_q4_workspace_bytes(T, H, I), dtype=torch.uint8, device=dev)
+    wbytes = (2 * I * H + H * I) * 9 // 16
+    return [Call("ffn chain q4->bf16", lambda: cq.cq_ffn_q4(X, guq, gus, dq, ds, Y, ws),
+                 2.0 * T * (2 * I * H + H * I), wbytes, X.numel() * 2 + Y.numel() * 2, 4,
+                 h2d=[X], d2h=[Y])]
+
+
 def _dtype_of(name, info):
     """The arithmetic each call of the workload runs in: the tcgen05 path (T > 32)
     multiplies guarded fp16 activations by fp16 weights; the weight-streaming path
@@ -172,6 +191,11 @@ def build_workload(name, dev, max_sets=16):
         gu, dn = synth.c3()
         make = lambda: _q4_calls(cq, gu, ["bf16"], dev, "gate/up") + _q4_calls(cq, dn, ["bf16"], dev, "down")
         info = {"T": 1024, "gate_up": [3072, 24576], "down": [12288, 3072], "formats": ["q4"], "outputs": ["bf16"]}
+    elif name == "denoiser_ffn_chain":
+        gu, dn = synth.c3()
+        make = lambda: _ffn_calls(cq, gu, dn, dev)
+        info = {"T": 1024, "H": 3072, "I": 12288, "formats": ["q4"], "outputs": ["bf16"],
+                "chain": "gate/up + SwiGLU epilogue -> guard -> down"}
     elif name == "moe_panels":
         m = synth.c4()
         calls, touched = _moe_calls(cq, m, dev)
@@ -262,7 +286,7 @@ def whole_job_rate(units_per_step: float, world: int, ms_per_step_max: float) ->
     return units_per_step * world / (ms_per_step_max * 1e-3)
 
 
-PER_CONFIG = (["smallest_q4", "prefill_projection_4096", "moe_panels"]
+PER_CONFIG = (["smallest_q4", "prefill_projection_4096", "denoiser_ffn_chain", "moe_panels"]
               + [f"sweep_{f}_T{t}" for f in ("q4", "q8") for t in (1, 8, 32, 128, 512, 2048)])
 
 TRAFFIC_MD = os.path.join(ROOT, "profiles", "traffic_per_call.md")

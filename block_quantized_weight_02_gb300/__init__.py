@@ -31,6 +31,9 @@ _SIGS = {
     "cq_gemm_q4_noalloc": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p, _c_int, _c_p]),
     "cq_gemm_q8row": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p, _c_int, _c_p]),
     "cq_moe_workspace_bytes": (_c_sz, [_c_i64] * 5),
+    "cq_ffn_q4_workspace_bytes": (_c_sz, [_c_i64] * 3),
+    "cq_ffn_q4": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_sz,
+                           _c_p]),
     "cq_moe_panels": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p,
                                _c_p, _c_p, _c_p, _c_int, _c_p, _c_sz, _c_p]),
     "cq_moe_layout": (_c_int, [_c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p]),
@@ -142,6 +145,22 @@ def cq_moe_panels(X, idx, w, Wgu_q, Wgu_s, Wd_q, Wd_s, Y, ws, stream=None, raise
     st = lib().cq_moe_panels(_ptr(X), _xt(X), T, H, E, twoI // 2, topk, _ptr(idx), _ptr(w), _ptr(Wgu_q),
                              _ptr(Wgu_s), _ptr(Wd_q), _ptr(Wd_s), _ptr(Y), _xt(Y), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream))
+    if raise_on_error:
+        _check(st)
+    return st
+
+
+def cq_ffn_q4_workspace_bytes(T, H, I) -> int:
+    return lib().cq_ffn_q4_workspace_bytes(T, H, I)
+
+
+def cq_ffn_q4(X, Wgu_q, Wgu_s, Wd_q, Wd_s, Y, ws, stream=None, raise_on_error=True):
+    """Y[T][H] = Wd . (silu(Wg . x) * (Wu . x)) per token; Wgu_q uint8 [2I][H/2]
+    (gate rows then up rows), Wd_q uint8 [H][I/2], fp16-bit scales."""
+    T, H = X.shape
+    I = Wgu_q.shape[0] // 2
+    st = lib().cq_ffn_q4(_ptr(X), _xt(X), T, H, I, _ptr(Wgu_q), _ptr(Wgu_s), _ptr(Wd_q), _ptr(Wd_s), _ptr(Y), _xt(Y),
+                         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     if raise_on_error:
         _check(st)
     return st

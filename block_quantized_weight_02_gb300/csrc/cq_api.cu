@@ -6,7 +6,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "cq_internal.h"
 
@@ -53,6 +55,59 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// ---- per-stream device error words ----------------------------------------
+// A fixed table in device memory (every GPU that loads the library holds it):
+// slot 0 is shared by the streams beyond the first CQ_ERR_SLOTS - 1 of a device,
+// every other slot belongs to one (device, stream) pair from its first call on.
+constexpr int CQ_ERR_SLOTS = 1024;
+static __device__ int g_err_slots[CQ_ERR_SLOTS];
+
+namespace {
+constexpr int MAX_DEVICES = 64;
+std::mutex g_slot_mu;
+int* g_slot_base[MAX_DEVICES] = {};
+int g_slot_next[MAX_DEVICES] = {};
+std::map<std::pair<int, uintptr_t>, int>& slot_map() {
+    static std::map<std::pair<int, uintptr_t>, int> m;
+    return m;
+}
+}  // namespace
+
+int* stream_error_word(cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "cudaGetDevice");
+        return nullptr;
+    }
+    if (dev < 0 || dev >= MAX_DEVICES) {
+        fail(CQ_ERR_ARG, "device index %d out of range", dev);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_slot_mu);
+    if (!g_slot_base[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_err_slots);   // the array's address on this device
+        if (e != cudaSuccess || !p) {
+            cuda_fail(e, "cudaGetSymbolAddress (device error words)");
+            return nullptr;
+        }
+        g_slot_base[dev] = static_cast<int*>(p);
+        g_slot_next[dev] = 1;
+    }
+    auto& m = slot_map();
+    const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(s));
+    auto it = m.find(key);
+    int slot = 0;
+    if (it != m.end()) {
+        slot = it->second;
+    } else if (g_slot_next[dev] < CQ_ERR_SLOTS) {
+        slot = g_slot_next[dev]++;
+        m.emplace(key, slot);
+    }
+    return g_slot_base[dev] + slot;
 }
 
 int num_sms() {
@@ -118,6 +173,23 @@ MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
     l.ah = o; o += up(P * I * 2);
     l.rsa = o; o += up(P * 4);
     l.eo = o; o += up(P * H * 4);
+    l.total = o;
+    return l;
+}
+
+// Workspace of the dense FFN chain: guarded fp16 X and its scales, the f32
+// SwiGLU activations a, their guarded fp16 copy and its scales.
+struct FfnLayout {
+    size_t xh, rsx, a, ah, rsa, total;
+};
+FfnLayout ffn_layout(int64_t T, int64_t H, int64_t I) {
+    FfnLayout l;
+    size_t o = 0;
+    l.xh = o; o += up((size_t)T * H * 2);
+    l.rsx = o; o += up((size_t)T * 4);
+    l.a = o; o += up((size_t)T * I * 4);
+    l.ah = o; o += up((size_t)T * I * 2);
+    l.rsa = o; o += up((size_t)T * 4);
     l.total = o;
     return l;
 }
@@ -221,15 +293,17 @@ cq_status cq_gemm_q4(const void* X, int xt, int64_t T, int64_t K, const uint8_t*
     if ((reinterpret_cast<uintptr_t>(ws) & (ALIGN - 1)) || ws_bytes < q4_ws_bytes(T, K)) return fail(CQ_ERR_WORKSPACE, "cq_gemm_q4: workspace needs %zu bytes, 256-aligned", q4_ws_bytes(T, K));
     if ((st = check_arch())) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = stream_error_word(s);
+    if (!err) return CQ_ERR_CUDA;
     const Q4Ws w = q4_ws(ws, T, K);
     const bool skinny = use_skinny(T);
     if (skinny && T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4: the weight-streaming path serves T <= 32");
     if (skinny) {   // the activations as given: no guard pass
-        SkinnyDense a = {X, xt == CQ_BF16 ? 1 : 0, nullptr, nullptr, Wq, Ws, T, K, N, Y, yt};
+        SkinnyDense a = {X, xt == CQ_BF16 ? 1 : 0, nullptr, nullptr, Wq, Ws, T, K, N, Y, yt, err};
         return launched(launch_skinny_q4(a, s), "weight-streaming Q4 GEMM");
     }
     if ((st = launched(launch_x_half(X, xt, T, K, w.xh, w.rsx, s), "activation guard pass"))) return st;
-    TcArgs a = {w.xh, 0, w.rsx, nullptr, Wq, Ws, T, K, N, Y, yt};
+    TcArgs a = {w.xh, 0, w.rsx, nullptr, Wq, Ws, T, K, N, Y, yt, err};
     return launched(launch_tc_q4(a, s), "tcgen05 Q4 GEMM");
 }
 
@@ -244,12 +318,14 @@ cq_status cq_gemm_q8row(const void* X, int xt, int64_t T, int64_t K, const int8_
     if (!aligned16(X) || !aligned16(Wq) || !aligned16(rs) || !aligned16(Y)) return fail(CQ_ERR_ALIGN, "cq_gemm_q8row: pointers must be 16-byte aligned");
     if ((st = check_arch())) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = stream_error_word(s);
+    if (!err) return CQ_ERR_CUDA;
     if (use_skinny(T)) {
         if (T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q8row: the weight-streaming path serves T <= 32");
-        SkinnyDense a = {X, xt == CQ_BF16, nullptr, rs, reinterpret_cast<const uint8_t*>(Wq), nullptr, T, K, N, Y, yt};
+        SkinnyDense a = {X, xt == CQ_BF16, nullptr, rs, reinterpret_cast<const uint8_t*>(Wq), nullptr, T, K, N, Y, yt, err};
         return launched(launch_skinny_q8(a, s), "weight-streaming Q8-row GEMM");
     }
-    TcArgs a = {X, xt == CQ_BF16, nullptr, rs, reinterpret_cast<const uint8_t*>(Wq), nullptr, T, K, N, Y, yt};
+    TcArgs a = {X, xt == CQ_BF16, nullptr, rs, reinterpret_cast<const uint8_t*>(Wq), nullptr, T, K, N, Y, yt, err};
     return launched(launch_tc_q8(a, s), "tcgen05 Q8-row GEMM");
 }
 
@@ -277,9 +353,12 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E, 
     if ((reinterpret_cast<uintptr_t>(ws) & (ALIGN - 1)) || ws_bytes < l.total) return fail(CQ_ERR_WORKSPACE, "cq_moe_panels: workspace needs %zu bytes, 256-aligned", l.total);
     if ((st = check_arch())) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = stream_error_word(s);
+    if (!err) return CQ_ERR_CUDA;
     uint8_t* b = static_cast<uint8_t*>(ws);
     int32_t* status = reinterpret_cast<int32_t*>(b + l.status);
     SkinnyMoe m = {};
+    m.err = err;
     m.xh = reinterpret_cast<uint16_t*>(b + l.xh);
     m.rsx = reinterpret_cast<float*>(b + l.rsx);
     m.ah = reinterpret_cast<uint16_t*>(b + l.ah);
@@ -303,12 +382,52 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E, 
     int32_t* act = reinterpret_cast<int32_t*>(b + l.act);
     m.act = act;
     m.n_act = act + E;
-    if ((st = launched(launch_moe_route(idx, T, topk, E, const_cast<int32_t*>(m.seg), const_cast<int32_t*>(m.perm), inv, act, act + E, status, s), "MoE routing layout"))) return st;
+    if ((st = launched(launch_moe_route(idx, T, topk, E, const_cast<int32_t*>(m.seg), const_cast<int32_t*>(m.perm), inv, act, act + E, status, err, s), "MoE routing layout"))) return st;
     if ((st = launched(launch_x_half_gather(X, xt, T * topk, H, const_cast<uint16_t*>(m.xh), const_cast<float*>(m.rsx), m.perm, (int)topk, status, s), "MoE activation gather + guard pass"))) return st;
     if ((st = launched(launch_moe_gateup(m, s), "MoE gate/up panels"))) return st;
     if ((st = launched(launch_a_half(m.a, T * topk, I, const_cast<uint16_t*>(m.ah), const_cast<float*>(m.rsa), status, s), "MoE SwiGLU guard pass"))) return st;
     if ((st = launched(launch_moe_down(m, s), "MoE down panels"))) return st;
     return launched(launch_moe_combine(m.eo, inv, T, topk, H, Y, yt, status, s), "MoE combine");
+}
+
+size_t cq_ffn_q4_workspace_bytes(int64_t T, int64_t H, int64_t I) {
+    if (T < 1 || H < 1 || I < 1) return 0;
+    return ffn_layout(T, H, I).total;
+}
+
+cq_status cq_ffn_q4(const void* X, int xt, int64_t T, int64_t H, int64_t I, const uint8_t* Wgu_q,
+                    const uint16_t* Wgu_s, const uint8_t* Wd_q, const uint16_t* Wd_s, void* Y, int yt, void* ws,
+                    size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    if (!X || !Wgu_q || !Wgu_s || !Wd_q || !Wd_s || !Y || !ws) return fail(CQ_ERR_NULL, "cq_ffn_q4: null pointer");
+    cq_status st;
+    if ((st = check_x(xt)) || (st = check_y(yt))) return st;
+    if (T < 1 || H < 256 || H % 256 || I < 256 || I % 256 || T > (1LL << 31) - 1 || H > (1LL << 30) ||
+        I > (1LL << 30))
+        return fail(CQ_ERR_SHAPE, "cq_ffn_q4: need T>=1, H%%256==0, I%%256==0 (T=%lld H=%lld I=%lld)", (long long)T,
+                    (long long)H, (long long)I);
+    if (!aligned16(X) || !aligned16(Wgu_q) || !aligned16(Wgu_s) || !aligned16(Wd_q) || !aligned16(Wd_s) ||
+        !aligned16(Y))
+        return fail(CQ_ERR_ALIGN, "cq_ffn_q4: pointers must be 16-byte aligned");
+    const FfnLayout l = ffn_layout(T, H, I);
+    if ((reinterpret_cast<uintptr_t>(ws) & (ALIGN - 1)) || ws_bytes < l.total)
+        return fail(CQ_ERR_WORKSPACE, "cq_ffn_q4: workspace needs %zu bytes, 256-aligned", l.total);
+    if ((st = check_arch())) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = stream_error_word(s);
+    if (!err) return CQ_ERR_CUDA;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    uint16_t* xh = reinterpret_cast<uint16_t*>(b + l.xh);
+    float* rsx = reinterpret_cast<float*>(b + l.rsx);
+    float* a = reinterpret_cast<float*>(b + l.a);
+    uint16_t* ah = reinterpret_cast<uint16_t*>(b + l.ah);
+    float* rsa = reinterpret_cast<float*>(b + l.rsa);
+    if ((st = launched(launch_x_half(X, xt, T, H, xh, rsx, s), "FFN activation guard pass"))) return st;
+    TcArgs g = {xh, 0, rsx, nullptr, Wgu_q, Wgu_s, T, H, I, a, CQ_F32, err};
+    if ((st = launched(launch_tc_q4_gateup(g, s), "FFN gate/up GEMM + SwiGLU"))) return st;
+    if ((st = launched(launch_a_half(a, T, I, ah, rsa, nullptr, s), "FFN SwiGLU guard pass"))) return st;
+    TcArgs d = {ah, 0, rsa, nullptr, Wd_q, Wd_s, T, I, H, Y, yt, err};
+    return launched(launch_tc_q4(d, s), "FFN down GEMM");
 }
 
 cq_status cq_moe_layout(const void* ws, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk, int32_t* perm_out,
@@ -344,10 +463,16 @@ cq_status cq_dequant_q8row(const int8_t* Wq, const float* rs, int64_t N, int64_t
 }
 
 cq_status cq_get_device_error(void* stream) {
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    const int a = take_error_aux(), b = take_error_skinny(), c = take_error_tc();
-    const int v = a ? a : (b ? b : c);
+    g_msg[0] = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* word = stream_error_word(s);
+    if (!word) return CQ_ERR_CUDA;
+    // read, then clear, with copies ordered on this stream only
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, word, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(word, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the stream's device error word");
     if (v == DEV_INDEX) return fail(CQ_ERR_INDEX, "a routing index is outside [0, E)");
     if (v == DEV_TIMEOUT) return fail(CQ_ERR_TIMEOUT, "a device pipeline wait ran past its limit");
     return CQ_OK;

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 #include <cstddef>
 #include <cstdio>
@@ -13,18 +14,27 @@ namespace cq {
 // Device error word values (shared by all kernels; first writer wins).
 enum DevErr : int { DEV_OK = 0, DEV_INDEX = 1, DEV_TIMEOUT = 2 };
 
+// Process-wide options (every thread and stream sees the same values); each
+// field is read and written atomically.
 struct Options {
-    int64_t small_t_max = 32;
-    int64_t force_path = 0;
-    int64_t wait_ns = 1000000000LL;
-    int64_t test_stall = 0;
-    int64_t trace = 0;
-    int64_t tc_bn = 0;
-    int64_t tc_ksplit = 0;
-    int64_t tc_amode = 0;
-    int64_t tc_pair = 0;
+    std::atomic<int64_t> small_t_max{32};
+    std::atomic<int64_t> force_path{0};
+    std::atomic<int64_t> wait_ns{1000000000LL};
+    std::atomic<int64_t> test_stall{0};
+    std::atomic<int64_t> trace{0};
+    std::atomic<int64_t> tc_bn{0};
+    std::atomic<int64_t> tc_ksplit{0};
+    std::atomic<int64_t> tc_amode{0};
+    std::atomic<int64_t> tc_pair{0};
 };
 Options& options();
+
+// The device error word of a stream: one slot of a fixed table in device
+// memory, assigned to the (device, stream) pair on first use.  Kernels set it
+// (first writer wins) and cq_get_device_error(stream) reads and clears it with
+// copies ordered on that stream only.  Returns nullptr (and sets the message)
+// if the runtime fails.
+int* stream_error_word(cudaStream_t s);
 
 // Host error reporting (a thread-local "decline: ..." message).
 cq_status fail(cq_status st, const char* fmt, ...);
@@ -41,11 +51,6 @@ int num_sms();
 
 // ---- launchers (one translation unit each) ------------------------------
 
-// Per-TU device error words: read-and-clear (synchronous copies).
-int take_error_aux();
-int take_error_skinny();
-int take_error_tc();
-
 // aux kernels
 cudaError_t launch_dequant_q4(const uint8_t* wq, const uint16_t* ws, int64_t N, int64_t K, float* w, cudaStream_t s);
 cudaError_t launch_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, int64_t K, float* w, cudaStream_t s);
@@ -60,8 +65,9 @@ cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K,
 struct MoeWs;  // workspace carve-up (cq_api.cu)
 // Also writes the active experts (count > 0, ascending) to act[] and their number to *n_act.
 cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
-                             int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, cudaStream_t s);
-// Writes the weight-streaming order (the down panels read it).
+                             int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, int* err, cudaStream_t s);
+// f32 rows -> fp16 behind a per-row power-of-two guard, in the Q4 streaming
+// order (the down panels and the tcgen05 Q4 GEMM read it); status nullable.
 cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,
                           cudaStream_t s);
 cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, int64_t topk, int64_t H, void* y,
@@ -78,6 +84,7 @@ struct SkinnyDense {
     int64_t T, K, N;
     void* y;
     int yt;
+    int* err;            // the stream's device error word
 };
 cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s);
 cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s);
@@ -98,6 +105,7 @@ struct SkinnyMoe {
     float* a;               // [P][I] f32 SwiGLU output, grouped order
     float* eo;              // [P][H] f32 weighted expert outputs, grouped order
     int64_t T, H, I, E, topk;
+    int* err;               // the stream's device error word
 };
 cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s);
 cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s);
@@ -113,8 +121,12 @@ struct TcArgs {
     int64_t T, K, N;
     void* y;
     int yt;
+    int* err;            // the stream's device error word
 };
 cudaError_t launch_tc_q4(const TcArgs& a, cudaStream_t s);
 cudaError_t launch_tc_q8(const TcArgs& a, cudaStream_t s);
+// Gate/up mode: wq is the Q4 [2I][K] gate|up matrix, N = I; y = a[T][I] f32,
+// a = silu(gate) * up (x: guarded fp16 in the streaming order, rsx its scales).
+cudaError_t launch_tc_q4_gateup(const TcArgs& a, cudaStream_t s);
 
 }  // namespace cq

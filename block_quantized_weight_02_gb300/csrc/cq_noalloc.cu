@@ -82,17 +82,19 @@ extern "C" cq_status cq_gemm_q4_noalloc(const void* X, int xt, int64_t T, int64_
     uint16_t* xh = static_cast<uint16_t*>(scratch);
     float* rsx = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + xh_bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = stream_error_word(s);
+    if (!err) return CQ_ERR_CUDA;
     const Options& o = options();
     const bool skinny = o.force_path == 1 || (o.force_path == 0 && T <= o.small_t_max);
     if (skinny && T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4_noalloc: the weight-streaming path serves T <= 32");
     if (skinny) {   // the activations as given: no guard pass
-        SkinnyDense a = {X, xt == CQ_BF16 ? 1 : 0, nullptr, nullptr, Wq, Ws, T, K, N, Y, yt};
+        SkinnyDense a = {X, xt == CQ_BF16 ? 1 : 0, nullptr, nullptr, Wq, Ws, T, K, N, Y, yt, err};
         e = launch_skinny_q4(a, s);
         return e == cudaSuccess ? CQ_OK : cuda_fail(e, "weight-streaming Q4 GEMM");
     }
     e = launch_x_half(X, xt, T, K, xh, rsx, s);
     if (e != cudaSuccess) return cuda_fail(e, "activation guard pass");
-    TcArgs a = {xh, 0, rsx, nullptr, Wq, Ws, T, K, N, Y, yt};
+    TcArgs a = {xh, 0, rsx, nullptr, Wq, Ws, T, K, N, Y, yt, err};
     e = launch_tc_q4(a, s);
     return e == cudaSuccess ? CQ_OK : cuda_fail(e, "tcgen05 Q4 GEMM");
 }

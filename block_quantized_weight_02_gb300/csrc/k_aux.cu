@@ -9,8 +9,6 @@
 
 namespace cq {
 
-__device__ int g_err_aux = 0;
-
 // Launch with a programmatic dependency on the previous kernel in the
 // stream: the kernel may be scheduled while that one finishes, and waits for
 // it (griddepcontrol.wait) before touching anything.
@@ -29,14 +27,8 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-__device__ __forceinline__ void set_err(int code) { atomicCAS(&g_err_aux, 0, code); }
-
-int take_error_aux() {
-    int v = 0, z = 0;
-    cudaMemcpyFromSymbol(&v, g_err_aux, sizeof(int));
-    cudaMemcpyToSymbol(g_err_aux, &z, sizeof(int));
-    return v;
-}
+// First writer wins: a later error of the same call does not replace the first.
+__device__ __forceinline__ void set_err(int* err, int code) { atomicCAS(err, 0, code); }
 
 // ---- dequantization hooks ---------------------------------------------
 // Q4 ("oxinfer 0.0.5 src/metal.rs", Dequantizers / load(Q4W ...)): one
@@ -241,7 +233,8 @@ cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K,
 __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ idx, int P, int E,
                                                    int32_t* __restrict__ seg, int32_t* __restrict__ perm,
                                                    int32_t* __restrict__ inv, int32_t* __restrict__ act,
-                                                   int32_t* __restrict__ n_act, int32_t* __restrict__ status) {
+                                                   int32_t* __restrict__ n_act, int32_t* __restrict__ status,
+                                                   int* __restrict__ err) {
     pdl_launch_dependents();  // the gather pass after this one may be scheduled now
     pdl_wait();               // idx may come from the previous kernel; the previous call's readers are done
     extern __shared__ int sh[];
@@ -264,7 +257,7 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
     if (bad) {
         if (tid == 0) {
             *status = 1;
-            set_err(DEV_INDEX);
+            set_err(err, DEV_INDEX);
         }
         return;
     }
@@ -338,10 +331,10 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
 }
 
 cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
-                             int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, cudaStream_t s) {
+                             int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, int* err, cudaStream_t s) {
     const size_t smem = (size_t)(2 * E) * sizeof(int);
     return launch_pdl(k_moe_route, dim3(1), dim3(256), smem, s, idx, (int)(T * topk), (int)E, seg, perm, inv, act, n_act,
-                      status);
+                      status, err);
 }
 
 // SwiGLU activations (f32, grouped order) -> fp16 behind the same
@@ -351,7 +344,7 @@ __global__ void __launch_bounds__(256) k_a_half(const float* __restrict__ a, int
                                                 float* __restrict__ rsa, const int32_t* __restrict__ status) {
     pdl_launch_dependents();
     pdl_wait();
-    if (*status != 0) return;
+    if (status && *status != 0) return;
     __shared__ float red[8];
     const int64_t row = blockIdx.x;
     const float4* src = reinterpret_cast<const float4*>(a + row * I);

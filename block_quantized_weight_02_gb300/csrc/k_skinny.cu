@@ -60,15 +60,6 @@ namespace cg = cooperative_groups;
 
 namespace cq {
 
-__device__ int g_err_skinny = 0;
-
-int take_error_skinny() {
-    int v = 0, z = 0;
-    cudaMemcpyFromSymbol(&v, g_err_skinny, sizeof(int));
-    cudaMemcpyToSymbol(g_err_skinny, &z, sizeof(int));
-    return v;
-}
-
 namespace {
 
 constexpr int CONSUMERS = 8;     // consumer warps, all of them in every stage
@@ -100,6 +91,7 @@ struct Params {
     const int32_t* act;   // MoE: active experts, ascending
     const int32_t* n_act; // MoE: number of active experts
     int rbs;              // MoE: row blocks per expert matrix
+    int* err;             // the stream's device error word
 };
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -388,7 +380,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
             }
             if (!ok) {
                 *abort_flag = 1;
-                atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
+                atomicCAS(p.err, 0, DEV_TIMEOUT);
             }
             if (*abort_flag && last_gi >= 0) {  // this lane's last copies must land before the CTA can exit
                 mbar_wait(full_bar(s), last_phase, p.wait_ns, never_flag);
@@ -432,7 +424,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 if (!mbar_wait(full_bar((int)slot), phase, p.wait_ns, abort_flag)) {
                     ok = false;
                     *abort_flag = 1;
-                    atomicCAS(&g_err_skinny, 0, DEV_TIMEOUT);
+                    atomicCAS(p.err, 0, DEV_TIMEOUT);
                     break;
                 }
                 const uint32_t sW = smem_base + slot * (uint32_t)G::BYTES;
@@ -786,6 +778,7 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     p.yt = a.yt;
     p.wait_ns = (uint64_t)options().wait_ns;
     p.pdl = 1;
+    p.err = a.err;
     // K split (cluster size): as many CTAs as fit two per SM (a CTA alone keeps too few
     // bytes in flight to draw its share of the bandwidth), at least two stages each.
     const int64_t rbs = (a.N + cf.rb - 1) / cf.rb;
@@ -834,6 +827,7 @@ cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s) {
     p.act = m.act;
     p.n_act = m.n_act;
     p.pdl = 1;
+    p.err = m.err;
     p.rbs = (int)(m.I / (RB / 2));
     // persistent: two CTAs per SM share the (active expert x row block) items
     const int64_t items_max = m.E * p.rbs;
@@ -862,6 +856,7 @@ cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s) {
     p.act = m.act;
     p.n_act = m.n_act;
     p.pdl = 1;
+    p.err = m.err;
     p.rbs = (int)(m.H / RB);
     const int64_t items_max = m.E * p.rbs;
     dim3 grid((unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items_max), 1, 1);

@@ -1,841 +1,21 @@
-// Large-T GEMM on the 5th-generation tensor cores (tcgen05, accumulator in
-// tensor memory), weights dequantized on the fly in shared memory.
-//
-// Y^T tile = W tile (128 weight rows, M) x X tile^T (BN activation rows, N),
-// K in stages of 64, loaded in super-stages of G stages (one weight box of
-// G * 32 or G * 64 bytes per row and one activation box of G 64-k chunks:
-// a TMA box costs nearly the same whatever its size, so fewer, larger boxes
-// keep the copies ahead of the tensor core).  Warp roles in a CTA of 576
-// threads:
-//   warp 16     TMA producers: lane s issues the weight box of super-slot s,
-//               lane LSS + s its activation box;
-//   warps 0-15  decoders: group w / 4 takes every fourth stage, warp w
-//               rows 32 (w % 4) .. +31 of it (one 64-k row per thread),
-//               decoded into the A operand (tensor memory by default, else
-//               the 128-byte swizzled K-major tile in shared memory); four
-//               stages are in decode at once.  Then the epilogue;
-//   warp 17     allocates the tensor memory and issues tcgen05.mma
-//               (M = 128, N = BN, K = 16) from one thread, a round of 2 or 4
-//               stages at a time, committing each round's decoded slots and
-//               each super-stage's load slot back, and the last round to the
-//               epilogue.
-// CTA pairs (cta_group::2): two neighbouring weight-row tiles share one MMA
-// of M = 256; each CTA decodes its own rows into its own tensor memory and
-// loads half of the activation rows; the even CTA issues.  K split: two CTAs
-// of a cluster take the two halves of K and exchange half of their f32
-// accumulators through distributed shared memory.  Epilogue: scaled,
-// staged in shared memory and stored with TMA per decoder group and chunk.
-// Q4 decode: (nibble - 8) * fp16 block scale, rounded once to fp16 (the
-// scale folded into the half operand, as in mma_tile of "oxinfer 0.0.5
-// src/metal.rs"); the activations arrive as fp16 behind a per-row
-// power-of-two guard whose inverse the epilogue applies, stored by the
-// guard pass in the streaming order inside each 32-k block, the order in
-// which two masks per word yield the nibble pairs; the decoded weights are
-// written in that same order, so the contraction is unchanged.  Q8-row decode:
-// int8 -> the activation type exactly; the row scale is applied to the f32
-// accumulator in the epilogue ("cortiq-engine 0.8.3 src/gpu_metal/qi21.rs",
-// module header on q8_row).
-// Every wait is time-bounded; on a timeout the CTA stops, lets copies in
-// flight land, frees its tensor memory and reports CQ_ERR_TIMEOUT.
-#include <algorithm>
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include "cq_internal.h"
-#include "cq_ptx.cuh"
+// Large-T Q4 / Q8-row GEMMs on the tcgen05 tensor cores: the dense
+// instantiations of the kernel in k_tc.cuh (which describes the design).
+#include "k_tc.cuh"
 
 namespace cq {
-
-__device__ int g_err_tc = 0;
-
-int take_error_tc() {
-    int v = 0, z = 0;
-    cudaMemcpyFromSymbol(&v, g_err_tc, sizeof(int));
-    cudaMemcpyToSymbol(g_err_tc, &z, sizeof(int));
-    return v;
-}
-
 namespace {
-
-constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-
-struct Params {
-    const float* rsx;
-    const float* rs;
-    const uint16_t* ws;   // Q4 block scales [N][K/32]
-    void* y;
-    int yt;
-    int64_t T, N, K;
-    uint64_t wait_ns;
-    int stall;
-    int pdl;   // launched with a programmatic dependency on the guard pass
-    int y_tma; // Y row pitch is a multiple of 16 bytes: tiles leave through a TMA store
-};
-
-__device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t w, uint32_t sel) {
-    return sub_f16x2(prmt(w ^ 0x80808080u, 0x64646464u, sel), 0x64806480u);
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-
-// Eight nibbles (bytes b0..b3 of w) -> four fp16 pairs (n - 8) * scale, each
-// rounded once, in the activations' streaming order: (low b0, low b2),
-// (high b0, high b2), (low b1, low b3), (high b1, high b3).  0x6400 | n is
-// 1024 + n and 0x6400 | (n << 4) is 1024 + 16 n; 1024 + n - 1032 and
-// (1024 + 16 n) / 16 - 72 are n - 8 exactly.
-__device__ __forceinline__ void decode_q4_word_scaled(uint32_t w, uint32_t sc, uint32_t* o) {
-    const uint32_t c6400 = 0x64006400u, k1032 = 0x64086408u, k16th = 0x2C002C00u, km72 = 0xD480D480u;
-    const uint32_t w8 = w >> 8;
-    o[0] = mul_f16x2(sub_f16x2(and_or<0x000F000Fu>(w, c6400), k1032), sc);
-    o[1] = mul_f16x2(fma_f16x2(and_or<0x00F000F0u>(w, c6400), k16th, km72), sc);
-    o[2] = mul_f16x2(sub_f16x2(and_or<0x000F000Fu>(w8, c6400), k1032), sc);
-    o[3] = mul_f16x2(fma_f16x2(and_or<0x00F000F0u>(w8, c6400), k16th, km72), sc);
-}
-
-template <int FMT>
-struct Raw;
-template <>
-struct Raw<0> { static constexpr int ROW = 32; };   // Q4: 64 k = 32 bytes per row and stage
-template <>
-struct Raw<1> { static constexpr int ROW = 64; };   // Q8: 64 bytes per row and stage
-
-// Loads come in super-stages of G stages (G x 64 k), two TMA boxes each: a TMA
-// box costs about the same however few bytes it holds, so the weight rows are
-// fetched G stages at a time (G * ROW bytes per row) and the activation tile as
-// one 3-D box of G 64-k chunks.
-// Shared memory per super-slot: X [G][BN rows][128 B] (each chunk one
-// 128-byte-swizzled K-major operand tile), then W [128 rows][G * ROW B]
-// (128- or 64-byte swizzle).  AM 0 adds AS decoded tiles [128][128 B] in
-// front; AM 1 keeps the decoded tiles in tensor memory.  With CTA pairs (CG 2)
-// each CTA holds half of the activation rows (its half of the MMA's B operand).
-template <int FMT, int BN, int G, int LSS, int AS, int AM, int CG = 1>
-struct Layout {
-    static constexpr int WROW = G * Raw<FMT>::ROW;            // 64 or 128 bytes
-    static constexpr int X_CHUNK = (BN / CG) * 128;
-    static constexpr int X_BYTES = G * X_CHUNK;
-    static constexpr int W_BYTES = BM * WROW;
-    static constexpr int SLOT = X_BYTES + W_BYTES;             // multiple of 1024
-    static constexpr int A_OFF = 0;
-    static constexpr int S_OFF = AM == 0 ? AS * A_BYTES : 0;
-    static constexpr int BAR_OFF = S_OFF + LSS * SLOT;
-    // Decoded slots are handed over in rounds of RS stages, NRB rounds in flight: four stages
-    // when the ring holds many stages (tensor-memory slots with BN < 256, or a CTA pair,
-    // whose half activation tiles leave room for more), else two, so that a round never
-    // waits for ring slots its own MMAs free.
-    static constexpr int RS = (AM == 1 && BN <= 128) ? 4 : 2;
-    static constexpr int NRB = AS / RS;
-    // When a round is one super-stage, the super-slot's release (committed after the
-    // round's MMAs) also frees the round's decoded slots: the decoders wait on it and no
-    // separate release is committed.  With LSS >= NRB no wait can fall two phases behind.
-    static constexpr bool MERGE = RS == G && LSS >= NRB;
-    // full[LSS], empty[LSS], afull[NRB], aempty[NRB] (one per round in flight), accf,
-    // xchg[4] (split K: one per decoder group); then tmem slot, abort, never
-    static constexpr int NBAR = 2 * LSS + 2 * NRB + 5;
-    static constexpr int MISC = NBAR * 8 + 16;
-    static constexpr int TOTAL = BAR_OFF + MISC + 1024;  // + alignment slack
-    // tensor memory: accumulator in columns [0, BN); AM 1 adds AS decoded A tiles of 32 columns
-    static constexpr int A_COL = BN;
-    static constexpr int NEED = AM == 0 ? BN : BN + AS * 32;
-    static constexpr int TMEM_COLS = NEED <= 32 ? 32 : NEED <= 64 ? 64 : NEED <= 128 ? 128 : NEED <= 256 ? 256 : 512;
-    static_assert(NEED <= 512, "tensor memory budget");
-    static_assert(SLOT % 1024 == 0 && X_CHUNK % 1024 == 0, "1024-byte aligned swizzled tiles");
-    static_assert(WROW == 32 || WROW == 64 || WROW == 128, "weight rows of 32, 64 or 128 bytes");
-};
-
-// Epilogue geometry: a CTA finishes NC columns of its tile (all BN, or its half under a
-// K split); each of the first NG decoder groups (all four from 64 columns, else group 0)
-// owns NC / NG of them and handles them CH at a time (one tensor-memory load, one
-// output box, one exchange copy per chunk).
-constexpr int ep_cols(int BN, int KS) { return KS > 1 ? BN / 2 : BN; }
-constexpr int ep_groups(int BN, int KS) { return ep_cols(BN, KS) >= 64 ? 4 : 1; }
-constexpr int ep_chunk(int BN, int KS) {
-    return (ep_cols(BN, KS) / ep_groups(BN, KS)) % 32 == 0 ? 32 : 16;
-}
-
-template <int CH>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[CH]) {
-    static_assert(CH == 16 || CH == 32, "16 or 32 columns per load");
-    if constexpr (CH == 32) tmem_ld_32x32b_x32(taddr, v);
-    else tmem_ld_32x32b_x16(taddr, v);
-}
-
-constexpr int DEC_WARPS = 16;                // 4 groups (stages kb % 4) x 4 row quarters
-constexpr int THREADS = (DEC_WARPS + 2) * 32;
-constexpr int PRODUCER_WARP = DEC_WARPS;
-constexpr int MMA_WARP = DEC_WARPS + 1;
-
-// int8 pair (bytes sel of w) -> bf16x2 exactly: with 0x43 as the high byte, the
-// low seven bits of v give 128 + (v & 127) and the sign bit gives 128 or 256
-// (0x4300 / 0x4380); their difference is v, an integer bf16 holds exactly.
-__device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
-    const uint32_t t = prmt(w, 0x43434343u, sel);
-    return sub_bf16x2(and_mask<0xFF7FFF7Fu>(t), and_mask<0xFF80FF80u>(t));
-}
-
-// KS: K split over a cluster of KS CTAs along z (1 or 2); the two partial
-// accumulators are exchanged through distributed shared memory and each CTA
-// finishes half of the tile's columns.
-// CG: CTA pairs along x (1 or 2).  With 2, two neighbouring weight-row tiles share
-// one 256-row MMA (cta_group::2): each CTA decodes its 128 rows into its own tensor
-// memory and loads half of the activation rows; the even CTA's MMA thread issues
-// for both once both CTAs' decoders have arrived on its barrier, and every release
-// it commits reaches both CTAs.  Each CTA's accumulator holds its rows x all BN
-// columns, so the epilogue is unchanged.  Cluster ranks run x fastest: the pair
-// peer is rank ^ 1, the K-split partner rank ^ CG.
-template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS, int CG>
-__global__ void __launch_bounds__(THREADS, 1)
-k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-     const __grid_constant__ CUtensorMap tmY, const Params p) {
-    using L = Layout<FMT, BN, G, LSS, AS, AM, CG>;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t sb = smem_u32(smem);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM;          // first weight row
-    const int t0 = blockIdx.y * BN;          // first activation row
-    const int kz = KS > 1 ? (int)blockIdx.z : 0;
-    const uint32_t crank = (KS > 1 || CG > 1) ? cluster_ctarank() : 0u;   // rank in the cluster
-    const int cx = CG > 1 ? (int)(crank & 1u) : 0;                // position in the CTA pair
-    const bool leader = cx == 0;                                   // issues the pair's MMAs
-    const uint16_t pair_mask = (uint16_t)(3u << (crank - (uint32_t)cx));
-    const int nk = (int)(p.K / BK) / KS;     // stages of this CTA's k range
-    const int k0 = kz * nk;                  // its first stage
-    const int ns = nk / G;                   // super-stages
-    const int j0 = k0 / G;
-
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-    const uint32_t bar0 = smem_u32(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (LSS + s); };
-    // Decoded slots come in rounds of RS stages (stages r RS .. r RS + RS - 1 in slots
-    // (r % NRB) RS ..): per round in flight one barrier says the round is decoded, one
-    // that its MMAs are done.
-    constexpr int RS = L::RS, NRB = L::NRB;
-    constexpr bool MERGE = L::MERGE;
-    auto afull_bar = [&](int rb) { return bar0 + 8u * (2 * LSS + rb); };
-    auto aempty_bar = [&](int rb) { return bar0 + 8u * (2 * LSS + NRB + rb); };
-    const uint32_t accf_bar = bar0 + 8u * (2 * LSS + 2 * NRB);
-    // split K: the partner's columns of decoder group g have arrived
-    auto xchg_bar = [&](int g) { return accf_bar + 8u + 8u * (uint32_t)g; };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* never_flag = abort_flag + 1;
-    auto slot_base = [&](int s) { return sb + (uint32_t)(L::S_OFF + s * L::SLOT); };
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < LSS; ++s) {
-            mbar_init(full_bar(s), 1);   // the weight lane's arrival + both boxes' bytes
-            mbar_init(empty_bar(s), 1);  // the MMA's commit after the super-stage's last stage
-        }
-        for (int rb = 0; rb < NRB; ++rb) {
-            // one arrival per warp of each of the round's RS stages; in a pair the even CTA's
-            // barrier also takes the odd CTA's relayed arrival
-            mbar_init(afull_bar(rb), 4 * RS + (CG > 1 && leader ? 1 : 0));
-            mbar_init(aempty_bar(rb), 1);       // the MMA's commit of the round
-        }
-        mbar_init(accf_bar, 1);
-        for (int g = 0; g < 4; ++g) mbar_init(xchg_bar(g), 1);
-        *abort_flag = 0;
-        *never_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == MMA_WARP) {
-        if (CG > 1) {
-            tmem_alloc_pair(smem_u32(tmem_slot), L::TMEM_COLS);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
-            tmem_relinquish();
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (CG > 1) cluster_sync_all();   // the peer's barriers and tensor memory exist before any use
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    auto give_up = [&]() {
-        *abort_flag = 1;
-        atomicCAS(&g_err_tc, 0, DEV_TIMEOUT);
-    };
-    // The next kernel in the stream may be scheduled on idle SMs now; it waits for this
-    // grid to finish before it touches memory.
-    pdl_launch_dependents();
-
-    constexpr int NC = ep_cols(BN, KS);      // epilogue: columns this CTA finishes
-    constexpr int NG = ep_groups(BN, KS);    //           decoder groups that take part
-    constexpr int CW = NC / NG;              //           columns per such group
-    constexpr int CH = ep_chunk(BN, KS);     //           columns per chunk
-    static_assert(CW % 16 == 0 && CW % CH == 0 && CW <= 64, "epilogue chunks");
-    const int cbase = kz * NC;               // first column finished here
-    float esc0 = 0.f, esc1 = 0.f;            // epilogue scales, loaded before the last MMAs end
-
-    if (warp == PRODUCER_WARP) {
-        // ================= TMA producers =================
-        // Lane s < LSS issues the weight box of super-slot s (and posts the bytes of
-        // both boxes), lane LSS + s its activation box: a thread keeps only a few bulk
-        // copies in flight, so the boxes come from 2 LSS threads.
-        const int s = lane % LSS;
-        const bool wl = lane < LSS, xl = lane >= LSS && lane < 2 * LSS;
-        if (wl || xl) {
-            if (lane == 0) {
-                tma_prefetch_desc(&tmW);
-                tma_prefetch_desc(&tmX);
-            }
-            const uint32_t base = slot_base(s);
-            int issued = 0;        // super-stages issued by this lane
-            auto issue = [&](int j) {
-                if (wl) {
-                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::X_BYTES + L::W_BYTES));
-                    tma_load_2d(base + L::X_BYTES, &tmW, full_bar(s), (j0 + j) * L::WROW, m0);
-                } else {
-                    tma_load_3d(base, &tmX, full_bar(s), 0, t0 + cx * (BN / CG), (j0 + j) * G);
-                }
-            };
-            if (!p.stall) {
-                // With a programmatic dependency the weights of the first ring fill are
-                // requested before waiting for the previous kernel (the guard pass);
-                // the activations only after it.
-                const bool pre = s < ns;
-                if (pre && wl) issue(s);
-                pdl_wait();
-                if (pre) {
-                    if (xl) issue(s);
-                    ++issued;
-                }
-                uint32_t ph = pre ? 1u : 0u;     // phase of this slot's round for super-stage j
-                for (int j = s + (pre ? LSS : 0); j < ns; j += LSS, ph ^= 1u) {
-                    if (!mbar_wait(empty_bar(s), ph ^ 1u, p.wait_ns, abort_flag)) {
-                        give_up();
-                        break;
-                    }
-                    issue(j);
-                    ++issued;
-                }
-            } else {
-                pdl_wait();   // every path waits once, so kernels later in the stream stay ordered
-            }
-            if (*abort_flag && issued > 0) {
-                // this lane's last copy must land before the CTA can exit (round issued - 1)
-                mbar_wait(full_bar(s), (uint32_t)((issued - 1) & 1), p.wait_ns, never_flag);
-            }
-        }
-        __syncwarp();
-    } else if (warp == MMA_WARP) {
-        // ================= MMA issuer =================
-        // One thread issues the tensor-core work, two stages per round: wait for both
-        // decoded slots (their groups had waited for the super-slot, so the activations are
-        // in too), eight MMAs, one commit that frees the pair of decoded slots and, at the end
-        // of a super-stage, one that frees the super-slot.  Descriptors advance by adding.
-        // A super-slot's (decoded round's) release is committed only when a later load
-        // (decode) waits for it.  In a CTA pair only the even CTA's thread issues.
-        if (lane == 0 && (CG == 1 || leader)) {
-            constexpr uint32_t idesc = idesc_f16(BM * CG, BN, XBF);
-            // One thread's serial address arithmetic sits between MMAs, so the operand
-            // addresses advance by adding constants: the descriptors' address field is the
-            // shared-memory address in 16-byte units (no carry: addresses stay below 256 KB).
-            const uint64_t bd0 = smem_desc_sw128(slot_base(0));
-            const uint64_t ad0 = AM == 0 ? smem_desc_sw128(sb + L::A_OFF) : 0;
-            const uint32_t at0 = tmem + (uint32_t)L::A_COL;
-            constexpr uint32_t X_STEP = (uint32_t)(L::X_CHUNK >> 4);                      // next chunk
-            constexpr uint32_t S_STEP = (uint32_t)((L::SLOT - (G - 1) * L::X_CHUNK) >> 4); // next super-slot
-            const int nr = (nk + RS - 1) / RS;     // rounds (the last one may be short)
-            int s = 0, u = 0, js = 0;             // super-slot, chunk and super-stage of the next stage
-            uint32_t boff = 0;                    // its activation tile, 16-byte units from super-slot 0
-            for (int r = 0; r < nr; ++r) {
-                const int rb = r % NRB;
-                const bool got = CG > 1 ? mbar_wait_cluster_spin(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag)
-                                        : mbar_wait_spin(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag);
-                if (!got) {
-                    give_up();
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a_r = (uint32_t)(rb * RS);   // the round's first decoded slot
-#pragma unroll
-                for (int i = 0; i < RS; ++i) {
-                    const int kb = r * RS + i;
-                    if (kb < nk) {
-                        const uint64_t bd = bd0 + boff;
-                        const uint64_t ad = AM == 0 ? ad0 + (uint64_t)((a_r + (uint32_t)i) * (uint32_t)(A_BYTES >> 4)) : 0;
-                        const uint32_t at = at0 + (a_r + (uint32_t)i) * 32u;
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk) {
-                            const uint32_t acc = (kb + kk) != 0 ? 1u : 0u;
-                            // +32 bytes of K = +2 in the descriptor's 16-byte address units
-                            if (AM == 0) tc_mma_f16(tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
-                            else if (CG > 1) tc_mma_f16_ts_pair(tmem, at + 8u * kk, bd + 2u * kk, idesc, acc);
-                            else tc_mma_f16_ts(tmem, at + 8u * kk, bd + 2u * kk, idesc, acc);
-                        }
-                        if (++u == G) {
-                            u = 0;
-                            // super-slot free (and, merged, the round's decoded slots)
-                            if (js + (MERGE && NRB < LSS ? NRB : LSS) < ns) {
-                                if (CG > 1) tc_commit_pair_mc(empty_bar(s), pair_mask);
-                                else tc_commit(empty_bar(s));
-                            }
-                            ++js;
-                            if (++s == LSS) {
-                                s = 0;
-                                boff = 0;
-                            } else {
-                                boff += S_STEP;
-                            }
-                        } else {
-                            boff += X_STEP;
-                        }
-                    }
-                }
-                if (!MERGE && r + NRB < nr) {                   // the round's decoded slots free
-                    if (CG > 1) tc_commit_pair_mc(aempty_bar(rb), pair_mask);
-                    else tc_commit(aempty_bar(rb));
-                }
-            }
-            // also lets teardown know every MMA has finished
-            if (CG > 1) tc_commit_pair_mc(accf_bar, pair_mask);
-            else tc_commit(accf_bar);
-        } else if (CG > 1 && lane == 0) {
-            // The odd CTA of a pair relays each round: once its own decoders have arrived,
-            // one arrival (release at cluster scope) on the even CTA's barrier.
-            const int nr = (nk + RS - 1) / RS;
-            const uint32_t peer_afull = mapa_shared(afull_bar(0), crank ^ 1u);
-            for (int r = 0; r < nr; ++r) {
-                const int rb = r % NRB;
-                if (!mbar_wait_spin(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag)) {
-                    give_up();
-                    break;
-                }
-                mbar_arrive_remote(peer_afull + 8u * (uint32_t)rb);
-            }
-        }
-        __syncwarp();
-    } else {
-        // ================= decoders, then epilogue =================
-        // Four groups of four warps; group g = w / 4 decodes stages g, g + 4, g + 8, ...
-        // and in each of them warp w covers rows 32 (w % 4) .. +31 (its tensor-memory lane
-        // quarter), one whole 64-k row per thread.  Four stages are decoded at once, so the
-        // per-stage chain (wait, load, decode, store, hand-off) of one warp overlaps the
-        // others' instead of setting the pace.
-        const int q4w = warp & 3, grp = warp >> 2;
-        const int r = 32 * q4w + lane;             // weight row within the tile
-        const int64_t n = (int64_t)m0 + r;
-        const bool row_ok = n < p.N;
-        const uint32_t xr = (uint32_t)(r & 7);
-        const uint32_t t_lane = (uint32_t)(32 * q4w) << 16;
-        // weight rows of G * ROW bytes: 128-byte swizzle (chunk c at c ^ (r % 8)), 64-byte
-        // swizzle (chunk c at c ^ ((r / 2) % 4)) or 32-byte swizzle (chunk c at c ^ ((r / 4) % 2))
-        const uint32_t wsw = L::WROW == 128 ? (uint32_t)(r & 7)
-                           : L::WROW == 64  ? (uint32_t)((r >> 1) & 3)
-                                            : (uint32_t)((r >> 2) & 1);
-        // Q4 scales of this row: the two fp16 of stage kb (blocks 2 kb, 2 kb + 1), loaded two
-        // of this group's stages ahead
-        const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.ws + n * (p.K / 32)) + k0;
-        uint32_t sc0 = 0, sc1 = 0;
-        if (FMT == 0 && row_ok) {
-            if (grp < nk) sc0 = __ldg(srow + grp);
-            if (grp + 4 < nk) sc1 = __ldg(srow + grp + 4);
-        }
-        // Every group waits for every super-stage in order (decoding only its own stages
-        // in it), so each round of each super-slot is waited for in order and a parity
-        // wait never mistakes round r for round r - 2, whatever LSS is.
-        int s = 0;
-        uint32_t ph = 0;
-        bool stop = false;
-        for (int j = 0; j < ns && !stop; ++j) {
-          if (!mbar_wait_spin(full_bar(s), ph, p.wait_ns, abort_flag)) {
-              give_up();
-              break;
-          }
-#pragma unroll
-          for (int u = 0; u < G; ++u) {
-            const int kb = j * G + u;
-            if ((kb & 3) != grp) continue;
-            const int a = kb % AS;                             // decoded slot
-            const int rb = (kb / RS) % NRB;                    // its round's barriers
-            const uint32_t rph = (uint32_t)((kb / AS) & 1);    // and their phase
-            uint32_t sc_next = 0;
-            if (FMT == 0 && row_ok && kb + 8 < nk) sc_next = __ldg(srow + kb + 8);
-            // the slot's previous round (NRB back) must have been consumed
-            const int rp = kb / RS - NRB;
-            const bool freed = MERGE ? (rp < 0 || mbar_wait_spin(empty_bar(rp % LSS), (uint32_t)((rp / LSS) & 1), p.wait_ns, abort_flag))
-                                     : mbar_wait_spin(aempty_bar(rb), rph ^ 1u, p.wait_ns, abort_flag);
-            if (!freed) {
-                give_up();
-                stop = true;
-                break;
-            }
-            tc_fence_after();   // the slot's earlier MMAs (committed by this or the pair's CTA) are done
-            const uint32_t wrow = slot_base(s) + (uint32_t)(L::X_BYTES + r * L::WROW);
-            // this thread's 64 decoded values (the whole stage for row r), two per word
-            uint32_t o[32];
-            if (FMT == 0) {
-                // stage u = chunks 2u, 2u + 1 (one 32-k block each) of the row.  Each block is
-                // decoded in the activations' streaming order (the guard pass wrote them in
-                // that order): columns 16 b .. 16 b + 15 for block b.
-                const uint4 v0 = ld_shared_v4(wrow + (((uint32_t)(2 * u) ^ wsw) << 4));
-                const uint4 v1 = ld_shared_v4(wrow + (((uint32_t)(2 * u + 1) ^ wsw) << 4));
-                // the block scales, each in both halves of a register
-                const uint32_t s0 = prmt(sc0, sc0, 0x1010u), s1 = prmt(sc0, sc0, 0x3232u);
-                decode_q4_word_scaled(v0.x, s0, o);
-                decode_q4_word_scaled(v0.y, s0, o + 4);
-                decode_q4_word_scaled(v0.z, s0, o + 8);
-                decode_q4_word_scaled(v0.w, s0, o + 12);
-                decode_q4_word_scaled(v1.x, s1, o + 16);
-                decode_q4_word_scaled(v1.y, s1, o + 20);
-                decode_q4_word_scaled(v1.z, s1, o + 24);
-                decode_q4_word_scaled(v1.w, s1, o + 28);
-            } else {
-                // stage u = chunks 4u .. 4u + 3 of the row, in k order
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 v = ld_shared_v4(wrow + (((uint32_t)(4 * u + c) ^ wsw) << 4));
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (XBF) {
-                            o[8 * c + 2 * i] = i8x2_to_bf2(wv[i], 0x4140u);
-                            o[8 * c + 2 * i + 1] = i8x2_to_bf2(wv[i], 0x4342u);
-                        } else {
-                            o[8 * c + 2 * i] = i8x2_to_h2(wv[i], 0x4140u);
-                            o[8 * c + 2 * i + 1] = i8x2_to_h2(wv[i], 0x4342u);
-                        }
-                    }
-                }
-            }
-            if (AM == 0) {
-                // shared-memory A tile, 128-byte swizzled K-major: the 8 chunks of row r
-                const uint32_t adst = sb + L::A_OFF + a * A_BYTES + (uint32_t)(r * 128);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(adst + ((((uint32_t)c) ^ xr) << 4), o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-                fence_proxy_async_smem();
-            } else {
-                // tensor-memory A tile: lane r, columns A_COL + 32 a .. +31
-                tmem_st_32x32b_x32(tmem + t_lane + (uint32_t)(L::A_COL + a * 32), o);
-                tmem_st_wait();
-                tc_fence_before();
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(rb));
-            sc0 = sc1;
-            sc1 = sc_next;
-          }
-          if (++s == LSS) {
-              s = 0;
-              ph ^= 1u;
-          }
-        }
-        // A short last round: the groups without a stage in it still arrive (after the
-        // round NRB back has freed the barrier), so the MMA thread's wait completes.
-        for (int kb = nk; kb < (nk + RS - 1) / RS * RS && !stop && !*abort_flag; ++kb) {
-            if ((kb & 3) != grp) continue;
-            const int rb = (kb / RS) % NRB;
-            const int rp = kb / RS - NRB;
-            const bool freed = MERGE ? (rp < 0 || mbar_wait(empty_bar(rp % LSS), (uint32_t)((rp / LSS) & 1), p.wait_ns, abort_flag))
-                                     : mbar_wait(aempty_bar(rb), (uint32_t)(((kb / AS) & 1) ^ 1), p.wait_ns, abort_flag);
-            if (!freed) {
-                give_up();
-                break;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(rb));
-        }
-
-        // Output scales of the epilogue (Q4: the guard inverse of each token this thread's
-        // group finishes, lane l holding columns l and 32 + l; Q8: the row scale), read
-        // while the last MMAs run.  Outputs and guard scales only after the previous
-        // kernel has finished.
-        pdl_wait();
-        if (FMT == 0) {
-            const int64_t tb = (int64_t)t0 + cbase + grp * CW;
-            if (grp < NG && lane < CW && tb + lane < p.T) esc0 = p.rsx[tb + lane];
-            if (grp < NG && CW > 32 && tb + 32 + lane < p.T) esc1 = p.rsx[tb + 32 + lane];
-        } else if (row_ok) {
-            esc0 = p.rs[n];
-        }
-        // the accumulator is complete once the MMA thread's last commit arrives
-        if (!*abort_flag && !mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) give_up();
-        tc_fence_after();
-    }
-
-    // ================= epilogue (every thread reaches it) =================
-    // The decoder warps read the accumulator (warp w: TMEM lanes 32 (w % 4).., the CW
-    // columns of its group g = w / 4, CH at a time), scale it and stage each chunk in the
-    // idle ring memory as [token][128 rows] in the output type; after a barrier of the
-    // group's four warps its first thread stores the chunk with TMA (rows and tokens
-    // outside Y are clipped), so the stores overlap the staging of later chunks.  When
-    // Y's row pitch is not a multiple of 16 bytes the decoders store element by element.
-    // Split K: after a first cluster barrier both CTAs' MMAs are done and their rings
-    // idle; the CTA of k half z finishes columns [z BN/2, (z + 1) BN/2).  Each stages the other half of
-    // its accumulator ([column][128 rows] f32) chunk by chunk, and the group's first
-    // thread copies each chunk in bulk into the partner, completing on the partner's
-    // exchange barrier of the same group, so each group finishes as soon as its own
-    // columns are in.  The sum is own + partner (a + b, the same in both orders).  A
-    // thread arrives on a second cluster barrier once its group's columns are in and
-    // waits on it before exiting, so no copy still reads the memory of a CTA that has left.
-    // Barriers are taken by every decoder warp whatever the abort flag; only the copies
-    // and stores are skipped after a timeout.
-    {
-        constexpr int HALF = BN / 2;
-        constexpr uint32_t SEND_OFF = 0;              // split K: outgoing half
-        constexpr uint32_t RECV_OFF = HALF * 128 * 4; //          incoming half
-        constexpr uint32_t YST_OFF = KS > 1 ? 2 * HALF * 128 * 4 : 0;   // staged output tile
-        const bool dec = warp < DEC_WARPS;
-        const int q4w = warp & 3, grp = warp >> 2;
-        const int r = 32 * q4w + lane;
-        const uint32_t t_lane = (uint32_t)(32 * q4w) << 16;
-        const bool lead = q4w == 0 && lane == 0;     // issues the group's copies and stores
-        const int gbar = 2 + grp;                    // the group's named barrier (1 is all decoders)
-        if (KS > 1) {
-            const uint32_t partner = crank ^ (uint32_t)CG;
-            cluster_sync_all();
-            // each group receives the partner's values of its own CW columns
-            if (dec && grp < NG && lead) mbar_arrive_expect_tx(xchg_bar(grp), (uint32_t)(CW * 128 * 4));
-            if (dec && grp < NG) {
-                const int hb = (kz ^ 1) * HALF;         // the columns the partner finishes
-                uint32_t* st = reinterpret_cast<uint32_t*>(smem + SEND_OFF);
-#pragma unroll 1
-                for (int cc = grp * CW; cc < (grp + 1) * CW; cc += CH) {
-                    uint32_t v[CH];
-                    tmem_ld_cols<CH>(tmem + t_lane + (uint32_t)(hb + cc), v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int jj = 0; jj < CH; ++jj) st[(cc + jj) * 128 + r] = v[jj];
-                    fence_proxy_async_smem();
-                    named_bar_sync(gbar, 128);
-                    if (lead && !*abort_flag)
-                        bulk_copy_to_cluster(mapa_shared(sb + RECV_OFF + (uint32_t)(cc * 512), partner),
-                                             sb + SEND_OFF + (uint32_t)(cc * 512), (uint32_t)(CH * 512),
-                                             mapa_shared(xchg_bar(grp), partner));
-                }
-                if (!*abort_flag && !mbar_wait(xchg_bar(grp), 0, p.wait_ns, abort_flag)) give_up();
-            }
-            cluster_arrive_release();
-        } else if (CG > 1) {
-            cluster_arrive_release();   // neither CTA of a pair leaves while the other may still use it
-        }
-        if (dec && grp < NG) {
-            const int64_t n = (int64_t)m0 + r;
-            const bool row_ok = n < p.N;
-            const float* recv = reinterpret_cast<const float*>(smem + RECV_OFF);
-            const bool f32 = p.yt == CQ_F32;
-            const int esz = f32 ? 4 : 2;
-#pragma unroll 1
-            for (int ci = 0; ci < CW / CH; ++ci) {
-                const int cc = grp * CW + ci * CH;
-                uint32_t v[CH];
-                tmem_ld_cols<CH>(tmem + t_lane + (uint32_t)(cbase + cc), v);
-                tmem_ld_wait();
-                const int64_t tb = (int64_t)t0 + cbase + cc;
-                const bool skip = *abort_flag != 0;
-#pragma unroll
-                for (int jj = 0; jj < CH; ++jj) {
-                    // column ci CH + jj of the group: its scale sits in lane (column % 32) of esc0
-                    // (columns 0..31) or esc1 (32..63)
-                    const int gc = ci * CH + jj;
-                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, gc < 32 ? esc0 : esc1, gc & 31) : esc0;
-                    float acc = __uint_as_float(v[jj]);
-                    if (KS > 1) acc += recv[(cc + jj) * 128 + r];
-                    const float val = acc * sx;
-                    const int64_t t = tb + jj;
-                    if (p.y_tma) {
-                        if (f32) reinterpret_cast<float*>(smem + YST_OFF)[(cc + jj) * 128 + r] = val;
-                        else reinterpret_cast<__nv_bfloat16*>(smem + YST_OFF)[(cc + jj) * 128 + r] = __float2bfloat16_rn(val);
-                    } else if (!skip && row_ok && t < p.T) {
-                        if (f32) reinterpret_cast<float*>(p.y)[t * p.N + n] = val;
-                        else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(val);
-                    }
-                }
-                if (p.y_tma) {
-                    fence_proxy_async_smem();
-                    named_bar_sync(gbar, 128);
-                    if (lead && !*abort_flag) {
-                        tma_store_2d(&tmY, sb + YST_OFF + (uint32_t)(cc * 128 * esz), m0, (int)tb);
-                        bulk_commit();
-                    }
-                }
-            }
-            if (lead) bulk_wait_read0();   // the staging memory must stay valid until TMA has read it
-        }
-        if (KS > 1 || CG > 1) cluster_wait_acquire();
-    }
-
-    // ---- teardown ----
-    tc_fence_before();
-    __syncthreads();
-    if (warp == MMA_WARP) {
-        if (*abort_flag && lane == 0) mbar_wait(accf_bar, 0, p.wait_ns, never_flag);  // MMAs done
-        __syncwarp();
-        tc_fence_after();
-        if (CG > 1) tmem_dealloc_pair(tmem, L::TMEM_COLS);
-        else tmem_dealloc(tmem, L::TMEM_COLS);
-    }
-}
-
-template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS = 1, int CG = 1>
-cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t s) {
-    using L = Layout<FMT, BN, G, LSS, AS, AM, CG>;
-    static_assert(CG == 1 || (CG == 2 && AM == 1 && BN >= 32), "CTA pairs: decoded weights in tensor memory");
-    static_assert(L::TOTAL <= 232448, "shared memory budget");
-    // epilogue staging (f32 at most) below the barriers: split K needs the outgoing and the
-    // incoming half and the staged output half; otherwise the staged output tile
-    static_assert(L::S_OFF + LSS * L::SLOT >= (KS > 1 ? 3 * (BN / 2) * 128 * 4 : BN * 128 * 4),
-                  "epilogue staging fits in the ring memory");
-    static_assert(2 * LSS <= 32, "two producer lanes per super-slot");
-    // Group g decodes the stages kb % 4 == g, in rounds of RS = 2 or 4 stages, NRB = AS / RS
-    // rounds in flight: with RS = 4 every group is in every round; with RS = 2 groups 0, 1
-    // take the even rounds and 2, 3 the odd ones, so NRB must be even.  Either way each
-    // round barrier is waited for by fixed groups, every one of its rounds in order.
-    static_assert(AS % L::RS == 0 && (L::RS == 4 || L::NRB % 2 == 0) && (G == 1 || G == 2 || G == 4),
-                  "decoded slots owned by fixed decoder groups");
-    // weights: rows of G stages (G * ROW bytes) per box
-    CUtensorMap mw, mx;
-    {
-        const uint64_t kbytes = FMT == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
-        uint64_t d[2] = {kbytes, (uint64_t)a.N};
-        uint64_t st[1] = {kbytes};
-        uint32_t box[2] = {(uint32_t)L::WROW, (uint32_t)BM};
-        if (!encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.wq, d, st, box,
-                          L::WROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                          : L::WROW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B))
-            return cudaErrorInvalidValue;
-    }
-    // activations seen as {64 elements, T rows, K/64 chunks} (strides K*2 B, 128 B): one
-    // box of G chunks of BN / CG rows lands as [chunk][row][128 B], G operand tiles
-    {
-        uint64_t d[3] = {64, (uint64_t)a.T, (uint64_t)a.K / 64};
-        uint64_t st[2] = {(uint64_t)a.K * 2, 128};
-        uint32_t box[3] = {64, (uint32_t)(BN / CG), (uint32_t)G};
-        if (!encode_tiled(&mx, XBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, d,
-                          st, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
-    }
-    // output tiles: Y [T][N] seen as {N, T}; a box is 128 rows x one epilogue chunk of columns
-    CUtensorMap my = mx;
-    if (p.y_tma) {
-        const uint64_t es = a.yt == CQ_F32 ? 4 : 2;
-        uint64_t d[2] = {(uint64_t)a.N, (uint64_t)a.T};
-        uint64_t st[1] = {(uint64_t)a.N * es};
-        uint32_t box[2] = {(uint32_t)BM, (uint32_t)ep_chunk(BN, KS)};
-        if (!encode_tiled(&my, a.yt == CQ_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                          a.y, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
-    }
-    auto kern = k_tc<FMT, BN, XBF, G, LSS, AS, AM, KS, CG>;
-    static int configured_device = -1;       // attributes are per device; set once per instantiation
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = L::TOTAL;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    if (KS > 1 || CG > 1) {
-        if (grid.x % CG != 0) return cudaErrorInvalidValue;
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = CG;
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = KS;
-        ++na;
-    }
-    if (p.pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, mw, mx, my, p);
-}
 
 cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     const int xbf = fmt == 0 ? 0 : a.x_bf16;
     const int64_t mt = (a.N + BM - 1) / BM;
-    const int64_t nk = a.K / BK;
-    // One CTA per SM.  Time of a CTA ~ its stages x the measured cost of a 64-k stage
-    // (clock stamps in the kernel: about 520 cycles at BN = 64, 570 at 128 and 800 at 256,
-    // 515, 680 and 690 in CTA pairs at 128, 192 and 256; 192-column pairs fill the SMs
-    // where 256-column tiles leave a third idle), plus about 6000 cycles for the exchange when K is split
-    // over two CTAs; times the waves.  Tiles at least twice as wide as the tokens are not
-    // considered.  The cheapest candidate wins (ties: the earlier, wider one).
-    int bn = (int)options().tc_bn;
-    int ks = (int)options().tc_ksplit;
-    if (bn == 32 && options().tc_amode == 1) bn = 64;   // 32-column tiles keep decoded weights in tensor memory
-    if (bn == 192 && !(mt % 2 == 0 && options().tc_amode != 1 && options().tc_pair != 1)) bn = 256;   // pairs only
-    if (bn == 192 && options().tc_ksplit == 2) ks = 1;                                                 // no K split
-    const bool ks2_ok = nk % 8 == 0;
-    // 256-column tiles in CTA pairs (one 256-row MMA over two neighbouring row tiles):
-    // an even number of row tiles and decoded weights in tensor memory
-    const bool pair_ok = mt % 2 == 0 && options().tc_amode != 1 && options().tc_pair != 1;
-    {
-        struct Cand { int bn, ks; };
-        const Cand cands[] = {{256, 1}, {256, 2}, {192, 1}, {128, 1}, {128, 2}, {64, 1}, {32, 1}, {32, 2}};
-        double best = -1.0;
-        int bbn = 128, bks = 1;
-        for (const Cand& c : cands) {
-            if (bn != 0 && c.bn != bn) continue;
-            if (ks != 0 && c.ks != ks) continue;
-            if (bn == 0 && 2 * a.T <= c.bn && c.bn > 32) continue;   // at least half of every tile's columns unused
-            if (c.bn == 32 && options().tc_amode == 1) continue;
-            // split only to fill the GPU: when the unsplit tiles leave a quarter of the SMs idle
-            if (c.ks == 2 && (!ks2_ok || (ks == 0 && mt * ((a.T + c.bn - 1) / c.bn) * 4 > 3 * num_sms()))) continue;
-            if (c.bn == 192 && c.ks != 1) continue;
-            if (c.bn == 192 && !pair_ok) continue;   // 192-column tiles only in CTA pairs
-            const double stage = c.bn == 256 ? (pair_ok ? 690.0 : 800.0) : c.bn == 192 ? 680.0
-                               : c.bn == 128 ? (pair_ok ? 515.0 : 570.0) : c.bn == 64 ? 520.0 : (pair_ok ? 300.0 : 520.0);
-            const int64_t ctas = mt * ((a.T + c.bn - 1) / c.bn) * c.ks;
-            const int64_t waves = (ctas + num_sms() - 1) / num_sms();
-            const double cost = (double)waves * ((double)(nk / c.ks) * stage + (c.ks > 1 ? 6000.0 : 0.0));
-            if (best < 0.0 || cost < best - 1e-9) {
-                best = cost;
-                bbn = c.bn;
-                bks = c.ks;
-            }
-        }
-        if (best < 0.0) {   // a forced combination that cannot run: fall back to no split
-            bbn = bn != 0 ? bn : 128;
-            bks = 1;
-        }
-        bn = bbn;
-        ks = bks;
-    }
-    Params p = {};
-    p.rsx = a.rsx;
-    p.rs = a.rs;
-    p.ws = a.ws;
-    p.y = a.y;
-    p.yt = a.yt;
-    p.T = a.T;
-    p.N = a.N;
-    p.K = a.K;
-    p.wait_ns = (uint64_t)options().wait_ns;
-    p.stall = (int)options().test_stall;
-    options().test_stall = 0;
-    p.pdl = 1;   // the guard pass (Q4) or the previous kernel touches neither the weights nor anything before the wait
-    p.y_tma = ((a.N * (a.yt == CQ_F32 ? 4 : 2)) % 16 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0) ? 1 : 0;
+    const Plan pl = plan_tiles(a, mt, false);
+    const int bn = pl.bn, ks = pl.ks;
+    const Params p = make_params(a);
     dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), (unsigned)ks);
-    if (options().trace)
-        fprintf(stderr, "cq: tcgen05 fmt=%d T=%lld N=%lld K=%lld BN=%d ksplit=%d pair=%d grid=(%u,%u,%u)\n", fmt,
-                (long long)a.T, (long long)a.N, (long long)a.K, bn, ks, (int)((bn >= 128 || bn == 32) && pair_ok), grid.x, grid.y,
-                grid.z);
     // decoded weight operand: 1 = shared memory, 2 = tensor memory (default)
     const int am = options().tc_amode == 1 ? 0 : 1;
+    const bool pair = am == 1 && (bn >= 128 || bn == 32) && pl.pair_ok;
+    trace_plan("dense", fmt, a, pl, pair, grid);
     // <FMT, BN, XBF, G, LSS, AS, AM>: super-stages of G stages (weight rows of 64 or 128
     // bytes per box), as many super-slots as fit next to the decoded slots
     if (am == 0) {
@@ -853,19 +33,7 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
         if (bn == 128) return ks == 2 ? launch_bn<1, 128, 0, 2, 3, 4, 0, 2>(a, p, grid, s) : launch_bn<1, 128, 0, 2, 3, 4, 0, 1>(a, p, grid, s);
         return launch_bn<1, 64, 0, 2, 4, 4, 0>(a, p, grid, s);
     }
-    const bool pair = (bn >= 128 || bn == 32) && pair_ok;
-    if (fmt == 0) {
-        if (bn == 192) return launch_bn<0, 192, 0, 2, 6, 8, 1, 1, 2>(a, p, grid, s);
-        if (bn == 32) {
-            if (pair) return ks == 2 ? launch_bn<0, 32, 0, 4, 8, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 32, 0, 4, 8, 12, 1, 1, 2>(a, p, grid, s);
-            return ks == 2 ? launch_bn<0, 32, 0, 4, 6, 12, 1, 2>(a, p, grid, s) : launch_bn<0, 32, 0, 4, 6, 12, 1, 1>(a, p, grid, s);
-        }
-        if (pair && bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 4, 4, 12, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 4, 4, 12, 1, 1, 2>(a, p, grid, s);
-        if (pair) return ks == 2 ? launch_bn<0, 256, 0, 2, 5, 8, 1, 2, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 2, 5, 8, 1, 1, 2>(a, p, grid, s);
-        if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 1, 6, 8, 1, 2>(a, p, grid, s) : launch_bn<0, 256, 0, 1, 6, 8, 1, 1>(a, p, grid, s);
-        if (bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 2, 5, 12, 1, 2>(a, p, grid, s) : launch_bn<0, 128, 0, 2, 5, 12, 1, 1>(a, p, grid, s);
-        return launch_bn<0, 64, 0, 4, 4, 12, 1>(a, p, grid, s);
-    }
+    if (fmt == 0) return launch_q4_tmem<0>(a, p, pl, grid, s);
     if (xbf) {
         if (bn == 192) return launch_bn<1, 192, 1, 2, 5, 8, 1, 1, 2>(a, p, grid, s);
         if (bn == 32) {

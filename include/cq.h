@@ -29,8 +29,11 @@
  *    "decline: <reason>" (cortiq-engine src/gpu_metal/qi21.rs, decline()).
  *    A failed launch returns CQ_ERR_CUDA.  Problems only the device can see
  *    (a routing index out of range, a pipeline wait that exceeded its time
- *    limit) set a device error word that cq_get_device_error reports; the
- *    remaining kernels of that call do no work.
+ *    limit) set the device error word of the stream the call was enqueued
+ *    on, which cq_get_device_error(stream) reports; the remaining kernels of
+ *    that call do no work.  Each (device, stream) pair gets its own word on
+ *    first use, from a fixed table of 1023 per device (further streams share
+ *    one more word); a word is cleared when it is read.
  *  - Outputs are overwritten, never accumulated into.
  */
 #ifndef CQ_H
@@ -124,6 +127,29 @@ cq_status cq_gemm_q8row(const void* X, int xt, int64_t T, int64_t K,
                         void* Y, int yt, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Dense FFN chain (Q4):  Y[t] = Wd . (silu(Wg . x_t) * (Wu . x_t))
+ *
+ * The denoiser block's gate/up GEMM, SwiGLU and down GEMM as one call
+ * ("cortiq-engine 0.8.3 src/gpu_metal/qi21.rs", fn blocks: gemm(TG, TU) ->
+ * swiglu -> gemm(TD); gate and up fused into one [2I][H] weight as its
+ * module header describes).  SwiGLU runs in the gate/up GEMM's epilogue.
+ *
+ * X: fp16/bf16 [T][H].  Wgu_q: [2I][H/2], Wgu_s: fp16 [2I][H/32] (rows
+ * 0..I-1 gate, I..2I-1 up).  Wd_q: [H][I/2], Wd_s: fp16 [H][I/32].
+ * Y: f32 or bf16 [T][H], overwritten.
+ * Arithmetic: both GEMMs as the tcgen05 path of cq_gemm_q4 (guarded fp16
+ * operands, f32 accumulation); a = g / (1 + exp(-g)) * u in f32, then a
+ * guarded fp16 copy of a feeds the down GEMM.  Every T takes this path.
+ * Shape rules: T >= 1, H >= 256, H % 256 == 0, I >= 256, I % 256 == 0.
+ * Workspace: cq_ffn_q4_workspace_bytes(T, H, I) bytes (256-byte aligned).
+ * ------------------------------------------------------------------------- */
+size_t cq_ffn_q4_workspace_bytes(int64_t T, int64_t H, int64_t I);
+cq_status cq_ffn_q4(const void* X, int xt, int64_t T, int64_t H, int64_t I,
+                    const uint8_t* Wgu_q, const uint16_t* Wgu_s,
+                    const uint8_t* Wd_q, const uint16_t* Wd_s,
+                    void* Y, int yt, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Routed MoE expert panels (all experts Q4):
  *   for each token t and slot j < topk, e = idx[t][j]:
  *     g = Wgate[e] . x_t,  u = Wup[e] . x_t          (Wgu rows 0..I-1, I..2I-1)
@@ -176,8 +202,11 @@ cq_status cq_dequant_q8row(const int8_t* Wq, const float* rs, int64_t N, int64_t
 /* ---------------------------------------------------------------------------
  * Errors and options
  * ------------------------------------------------------------------------- */
-/* Synchronises `stream`, then returns and clears the device error word
- * (CQ_OK, CQ_ERR_INDEX or CQ_ERR_TIMEOUT); CQ_ERR_CUDA if the sync failed. */
+/* Reads and clears the device error word of `stream` (on the current
+ * device) with copies ordered on that stream, and synchronises that stream
+ * only; returns CQ_OK, CQ_ERR_INDEX or CQ_ERR_TIMEOUT, or CQ_ERR_CUDA if a
+ * copy or the synchronisation failed.  Errors of other streams stay where
+ * they are. */
 cq_status cq_get_device_error(void* stream);
 /* The calling thread's last host-side error message ("" if none). */
 const char* cq_last_error(void);
@@ -195,7 +224,10 @@ typedef enum {
                                 (neighbouring weight-row tiles share one 256-row MMA on a CTA pair, each CTA
                                 loading half of the activation tile; needs an even number of row tiles), 1 off */
 } cq_option;
-/* Process-wide; returns CQ_ERR_ARG for an unknown option or value. */
+/* Process-wide: one value for every thread, stream and device (set before
+ * the calls it should affect); reads and writes are atomic, so concurrent
+ * callers see either the old or the new value.  Returns CQ_ERR_ARG for an
+ * unknown option or value. */
 cq_status cq_set_option(int option, int64_t value);
 int64_t cq_get_option(int option);
 

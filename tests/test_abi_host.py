@@ -156,3 +156,21 @@ def test_product_path_never_imports_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src and "oracle.c" not in src, f
+
+
+def _ffn(L, X=FAKE, xt=1, T=16, H=512, I=768, g=FAKE, gs=FAKE, d=FAKE, ds=FAKE, Y=FAKE, yt=2, ws=FAKE, wsb=1 << 30):
+    return L.cq_ffn_q4(X, xt, T, H, I, g, gs, d, ds, Y, yt, ws, wsb, None)
+
+
+def test_ffn_validation(L):
+    assert _ffn(L, X=None) == 1 and _ffn(L, ds=None) == 1 and _ffn(L, ws=None) == 1
+    assert _ffn(L, xt=2) == 2 and _ffn(L, yt=0) == 2
+    assert _ffn(L, T=0) == 3
+    assert _ffn(L, H=384) == 3 and _ffn(L, I=128) == 3 and _ffn(L, I=300) == 3
+    assert _ffn(L, g=ODD) == 4 and _ffn(L, Y=ODD) == 4
+    need = L.cq_ffn_q4_workspace_bytes(16, 512, 768)
+    # guarded X (16x512 fp16), its scales, a (16x768 f32), its fp16 copy and scales, each 256-aligned
+    assert need == 16384 + 256 + 49152 + 24576 + 256
+    assert _ffn(L, wsb=need - 1) == 6
+    assert _ffn(L, ws=FAKE + 16) == 6
+    assert "decline" in cq.cq_last_error()

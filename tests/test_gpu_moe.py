@@ -124,3 +124,30 @@ def test_moe_deterministic():
     a = _run(m)[0]
     b = _run(m)[0]
     assert torch.equal(a, b)
+
+
+def test_device_errors_are_per_stream():
+    """A bad routing index on one stream sets that stream's error word only:
+    a clean call on a second stream reports CQ_OK, the first stream reports
+    CQ_ERR_INDEX once, and reading clears it."""
+    m = synth.moe_case(43, T=6, H=256, I=256, E=4, topk=2)
+    idx = m["idx"].copy()
+    idx[2, 0] = -1
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    guq, dq = pack.pack_q4(m["gu_codes"]), pack.pack_q4(m["d_codes"])
+    args = (to_dev_x(m["x"], "bf16"), to_dev(np.ascontiguousarray(idx, np.int32)), to_dev(m["w"]), to_dev(guq),
+            to_dev(m["gu_scales"]), to_dev(dq), to_dev(m["d_scales"]))
+    Y = torch.zeros(6, 256, dtype=torch.float32, device=DEV)
+    ws = torch.empty(cq.cq_moe_workspace_bytes(6, 256, 256, 4, 2), dtype=torch.uint8, device=DEV)
+    torch.cuda.synchronize()
+    cq.cq_moe_panels(*args, Y, ws, stream=sa)
+    case = synth.gemm_q4_case(44, 8, 512, 128)
+    wq = pack.pack_q4(case["codes"])
+    Yb = torch.empty(8, 128, dtype=torch.float32, device=DEV)
+    wsb = torch.empty(cq.cq_gemm_q4_workspace_bytes(8, 512), dtype=torch.uint8, device=DEV)
+    cq.cq_gemm_q4(to_dev_x(case["x"], "bf16"), to_dev(wq), to_dev(case["scales"]), Yb, wsb, stream=sb)
+    assert cq.cq_get_device_error(sb) == 0
+    assert cq.cq_get_device_error(sa) == 5                 # CQ_ERR_INDEX
+    assert cq.cq_get_device_error(sa) == 0                 # cleared by the read
+    yref, S = oracle.gemm_q4(wq, case["scales"], 128, 512, oracle.x_to_f64(case["x"], "bf16"))
+    check(y_host(Yb), yref, S, "f32", "clean call on the other stream")
