@@ -133,7 +133,7 @@ def _moe_calls(cq, m, dev):
     per_expert = (2 * I * H + H * I) * 9 // 16
     flops = T * topk * (2.0 * H * 2 * I + 2.0 * I * H)
     return [Call("moe panels", lambda: cq.cq_moe_panels(X, idx, w, guq, gus, dq, ds, Y, ws), flops,
-                 touched * per_expert, X.numel() * 2 + Y.numel() * 4 + idx.numel() * 8, 6,
+                 touched * per_expert, X.numel() * 2 + Y.numel() * 4 + idx.numel() * 8, 5,
                  h2d=[X, idx, w], d2h=[Y])], touched
 
 

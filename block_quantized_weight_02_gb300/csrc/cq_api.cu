@@ -156,7 +156,7 @@ Q4Ws q4_ws(void* ws, int64_t T, int64_t K) {
 }
 
 struct MoeLayout {
-    size_t status, seg, perm, inv, act, xh, rsx, a, ah, rsa, eo, total;
+    size_t status, seg, perm, inv, act, cnt, xh, rsx, a, ah, rsa, eo, total;
 };
 MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
     const size_t P = (size_t)(T * topk);
@@ -167,6 +167,7 @@ MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
     l.perm = o; o += up(P * 4);
     l.inv = o; o += up(P * 4);
     l.act = o; o += up((size_t)(E + 1) * 4);   // active experts, then their count
+    l.cnt = o; o += up((size_t)(H / 128) * 4);  // down items finished per 128-row block
     l.xh = o; o += up(P * H * 2);
     l.rsx = o; o += up(P * 4);
     l.a = o; o += up(P * I * 4);
@@ -382,12 +383,18 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E, 
     int32_t* act = reinterpret_cast<int32_t*>(b + l.act);
     m.act = act;
     m.n_act = act + E;
-    if ((st = launched(launch_moe_route(idx, T, topk, E, const_cast<int32_t*>(m.seg), const_cast<int32_t*>(m.perm), inv, act, act + E, status, err, s), "MoE routing layout"))) return st;
-    if ((st = launched(launch_x_half_gather(X, xt, T * topk, H, const_cast<uint16_t*>(m.xh), const_cast<float*>(m.rsx), m.perm, (int)topk, status, s), "MoE activation gather + guard pass"))) return st;
+    m.inv = inv;
+    m.cnt = reinterpret_cast<int32_t*>(b + l.cnt);
+    m.y = Y;
+    m.yt = yt;
+    if ((st = launched(launch_moe_route_gather(idx, T, topk, E, const_cast<int32_t*>(m.seg), const_cast<int32_t*>(m.perm),
+                                               inv, act, act + E, status, m.cnt, (int)(H / 128), err, X, xt, H,
+                                               const_cast<uint16_t*>(m.xh), const_cast<float*>(m.rsx), s),
+                       "MoE routing layout + gathered guard pass")))
+        return st;
     if ((st = launched(launch_moe_gateup(m, s), "MoE gate/up panels"))) return st;
     if ((st = launched(launch_a_half(m.a, T * topk, I, const_cast<uint16_t*>(m.ah), const_cast<float*>(m.rsa), status, s), "MoE SwiGLU guard pass"))) return st;
-    if ((st = launched(launch_moe_down(m, s), "MoE down panels"))) return st;
-    return launched(launch_moe_combine(m.eo, inv, T, topk, H, Y, yt, status, s), "MoE combine");
+    return launched(launch_moe_down(m, s), "MoE down panels + combine");
 }
 
 size_t cq_ffn_q4_workspace_bytes(int64_t T, int64_t H, int64_t I) {

@@ -58,20 +58,20 @@ cudaError_t launch_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, i
 // Inside each 32-k block the output is in the Q4 streaming order (position
 // 8 wi + t <- k = 4 wi + {0,2,16,18,1,3,17,19}[t]) that both Q4 GEMMs read.
 cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s);
-// The same for gathered rows: output row r <- input row gather[r] / per.
-cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K, uint16_t* xh, float* rsx,
-                                 const int32_t* gather, int per, const int32_t* status, cudaStream_t s);
-
-struct MoeWs;  // workspace carve-up (cq_api.cu)
-// Also writes the active experts (count > 0, ascending) to act[] and their number to *n_act.
-cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
-                             int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, int* err, cudaStream_t s);
+// MoE routing layout and gathered guard pass in one launch: the layout (counts,
+// segment starts, stable grouping by expert, inverse map, active experts and
+// their number, status) and, for every pair in grouped order, its token's row
+// of x guarded into xh / rsx; also zeroes the down panels' per-row-block
+// counters cnt[ncnt].  An index outside [0, E) sets status = 1 and the device
+// error, and no row is written.
+cudaError_t launch_moe_route_gather(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg,
+                                    int32_t* perm, int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status,
+                                    int32_t* cnt, int ncnt, int* err, const void* x, int xt, int64_t H, uint16_t* xh,
+                                    float* rsx, cudaStream_t s);
 // f32 rows -> fp16 behind a per-row power-of-two guard, in the Q4 streaming
 // order (the down panels and the tcgen05 Q4 GEMM read it); status nullable.
 cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,
                           cudaStream_t s);
-cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, int64_t topk, int64_t H, void* y,
-                               int yt, const int32_t* status, cudaStream_t s);
 
 // Weight-streaming (small-T) GEMM.
 struct SkinnyDense {
@@ -106,6 +106,10 @@ struct SkinnyMoe {
     float* eo;              // [P][H] f32 weighted expert outputs, grouped order
     int64_t T, H, I, E, topk;
     int* err;               // the stream's device error word
+    const int32_t* inv;     // [P] grouped position of each pair id
+    int32_t* cnt;           // [H / 128] down items finished per row block
+    void* y;                // Y [T][H], f32 or bf16 (yt): written by the down panels' folded combine
+    int yt;
 };
 cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s);
 cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s);

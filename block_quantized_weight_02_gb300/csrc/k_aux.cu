@@ -1,6 +1,7 @@
 // Small kernels around the GEMMs: the dequantization test hooks, the
 // activation guard pass (rows -> fp16 behind a power-of-two scale), the
-// MoE routing layout, the SwiGLU-activation guard pass and the combine.
+// MoE routing layout and the SwiGLU-activation guard pass.  (The MoE
+// combine runs inside the down panels, k_skinny.cu.)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -125,22 +126,13 @@ __device__ __forceinline__ void store_block_stream_order(const float* v, uint4* 
     }
 }
 
-// One CTA of 256 threads per output row; K % 32 == 0; the output is in the
-// streaming order above.  With a gather list, output row r is source row
-// gather[r] / per (the MoE pairs in grouped order, as the pages' x_half
-// gathers through `src`).
+// One row by one CTA of 256 threads; K % 32 == 0; the output is in the
+// streaming order above, its inverse guard scale in *rs_out.
 template <typename T>
-__global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t K, __half* __restrict__ xh,
-                                                float* __restrict__ rsx, const int32_t* __restrict__ gather, int per,
-                                                const int32_t* __restrict__ status) {
-    pdl_launch_dependents();   // the GEMM after this pass may start streaming its weights now
-    pdl_wait();                // inputs ready and the previous readers of xh done
-    if (status && *status != 0) return;
-    __shared__ float red[8];
-    const int64_t row = blockIdx.x;
-    const int64_t src_row = gather ? (int64_t)(gather[row] / per) : row;
-    const uint4* src = reinterpret_cast<const uint4*>(x + src_row * K);
-    uint4* dst = reinterpret_cast<uint4*>(xh + row * K);
+__device__ __forceinline__ void guard_row(const T* __restrict__ xrow, int64_t K, __half* __restrict__ dst_row,
+                                          float* __restrict__ rs_out, float* red) {
+    const uint4* src = reinterpret_cast<const uint4*>(xrow);
+    uint4* dst = reinterpret_cast<uint4*>(dst_row);
     const int64_t nblk = K / 32;
     const int tid = threadIdx.x;
     int sh;
@@ -203,21 +195,26 @@ __global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t
             store_block_stream_order(v, dst + 4 * blk);
         }
     }
-    if (threadIdx.x == 0) rsx[row] = pow2f(-sh);
+    if (threadIdx.x == 0) *rs_out = pow2f(-sh);
+}
+
+// One CTA of 256 threads per activation row.
+template <typename T>
+__global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t K, __half* __restrict__ xh,
+                                                float* __restrict__ rsx) {
+    pdl_launch_dependents();   // the GEMM after this pass may start streaming its weights now
+    pdl_wait();                // inputs ready and the previous readers of xh done
+    __shared__ float red[8];
+    const int64_t row = blockIdx.x;
+    guard_row<T>(x + row * K, K, xh + row * K, rsx + row, red);
 }
 
 cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s) {
-    return launch_x_half_gather(x, xt, T, K, xh, rsx, nullptr, 1, nullptr, s);
-}
-
-cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K, uint16_t* xh, float* rsx,
-                                 const int32_t* gather, int per, const int32_t* status, cudaStream_t s) {
     if (xt == CQ_BF16)
-        return launch_pdl(k_x_half<__nv_bfloat16>, dim3((unsigned)rows), dim3(256), 0, s,
-                          reinterpret_cast<const __nv_bfloat16*>(x), K, reinterpret_cast<__half*>(xh), rsx, gather, per,
-                          status);
-    return launch_pdl(k_x_half<__half>, dim3((unsigned)rows), dim3(256), 0, s, reinterpret_cast<const __half*>(x), K,
-                      reinterpret_cast<__half*>(xh), rsx, gather, per, status);
+        return launch_pdl(k_x_half<__nv_bfloat16>, dim3((unsigned)T), dim3(256), 0, s,
+                          reinterpret_cast<const __nv_bfloat16*>(x), K, reinterpret_cast<__half*>(xh), rsx);
+    return launch_pdl(k_x_half<__half>, dim3((unsigned)T), dim3(256), 0, s, reinterpret_cast<const __half*>(x), K,
+                      reinterpret_cast<__half*>(xh), rsx);
 }
 
 // ---- MoE routing layout -------------------------------------------------
@@ -230,13 +227,11 @@ cudaError_t launch_x_half_gather(const void* x, int xt, int64_t rows, int64_t K,
 //   perm[q]  = pair id (t*topk + j) at grouped position q
 //   inv[p]   = grouped position of pair p
 //   status   = 0, or 1 if an index is outside [0, E) (nothing else written)
-__global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ idx, int P, int E,
-                                                   int32_t* __restrict__ seg, int32_t* __restrict__ perm,
-                                                   int32_t* __restrict__ inv, int32_t* __restrict__ act,
-                                                   int32_t* __restrict__ n_act, int32_t* __restrict__ status,
-                                                   int* __restrict__ err) {
-    pdl_launch_dependents();  // the gather pass after this one may be scheduled now
-    pdl_wait();               // idx may come from the previous kernel; the previous call's readers are done
+__device__ __forceinline__ void route_layout(const int32_t* __restrict__ idx, int P, int E, int32_t* __restrict__ seg,
+                                             int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                                             int32_t* __restrict__ act, int32_t* __restrict__ n_act,
+                                             int32_t* __restrict__ status, int32_t* __restrict__ rb_cnt, int ncnt,
+                                             int* __restrict__ err) {
     extern __shared__ int sh[];
     int* cnt = sh;            // [E] pairs per expert
     int* fill = sh + E;       // [E] next free grouped position of each expert
@@ -244,6 +239,7 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
     __shared__ int wsum[2][8];  // per-warp totals of the block scan (counts, active flags)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) bad = 0;
+    for (int i = tid; i < ncnt; i += 256) rb_cnt[i] = 0;   // the down panels' row-block counters
     for (int e = tid; e < E; e += 256) cnt[e] = 0;
     __syncthreads();
     for (int p = tid; p < P; p += 256) {
@@ -330,11 +326,71 @@ __global__ void __launch_bounds__(256) k_moe_route(const int32_t* __restrict__ i
     if (tid == 0) *status = 0;
 }
 
-cudaError_t launch_moe_route(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg, int32_t* perm,
-                             int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status, int* err, cudaStream_t s) {
+// Routing layout and gathered guard pass in one launch of P + 1 CTAs.  CTA P
+// writes the layout (route_layout above).  CTA p < P guards the activation row
+// of pair p = t * topk + j into its grouped position, which it finds from the
+// indices alone: the pairs routed to lower experts plus the earlier pairs of
+// its own expert (the same stable order as the layout).  With an index out of
+// range anywhere, no CTA writes a row and the layout CTA reports it.
+template <typename T>
+__global__ void __launch_bounds__(256) k_moe_route_gather(const int32_t* __restrict__ idx, int P, int E, int topk,
+                                                          int32_t* __restrict__ seg, int32_t* __restrict__ perm,
+                                                          int32_t* __restrict__ inv, int32_t* __restrict__ act,
+                                                          int32_t* __restrict__ n_act, int32_t* __restrict__ status,
+                                                          int32_t* __restrict__ rb_cnt, int ncnt, int* __restrict__ err,
+                                                          const T* __restrict__ x, int64_t H, __half* __restrict__ xh,
+                                                          float* __restrict__ rsx) {
+    pdl_launch_dependents();  // the gate/up panels may be scheduled (and stream weights) now
+    pdl_wait();               // idx and x may come from the previous kernel; the previous call's readers are done
+    if ((int)blockIdx.x == P) {
+        route_layout(idx, P, E, seg, perm, inv, act, n_act, status, rb_cnt, ncnt, err);
+        return;
+    }
+    __shared__ int s_below, s_before, s_bad;
+    __shared__ float red[8];
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid == 0) {
+        s_below = 0;
+        s_before = 0;
+        s_bad = 0;
+    }
+    __syncthreads();
+    const int p = blockIdx.x;
+    const int e = idx[p];
+    int below = 0, before = 0, bad = 0;
+    for (int q = tid; q < P; q += 256) {
+        const int f = idx[q];
+        bad |= (f < 0 || f >= E) ? 1 : 0;
+        below += f < e ? 1 : 0;
+        before += (f == e && q < p) ? 1 : 0;
+    }
+    below = __reduce_add_sync(0xffffffffu, below);
+    before = __reduce_add_sync(0xffffffffu, before);
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        atomicAdd(&s_below, below);
+        atomicAdd(&s_before, before);
+        atomicOr(&s_bad, bad);
+    }
+    __syncthreads();
+    if (s_bad) return;
+    const int pos = s_below + s_before;
+    guard_row<T>(x + (int64_t)(p / topk) * H, H, xh + (int64_t)pos * H, rsx + pos, red);
+}
+
+cudaError_t launch_moe_route_gather(const int32_t* idx, int64_t T, int64_t topk, int64_t E, int32_t* seg,
+                                    int32_t* perm, int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status,
+                                    int32_t* cnt, int ncnt, int* err, const void* x, int xt, int64_t H, uint16_t* xh,
+                                    float* rsx, cudaStream_t s) {
     const size_t smem = (size_t)(2 * E) * sizeof(int);
-    return launch_pdl(k_moe_route, dim3(1), dim3(256), smem, s, idx, (int)(T * topk), (int)E, seg, perm, inv, act, n_act,
-                      status, err);
+    const int P = (int)(T * topk);
+    if (xt == CQ_BF16)
+        return launch_pdl(k_moe_route_gather<__nv_bfloat16>, dim3((unsigned)P + 1), dim3(256), smem, s, idx, P, (int)E,
+                          (int)topk, seg, perm, inv, act, n_act, status, cnt, ncnt, err,
+                          reinterpret_cast<const __nv_bfloat16*>(x), H, reinterpret_cast<__half*>(xh), rsx);
+    return launch_pdl(k_moe_route_gather<__half>, dim3((unsigned)P + 1), dim3(256), smem, s, idx, P, (int)E, (int)topk,
+                      seg, perm, inv, act, n_act, status, cnt, ncnt, err, reinterpret_cast<const __half*>(x), H,
+                      reinterpret_cast<__half*>(xh), rsx);
 }
 
 // SwiGLU activations (f32, grouped order) -> fp16 behind the same
@@ -377,42 +433,6 @@ __global__ void __launch_bounds__(256) k_a_half(const float* __restrict__ a, int
 cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,
                           cudaStream_t s) {
     return launch_pdl(k_a_half, dim3((unsigned)P), dim3(256), 0, s, a, I, reinterpret_cast<__half*>(ah), rsa, status);
-}
-
-// Y[t][n] = sum over slots j (in order) of eo[inv[t*topk + j]][n]; the
-// routing weight is already in eo ("oxinfer 0.0.5 src/metal.rs",
-// moe_combine).  f32 sums, one rounding to the output type.
-__global__ void __launch_bounds__(256) k_moe_combine(const float* __restrict__ eo, const int32_t* __restrict__ inv,
-                                                     int topk, int64_t H, void* __restrict__ y, int yt,
-                                                     const int32_t* __restrict__ status) {
-    pdl_wait();
-    pdl_launch_dependents();
-    if (*status != 0) return;
-    const int64_t t = blockIdx.y;
-    const int64_t c = ((int64_t)blockIdx.x * 256 + threadIdx.x) * 4;
-    if (c >= H) return;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < topk; ++j) {
-        const int64_t r = inv[t * topk + j];
-        const float4 v = *reinterpret_cast<const float4*>(eo + r * H + c);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-    }
-    if (yt == CQ_F32) {
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(y) + t * H + c) = acc;
-    } else {
-        __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(y) + t * H + c);
-        o[0] = __floats2bfloat162_rn(acc.x, acc.y);
-        o[1] = __floats2bfloat162_rn(acc.z, acc.w);
-    }
-}
-
-cudaError_t launch_moe_combine(const float* eo, const int32_t* inv, int64_t T, int64_t topk, int64_t H, void* y,
-                               int yt, const int32_t* status, cudaStream_t s) {
-    dim3 grid((unsigned)((H / 4 + 255) / 256), (unsigned)T);
-    return launch_pdl(k_moe_combine, grid, dim3(256), 0, s, eo, inv, (int)topk, H, y, yt, status);
 }
 
 }  // namespace cq

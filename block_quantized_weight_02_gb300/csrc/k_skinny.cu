@@ -92,6 +92,10 @@ struct Params {
     const int32_t* n_act; // MoE: number of active experts
     int rbs;              // MoE: row blocks per expert matrix
     int* err;             // the stream's device error word
+    // DOWN: the weighted combine, folded in (Y [T][H] written by the last item of each row block)
+    const int32_t* inv;   // grouped position of each pair id
+    int32_t* cnt;         // [H / 128] items finished per row block (zero at the start of the call)
+    int topk;
 };
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -281,6 +285,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NSLOT);
     volatile int* never_flag = abort_flag + 1;  // stays 0: waits that must not be cut short
+    volatile int* last_flag = abort_flag + 2;   // DOWN: this CTA finished a row block's last item
 
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t bar_base = smem_u32(bars);
@@ -613,6 +618,33 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
               asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
             }
           }
+          if (MODE == DOWN) {
+              // The weighted combine, folded in: every item counts itself for its row block
+              // once its eo rows are out (fence, then one atomic); the CTA whose count
+              // completes the row block (all active experts in) sums, for every token, the
+              // eo rows of its slots in slot order j = 0 .. topk - 1, so the result does not
+              // depend on which CTA finishes last.  It also resets the counter.
+              __threadfence();
+              asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
+              if (threadIdx.x == 0) *last_flag = !*abort_flag && atomicAdd(p.cnt + rb, 1) == *p.n_act - 1;
+              asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
+              if (*last_flag) {
+                  __threadfence();
+                  const int64_t n0 = (int64_t)rb * RB;
+                  for (int e = threadIdx.x; e < (int)p.T * RB; e += CONSUMERS * 32) {
+                      const int64_t t = e / RB;
+                      const int r = e & (RB - 1);
+                      float acc = 0.f;
+                      for (int j = 0; j < p.topk; ++j) {
+                          const int64_t q = p.inv[t * p.topk + j];
+                          acc += __ldcg(p.out + q * p.H + n0 + r);   // other CTAs' rows: not from L1
+                      }
+                      if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.H + n0 + r] = acc;
+                      else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.H + n0 + r] = __float2bfloat16_rn(acc);
+                  }
+                  if (threadIdx.x == 0) p.cnt[rb] = 0;
+              }
+          }
         }
     }
 
@@ -671,7 +703,7 @@ constexpr size_t smem_bytes() {
     constexpr int PART_BYTES = RB * NCOL * 4;
     constexpr int RECV_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
     constexpr int BAR_OFF = RECV_OFF + ((MODE == DENSE) ? PART_BYTES : 0);
-    return (size_t)BAR_OFF + 2 * NSLOT * 8 + 16 + 1024;
+    return (size_t)BAR_OFF + 2 * NSLOT * 8 + 16 + 1024;   // + abort, never and last flags
 }
 
 // Weights [E][R][K bytes] and scales [E][R][K/32], boxes of rows_box rows.
@@ -852,6 +884,12 @@ cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s) {
     p.out = m.eo;
     p.I = m.I;
     p.H = m.H;
+    p.T = m.T;
+    p.topk = (int)m.topk;
+    p.inv = m.inv;
+    p.cnt = m.cnt;
+    p.y = m.y;
+    p.yt = m.yt;
     p.wait_ns = (uint64_t)options().wait_ns;
     p.act = m.act;
     p.n_act = m.n_act;

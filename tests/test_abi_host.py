@@ -103,7 +103,8 @@ def test_workspace_sizes(L):
     assert cq.cq_gemm_q4_workspace_bytes(3, 256) == 1536 + 256
     b = cq.cq_moe_workspace_bytes(32, 2048, 768, 128, 8)
     P = 256
-    need = 256 + 768 + P * 4 * 2 + 768 + P * 2048 * 2 + P * 4 + P * 768 * 4 + P * 768 * 2 + P * 4 + P * 2048 * 4
+    # status, seg, perm, inv, active experts, 16 row-block counters, then the gathered rows and the panels' buffers
+    need = 256 + 768 + P * 4 * 2 + 768 + 256 + P * 2048 * 2 + P * 4 + P * 768 * 4 + P * 768 * 2 + P * 4 + P * 2048 * 4
     assert b == need
 
 

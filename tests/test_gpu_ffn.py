@@ -72,10 +72,9 @@ def test_ffn_small(T, H, I, out, xdt):
 @pytest.mark.parametrize("ks", [1, 2])
 @pytest.mark.parametrize("pair", [1, 2])
 def test_ffn_gateup_tile_options(bn, ks, pair):
-    """Every token tile, K split and CTA-pair setting of the gate/up kernel
-    (I = 640: an odd number of 64-row gate tiles, so pairs fall back, and
-    I = 768: an even number), ragged T."""
-    for I in (640, 768):
+    """Every token tile, K split and CTA-pair setting of the gate/up kernel,
+    at I = 256 (four 64-row gate tiles) and I = 768 (twelve), ragged T."""
+    for I in (256, 768):
         c = _case(9100 + bn + ks + I, 300, 512, I, "bf16")
         with _Opt(cq.CQ_OPT_TC_BN, bn), _Opt(cq.CQ_OPT_TC_KSPLIT, ks), _Opt(cq.CQ_OPT_TC_PAIR, pair):
             Y = _run(c, "f32")

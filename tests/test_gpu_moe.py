@@ -151,3 +151,27 @@ def test_device_errors_are_per_stream():
     assert cq.cq_get_device_error(sa) == 0                 # cleared by the read
     yref, S = oracle.gemm_q4(wq, case["scales"], 128, 512, oracle.x_to_f64(case["x"], "bf16"))
     check(y_host(Yb), yref, S, "f32", "clean call on the other stream")
+
+
+def test_moe_reused_workspace_of_any_contents():
+    """The workspace starts as 0xFF bytes and serves three calls in a row with
+    two routings: the down panels' row-block counters are reset by every call,
+    so each result matches the oracle and the repeated call is bit-identical."""
+    m = synth.moe_case(45, T=16, H=512, I=256, E=8, topk=4)
+    T, H, I, E, topk = 16, 512, 256, 8, 4
+    rng = np.random.default_rng(46)
+    idx2 = np.stack([rng.permutation(E)[:topk] for _ in range(T)]).astype(np.int32)
+    w2 = rng.uniform(0.1, 1.0, (T, topk)).astype(np.float32)
+    guq, dq = pack.pack_q4(m["gu_codes"]), pack.pack_q4(m["d_codes"])
+    X = to_dev_x(m["x"], "bf16")
+    G = (to_dev(guq), to_dev(m["gu_scales"]), to_dev(dq), to_dev(m["d_scales"]))
+    ws = torch.full((cq.cq_moe_workspace_bytes(T, H, I, E, topk),), 0xFF, dtype=torch.uint8, device=DEV)
+    outs = []
+    for idx, w in ((m["idx"], m["w"]), (idx2, w2), (m["idx"], m["w"])):
+        Y = torch.full((T, H), float("nan"), dtype=torch.float32, device=DEV)
+        cq.cq_moe_panels(X, to_dev(np.ascontiguousarray(idx, np.int32)), to_dev(np.ascontiguousarray(w)), *G, Y, ws)
+        assert cq.cq_get_device_error() == 0
+        yref, S = oracle.moe(oracle.x_to_f64(m["x"], "bf16"), idx, w, guq, m["gu_scales"], dq, m["d_scales"], E, I)
+        check(y_host(Y), yref, S, "f32", "moe reused workspace")
+        outs.append(Y)
+    assert torch.equal(outs[0], outs[2])
