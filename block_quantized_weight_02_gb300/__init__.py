@@ -32,6 +32,9 @@ _SIGS = {
     "cq_gemm_q8row": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p, _c_int, _c_p]),
     "cq_moe_workspace_bytes": (_c_sz, [_c_i64] * 5),
     "cq_ffn_q4_workspace_bytes": (_c_sz, [_c_i64] * 3),
+    "cq_gemm_q4_batched_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_int]),
+    "cq_gemm_q4_batched": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_int, _c_i64, _c_p, _c_int, _c_i64,
+                                    _c_p, _c_sz, _c_p]),
     "cq_ffn_q4": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_sz,
                            _c_p]),
     "cq_moe_panels": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p,
@@ -145,6 +148,28 @@ def cq_moe_panels(X, idx, w, Wgu_q, Wgu_s, Wd_q, Wd_s, Y, ws, stream=None, raise
     st = lib().cq_moe_panels(_ptr(X), _xt(X), T, H, E, twoI // 2, topk, _ptr(idx), _ptr(w), _ptr(Wgu_q),
                              _ptr(Wgu_s), _ptr(Wd_q), _ptr(Wd_s), _ptr(Y), _xt(Y), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream))
+    if raise_on_error:
+        _check(st)
+    return st
+
+
+class cq_q4_job(ctypes.Structure):
+    """One job of cq_gemm_q4_batched (the C struct of the same name)."""
+    _fields_ = [("Wq", ctypes.c_void_p), ("Ws", ctypes.c_void_p), ("x_off", ctypes.c_int64), ("y_off", ctypes.c_int64)]
+
+
+def cq_gemm_q4_batched_workspace_bytes(T, K, z) -> int:
+    return lib().cq_gemm_q4_batched_workspace_bytes(T, K, z)
+
+
+def cq_gemm_q4_batched(X, K, jobs, N, Y, ws, stream=None, raise_on_error=True):
+    """jobs: list of (Wq, Ws, x_off, y_off) with device tensors; X [T][ldx],
+    Y [T][ldy] (the pitches are the tensors' row strides)."""
+    T = X.shape[0]
+    arr = (cq_q4_job * len(jobs))(*[cq_q4_job(Wq.data_ptr(), Ws.data_ptr(), xo, yo) for Wq, Ws, xo, yo in jobs])
+    st = lib().cq_gemm_q4_batched(_ptr(X), _xt(X), T, K, X.stride(0), ctypes.cast(arr, ctypes.c_void_p), len(jobs), N,
+                                  _ptr(Y), _xt(Y), Y.stride(0), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream))
     if raise_on_error:
         _check(st)
     return st

@@ -397,6 +397,97 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E, 
     return launched(launch_moe_down(m, s), "MoE down panels + combine");
 }
 
+size_t cq_gemm_q4_batched_workspace_bytes(int64_t T, int64_t K, int z) {
+    if (T < 1 || K < 1 || z < 1 || z > ZMAX) return 0;
+    return (size_t)z * q4_ws_bytes(T, K);
+}
+
+cq_status cq_gemm_q4_batched(const void* X, int xt, int64_t T, int64_t K, int64_t ldx, const cq_q4_job* jobs, int z,
+                             int64_t N, void* Y, int yt, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    if (!X || !jobs || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q4_batched: null pointer");
+    if (z < 1 || z > ZMAX) return fail(CQ_ERR_ARG, "cq_gemm_q4_batched: z must be in [1, %d] (got %d)", ZMAX, z);
+    cq_status st;
+    if ((st = check_x(xt)) || (st = check_y(yt))) return st;
+    if (T < 1 || N < 1 || K < 256 || K % 256 || T > (1LL << 31) - 1 || N > (1LL << 31) - 1)
+        return fail(CQ_ERR_SHAPE, "cq_gemm_q4_batched: need T>=1, N>=1, K%%256==0 (T=%lld K=%lld N=%lld)", (long long)T,
+                    (long long)K, (long long)N);
+    if (ldx < K || ldx % 8 || ldy < N)
+        return fail(CQ_ERR_SHAPE, "cq_gemm_q4_batched: need ldx >= K, ldx %% 8 == 0, ldy >= N (ldx=%lld ldy=%lld)",
+                    (long long)ldx, (long long)ldy);
+    for (int j = 0; j < z; ++j) {
+        const cq_q4_job& jb = jobs[j];
+        if (!jb.Wq || !jb.Ws) return fail(CQ_ERR_NULL, "cq_gemm_q4_batched: job %d: null weight pointer", j);
+        if (!aligned16(jb.Wq) || !aligned16(jb.Ws)) return fail(CQ_ERR_ALIGN, "cq_gemm_q4_batched: job %d: weights must be 16-byte aligned", j);
+        if (jb.x_off < 0 || jb.x_off % 8 || jb.x_off + K > ldx || jb.y_off < 0 || jb.y_off + N > ldy)
+            return fail(CQ_ERR_SHAPE, "cq_gemm_q4_batched: job %d: need x_off %% 8 == 0, x_off + K <= ldx, y_off + N <= ldy", j);
+    }
+    if (!aligned16(X) || !aligned16(Y)) return fail(CQ_ERR_ALIGN, "cq_gemm_q4_batched: X and Y must be 16-byte aligned");
+    const size_t need = (size_t)z * q4_ws_bytes(T, K);
+    if ((reinterpret_cast<uintptr_t>(ws) & (ALIGN - 1)) || ws_bytes < need)
+        return fail(CQ_ERR_WORKSPACE, "cq_gemm_q4_batched: workspace needs %zu bytes, 256-aligned", need);
+    if ((st = check_arch())) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = stream_error_word(s);
+    if (!err) return CQ_ERR_CUDA;
+    const size_t esz = yt == CQ_F32 ? 4 : 2;
+    const uint16_t* x16 = static_cast<const uint16_t*>(X);
+    uint8_t* y8 = static_cast<uint8_t*>(Y);
+    if (use_skinny(T)) {   // the activations as given: no guard pass
+        if (T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4_batched: the weight-streaming path serves T <= 32");
+        SkinnyDense a = {};
+        a.x_bf16 = xt == CQ_BF16;
+        a.T = T;
+        a.K = K;
+        a.N = N;
+        a.yt = yt;
+        a.err = err;
+        a.nz = z;
+        a.ldx = ldx;
+        a.ldy = ldy;
+        for (int j = 0; j < z; ++j)
+            a.more[j] = {x16 + jobs[j].x_off, nullptr, jobs[j].Wq, jobs[j].Ws, y8 + jobs[j].y_off * esz};
+        a.x = a.more[0].x;
+        a.wq = a.more[0].wq;
+        a.ws = a.more[0].ws;
+        a.y = a.more[0].y;
+        return launched(launch_skinny_q4(a, s), "z-batched weight-streaming Q4 GEMM");
+    }
+    // one guard pass per distinct activation slice (jobs that share X share it)
+    TcArgs a = {};
+    a.T = T;
+    a.K = K;
+    a.N = N;
+    a.yt = yt;
+    a.err = err;
+    a.nz = z;
+    a.ldy = ldy;
+    int slot_of[ZMAX];
+    int64_t slot_off[ZMAX];
+    int nslots = 0;
+    for (int j = 0; j < z; ++j) {
+        int c = 0;
+        while (c < nslots && slot_off[c] != jobs[j].x_off) ++c;
+        if (c == nslots) {
+            slot_off[nslots++] = jobs[j].x_off;
+            const Q4Ws w = q4_ws(static_cast<uint8_t*>(ws) + (size_t)c * q4_ws_bytes(T, K), T, K);
+            if ((st = launched(launch_x_half(x16 + jobs[j].x_off, xt, T, K, w.xh, w.rsx, s, ldx), "activation guard pass")))
+                return st;
+        }
+        slot_of[j] = c;
+    }
+    for (int j = 0; j < z; ++j) {
+        const Q4Ws w = q4_ws(static_cast<uint8_t*>(ws) + (size_t)slot_of[j] * q4_ws_bytes(T, K), T, K);
+        a.more[j] = {w.xh, w.rsx, nullptr, jobs[j].Wq, jobs[j].Ws, y8 + jobs[j].y_off * esz};
+    }
+    a.x = a.more[0].x;
+    a.rsx = a.more[0].rsx;
+    a.wq = a.more[0].wq;
+    a.ws = a.more[0].ws;
+    a.y = a.more[0].y;
+    return launched(launch_tc_q4(a, s), "z-batched tcgen05 Q4 GEMM");
+}
+
 size_t cq_ffn_q4_workspace_bytes(int64_t T, int64_t H, int64_t I) {
     if (T < 1 || H < 1 || I < 1) return 0;
     return ffn_layout(T, H, I).total;

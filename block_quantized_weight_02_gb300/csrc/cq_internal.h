@@ -57,7 +57,9 @@ cudaError_t launch_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, i
 // X rows -> fp16 with a per-row power-of-two guard; rsx = inverse scales.
 // Inside each 32-k block the output is in the Q4 streaming order (position
 // 8 wi + t <- k = 4 wi + {0,2,16,18,1,3,17,19}[t]) that both Q4 GEMMs read.
-cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s);
+// x rows of pitch ldx elements (0: K), 16-byte aligned.
+cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s,
+                          int64_t ldx = 0);
 // MoE routing layout and gathered guard pass in one launch: the layout (counts,
 // segment starts, stable grouping by expert, inverse map, active experts and
 // their number, status) and, for every pair in grouped order, its token's row
@@ -73,7 +75,19 @@ cudaError_t launch_moe_route_gather(const int32_t* idx, int64_t T, int64_t topk,
 cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,
                           cudaStream_t s);
 
-// Weight-streaming (small-T) GEMM.
+// Up to ZMAX weights of one shape in one launch (z-batched GEMM).
+constexpr int ZMAX = 4;
+
+// Weight-streaming (small-T) GEMM.  One job: the fields below; z-batched
+// (nz > 1): job j takes its activations, weights, scales and output from
+// more[j].  Activation rows have pitch ldx (0: K), output rows pitch ldy (0: N).
+struct SkJob {
+    const void* x;
+    const float* rs;
+    const uint8_t* wq;
+    const uint16_t* ws;
+    void* y;
+};
 struct SkinnyDense {
     const void* x;       // fp16/bf16 [T][K] as given (k order)
     int x_bf16;
@@ -85,6 +99,11 @@ struct SkinnyDense {
     void* y;
     int yt;
     int* err;            // the stream's device error word
+    int nz;
+    SkJob more[ZMAX];
+    int64_t ldx, ldy;
+    SkJob job(int j) const { return nz > 1 ? more[j] : SkJob{x, rs, wq, ws, y}; }
+    int jobs() const { return nz > 1 ? nz : 1; }
 };
 cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s);
 cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s);
@@ -114,7 +133,16 @@ struct SkinnyMoe {
 cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s);
 cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s);
 
-// tcgen05 (large-T) GEMM.
+// tcgen05 (large-T) GEMM.  One job: the fields below; z-batched (nz > 1):
+// job j takes its activations, scales, weights and output from more[j].
+struct TcJob {
+    const void* x;
+    const float* rsx;
+    const float* rs;
+    const uint8_t* wq;
+    const uint16_t* ws;
+    void* y;
+};
 struct TcArgs {
     const void* x;       // [T][K] fp16/bf16 (Q4: guarded fp16 in the streaming order)
     int x_bf16;
@@ -126,6 +154,11 @@ struct TcArgs {
     void* y;
     int yt;
     int* err;            // the stream's device error word
+    int nz;              // z-batched: number of jobs in more[] (0 or 1: the single job above)
+    TcJob more[ZMAX];
+    int64_t ldy;         // output row pitch in elements (0: N)
+    TcJob job(int j) const { return nz > 1 ? more[j] : TcJob{x, rsx, rs, wq, ws, y}; }
+    int jobs() const { return nz > 1 ? nz : 1; }
 };
 cudaError_t launch_tc_q4(const TcArgs& a, cudaStream_t s);
 cudaError_t launch_tc_q8(const TcArgs& a, cudaStream_t s);

@@ -200,20 +200,22 @@ __device__ __forceinline__ void guard_row(const T* __restrict__ xrow, int64_t K,
 
 // One CTA of 256 threads per activation row.
 template <typename T>
-__global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t K, __half* __restrict__ xh,
+__global__ void __launch_bounds__(256) k_x_half(const T* __restrict__ x, int64_t K, int64_t ldx, __half* __restrict__ xh,
                                                 float* __restrict__ rsx) {
     pdl_launch_dependents();   // the GEMM after this pass may start streaming its weights now
     pdl_wait();                // inputs ready and the previous readers of xh done
     __shared__ float red[8];
     const int64_t row = blockIdx.x;
-    guard_row<T>(x + row * K, K, xh + row * K, rsx + row, red);
+    guard_row<T>(x + row * ldx, K, xh + row * K, rsx + row, red);
 }
 
-cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s) {
+cudaError_t launch_x_half(const void* x, int xt, int64_t T, int64_t K, uint16_t* xh, float* rsx, cudaStream_t s,
+                          int64_t ldx) {
+    if (ldx <= 0) ldx = K;
     if (xt == CQ_BF16)
         return launch_pdl(k_x_half<__nv_bfloat16>, dim3((unsigned)T), dim3(256), 0, s,
-                          reinterpret_cast<const __nv_bfloat16*>(x), K, reinterpret_cast<__half*>(xh), rsx);
-    return launch_pdl(k_x_half<__half>, dim3((unsigned)T), dim3(256), 0, s, reinterpret_cast<const __half*>(x), K,
+                          reinterpret_cast<const __nv_bfloat16*>(x), K, ldx, reinterpret_cast<__half*>(xh), rsx);
+    return launch_pdl(k_x_half<__half>, dim3((unsigned)T), dim3(256), 0, s, reinterpret_cast<const __half*>(x), K, ldx,
                       reinterpret_cast<__half*>(xh), rsx);
 }
 

@@ -50,6 +50,7 @@
 // short inputs ("oxinfer 0.0.5 src/metal.rs", mma_tile with TM = 32).
 #include <algorithm>
 #include <cooperative_groups.h>
+#include <cstring>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -92,10 +93,21 @@ struct Params {
     const int32_t* n_act; // MoE: number of active experts
     int rbs;              // MoE: row blocks per expert matrix
     int* err;             // the stream's device error word
+    // DENSE, z-batched: job blockIdx.z writes yj[z] (rows of pitch ldy), Q8 row scales rsj[z]
+    void* yj[ZMAX];
+    const float* rsj[ZMAX];
+    int64_t ldy;
     // DOWN: the weighted combine, folded in (Y [T][H] written by the last item of each row block)
     const int32_t* inv;   // grouped position of each pair id
     int32_t* cnt;         // [H / 128] items finished per row block (zero at the start of the call)
     int topk;
+};
+
+// Tensor maps of every job (MoE modes: job 0 only): weights, Q4 scales, activations.
+struct SMaps {
+    CUtensorMap w[ZMAX];
+    CUtensorMap s[ZMAX];
+    CUtensorMap x[ZMAX];
 };
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -203,8 +215,7 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_
 // matched by the adjacent-k decode; no guard scale applies (Q4 dense only).
 template <int FMT, int NT, int MT, int KW, int XBF, int MODE, int NSLOT, int RAW>
 __global__ void __launch_bounds__(THREADS, 2)
-k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
-         const __grid_constant__ CUtensorMap tmX, const Params p) {
+k_skinny(const __grid_constant__ SMaps maps, const Params p) {
     constexpr int NCOL = 8 * NT;
     constexpr int RG = CONSUMERS / KW;        // warps along rows
     constexpr int RB = rows_per_stage(MT, KW);
@@ -218,6 +229,11 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
+    // dense, z-batched: job blockIdx.z (its own weights, activations and output)
+    const int jz = MODE == DENSE ? (int)blockIdx.z : 0;
+    const CUtensorMap* tmW = &maps.w[jz];
+    const CUtensorMap* tmS = &maps.s[jz];
+    const CUtensorMap* tmX = &maps.x[jz];
     pdl_launch_dependents();   // the next kernel in the stream may be scheduled now
     // ---- work items: (expert, row block) pairs; each may hold several column groups ----
     // dense: one item per CTA (row block blockIdx.y, k range blockIdx.x of the cluster);
@@ -311,9 +327,9 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
         if (lane < NSLOT) {
             const int s = lane;
             if (lane == 0) {
-                tma_prefetch_desc(&tmW);
-                if (FMT == 0) tma_prefetch_desc(&tmS);
-                tma_prefetch_desc(&tmX);
+                tma_prefetch_desc(tmW);
+                if (FMT == 0) tma_prefetch_desc(tmS);
+                tma_prefetch_desc(tmX);
             }
             int last_gi = -1;         // the last stage this lane issued
             uint32_t last_phase = 0;  // and the phase of its round
@@ -323,14 +339,14 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 const int st = st0 + i;
                 if (MODE == GATEUP) {      // gate rows and up rows are two 64-row boxes
                     for (int bx = 0; bx < 2; ++bx) {
-                        tma_load_3d(sbase + (uint32_t)(bx * (RB / 2) * 128), &tmW, full_bar(s), st * 128,
+                        tma_load_3d(sbase + (uint32_t)(bx * (RB / 2) * 128), tmW, full_bar(s), st * 128,
                                     it.row_box[bx], it.expert);
-                        tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * (RB / 2) * 16), &tmS, full_bar(s), st * 8,
+                        tma_load_3d(sbase + (uint32_t)(G::W_BYTES + bx * (RB / 2) * 16), tmS, full_bar(s), st * 8,
                                     it.row_box[bx], it.expert);
                     }
                 } else {
-                    tma_load_3d(sbase, &tmW, full_bar(s), st * 128, it.row_box[0], it.expert);
-                    if (FMT == 0) tma_load_3d(sbase + (uint32_t)G::W_BYTES, &tmS, full_bar(s), st * 8, it.row_box[0], it.expert);
+                    tma_load_3d(sbase, tmW, full_bar(s), st * 128, it.row_box[0], it.expert);
+                    if (FMT == 0) tma_load_3d(sbase + (uint32_t)G::W_BYTES, tmS, full_bar(s), st * 8, it.row_box[0], it.expert);
                 }
             };
             auto load_x = [&](const Item& it, int i, int grp) {
@@ -338,7 +354,7 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 const int st = st0 + i;
                 // activation rows of this column group (dense: tokens; MoE: grouped pairs)
                 const int xrow0 = (int)(it.col0 + (int64_t)grp * NCOL);
-                tma_load_3d(sbase + (uint32_t)G::X_OFF, &tmX, full_bar(s), 0, st * G::XSL, xrow0);
+                tma_load_3d(sbase + (uint32_t)G::X_OFF, tmX, full_bar(s), 0, st * G::XSL, xrow0);
             };
             constexpr uint32_t FULL_BYTES = (uint32_t)G::BYTES;   // bytes of a stage
             // The weights of the first ring fill are requested before waiting for the
@@ -630,17 +646,38 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
               asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
               if (*last_flag) {
                   __threadfence();
-                  const int64_t n0 = (int64_t)rb * RB;
-                  for (int e = threadIdx.x; e < (int)p.T * RB; e += CONSUMERS * 32) {
-                      const int64_t t = e / RB;
-                      const int r = e & (RB - 1);
-                      float acc = 0.f;
-                      for (int j = 0; j < p.topk; ++j) {
-                          const int64_t q = p.inv[t * p.topk + j];
-                          acc += __ldcg(p.out + q * p.H + n0 + r);   // other CTAs' rows: not from L1
+                  // one consumer warp per token, lane l owning rows 4 l .. 4 l + 3 of the block;
+                  // the slots' rows are loaded eight at a time (independent loads in flight),
+                  // then added in slot order
+                  const int64_t n0 = (int64_t)rb * RB + 4 * lane;
+                  for (int64_t t = warp; t < p.T; t += CONSUMERS) {
+                      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                      for (int j0 = 0; j0 < p.topk; j0 += 8) {
+                          float4 v[8];
+#pragma unroll
+                          for (int jj = 0; jj < 8; ++jj) {
+                              if (j0 + jj < p.topk) {
+                                  const int64_t q = __ldg(p.inv + t * p.topk + j0 + jj);
+                                  v[jj] = __ldcg(reinterpret_cast<const float4*>(p.out + q * p.H + n0));   // not from L1
+                              }
+                          }
+#pragma unroll
+                          for (int jj = 0; jj < 8; ++jj) {
+                              if (j0 + jj < p.topk) {
+                                  acc.x += v[jj].x;
+                                  acc.y += v[jj].y;
+                                  acc.z += v[jj].z;
+                                  acc.w += v[jj].w;
+                              }
+                          }
                       }
-                      if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.H + n0 + r] = acc;
-                      else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.H + n0 + r] = __float2bfloat16_rn(acc);
+                      if (p.yt == CQ_F32) {
+                          *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + t * p.H + n0) = acc;
+                      } else {
+                          __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.y) + t * p.H + n0);
+                          o[0] = __floats2bfloat162_rn(acc.x, acc.y);
+                          o[1] = __floats2bfloat162_rn(acc.z, acc.w);
+                      }
                   }
                   if (threadIdx.x == 0) p.cnt[rb] = 0;
               }
@@ -650,6 +687,8 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
 
     if (MODE == DENSE) {
         const int rb = blockIdx.y;
+        void* const Yj = jz == 0 ? p.yj[0] : jz == 1 ? p.yj[1] : jz == 2 ? p.yj[2] : p.yj[3];
+        const float* const RSj = jz == 0 ? p.rsj[0] : jz == 1 ? p.rsj[1] : jz == 2 ? p.rsj[2] : p.rsj[3];
         pdl_wait();   // outputs only after the previous kernel has finished
         // ---- sum the cluster's partial tiles in rank order, epilogue ----
         // Rank q finishes slice q of the tile.  Every rank pushes its partial values of
@@ -675,9 +714,9 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                     for (int q = 0; q < p.ks; ++q) s += recv[q * per + (e - lo)];
                     const int64_t n = (int64_t)rb * RB + r, t = col;
                     if (n < p.N && t < p.T) {
-                        const float v = s * (FMT == 0 ? (RAW ? 1.f : p.rsx[t]) : p.rs[n]);
-                        if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = v;
-                        else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(v);
+                        const float v = s * (FMT == 0 ? (RAW ? 1.f : p.rsx[t]) : RSj[n]);
+                        if (p.yt == CQ_F32) reinterpret_cast<float*>(Yj)[t * p.ldy + n] = v;
+                        else reinterpret_cast<__nv_bfloat16*>(Yj)[t * p.ldy + n] = __float2bfloat16_rn(v);
                     }
                 }
             }
@@ -686,9 +725,9 @@ k_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtens
                 const int r = e & (RB - 1), col = e / RB;
                 const int64_t n = (int64_t)rb * RB + r, t = col;
                 if (n < p.N && t < p.T) {
-                    const float v = part[r * NCOL + col] * (FMT == 0 ? (RAW ? 1.f : p.rsx[t]) : p.rs[n]);
-                    if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = v;
-                    else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(v);
+                    const float v = part[r * NCOL + col] * (FMT == 0 ? (RAW ? 1.f : p.rsx[t]) : RSj[n]);
+                    if (p.yt == CQ_F32) reinterpret_cast<float*>(Yj)[t * p.ldy + n] = v;
+                    else reinterpret_cast<__nv_bfloat16*>(Yj)[t * p.ldy + n] = __float2bfloat16_rn(v);
                 }
             }
         }
@@ -728,20 +767,23 @@ bool make_maps(CUtensorMap* mw, CUtensorMap* ms, int fmt, const uint8_t* wq, con
 
 // Activations [rows][K] 16-bit seen as {64 elements, K/64 slabs, rows}; one box
 // is xsl slabs of ncol rows, stored [row][slab][128 B] with the 128-byte swizzle.
-bool make_xmap(CUtensorMap* mx, const void* x, int64_t rows, int64_t K, int bf16, int ncol, int xsl) {
+bool make_xmap(CUtensorMap* mx, const void* x, int64_t rows, int64_t K, int64_t ldx, int bf16, int ncol, int xsl) {
     uint64_t d[3] = {64, (uint64_t)K / 64, (uint64_t)rows};
-    uint64_t st[2] = {128, (uint64_t)K * 2};
+    uint64_t st[2] = {128, (uint64_t)ldx * 2};
     uint32_t box[3] = {64, (uint32_t)xsl, (uint32_t)ncol};
     return encode_tiled(mx, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x, d, st,
                         box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// maps: w and s filled for each of the nz jobs; xs[j] the activations of job j
+// (xrows rows of pitch ldx).
 template <int FMT, int NT, int MT, int KW, int XBF, int MODE, int NSLOT, int RAW = 0>
-cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, int64_t xrows, const Params& p,
+cudaError_t launch_t(SMaps maps, const void* const* xs, int nz, int64_t xrows, int64_t ldx, const Params& p,
                      dim3 grid, int cluster, cudaStream_t s) {
     constexpr int RB = rows_per_stage(MT, KW);
-    CUtensorMap mx;
-    if (!make_xmap(&mx, x, xrows, p.K, XBF, 8 * NT, StageGeo<FMT, 8 * NT, RB>::XSL)) return cudaErrorInvalidValue;
+    for (int j = 0; j < nz; ++j)
+        if (!make_xmap(&maps.x[j], xs[j], xrows, p.K, ldx, XBF, 8 * NT, StageGeo<FMT, 8 * NT, RB>::XSL))
+            return cudaErrorInvalidValue;
     auto kern = k_skinny<FMT, NT, MT, KW, XBF, MODE, NSLOT, RAW>;
     constexpr size_t smem = smem_bytes<FMT, NT, RB, MODE, NSLOT>();
     static_assert(smem <= 113 * 1024, "two CTAs per SM");
@@ -769,7 +811,7 @@ cudaError_t launch_t(const CUtensorMap& mw, const CUtensorMap& ms, const void* x
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, mw, ms, mx, p);
+    return cudaLaunchKernelEx(&cfg, kern, maps, p);
 }
 
 // Layout and ring depth per column count (as many stages as fit two CTAs
@@ -787,19 +829,28 @@ DenseCfg dense_cfg(int64_t T) {
 
 // Q4 takes the activations as given (RAW), in k order.
 template <int FMT, int XBF>
-cudaError_t launch_dense_nt(const CUtensorMap& mw, const CUtensorMap& ms, const void* x, const Params& p, dim3 grid,
+cudaError_t launch_dense_nt(const SMaps& maps, const void* const* xs, int nz, int64_t ldx, const Params& p, dim3 grid,
                             int cluster, int64_t T, cudaStream_t s) {
     constexpr int RAW = FMT == 0 ? 1 : 0;
-    if (T <= 8) return launch_t<FMT, 1, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 5, RAW>(mw, ms, x, T, p, grid, cluster, s);
-    if (T <= 16) return launch_t<FMT, 2, 1, 1, XBF, DENSE, FMT == 0 ? 3 : 5, RAW>(mw, ms, x, T, p, grid, cluster, s);
-    return launch_t<FMT, 4, 1, 2, XBF, DENSE, FMT == 0 ? 4 : 6, RAW>(mw, ms, x, T, p, grid, cluster, s);
+    if (T <= 8) return launch_t<FMT, 1, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 5, RAW>(maps, xs, nz, T, ldx, p, grid, cluster, s);
+    if (T <= 16) return launch_t<FMT, 2, 1, 1, XBF, DENSE, FMT == 0 ? 3 : 5, RAW>(maps, xs, nz, T, ldx, p, grid, cluster, s);
+    return launch_t<FMT, 4, 1, 2, XBF, DENSE, FMT == 0 ? 4 : 6, RAW>(maps, xs, nz, T, ldx, p, grid, cluster, s);
 }
 
 cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     const DenseCfg cf = dense_cfg(a.T);
-    CUtensorMap mw, ms;
-    if (!make_maps(&mw, &ms, fmt, a.wq, a.ws, a.N, a.K, 1, cf.rb)) return cudaErrorInvalidValue;
+    const int nz = a.jobs();
+    SMaps maps;
+    memset(&maps, 0, sizeof maps);
+    const void* xs[ZMAX] = {};
     Params p = {};
+    for (int j = 0; j < nz; ++j) {
+        const SkJob jb = a.job(j);
+        if (!make_maps(&maps.w[j], &maps.s[j], fmt, jb.wq, jb.ws, a.N, a.K, 1, cf.rb)) return cudaErrorInvalidValue;
+        xs[j] = jb.x;
+        p.yj[j] = jb.y;
+        p.rsj[j] = jb.rs;
+    }
     p.K = a.K;
     p.nst_total = (int)(a.K / (fmt == 0 ? 256 : 128));
     p.N = a.N;
@@ -808,6 +859,7 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     p.rs = a.rs;
     p.y = a.y;
     p.yt = a.yt;
+    p.ldy = a.ldy > 0 ? a.ldy : a.N;
     p.wait_ns = (uint64_t)options().wait_ns;
     p.pdl = 1;
     p.err = a.err;
@@ -817,17 +869,18 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     int ks = 1;
     const int64_t cap = 2 * (int64_t)num_sms();
     for (int cand : {2, 4, 8})
-        if (rbs * cand <= cap && p.nst_total / cand >= 2) ks = cand;
+        if (rbs * cand * nz <= cap && p.nst_total / cand >= 2) ks = cand;
     p.ks = ks;
-    dim3 grid((unsigned)ks, (unsigned)rbs, 1);
+    dim3 grid((unsigned)ks, (unsigned)rbs, (unsigned)nz);
     if (options().trace)
-        fprintf(stderr, "cq: skinny fmt=%d T=%lld N=%lld K=%lld rows/stage=%d grid=(%d,%lld) cluster=%d\n", fmt,
-                (long long)a.T, (long long)a.N, (long long)a.K, cf.rb, ks, (long long)rbs, ks);
+        fprintf(stderr, "cq: skinny fmt=%d T=%lld N=%lld K=%lld rows/stage=%d grid=(%d,%lld,%d) cluster=%d\n", fmt,
+                (long long)a.T, (long long)a.N, (long long)a.K, cf.rb, ks, (long long)rbs, nz, ks);
+    const int64_t ldx = a.ldx > 0 ? a.ldx : a.K;
     if (fmt == 0)
-        return a.x_bf16 ? launch_dense_nt<0, 1>(mw, ms, a.x, p, grid, ks, a.T, s)
-                        : launch_dense_nt<0, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
-    return a.x_bf16 ? launch_dense_nt<1, 1>(mw, ms, a.x, p, grid, ks, a.T, s)
-                    : launch_dense_nt<1, 0>(mw, ms, a.x, p, grid, ks, a.T, s);
+        return a.x_bf16 ? launch_dense_nt<0, 1>(maps, xs, nz, ldx, p, grid, ks, a.T, s)
+                        : launch_dense_nt<0, 0>(maps, xs, nz, ldx, p, grid, ks, a.T, s);
+    return a.x_bf16 ? launch_dense_nt<1, 1>(maps, xs, nz, ldx, p, grid, ks, a.T, s)
+                    : launch_dense_nt<1, 0>(maps, xs, nz, ldx, p, grid, ks, a.T, s);
 }
 
 }  // namespace
@@ -839,9 +892,10 @@ cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s) { return laun
 // grouped order ([P][H] fp16, inverse scales [P]).  One item is 64 gate rows
 // and the 64 matching up rows of one expert.
 cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s) {
-    CUtensorMap mw, ms;
+    SMaps maps;
+    memset(&maps, 0, sizeof maps);
     constexpr int RB = rows_per_stage(1, 1);
-    if (!make_maps(&mw, &ms, 0, m.gu_q, m.gu_s, 2 * m.I, m.H, m.E, RB / 2)) return cudaErrorInvalidValue;
+    if (!make_maps(&maps.w[0], &maps.s[0], 0, m.gu_q, m.gu_s, 2 * m.I, m.H, m.E, RB / 2)) return cudaErrorInvalidValue;
     Params p = {};
     p.K = m.H;
     p.nst_total = (int)(m.H / 256);
@@ -864,13 +918,15 @@ cudaError_t launch_moe_gateup(const SkinnyMoe& m, cudaStream_t s) {
     // persistent: two CTAs per SM share the (active expert x row block) items
     const int64_t items_max = m.E * p.rbs;
     dim3 grid((unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items_max), 1, 1);
-    return launch_t<0, 1, 1, 1, 0, GATEUP, 4>(mw, ms, m.xh, m.T * m.topk, p, grid, 1, s);
+    const void* xs[1] = {m.xh};
+    return launch_t<0, 1, 1, 1, 0, GATEUP, 4>(maps, xs, 1, m.T * m.topk, m.H, p, grid, 1, s);
 }
 
 cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s) {
-    CUtensorMap mw, ms;
+    SMaps maps;
+    memset(&maps, 0, sizeof maps);
     constexpr int RB = rows_per_stage(1, 1);
-    if (!make_maps(&mw, &ms, 0, m.d_q, m.d_s, m.H, m.I, m.E, RB)) return cudaErrorInvalidValue;
+    if (!make_maps(&maps.w[0], &maps.s[0], 0, m.d_q, m.d_s, m.H, m.I, m.E, RB)) return cudaErrorInvalidValue;
     Params p = {};
     p.K = m.I;
     p.nst_total = (int)(m.I / 256);
@@ -898,7 +954,8 @@ cudaError_t launch_moe_down(const SkinnyMoe& m, cudaStream_t s) {
     p.rbs = (int)(m.H / RB);
     const int64_t items_max = m.E * p.rbs;
     dim3 grid((unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items_max), 1, 1);
-    return launch_t<0, 1, 1, 1, 0, DOWN, 4>(mw, ms, m.ah, m.T * m.topk, p, grid, 1, s);
+    const void* xs[1] = {m.ah};
+    return launch_t<0, 1, 1, 1, 0, DOWN, 4>(maps, xs, 1, m.T * m.topk, m.I, p, grid, 1, s);
 }
 
 }  // namespace cq

@@ -10,8 +10,9 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     const int64_t mt = (a.N + BM - 1) / BM;
     const Plan pl = plan_tiles(a, mt, false);
     const int bn = pl.bn, ks = pl.ks;
-    const Params p = make_params(a);
-    dim3 grid((unsigned)mt, (unsigned)((a.T + bn - 1) / bn), (unsigned)ks);
+    Params p = make_params(a);
+    p.tiles_y = (int)((a.T + bn - 1) / bn);
+    dim3 grid((unsigned)mt, (unsigned)(p.tiles_y * a.jobs()), (unsigned)ks);
     // decoded weight operand: 1 = shared memory, 2 = tensor memory (default)
     const int am = options().tc_amode == 1 ? 0 : 1;
     const bool pair = am == 1 && (bn >= 128 || bn == 32) && pl.pair_ok;

@@ -49,6 +49,7 @@
 // the two sets of instantiations compile in parallel.
 #pragma once
 #include <algorithm>
+#include <cstring>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -62,11 +63,24 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 
-struct Params {
-    const float* rsx;
-    const float* rs;
+// Per-job pointers of a z-batched launch (job = blockIdx.y / tiles_y).
+struct Job {
+    const float* rsx;     // Q4: guard inverse scale per activation row
+    const float* rs;      // Q8: row scales
     const uint16_t* ws;   // Q4 block scales [N][K/32]
-    void* y;
+    void* y;              // output rows of pitch ldy
+};
+// Tensor maps of every job: weights, activations, outputs.
+struct Maps {
+    CUtensorMap w[ZMAX];
+    CUtensorMap x[ZMAX];
+    CUtensorMap y[ZMAX];
+};
+
+struct Params {
+    Job job[ZMAX];
+    int tiles_y;          // token tiles per job
+    int64_t ldy;          // output row pitch (elements)
     int yt;
     int64_t T, N, K;
     uint64_t wait_ns;
@@ -194,8 +208,7 @@ __device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
 // peer is rank ^ 1, the K-split partner rank ^ CG.
 template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS, int CG, int GU>
 __global__ void __launch_bounds__(THREADS, 1)
-k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-     const __grid_constant__ CUtensorMap tmY, const Params p) {
+k_tc(const __grid_constant__ Maps maps, const Params p) {
     using L = Layout<FMT, BN, G, LSS, AS, AM, CG>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -204,7 +217,12 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // first weight row (gate/up mode: first gate row i0; the tile is i0 .. i0 + 63 and I + i0 ..)
     const int m0 = blockIdx.x * (GU ? BM / 2 : BM);
-    const int t0 = blockIdx.y * BN;          // first activation row
+    const int jz = (int)blockIdx.y / p.tiles_y;                 // job of a z-batched launch
+    const int t0 = ((int)blockIdx.y - jz * p.tiles_y) * BN;    // first activation row
+    const Job J = jz == 0 ? p.job[0] : jz == 1 ? p.job[1] : jz == 2 ? p.job[2] : p.job[3];
+    const CUtensorMap* tmW = &maps.w[jz];
+    const CUtensorMap* tmX = &maps.x[jz];
+    const CUtensorMap* tmY = &maps.y[jz];
     const int kz = KS > 1 ? (int)blockIdx.z : 0;
     const uint32_t crank = (KS > 1 || CG > 1) ? cluster_ctarank() : 0u;   // rank in the cluster
     const int cx = CG > 1 ? (int)(crank & 1u) : 0;                // position in the CTA pair
@@ -291,18 +309,18 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         const bool wl = lane < LSS, xl = lane >= LSS && lane < 2 * LSS;
         if (wl || xl) {
             if (lane == 0) {
-                tma_prefetch_desc(&tmW);
-                tma_prefetch_desc(&tmX);
+                tma_prefetch_desc(tmW);
+                tma_prefetch_desc(tmX);
             }
             const uint32_t base = slot_base(s);
             int issued = 0;        // super-stages issued by this lane
             auto issue = [&](int j) {
                 if (wl) {
                     mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::X_BYTES + L::W_BYTES));
-                    if (GU) tma_load_3d(base + L::X_BYTES, &tmW, full_bar(s), (j0 + j) * L::WROW, m0, 0);
-                    else tma_load_2d(base + L::X_BYTES, &tmW, full_bar(s), (j0 + j) * L::WROW, m0);
+                    if (GU) tma_load_3d(base + L::X_BYTES, tmW, full_bar(s), (j0 + j) * L::WROW, m0, 0);
+                    else tma_load_2d(base + L::X_BYTES, tmW, full_bar(s), (j0 + j) * L::WROW, m0);
                 } else {
-                    tma_load_3d(base, &tmX, full_bar(s), 0, t0 + cx * (BN / CG), (j0 + j) * G);
+                    tma_load_3d(base, tmX, full_bar(s), 0, t0 + cx * (BN / CG), (j0 + j) * G);
                 }
             };
             if (!p.stall) {
@@ -443,7 +461,7 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                                             : (uint32_t)((r >> 2) & 1);
         // Q4 scales of this row: the two fp16 of stage kb (blocks 2 kb, 2 kb + 1), loaded two
         // of this group's stages ahead
-        const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.ws + n * (p.K / 32)) + k0;
+        const uint32_t* srow = reinterpret_cast<const uint32_t*>(J.ws + n * (p.K / 32)) + k0;
         uint32_t sc0 = 0, sc1 = 0;
         if (FMT == 0 && row_ok) {
             if (grp < nk) sc0 = __ldg(srow + grp);
@@ -562,10 +580,10 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
         pdl_wait();
         if (FMT == 0) {
             const int64_t tb = (int64_t)t0 + cbase + grp * CW;
-            if (grp < NG && lane < CW && tb + lane < p.T) esc0 = p.rsx[tb + lane];
-            if (grp < NG && CW > 32 && tb + 32 + lane < p.T) esc1 = p.rsx[tb + 32 + lane];
+            if (grp < NG && lane < CW && tb + lane < p.T) esc0 = J.rsx[tb + lane];
+            if (grp < NG && CW > 32 && tb + 32 + lane < p.T) esc1 = J.rsx[tb + 32 + lane];
         } else if (row_ok) {
-            esc0 = p.rs[n];
+            esc0 = J.rs[n];
         }
         // the accumulator is complete once the MMA thread's last commit arrives
         if (!*abort_flag && !mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) give_up();
@@ -658,8 +676,8 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                         if (f32) reinterpret_cast<float*>(smem + YST_OFF)[(cc + jj) * 128 + r] = val;
                         else reinterpret_cast<__nv_bfloat16*>(smem + YST_OFF)[(cc + jj) * 128 + r] = __float2bfloat16_rn(val);
                     } else if (!skip && row_ok && t < p.T) {
-                        if (f32) reinterpret_cast<float*>(p.y)[t * p.N + n] = val;
-                        else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(val);
+                        if (f32) reinterpret_cast<float*>(J.y)[t * p.ldy + n] = val;
+                        else reinterpret_cast<__nv_bfloat16*>(J.y)[t * p.ldy + n] = __float2bfloat16_rn(val);
                     }
                 }
                 if (GU) {
@@ -677,13 +695,13 @@ k_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMa
                         const int64_t t = tb + jj;
                         const float g = stg[(cc + jj) * 128 + i], u = stg[(cc + jj) * 128 + BM / 2 + i];
                         if (!skip && gi < p.N && t < p.T)
-                            reinterpret_cast<float*>(p.y)[t * p.N + gi] = g / (1.0f + expf(-g)) * u;
+                            reinterpret_cast<float*>(J.y)[t * p.ldy + gi] = g / (1.0f + expf(-g)) * u;
                     }
                 } else if (p.y_tma) {
                     fence_proxy_async_smem();
                     named_bar_sync(gbar, 128);
                     if (lead && !*abort_flag) {
-                        tma_store_2d(&tmY, sb + YST_OFF + (uint32_t)(cc * 128 * esz), m0, (int)tb);
+                        tma_store_2d(tmY, sb + YST_OFF + (uint32_t)(cc * 128 * esz), m0, (int)tb);
                         bulk_commit();
                     }
                 }
@@ -723,44 +741,49 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
                   "decoded slots owned by fixed decoder groups");
     static_assert(GU == 0 || FMT == 0, "gate/up mode: Q4 weights");
     // weights: rows of G stages (G * ROW bytes) per box
-    CUtensorMap mw, mx;
-    {
-        const uint64_t kbytes = FMT == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
-        const CUtensorMapSwizzle swz = L::WROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                       : L::WROW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    // one set of tensor maps per job (a z-batched launch holds up to ZMAX jobs of one shape)
+    Maps maps;
+    memset(&maps, 0, sizeof maps);
+    const uint64_t kbytes = FMT == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+    const CUtensorMapSwizzle swz = L::WROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : L::WROW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    const int64_t ldy = a.ldy > 0 ? a.ldy : a.N;
+    for (int j = 0; j < a.jobs(); ++j) {
+        const TcJob jb = a.job(j);
         if (GU) {
             // [2][I][K bytes]: gate half, up half; one box = 64 gate rows then the 64 matching up rows
             uint64_t d[3] = {kbytes, (uint64_t)a.N, 2};
             uint64_t st[2] = {kbytes, kbytes * (uint64_t)a.N};
             uint32_t box[3] = {(uint32_t)L::WROW, (uint32_t)(BM / 2), 2};
-            if (!encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.wq, d, st, box, swz)) return cudaErrorInvalidValue;
+            if (!encode_tiled(&maps.w[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, jb.wq, d, st, box, swz))
+                return cudaErrorInvalidValue;
         } else {
             uint64_t d[2] = {kbytes, (uint64_t)a.N};
             uint64_t st[1] = {kbytes};
             uint32_t box[2] = {(uint32_t)L::WROW, (uint32_t)BM};
-            if (!encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.wq, d, st, box, swz)) return cudaErrorInvalidValue;
+            if (!encode_tiled(&maps.w[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, jb.wq, d, st, box, swz))
+                return cudaErrorInvalidValue;
         }
-    }
-    // activations seen as {64 elements, T rows, K/64 chunks} (strides K*2 B, 128 B): one
-    // box of G chunks of BN / CG rows lands as [chunk][row][128 B], G operand tiles
-    {
-        uint64_t d[3] = {64, (uint64_t)a.T, (uint64_t)a.K / 64};
-        uint64_t st[2] = {(uint64_t)a.K * 2, 128};
-        uint32_t box[3] = {64, (uint32_t)(BN / CG), (uint32_t)G};
-        if (!encode_tiled(&mx, XBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.x, d,
-                          st, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
-    }
-    // output tiles: Y [T][N] seen as {N, T}; a box is 128 rows x one epilogue chunk of columns
-    CUtensorMap my = mx;
-    if (p.y_tma) {
-        const uint64_t es = a.yt == CQ_F32 ? 4 : 2;
-        uint64_t d[2] = {(uint64_t)a.N, (uint64_t)a.T};
-        uint64_t st[1] = {(uint64_t)a.N * es};
-        uint32_t box[2] = {(uint32_t)BM, (uint32_t)ep_chunk(BN, KS)};
-        if (!encode_tiled(&my, a.yt == CQ_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                          a.y, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
+        // activations seen as {64 elements, T rows, K/64 chunks} (strides K*2 B, 128 B): one
+        // box of G chunks of BN / CG rows lands as [chunk][row][128 B], G operand tiles
+        {
+            uint64_t d[3] = {64, (uint64_t)a.T, (uint64_t)a.K / 64};
+            uint64_t st[2] = {(uint64_t)a.K * 2, 128};
+            uint32_t box[3] = {64, (uint32_t)(BN / CG), (uint32_t)G};
+            if (!encode_tiled(&maps.x[j], XBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                              jb.x, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+        }
+        // output tiles: Y [T][N] (pitch ldy) seen as {N, T}; a box is 128 rows x one epilogue chunk
+        if (p.y_tma) {
+            const uint64_t es = a.yt == CQ_F32 ? 4 : 2;
+            uint64_t d[2] = {(uint64_t)a.N, (uint64_t)a.T};
+            uint64_t st[1] = {(uint64_t)ldy * es};
+            uint32_t box[2] = {(uint32_t)BM, (uint32_t)ep_chunk(BN, KS)};
+            if (!encode_tiled(&maps.y[j], a.yt == CQ_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              2, jb.y, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+                return cudaErrorInvalidValue;
+        }
     }
     auto kern = k_tc<FMT, BN, XBF, G, LSS, AS, AM, KS, CG, GU>;
     static int configured_device = -1;       // attributes are per device; set once per instantiation
@@ -793,7 +816,7 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, mw, mx, my, p);
+    return cudaLaunchKernelEx(&cfg, kern, maps, p);
 }
 
 // Tile plan: token tile BN and K split.  One CTA per SM.  Time of a CTA ~ its
@@ -830,12 +853,12 @@ Plan plan_tiles(const TcArgs& a, int64_t mt, bool tmem_only) {
         if (bn == 0 && 2 * a.T <= c.bn && c.bn > 32) continue;   // at least half of every tile's columns unused
         if (c.bn == 32 && amode == 1) continue;
         // split only to fill the GPU: when the unsplit tiles leave a quarter of the SMs idle
-        if (c.ks == 2 && (!ks2_ok || (ks == 0 && mt * ((a.T + c.bn - 1) / c.bn) * 4 > 3 * num_sms()))) continue;
+        if (c.ks == 2 && (!ks2_ok || (ks == 0 && mt * ((a.T + c.bn - 1) / c.bn) * a.jobs() * 4 > 3 * num_sms()))) continue;
         if (c.bn == 192 && c.ks != 1) continue;
         if (c.bn == 192 && !pair_ok) continue;   // 192-column tiles only in CTA pairs
         const double stage = c.bn == 256 ? (pair_ok ? 690.0 : 800.0) : c.bn == 192 ? 680.0
                            : c.bn == 128 ? (pair_ok ? 515.0 : 570.0) : c.bn == 64 ? 520.0 : (pair_ok ? 300.0 : 520.0);
-        const int64_t ctas = mt * ((a.T + c.bn - 1) / c.bn) * c.ks;
+        const int64_t ctas = mt * ((a.T + c.bn - 1) / c.bn) * c.ks * a.jobs();
         const int64_t waves = (ctas + num_sms() - 1) / num_sms();
         const double cost = (double)waves * ((double)(nk / c.ks) * stage + (c.ks > 1 ? 6000.0 : 0.0));
         if (best < 0.0 || cost < best - 1e-9) {
@@ -853,10 +876,12 @@ Plan plan_tiles(const TcArgs& a, int64_t mt, bool tmem_only) {
 
 Params make_params(const TcArgs& a) {
     Params p = {};
-    p.rsx = a.rsx;
-    p.rs = a.rs;
-    p.ws = a.ws;
-    p.y = a.y;
+    for (int j = 0; j < a.jobs(); ++j) {
+        const TcJob jb = a.job(j);
+        p.job[j] = {jb.rsx, jb.rs, jb.ws, jb.y};
+    }
+    p.tiles_y = 1;
+    p.ldy = a.ldy > 0 ? a.ldy : a.N;
     p.yt = a.yt;
     p.T = a.T;
     p.N = a.N;
@@ -864,7 +889,10 @@ Params make_params(const TcArgs& a) {
     p.wait_ns = (uint64_t)options().wait_ns;
     p.stall = (int)options().test_stall.exchange(0);
     p.pdl = 1;   // the guard pass (Q4) or the previous kernel touches neither the weights nor anything before the wait
-    p.y_tma = ((a.N * (a.yt == CQ_F32 ? 4 : 2)) % 16 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0) ? 1 : 0;
+    // every job's output tiles leave through TMA stores when every row pitch and base is 16-byte aligned
+    p.y_tma = (p.ldy * (a.yt == CQ_F32 ? 4 : 2)) % 16 == 0 ? 1 : 0;
+    for (int j = 0; j < a.jobs(); ++j)
+        if (reinterpret_cast<uintptr_t>(a.job(j).y) & 15) p.y_tma = 0;
     p.err = a.err;
     return p;
 }

@@ -12,7 +12,8 @@ cudaError_t launch_tc_q4_gateup(const TcArgs& a, cudaStream_t s) {
     const Plan pl = plan_tiles(a, mt, true);
     Params p = make_params(a);
     p.y_tma = 0;    // a[T][I] f32 leaves by direct stores after the SwiGLU
-    dim3 grid((unsigned)mt, (unsigned)((a.T + pl.bn - 1) / pl.bn), (unsigned)pl.ks);
+    p.tiles_y = (int)((a.T + pl.bn - 1) / pl.bn);
+    dim3 grid((unsigned)mt, (unsigned)p.tiles_y, (unsigned)pl.ks);
     trace_plan("gate/up", 0, a, pl, (pl.bn >= 128 || pl.bn == 32) && pl.pair_ok, grid);
     return launch_q4_tmem<1>(a, p, pl, grid, s);
 }

@@ -115,6 +115,40 @@ cq_status cq_gemm_q4_noalloc(const void* X, int xt, int64_t T, int64_t K,
                              void* Y, int yt, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * z-batched Q4 GEMM: up to four weights of one shape in one launch.
+ *   for each job j < z:
+ *     Y[t][y_off_j + n] = sum_k X[t][x_off_j + k] * dequant(Wq_j, Ws_j)[n][k]
+ * The pages dispatch the tensors of one shape and codec that read one
+ * activation buffer as one z-batched launch (the qkv GEMM with z = 3, the
+ * gate/up GEMM with z = 2), each with its own activation and output offset:
+ * "cortiq-engine 0.8.3 src/gpu_metal/qi21.rs", struct PMm (x_off[4],
+ * y_off[4]) and Enc::gemm; "oxinfer 0.0.5 src/metal.rs", fn matmul_mma (jobs
+ * sharing one guarded X).
+ *
+ * X: fp16/bf16 rows of pitch ldx elements ([T][ldx]).  jobs: HOST array of
+ * z descriptors (the library reads it during the call only).  Each job's
+ * Wq [N][K/2], Ws fp16 [N][K/32] as for cq_gemm_q4.  Y: f32 or bf16 rows of
+ * pitch ldy ([T][ldy]); job j overwrites columns y_off_j .. y_off_j + N - 1
+ * of every row and nothing else (the jobs' column ranges must not overlap).
+ * Shape rules: 1 <= z <= 4, T >= 1, N >= 1, K % 256 == 0, ldx % 8 == 0,
+ * x_off_j % 8 == 0, x_off_j + K <= ldx, y_off_j + N <= ldy; X, Y and every
+ * weight pointer 16-byte aligned.  Arithmetic: as cq_gemm_q4 on each job
+ * (T <= 32 the weight-streaming path, else tcgen05 behind one guard pass per
+ * distinct x_off).
+ * Workspace: cq_gemm_q4_batched_workspace_bytes(T, K, z) bytes.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    const uint8_t* Wq;     /* [N][K/2] packed nibbles (device) */
+    const uint16_t* Ws;    /* [N][K/32] fp16 block scales (device) */
+    int64_t x_off;         /* first activation column of this job */
+    int64_t y_off;         /* first output column of this job */
+} cq_q4_job;
+size_t cq_gemm_q4_batched_workspace_bytes(int64_t T, int64_t K, int z);
+cq_status cq_gemm_q4_batched(const void* X, int xt, int64_t T, int64_t K, int64_t ldx,
+                             const cq_q4_job* jobs, int z, int64_t N,
+                             void* Y, int yt, int64_t ldy, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Q8-row GEMM:  Y[T][N] = (X[T][K] . Wq[N][K]^T) * rs[N]
  *
  * X: fp16 or bf16 [T][K]; the int8 weights are converted exactly to the

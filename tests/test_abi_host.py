@@ -175,3 +175,21 @@ def test_ffn_validation(L):
     assert _ffn(L, wsb=need - 1) == 6
     assert _ffn(L, ws=FAKE + 16) == 6
     assert "decline" in cq.cq_last_error()
+
+
+def test_batched_validation(L):
+    J = cq.cq_q4_job * 4
+    good = J(*[cq.cq_q4_job(FAKE, FAKE, 0, 256 * j) for j in range(4)])
+    call = lambda jobs=good, z=3, X=FAKE, T=16, K=512, ldx=512, N=256, Y=FAKE, ldy=1024, ws=FAKE, wsb=1 << 30: \
+        L.cq_gemm_q4_batched(X, 1, T, K, ldx, ctypes.cast(jobs, ctypes.c_void_p), z, N, Y, 2, ldy, ws, wsb, None)
+    assert call(X=None) == 1 and call(jobs=None) == 1
+    assert call(z=0) == 10 and call(z=5) == 10
+    assert call(K=384) == 3 and call(ldx=500) == 3 and call(ldy=700) == 3
+    bad = J(cq.cq_q4_job(FAKE, FAKE, 4, 0), *[cq.cq_q4_job(FAKE, FAKE, 0, 0)] * 3)   # x_off not a multiple of 8
+    assert call(jobs=bad, z=1) == 3
+    bad = J(cq.cq_q4_job(FAKE, FAKE, 0, 900), *[cq.cq_q4_job(FAKE, FAKE, 0, 0)] * 3)  # y_off + N > ldy
+    assert call(jobs=bad, z=1) == 3
+    bad = J(cq.cq_q4_job(ODD, FAKE, 0, 0), *[cq.cq_q4_job(FAKE, FAKE, 0, 0)] * 3)
+    assert call(jobs=bad, z=1) == 4
+    assert L.cq_gemm_q4_batched_workspace_bytes(16, 512, 3) == 3 * (16 * 512 * 2 + 256)
+    assert call(wsb=3 * (16 * 512 * 2 + 256) - 1) == 6
