@@ -235,3 +235,21 @@ def ffn(X, gu_q, gu_s, d_q, d_s, I, want_a=False):
     _load().or_ffn(_p(X), _i(T), _i(H), _i(I), _p(gu_q), _p(gu_s), _p(d_q), _p(d_s), _p(Y), _p(S),
                    _p(A) if want_a else None)
     return (Y, S, A) if want_a else (Y, S)
+
+
+# ---- MoE routing from router logits ----------------------------------------
+
+def route(logits, topk, shared=False):
+    """(idx, w): top-k by logit (descending, lower index first on ties),
+    weights p_e / sum over the picked experts from an f64 softmax, rounded to
+    f32; with `shared` the last logit column is the shared expert's gate and
+    slot topk is expert E with weight sigmoid(gate).  logits [T][E (+1)] f32."""
+    lg = _c(logits, np.float32)
+    T, cols = lg.shape
+    E = cols - (1 if shared else 0)
+    assert 1 <= topk <= min(E, 64)
+    slots = topk + (1 if shared else 0)
+    idx = np.empty((T, slots), np.int32)
+    w = np.empty((T, slots), np.float32)
+    _load().or_route(_p(lg), _i(T), _i(E), _i(topk), ctypes.c_int(1 if shared else 0), _p(idx), _p(w))
+    return idx, w

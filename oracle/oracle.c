@@ -25,6 +25,10 @@
  *    weighted sum): same tests module, mma_moe_matches_cpu; SiLU as
  *    g/(1+exp(-g)) from the silu_half shader.  Expert-major grouping of the
  *    routed rows, token order inside an expert: same page, Backend::moe.
+ *  - Routing from router logits (top-k, lower index first on ties, weights
+ *    renormalised over the picked experts; the shared expert's sigmoid gate):
+ *    "cortiq-engine 0.8.44 src/clover.rs" (moe_route, the route closure) and
+ *    "cortiq-engine 0.8.41 src/gpu_metal/clover.rs", fn run_on.
  *  - Dense FFN chain (gate/up, SwiGLU, down for every token): "cortiq-engine
  *    0.8.3 src/gpu_metal/qi21.rs", fn blocks (gemm(TG, TU) -> swiglu ->
  *    gemm(TD)) and its module header.
@@ -35,7 +39,8 @@
  * Pins (tests marked "not gpu"): hand-built blocks for the dequantizers,
  * exact rational brute force and a library f64 matmul for the GEMM, closed
  * forms and invariants for the MoE chain and the layout, a one-hot closed
- * form, library matmuls and the one-expert MoE chain for the dense FFN.  No function here
+ * form, library matmuls and the one-expert MoE chain for the dense FFN,
+ * a stable library argsort and closed-form weights for the routing.  No function here
  * is left without a pin.
  */
 #include <math.h>
@@ -373,4 +378,51 @@ void or_ffn(const double* X, int64_t T, int64_t H, int64_t I,
     }
     free(wgu);
     free(wd);
+}
+
+/* ---- MoE routing from router logits ---- */
+
+/* Per token t with logits l[0..E) (f32; one more, l[E], the shared expert's
+ * gate logit when `shared`):
+ *   - the top-k experts by logit, descending, the lower index first on ties
+ *     (picked one at a time: the largest logit not yet picked, lowest index
+ *     among equals), which is the top-k by softmax probability since exp is
+ *     strictly increasing;
+ *   - p_e = exp(l_e - max l) / sum_e' exp(l_e' - max l) in f64, and
+ *     w_j = p_{e_j} / sum_{j'} p_{e_j'} over the picked experts, rounded to f32;
+ *   - with `shared`, slot topk is the shared expert (index E) with weight
+ *     1 / (1 + exp(-l[E])) (f64, rounded to f32).
+ * ("cortiq-engine 0.8.44 src/clover.rs": the coreset's top-k comment
+ * (descending, lower index first on ties), moe_route and the route closure
+ * (p[e] / wsum); "cortiq-engine 0.8.41 src/gpu_metal/clover.rs", fn run_on:
+ * the shared expert's slot appended after the routed ones with weight
+ * 1 / (1 + exp(-sg)).)  idx[T][topk + shared], w[T][topk + shared]. */
+void or_route(const float* logits, int64_t T, int64_t E, int64_t topk, int shared, int32_t* idx, float* w) {
+    const int64_t ld = E + (shared ? 1 : 0), slots = topk + (shared ? 1 : 0);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    for (int64_t t = 0; t < T; t++) {
+        const float* l = logits + t * ld;
+        double mx = -INFINITY;
+        for (int64_t e = 0; e < E; e++) if ((double)l[e] > mx) mx = (double)l[e];
+        double sum = 0.0;
+        for (int64_t e = 0; e < E; e++) sum += exp((double)l[e] - mx);
+        memset(taken, 0, (size_t)E);
+        double wsum = 0.0;
+        double p[64];
+        for (int64_t j = 0; j < topk; j++) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; e++)
+                if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;   /* strict: the lower index wins ties */
+            taken[best] = 1;
+            idx[t * slots + j] = (int32_t)best;
+            p[j] = exp((double)l[best] - mx) / sum;
+            wsum += p[j];
+        }
+        for (int64_t j = 0; j < topk; j++) w[t * slots + j] = (float)(p[j] / wsum);
+        if (shared) {
+            idx[t * slots + topk] = (int32_t)E;
+            w[t * slots + topk] = (float)(1.0 / (1.0 + exp(-(double)l[E])));
+        }
+    }
+    free(taken);
 }

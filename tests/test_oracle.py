@@ -502,3 +502,60 @@ def test_ffn_matches_library_matmuls():
     Yt = At @ wd.T
     assert np.allclose(A, At.numpy(), rtol=1e-12, atol=1e-13)
     assert np.all(np.abs(Y - Yt.numpy()) <= 1e-12 * S + 1e-15)
+
+
+# ---- routing from router logits ---------------------------------------------
+
+def test_route_equal_logits_take_the_lowest_indices_with_equal_weights():
+    idx, w = oracle.route(np.zeros((3, 16), np.float32), 5)
+    assert idx.tolist() == [[0, 1, 2, 3, 4]] * 3
+    assert np.all(w == np.float32(0.2))
+
+
+def test_route_order_matches_a_stable_library_argsort():
+    """The picked experts and their order are the first k of numpy's stable
+    argsort of -logits (ties: lower index first), including heavy ties."""
+    rng = np.random.default_rng(81)
+    lg = rng.integers(-3, 4, (50, 32)).astype(np.float32) * 0.5        # many equal logits
+    lg[10] = rng.standard_normal(32).astype(np.float32)
+    idx, _ = oracle.route(lg, 8)
+    ref = np.argsort(-lg, axis=1, kind="stable")[:, :8]
+    assert np.array_equal(idx, ref)
+
+
+def test_route_weights_closed_form():
+    """w_i / w_j = exp(l_i - l_j) for picked experts i, j, and the weights of a
+    row sum to 1 (to f32 rounding); two logits ln 3 apart give 3/4 and 1/4."""
+    lg = np.array([[0.0, np.log(3.0), -5.0, -6.0]], np.float32)
+    idx, w = oracle.route(lg, 2)
+    assert idx.tolist() == [[1, 0]]
+    e = np.exp(np.float64(lg[0, 1]) - np.float64(lg[0, 0]))
+    assert np.allclose(w[0], [e / (1 + e), 1 / (1 + e)], rtol=1e-7)
+    rng = np.random.default_rng(82)
+    lg = rng.standard_normal((20, 64)).astype(np.float32)
+    idx, w = oracle.route(lg, 8)
+    assert np.allclose(w.sum(axis=1), 1.0, rtol=4e-7)
+    for t in range(20):
+        l = lg[t, idx[t]].astype(np.float64)
+        assert np.allclose(w[t] / w[t, 0], np.exp(l - l[0]), rtol=1e-6)
+        assert np.all(np.diff(l) <= 0)
+
+
+def test_route_shared_expert_slot():
+    """The shared slot is expert E with weight 1 / (1 + exp(-gate)): 1/2 at
+    gate 0, 3/4 at gate ln 3; the routed slots ignore the gate column."""
+    lg = np.array([[1.0, 2.0, 0.5, 0.0], [1.0, 2.0, 0.5, np.log(3.0)]], np.float32)
+    idx, w = oracle.route(lg, 2, shared=True)
+    assert idx.tolist() == [[1, 0, 3], [1, 0, 3]]
+    assert w[0, 2] == np.float32(0.5) and abs(float(w[1, 2]) - 0.75) < 1e-7
+    idx2, w2 = oracle.route(lg[:, :3], 2)
+    assert np.array_equal(idx[:, :2], idx2) and np.array_equal(w[:, :2], w2)
+
+
+def test_route_agrees_with_the_input_recipe():
+    """The recipe's own routing of the MoE workload (synth.route_topk, written
+    separately from the oracle) picks the same experts with the same weights."""
+    m = synth.moe_case(4, T=8, H=256, I=256, E=128, topk=8)
+    idx, w = oracle.route(m["logits"], 8)
+    assert np.array_equal(idx, m["idx"])
+    assert np.allclose(w, m["w"], rtol=1e-6)

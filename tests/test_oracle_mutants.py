@@ -140,3 +140,43 @@ def test_ffn_mutant_fails_closed_form(name):
         so = os.path.join(tmp, f"{name}.so")
         subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", path, "-o", so, "-lm"])
         assert not _ffn_closed_form_passes(ctypes.CDLL(so)), f"mutant {name} slipped through"
+
+
+# ---- routing: mutants against the library argsort and the closed-form weights ----
+
+ROUTE_MUTANTS = {
+    "route_ties_prefer_higher_index": ("(best < 0 || l[e] > l[best])", "(best < 0 || l[e] >= l[best])"),
+    "route_no_renormalise": ("w[t * slots + j] = (float)(p[j] / wsum);", "w[t * slots + j] = (float)p[j];"),
+    "route_shared_sign": ("(1.0 / (1.0 + exp(-(double)l[E])))", "(1.0 / (1.0 + exp((double)l[E])))"),
+}
+
+
+def _route_pins_pass(lib):
+    rng = np.random.default_rng(83)
+    lg = np.ascontiguousarray(np.concatenate([rng.integers(-2, 3, (20, 16)).astype(np.float32) * 0.5,
+                                              np.full((20, 1), np.log(3.0), np.float32)], axis=1))
+    T, E, k = 20, 16, 4
+    idx = np.empty((T, k + 1), np.int32)
+    w = np.empty((T, k + 1), np.float32)
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)
+    lib.or_route(p(lg), ctypes.c_int64(T), ctypes.c_int64(E), ctypes.c_int64(k), ctypes.c_int(1), p(idx), p(w))
+    if not np.array_equal(idx[:, :k], np.argsort(-lg[:, :E], axis=1, kind="stable")[:, :k]):
+        return False
+    if not np.allclose(w[:, :k].sum(axis=1), 1.0, rtol=1e-6):
+        return False
+    return bool(np.all(np.abs(w[:, k] - 0.75) < 1e-7))
+
+
+@pytest.mark.parametrize("name", sorted(ROUTE_MUTANTS) + ["none"])
+def test_route_mutants_fail_pins(name):
+    src = open(SRC).read()
+    if name != "none":
+        old, new = ROUTE_MUTANTS[name]
+        assert src.count(old) == 1, name
+        src = src.replace(old, new)
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, f"{name}.c")
+        open(path, "w").write(src)
+        so = os.path.join(tmp, f"{name}.so")
+        subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", path, "-o", so, "-lm"])
+        assert _route_pins_pass(ctypes.CDLL(so)) == (name == "none")
