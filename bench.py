@@ -156,13 +156,40 @@ def _ffn_calls(cq, gu, dn, dev):
                  h2d=[X], d2h=[Y])]
 
 
+def _moe_routed_calls(cq, m, dev):
+    """The MoE block from its router logits: routing on the device (softmax,
+    top-8, renormalised weights), then the expert panels, as one step."""
+    import torch
+    from block_quantized_weight_02_gb300 import pack
+    T, H, I, E, topk = m["T"], m["H"], m["I"], m["E"], m["topk"]
+    X = _dev_x(m["x"], m["x_dtype"], dev)
+    lg = torch.from_numpy(np.ascontiguousarray(m["logits"], np.float32)).to(dev)
+    idx = torch.empty(T, topk, dtype=torch.int32, device=dev)
+    w = torch.empty(T, topk, dtype=torch.float32, device=dev)
+    guq = torch.from_numpy(pack.pack_q4(m["gu_codes"])).to(dev)
+    gus = _u16(m["gu_scales"], dev)
+    dq = torch.from_numpy(pack.pack_q4(m["d_codes"])).to(dev)
+    ds = _u16(m["d_scales"], dev)
+    Y = torch.empty(T, H, dtype=torch.float32, device=dev)
+    ws = torch.empty(cq.cq_moe_workspace_bytes(T, H, I, E, topk), dtype=torch.uint8, device=dev)
+    touched = len(np.unique(m["idx"]))
+    per_expert = (2 * I * H + H * I) * 9 // 16
+    flops = T * topk * (2.0 * H * 2 * I + 2.0 * I * H)
+
+    def fn():
+        cq.cq_moe_route(lg, topk, idx, w)
+        cq.cq_moe_panels(X, idx, w, guq, gus, dq, ds, Y, ws)
+    return [Call("route + moe panels", fn, flops, touched * per_expert, X.numel() * 2 + Y.numel() * 4 + lg.numel() * 4,
+                 6, h2d=[X, lg], d2h=[Y])], touched
+
+
 def _dtype_of(name, info):
     """The arithmetic each call of the workload runs in: the tcgen05 path (T > 32)
     multiplies guarded fp16 activations by fp16 weights; the weight-streaming path
     (T <= 32) multiplies the activations as given (bf16 here, fp16 for the smallest
     case) by the exact nibble - 8 and scales each 32-k block in f32; Q8-row is
     bf16 x bf16 (int8 exact); all accumulate in f32."""
-    if name == "moe_panels":
+    if name.startswith("moe"):
         return "q4:fp16xfp16->f32"
     if name == "smallest_q4":
         return "q4:fp16xfp16->f32"
@@ -196,6 +223,12 @@ def build_workload(name, dev, max_sets=16):
         make = lambda: _ffn_calls(cq, gu, dn, dev)
         info = {"T": 1024, "H": 3072, "I": 12288, "formats": ["q4"], "outputs": ["bf16"],
                 "chain": "gate/up + SwiGLU epilogue -> guard -> down"}
+    elif name == "moe_routed_from_logits":
+        m = synth.c4()
+        calls, touched = _moe_routed_calls(cq, m, dev)
+        info = {"T": 32, "H": 2048, "I": 768, "E": 128, "topk": 8, "touched_experts": touched, "outputs": ["f32"],
+                "routing": "on the device from the router logits"}
+        return (lambda: [calls]), info, 1
     elif name == "moe_panels":
         m = synth.c4()
         calls, touched = _moe_calls(cq, m, dev)
@@ -286,7 +319,7 @@ def whole_job_rate(units_per_step: float, world: int, ms_per_step_max: float) ->
     return units_per_step * world / (ms_per_step_max * 1e-3)
 
 
-PER_CONFIG = (["smallest_q4", "prefill_projection_4096", "denoiser_ffn_chain", "moe_panels"]
+PER_CONFIG = (["smallest_q4", "prefill_projection_4096", "denoiser_ffn_chain", "moe_panels", "moe_routed_from_logits"]
               + [f"sweep_{f}_T{t}" for f in ("q4", "q8") for t in (1, 8, 32, 128, 512, 2048)])
 
 TRAFFIC_MD = os.path.join(ROOT, "profiles", "traffic_per_call.md")

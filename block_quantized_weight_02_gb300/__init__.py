@@ -39,6 +39,7 @@ _SIGS = {
                            _c_p]),
     "cq_moe_panels": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p,
                                _c_p, _c_p, _c_p, _c_int, _c_p, _c_sz, _c_p]),
+    "cq_moe_route": (_c_int, [_c_p, _c_i64, _c_i64, _c_i64, _c_int, _c_p, _c_p, _c_p]),
     "cq_moe_layout": (_c_int, [_c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p]),
     "cq_dequant_q4": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p]),
     "cq_dequant_q8row": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p]),
@@ -189,6 +190,13 @@ def cq_ffn_q4(X, Wgu_q, Wgu_s, Wd_q, Wd_s, Y, ws, stream=None, raise_on_error=Tr
     if raise_on_error:
         _check(st)
     return st
+
+
+def cq_moe_route(logits, topk, idx, w, shared=False, stream=None):
+    """idx [T][topk + shared] int32, w [T][topk + shared] f32 from logits [T][E + shared] f32."""
+    T, cols = logits.shape
+    E = cols - (1 if shared else 0)
+    _check(lib().cq_moe_route(_ptr(logits), T, E, topk, 1 if shared else 0, _ptr(idx), _ptr(w), _stream(stream)))
 
 
 def cq_moe_layout(ws, T, H, I, E, topk, perm_out, seg_out, stream=None):

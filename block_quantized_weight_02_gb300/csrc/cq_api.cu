@@ -528,6 +528,22 @@ cq_status cq_ffn_q4(const void* X, int xt, int64_t T, int64_t H, int64_t I, cons
     return launched(launch_tc_q4(d, s), "FFN down GEMM");
 }
 
+cq_status cq_moe_route(const float* logits, int64_t T, int64_t E, int64_t topk, int shared, int32_t* idx, float* w,
+                       void* stream) {
+    g_msg[0] = 0;
+    if (!logits || !idx || !w) return fail(CQ_ERR_NULL, "cq_moe_route: null pointer");
+    if (T < 1 || T > (1LL << 31) - 1 || E < 1 || E > 1024 || topk < 1 || topk > 64 || topk > E ||
+        (shared != 0 && shared != 1))
+        return fail(CQ_ERR_SHAPE, "cq_moe_route: need T>=1, 1<=E<=1024, 1<=topk<=min(E,64), shared 0 or 1 "
+                    "(T=%lld E=%lld topk=%lld shared=%d)", (long long)T, (long long)E, (long long)topk, shared);
+    if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(idx) | reinterpret_cast<uintptr_t>(w)) & 3)
+        return fail(CQ_ERR_ALIGN, "cq_moe_route: pointers must be 4-byte aligned");
+    cq_status st;
+    if ((st = check_arch())) return st;
+    return launched(launch_route_logits(logits, T, E, topk, shared, idx, w, static_cast<cudaStream_t>(stream)),
+                    "MoE routing from logits");
+}
+
 cq_status cq_moe_layout(const void* ws, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk, int32_t* perm_out,
                         int32_t* seg_out, void* stream) {
     g_msg[0] = 0;

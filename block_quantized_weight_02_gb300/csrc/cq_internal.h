@@ -70,6 +70,9 @@ cudaError_t launch_moe_route_gather(const int32_t* idx, int64_t T, int64_t topk,
                                     int32_t* perm, int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status,
                                     int32_t* cnt, int ncnt, int* err, const void* x, int xt, int64_t H, uint16_t* xh,
                                     float* rsx, cudaStream_t s);
+// Routing from router logits [T][E (+1 with shared)] -> idx, w [T][topk (+1)].
+cudaError_t launch_route_logits(const float* logits, int64_t T, int64_t E, int64_t topk, int shared, int32_t* idx,
+                                float* w, cudaStream_t s);
 // f32 rows -> fp16 behind a per-row power-of-two guard, in the Q4 streaming
 // order (the down panels and the tcgen05 Q4 GEMM read it); status nullable.
 cudaError_t launch_a_half(const float* a, int64_t P, int64_t I, uint16_t* ah, float* rsa, const int32_t* status,

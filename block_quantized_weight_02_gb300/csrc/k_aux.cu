@@ -395,6 +395,87 @@ cudaError_t launch_moe_route_gather(const int32_t* idx, int64_t T, int64_t topk,
                       reinterpret_cast<__half*>(xh), rsx);
 }
 
+// ---- MoE routing from router logits ---------------------------------------
+// One warp per token ("cortiq-engine 0.8.44 src/clover.rs": moe_route and the
+// route closure; the shared expert's slot from "cortiq-engine 0.8.41
+// src/gpu_metal/clover.rs", fn run_on).  The top-k experts are picked one at a
+// time by a warp-wide argmax over the f32 logits not yet taken (ties: the lower
+// index), which is the top-k by softmax probability because exp is increasing;
+// lane l holds the logits l, l + 32, ... and a bit per held logit marks it
+// taken.  Weights: p_e = exp(l_e - max) / sum exp(l - max) in f64, w_j = p_j /
+// sum of the picked p_j (summed in pick order), rounded to f32.  With `shared`,
+// slot topk is expert E with weight 1 / (1 + exp(-l[E])).
+__global__ void __launch_bounds__(256) k_route_logits(const float* __restrict__ logits, int T, int E, int topk,
+                                                      int shared, int32_t* __restrict__ idx, float* __restrict__ w) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int t = (int)blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const int ld = E + (shared ? 1 : 0), slots = topk + (shared ? 1 : 0);
+    const float* l = logits + (int64_t)t * ld;
+    const int per = (E + 31) / 32;
+    float mxf = -INFINITY;
+    for (int i = 0; i < per; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) mxf = fmaxf(mxf, l[e]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mxf = fmaxf(mxf, __shfl_xor_sync(0xffffffffu, mxf, o));
+    const double mx = (double)mxf;
+    double sum = 0.0;
+    for (int i = 0; i < per; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) sum += exp((double)l[e] - mx);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    uint32_t taken = 0;
+    double wsum = 0.0, p0 = 0.0, p1 = 0.0;   // lane j keeps p of slots j and 32 + j
+    for (int j = 0; j < topk; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int i = 0; i < per; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u)) {
+                const float v = l[e];
+                if (v > bv || (v == bv && e < bi)) {
+                    bv = v;
+                    bi = e;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        const double pv = exp((double)bv - mx) / sum;
+        wsum += pv;
+        if (lane == (j & 31)) {
+            if (j < 32) p0 = pv;
+            else p1 = pv;
+        }
+        if (lane == 0) idx[(int64_t)t * slots + j] = bi;
+    }
+    if (lane < topk) w[(int64_t)t * slots + lane] = (float)(p0 / wsum);
+    if (lane + 32 < topk) w[(int64_t)t * slots + lane + 32] = (float)(p1 / wsum);
+    if (shared && lane == 0) {
+        idx[(int64_t)t * slots + topk] = E;
+        w[(int64_t)t * slots + topk] = (float)(1.0 / (1.0 + exp(-(double)l[E])));
+    }
+}
+
+cudaError_t launch_route_logits(const float* logits, int64_t T, int64_t E, int64_t topk, int shared, int32_t* idx,
+                                float* w, cudaStream_t s) {
+    return launch_pdl(k_route_logits, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, s, logits, (int)T, (int)E,
+                      (int)topk, shared, idx, w);
+}
+
 // SwiGLU activations (f32, grouped order) -> fp16 behind the same
 // power-of-two guard as the inputs, in the weight-streaming order ("oxinfer 0.0.5 src/metal.rs",
 // silu_half: scaled half rows and an inverse scale per row).

@@ -215,6 +215,29 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E,
                         const uint8_t* Wd_q, const uint16_t* Wd_s,
                         void* Y, int yt, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Routing on the device, from the router logits, and the shared expert:
+ *   idx[t][0..topk) = the topk experts with the largest logits, descending,
+ *                     the lower index first on ties;
+ *   w[t][j]         = p_e / sum of p over the picked experts, where
+ *                     p = softmax of the row's E logits (f64, rounded to f32);
+ *   shared = 1:       logits rows hold E + 1 values, the last one the shared
+ *                     expert's gate g; slot topk is expert E with weight
+ *                     1 / (1 + exp(-g)).
+ * ("cortiq-engine 0.8.44 src/clover.rs": the coreset's top-k rule and the
+ * route closure, p[e] / wsum; "cortiq-engine 0.8.41 src/gpu_metal/clover.rs",
+ * fn run_on: the shared expert appended as one more slot of every row with
+ * its sigmoid gate weight.)
+ * logits: f32 [T][E + shared].  idx: int32 [T][topk + shared], w: f32
+ * [T][topk + shared], written on `stream`; cq_moe_panels then takes them as
+ * its idx and w with topk + shared slots, the shared expert stacked as
+ * expert E of its weight arrays (E + 1 experts; every expert of one shape).
+ * Shape rules: T >= 1, 1 <= E <= 1024, 1 <= topk <= min(E, 64), shared 0/1;
+ * pointers 4-byte aligned.
+ * ------------------------------------------------------------------------- */
+cq_status cq_moe_route(const float* logits, int64_t T, int64_t E, int64_t topk, int shared,
+                       int32_t* idx, float* w, void* stream);
+
 /* Copies the routing layout of the last cq_moe_panels call on `ws` into
  * perm_out[T*topk] (pair ids t*topk + j in grouped order) and
  * seg_out[E+1] (exclusive prefix of per-expert pair counts), both device

@@ -193,3 +193,10 @@ def test_batched_validation(L):
     assert call(jobs=bad, z=1) == 4
     assert L.cq_gemm_q4_batched_workspace_bytes(16, 512, 3) == 3 * (16 * 512 * 2 + 256)
     assert call(wsb=3 * (16 * 512 * 2 + 256) - 1) == 6
+
+
+def test_route_validation(L):
+    r = lambda T=4, E=16, k=4, sh=0, lg=FAKE, idx=FAKE, w=FAKE: L.cq_moe_route(lg, T, E, k, sh, idx, w, None)
+    assert r(lg=None) == 1 and r(w=None) == 1
+    assert r(T=0) == 3 and r(E=1025) == 3 and r(k=0) == 3 and r(k=17) == 3 and r(E=100, k=65) == 3 and r(sh=2) == 3
+    assert r(lg=FAKE + 2) == 4
