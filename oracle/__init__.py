@@ -253,3 +253,49 @@ def route(logits, topk, shared=False):
     w = np.empty((T, slots), np.float32)
     _load().or_route(_p(lg), _i(T), _i(E), _i(topk), ctypes.c_int(1 if shared else 0), _p(idx), _p(w))
     return idx, w
+
+
+# ---- format variants -------------------------------------------------------
+
+def dequant_q8b(q, s):
+    """Q8 per 32-k block: W = f32(q) * s[n][k/32] (f32 scales)."""
+    q = _c(q, np.int8)
+    s = _c(s, np.float32)
+    N, K = q.shape
+    assert s.shape == (N, K // 32)
+    out = np.empty((N, K), np.float32)
+    _load().or_dequant_q8b(_p(q), _p(s), _i(N), _i(K), _p(out))
+    return out
+
+
+def dequant_q4a(wq, ws, off, gk, N, K):
+    """Affine Q4: (nibble - 8) * d + bf16 offset of the group of gk blocks."""
+    wq = _c(wq, np.uint8)
+    ws = _c(ws, np.uint16)
+    off = _c(off, np.uint16)
+    assert off.size == N * (K // 32 // gk)
+    out = np.empty((N, K), np.float32)
+    _load().or_dequant_q4a(_p(wq), _p(ws), _p(off), _i(gk), _i(N), _i(K), _p(out))
+    return out
+
+
+def gemm_q8b(q, s, X):
+    return gemm(dequant_q8b(q, s), X)
+
+
+def gemm_q4a(wq, ws, off, gk, N, K, X):
+    return gemm(dequant_q4a(wq, ws, off, gk, N, K), X)
+
+
+def gemm_q8_2f(q, rs, col, X):
+    """(Y, S) f64: Y[t][n] = rs[n] * sum_k q[n][k] col[k] X[t][k]."""
+    q = _c(q, np.int8)
+    rs = _c(rs, np.float32)
+    col = _c(col, np.float32)
+    X = _c(X, np.float64)
+    N, K = q.shape
+    T = X.shape[0]
+    Y = np.empty((T, N), np.float64)
+    S = np.empty((T, N), np.float64)
+    _load().or_gemm_q8_2f(_p(q), _p(rs), _p(col), _p(X), _i(T), _i(N), _i(K), _p(Y), _p(S))
+    return Y, S

@@ -25,6 +25,9 @@
  *    weighted sum): same tests module, mma_moe_matches_cpu; SiLU as
  *    g/(1+exp(-g)) from the silu_half shader.  Expert-major grouping of the
  *    routed rows, token order inside an expert: same page, Backend::moe.
+ *  - Format variants: Q8 per 32-k block and affine Q4 from the same
+ *    "Dequantizers" section (load(Q8W ...), load(Q4A ...)); q8_2f from
+ *    "cortiq-engine 0.8.3 src/gpu_metal/qi21.rs" (module header, fn build_block).
  *  - Routing from router logits (top-k, lower index first on ties, weights
  *    renormalised over the picked experts; the shared expert's sigmoid gate):
  *    "cortiq-engine 0.8.44 src/clover.rs" (moe_route, the route closure) and
@@ -40,7 +43,9 @@
  * exact rational brute force and a library f64 matmul for the GEMM, closed
  * forms and invariants for the MoE chain and the layout, a one-hot closed
  * form, library matmuls and the one-expert MoE chain for the dense FFN,
- * a stable library argsort and closed-form weights for the routing.  No function here
+ * a stable library argsort and closed-form weights for the routing,
+ * reductions to the pinned formats, library f32 arithmetic and exact
+ * rationals for the format variants.  No function here
  * is left without a pin.
  */
 #include <math.h>
@@ -425,4 +430,56 @@ void or_route(const float* logits, int64_t T, int64_t E, int64_t topk, int share
         }
     }
     free(taken);
+}
+
+/* ---- format variants ---- */
+
+/* Q8 per 32-k block ("oxinfer 0.0.5 src/metal.rs", Dequantizers, struct Q8W
+ * and load(Q8W ...)): int8 q[N][K], f32 scale s[N][K/32];
+ * W[n][k] = f32(q[n][k]) * s[n][k/32] (one f32 rounding). */
+void or_dequant_q8b(const int8_t* q, const float* s, int64_t N, int64_t K, float* w) {
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++) w[n * K + k] = (float)q[n * K + k] * s[n * (K / 32) + k / 32];
+}
+
+/* Affine Q4 ("oxinfer 0.0.5 src/metal.rs", Dequantizers, struct Q4A and
+ * load(Q4A ...)): the Q4 split-plane element (nibble - 8) * d (exact in f32)
+ * plus the bf16 offset of its group of gk blocks, off[n][b / gk] (gpr = K/32/gk
+ * offsets per row), added in f32 (one rounding). */
+static float or_bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+void or_dequant_q4a(const uint8_t* wq, const uint16_t* ws, const uint16_t* off, int64_t gk, int64_t N, int64_t K,
+                    float* w) {
+    const int64_t gpr = K / 32 / gk;
+    or_dequant_q4(wq, ws, N, K, w);
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++) w[n * K + k] = w[n * K + k] + or_bf16_to_f32(off[n * gpr + (k / 32) / gk]);
+}
+
+/* q8_2f ("cortiq-engine 0.8.3 src/gpu_metal/qi21.rs", module header: int8
+ * weights staged times the column field, the row scale in the epilogue; the
+ * blob layout q[rows][cols], rs[rows], col[cols] from fn build_block):
+ *   Y[t][n] = rs[n] * sum_k q[n][k] * col[k] * X[t][k]   (f64, k ascending),
+ *   S[t][n] = |rs[n]| * sum_k |q[n][k] * col[k] * X[t][k]|.
+ * rs and col as f32 (the stored f16 values widened exactly). */
+void or_gemm_q8_2f(const int8_t* q, const float* rs, const float* col, const double* X, int64_t T, int64_t N,
+                   int64_t K, double* Y, double* S) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t t = 0; t < T; t++)
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0, abs_acc = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double p = (double)q[n * K + k] * (double)col[k] * X[t * K + k];
+                acc += p;
+                abs_acc += fabs(p);
+            }
+            Y[t * N + n] = acc * (double)rs[n];
+            S[t * N + n] = abs_acc * fabs((double)rs[n]);
+        }
 }

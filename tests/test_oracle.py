@@ -559,3 +559,76 @@ def test_route_agrees_with_the_input_recipe():
     idx, w = oracle.route(m["logits"], 8)
     assert np.array_equal(idx, m["idx"])
     assert np.allclose(w, m["w"], rtol=1e-6)
+
+
+# ---- format variants ---------------------------------------------------------
+
+def test_q8b_dequant_is_one_f32_product_per_element():
+    """W = RNE_f32(q * s): q * s is exact in f64 (8 + 24 bits), numpy's cast
+    to f32 rounds it once; equal to the Q8-row dequantisation when every block
+    scale of a row is that row's scale."""
+    rng = np.random.default_rng(91)
+    q = rng.integers(-128, 128, (7, 96)).astype(np.int8)
+    s = rng.uniform(1e-3, 1e-2, (7, 3)).astype(np.float32) * np.where(rng.random((7, 3)) < 0.3, -1, 1).astype(np.float32)
+    s[0, 0] = 0.0
+    W = oracle.dequant_q8b(q, s)
+    ref = (q.astype(np.float64) * np.repeat(s.astype(np.float64), 32, axis=1)).astype(np.float32)
+    assert np.array_equal(W.view(np.uint32), ref.view(np.uint32))
+    rs = rng.uniform(1e-3, 1e-2, 7).astype(np.float32)
+    assert np.array_equal(oracle.dequant_q8b(q, np.repeat(rs[:, None], 3, axis=1)), oracle.dequant_q8row(q, rs))
+
+
+def test_q4a_dequant_adds_the_group_offset_once():
+    """Offsets -0 reproduce the plain Q4 dequantisation bit for bit (adding
+    -0 is the IEEE identity, zero signs included; +0 would turn -0 into +0); with
+    distinct offsets per group of gk = 2 blocks every element is the f32 sum
+    of the exact Q4 value and its group's bf16 offset (numpy f32 addition)."""
+    rng = np.random.default_rng(92)
+    N, K, gk = 5, 256, 2
+    codes, ws = synth.draw_q4(rng, N, K, signed=True)
+    wq = oracle.pack_q4(codes)
+    zero = np.full((N, K // 32 // gk), 0x8000, np.uint16)
+    assert np.array_equal(oracle.dequant_q4a(wq, ws, zero, gk, N, K).view(np.uint32),
+                          oracle.dequant_q4(wq, ws, N, K).view(np.uint32))
+    off = synth.f32_to_bf16_bits(rng.uniform(-0.1, 0.1, (N, K // 32 // gk)).astype(np.float32))
+    W = oracle.dequant_q4a(wq, ws, off, gk, N, K)
+    base = (codes.astype(np.float32) - 8) * np.repeat(ws.view(np.float16).astype(np.float32), 32, axis=1)
+    m = np.repeat(synth.bf16_bits_to_f32(off), 32 * gk, axis=1)
+    assert np.array_equal(W.view(np.uint32), (base + m).astype(np.float32).view(np.uint32))
+
+
+@pytest.mark.parametrize("T,N,K", [(1, 2, 32), (3, 5, 64)])
+def test_q8_2f_vs_exact_rationals(T, N, K):
+    rng = np.random.default_rng(93 + K)
+    q = rng.integers(-128, 128, (N, K)).astype(np.int8)
+    rs = rng.uniform(1e-3, 1e-2, N).astype(np.float16).astype(np.float32)
+    col = rng.uniform(0.5, 2.0, K).astype(np.float16).astype(np.float32)
+    X = oracle.x_to_f64(synth.draw_x(rng, T, K), "bf16")
+    Y, S = oracle.gemm_q8_2f(q, rs, col, X)
+    for t in range(T):
+        for n in range(N):
+            exact = Fraction(float(rs[n])) * sum(Fraction(int(q[n, k])) * Fraction(float(col[k])) * Fraction(X[t, k])
+                                                 for k in range(K))
+            assert abs(Fraction(Y[t, n]) - exact) <= Fraction(2 ** -50) * Fraction(S[t, n])
+
+
+def test_q8_2f_with_unit_column_field_is_q8_row():
+    rng = np.random.default_rng(94)
+    q, rs = synth.draw_q8row(rng, 40, 128)
+    X = oracle.x_to_f64(synth.draw_x(rng, 6, 128), "bf16")
+    Y, S = oracle.gemm_q8_2f(q, rs, np.ones(128, np.float32), X)
+    Yr, Sr = oracle.gemm_q8row(q, rs, X)
+    assert np.array_equal(Y, Yr) and np.array_equal(S, Sr)
+
+
+def test_q8_2f_column_field_scales_activation_columns():
+    """Doubling col[k] for one k equals doubling X[:, k] (power of two: exact)."""
+    rng = np.random.default_rng(95)
+    q, rs = synth.draw_q8row(rng, 16, 64)
+    col = rng.uniform(0.5, 2.0, 64).astype(np.float16).astype(np.float32)
+    X = oracle.x_to_f64(synth.draw_x(rng, 3, 64), "bf16")
+    col2 = col.copy()
+    col2[17] *= 2
+    X2 = X.copy()
+    X2[:, 17] *= 2
+    assert np.array_equal(oracle.gemm_q8_2f(q, rs, col2, X)[0], oracle.gemm_q8_2f(q, rs, col, X2)[0])

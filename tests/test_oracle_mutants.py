@@ -180,3 +180,60 @@ def test_route_mutants_fail_pins(name):
         so = os.path.join(tmp, f"{name}.so")
         subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", path, "-o", so, "-lm"])
         assert _route_pins_pass(ctypes.CDLL(so)) == (name == "none")
+
+
+# ---- format variants: mutants against their pins ----------------------------
+
+FORMAT_MUTANTS = {
+    "q8b_scale_per_16": ("s[n * (K / 32) + k / 32]", "s[n * (K / 32) + k / 16 % (K / 32)]"),
+    "q4a_offset_per_block": ("off[n * gpr + (k / 32) / gk]", "off[n * gpr + (k / 32) % gpr]"),
+    "q8_2f_col_by_row": ("(double)col[k] * X[t * K + k]", "(double)col[n % K] * X[t * K + k]"),
+}
+
+
+def _format_pins_pass(lib):
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)
+    i64 = ctypes.c_int64
+    rng = np.random.default_rng(97)
+    # Q8 per 32: one f32 rounding of q * s[n][k/32]
+    q = rng.integers(-128, 128, (4, 128)).astype(np.int8)
+    s = rng.uniform(1e-3, 1e-2, (4, 4)).astype(np.float32)
+    w = np.empty((4, 128), np.float32)
+    lib.or_dequant_q8b(p(q), p(s), i64(4), i64(128), p(w))
+    if not np.array_equal(w, (q.astype(np.float64) * np.repeat(s.astype(np.float64), 32, axis=1)).astype(np.float32)):
+        return False
+    # affine Q4, gk = 2: (nibble - 8) * 1 + offset of the group
+    codes = rng.integers(0, 16, (3, 256)).astype(np.uint8)
+    wq = (codes.reshape(3, -1, 2, 16)[:, :, 0, :] | (codes.reshape(3, -1, 2, 16)[:, :, 1, :] << 4)).reshape(3, -1).astype(np.uint8)
+    ws = np.full((3, 8), 0x3C00, np.uint16)
+    offv = rng.integers(-8, 8, (3, 4)).astype(np.float32) * 0.125
+    off = np.ascontiguousarray((offv.view(np.uint32) >> 16).astype(np.uint16))
+    w = np.empty((3, 256), np.float32)
+    lib.or_dequant_q4a(p(wq), p(ws), p(off), i64(2), i64(3), i64(256), p(w))
+    if not np.array_equal(w, (codes.astype(np.float32) - 8) + np.repeat(offv, 64, axis=1)):
+        return False
+    # q8_2f: unit activations pick one column: Y = rs * q[n][k] * col[k]
+    q = rng.integers(-128, 128, (6, 64)).astype(np.int8)
+    rs = np.full(6, 0.5, np.float32)
+    col = rng.integers(1, 8, 64).astype(np.float32)
+    X = np.zeros((2, 64))
+    X[0, 5] = X[1, 40] = 1.0
+    Y = np.empty((2, 6))
+    S = np.empty((2, 6))
+    lib.or_gemm_q8_2f(p(q), p(rs), p(col), p(X), i64(2), i64(6), i64(64), p(Y), p(S))
+    return np.array_equal(Y[0], 0.5 * q[:, 5] * col[5]) and np.array_equal(Y[1], 0.5 * q[:, 40] * col[40])
+
+
+@pytest.mark.parametrize("name", sorted(FORMAT_MUTANTS) + ["none"])
+def test_format_mutants_fail_pins(name):
+    src = open(SRC).read()
+    if name != "none":
+        old, new = FORMAT_MUTANTS[name]
+        assert src.count(old) == 1, name
+        src = src.replace(old, new)
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, f"{name}.c")
+        open(path, "w").write(src)
+        so = os.path.join(tmp, f"{name}.so")
+        subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", path, "-o", so, "-lm"])
+        assert _format_pins_pass(ctypes.CDLL(so)) == (name == "none")
