@@ -344,7 +344,7 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E, 
     cq_status st;
     if ((st = check_x(xt)) || (st = check_y(yt))) return st;
     if (T < 1 || topk < 1 || topk > 64 || E < 1 || E > 1024 || T * topk > 65536 || H < 256 || H % 256 || I < 256 ||
-        I % 256)
+        I % 256 || H > 16384)
         return fail(CQ_ERR_SHAPE, "cq_moe_panels: shape rules broken (T=%lld H=%lld I=%lld E=%lld topk=%lld)",
                     (long long)T, (long long)H, (long long)I, (long long)E, (long long)topk);
     if (!aligned16(X) || !aligned16(idx) || !aligned16(w) || !aligned16(Wgu_q) || !aligned16(Wgu_s) ||

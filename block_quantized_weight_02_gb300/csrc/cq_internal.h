@@ -70,6 +70,13 @@ cudaError_t launch_moe_route_gather(const int32_t* idx, int64_t T, int64_t topk,
                                     int32_t* perm, int32_t* inv, int32_t* act, int32_t* n_act, int32_t* status,
                                     int32_t* cnt, int ncnt, int* err, const void* x, int xt, int64_t H, uint16_t* xh,
                                     float* rsx, cudaStream_t s);
+// Activations times the column field col[K] (nullable: none) -> fp16 behind the
+// per-row guard, in k order (q8_2f and the Q8 per-32-block tcgen05 path).
+cudaError_t launch_x_col_half(const void* x, int xt, const float* col, int64_t T, int64_t K, uint16_t* xh, float* rsx,
+                              cudaStream_t s);
+// Affine Q4 offset term: xs[T][G] group sums of X, add[T][N] = off . xs^T (G = K/32/gk <= 512).
+cudaError_t launch_offset_term(const void* x, int xt, int64_t T, int64_t K, const uint16_t* off, int gk, int64_t N,
+                               float* xs, float* add, cudaStream_t s);
 // Routing from router logits [T][E (+1 with shared)] -> idx, w [T][topk (+1)].
 cudaError_t launch_route_logits(const float* logits, int64_t T, int64_t E, int64_t topk, int shared, int32_t* idx,
                                 float* w, cudaStream_t s);

@@ -395,6 +395,110 @@ cudaError_t launch_moe_route_gather(const int32_t* idx, int64_t T, int64_t topk,
                       reinterpret_cast<__half*>(xh), rsx);
 }
 
+// ---- format variants: activation pre-passes --------------------------------
+// Activations times an optional column field (q8_2f: "cortiq-engine 0.8.3
+// src/gpu_metal/qi21.rs", module header: int8 staged times the column field),
+// to fp16 behind the same per-row power-of-two guard, in k order (the int8
+// decoders produce k order).  One CTA of 256 threads per row, K % 8 == 0.
+template <typename T>
+__global__ void __launch_bounds__(256) k_x_col_half(const T* __restrict__ x, const float* __restrict__ col, int64_t K,
+                                                    __half* __restrict__ xh, float* __restrict__ rsx) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ float red[8];
+    const int64_t row = blockIdx.x;
+    const uint4* src = reinterpret_cast<const uint4*>(x + row * K);
+    const int64_t n8 = K / 8;
+    float m = 0.f;
+    for (int64_t i = threadIdx.x; i < n8; i += 256) {
+        const uint4 u = src[i];
+        const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(to_f32<T>(e[j]) * (col ? col[8 * i + j] : 1.f)));
+    }
+    m = block_max_256(m, red);
+    const int sh = guard_shift(m);
+    const float sc = pow2f(sh);
+    uint4* dst = reinterpret_cast<uint4*>(xh + row * K);
+    for (int64_t i = threadIdx.x; i < n8; i += 256) {
+        const uint4 u = src[i];
+        const T* e = reinterpret_cast<const T*>(&u);
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = to_f32<T>(e[j]) * (col ? col[8 * i + j] : 1.f) * sc;
+        dst[i] = make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
+    }
+    if (threadIdx.x == 0) rsx[row] = pow2f(-sh);
+}
+
+cudaError_t launch_x_col_half(const void* x, int xt, const float* col, int64_t T, int64_t K, uint16_t* xh, float* rsx,
+                              cudaStream_t s) {
+    if (xt == CQ_BF16)
+        return launch_pdl(k_x_col_half<__nv_bfloat16>, dim3((unsigned)T), dim3(256), 0, s,
+                          reinterpret_cast<const __nv_bfloat16*>(x), col, K, reinterpret_cast<__half*>(xh), rsx);
+    return launch_pdl(k_x_col_half<__half>, dim3((unsigned)T), dim3(256), 0, s, reinterpret_cast<const __half*>(x), col,
+                      K, reinterpret_cast<__half*>(xh), rsx);
+}
+
+// Affine Q4 ("oxinfer 0.0.5 src/metal.rs", Dequantizers, load(Q4A ...)): every
+// element of group g (gk blocks of 32) of row n carries the offset m[n][g], so
+// the product with X has the term sum_g m[n][g] * xs[t][g], xs[t][g] the sum of
+// X[t] over the group.  These two kernels form that term in f32; the Q4 GEMM's
+// epilogue adds it before its final rounding.
+// xs[t][g]: one warp per (t, g), f32 sum of the group's 32 gk activations.
+template <typename T>
+__global__ void __launch_bounds__(256) k_group_sums(const T* __restrict__ x, int64_t Tn, int64_t K, int gk,
+                                                    float* __restrict__ xs) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t G = K / 32 / gk;
+    const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (wid >= Tn * G) return;
+    const int64_t t = wid / G, g = wid % G;
+    const T* src = x + t * K + g * 32 * gk;
+    float s = 0.f;
+    for (int i = lane; i < 32 * gk; i += 32) s += to_f32<T>(src[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) xs[wid] = s;
+}
+
+// add[t][n] = sum_g m[n][g] * xs[t][g]: a CTA of 128 threads takes 128 rows n
+// and 8 tokens; xs of those tokens is staged in shared memory (G <= 512).
+__global__ void __launch_bounds__(128) k_offset_term(const uint16_t* __restrict__ off, const float* __restrict__ xs,
+                                                     int64_t Tn, int64_t N, int G, float* __restrict__ add) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ float sx[8 * 512];
+    const int64_t t0 = (int64_t)blockIdx.y * 8;
+    const int nt = Tn - t0 < 8 ? (int)(Tn - t0) : 8;
+    for (int i = threadIdx.x; i < nt * G; i += 128) sx[i] = xs[t0 * G + i];
+    __syncthreads();
+    const int64_t n = (int64_t)blockIdx.x * 128 + threadIdx.x;
+    if (n >= N) return;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int g = 0; g < G; ++g) {
+        const float m = __uint_as_float((uint32_t)off[n * G + g] << 16);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = fmaf(m, sx[u * G + g], acc[u]);
+    }
+    for (int u = 0; u < nt; ++u) add[(t0 + u) * N + n] = acc[u];
+}
+
+cudaError_t launch_offset_term(const void* x, int xt, int64_t T, int64_t K, const uint16_t* off, int gk, int64_t N,
+                               float* xs, float* add, cudaStream_t s) {
+    const int64_t G = K / 32 / gk;
+    const unsigned gs = (unsigned)((T * G + 7) / 8);
+    cudaError_t e = xt == CQ_BF16
+        ? launch_pdl(k_group_sums<__nv_bfloat16>, dim3(gs), dim3(256), 0, s, reinterpret_cast<const __nv_bfloat16*>(x),
+                     T, K, gk, xs)
+        : launch_pdl(k_group_sums<__half>, dim3(gs), dim3(256), 0, s, reinterpret_cast<const __half*>(x), T, K, gk, xs);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_offset_term, dim3((unsigned)((N + 127) / 128), (unsigned)((T + 7) / 8)), dim3(128), 0, s, off,
+                      (const float*)xs, T, N, (int)G, add);
+}
+
 // ---- MoE routing from router logits ---------------------------------------
 // One warp per token ("cortiq-engine 0.8.44 src/clover.rs": moe_route and the
 // route closure; the shared expert's slot from "cortiq-engine 0.8.41
@@ -402,9 +506,11 @@ cudaError_t launch_moe_route_gather(const int32_t* idx, int64_t T, int64_t topk,
 // time by a warp-wide argmax over the f32 logits not yet taken (ties: the lower
 // index), which is the top-k by softmax probability because exp is increasing;
 // lane l holds the logits l, l + 32, ... and a bit per held logit marks it
-// taken.  Weights: p_e = exp(l_e - max) / sum exp(l - max) in f64, w_j = p_j /
-// sum of the picked p_j (summed in pick order), rounded to f32.  With `shared`,
-// slot topk is expert E with weight 1 / (1 + exp(-l[E])).
+// taken.  Weights: w_j = exp(l_j - max) / sum over the picked experts of
+// exp(l - max), in f32: the softmax's own denominator cancels in the
+// renormalisation (p_e = exp(l_e - max) / sum_e' ..., w_j = p_j / sum p), so it
+// is not formed.  With `shared`, slot topk is expert E with weight
+// 1 / (1 + exp(-l[E])).
 __global__ void __launch_bounds__(256) k_route_logits(const float* __restrict__ logits, int T, int E, int topk,
                                                       int shared, int32_t* __restrict__ idx, float* __restrict__ w) {
     pdl_launch_dependents();
@@ -414,23 +520,8 @@ __global__ void __launch_bounds__(256) k_route_logits(const float* __restrict__ 
     const int ld = E + (shared ? 1 : 0), slots = topk + (shared ? 1 : 0);
     const float* l = logits + (int64_t)t * ld;
     const int per = (E + 31) / 32;
-    float mxf = -INFINITY;
-    for (int i = 0; i < per; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) mxf = fmaxf(mxf, l[e]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mxf = fmaxf(mxf, __shfl_xor_sync(0xffffffffu, mxf, o));
-    const double mx = (double)mxf;
-    double sum = 0.0;
-    for (int i = 0; i < per; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) sum += exp((double)l[e] - mx);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     uint32_t taken = 0;
-    double wsum = 0.0, p0 = 0.0, p1 = 0.0;   // lane j keeps p of slots j and 32 + j
+    float mx = 0.f, wsum = 0.f, e0 = 0.f, e1 = 0.f;   // lane j keeps exp(l - max) of slots j and 32 + j
     for (int j = 0; j < topk; ++j) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
@@ -454,19 +545,20 @@ __global__ void __launch_bounds__(256) k_route_logits(const float* __restrict__ 
             }
         }
         if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        const double pv = exp((double)bv - mx) / sum;
-        wsum += pv;
+        if (j == 0) mx = bv;                 // the first pick is the row's largest logit
+        const float ev = expf(bv - mx);
+        wsum += ev;
         if (lane == (j & 31)) {
-            if (j < 32) p0 = pv;
-            else p1 = pv;
+            if (j < 32) e0 = ev;
+            else e1 = ev;
         }
         if (lane == 0) idx[(int64_t)t * slots + j] = bi;
     }
-    if (lane < topk) w[(int64_t)t * slots + lane] = (float)(p0 / wsum);
-    if (lane + 32 < topk) w[(int64_t)t * slots + lane + 32] = (float)(p1 / wsum);
+    if (lane < topk) w[(int64_t)t * slots + lane] = e0 / wsum;
+    if (lane + 32 < topk) w[(int64_t)t * slots + lane + 32] = e1 / wsum;
     if (shared && lane == 0) {
         idx[(int64_t)t * slots + topk] = E;
-        w[(int64_t)t * slots + topk] = (float)(1.0 / (1.0 + exp(-(double)l[E])));
+        w[(int64_t)t * slots + topk] = 1.0f / (1.0f + expf(-l[E]));
     }
 }
 

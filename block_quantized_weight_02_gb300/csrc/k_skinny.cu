@@ -634,79 +634,88 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
               asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
             }
           }
-          if (MODE == DOWN) {
-              // The weighted combine, folded in: every item counts itself for its row block
-              // once its eo rows are out (all consumer threads' stores, then a CTA barrier,
-              // then one device-scope fence and one atomic by thread 0, which orders the
-              // whole CTA's stores before the count); the CTA whose count completes the row
-              // block (all active experts in) fences again and sums, for every token, the
-              // eo rows of its slots in slot order j = 0 .. topk - 1, so the result does not
-              // depend on which CTA finishes last.  It also resets the counter.
-              asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
-              if (threadIdx.x == 0) {
-                  __threadfence();
-                  const bool last = !*abort_flag && atomicAdd(p.cnt + rb, 1) == *p.n_act - 1;
-                  if (last) __threadfence();
-                  *last_flag = last;
-              }
-              asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
-              if (*last_flag) {
-                  // one consumer warp per pair of tokens, lane l owning rows 4 l .. 4 l + 3 of the
-                  // block; the slots' grouped positions come in one coalesced load per token
-                  // (lane j holds slot j's), then the rows of eight slots of both tokens are
-                  // loaded together (independent loads in flight) and added in slot order
-                  const int64_t n0 = (int64_t)rb * RB + 4 * lane;
-                  for (int64_t t0 = 2 * warp; t0 < p.T; t0 += 2 * CONSUMERS) {
-                      const bool two = t0 + 1 < p.T;
-                      float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-                      for (int j0 = 0; j0 < p.topk; j0 += 32) {
-                          int qa = 0, qb = 0;
-                          if (j0 + lane < p.topk) {
-                              qa = __ldg(p.inv + t0 * p.topk + j0 + lane);
-                              if (two) qb = __ldg(p.inv + (t0 + 1) * p.topk + j0 + lane);
-                          }
-                          const int nj = min(32, p.topk - j0);
-                          for (int j1 = 0; j1 < nj; j1 += 8) {
-                              float4 v[2][8];
+        }
+        if (MODE == DOWN) {
+            // The weighted combine, folded in.  Once this CTA's items are done (their eo
+            // rows written by every consumer thread, then a CTA barrier), thread 0 makes
+            // them visible with one device-scope fence and counts each item for its row
+            // block with one atomic; the CTA whose count completes a row block (all active
+            // experts in) fences again and sums, for every token, the eo rows of its slots
+            // in slot order j = 0 .. topk - 1, so the result does not depend on which CTA
+            // finishes last.  It also resets the counter.  The row blocks to finish go
+            // through shared memory (the idle partial-tile buffer).
+            int* done = reinterpret_cast<int*>(part);
+            asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
+            if (threadIdx.x == 0) {
+                int nd = 0;
+                if (!*abort_flag) {
+                    __threadfence();
+                    for (int idx = first; idx < nitems; idx += stride) {
+                        const int rbi = idx % p.rbs;
+                        if (atomicAdd(p.cnt + rbi, 1) == *p.n_act - 1) done[nd++] = rbi;
+                    }
+                    if (nd) __threadfence();
+                }
+                *last_flag = nd;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
+            for (int di = 0; di < *last_flag; ++di) {
+                const int rb = done[di];
+                // one consumer warp per pair of tokens, lane l owning rows 4 l .. 4 l + 3 of the
+                // block; the slots' grouped positions come in one coalesced load per token
+                // (lane j holds slot j's), then the rows of eight slots of both tokens are
+                // loaded together (independent loads in flight) and added in slot order
+                const int64_t n0 = (int64_t)rb * RB + 4 * lane;
+                for (int64_t t0 = 2 * warp; t0 < p.T; t0 += 2 * CONSUMERS) {
+                    const bool two = t0 + 1 < p.T;
+                    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+                    for (int j0 = 0; j0 < p.topk; j0 += 32) {
+                        int qa = 0, qb = 0;
+                        if (j0 + lane < p.topk) {
+                            qa = __ldg(p.inv + t0 * p.topk + j0 + lane);
+                            if (two) qb = __ldg(p.inv + (t0 + 1) * p.topk + j0 + lane);
+                        }
+                        const int nj = min(32, p.topk - j0);
+                        for (int j1 = 0; j1 < nj; j1 += 8) {
+                            float4 v[2][8];
 #pragma unroll
-                              for (int jj = 0; jj < 8; ++jj) {
-                                  const int64_t q0 = __shfl_sync(0xffffffffu, qa, (j1 + jj) & 31);
-                                  const int64_t q1 = __shfl_sync(0xffffffffu, qb, (j1 + jj) & 31);
-                                  if (j1 + jj < nj) {
-                                      v[0][jj] = __ldcg(reinterpret_cast<const float4*>(p.out + q0 * p.H + n0));
-                                      if (two) v[1][jj] = __ldcg(reinterpret_cast<const float4*>(p.out + q1 * p.H + n0));
-                                  }
-                              }
+                            for (int jj = 0; jj < 8; ++jj) {
+                                const int64_t q0 = __shfl_sync(0xffffffffu, qa, (j1 + jj) & 31);
+                                const int64_t q1 = __shfl_sync(0xffffffffu, qb, (j1 + jj) & 31);
+                                if (j1 + jj < nj) {
+                                    v[0][jj] = __ldcg(reinterpret_cast<const float4*>(p.out + q0 * p.H + n0));
+                                    if (two) v[1][jj] = __ldcg(reinterpret_cast<const float4*>(p.out + q1 * p.H + n0));
+                                }
+                            }
 #pragma unroll
-                              for (int u = 0; u < 2; ++u) {
+                            for (int u = 0; u < 2; ++u) {
 #pragma unroll
-                                  for (int jj = 0; jj < 8; ++jj) {
-                                      if (j1 + jj < nj && (u == 0 || two)) {
-                                          acc[u].x += v[u][jj].x;
-                                          acc[u].y += v[u][jj].y;
-                                          acc[u].z += v[u][jj].z;
-                                          acc[u].w += v[u][jj].w;
-                                      }
-                                  }
-                              }
-                          }
-                      }
+                                for (int jj = 0; jj < 8; ++jj) {
+                                    if (j1 + jj < nj && (u == 0 || two)) {
+                                        acc[u].x += v[u][jj].x;
+                                        acc[u].y += v[u][jj].y;
+                                        acc[u].z += v[u][jj].z;
+                                        acc[u].w += v[u][jj].w;
+                                    }
+                                }
+                            }
+                        }
+                    }
 #pragma unroll
-                      for (int u = 0; u < 2; ++u) {
-                          if (u == 1 && !two) break;
-                          const int64_t t = t0 + u;
-                          if (p.yt == CQ_F32) {
-                              *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + t * p.H + n0) = acc[u];
-                          } else {
-                              __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.y) + t * p.H + n0);
-                              o[0] = __floats2bfloat162_rn(acc[u].x, acc[u].y);
-                              o[1] = __floats2bfloat162_rn(acc[u].z, acc[u].w);
-                          }
-                      }
-                  }
-                  if (threadIdx.x == 0) p.cnt[rb] = 0;
-              }
-          }
+                    for (int u = 0; u < 2; ++u) {
+                        if (u == 1 && !two) break;
+                        const int64_t t = t0 + u;
+                        if (p.yt == CQ_F32) {
+                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + t * p.H + n0) = acc[u];
+                        } else {
+                            __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.y) + t * p.H + n0);
+                            o[0] = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+                            o[1] = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+                        }
+                    }
+                }
+                if (threadIdx.x == 0) p.cnt[rb] = 0;
+            }
         }
     }
 

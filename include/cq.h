@@ -201,7 +201,7 @@ cq_status cq_ffn_q4(const void* X, int xt, int64_t T, int64_t H, int64_t I,
  * expert; each (t, j) is its own entry, so repeated experts in a row are
  * counted twice.  The j-sum per token runs in slot order (deterministic).
  * Shape rules: T >= 1, 1 <= topk <= 64, 1 <= E <= 1024, T*topk <= 65536,
- * H % 256 == 0, I % 256 == 0, H >= 256, I >= 256.
+ * H % 256 == 0, I % 256 == 0, 256 <= H <= 16384, I >= 256.
  * Workspace: cq_moe_workspace_bytes(T, H, I, E, topk) bytes.  After the
  * call completes, cq_moe_layout reads the routing layout kept there.
  * An index outside [0, E) sets CQ_ERR_INDEX on the device and leaves Y
@@ -220,7 +220,9 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E,
  *   idx[t][0..topk) = the topk experts with the largest logits, descending,
  *                     the lower index first on ties;
  *   w[t][j]         = p_e / sum of p over the picked experts, where
- *                     p = softmax of the row's E logits (f64, rounded to f32);
+ *                     p = softmax of the row's E logits (computed in f32 as
+ *                     exp(l - max) / its sum over the picked experts: the
+ *                     softmax denominator cancels);
  *   shared = 1:       logits rows hold E + 1 values, the last one the shared
  *                     expert's gate g; slot topk is expert E with weight
  *                     1 / (1 + exp(-g)).

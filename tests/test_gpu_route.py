@@ -1,6 +1,8 @@
 """GPU parity of the device routing (router logits -> top-k experts and
 renormalised weights, the shared expert's sigmoid-gated slot) against the
-CPU oracle: the expert indices bit-exact, the weights within two f32 ulps;
+CPU oracle: the expert indices bit-exact (both sides pick by comparing the
+f32 logits), the weights (f32 exponentials on the device, f64 in the oracle)
+within 8 f32 ulps;
 then the whole routed MoE block with a shared expert (device routing, then
 the expert panels with the shared expert stacked as expert E) against the
 oracle's f64 chain."""
@@ -42,7 +44,7 @@ def test_route_matches_oracle(T, E, topk, shared):
     idx, w = _route_dev(lg, topk, shared)
     oidx, ow = oracle.route(lg, topk, shared)
     assert np.array_equal(idx, oidx)
-    assert np.all(np.abs(w - ow) <= 2 * np.spacing(np.abs(ow)))
+    assert np.all(np.abs(w - ow) <= 8 * np.spacing(np.abs(ow)))
 
 
 def test_route_heavy_ties():
@@ -51,7 +53,7 @@ def test_route_heavy_ties():
     idx, w = _route_dev(lg, 16, False)
     oidx, ow = oracle.route(lg, 16)
     assert np.array_equal(idx, oidx)
-    assert np.all(np.abs(w - ow) <= 2 * np.spacing(np.abs(ow)))
+    assert np.all(np.abs(w - ow) <= 8 * np.spacing(np.abs(ow)))
 
 
 @pytest.mark.parametrize("out", ["f32", "bf16"])
