@@ -32,6 +32,13 @@ _SIGS = {
     "cq_gemm_q8row": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p, _c_int, _c_p]),
     "cq_moe_workspace_bytes": (_c_sz, [_c_i64] * 5),
     "cq_ffn_q4_workspace_bytes": (_c_sz, [_c_i64] * 3),
+    "cq_gemm_q8b_workspace_bytes": (_c_sz, [_c_i64, _c_i64]),
+    "cq_gemm_q8b": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p, _c_int, _c_p, _c_sz, _c_p]),
+    "cq_gemm_q4a_workspace_bytes": (_c_sz, [_c_i64] * 4),
+    "cq_gemm_q4a": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_p, _c_int, _c_p, _c_sz,
+                             _c_p]),
+    "cq_gemm_q8_2f_workspace_bytes": (_c_sz, [_c_i64, _c_i64]),
+    "cq_gemm_q8_2f": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_int, _c_p, _c_sz, _c_p]),
     "cq_gemm_q4_batched_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_int]),
     "cq_gemm_q4_batched": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_int, _c_i64, _c_p, _c_int, _c_i64,
                                     _c_p, _c_sz, _c_p]),
@@ -171,6 +178,48 @@ def cq_gemm_q4_batched(X, K, jobs, N, Y, ws, stream=None, raise_on_error=True):
     st = lib().cq_gemm_q4_batched(_ptr(X), _xt(X), T, K, X.stride(0), ctypes.cast(arr, ctypes.c_void_p), len(jobs), N,
                                   _ptr(Y), _xt(Y), Y.stride(0), _ptr(ws), ws.numel() * ws.element_size(),
                                   _stream(stream))
+    if raise_on_error:
+        _check(st)
+    return st
+
+
+def cq_gemm_q8b_workspace_bytes(T, K) -> int:
+    return lib().cq_gemm_q8b_workspace_bytes(T, K)
+
+
+def cq_gemm_q8b(X, Wq, Ws, Y, ws, stream=None, raise_on_error=True):
+    """Q8 per 32-k block: Wq int8 [N][K], Ws f32 [N][K/32]."""
+    T, K = X.shape
+    st = lib().cq_gemm_q8b(_ptr(X), _xt(X), T, K, _ptr(Wq), _ptr(Ws), Wq.shape[0], _ptr(Y), _xt(Y), _ptr(ws),
+                           ws.numel() * ws.element_size(), _stream(stream))
+    if raise_on_error:
+        _check(st)
+    return st
+
+
+def cq_gemm_q4a_workspace_bytes(T, K, N, gk) -> int:
+    return lib().cq_gemm_q4a_workspace_bytes(T, K, N, gk)
+
+
+def cq_gemm_q4a(X, Wq, Ws, Wo, gk, Y, ws, stream=None, raise_on_error=True):
+    """Affine Q4: the Q4 split plane plus Wo bf16-bit offsets [N][K/32/gk]."""
+    T, K = X.shape
+    st = lib().cq_gemm_q4a(_ptr(X), _xt(X), T, K, _ptr(Wq), _ptr(Ws), _ptr(Wo), gk, Wq.shape[0], _ptr(Y), _xt(Y),
+                           _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    if raise_on_error:
+        _check(st)
+    return st
+
+
+def cq_gemm_q8_2f_workspace_bytes(T, K) -> int:
+    return lib().cq_gemm_q8_2f_workspace_bytes(T, K)
+
+
+def cq_gemm_q8_2f(X, Wq, rs, col, Y, ws, stream=None, raise_on_error=True):
+    """q8_2f: Wq int8 [N][K], rs f32 [N], col f32 [K]."""
+    T, K = X.shape
+    st = lib().cq_gemm_q8_2f(_ptr(X), _xt(X), T, K, _ptr(Wq), _ptr(rs), _ptr(col), Wq.shape[0], _ptr(Y), _xt(Y),
+                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     if raise_on_error:
         _check(st)
     return st

@@ -488,6 +488,115 @@ cq_status cq_gemm_q4_batched(const void* X, int xt, int64_t T, int64_t K, int64_
     return launched(launch_tc_q4(a, s), "z-batched tcgen05 Q4 GEMM");
 }
 
+// ---- format variants --------------------------------------------------------
+
+size_t cq_gemm_q8_2f_workspace_bytes(int64_t T, int64_t K) { return (T < 1 || K < 1) ? 0 : q4_ws_bytes(T, K); }
+size_t cq_gemm_q8b_workspace_bytes(int64_t T, int64_t K) { return (T < 1 || K < 1) ? 0 : q4_ws_bytes(T, K); }
+size_t cq_gemm_q4a_workspace_bytes(int64_t T, int64_t K, int64_t N, int64_t gk) {
+    if (T < 1 || K < 32 || N < 1 || gk < 1) return 0;
+    return q4_ws_bytes(T, K) + up((size_t)T * (size_t)(K / 32 / gk) * 4) + up((size_t)T * N * 4);
+}
+
+cq_status cq_gemm_q8_2f(const void* X, int xt, int64_t T, int64_t K, const int8_t* Wq, const float* rs, const float* col,
+                        int64_t N, void* Y, int yt, void* ws, size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    if (!X || !Wq || !rs || !col || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q8_2f: null pointer");
+    cq_status st;
+    if ((st = check_x(xt)) || (st = check_y(yt))) return st;
+    if (T < 1 || N < 1 || K < 128 || K % 128 || T > (1LL << 31) - 1 || N > (1LL << 31) - 1)
+        return fail(CQ_ERR_SHAPE, "cq_gemm_q8_2f: need T>=1, N>=1, K%%128==0 (T=%lld K=%lld N=%lld)", (long long)T,
+                    (long long)K, (long long)N);
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(rs) || !aligned16(col) || !aligned16(Y))
+        return fail(CQ_ERR_ALIGN, "cq_gemm_q8_2f: pointers must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(ws) & (ALIGN - 1)) || ws_bytes < q4_ws_bytes(T, K))
+        return fail(CQ_ERR_WORKSPACE, "cq_gemm_q8_2f: workspace needs %zu bytes, 256-aligned", q4_ws_bytes(T, K));
+    if ((st = check_arch())) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = stream_error_word(s);
+    if (!err) return CQ_ERR_CUDA;
+    const Q4Ws w = q4_ws(ws, T, K);
+    // X times the column field, to fp16 behind the guard (k order); the Q8-row kernels then apply
+    // the row scale and the guard's inverse per token
+    if ((st = launched(launch_x_col_half(X, xt, col, T, K, w.xh, w.rsx, s), "q8_2f column-field guard pass"))) return st;
+    const uint8_t* q = reinterpret_cast<const uint8_t*>(Wq);
+    if (use_skinny(T)) {
+        if (T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q8_2f: the weight-streaming path serves T <= 32");
+        SkinnyDense a = {w.xh, 0, w.rsx, rs, q, nullptr, T, K, N, Y, yt, err};
+        return launched(launch_skinny_q8(a, s), "weight-streaming q8_2f GEMM");
+    }
+    TcArgs a = {w.xh, 0, w.rsx, rs, q, nullptr, T, K, N, Y, yt, err};
+    return launched(launch_tc_q8(a, s), "tcgen05 q8_2f GEMM");
+}
+
+cq_status cq_gemm_q8b(const void* X, int xt, int64_t T, int64_t K, const int8_t* Wq, const float* Ws, int64_t N,
+                      void* Y, int yt, void* ws, size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    if (!X || !Wq || !Ws || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q8b: null pointer");
+    cq_status st;
+    if ((st = check_x(xt)) || (st = check_y(yt))) return st;
+    if (T < 1 || N < 1 || K < 128 || K % 128 || T > (1LL << 31) - 1 || N > (1LL << 31) - 1)
+        return fail(CQ_ERR_SHAPE, "cq_gemm_q8b: need T>=1, N>=1, K%%128==0 (T=%lld K=%lld N=%lld)", (long long)T,
+                    (long long)K, (long long)N);
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(Y))
+        return fail(CQ_ERR_ALIGN, "cq_gemm_q8b: pointers must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(ws) & (ALIGN - 1)) || ws_bytes < q4_ws_bytes(T, K))
+        return fail(CQ_ERR_WORKSPACE, "cq_gemm_q8b: workspace needs %zu bytes, 256-aligned", q4_ws_bytes(T, K));
+    if ((st = check_arch())) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = stream_error_word(s);
+    if (!err) return CQ_ERR_CUDA;
+    const uint8_t* q = reinterpret_cast<const uint8_t*>(Wq);
+    if (use_skinny(T)) {   // the activations as given
+        if (T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q8b: the weight-streaming path serves T <= 32");
+        SkinnyDense a = {X, xt == CQ_BF16 ? 1 : 0, nullptr, nullptr, q, nullptr, T, K, N, Y, yt, err};
+        a.wsf = Ws;
+        return launched(launch_skinny_q8b(a, s), "weight-streaming Q8/32 GEMM");
+    }
+    const Q4Ws w = q4_ws(ws, T, K);
+    if ((st = launched(launch_x_col_half(X, xt, nullptr, T, K, w.xh, w.rsx, s), "Q8/32 activation guard pass"))) return st;
+    TcArgs a = {w.xh, 0, w.rsx, nullptr, q, nullptr, T, K, N, Y, yt, err};
+    a.wsf = Ws;
+    return launched(launch_tc_q8b(a, s), "tcgen05 Q8/32 GEMM");
+}
+
+cq_status cq_gemm_q4a(const void* X, int xt, int64_t T, int64_t K, const uint8_t* Wq, const uint16_t* Ws,
+                      const uint16_t* Wo, int64_t gk, int64_t N, void* Y, int yt, void* ws, size_t ws_bytes,
+                      void* stream) {
+    g_msg[0] = 0;
+    if (!X || !Wq || !Ws || !Wo || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q4a: null pointer");
+    cq_status st;
+    if ((st = check_x(xt)) || (st = check_y(yt))) return st;
+    if (T < 1 || N < 1 || K < 256 || K % 256 || T > (1LL << 31) - 1 || N > (1LL << 31) - 1 || gk < 1 ||
+        (K / 32) % gk || K / 32 / gk > 512)
+        return fail(CQ_ERR_SHAPE, "cq_gemm_q4a: need T>=1, N>=1, K%%256==0, gk dividing K/32, K/32/gk <= 512 "
+                    "(T=%lld K=%lld N=%lld gk=%lld)", (long long)T, (long long)K, (long long)N, (long long)gk);
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(Wo) & 1))
+        return fail(CQ_ERR_ALIGN, "cq_gemm_q4a: X, Wq, Ws, Y must be 16-byte aligned, Wo 2-byte aligned");
+    const size_t need = cq_gemm_q4a_workspace_bytes(T, K, N, gk);
+    if ((reinterpret_cast<uintptr_t>(ws) & (ALIGN - 1)) || ws_bytes < need)
+        return fail(CQ_ERR_WORKSPACE, "cq_gemm_q4a: workspace needs %zu bytes, 256-aligned", need);
+    if ((st = check_arch())) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = stream_error_word(s);
+    if (!err) return CQ_ERR_CUDA;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    const Q4Ws w = q4_ws(ws, T, K);
+    float* xs = reinterpret_cast<float*>(b + q4_ws_bytes(T, K));
+    float* add = reinterpret_cast<float*>(b + q4_ws_bytes(T, K) + up((size_t)T * (size_t)(K / 32 / gk) * 4));
+    // the offsets' term sum_g off[n][g] * (sum of X over group g), added by the GEMM's epilogue
+    if ((st = launched(launch_offset_term(X, xt, T, K, Wo, (int)gk, N, xs, add, s), "affine Q4 offset term"))) return st;
+    if (use_skinny(T)) {
+        if (T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4a: the weight-streaming path serves T <= 32");
+        SkinnyDense a = {X, xt == CQ_BF16 ? 1 : 0, nullptr, nullptr, Wq, Ws, T, K, N, Y, yt, err};
+        a.add = add;
+        return launched(launch_skinny_q4(a, s), "weight-streaming affine Q4 GEMM");
+    }
+    if ((st = launched(launch_x_half(X, xt, T, K, w.xh, w.rsx, s), "activation guard pass"))) return st;
+    TcArgs a = {w.xh, 0, w.rsx, nullptr, Wq, Ws, T, K, N, Y, yt, err};
+    a.add = add;
+    return launched(launch_tc_q4(a, s), "tcgen05 affine Q4 GEMM");
+}
+
 size_t cq_ffn_q4_workspace_bytes(int64_t T, int64_t H, int64_t I) {
     if (T < 1 || H < 1 || I < 1) return 0;
     return ffn_layout(T, H, I).total;

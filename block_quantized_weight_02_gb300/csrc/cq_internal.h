@@ -112,11 +112,14 @@ struct SkinnyDense {
     int nz;
     SkJob more[ZMAX];
     int64_t ldx, ldy;
+    const float* wsf;    // Q8 per 32-k block: f32 block scales [N][K/32] (single job)
+    const float* add;    // nullable f32 [T][N] added before the output rounding (single job)
     SkJob job(int j) const { return nz > 1 ? more[j] : SkJob{x, rs, wq, ws, y}; }
     int jobs() const { return nz > 1 ? nz : 1; }
 };
 cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s);
-cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s);
+cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s);    // rsx nullable: per-token scales (q8_2f)
+cudaError_t launch_skinny_q8b(const SkinnyDense& a, cudaStream_t s);   // Q8 per 32-k block, activations as given
 
 struct SkinnyMoe {
     const uint16_t* xh;     // [P][H] fp16 (guarded, streaming order), rows gathered into grouped order
@@ -152,6 +155,8 @@ struct TcJob {
     const uint8_t* wq;
     const uint16_t* ws;
     void* y;
+    const float* wsf;    // Q8 per 32-k block: f32 block scales [N][K/32]
+    const float* add;    // nullable f32 [T][N] added before the output rounding
 };
 struct TcArgs {
     const void* x;       // [T][K] fp16/bf16 (Q4: guarded fp16 in the streaming order)
@@ -167,11 +172,15 @@ struct TcArgs {
     int nz;              // z-batched: number of jobs in more[] (0 or 1: the single job above)
     TcJob more[ZMAX];
     int64_t ldy;         // output row pitch in elements (0: N)
-    TcJob job(int j) const { return nz > 1 ? more[j] : TcJob{x, rsx, rs, wq, ws, y}; }
+    const float* wsf;    // single job: Q8/32 block scales
+    const float* add;    // single job: addend
+    TcJob job(int j) const { return nz > 1 ? more[j] : TcJob{x, rsx, rs, wq, ws, y, wsf, add}; }
     int jobs() const { return nz > 1 ? nz : 1; }
 };
 cudaError_t launch_tc_q4(const TcArgs& a, cudaStream_t s);
-cudaError_t launch_tc_q8(const TcArgs& a, cudaStream_t s);
+cudaError_t launch_tc_q8(const TcArgs& a, cudaStream_t s);   // x fp16 or bf16; rsx nullable (q8_2f: the guard)
+// Q8 per 32-k block: x guarded fp16 in k order, rsx its scales, wsf the f32 block scales.
+cudaError_t launch_tc_q8b(const TcArgs& a, cudaStream_t s);
 // Gate/up mode: wq is the Q4 [2I][K] gate|up matrix, N = I; y = a[T][I] f32,
 // a = silu(gate) * up (x: guarded fp16 in the streaming order, rsx its scales).
 cudaError_t launch_tc_q4_gateup(const TcArgs& a, cudaStream_t s);

@@ -97,6 +97,7 @@ struct Params {
     void* yj[ZMAX];
     const float* rsj[ZMAX];
     int64_t ldy;
+    const float* add;     // DENSE: nullable f32 [T][N] added before the output rounding
     // DOWN: the weighted combine, folded in (Y [T][H] written by the last item of each row block)
     const int32_t* inv;   // grouped position of each pair id
     int32_t* cnt;         // [H / 128] items finished per row block (zero at the start of the call)
@@ -197,9 +198,9 @@ __host__ __device__ constexpr int rows_per_stage(int MT, int KW) { return CONSUM
 
 template <int FMT, int NCOL, int RB>
 struct StageGeo {
-    static constexpr int KSTAGE = FMT == 0 ? 256 : 128;
+    static constexpr int KSTAGE = FMT == 0 ? 256 : 128;   // FMT 1 Q8-row, 2 Q8 per 32-k block: 128 k
     static constexpr int W_BYTES = RB * 128;
-    static constexpr int S_BYTES = FMT == 0 ? RB * 16 : 0;
+    static constexpr int S_BYTES = FMT != 1 ? RB * 16 : 0;   // Q4: 8 fp16 per row, Q8/32: 4 f32
     static constexpr int XSL = KSTAGE / 64;            // 64-k slabs per stage
     static constexpr int X_OFF = W_BYTES + S_BYTES;    // 1024-aligned
     static constexpr int X_BYTES = NCOL * XSL * 128;
@@ -221,7 +222,8 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
     constexpr int RB = rows_per_stage(MT, KW);
     static_assert(KW == 1 || KW == 2, "k split over one or two warp groups");
     static_assert(FMT == 1 || (MT == 1 && (XBF == 0 || RAW)), "Q4 stages: one m16 tile per warp; bf16 activations as given");
-    static_assert(RAW == 0 || (FMT == 0 && MODE == DENSE), "activations as given: dense Q4");
+    static_assert(RAW == 0 || (FMT != 1 && MODE == DENSE), "activations as given: dense Q4 or Q8/32");
+    static_assert(FMT != 2 || (RAW == 1 && KW == 1), "Q8/32: activations as given, every warp on the whole stage");
     static_assert(MODE == DENSE || RB == 128, "expert panels use 128-row stages");
     using G = StageGeo<FMT, NCOL, RB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -328,7 +330,7 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
             const int s = lane;
             if (lane == 0) {
                 tma_prefetch_desc(tmW);
-                if (FMT == 0) tma_prefetch_desc(tmS);
+                if (FMT != 1) tma_prefetch_desc(tmS);
                 tma_prefetch_desc(tmX);
             }
             int last_gi = -1;         // the last stage this lane issued
@@ -346,7 +348,8 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
                     }
                 } else {
                     tma_load_3d(sbase, tmW, full_bar(s), st * 128, it.row_box[0], it.expert);
-                    if (FMT == 0) tma_load_3d(sbase + (uint32_t)G::W_BYTES, tmS, full_bar(s), st * 8, it.row_box[0], it.expert);
+                    if (FMT != 1)   // block scales: 8 fp16 (Q4) or 4 f32 (Q8/32) per row and stage
+                        tma_load_3d(sbase + (uint32_t)G::W_BYTES, tmS, full_bar(s), st * (FMT == 0 ? 8 : 4), it.row_box[0], it.expert);
                 }
             };
             auto load_x = [&](const Item& it, int i, int grp) {
@@ -500,6 +503,61 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
                         }
                         const uint32_t a1[4] = {d[0], e[0], d[1], e[1]};
                         const uint32_t a2[4] = {d[2], e[2], d[3], e[3]};
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            float pb[4] = {0.f, 0.f, 0.f, 0.f};
+                            if (XBF) {
+                                mma_16816_bf16(pb, a1, bx[nt].x, bx[nt].y);
+                                mma_16816_bf16(pb, a2, bx[nt].z, bx[nt].w);
+                            } else {
+                                mma_16816_f16(pb, a1, bx[nt].x, bx[nt].y);
+                                mma_16816_f16(pb, a2, bx[nt].z, bx[nt].w);
+                            }
+                            acc[0][nt][0] = fmaf(sa, pb[0], acc[0][nt][0]);
+                            acc[0][nt][1] = fmaf(sa, pb[1], acc[0][nt][1]);
+                            acc[0][nt][2] = fmaf(sb, pb[2], acc[0][nt][2]);
+                            acc[0][nt][3] = fmaf(sb, pb[3], acc[0][nt][3]);
+                        }
+                    }
+                } else if (FMT == 2) {
+                    // Q8 per 32-k block, activations as given (k order): four blocks per stage.
+                    // Lane c of a quad takes words c (k = 4c .. 4c + 3) and c + 4 (k = 16 + 4c ..)
+                    // of each block for its rows, the same k as the two 8-byte activation runs
+                    // it reads, so each pair of bytes is an adjacent-k pair of both operands; the
+                    // block's two MMAs see one f32 scale per row, applied to their f32 result.
+                    const uint32_t wS = sW + w_lane;
+                    const uint32_t sS = sW + (uint32_t)G::W_BYTES + (uint32_t)(row0 * 16);
+                    const uint4 sc0 = lds128a(sS), sc1 = lds128a(sS + 128);   // rows row0, row0 + 8
+#pragma unroll
+                    for (int jf = 0; jf < 4; ++jf) {
+                        const uint32_t wa = wS ^ ((uint32_t)(2 * jf) << 4), wb = wS ^ ((uint32_t)(2 * jf + 1) << 4);
+                        uint32_t wa0 = lds32(wa), wa1 = lds32(wb), wb0 = lds32(wa + 1024), wb1 = lds32(wb + 1024);
+                        uint4 bx[NT];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            // row r = 8 nt + g, slab jf / 2, chunks 4 (jf % 2) + c / 2 (+ 2 for the high run),
+                            // 128-byte swizzle key (2 r + slab) % 8 over the [row][2 slabs][128 B] box
+                            const uint32_t slab = (uint32_t)(jf >> 1), key = ((uint32_t)(2 * g) + slab) & 7u;
+                            const uint32_t rowb = sX + (uint32_t)((8 * nt + g) * 256) + slab * 128u + 8u * (uint32_t)(c & 1);
+                            const uint32_t clo = (uint32_t)(4 * (jf & 1) + (c >> 1));
+                            const uint2 lo = lds64(rowb + ((clo ^ key) << 4)), hi = lds64(rowb + (((clo + 2u) ^ key) << 4));
+                            bx[nt] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                        }
+                        uint32_t a1[4], a2[4];
+                        if (XBF) {
+                            a1[0] = i8x2_to_bf2(wa0, 0x4140u); a1[1] = i8x2_to_bf2(wb0, 0x4140u);
+                            a1[2] = i8x2_to_bf2(wa0, 0x4342u); a1[3] = i8x2_to_bf2(wb0, 0x4342u);
+                            a2[0] = i8x2_to_bf2(wa1, 0x4140u); a2[1] = i8x2_to_bf2(wb1, 0x4140u);
+                            a2[2] = i8x2_to_bf2(wa1, 0x4342u); a2[3] = i8x2_to_bf2(wb1, 0x4342u);
+                        } else {
+                            wa0 ^= 0x80808080u; wb0 ^= 0x80808080u; wa1 ^= 0x80808080u; wb1 ^= 0x80808080u;
+                            a1[0] = i8x2_to_h2(wa0, 0x4140u); a1[1] = i8x2_to_h2(wb0, 0x4140u);
+                            a1[2] = i8x2_to_h2(wa0, 0x4342u); a1[3] = i8x2_to_h2(wb0, 0x4342u);
+                            a2[0] = i8x2_to_h2(wa1, 0x4140u); a2[1] = i8x2_to_h2(wb1, 0x4140u);
+                            a2[2] = i8x2_to_h2(wa1, 0x4342u); a2[3] = i8x2_to_h2(wb1, 0x4342u);
+                        }
+                        const float sa = __uint_as_float(jf == 0 ? sc0.x : jf == 1 ? sc0.y : jf == 2 ? sc0.z : sc0.w);
+                        const float sb = __uint_as_float(jf == 0 ? sc1.x : jf == 1 ? sc1.y : jf == 2 ? sc1.z : sc1.w);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             float pb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -748,7 +806,8 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
                     for (int q = 0; q < p.ks; ++q) s += recv[q * per + (e - lo)];
                     const int64_t n = (int64_t)rb * RB + r, t = col;
                     if (n < p.N && t < p.T) {
-                        const float v = s * (FMT == 0 ? (RAW ? 1.f : p.rsx[t]) : RSj[n]);
+                        float v = s * (FMT == 1 ? RSj[n] * (p.rsx ? p.rsx[t] : 1.f) : (RAW ? 1.f : p.rsx[t]));
+                        if (p.add) v += p.add[t * p.N + n];
                         if (p.yt == CQ_F32) reinterpret_cast<float*>(Yj)[t * p.ldy + n] = v;
                         else reinterpret_cast<__nv_bfloat16*>(Yj)[t * p.ldy + n] = __float2bfloat16_rn(v);
                     }
@@ -759,7 +818,8 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
                 const int r = e & (RB - 1), col = e / RB;
                 const int64_t n = (int64_t)rb * RB + r, t = col;
                 if (n < p.N && t < p.T) {
-                    const float v = part[r * NCOL + col] * (FMT == 0 ? (RAW ? 1.f : p.rsx[t]) : RSj[n]);
+                    float v = part[r * NCOL + col] * (FMT == 1 ? RSj[n] * (p.rsx ? p.rsx[t] : 1.f) : (RAW ? 1.f : p.rsx[t]));
+                    if (p.add) v += p.add[t * p.N + n];
                     if (p.yt == CQ_F32) reinterpret_cast<float*>(Yj)[t * p.ldy + n] = v;
                     else reinterpret_cast<__nv_bfloat16*>(Yj)[t * p.ldy + n] = __float2bfloat16_rn(v);
                 }
@@ -782,7 +842,7 @@ constexpr size_t smem_bytes() {
 // Weights [E][R][K bytes] and scales [E][R][K/32], boxes of rows_box rows.
 bool make_maps(CUtensorMap* mw, CUtensorMap* ms, int fmt, const uint8_t* wq, const uint16_t* ws, int64_t R,
                int64_t K, int64_t E, int rows_box) {
-    const uint64_t kbytes = fmt == 0 ? (uint64_t)K / 2 : (uint64_t)K;
+    const uint64_t kbytes = fmt == 0 ? (uint64_t)K / 2 : (uint64_t)K;   // fmt 1, 2: int8
     uint64_t dw[3] = {kbytes, (uint64_t)R, (uint64_t)E};
     uint64_t sw[2] = {kbytes, kbytes * (uint64_t)R};
     uint32_t bw[3] = {128, (uint32_t)rows_box, 1};
@@ -792,6 +852,12 @@ bool make_maps(CUtensorMap* mw, CUtensorMap* ms, int fmt, const uint8_t* wq, con
         uint64_t ss[2] = {(uint64_t)K / 32 * 2, (uint64_t)K / 32 * 2 * (uint64_t)R};
         uint32_t bs[3] = {8, (uint32_t)rows_box, 1};
         if (!encode_tiled(ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, ws, ds, ss, bs, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
+    } else if (fmt == 2) {   // f32 block scales [E][R][K/32], boxes of 4 per row (one 128-k stage)
+        uint64_t ds[3] = {(uint64_t)K / 32, (uint64_t)R, (uint64_t)E};
+        uint64_t ss[2] = {(uint64_t)K / 32 * 4, (uint64_t)K / 32 * 4 * (uint64_t)R};
+        uint32_t bs[3] = {4, (uint32_t)rows_box, 1};
+        if (!encode_tiled(ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws, ds, ss, bs, CU_TENSOR_MAP_SWIZZLE_NONE))
             return false;
     } else {
         *ms = *mw;
@@ -865,14 +931,20 @@ DenseCfg dense_cfg(int64_t T) {
 template <int FMT, int XBF>
 cudaError_t launch_dense_nt(const SMaps& maps, const void* const* xs, int nz, int64_t ldx, const Params& p, dim3 grid,
                             int cluster, int64_t T, cudaStream_t s) {
-    constexpr int RAW = FMT == 0 ? 1 : 0;
-    if (T <= 8) return launch_t<FMT, 1, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 5, RAW>(maps, xs, nz, T, ldx, p, grid, cluster, s);
-    if (T <= 16) return launch_t<FMT, 2, 1, 1, XBF, DENSE, FMT == 0 ? 3 : 5, RAW>(maps, xs, nz, T, ldx, p, grid, cluster, s);
-    return launch_t<FMT, 4, 1, 2, XBF, DENSE, FMT == 0 ? 4 : 6, RAW>(maps, xs, nz, T, ldx, p, grid, cluster, s);
+    if constexpr (FMT == 2) {   // Q8/32: 128-row stages, every warp on the whole stage
+        if (T <= 8) return launch_t<2, 1, 1, 1, XBF, DENSE, 5, 1>(maps, xs, nz, T, ldx, p, grid, cluster, s);
+        if (T <= 16) return launch_t<2, 2, 1, 1, XBF, DENSE, 4, 1>(maps, xs, nz, T, ldx, p, grid, cluster, s);
+        return launch_t<2, 4, 1, 1, XBF, DENSE, 3, 1>(maps, xs, nz, T, ldx, p, grid, cluster, s);
+    } else {
+        constexpr int RAW = FMT == 0 ? 1 : 0;
+        if (T <= 8) return launch_t<FMT, 1, 1, 1, XBF, DENSE, FMT == 0 ? 4 : 5, RAW>(maps, xs, nz, T, ldx, p, grid, cluster, s);
+        if (T <= 16) return launch_t<FMT, 2, 1, 1, XBF, DENSE, FMT == 0 ? 3 : 5, RAW>(maps, xs, nz, T, ldx, p, grid, cluster, s);
+        return launch_t<FMT, 4, 1, 2, XBF, DENSE, FMT == 0 ? 4 : 6, RAW>(maps, xs, nz, T, ldx, p, grid, cluster, s);
+    }
 }
 
 cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
-    const DenseCfg cf = dense_cfg(a.T);
+    const DenseCfg cf = fmt == 2 ? DenseCfg{a.T <= 8 ? 1 : a.T <= 16 ? 2 : 4, 1, 1, rows_per_stage(1, 1)} : dense_cfg(a.T);
     const int nz = a.jobs();
     SMaps maps;
     memset(&maps, 0, sizeof maps);
@@ -880,13 +952,15 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     Params p = {};
     for (int j = 0; j < nz; ++j) {
         const SkJob jb = a.job(j);
-        if (!make_maps(&maps.w[j], &maps.s[j], fmt, jb.wq, jb.ws, a.N, a.K, 1, cf.rb)) return cudaErrorInvalidValue;
+        const uint16_t* scales = fmt == 2 ? reinterpret_cast<const uint16_t*>(a.wsf) : jb.ws;
+        if (!make_maps(&maps.w[j], &maps.s[j], fmt, jb.wq, scales, a.N, a.K, 1, cf.rb)) return cudaErrorInvalidValue;
         xs[j] = jb.x;
         p.yj[j] = jb.y;
         p.rsj[j] = jb.rs;
     }
     p.K = a.K;
     p.nst_total = (int)(a.K / (fmt == 0 ? 256 : 128));
+    p.add = a.add;
     p.N = a.N;
     p.T = a.T;
     p.rsx = a.rsx;
@@ -913,6 +987,9 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
     if (fmt == 0)
         return a.x_bf16 ? launch_dense_nt<0, 1>(maps, xs, nz, ldx, p, grid, ks, a.T, s)
                         : launch_dense_nt<0, 0>(maps, xs, nz, ldx, p, grid, ks, a.T, s);
+    if (fmt == 2)
+        return a.x_bf16 ? launch_dense_nt<2, 1>(maps, xs, nz, ldx, p, grid, ks, a.T, s)
+                        : launch_dense_nt<2, 0>(maps, xs, nz, ldx, p, grid, ks, a.T, s);
     return a.x_bf16 ? launch_dense_nt<1, 1>(maps, xs, nz, ldx, p, grid, ks, a.T, s)
                     : launch_dense_nt<1, 0>(maps, xs, nz, ldx, p, grid, ks, a.T, s);
 }
@@ -921,6 +998,7 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
 
 cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s) { return launch_dense(0, a, s); }
 cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s) { return launch_dense(1, a, s); }
+cudaError_t launch_skinny_q8b(const SkinnyDense& a, cudaStream_t s) { return launch_dense(2, a, s); }
 
 // Gate/up panels: activations are the guarded rows already gathered into
 // grouped order ([P][H] fp16, inverse scales [P]).  One item is 64 gate rows

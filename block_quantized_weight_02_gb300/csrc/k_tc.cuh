@@ -65,9 +65,11 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 
 // Per-job pointers of a z-batched launch (job = blockIdx.y / tiles_y).
 struct Job {
-    const float* rsx;     // Q4: guard inverse scale per activation row
-    const float* rs;      // Q8: row scales
-    const uint16_t* ws;   // Q4 block scales [N][K/32]
+    const float* rsx;     // guard inverse scale per activation row (Q4, Q8/32; Q8-row: nullable)
+    const float* rs;      // Q8-row: row scales
+    const uint16_t* ws;   // Q4 block scales [N][K/32] fp16
+    const float* wsf;     // Q8/32 block scales [N][K/32] f32
+    const float* add;     // nullable: f32 [T][N] added to the scaled accumulator before the rounding
     void* y;              // output rows of pitch ldy
 };
 // Tensor maps of every job: weights, activations, outputs.
@@ -122,6 +124,8 @@ template <>
 struct Raw<0> { static constexpr int ROW = 32; };   // Q4: 64 k = 32 bytes per row and stage
 template <>
 struct Raw<1> { static constexpr int ROW = 64; };   // Q8: 64 bytes per row and stage
+template <>
+struct Raw<2> { static constexpr int ROW = 64; };   // Q8 per 32-k block: 64 bytes per row and stage
 
 // Loads come in super-stages of G stages (G x 64 k), two TMA boxes each: a TMA
 // box costs about the same however few bytes it holds, so the weight rows are
@@ -298,7 +302,9 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
     constexpr int CH = ep_chunk(BN, KS);     //           columns per chunk
     static_assert(CW % 16 == 0 && CW % CH == 0 && CW <= 64, "epilogue chunks");
     const int cbase = kz * NC;               // first column finished here
-    float esc0 = 0.f, esc1 = 0.f;            // epilogue scales, loaded before the last MMAs end
+    // epilogue scales, loaded before the last MMAs end: per token (guard inverse; lane l of a
+    // group holds columns l and 32 + l) and, for Q8-row, per weight row
+    float etk0 = 1.f, etk1 = 1.f, erow = 1.f;
 
     if (warp == PRODUCER_WARP) {
         // ================= TMA producers =================
@@ -459,13 +465,20 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
         const uint32_t wsw = L::WROW == 128 ? (uint32_t)(r & 7)
                            : L::WROW == 64  ? (uint32_t)((r >> 1) & 3)
                                             : (uint32_t)((r >> 2) & 1);
-        // Q4 scales of this row: the two fp16 of stage kb (blocks 2 kb, 2 kb + 1), loaded two
-        // of this group's stages ahead
+        // Block scales of this row: the two of stage kb (blocks 2 kb, 2 kb + 1) as an fp16 pair
+        // (Q4: stored so; Q8/32: f32, rounded to fp16), loaded two of this group's stages ahead
         const uint32_t* srow = reinterpret_cast<const uint32_t*>(J.ws + n * (p.K / 32)) + k0;
+        const float2* srowf = reinterpret_cast<const float2*>(J.wsf + n * (p.K / 32)) + k0;
+        auto scale_pair = [&](int kbi) -> uint32_t {
+            if (FMT == 0) return __ldg(srow + kbi);
+            const float2 f = __ldg(srowf + kbi);
+            const __half2 h = __floats2half2_rn(f.x, f.y);
+            return *reinterpret_cast<const uint32_t*>(&h);
+        };
         uint32_t sc0 = 0, sc1 = 0;
-        if (FMT == 0 && row_ok) {
-            if (grp < nk) sc0 = __ldg(srow + grp);
-            if (grp + 4 < nk) sc1 = __ldg(srow + grp + 4);
+        if (FMT != 1 && row_ok) {
+            if (grp < nk) sc0 = scale_pair(grp);
+            if (grp + 4 < nk) sc1 = scale_pair(grp + 4);
         }
         // Every group waits for every super-stage in order (decoding only its own stages
         // in it), so each round of each super-slot is waited for in order and a parity
@@ -486,7 +499,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             const int rb = (kb / RS) % NRB;                    // its round's barriers
             const uint32_t rph = (uint32_t)((kb / AS) & 1);    // and their phase
             uint32_t sc_next = 0;
-            if (FMT == 0 && row_ok && kb + 8 < nk) sc_next = __ldg(srow + kb + 8);
+            if (FMT != 1 && row_ok && kb + 8 < nk) sc_next = scale_pair(kb + 8);
             // the slot's previous round (NRB back) must have been consumed
             const int rp = kb / RS - NRB;
             const bool freed = MERGE ? (rp < 0 || mbar_wait_spin(empty_bar(rp % LSS), (uint32_t)((rp / LSS) & 1), p.wait_ns, abort_flag))
@@ -517,16 +530,22 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                 decode_q4_word_scaled(v1.z, s1, o + 24);
                 decode_q4_word_scaled(v1.w, s1, o + 28);
             } else {
-                // stage u = chunks 4u .. 4u + 3 of the row, in k order
+                // stage u = chunks 4u .. 4u + 3 of the row, in k order; Q8/32: chunks 0, 1 are
+                // block 2 kb, chunks 2, 3 block 2 kb + 1, each pair times its fp16 block scale
+                // (one rounding of q * fp16(scale))
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint4 v = ld_shared_v4(wrow + (((uint32_t)(4 * u + c) ^ wsw) << 4));
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                    const uint32_t sh2 = FMT == 2 ? prmt(sc0, sc0, c < 2 ? 0x1010u : 0x3232u) : 0u;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         if (XBF) {
                             o[8 * c + 2 * i] = i8x2_to_bf2(wv[i], 0x4140u);
                             o[8 * c + 2 * i + 1] = i8x2_to_bf2(wv[i], 0x4342u);
+                        } else if (FMT == 2) {
+                            o[8 * c + 2 * i] = mul_f16x2(i8x2_to_h2(wv[i], 0x4140u), sh2);
+                            o[8 * c + 2 * i + 1] = mul_f16x2(i8x2_to_h2(wv[i], 0x4342u), sh2);
                         } else {
                             o[8 * c + 2 * i] = i8x2_to_h2(wv[i], 0x4140u);
                             o[8 * c + 2 * i + 1] = i8x2_to_h2(wv[i], 0x4342u);
@@ -578,13 +597,12 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
         // while the last MMAs run.  Outputs and guard scales only after the previous
         // kernel has finished.
         pdl_wait();
-        if (FMT == 0) {
+        if (FMT != 1 || J.rsx) {
             const int64_t tb = (int64_t)t0 + cbase + grp * CW;
-            if (grp < NG && lane < CW && tb + lane < p.T) esc0 = J.rsx[tb + lane];
-            if (grp < NG && CW > 32 && tb + 32 + lane < p.T) esc1 = J.rsx[tb + 32 + lane];
-        } else if (row_ok) {
-            esc0 = J.rs[n];
+            if (grp < NG && lane < CW && tb + lane < p.T) etk0 = J.rsx[tb + lane];
+            if (grp < NG && CW > 32 && tb + 32 + lane < p.T) etk1 = J.rsx[tb + 32 + lane];
         }
+        if (FMT == 1 && row_ok) erow = J.rs[n];
         // the accumulator is complete once the MMA thread's last commit arrives
         if (!*abort_flag && !mbar_wait(accf_bar, 0, p.wait_ns, abort_flag)) give_up();
         tc_fence_after();
@@ -662,14 +680,15 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                 const bool skip = *abort_flag != 0;
 #pragma unroll
                 for (int jj = 0; jj < CH; ++jj) {
-                    // column ci CH + jj of the group: its scale sits in lane (column % 32) of esc0
-                    // (columns 0..31) or esc1 (32..63)
+                    // column ci CH + jj of the group: its token scale sits in lane (column % 32) of
+                    // etk0 (columns 0..31) or etk1 (32..63)
                     const int gc = ci * CH + jj;
-                    const float sx = FMT == 0 ? __shfl_sync(0xffffffffu, gc < 32 ? esc0 : esc1, gc & 31) : esc0;
+                    const float tsc = __shfl_sync(0xffffffffu, gc < 32 ? etk0 : etk1, gc & 31);
                     float acc = __uint_as_float(v[jj]);
                     if (KS > 1) acc += recv[(cc + jj) * 128 + r];
-                    const float val = acc * sx;
                     const int64_t t = tb + jj;
+                    float val = acc * tsc * erow;
+                    if (J.add && row_ok && t < p.T) val += J.add[t * p.N + n];
                     if (GU) {
                         reinterpret_cast<float*>(smem + YST_OFF)[(cc + jj) * 128 + r] = val;
                     } else if (p.y_tma) {
@@ -878,7 +897,7 @@ Params make_params(const TcArgs& a) {
     Params p = {};
     for (int j = 0; j < a.jobs(); ++j) {
         const TcJob jb = a.job(j);
-        p.job[j] = {jb.rsx, jb.rs, jb.ws, jb.y};
+        p.job[j] = {jb.rsx, jb.rs, jb.ws, jb.wsf, jb.add, jb.y};
     }
     p.tiles_y = 1;
     p.ldy = a.ldy > 0 ? a.ldy : a.N;

@@ -149,6 +149,48 @@ cq_status cq_gemm_q4_batched(const void* X, int xt, int64_t T, int64_t K, int64_
                              void* Y, int yt, int64_t ldy, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Format variants
+ *
+ * Q8 per 32-k block ("oxinfer 0.0.5 src/metal.rs", Dequantizers, struct Q8W
+ * and load(Q8W ...)): Wq int8 [N][K], Ws f32 [N][K/32];
+ *   W[n][k] = q[n][k] * Ws[n][k/32].
+ *   T <= 32: the activations as given, int8 -> the activation type exactly,
+ *   the block scale on the f32 result of its block; T > 32 (tcgen05): X to
+ *   fp16 behind the per-row power-of-two guard, each weight q * fp16(scale)
+ *   rounded once to fp16, f32 accumulation, the guard's inverse per token.
+ *   Shape rules: T >= 1, N >= 1, K >= 128, K % 128 == 0.
+ *
+ * Affine Q4 ("oxinfer 0.0.5 src/metal.rs", Dequantizers, struct Q4A and
+ * load(Q4A ...)): the Q4 split plane Wq, Ws plus Wo bf16 [N][K/32/gk], one
+ * offset per group of gk blocks of 32;  W[n][k] = (nibble - 8) * scale +
+ * Wo[n][(k/32)/gk].  Computed as the Q4 GEMM plus the offsets' term
+ * sum_g Wo[n][g] * (sum of X[t] over group g) (f32), added before the
+ * output's rounding.  Shape rules: as cq_gemm_q4, gk >= 1 dividing K/32,
+ * K/32/gk <= 512.
+ *
+ * q8_2f ("cortiq-engine 0.8.3 src/gpu_metal/qi21.rs", module header: int8
+ * weights staged times the column field, the row scale in the epilogue; the
+ * blob q[rows][cols], f16 rs[rows], f16 col[cols] of fn build_block):
+ *   Y[t][n] = rs[n] * sum_k q[n][k] * col[k] * X[t][k]
+ * rs f32 [N] and col f32 [K] (the stored f16 values widened exactly).  X
+ * times the column field goes to fp16 behind the per-row guard; the Q8-row
+ * kernels take it from there with the row scale and the guard's inverse.
+ * Shape rules: as cq_gemm_q8row.
+ *
+ * Each takes a workspace of the size its *_workspace_bytes query returns.
+ * ------------------------------------------------------------------------- */
+size_t cq_gemm_q8b_workspace_bytes(int64_t T, int64_t K);
+cq_status cq_gemm_q8b(const void* X, int xt, int64_t T, int64_t K, const int8_t* Wq, const float* Ws,
+                      int64_t N, void* Y, int yt, void* ws, size_t ws_bytes, void* stream);
+size_t cq_gemm_q4a_workspace_bytes(int64_t T, int64_t K, int64_t N, int64_t gk);
+cq_status cq_gemm_q4a(const void* X, int xt, int64_t T, int64_t K, const uint8_t* Wq, const uint16_t* Ws,
+                      const uint16_t* Wo, int64_t gk, int64_t N, void* Y, int yt, void* ws, size_t ws_bytes,
+                      void* stream);
+size_t cq_gemm_q8_2f_workspace_bytes(int64_t T, int64_t K);
+cq_status cq_gemm_q8_2f(const void* X, int xt, int64_t T, int64_t K, const int8_t* Wq, const float* rs,
+                        const float* col, int64_t N, void* Y, int yt, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Q8-row GEMM:  Y[T][N] = (X[T][K] . Wq[N][K]^T) * rs[N]
  *
  * X: fp16 or bf16 [T][K]; the int8 weights are converted exactly to the

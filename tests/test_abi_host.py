@@ -200,3 +200,17 @@ def test_route_validation(L):
     assert r(lg=None) == 1 and r(w=None) == 1
     assert r(T=0) == 3 and r(E=1025) == 3 and r(k=0) == 3 and r(k=17) == 3 and r(E=100, k=65) == 3 and r(sh=2) == 3
     assert r(lg=FAKE + 2) == 4
+
+
+def test_format_variant_validation(L):
+    q8b = lambda K=512, Ws=FAKE, ws=FAKE, wsb=1 << 30: L.cq_gemm_q8b(FAKE, 1, 16, K, FAKE, Ws, 64, FAKE, 2, ws, wsb, None)
+    assert q8b(Ws=None) == 1 and q8b(K=192) == 3 and q8b(Ws=ODD) == 4 and q8b(wsb=100) == 6
+    q4a = lambda K=512, gk=2, Wo=FAKE, wsb=1 << 30: L.cq_gemm_q4a(FAKE, 1, 16, K, FAKE, FAKE, Wo, gk, 64, FAKE, 2, FAKE,
+                                                                  wsb, None)
+    assert q4a(Wo=None) == 1 and q4a(gk=0) == 3 and q4a(gk=3) == 3 and q4a(K=384) == 3 and q4a(Wo=FAKE + 1) == 4
+    assert q4a(K=65536, gk=1) == 3                                   # 2048 offsets per row > 512
+    need = L.cq_gemm_q4a_workspace_bytes(16, 512, 64, 2)
+    assert need == 16 * 512 * 2 + 256 + 16 * 8 * 4 + 16 * 64 * 4       # guard copy + scales, group sums, offset term
+    assert q4a(wsb=need - 1) == 6
+    q82 = lambda col=FAKE, K=512: L.cq_gemm_q8_2f(FAKE, 1, 16, K, FAKE, FAKE, col, 64, FAKE, 2, FAKE, 1 << 30, None)
+    assert q82(col=None) == 1 and q82(K=200) == 3 and q82(col=ODD) == 4
