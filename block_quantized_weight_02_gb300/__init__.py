@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(_HERE), "include", "cq.h")
 
 CQ_F16, CQ_BF16, CQ_F32 = 0, 1, 2
 CQ_OPT_SMALL_T_MAX, CQ_OPT_FORCE_PATH, CQ_OPT_WAIT_NS, CQ_OPT_TEST_STALL, CQ_OPT_TRACE, CQ_OPT_TC_BN, CQ_OPT_TC_KSPLIT, \
-    CQ_OPT_TC_AMODE, CQ_OPT_TC_PAIR = 0, 1, 2, 3, 4, 5, 6, 7, 8
+    CQ_OPT_TC_AMODE, CQ_OPT_TC_PAIR, CQ_OPT_STREAM_KERNEL = 0, 1, 2, 3, 4, 5, 6, 7, 8, 9
 STATUS = {0: "CQ_OK", 1: "CQ_ERR_NULL", 2: "CQ_ERR_DTYPE", 3: "CQ_ERR_SHAPE", 4: "CQ_ERR_ALIGN",
           5: "CQ_ERR_INDEX", 6: "CQ_ERR_WORKSPACE", 7: "CQ_ERR_CUDA", 8: "CQ_ERR_TIMEOUT", 9: "CQ_ERR_ARCH",
           10: "CQ_ERR_ARG"}

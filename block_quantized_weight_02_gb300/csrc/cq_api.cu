@@ -256,6 +256,10 @@ cq_status cq_set_option(int option, int64_t value) {
             if (value < 0 || value > 2) return fail(CQ_ERR_ARG, "CTA pair mode must be 0, 1 or 2");
             o.tc_pair = value;
             return CQ_OK;
+        case CQ_OPT_STREAM_KERNEL:
+            if (value < 0 || value > 2) return fail(CQ_ERR_ARG, "weight-streaming kernel must be 0, 1 or 2");
+            o.stream_kernel = value;
+            return CQ_OK;
         default:
             return fail(CQ_ERR_ARG, "unknown option %d", option);
     }
@@ -273,6 +277,7 @@ int64_t cq_get_option(int option) {
         case CQ_OPT_TC_KSPLIT: return o.tc_ksplit;
         case CQ_OPT_TC_AMODE: return o.tc_amode;
         case CQ_OPT_TC_PAIR: return o.tc_pair;
+        case CQ_OPT_STREAM_KERNEL: return o.stream_kernel;
         default: return -1;
     }
 }

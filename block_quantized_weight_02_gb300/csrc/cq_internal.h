@@ -26,6 +26,7 @@ struct Options {
     std::atomic<int64_t> tc_ksplit{0};
     std::atomic<int64_t> tc_amode{0};
     std::atomic<int64_t> tc_pair{0};
+    std::atomic<int64_t> stream_kernel{0};
 };
 Options& options();
 
@@ -120,6 +121,10 @@ struct SkinnyDense {
 cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s);
 cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s);    // rsx nullable: per-token scales (q8_2f)
 cudaError_t launch_skinny_q8b(const SkinnyDense& a, cudaStream_t s);   // Q8 per 32-k block, activations as given
+// Row-partitioned weight streaming (k_rows.cu) for T <= 16, one job, K a multiple of the
+// stage (512 for Q4, 256 for Q8); fmt 0 Q4, 1 Q8-row, 2 Q8/32.
+bool rows_path_serves(int fmt, int64_t T, int64_t K, int nz);
+cudaError_t launch_rows(int fmt, const SkinnyDense& a, cudaStream_t s);
 
 struct SkinnyMoe {
     const uint16_t* xh;     // [P][H] fp16 (guarded, streaming order), rows gathered into grouped order

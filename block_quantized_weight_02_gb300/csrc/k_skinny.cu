@@ -996,9 +996,15 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s) { return launch_dense(0, a, s); }
-cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s) { return launch_dense(1, a, s); }
-cudaError_t launch_skinny_q8b(const SkinnyDense& a, cudaStream_t s) { return launch_dense(2, a, s); }
+// Up to 16 activation rows, one job and a whole number of stages: the row-partitioned kernel
+// (k_rows.cu), unless the K-split kernel here is asked for.
+cudaError_t launch_small_t(int fmt, const SkinnyDense& a, cudaStream_t s) {
+    if (options().stream_kernel != 1 && rows_path_serves(fmt, a.T, a.K, a.jobs())) return launch_rows(fmt, a, s);
+    return launch_dense(fmt, a, s);
+}
+cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s) { return launch_small_t(0, a, s); }
+cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s) { return launch_small_t(1, a, s); }
+cudaError_t launch_skinny_q8b(const SkinnyDense& a, cudaStream_t s) { return launch_small_t(2, a, s); }
 
 // Gate/up panels: activations are the guarded rows already gathered into
 // grouped order ([P][H] fp16, inverse scales [P]).  One item is 64 gate rows

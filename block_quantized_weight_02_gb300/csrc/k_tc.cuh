@@ -687,8 +687,9 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                     float acc = __uint_as_float(v[jj]);
                     if (KS > 1) acc += recv[(cc + jj) * 128 + r];
                     const int64_t t = tb + jj;
-                    float val = acc * tsc * erow;
-                    if (J.add && row_ok && t < p.T) val += J.add[t * p.N + n];
+                    float val = acc * tsc;
+                    if (FMT == 1) val *= erow;
+                    if (FMT != 1 && J.add && row_ok && t < p.T) val += J.add[t * p.N + n];
                     if (GU) {
                         reinterpret_cast<float*>(smem + YST_OFF)[(cc + jj) * 128 + r] = val;
                     } else if (p.y_tma) {

@@ -321,9 +321,13 @@ typedef enum {
     CQ_OPT_TC_BN = 5,        /* tcgen05 token tile: 0 auto (default), or 32, 64, 128, 192 (CTA pairs only, no K split), 256 */
     CQ_OPT_TC_KSPLIT = 6,    /* tcgen05 K split over a 2-CTA cluster (partials exchanged in shared memory): 0 auto, 1, 2 */
     CQ_OPT_TC_AMODE = 7,     /* decoded weight operand of the tcgen05 MMA: 0 auto (tensor memory), 1 shared, 2 tensor memory */
-    CQ_OPT_TC_PAIR = 8       /* tcgen05, 256-column tiles with decoded weights in tensor memory: 0 auto / 2 on
+    CQ_OPT_TC_PAIR = 8,      /* tcgen05, 256-column tiles with decoded weights in tensor memory: 0 auto / 2 on
                                 (neighbouring weight-row tiles share one 256-row MMA on a CTA pair, each CTA
                                 loading half of the activation tile; needs an even number of row tiles), 1 off */
+    CQ_OPT_STREAM_KERNEL = 9 /* weight-streaming kernel for T <= 16: 0 auto / 2 the row-partitioned kernel (one
+                                CTA per SM, each streaming the whole K of an equal share of the weight rows) where
+                                it serves (one job, K % 512 == 0 for Q4, K % 256 == 0 for Q8), 1 the K-split
+                                cluster kernel */
 } cq_option;
 /* Process-wide: one value for every thread, stream and device (set before
  * the calls it should affect); reads and writes are atomic, so concurrent

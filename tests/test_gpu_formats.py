@@ -109,3 +109,37 @@ def test_q8_2f(path, T, K, N, out, xdt):
     assert cq.cq_get_device_error() == 0
     yref, S = oracle.gemm_q8_2f(q, rs, col, oracle.x_to_f64(x, xdt))
     check(y_host(Y), yref, S, out, f"q8_2f path={path} T={T} K={K} N={N} {xdt}->{out}")
+
+
+@pytest.mark.parametrize("T", [1, 8, 16])
+@pytest.mark.parametrize("fmt", ["q8b", "q4a", "q8_2f"])
+def test_formats_on_the_row_partitioned_kernel(T, fmt):
+    """The format variants at T <= 16 with K a whole number of stages, so the
+    row-partitioned streaming kernel serves them (Q8/32 decode, the affine
+    addend, q8_2f's guarded activations with per-token scales)."""
+    K, N = 1024, 600
+    rng = np.random.default_rng(9990 + T)
+    x = synth.draw_x(rng, T, K, 1.0, "bf16")
+    X = oracle.x_to_f64(x, "bf16")
+    Y = torch.full((T, N), float("nan"), dtype=torch.float32, device=DEV)
+    if fmt == "q8b":
+        _, q, s = _q8b_case(9991 + T, 1, K, N, "bf16")
+        ws = torch.empty(cq.cq_gemm_q8b_workspace_bytes(T, K), dtype=torch.uint8, device=DEV)
+        cq.cq_gemm_q8b(to_dev_x(x, "bf16"), to_dev(q), to_dev(s), Y, ws)
+        yref, S = oracle.gemm_q8b(q, s, X)
+    elif fmt == "q4a":
+        codes, sc = synth.draw_q4(rng, N, K, signed=True)
+        off = synth.f32_to_bf16_bits(rng.uniform(-0.15, 0.15, (N, K // 64)).astype(np.float32))
+        wq = pack.pack_q4(codes)
+        ws = torch.empty(cq.cq_gemm_q4a_workspace_bytes(T, K, N, 2), dtype=torch.uint8, device=DEV)
+        cq.cq_gemm_q4a(to_dev_x(x, "bf16"), to_dev(wq), to_dev(sc), to_dev(off), 2, Y, ws)
+        yref, S = oracle.gemm_q4a(wq, sc, off, 2, N, K, X)
+    else:
+        q = rng.integers(-127, 128, (N, K)).astype(np.int8)
+        rs = rng.uniform(1e-3, 1e-2, N).astype(np.float16).astype(np.float32)
+        col = rng.uniform(0.25, 4.0, K).astype(np.float16).astype(np.float32)
+        ws = torch.empty(cq.cq_gemm_q8_2f_workspace_bytes(T, K), dtype=torch.uint8, device=DEV)
+        cq.cq_gemm_q8_2f(to_dev_x(x, "bf16"), to_dev(q), to_dev(rs), to_dev(col), Y, ws)
+        yref, S = oracle.gemm_q8_2f(q, rs, col, X)
+    assert cq.cq_get_device_error() == 0
+    check(y_host(Y), yref, S, "f32", f"{fmt} on the row-partitioned kernel T={T}")

@@ -503,3 +503,46 @@ def test_c3_denoiser_block_f32():
     gu, dn = synth.c3()
     _sampled_q4(gu, "f32", count=2000, seed=3)
     _sampled_q4(dn, "f32", count=2000, seed=4)
+
+
+# ---- the row-partitioned weight-streaming kernel (T <= 16) -------------------
+
+@pytest.mark.parametrize("T", [1, 3, 8, 9, 16])
+@pytest.mark.parametrize("K,N", [(512, 8), (1024, 100), (2048, 1001), (4096, 2500), (512, 20000)])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_q4_rows_kernel(T, K, N, xdt):
+    """Units of 8 weight rows spread over one CTA per SM (ragged last unit,
+    fewer units than SMs, several passes of eight units per CTA at N = 20000),
+    the whole K per CTA; f32 output for even T, bf16 for odd."""
+    out = "f32" if T % 2 == 0 else "bf16"
+    case = synth.gemm_q4_case(8400 + T + K + N, T, K, N, x_dtype=xdt, signed=True)
+    with ForcePath(1), _Opt(cq.CQ_OPT_STREAM_KERNEL, 2):
+        Y, wq = run_q4(case, out)
+    yref, S = oracle_q4(case, wq)
+    check(y_host(Y), yref, S, out, f"q4 rows T={T} K={K} N={N} {xdt}")
+
+
+@pytest.mark.parametrize("T", [1, 8, 16])
+@pytest.mark.parametrize("K,N", [(256, 8), (768, 300), (2048, 1001)])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_q8_rows_kernel(T, K, N, xdt):
+    case = synth.gemm_q8_case(8500 + T + K + N, T, K, N, x_dtype=xdt)
+    with ForcePath(1), _Opt(cq.CQ_OPT_STREAM_KERNEL, 2):
+        Y = run_q8(case, "f32")
+    yref, S = oracle_q8(case)
+    check(y_host(Y), yref, S, "f32", f"q8 rows T={T} K={K} N={N} {xdt}")
+
+
+def test_small_t_kernels_agree():
+    """The row-partitioned and the K-split cluster kernels on the same inputs:
+    both within the bound of the oracle (the sums run in different orders)."""
+    case = synth.gemm_q4_case(8600, 8, 4096, 1000, x_dtype="bf16", signed=True)
+    outs = []
+    for kern in (1, 2):
+        with ForcePath(1), _Opt(cq.CQ_OPT_STREAM_KERNEL, kern):
+            Y, wq = run_q4(case, "f32")
+        outs.append(y_host(Y))
+    yref, S = oracle_q4(case, wq)
+    for y in outs:
+        check(y, yref, S, "f32", "small-T kernels")
+    assert np.all(np.abs(outs[0] - outs[1]) <= 4e-3 * S + 2e-6)
