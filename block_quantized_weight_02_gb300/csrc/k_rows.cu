@@ -1,35 +1,40 @@
 // Weight-streaming GEMM for up to 16 activation rows, partitioned by weight
 // rows so that every SM streams the same number of weight bytes.
 //
-// The weight rows are cut into units of 8 (the N = 8 side of mma.sync
-// m16n8k16: weights are the MMA's B operand, the activation rows its A
-// operand, padded to 16), and the units are spread over one CTA per SM as
-// evenly as integers allow (for N = 8192 on 148 SMs: 7 or 6 units, within
-// 1.2 % of the mean).  Each CTA streams the whole K range of its rows, so no
-// partial sums cross CTAs and nothing is reduced afterwards.  Inside a CTA,
-// consumer warp w owns unit w of the current pass (eight units per pass) for
-// every k-block, so no partial sums cross warps either.
+// The weight rows are cut into units of 8 and the units are spread over one
+// CTA per SM as evenly as integers allow (for N = 8192 on 152 SMs: 7 or 6
+// units, within 4 % of the mean).  Each CTA streams the whole K range of its
+// rows, so no partial sums cross CTAs.  Inside a CTA the units come in passes
+// of up to eight (as many passes as needed, units split evenly over them);
+// a pass is four m16 tiles of two units each (the weights are the A operand
+// of mma.sync m16n8k16, the activation rows its n8 B operand), and consumer
+// warp w takes tile w % 4 and the quarter w / 4 of every stage's 32-k blocks.
+// The four quarters' sums of a tile are added in a fixed order at the end of
+// the pass.  A tile whose second unit lies past the CTA's units multiplies
+// whatever its rows 8..15 hold; an MMA's output row depends only on its own A
+// row, and those outputs are not stored.
 //
-// Stages of 512 k (Q4) or 256 k (Q8): for every unit of the pass two 8-row
-// x 128-byte weight boxes (128-byte swizzle: 16-byte chunk j of row r at
-// j ^ r) and, for the block-scaled formats, one 8-row box of scales; one box of
-// the activations {64 k, 8 or 16 rows, stage / 64 slabs}.  Producer lane s
-// issues every copy of the stages that land in ring slot s.
+// Stages of 512 k: weight boxes {128 bytes, the pass's rows} (two for Q4, four
+// for Q8; 128-byte swizzle: 16-byte chunk j of row r at j ^ (r % 8)), for the
+// block-scaled formats one box of scales over the same rows, and one box of
+// the activations {64 k, 8 or 16 rows, 8 slabs} -- at most six boxes per
+// stage, since a TMA box costs about the same however few bytes it holds.
+// Producer lane s issues every copy of the stages that land in ring slot s.
 //
-// Decode (lane c of a quad, row g of its warp's unit): Q4 word c of a 32-k
-// block holds k = 4c .. 4c + 3 (low nibbles) and 16 + 4c .. (high nibbles);
-// adjacent nibbles are paired, so the MMA's virtual k = 2c, 2c + 1, 2c + 8,
-// 2c + 9 are the physical k = 4c .. 4c + 3 (first MMA) and 16 + 4c .. (second),
-// and the activation operand of each MMA is one 8-byte run of a row.  Q8:
-// words c and c + 4 of the block's 32 bytes give the same k.  Every product
-// of the Q4 and Q8 decodes is exact (q - 8, or q, in the activation type); the
-// block scale multiplies the f32 result of the block's two MMAs (Q4, Q8 per
-// 32-k block), the Q8-row scale multiplies the finished sum.
+// Decode (lane c of a quad, rows g and g + 8 of its warp's tile): Q4 word c
+// of a 32-k block holds k = 4c .. 4c + 3 (low nibbles) and 16 + 4c ..
+// (high nibbles); adjacent nibbles are paired, so the MMA's virtual k = 2c,
+// 2c + 1, 2c + 8, 2c + 9 are the physical k = 4c .. 4c + 3 (first MMA) and
+// 16 + 4c .. (second), and the activation operand of each MMA is one 8-byte
+// run of a token's row.  Q8: words c of the block's two 16-byte chunks give
+// the same k.  Every product of the Q4 and Q8 decodes is exact (q - 8, or q,
+// in the activation type); the block scale multiplies the f32 result of the
+// block's two MMAs (Q4, Q8 per 32-k block), the Q8-row scale multiplies the
+// finished sum.
 //
-// The CTA is small (288 threads, at most about 105 KB of shared memory) so
-// that the next call's CTA can be resident beside it: launched with
-// programmatic dependent launch, it requests the weights of its first ring
-// fill before it waits for this kernel, and the activations after.
+// Launched with programmatic dependent launch: the producer requests the
+// weights of its first ring fill before it waits for the previous kernel, and
+// the activations after.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -42,16 +47,22 @@
 namespace cq {
 namespace {
 
-constexpr int RW_CONS = 8;                    // consumer warps: one unit each per pass
+constexpr int UPASS = 8;                      // units per pass at most
+constexpr int TILES = UPASS / 2;              // m16 tiles per pass
+constexpr int PARTS = 4;                      // warps along the k-blocks of a stage
+constexpr int RW_CONS = TILES * PARTS;        // consumer warps
 constexpr int RW_PROD = RW_CONS;              // the producer warp
 constexpr int RW_THREADS = (RW_CONS + 1) * 32;
 constexpr int UNIT = 8;                       // weight rows per unit
+constexpr int KSTAGE = 512;                   // k per stage
 
 struct RParams {
     int64_t N, K, T;
     int units;           // ceil(N / 8)
+    int upp;             // units per pass (the boxes span 8 upp rows)
     int nst;             // stages over K
     const float* rs;     // Q8-row: row scales
+    const float* rsx;    // nullable: per-token scale of the activations (q8_2f: the guard's inverse)
     const float* add;    // nullable f32 [T][N] added before the rounding
     void* y;
     int yt;
@@ -60,8 +71,8 @@ struct RParams {
 };
 
 struct RMaps {
-    CUtensorMap w;       // weights {K bytes, N}, box {128 B, 8 rows}
-    CUtensorMap s;       // Q4: fp16 scales {K/32, N} box {16, 8}; Q8/32: f32 {K/32, N} box {8, 8}
+    CUtensorMap w;       // weights {K bytes, N}, box {128 B, 8 upp rows}
+    CUtensorMap s;       // Q4: fp16 scales {K/32, N} box {16, 8 upp}; Q8/32: f32 {K/32, N} box {8, 8 upp}
     CUtensorMap x;       // activations {64, T, K/64}, box {64, TP, stage/64}
 };
 
@@ -123,13 +134,14 @@ __device__ __forceinline__ void mma_f(float (&d)[4], const uint32_t (&a)[4], uin
 
 template <int FMT>
 struct RGeo {
-    static constexpr int KSTAGE = FMT == 0 ? 512 : 256;       // k per stage
     static constexpr int BPS = KSTAGE / 32;                   // 32-k blocks per stage
+    static constexpr int BPW = BPS / PARTS;                   // ... per warp and stage
     static constexpr int ROWB = FMT == 0 ? KSTAGE / 2 : KSTAGE;   // weight bytes per row and stage
-    static constexpr int NBOX = ROWB / 128;                   // 128-byte boxes per unit and stage (2)
-    static constexpr int W_BYTES = NBOX * RW_CONS * UNIT * 128;
-    static constexpr int S_UNIT = FMT == 1 ? 0 : 256;         // scale box per unit (8 rows x 32 B)
-    static constexpr int S_BYTES = RW_CONS * S_UNIT;
+    static constexpr int NBOX = ROWB / 128;                   // 128-byte weight boxes per stage
+    static constexpr int WBOX = UPASS * UNIT * 128;           // room of one weight box (64 rows)
+    static constexpr int W_BYTES = NBOX * WBOX;
+    static constexpr int S_ROW = FMT == 0 ? 32 : FMT == 2 ? 64 : 0;   // scale bytes per row and stage
+    static constexpr int S_BYTES = UPASS * UNIT * S_ROW;
     static constexpr int XSL = KSTAGE / 64;                   // 64-k slabs per stage
 };
 
@@ -139,20 +151,22 @@ struct RLayout {
     static constexpr int X_BYTES = G::XSL * TP * 128;
     static constexpr int X_OFF = G::W_BYTES + G::S_BYTES;     // 1024-aligned
     static constexpr int SLOT = X_OFF + X_BYTES;
+    static constexpr int RED_BYTES = TILES * (PARTS - 1) * 32 * 8 * 4;   // quarters 1..3 of each tile
     static_assert(G::W_BYTES % 1024 == 0 && X_OFF % 1024 == 0 && SLOT % 1024 == 0, "1024-byte aligned boxes");
 };
 
 // FMT 0: Q4 (fp16 block scales), 1: Q8-row, 2: Q8 per 32-k block (f32 block scales).
-// TP: activation rows of the MMA tile (8: rows g + 8 are zero; 16).  XBF: bf16 activations.
+// TP: activation rows, 8 or 16 (one or two n8 tiles).  XBF: bf16 activations.
 template <int FMT, int TP, int XBF, int NSLOT>
-__global__ void __maxnreg__(112)
+__global__ void __launch_bounds__(RW_THREADS, 1)
 k_rows(const __grid_constant__ RMaps maps, const RParams p) {
     using G = RGeo<FMT>;
     using L = RLayout<FMT, TP>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NSLOT * L::SLOT);
+    float* red = reinterpret_cast<float*>(smem + NSLOT * L::SLOT);   // [TILES][PARTS - 1][32 lanes][8]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NSLOT * L::SLOT + L::RED_BYTES);
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(NSLOT + s); };
@@ -161,10 +175,11 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    // this CTA's units (as even a split as integers allow) and its passes of eight
+    // this CTA's units (as even a split as integers allow) and its passes of upp units
     const int u0 = (int)((int64_t)blockIdx.x * p.units / gridDim.x);
     const int u1 = (int)((int64_t)(blockIdx.x + 1) * p.units / gridDim.x);
-    const int npass = (u1 - u0 + RW_CONS - 1) / RW_CONS;
+    const int upp = p.upp;
+    const int npass = (u1 - u0 + upp - 1) / upp;
     const int nst = p.nst;
 
     if (threadIdx.x == 0) {
@@ -190,24 +205,18 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
                 tma_prefetch_desc(&maps.x);
             }
             const uint32_t base = sb + (uint32_t)(s * L::SLOT);
-            auto issue_w = [&](int pass, int i) {   // weights (and scales) of every unit of the pass
-                const int ub = u0 + pass * RW_CONS, nu = min(RW_CONS, u1 - ub);
-#pragma unroll 1
-                for (int u = 0; u < nu; ++u) {
-                    const int row = (ub + u) * UNIT;
+            // weights (and scales) of the pass: one box per 128-byte column of the stage, over
+            // the pass's 8 upp rows (rows of other CTAs, or past N, in a short pass are loaded
+            // and not used)
+            auto issue_w = [&](int pass, int i) {
+                const int row = (u0 + pass * upp) * UNIT;
 #pragma unroll
-                    for (int q = 0; q < G::NBOX; ++q)
-                        tma_load_2d(base + (uint32_t)((q * RW_CONS + u) * UNIT * 128), &maps.w, full_bar(s),
-                                    i * G::ROWB + q * 128, row);
-                    if (FMT != 1)
-                        tma_load_2d(base + (uint32_t)(G::W_BYTES + u * G::S_UNIT), &maps.s, full_bar(s),
-                                    i * G::BPS, row);
-                }
+                for (int q = 0; q < G::NBOX; ++q)
+                    tma_load_2d(base + (uint32_t)(q * G::WBOX), &maps.w, full_bar(s), i * G::ROWB + q * 128, row);
+                if (FMT != 1) tma_load_2d(base + (uint32_t)G::W_BYTES, &maps.s, full_bar(s), i * G::BPS, row);
             };
-            auto bytes_of = [&](int pass) {
-                const int nu = min(RW_CONS, u1 - (u0 + pass * RW_CONS));
-                return (uint32_t)(nu * (G::NBOX * UNIT * 128 + G::S_UNIT) + L::X_BYTES);
-            };
+            const uint32_t stage_bytes = (uint32_t)(upp * UNIT * (G::NBOX * 128 + G::S_ROW) + L::X_BYTES);
+            auto bytes_of = [&](int) { return stage_bytes; };
             int gi_last = -1;
             bool ok = true;
             int gi = 0;
@@ -244,11 +253,15 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
 
     // ================= consumers =================
     pdl_wait();   // outputs (and the previous kernel's readers of them) only after the previous kernel
+    constexpr int NT = TP / 8;                             // n8 tiles of activation rows
+    const int tile = warp % TILES, part = warp / TILES;    // m16 tile of the pass, quarter of the blocks
     int gi = 0;
     for (int pass = 0; pass < npass; ++pass) {
-        const int unit = u0 + pass * RW_CONS + warp;
-        const bool active = unit < u1;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int ub = u0 + pass * upp, nu = min(upp, u1 - ub);
+        const bool lo_ok = 2 * tile < nu, hi_ok = 2 * tile + 1 < nu;
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
         bool ok = !*abort_flag;
         for (int i = 0; i < nst; ++i, ++gi) {
             const int slot = gi % NSLOT;
@@ -257,72 +270,76 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
                 *abort_flag = 1;
                 atomicCAS(p.err, 0, DEV_TIMEOUT);
             }
-            if (ok && active) {
+            if (ok && lo_ok) {
                 const uint32_t sW = sb + (uint32_t)(slot * L::SLOT);
                 const uint32_t sX = sW + (uint32_t)L::X_OFF;
-                // this lane's weight rows g of the unit: 128-byte rows, chunk j at j ^ g
-                const uint32_t wrow = sW + (uint32_t)((warp * UNIT + g) * 128 + 4 * c);
-                // scales of rows 2c and 2c + 1 of the unit (C-fragment columns): 32 bytes per row,
-                // loaded 16 bytes of each row at a time (8 Q4 blocks, or 4 Q8/32 blocks)
-                const uint32_t srow = sW + (uint32_t)(G::W_BYTES + warp * G::S_UNIT + 2 * c * 32);
-                uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+                // rows g (and g + 8, 1024 bytes on) of the tile: 128-byte rows, chunk j at j ^ g
+                const uint32_t wrow = sW + (uint32_t)((16 * tile + g) * 128 + 4 * c);
+                // block scales of this warp's quarter for rows g and g + 8
+                const uint32_t srow = sW + (uint32_t)(G::W_BYTES + (16 * tile + g) * G::S_ROW);
+                float slo[G::BPW], shi[G::BPW];
+                if (FMT == 0) {
+                    const uint2 a = r_lds64(srow + 8u * (uint32_t)part);
+                    const uint2 b = r_lds64(srow + 8u * G::S_ROW + 8u * (uint32_t)part);
+                    const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
 #pragma unroll
-                for (int jb = 0; jb < G::BPS; ++jb) {
-                    // activations: rows g (and g + 8), slab jb / 2, the 8-byte runs at k 4c (lo) and 16 + 4c (hi)
+                    for (int j = 0; j < G::BPW; ++j) {
+                        slo[j] = __half2float(__ushort_as_half((unsigned short)(j & 1 ? av[j >> 1] >> 16 : av[j >> 1] & 0xFFFFu)));
+                        shi[j] = __half2float(__ushort_as_half((unsigned short)(j & 1 ? bv[j >> 1] >> 16 : bv[j >> 1] & 0xFFFFu)));
+                    }
+                } else if (FMT == 2) {
+                    const uint4 a = r_lds128(srow + 16u * (uint32_t)part);
+                    const uint4 b = r_lds128(srow + 8u * G::S_ROW + 16u * (uint32_t)part);
+                    slo[0] = __uint_as_float(a.x), slo[1] = __uint_as_float(a.y);
+                    slo[2] = __uint_as_float(a.z), slo[3] = __uint_as_float(a.w);
+                    shi[0] = __uint_as_float(b.x), shi[1] = __uint_as_float(b.y);
+                    shi[2] = __uint_as_float(b.z), shi[3] = __uint_as_float(b.w);
+                }
+#pragma unroll
+                for (int jh = 0; jh < G::BPW; ++jh) {
+                    const int jb = part * G::BPW + jh;   // block of the stage
+                    // activations: token g (and g + 8), slab jb / 2, the 8-byte runs at k 4c (lo) and 16 + 4c (hi)
                     const uint32_t slab = (uint32_t)(jb >> 1);
                     const uint32_t clo = (uint32_t)(4 * (jb & 1) + (c >> 1)), off8 = 8u * (uint32_t)(c & 1);
                     const uint32_t xr = sX + (slab * TP + (uint32_t)g) * 128u + off8;
-                    const uint2 lo = r_lds64(xr + ((clo ^ (uint32_t)g) << 4));
-                    const uint2 hi = r_lds64(xr + (((clo + 2u) ^ (uint32_t)g) << 4));
-                    uint2 lo8 = make_uint2(0u, 0u), hi8 = make_uint2(0u, 0u);
-                    if (TP == 16) {
-                        lo8 = r_lds64(xr + 8u * 128u + ((clo ^ (uint32_t)g) << 4));
-                        hi8 = r_lds64(xr + 8u * 128u + (((clo + 2u) ^ (uint32_t)g) << 4));
+                    uint2 xlo[NT], xhi[NT];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        xlo[nt] = r_lds64(xr + 1024u * nt + ((clo ^ (uint32_t)g) << 4));
+                        xhi[nt] = r_lds64(xr + 1024u * nt + (((clo + 2u) ^ (uint32_t)g) << 4));
                     }
-                    const uint32_t a1[4] = {lo.x, lo8.x, lo.y, lo8.y};
-                    const uint32_t a2[4] = {hi.x, hi8.x, hi.y, hi8.y};
-                    uint32_t b[4];
+                    uint32_t a1[4], a2[4];
                     if (FMT == 0) {
-                        q4_adjacent<XBF>(r_lds32(wrow + (((uint32_t)((jb >> 3) * RW_CONS * UNIT * 128)) |
-                                                        ((((uint32_t)(jb & 7) ^ (uint32_t)g)) << 4))), b);
+                        const uint32_t wa = wrow + (uint32_t)((jb >> 3) * G::WBOX) + ((((uint32_t)(jb & 7)) ^ (uint32_t)g) << 4);
+                        uint32_t dl[4], dh[4];
+                        q4_adjacent<XBF>(r_lds32(wa), dl);
+                        q4_adjacent<XBF>(r_lds32(wa + 1024u), dh);
+                        a1[0] = dl[0], a1[1] = dh[0], a1[2] = dl[1], a1[3] = dh[1];
+                        a2[0] = dl[2], a2[1] = dh[2], a2[2] = dl[3], a2[3] = dh[3];
                     } else {
-                        const uint32_t rb = wrow + (uint32_t)((jb >> 2) * RW_CONS * UNIT * 128);
-                        const uint32_t w0 = r_lds32(rb + ((((uint32_t)(2 * (jb & 3))) ^ (uint32_t)g) << 4));
-                        const uint32_t w1 = r_lds32(rb + ((((uint32_t)(2 * (jb & 3) + 1)) ^ (uint32_t)g) << 4));
-                        b[0] = i8_pair<XBF>(w0, 0x4140u);
-                        b[1] = i8_pair<XBF>(w0, 0x4342u);
-                        b[2] = i8_pair<XBF>(w1, 0x4140u);
-                        b[3] = i8_pair<XBF>(w1, 0x4342u);
+                        const uint32_t rb = wrow + (uint32_t)((jb >> 2) * G::WBOX);
+                        const uint32_t o0 = (((uint32_t)(2 * (jb & 3))) ^ (uint32_t)g) << 4;
+                        const uint32_t o1 = (((uint32_t)(2 * (jb & 3) + 1)) ^ (uint32_t)g) << 4;
+                        const uint32_t l0 = r_lds32(rb + o0), l1 = r_lds32(rb + o1);
+                        const uint32_t h0 = r_lds32(rb + 1024u + o0), h1 = r_lds32(rb + 1024u + o1);
+                        a1[0] = i8_pair<XBF>(l0, 0x4140u), a1[1] = i8_pair<XBF>(h0, 0x4140u);
+                        a1[2] = i8_pair<XBF>(l0, 0x4342u), a1[3] = i8_pair<XBF>(h0, 0x4342u);
+                        a2[0] = i8_pair<XBF>(l1, 0x4140u), a2[1] = i8_pair<XBF>(h1, 0x4140u);
+                        a2[2] = i8_pair<XBF>(l1, 0x4342u), a2[3] = i8_pair<XBF>(h1, 0x4342u);
                     }
-                    if (FMT == 1) {
-                        mma_f<XBF>(acc, a1, b[0], b[1]);
-                        mma_f<XBF>(acc, a2, b[2], b[3]);
-                    } else {
-                        float pb[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_f<XBF>(pb, a1, b[0], b[1]);
-                        mma_f<XBF>(pb, a2, b[2], b[3]);
-                        float sa, sbv;   // block jb's scales of rows 2c, 2c + 1
-                        constexpr int PER16 = FMT == 0 ? 8 : 4;   // blocks per 16 bytes of scales
-                        if (jb % PER16 == 0) {
-                            v0 = r_lds128(srow + 16u * (uint32_t)(jb / PER16));
-                            v1 = r_lds128(srow + 32u + 16u * (uint32_t)(jb / PER16));
-                        }
-                        if (FMT == 0) {
-                            const int k = jb & 7;
-                            const uint32_t x0 = (k >> 1) == 0 ? v0.x : (k >> 1) == 1 ? v0.y : (k >> 1) == 2 ? v0.z : v0.w;
-                            const uint32_t x1 = (k >> 1) == 0 ? v1.x : (k >> 1) == 1 ? v1.y : (k >> 1) == 2 ? v1.z : v1.w;
-                            sa = __half2float(__ushort_as_half((unsigned short)((k & 1) ? (x0 >> 16) : (x0 & 0xFFFFu))));
-                            sbv = __half2float(__ushort_as_half((unsigned short)((k & 1) ? (x1 >> 16) : (x1 & 0xFFFFu))));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (FMT == 1) {
+                            mma_f<XBF>(acc[nt], a1, xlo[nt].x, xlo[nt].y);
+                            mma_f<XBF>(acc[nt], a2, xhi[nt].x, xhi[nt].y);
                         } else {
-                            const int k = jb & 3;
-                            sa = __uint_as_float(k == 0 ? v0.x : k == 1 ? v0.y : k == 2 ? v0.z : v0.w);
-                            sbv = __uint_as_float(k == 0 ? v1.x : k == 1 ? v1.y : k == 2 ? v1.z : v1.w);
-                        }
-                        acc[0] = fmaf(sa, pb[0], acc[0]);
-                        acc[1] = fmaf(sbv, pb[1], acc[1]);
-                        if (TP == 16) {
-                            acc[2] = fmaf(sa, pb[2], acc[2]);
-                            acc[3] = fmaf(sbv, pb[3], acc[3]);
+                            float pb[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_f<XBF>(pb, a1, xlo[nt].x, xlo[nt].y);
+                            mma_f<XBF>(pb, a2, xhi[nt].x, xhi[nt].y);
+                            acc[nt][0] = fmaf(slo[jh], pb[0], acc[nt][0]);
+                            acc[nt][1] = fmaf(slo[jh], pb[1], acc[nt][1]);
+                            acc[nt][2] = fmaf(shi[jh], pb[2], acc[nt][2]);
+                            acc[nt][3] = fmaf(shi[jh], pb[3], acc[nt][3]);
                         }
                     }
                 }
@@ -330,50 +347,61 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(slot));
         }
-        // ---- epilogue of this unit: (token g or g + 8, rows 2c and 2c + 1) ----
-        if (ok && active && !*abort_flag) {
-            const int64_t n = (int64_t)unit * UNIT + 2 * c;
-            float sc0 = 1.f, sc1 = 1.f;
-            if (FMT == 1) {
-                if (n < p.N) sc0 = p.rs[n];
-                if (n + 1 < p.N) sc1 = p.rs[n + 1];
-            }
+        // ---- the quarters' sums (quarters 1..3 handed over in shared memory, added in
+        // quarter order), then the epilogue of the tile by its first quarter: lane (g, c)
+        // holds rows g, g + 8 of the tile and tokens 2c, 2c + 1 of each n8 tile ----
+        float* rd = red + ((tile * (PARTS - 1)) * 32 + lane) * 8;
+        if (part > 0) {
 #pragma unroll
-            for (int h = 0; h < (TP == 16 ? 2 : 1); ++h) {
-                const int64_t t = g + 8 * h;
-                if (t >= p.T) continue;
-                float v0 = acc[2 * h] * sc0, v1 = acc[2 * h + 1] * sc1;
-                if (p.add) {
-                    if (n < p.N) v0 += p.add[t * p.N + n];
-                    if (n + 1 < p.N) v1 += p.add[t * p.N + n + 1];
+            for (int nt = 0; nt < NT; ++nt)
+                *reinterpret_cast<float4*>(rd + (part - 1) * 256 + 4 * nt) =
+                    make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(RW_CONS * 32) : "memory");
+        if (part == 0) {
+#pragma unroll
+            for (int q = 0; q < PARTS - 1; ++q) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float4 o = *reinterpret_cast<const float4*>(rd + q * 256 + 4 * nt);
+                    acc[nt][0] += o.x;
+                    acc[nt][1] += o.y;
+                    acc[nt][2] += o.z;
+                    acc[nt][3] += o.w;
                 }
-                if (p.yt == CQ_F32) {
-                    float* yr = reinterpret_cast<float*>(p.y) + t * p.N;
-                    if (n + 1 < p.N && (p.N & 1) == 0) {
-                        *reinterpret_cast<float2*>(yr + n) = make_float2(v0, v1);
-                    } else {
-                        if (n < p.N) yr[n] = v0;
-                        if (n + 1 < p.N) yr[n + 1] = v1;
-                    }
-                } else {
-                    __nv_bfloat16* yr = reinterpret_cast<__nv_bfloat16*>(p.y) + t * p.N;
-                    if (n + 1 < p.N && (p.N & 1) == 0) {
-                        *reinterpret_cast<__nv_bfloat162*>(yr + n) = __floats2bfloat162_rn(v0, v1);
-                    } else {
-                        if (n < p.N) yr[n] = __float2bfloat16_rn(v0);
-                        if (n + 1 < p.N) yr[n + 1] = __float2bfloat16_rn(v1);
+            }
+        }
+        if (part == 0 && ok && lo_ok && !*abort_flag) {
+            const int64_t n0 = (int64_t)(ub + 2 * tile) * UNIT + g;   // row g; row g + 8 is n0 + 8
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int64_t n = n0 + 8 * hr;
+                if ((hr == 1 && !hi_ok) || n >= p.N) continue;
+                const float sc = FMT == 1 ? p.rs[n] : 1.f;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int64_t t = 8 * nt + 2 * c + e;
+                        if (t >= p.T) continue;
+                        float v = acc[nt][2 * hr + e] * sc;
+                        if (p.rsx) v *= p.rsx[t];
+                        if (p.add) v += p.add[t * p.N + n];
+                        if (p.yt == CQ_F32) reinterpret_cast<float*>(p.y)[t * p.N + n] = v;
+                        else reinterpret_cast<__nv_bfloat16*>(p.y)[t * p.N + n] = __float2bfloat16_rn(v);
                     }
                 }
             }
         }
+        asm volatile("bar.sync 1, %0;" ::"n"(RW_CONS * 32) : "memory");   // the hand-over memory is free again
     }
 }
 
 template <int FMT, int TP, int XBF, int NSLOT>
 cudaError_t launch_rows_t(const RMaps& maps, const RParams& p, int grid, cudaStream_t s) {
     using L = RLayout<FMT, TP>;
-    constexpr size_t smem = (size_t)NSLOT * L::SLOT + 2 * NSLOT * 8 + 16 + 1024;
-    static_assert(smem <= 113 * 1024, "two CTAs per SM: the next call's CTA fits beside this one");
+    constexpr size_t smem = (size_t)NSLOT * L::SLOT + L::RED_BYTES + 2 * NSLOT * 8 + 16 + 1024;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
     auto kern = k_rows<FMT, TP, XBF, NSLOT>;
     static int configured_device = -1;   // attributes are per device; set once per instantiation
     int dev = 0;
@@ -400,20 +428,32 @@ cudaError_t launch_rows_t(const RMaps& maps, const RParams& p, int grid, cudaStr
 
 template <int FMT, int XBF>
 cudaError_t launch_rows_x(const RMaps& maps, const RParams& p, int grid, int64_t T, cudaStream_t s) {
-    // ring depth: as many stages as fit beside the next call's CTA
-    if (T <= 8) return launch_rows_t<FMT, 8, XBF, FMT == 0 ? 4 : 4>(maps, p, grid, s);
-    return launch_rows_t<FMT, 16, XBF, FMT == 0 ? 3 : 4>(maps, p, grid, s);
+    // ring depth: as many 512-k stages as fit (Q4 26 / 34 KB, Q8-row 40 / 48 KB, Q8/32 44 / 52 KB
+    // for 8 / 16 activation rows)
+    if (T <= 8) return launch_rows_t<FMT, 8, XBF, FMT == 0 ? 8 : FMT == 1 ? 5 : 4>(maps, p, grid, s);
+    return launch_rows_t<FMT, 16, XBF, FMT == 0 ? 6 : 4>(maps, p, grid, s);
 }
 
 }  // namespace
 
 bool rows_path_serves(int fmt, int64_t T, int64_t K, int nz) {
-    return nz <= 1 && T >= 1 && T <= 16 && K % (fmt == 0 ? 512 : 256) == 0;
+    (void)fmt;
+    return nz <= 1 && T >= 1 && T <= 16 && K % KSTAGE == 0;
+}
+
+bool rows_path_preferred(int fmt, int64_t T, int64_t K, int64_t N, int nz) {
+    if (!rows_path_serves(fmt, T, K, nz)) return false;
+    // measured on GB300 (T = 1, 8, 16; Q4 and Q8-row): faster than the K-split kernel, or level
+    // with it, when every CTA holds 6 to 8 units in one pass (at least three full tiles); with
+    // fewer units (idle warps) or two passes the K-split kernel was faster
+    const int64_t units = (N + UNIT - 1) / UNIT, grid = std::min<int64_t>((int64_t)num_sms(), units);
+    const int64_t maxu = (units + grid - 1) / grid;
+    return maxu >= 6 && maxu <= UPASS;
 }
 
 cudaError_t launch_rows(int fmt, const SkinnyDense& a, cudaStream_t s) {
     constexpr int TPX = 16;   // the activation box spans the padded rows; TMA fills the ones past T with zeros
-    const int64_t kstage = fmt == 0 ? 512 : 256;
+    const int64_t kstage = KSTAGE;
     RParams p = {};
     p.N = a.N;
     p.K = a.K;
@@ -421,31 +461,36 @@ cudaError_t launch_rows(int fmt, const SkinnyDense& a, cudaStream_t s) {
     p.units = (int)((a.N + UNIT - 1) / UNIT);
     p.nst = (int)(a.K / kstage);
     p.rs = a.rs;
+    p.rsx = a.rsx;
     p.add = a.add;
     p.y = a.y;
     p.yt = a.yt;
     p.wait_ns = (uint64_t)options().wait_ns;
     p.err = a.err;
+    const int grid = (int)std::min<int64_t>((int64_t)num_sms(), p.units);
+    // units per pass: the most units a CTA holds, split evenly over as few passes of <= 8 as needed
+    const int maxu = (p.units + grid - 1) / grid, np = (maxu + UPASS - 1) / UPASS;
+    p.upp = (maxu + np - 1) / np;
     RMaps maps;
     memset(&maps, 0, sizeof maps);
     const uint64_t kbytes = fmt == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
     {
         uint64_t d[2] = {kbytes, (uint64_t)a.N};
         uint64_t st[1] = {kbytes};
-        uint32_t box[2] = {128, UNIT};
+        uint32_t box[2] = {128, (uint32_t)(UNIT * p.upp)};
         if (!encode_tiled(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.wq, d, st, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
     if (fmt == 0) {
         uint64_t d[2] = {(uint64_t)a.K / 32, (uint64_t)a.N};
         uint64_t st[1] = {(uint64_t)a.K / 32 * 2};
-        uint32_t box[2] = {16, UNIT};
+        uint32_t box[2] = {16, (uint32_t)(UNIT * p.upp)};
         if (!encode_tiled(&maps.s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, a.ws, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     } else if (fmt == 2) {
         uint64_t d[2] = {(uint64_t)a.K / 32, (uint64_t)a.N};
         uint64_t st[1] = {(uint64_t)a.K / 32 * 4};
-        uint32_t box[2] = {8, UNIT};
+        uint32_t box[2] = {16, (uint32_t)(UNIT * p.upp)};
         if (!encode_tiled(&maps.s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.wsf, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
@@ -460,10 +505,9 @@ cudaError_t launch_rows(int fmt, const SkinnyDense& a, cudaStream_t s) {
                           d, st, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
-    const int grid = (int)std::min<int64_t>((int64_t)num_sms(), p.units);
     if (options().trace)
-        fprintf(stderr, "cq: rows fmt=%d T=%lld N=%lld K=%lld units=%d grid=%d\n", fmt, (long long)a.T,
-                (long long)a.N, (long long)a.K, p.units, grid);
+        fprintf(stderr, "cq: rows fmt=%d T=%lld N=%lld K=%lld units=%d per pass=%d grid=%d\n", fmt, (long long)a.T,
+                (long long)a.N, (long long)a.K, p.units, p.upp, grid);
     if (fmt == 0) return a.x_bf16 ? launch_rows_x<0, 1>(maps, p, grid, a.T, s) : launch_rows_x<0, 0>(maps, p, grid, a.T, s);
     if (fmt == 1) return a.x_bf16 ? launch_rows_x<1, 1>(maps, p, grid, a.T, s) : launch_rows_x<1, 0>(maps, p, grid, a.T, s);
     return a.x_bf16 ? launch_rows_x<2, 1>(maps, p, grid, a.T, s) : launch_rows_x<2, 0>(maps, p, grid, a.T, s);

@@ -999,7 +999,9 @@ cudaError_t launch_dense(int fmt, const SkinnyDense& a, cudaStream_t s) {
 // Up to 16 activation rows, one job and a whole number of stages: the row-partitioned kernel
 // (k_rows.cu), unless the K-split kernel here is asked for.
 cudaError_t launch_small_t(int fmt, const SkinnyDense& a, cudaStream_t s) {
-    if (options().stream_kernel != 1 && rows_path_serves(fmt, a.T, a.K, a.jobs())) return launch_rows(fmt, a, s);
+    const int64_t sk = options().stream_kernel;
+    if (sk == 2 ? rows_path_serves(fmt, a.T, a.K, a.jobs()) : sk == 0 && rows_path_preferred(fmt, a.T, a.K, a.N, a.jobs()))
+        return launch_rows(fmt, a, s);
     return launch_dense(fmt, a, s);
 }
 cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s) { return launch_small_t(0, a, s); }

@@ -670,6 +670,9 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             const float* recv = reinterpret_cast<const float*>(smem + RECV_OFF);
             const bool f32 = p.yt == CQ_F32;
             const int esz = f32 ? 4 : 2;
+            // the addend (affine offset term) only where a format uses it: its loads stay out of
+            // the loop that stages the outputs
+            const float* addp = (FMT != 1 && !GU && row_ok) ? J.add : nullptr;
 #pragma unroll 1
             for (int ci = 0; ci < CW / CH; ++ci) {
                 const int cc = grp * CW + ci * CH;
@@ -678,6 +681,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                 tmem_ld_wait();
                 const int64_t tb = (int64_t)t0 + cbase + cc;
                 const bool skip = *abort_flag != 0;
+                float vals[CH];
 #pragma unroll
                 for (int jj = 0; jj < CH; ++jj) {
                     // column ci CH + jj of the group: its token scale sits in lane (column % 32) of
@@ -686,10 +690,18 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                     const float tsc = __shfl_sync(0xffffffffu, gc < 32 ? etk0 : etk1, gc & 31);
                     float acc = __uint_as_float(v[jj]);
                     if (KS > 1) acc += recv[(cc + jj) * 128 + r];
+                    vals[jj] = acc * tsc;
+                    if (FMT == 1) vals[jj] *= erow;
+                }
+                if (addp) {
+#pragma unroll
+                    for (int jj = 0; jj < CH; ++jj)
+                        if (tb + jj < p.T) vals[jj] += addp[(tb + jj) * p.N + n];
+                }
+#pragma unroll
+                for (int jj = 0; jj < CH; ++jj) {
                     const int64_t t = tb + jj;
-                    float val = acc * tsc;
-                    if (FMT == 1) val *= erow;
-                    if (FMT != 1 && J.add && row_ok && t < p.T) val += J.add[t * p.N + n];
+                    const float val = vals[jj];
                     if (GU) {
                         reinterpret_cast<float*>(smem + YST_OFF)[(cc + jj) * 128 + r] = val;
                     } else if (p.y_tma) {

@@ -133,3 +133,27 @@ class ForcePath:
 
     def __exit__(self, *a):
         cq.cq_set_option(cq.CQ_OPT_FORCE_PATH, self.old)
+
+
+class Opt:
+    """Context manager setting one library option for the duration."""
+
+    def __init__(self, opt, value):
+        self.opt, self.value = opt, value
+
+    def __enter__(self):
+        self.old = cq.cq_get_option(self.opt)
+        cq.cq_set_option(self.opt, self.value)
+
+    def __exit__(self, *a):
+        cq.cq_set_option(self.opt, self.old)
+
+
+def traced_kernels(capfd, fn):
+    """Runs fn() with the library's launch trace on; returns the trace lines
+    (the library writes them to the process's standard error)."""
+    capfd.readouterr()
+    with Opt(cq.CQ_OPT_TRACE, 1):
+        fn()
+        torch.cuda.synchronize()
+    return [l for l in capfd.readouterr().err.splitlines() if l.startswith("cq:")]

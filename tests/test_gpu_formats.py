@@ -11,7 +11,7 @@ import oracle
 import block_quantized_weight_02_gb300 as cq
 from block_quantized_weight_02_gb300 import pack, synth
 
-from cqtest import DEV, ForcePath, TORCH_DT, check, to_dev, to_dev_x, y_host
+from cqtest import DEV, ForcePath, Opt, TORCH_DT, check, to_dev, to_dev_x, traced_kernels, y_host
 
 pytestmark = pytest.mark.gpu
 
@@ -113,10 +113,16 @@ def test_q8_2f(path, T, K, N, out, xdt):
 
 @pytest.mark.parametrize("T", [1, 8, 16])
 @pytest.mark.parametrize("fmt", ["q8b", "q4a", "q8_2f"])
-def test_formats_on_the_row_partitioned_kernel(T, fmt):
-    """The format variants at T <= 16 with K a whole number of stages, so the
-    row-partitioned streaming kernel serves them (Q8/32 decode, the affine
-    addend, q8_2f's guarded activations with per-token scales)."""
+def test_formats_on_the_row_partitioned_kernel(T, fmt, capfd):
+    """The format variants at T <= 16 with K a whole number of stages on the
+    row-partitioned streaming kernel (Q8/32 decode, the affine addend, q8_2f's
+    guarded activations with per-token scales)."""
+    with Opt(cq.CQ_OPT_STREAM_KERNEL, 2):
+        trace = traced_kernels(capfd, lambda: _formats_rows(T, fmt))
+    assert any(l.startswith("cq: rows") for l in trace), trace
+
+
+def _formats_rows(T, fmt):
     K, N = 1024, 600
     rng = np.random.default_rng(9990 + T)
     x = synth.draw_x(rng, T, K, 1.0, "bf16")

@@ -9,7 +9,7 @@ import block_quantized_weight_02_gb300 as cq
 from block_quantized_weight_02_gb300 import pack, synth
 
 from cqtest import (DEV, ForcePath, check, oracle_q4, oracle_q8, run_q4, run_q8, sample_positions, to_dev,
-                    to_dev_x, y_host)
+                    to_dev_x, traced_kernels, y_host)
 from test_oracle import _golden_blocks
 
 pytestmark = pytest.mark.gpu
@@ -510,27 +510,32 @@ def test_c3_denoiser_block_f32():
 @pytest.mark.parametrize("T", [1, 3, 8, 9, 16])
 @pytest.mark.parametrize("K,N", [(512, 8), (1024, 100), (2048, 1001), (4096, 2500), (512, 20000)])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
-def test_q4_rows_kernel(T, K, N, xdt):
-    """Units of 8 weight rows spread over one CTA per SM (ragged last unit,
-    fewer units than SMs, several passes of eight units per CTA at N = 20000),
-    the whole K per CTA; f32 output for even T, bf16 for odd."""
+def test_q4_rows_kernel(T, K, N, xdt, capfd):
+    """Units of 8 weight rows spread over one CTA per SM (ragged last unit, a
+    tile with one unit, fewer units than SMs, several passes of eight units per
+    CTA at N = 20000), the whole K per CTA; f32 output for even T, bf16 for odd."""
     out = "f32" if T % 2 == 0 else "bf16"
     case = synth.gemm_q4_case(8400 + T + K + N, T, K, N, x_dtype=xdt, signed=True)
+    res = {}
     with ForcePath(1), _Opt(cq.CQ_OPT_STREAM_KERNEL, 2):
-        Y, wq = run_q4(case, out)
+        trace = traced_kernels(capfd, lambda: res.update(r=run_q4(case, out)))
+    assert any(l.startswith("cq: rows") for l in trace), trace
+    Y, wq = res["r"]
     yref, S = oracle_q4(case, wq)
     check(y_host(Y), yref, S, out, f"q4 rows T={T} K={K} N={N} {xdt}")
 
 
 @pytest.mark.parametrize("T", [1, 8, 16])
-@pytest.mark.parametrize("K,N", [(256, 8), (768, 300), (2048, 1001)])
+@pytest.mark.parametrize("K,N", [(512, 8), (1536, 300), (2048, 1001), (512, 20000)])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
-def test_q8_rows_kernel(T, K, N, xdt):
+def test_q8_rows_kernel(T, K, N, xdt, capfd):
     case = synth.gemm_q8_case(8500 + T + K + N, T, K, N, x_dtype=xdt)
+    res = {}
     with ForcePath(1), _Opt(cq.CQ_OPT_STREAM_KERNEL, 2):
-        Y = run_q8(case, "f32")
+        trace = traced_kernels(capfd, lambda: res.update(Y=run_q8(case, "f32")))
+    assert any(l.startswith("cq: rows") for l in trace), trace
     yref, S = oracle_q8(case)
-    check(y_host(Y), yref, S, "f32", f"q8 rows T={T} K={K} N={N} {xdt}")
+    check(y_host(res["Y"]), yref, S, "f32", f"q8 rows T={T} K={K} N={N} {xdt}")
 
 
 def test_small_t_kernels_agree():
