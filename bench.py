@@ -63,12 +63,26 @@ def _peaks():
 # ---------------------------------------------------------------------------
 
 class Call:
-    """One C-ABI call with its algorithmic work and the buffers it reads and writes."""
+    """One C-ABI call with its algorithmic work and the buffers it reads and writes.
+    Its kernel launches are counted by the library (cq_last_launches) when the call
+    runs through run_counted(); `counter` replaces that for a step of several
+    library calls (it runs them and returns their launches)."""
 
-    def __init__(self, name, fn, flops, weight_bytes, other_bytes, launches, h2d=(), d2h=()):
+    def __init__(self, name, fn, flops, weight_bytes, other_bytes, h2d=(), d2h=(), counter=None):
         self.name, self.fn, self.flops = name, fn, flops
-        self.weight_bytes, self.other_bytes, self.launches = weight_bytes, other_bytes, launches
+        self.weight_bytes, self.other_bytes = weight_bytes, other_bytes
+        self.launches = None
         self.h2d, self.d2h = list(h2d), list(d2h)
+        self.counter = counter
+
+    def run_counted(self):
+        import block_quantized_weight_02_gb300 as cq
+        if self.counter is not None:
+            self.launches = int(self.counter())
+        else:
+            self.fn()
+            self.launches = int(cq.cq_last_launches())
+        return self.launches
 
 
 def _dev_x(x_bits, dtype, dev):
@@ -96,7 +110,6 @@ def _q4_calls(cq, case, outs, dev, tag):
         Y = torch.empty(T, N, dtype=torch.float32 if out == "f32" else torch.bfloat16, device=dev)
         calls.append(Call(f"{tag} q4->{out}", (lambda X=X, Wq=Wq, Ws=Ws, Y=Y, ws=ws: cq.cq_gemm_q4(X, Wq, Ws, Y, ws)),
                           2.0 * T * N * K, wbytes, X.numel() * 2 + Y.numel() * Y.element_size(),
-                          1 if T <= 32 else 2,   # weight-streaming path: one kernel; tcgen05: guard pass + GEMM
                           h2d=[X], d2h=[Y]))
     return calls
 
@@ -111,7 +124,7 @@ def _q8_calls(cq, case, outs, dev, tag):
     for out in outs:
         Y = torch.empty(T, N, dtype=torch.float32 if out == "f32" else torch.bfloat16, device=dev)
         calls.append(Call(f"{tag} q8row->{out}", (lambda X=X, Wq=Wq, rs=rs, Y=Y: cq.cq_gemm_q8row(X, Wq, rs, Y)),
-                          2.0 * T * N * K, N * K + 4 * N, X.numel() * 2 + Y.numel() * Y.element_size(), 1,
+                          2.0 * T * N * K, N * K + 4 * N, X.numel() * 2 + Y.numel() * Y.element_size(),
                           h2d=[X], d2h=[Y]))
     return calls
 
@@ -133,7 +146,7 @@ def _moe_calls(cq, m, dev):
     per_expert = (2 * I * H + H * I) * 9 // 16
     flops = T * topk * (2.0 * H * 2 * I + 2.0 * I * H)
     return [Call("moe panels", lambda: cq.cq_moe_panels(X, idx, w, guq, gus, dq, ds, Y, ws), flops,
-                 touched * per_expert, X.numel() * 2 + Y.numel() * 4 + idx.numel() * 8, 5,
+                 touched * per_expert, X.numel() * 2 + Y.numel() * 4 + idx.numel() * 8,
                  h2d=[X, idx, w], d2h=[Y])], touched
 
 
@@ -152,7 +165,7 @@ def _ffn_calls(cq, gu, dn, dev):
     ws = torch.empty(cq.cq_ffn_q4_workspace_bytes(T, H, I), dtype=torch.uint8, device=dev)
     wbytes = (2 * I * H + H * I) * 9 // 16
     return [Call("ffn chain q4->bf16", lambda: cq.cq_ffn_q4(X, guq, gus, dq, ds, Y, ws),
-                 2.0 * T * (2 * I * H + H * I), wbytes, X.numel() * 2 + Y.numel() * 2, 4,
+                 2.0 * T * (2 * I * H + H * I), wbytes, X.numel() * 2 + Y.numel() * 2,
                  h2d=[X], d2h=[Y])]
 
 
@@ -179,8 +192,14 @@ def _moe_routed_calls(cq, m, dev):
     def fn():
         cq.cq_moe_route(lg, topk, idx, w)
         cq.cq_moe_panels(X, idx, w, guq, gus, dq, ds, Y, ws)
+
+    def counter():
+        cq.cq_moe_route(lg, topk, idx, w)
+        n = cq.cq_last_launches()
+        cq.cq_moe_panels(X, idx, w, guq, gus, dq, ds, Y, ws)
+        return n + cq.cq_last_launches()
     return [Call("route + moe panels", fn, flops, touched * per_expert, X.numel() * 2 + Y.numel() * 4 + lg.numel() * 4,
-                 6, h2d=[X, lg], d2h=[Y])], touched
+                 h2d=[X, lg], d2h=[Y], counter=counter)], touched
 
 
 def _dtype_of(name, info):
@@ -384,6 +403,10 @@ def time_calls(rot, sets, reps, stream, use_graph):
     import torch
     out = []
     for j in range(len(rot[0])):
+        n = rot[0][j].run_counted()   # one more untimed call: its kernel launches, as the library counts them
+        torch.cuda.synchronize()
+        for calls in rot:
+            calls[j].launches = n
         g = None
         if use_graph:
             g = torch.cuda.CUDAGraph()
@@ -419,7 +442,7 @@ def traffic_pass(args, dev):
         for c in calls:
             c.fn()
             torch.cuda.synchronize()
-            c.fn()
+            c.run_counted()
             torch.cuda.synchronize()
             print(f"traffic-pass\t{name}\t{c.name}\t{c.launches}", flush=True)
         if cq.cq_get_device_error() != 0:
@@ -437,6 +460,7 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    cq.cq_set_option(cq.CQ_OPT_STREAM_KERNEL, args.stream_kernel)
     if args.traffic_pass:
         traffic_pass(args, dev)
         return
@@ -594,7 +618,7 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": _dtype_of(args.workload, info), "data": "synthetic (seeded)",
         "config": {"workload": args.workload, **info, "parallelism": f"replicas x{world}",
-                   "timing": timing,
+                   "timing": timing, **({"stream_kernel": args.stream_kernel} if args.stream_kernel else {}),
                    "l2": f"rotating {sets} input sets ({sets * sum(c.weight_bytes + c.other_bytes for c in calls) / 2**20:.0f} MiB) > L2"},
         "weight_gbs": round(wgbs, 1),
         "per_call_ms": {c.name: round(t, 5) for c, t in zip(calls, per_call_ms)},
@@ -748,6 +772,9 @@ def main():
     ap.add_argument("--configs", default="all", help="comma-separated workloads for --traffic-pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time direct calls instead of a captured CUDA graph")
+    ap.add_argument("--stream-kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="weight-streaming kernel for T <= 16 (CQ_OPT_STREAM_KERNEL): 0 the library's default, "
+                         "1 K-split, 2 row-partitioned")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

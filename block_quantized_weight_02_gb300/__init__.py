@@ -52,6 +52,7 @@ _SIGS = {
     "cq_dequant_q8row": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p]),
     "cq_get_device_error": (_c_int, [_c_p]),
     "cq_last_error": (ctypes.c_char_p, []),
+    "cq_last_launches": (_c_int, []),
     "cq_set_option": (_c_int, [_c_int, _c_i64]),
     "cq_get_option": (_c_i64, [_c_int]),
     "cq_version": (_c_int, []),
@@ -268,6 +269,11 @@ def cq_get_device_error(stream=None) -> int:
 
 def cq_last_error() -> str:
     return lib().cq_last_error().decode(errors="replace")
+
+
+def cq_last_launches() -> int:
+    """Kernel launches of the calling thread's most recent library call."""
+    return lib().cq_last_launches()
 
 
 def cq_set_option(option: int, value: int):

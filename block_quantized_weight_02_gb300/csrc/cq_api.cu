@@ -30,7 +30,17 @@ cq_status fail(cq_status st, const char* fmt, ...) {
     return st;
 }
 
-void clear_last_error() { g_msg[0] = 0; }
+static thread_local int g_launches = 0;   // kernel launches of the thread's current entry-point call
+
+void clear_last_error() {
+    g_msg[0] = 0;
+    g_launches = 0;
+}
+cudaError_t counted(cudaError_t e) {
+    if (e == cudaSuccess) ++g_launches;
+    return e;
+}
+int launches_so_far() { return g_launches; }
 
 cq_status cuda_fail(cudaError_t e, const char* what) {
     return fail(CQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -217,6 +227,7 @@ extern "C" {
 int cq_version(void) { return 100; }
 
 const char* cq_last_error(void) { return g_msg; }
+int cq_last_launches(void) { return launches_so_far(); }
 
 cq_status cq_set_option(int option, int64_t value) {
     Options& o = options();
@@ -289,7 +300,7 @@ size_t cq_gemm_q4_workspace_bytes(int64_t T, int64_t K) {
 
 cq_status cq_gemm_q4(const void* X, int xt, int64_t T, int64_t K, const uint8_t* Wq, const uint16_t* Ws, int64_t N,
                      void* Y, int yt, void* ws, size_t ws_bytes, void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!X || !Wq || !Ws || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q4: null pointer");
     cq_status st;
     if ((st = check_x(xt)) || (st = check_y(yt))) return st;
@@ -315,7 +326,7 @@ cq_status cq_gemm_q4(const void* X, int xt, int64_t T, int64_t K, const uint8_t*
 
 cq_status cq_gemm_q8row(const void* X, int xt, int64_t T, int64_t K, const int8_t* Wq, const float* rs, int64_t N,
                         void* Y, int yt, void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!X || !Wq || !rs || !Y) return fail(CQ_ERR_NULL, "cq_gemm_q8row: null pointer");
     cq_status st;
     if ((st = check_x(xt)) || (st = check_y(yt))) return st;
@@ -344,7 +355,7 @@ cq_status cq_moe_panels(const void* X, int xt, int64_t T, int64_t H, int64_t E, 
                         const int32_t* idx, const float* w, const uint8_t* Wgu_q, const uint16_t* Wgu_s,
                         const uint8_t* Wd_q, const uint16_t* Wd_s, void* Y, int yt, void* ws, size_t ws_bytes,
                         void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!X || !idx || !w || !Wgu_q || !Wgu_s || !Wd_q || !Wd_s || !Y || !ws) return fail(CQ_ERR_NULL, "cq_moe_panels: null pointer");
     cq_status st;
     if ((st = check_x(xt)) || (st = check_y(yt))) return st;
@@ -409,7 +420,7 @@ size_t cq_gemm_q4_batched_workspace_bytes(int64_t T, int64_t K, int z) {
 
 cq_status cq_gemm_q4_batched(const void* X, int xt, int64_t T, int64_t K, int64_t ldx, const cq_q4_job* jobs, int z,
                              int64_t N, void* Y, int yt, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!X || !jobs || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q4_batched: null pointer");
     if (z < 1 || z > ZMAX) return fail(CQ_ERR_ARG, "cq_gemm_q4_batched: z must be in [1, %d] (got %d)", ZMAX, z);
     cq_status st;
@@ -504,7 +515,7 @@ size_t cq_gemm_q4a_workspace_bytes(int64_t T, int64_t K, int64_t N, int64_t gk) 
 
 cq_status cq_gemm_q8_2f(const void* X, int xt, int64_t T, int64_t K, const int8_t* Wq, const float* rs, const float* col,
                         int64_t N, void* Y, int yt, void* ws, size_t ws_bytes, void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!X || !Wq || !rs || !col || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q8_2f: null pointer");
     cq_status st;
     if ((st = check_x(xt)) || (st = check_y(yt))) return st;
@@ -535,7 +546,7 @@ cq_status cq_gemm_q8_2f(const void* X, int xt, int64_t T, int64_t K, const int8_
 
 cq_status cq_gemm_q8b(const void* X, int xt, int64_t T, int64_t K, const int8_t* Wq, const float* Ws, int64_t N,
                       void* Y, int yt, void* ws, size_t ws_bytes, void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!X || !Wq || !Ws || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q8b: null pointer");
     cq_status st;
     if ((st = check_x(xt)) || (st = check_y(yt))) return st;
@@ -567,7 +578,7 @@ cq_status cq_gemm_q8b(const void* X, int xt, int64_t T, int64_t K, const int8_t*
 cq_status cq_gemm_q4a(const void* X, int xt, int64_t T, int64_t K, const uint8_t* Wq, const uint16_t* Ws,
                       const uint16_t* Wo, int64_t gk, int64_t N, void* Y, int yt, void* ws, size_t ws_bytes,
                       void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!X || !Wq || !Ws || !Wo || !Y || !ws) return fail(CQ_ERR_NULL, "cq_gemm_q4a: null pointer");
     cq_status st;
     if ((st = check_x(xt)) || (st = check_y(yt))) return st;
@@ -610,7 +621,7 @@ size_t cq_ffn_q4_workspace_bytes(int64_t T, int64_t H, int64_t I) {
 cq_status cq_ffn_q4(const void* X, int xt, int64_t T, int64_t H, int64_t I, const uint8_t* Wgu_q,
                     const uint16_t* Wgu_s, const uint8_t* Wd_q, const uint16_t* Wd_s, void* Y, int yt, void* ws,
                     size_t ws_bytes, void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!X || !Wgu_q || !Wgu_s || !Wd_q || !Wd_s || !Y || !ws) return fail(CQ_ERR_NULL, "cq_ffn_q4: null pointer");
     cq_status st;
     if ((st = check_x(xt)) || (st = check_y(yt))) return st;
@@ -644,7 +655,7 @@ cq_status cq_ffn_q4(const void* X, int xt, int64_t T, int64_t H, int64_t I, cons
 
 cq_status cq_moe_route(const float* logits, int64_t T, int64_t E, int64_t topk, int shared, int32_t* idx, float* w,
                        void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!logits || !idx || !w) return fail(CQ_ERR_NULL, "cq_moe_route: null pointer");
     if (T < 1 || T > (1LL << 31) - 1 || E < 1 || E > 1024 || topk < 1 || topk > 64 || topk > E ||
         (shared != 0 && shared != 1))
@@ -660,7 +671,7 @@ cq_status cq_moe_route(const float* logits, int64_t T, int64_t E, int64_t topk, 
 
 cq_status cq_moe_layout(const void* ws, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk, int32_t* perm_out,
                         int32_t* seg_out, void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!ws || !perm_out || !seg_out) return fail(CQ_ERR_NULL, "cq_moe_layout: null pointer");
     if (T < 1 || topk < 1 || E < 1) return fail(CQ_ERR_SHAPE, "cq_moe_layout: bad shape");
     const MoeLayout l = moe_layout(T, H, I, E, topk);
@@ -672,7 +683,7 @@ cq_status cq_moe_layout(const void* ws, int64_t T, int64_t H, int64_t I, int64_t
 }
 
 cq_status cq_dequant_q4(const uint8_t* Wq, const uint16_t* Ws, int64_t N, int64_t K, float* W, void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!Wq || !Ws || !W) return fail(CQ_ERR_NULL, "cq_dequant_q4: null pointer");
     if (N < 1 || K < 32 || K % 32) return fail(CQ_ERR_SHAPE, "cq_dequant_q4: need N>=1, K%%32==0");
     if (!aligned16(Wq) || !aligned16(W)) return fail(CQ_ERR_ALIGN, "cq_dequant_q4: Wq and W must be 16-byte aligned");
@@ -682,7 +693,7 @@ cq_status cq_dequant_q4(const uint8_t* Wq, const uint16_t* Ws, int64_t N, int64_
 }
 
 cq_status cq_dequant_q8row(const int8_t* Wq, const float* rs, int64_t N, int64_t K, float* W, void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     if (!Wq || !rs || !W) return fail(CQ_ERR_NULL, "cq_dequant_q8row: null pointer");
     if (N < 1 || K < 1) return fail(CQ_ERR_SHAPE, "cq_dequant_q8row: need N>=1, K>=1");
     cq_status st;
@@ -691,7 +702,7 @@ cq_status cq_dequant_q8row(const int8_t* Wq, const float* rs, int64_t N, int64_t
 }
 
 cq_status cq_get_device_error(void* stream) {
-    g_msg[0] = 0;
+    clear_last_error();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* word = stream_error_word(s);
     if (!word) return CQ_ERR_CUDA;

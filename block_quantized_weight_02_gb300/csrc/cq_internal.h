@@ -39,7 +39,10 @@ int* stream_error_word(cudaStream_t s);
 
 // Host error reporting (a thread-local "decline: ..." message).
 cq_status fail(cq_status st, const char* fmt, ...);
-void clear_last_error();
+void clear_last_error();   // start of an entry-point call: no message, no launches yet
+// Counts a successful kernel launch of the current entry-point call (returns e).
+cudaError_t counted(cudaError_t e);
+int launches_so_far();
 cq_status cuda_fail(cudaError_t e, const char* what);
 
 // Tensor map encoding (driver entry point fetched through the runtime, so

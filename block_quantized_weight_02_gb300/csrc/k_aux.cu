@@ -25,7 +25,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    return counted(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...));
 }
 
 // First writer wins: a later error of the same call does not replace the first.
@@ -62,13 +62,13 @@ __global__ void k_dequant_q8row(const int8_t* __restrict__ wq, const float* __re
 cudaError_t launch_dequant_q4(const uint8_t* wq, const uint16_t* ws, int64_t N, int64_t K, float* w, cudaStream_t s) {
     const int64_t nb = N * (K / 32);
     k_dequant_q4<<<(unsigned)((nb + 255) / 256), 256, 0, s>>>(wq, ws, nb, K / 32, w);
-    return cudaGetLastError();
+    return counted(cudaGetLastError());
 }
 
 cudaError_t launch_dequant_q8row(const int8_t* wq, const float* rs, int64_t N, int64_t K, float* w, cudaStream_t s) {
     const int64_t n = N * K;
     k_dequant_q8row<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(wq, rs, N, K, w);
-    return cudaGetLastError();
+    return counted(cudaGetLastError());
 }
 
 // ---- power-of-two guard -------------------------------------------------

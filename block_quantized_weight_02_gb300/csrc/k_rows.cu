@@ -423,7 +423,7 @@ cudaError_t launch_rows_t(const RMaps& maps, const RParams& p, int grid, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps, p);
+    return counted(cudaLaunchKernelEx(&cfg, kern, maps, p));
 }
 
 template <int FMT, int XBF>
@@ -444,8 +444,10 @@ bool rows_path_serves(int fmt, int64_t T, int64_t K, int nz) {
 bool rows_path_preferred(int fmt, int64_t T, int64_t K, int64_t N, int nz) {
     if (!rows_path_serves(fmt, T, K, nz)) return false;
     // measured on GB300 (T = 1, 8, 16; Q4 and Q8-row): faster than the K-split kernel, or level
-    // with it, when every CTA holds 6 to 8 units in one pass (at least three full tiles); with
-    // fewer units (idle warps) or two passes the K-split kernel was faster
+    // with it, when every CTA holds 6 to 8 units in one pass (at least three full tiles), and for
+    // very small weights (K = 512, N = 256: one launch without a cluster); with fewer units (idle
+    // warps) or two passes the K-split kernel was faster
+    if (N * K <= (int64_t)1 << 19) return true;
     const int64_t units = (N + UNIT - 1) / UNIT, grid = std::min<int64_t>((int64_t)num_sms(), units);
     const int64_t maxu = (units + grid - 1) / grid;
     return maxu >= 6 && maxu <= UPASS;

@@ -911,7 +911,7 @@ cudaError_t launch_t(SMaps maps, const void* const* xs, int nz, int64_t xrows, i
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps, p);
+    return counted(cudaLaunchKernelEx(&cfg, kern, maps, p));
 }
 
 // Layout and ring depth per column count (as many stages as fit two CTAs

@@ -81,6 +81,7 @@ struct Maps {
 
 struct Params {
     Job job[ZMAX];
+    int mt0;              // first weight-row tile of this launch (a call may split its tiles over two)
     int tiles_y;          // token tiles per job
     int64_t ldy;          // output row pitch (elements)
     int yt;
@@ -220,7 +221,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // first weight row (gate/up mode: first gate row i0; the tile is i0 .. i0 + 63 and I + i0 ..)
-    const int m0 = blockIdx.x * (GU ? BM / 2 : BM);
+    const int m0 = (p.mt0 + (int)blockIdx.x) * (GU ? BM / 2 : BM);
     const int jz = (int)blockIdx.y / p.tiles_y;                 // job of a z-batched launch
     const int t0 = ((int)blockIdx.y - jz * p.tiles_y) * BN;    // first activation row
     const Job J = jz == 0 ? p.job[0] : jz == 1 ? p.job[1] : jz == 2 ? p.job[2] : p.job[3];
@@ -848,7 +849,7 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, maps, p);
+    return counted(cudaLaunchKernelEx(&cfg, kern, maps, p));
 }
 
 // Tile plan: token tile BN and K split.  One CTA per SM.  Time of a CTA ~ its
@@ -906,12 +907,29 @@ Plan plan_tiles(const TcArgs& a, int64_t mt, bool tmem_only) {
     return {bbn, bks, pair_ok};
 }
 
+// Weight-row tiles to move into a second launch that splits K over CTA pairs of
+// a cluster, so that the first launch fills whole waves of the GPU: a last wave
+// that would hold only a few tiles (each as long as a full one) becomes a launch
+// of those tiles at half their length.  0 when there is nothing to gain or the
+// tile shape has no K-split form.
+int64_t tail_row_tiles(const Plan& pl, bool pair, int64_t mt, int64_t cols, int64_t K) {
+    const int64_t nk = K / BK;
+    if (pl.ks != 1 || !(pl.bn == 256 || pl.bn == 128 || pl.bn == 32) || nk % 8 != 0 || nk < 24) return 0;
+    const int64_t sms = num_sms(), ctas = mt * cols;
+    if (ctas <= sms || ctas % sms == 0) return 0;
+    int64_t r = (ctas % sms + cols - 1) / cols;   // row tiles of the partial last wave
+    if (pair) r = (r + 1) & ~(int64_t)1;          // CTA pairs take neighbouring row tiles
+    if (r >= mt || 2 * r * cols > sms) return 0;  // the split tiles must fit in one wave
+    return r;
+}
+
 Params make_params(const TcArgs& a) {
     Params p = {};
     for (int j = 0; j < a.jobs(); ++j) {
         const TcJob jb = a.job(j);
         p.job[j] = {jb.rsx, jb.rs, jb.ws, jb.wsf, jb.add, jb.y};
     }
+    p.mt0 = 0;
     p.tiles_y = 1;
     p.ldy = a.ldy > 0 ? a.ldy : a.N;
     p.yt = a.yt;
@@ -939,7 +957,7 @@ void trace_plan(const char* what, int fmt, const TcArgs& a, const Plan& pl, bool
 // gate/up (SwiGLU) mode.  <FMT, BN, XBF, G, LSS, AS, AM, KS, CG, GU>: super-stages
 // of G stages, as many super-slots as fit next to the decoded slots.
 template <int GU>
-cudaError_t launch_q4_tmem(const TcArgs& a, const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
+cudaError_t launch_q4_tmem_one(const TcArgs& a, const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
     const int bn = pl.bn, ks = pl.ks;
     const bool pair = (bn >= 128 || bn == 32) && pl.pair_ok;
     if (bn == 192) return launch_bn<0, 192, 0, 2, 6, 8, 1, 1, 2, GU>(a, p, grid, s);
@@ -952,6 +970,22 @@ cudaError_t launch_q4_tmem(const TcArgs& a, const Params& p, const Plan& pl, dim
     if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 1, 6, 8, 1, 2, 1, GU>(a, p, grid, s) : launch_bn<0, 256, 0, 1, 6, 8, 1, 1, 1, GU>(a, p, grid, s);
     if (bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 2, 5, 12, 1, 2, 1, GU>(a, p, grid, s) : launch_bn<0, 128, 0, 2, 5, 12, 1, 1, 1, GU>(a, p, grid, s);
     return launch_bn<0, 64, 0, 4, 4, 12, 1, 1, 1, GU>(a, p, grid, s);
+}
+
+// grid = (row tiles, token tiles x jobs, K split); the last row tiles may go to a second,
+// K-split launch (tail_row_tiles)
+template <int GU>
+cudaError_t launch_q4_tmem(const TcArgs& a, const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
+    const bool pair = (pl.bn >= 128 || pl.bn == 32) && pl.pair_ok;
+    const int64_t r = tail_row_tiles(pl, pair, grid.x, grid.y, a.K);
+    if (r == 0) return launch_q4_tmem_one<GU>(a, p, pl, grid, s);
+    cudaError_t e = launch_q4_tmem_one<GU>(a, p, pl, dim3(grid.x - (unsigned)r, grid.y, 1), s);
+    if (e != cudaSuccess) return e;
+    Params pt = p;
+    pt.mt0 = (int)(grid.x - r);
+    const Plan plt = {pl.bn, 2, pl.pair_ok};
+    trace_plan("tail", 0, a, plt, pair, dim3((unsigned)r, grid.y, 2));
+    return launch_q4_tmem_one<GU>(a, pt, plt, dim3((unsigned)r, grid.y, 2), s);
 }
 
 }  // namespace

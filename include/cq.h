@@ -311,6 +311,12 @@ cq_status cq_dequant_q8row(const int8_t* Wq, const float* rs, int64_t N, int64_t
 cq_status cq_get_device_error(void* stream);
 /* The calling thread's last host-side error message ("" if none). */
 const char* cq_last_error(void);
+/* Kernel launches the calling thread's most recent library call issued
+ * (0 if it declined before launching; a host-only call resets it to 0): the
+ * number of kernel nodes such a call adds to a captured CUDA graph.  The
+ * pages have no counterpart; it exists for callers that size graphs or
+ * count launches. */
+int cq_last_launches(void);
 
 typedef enum {
     CQ_OPT_SMALL_T_MAX = 0,  /* largest T served by the weight-streaming path (default 32, max 32) */
@@ -328,7 +334,8 @@ typedef enum {
                                 SM, each streaming the whole K of an equal share of the weight rows) wherever it
                                 serves (one job, K % 512 == 0), 1 the K-split cluster kernel, 0 (default) the
                                 row-partitioned kernel where it serves and every CTA holds 6 to 8 units of 8 rows
-                                (on 152 SMs: 6081 <= N <= 9728), else the K-split kernel */
+                                (on 152 SMs: 6081 <= N <= 9728) or N * K <= 2^19, else the
+                                K-split kernel */
 } cq_option;
 /* Process-wide: one value for every thread, stream and device (set before
  * the calls it should affect); reads and writes are atomic, so concurrent

@@ -68,6 +68,7 @@ def test_q4_validation(L):
     assert _q4(L, wsb=10) == 6
     assert _q4(L, ws=FAKE + 16) == 6          # workspace must be 256-aligned
     assert "decline" in cq.cq_last_error()
+    assert L.cq_last_launches() == 0          # a declined call launches nothing
 
 
 def test_q8_validation(L):

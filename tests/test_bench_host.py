@@ -14,7 +14,9 @@ PEAKS = {"hbm_gbs": 6000.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1600
 
 
 def _call(flops, wbytes, other):
-    return bench.Call("c", None, flops, wbytes, other, 1)
+    c = bench.Call("c", None, flops, wbytes, other)
+    c.launches = 1
+    return c
 
 
 def test_roofline_entry_picks_the_lower_roofline():

@@ -551,3 +551,31 @@ def test_small_t_kernels_agree():
     for y in outs:
         check(y, yref, S, "f32", "small-T kernels")
     assert np.all(np.abs(outs[0] - outs[1]) <= 4e-3 * S + 2e-6)
+
+
+# ---- a partial last wave moved into a K-split launch --------------------------
+
+@pytest.mark.parametrize("fmt", ["q4", "q8"])
+def test_tcgen05_tail_launch(fmt, capfd):
+    """T = 256, K = 1536, N = 20480 with 256-column tiles: 160 row tiles on the
+    GPU's SMs leave a partial last wave, whose row tiles go to a second launch
+    with K split over a cluster (trace line "tail").  Outputs sampled over all
+    rows and, more densely, over the last 2048 rows (the tail's and its
+    neighbours')."""
+    T, K, N = 256, 1536, 20480
+    case = (synth.gemm_q4_case(8700, T, K, N) if fmt == "q4" else synth.gemm_q8_case(8701, T, K, N))
+    res = {}
+    with ForcePath(2), _Opt(cq.CQ_OPT_TC_BN, 256):
+        run = (lambda: res.update(r=run_q4(case, "f32"))) if fmt == "q4" else (lambda: res.update(r=(run_q8(case, "f32"), None)))
+        trace = traced_kernels(capfd, run)
+    assert any(l.startswith("cq: tcgen05 tail") for l in trace), trace
+    Y, wq = res["r"]
+    rng = np.random.default_rng(8702)
+    tn = np.concatenate([sample_positions(T, N, 2000, 8703),
+                         np.stack([rng.integers(0, T, 3000), rng.integers(N - 2048, N, 3000)], 1)]).astype(np.int64)
+    X = oracle.x_to_f64(case["x"], case["x_dtype"])
+    if fmt == "q4":
+        yref, S = oracle.gemm_q4_sampled(wq, case["scales"], N, K, X, tn)
+    else:
+        yref, S = oracle.gemm_q8_sampled(case["q"], case["rs"], X, tn)
+    check(y_host(Y)[tn[:, 0], tn[:, 1]], yref, S, "f32", f"{fmt} tcgen05 with a K-split tail launch")
