@@ -124,8 +124,8 @@ struct SkinnyDense {
 cudaError_t launch_skinny_q4(const SkinnyDense& a, cudaStream_t s);
 cudaError_t launch_skinny_q8(const SkinnyDense& a, cudaStream_t s);    // rsx nullable: per-token scales (q8_2f)
 cudaError_t launch_skinny_q8b(const SkinnyDense& a, cudaStream_t s);   // Q8 per 32-k block, activations as given
-// Row-partitioned weight streaming (k_rows.cu) for T <= 16, one job, K a multiple of the
-// stage (512 for Q4, 256 for Q8); fmt 0 Q4, 1 Q8-row, 2 Q8/32.
+// Row-partitioned weight streaming (k_rows.cu) for T <= 32 (Q8/32: T <= 16), one job, K a
+// multiple of the 512-k stage; fmt 0 Q4, 1 Q8-row, 2 Q8/32.
 bool rows_path_serves(int fmt, int64_t T, int64_t K, int nz);
 bool rows_path_preferred(int fmt, int64_t T, int64_t K, int64_t N, int nz);   // the default's choice
 cudaError_t launch_rows(int fmt, const SkinnyDense& a, cudaStream_t s);

@@ -1,4 +1,4 @@
-// Weight-streaming GEMM for up to 16 activation rows, partitioned by weight
+// Weight-streaming GEMM for up to 32 activation rows, partitioned by weight
 // rows so that every SM streams the same number of weight bytes.
 //
 // The weight rows are cut into units of 8 and the units are spread over one
@@ -7,7 +7,8 @@
 // rows, so no partial sums cross CTAs.  Inside a CTA the units come in passes
 // of up to eight (as many passes as needed, units split evenly over them);
 // a pass is four m16 tiles of two units each (the weights are the A operand
-// of mma.sync m16n8k16, the activation rows its n8 B operand), and consumer
+// of mma.sync m16n8k16, the activation rows its n8 B operand in one to four
+// n8 tiles), and consumer
 // warp w takes tile w % 4 and the quarter w / 4 of every stage's 32-k blocks.
 // The four quarters' sums of a tile are added in a fixed order at the end of
 // the pass.  A tile whose second unit lies past the CTA's units multiplies
@@ -17,7 +18,7 @@
 // Stages of 512 k: weight boxes {128 bytes, the pass's rows} (two for Q4, four
 // for Q8; 128-byte swizzle: 16-byte chunk j of row r at j ^ (r % 8)), for the
 // block-scaled formats one box of scales over the same rows, and one box of
-// the activations {64 k, 8 or 16 rows, 8 slabs} -- at most six boxes per
+// the activations {64 k, 8, 16 or 32 rows, 8 slabs} -- at most six boxes per
 // stage, since a TMA box costs about the same however few bytes it holds.
 // Producer lane s issues every copy of the stages that land in ring slot s.
 //
@@ -151,12 +152,12 @@ struct RLayout {
     static constexpr int X_BYTES = G::XSL * TP * 128;
     static constexpr int X_OFF = G::W_BYTES + G::S_BYTES;     // 1024-aligned
     static constexpr int SLOT = X_OFF + X_BYTES;
-    static constexpr int RED_BYTES = TILES * (PARTS - 1) * 32 * 8 * 4;   // quarters 1..3 of each tile
+    static constexpr int RED_BYTES = TILES * (PARTS - 1) * 32 * TP / 2 * 4;   // quarters 1..3 of each tile
     static_assert(G::W_BYTES % 1024 == 0 && X_OFF % 1024 == 0 && SLOT % 1024 == 0, "1024-byte aligned boxes");
 };
 
 // FMT 0: Q4 (fp16 block scales), 1: Q8-row, 2: Q8 per 32-k block (f32 block scales).
-// TP: activation rows, 8 or 16 (one or two n8 tiles).  XBF: bf16 activations.
+// TP: activation rows, 8, 16 or 32 (one, two or four n8 tiles).  XBF: bf16 activations.
 template <int FMT, int TP, int XBF, int NSLOT>
 __global__ void __launch_bounds__(RW_THREADS, 1)
 k_rows(const __grid_constant__ RMaps maps, const RParams p) {
@@ -165,7 +166,7 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
-    float* red = reinterpret_cast<float*>(smem + NSLOT * L::SLOT);   // [TILES][PARTS - 1][32 lanes][8]
+    float* red = reinterpret_cast<float*>(smem + NSLOT * L::SLOT);   // [TILES][PARTS - 1][32 lanes][4 NT]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NSLOT * L::SLOT + L::RED_BYTES);
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
@@ -302,12 +303,6 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
                     const uint32_t slab = (uint32_t)(jb >> 1);
                     const uint32_t clo = (uint32_t)(4 * (jb & 1) + (c >> 1)), off8 = 8u * (uint32_t)(c & 1);
                     const uint32_t xr = sX + (slab * TP + (uint32_t)g) * 128u + off8;
-                    uint2 xlo[NT], xhi[NT];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        xlo[nt] = r_lds64(xr + 1024u * nt + ((clo ^ (uint32_t)g) << 4));
-                        xhi[nt] = r_lds64(xr + 1024u * nt + (((clo + 2u) ^ (uint32_t)g) << 4));
-                    }
                     uint32_t a1[4], a2[4];
                     if (FMT == 0) {
                         const uint32_t wa = wrow + (uint32_t)((jb >> 3) * G::WBOX) + ((((uint32_t)(jb & 7)) ^ (uint32_t)g) << 4);
@@ -328,14 +323,16 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
                         a2[2] = i8_pair<XBF>(l1, 0x4342u), a2[3] = i8_pair<XBF>(h1, 0x4342u);
                     }
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
+                    for (int nt = 0; nt < NT; ++nt) {   // tokens 8 nt + g
+                        const uint2 xlo = r_lds64(xr + 1024u * nt + ((clo ^ (uint32_t)g) << 4));
+                        const uint2 xhi = r_lds64(xr + 1024u * nt + (((clo + 2u) ^ (uint32_t)g) << 4));
                         if (FMT == 1) {
-                            mma_f<XBF>(acc[nt], a1, xlo[nt].x, xlo[nt].y);
-                            mma_f<XBF>(acc[nt], a2, xhi[nt].x, xhi[nt].y);
+                            mma_f<XBF>(acc[nt], a1, xlo.x, xlo.y);
+                            mma_f<XBF>(acc[nt], a2, xhi.x, xhi.y);
                         } else {
                             float pb[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma_f<XBF>(pb, a1, xlo[nt].x, xlo[nt].y);
-                            mma_f<XBF>(pb, a2, xhi[nt].x, xhi[nt].y);
+                            mma_f<XBF>(pb, a1, xlo.x, xlo.y);
+                            mma_f<XBF>(pb, a2, xhi.x, xhi.y);
                             acc[nt][0] = fmaf(slo[jh], pb[0], acc[nt][0]);
                             acc[nt][1] = fmaf(slo[jh], pb[1], acc[nt][1]);
                             acc[nt][2] = fmaf(shi[jh], pb[2], acc[nt][2]);
@@ -350,11 +347,11 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
         // ---- the quarters' sums (quarters 1..3 handed over in shared memory, added in
         // quarter order), then the epilogue of the tile by its first quarter: lane (g, c)
         // holds rows g, g + 8 of the tile and tokens 2c, 2c + 1 of each n8 tile ----
-        float* rd = red + ((tile * (PARTS - 1)) * 32 + lane) * 8;
+        float* rd = red + ((tile * (PARTS - 1)) * 32 + lane) * (4 * NT);
         if (part > 0) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-                *reinterpret_cast<float4*>(rd + (part - 1) * 256 + 4 * nt) =
+                *reinterpret_cast<float4*>(rd + (part - 1) * 32 * 4 * NT + 4 * nt) =
                     make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(RW_CONS * 32) : "memory");
@@ -363,7 +360,7 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
             for (int q = 0; q < PARTS - 1; ++q) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const float4 o = *reinterpret_cast<const float4*>(rd + q * 256 + 4 * nt);
+                    const float4 o = *reinterpret_cast<const float4*>(rd + q * 32 * 4 * NT + 4 * nt);
                     acc[nt][0] += o.x;
                     acc[nt][1] += o.y;
                     acc[nt][2] += o.z;
@@ -428,33 +425,34 @@ cudaError_t launch_rows_t(const RMaps& maps, const RParams& p, int grid, cudaStr
 
 template <int FMT, int XBF>
 cudaError_t launch_rows_x(const RMaps& maps, const RParams& p, int grid, int64_t T, cudaStream_t s) {
-    // ring depth: as many 512-k stages as fit (Q4 26 / 34 KB, Q8-row 40 / 48 KB, Q8/32 44 / 52 KB
-    // for 8 / 16 activation rows)
+    // ring depth: as many 512-k stages as fit (Q4 26 / 34 / 50 KB, Q8-row 40 / 48 / 64 KB,
+    // Q8/32 44 / 52 KB for 8 / 16 / 32 activation rows)
     if (T <= 8) return launch_rows_t<FMT, 8, XBF, FMT == 0 ? 8 : FMT == 1 ? 5 : 4>(maps, p, grid, s);
-    return launch_rows_t<FMT, 16, XBF, FMT == 0 ? 6 : 4>(maps, p, grid, s);
+    if (T <= 16) return launch_rows_t<FMT, 16, XBF, FMT == 0 ? 6 : 4>(maps, p, grid, s);
+    if constexpr (FMT != 2) return launch_rows_t<FMT, 32, XBF, FMT == 0 ? 4 : 3>(maps, p, grid, s);
+    return cudaErrorInvalidValue;   // Q8/32 serves T <= 16 (rows_path_serves)
 }
 
 }  // namespace
 
 bool rows_path_serves(int fmt, int64_t T, int64_t K, int nz) {
-    (void)fmt;
-    return nz <= 1 && T >= 1 && T <= 16 && K % KSTAGE == 0;
+    return nz <= 1 && T >= 1 && T <= (fmt == 2 ? 16 : 32) && K % KSTAGE == 0;
 }
 
 bool rows_path_preferred(int fmt, int64_t T, int64_t K, int64_t N, int nz) {
     if (!rows_path_serves(fmt, T, K, nz)) return false;
-    // measured on GB300 (T = 1, 8, 16; Q4 and Q8-row): faster than the K-split kernel, or level
-    // with it, when every CTA holds 6 to 8 units in one pass (at least three full tiles), and for
-    // very small weights (K = 512, N = 256: one launch without a cluster); with fewer units (idle
-    // warps) or two passes the K-split kernel was faster
+    // measured on GB300 (T = 1-32; Q4 and Q8-row): faster than the K-split kernel, or level
+    // with it, when every CTA holds 6 to 8 units in one pass (at least three full tiles) -- for
+    // Q8 only up to T = 16 -- and for very small weights (K = 512, N = 256: one launch without a
+    // cluster); with fewer units (idle warps) or two passes the K-split kernel was faster
     if (N * K <= (int64_t)1 << 19) return true;
+    if (fmt != 0 && T > 16) return false;
     const int64_t units = (N + UNIT - 1) / UNIT, grid = std::min<int64_t>((int64_t)num_sms(), units);
     const int64_t maxu = (units + grid - 1) / grid;
     return maxu >= 6 && maxu <= UPASS;
 }
 
 cudaError_t launch_rows(int fmt, const SkinnyDense& a, cudaStream_t s) {
-    constexpr int TPX = 16;   // the activation box spans the padded rows; TMA fills the ones past T with zeros
     const int64_t kstage = KSTAGE;
     RParams p = {};
     p.N = a.N;
@@ -499,7 +497,7 @@ cudaError_t launch_rows(int fmt, const SkinnyDense& a, cudaStream_t s) {
     {
         // {64 elements, T rows, K/64 slabs} (strides K*2 B, 128 B): a box of TP rows x stage/64 slabs
         // lands as [slab][row][128 B], 128-byte swizzled
-        const int tp = a.T <= 8 ? 8 : TPX;
+        const int tp = a.T <= 8 ? 8 : a.T <= 16 ? 16 : 32;
         uint64_t d[3] = {64, (uint64_t)a.T, (uint64_t)a.K / 64};
         uint64_t st[2] = {(uint64_t)a.K * 2, 128};
         uint32_t box[3] = {64, (uint32_t)tp, (uint32_t)(kstage / 64)};

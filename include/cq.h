@@ -330,12 +330,13 @@ typedef enum {
     CQ_OPT_TC_PAIR = 8,      /* tcgen05, 256-column tiles with decoded weights in tensor memory: 0 auto / 2 on
                                 (neighbouring weight-row tiles share one 256-row MMA on a CTA pair, each CTA
                                 loading half of the activation tile; needs an even number of row tiles), 1 off */
-    CQ_OPT_STREAM_KERNEL = 9 /* weight-streaming kernel for T <= 16: 2 the row-partitioned kernel (one CTA per
-                                SM, each streaming the whole K of an equal share of the weight rows) wherever it
-                                serves (one job, K % 512 == 0), 1 the K-split cluster kernel, 0 (default) the
+    CQ_OPT_STREAM_KERNEL = 9 /* weight-streaming kernel: 2 the row-partitioned kernel (one CTA per SM, each
+                                streaming the whole K of an equal share of the weight rows) wherever it serves
+                                (one job, K % 512 == 0, T <= 32; Q8/32: T <= 16), 1 the K-split cluster
+                                kernel, 0 (default) the
                                 row-partitioned kernel where it serves and every CTA holds 6 to 8 units of 8 rows
-                                (on 152 SMs: 6081 <= N <= 9728) or N * K <= 2^19, else the
-                                K-split kernel */
+                                (on 152 SMs: 6081 <= N <= 9728; Q8 formats: T <= 16) or
+                                N * K <= 2^19, else the K-split kernel */
 } cq_option;
 /* Process-wide: one value for every thread, stream and device (set before
  * the calls it should affect); reads and writes are atomic, so concurrent

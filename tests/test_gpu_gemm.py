@@ -507,7 +507,7 @@ def test_c3_denoiser_block_f32():
 
 # ---- the row-partitioned weight-streaming kernel (T <= 16) -------------------
 
-@pytest.mark.parametrize("T", [1, 3, 8, 9, 16])
+@pytest.mark.parametrize("T", [1, 3, 8, 9, 16, 17, 32])
 @pytest.mark.parametrize("K,N", [(512, 8), (1024, 100), (2048, 1001), (4096, 2500), (512, 20000)])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
 def test_q4_rows_kernel(T, K, N, xdt, capfd):
@@ -525,7 +525,7 @@ def test_q4_rows_kernel(T, K, N, xdt, capfd):
     check(y_host(Y), yref, S, out, f"q4 rows T={T} K={K} N={N} {xdt}")
 
 
-@pytest.mark.parametrize("T", [1, 8, 16])
+@pytest.mark.parametrize("T", [1, 8, 16, 25, 32])
 @pytest.mark.parametrize("K,N", [(512, 8), (1536, 300), (2048, 1001), (512, 20000)])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
 def test_q8_rows_kernel(T, K, N, xdt, capfd):
