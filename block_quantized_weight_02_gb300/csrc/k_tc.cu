@@ -64,15 +64,17 @@ cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     const bool pair = am == 1 && (pl.bn >= 128 || pl.bn == 32) && pl.pair_ok;
     trace_plan("dense", fmt, a, pl, pair, grid);
     // a partial last wave of full-length tiles moves into a second, K-split launch
-    const int64_t r = am == 1 ? tail_row_tiles(pl, pair, mt, grid.y, a.K) : 0;
-    if (r == 0) return launch_one(fmt, xbf, am, pl, a, p, grid, s);
-    cudaError_t e = launch_one(fmt, xbf, am, pl, a, p, dim3((unsigned)(mt - r), grid.y, 1), s);
+    const Tail tl = am == 1 ? tail_plan(pl, pair, mt, a.T, a.jobs(), a.K) : Tail{0, 0};
+    if (tl.r == 0) return launch_one(fmt, xbf, am, pl, a, p, grid, s);
+    cudaError_t e = launch_one(fmt, xbf, am, pl, a, p, dim3((unsigned)(mt - tl.r), grid.y, 1), s);
     if (e != cudaSuccess) return e;
     Params pt = p;
-    pt.mt0 = (int)(mt - r);
-    const Plan plt = {pl.bn, 2, pl.pair_ok};
-    trace_plan("tail", fmt, a, plt, pair, dim3((unsigned)r, grid.y, 2));
-    return launch_one(fmt, xbf, am, plt, a, pt, dim3((unsigned)r, grid.y, 2), s);
+    pt.mt0 = (int)(mt - tl.r);
+    pt.tiles_y = (int)((a.T + tl.bn - 1) / tl.bn);
+    const Plan plt = {tl.bn, 2, pl.pair_ok};
+    const dim3 gt((unsigned)tl.r, (unsigned)(pt.tiles_y * a.jobs()), 2);
+    trace_plan("tail", fmt, a, plt, pair, gt);
+    return launch_one(fmt, xbf, am, plt, a, pt, gt, s);
 }
 
 }  // namespace

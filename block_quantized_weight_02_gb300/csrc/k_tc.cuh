@@ -907,20 +907,29 @@ Plan plan_tiles(const TcArgs& a, int64_t mt, bool tmem_only) {
     return {bbn, bks, pair_ok};
 }
 
-// Weight-row tiles to move into a second launch that splits K over CTA pairs of
-// a cluster, so that the first launch fills whole waves of the GPU: a last wave
-// that would hold only a few tiles (each as long as a full one) becomes a launch
-// of those tiles at half their length.  0 when there is nothing to gain or the
-// tile shape has no K-split form.
-int64_t tail_row_tiles(const Plan& pl, bool pair, int64_t mt, int64_t cols, int64_t K) {
+// Weight-row tiles to move into a second launch that splits K over a cluster, so
+// that the first launch fills whole waves of the GPU: a last wave that would hold
+// only a few tiles (each as long as a full one) becomes a launch of those row
+// tiles at half their length, in the narrowest token tiles that still fit in one
+// wave (narrow tiles cost less per stage).  r = 0 when there is nothing to gain or
+// the tile shape has no K-split form.
+struct Tail {
+    int64_t r;   // row tiles of the tail launch (the last r)
+    int bn;      // its token-tile width
+};
+Tail tail_plan(const Plan& pl, bool pair, int64_t mt, int64_t T, int64_t jobs, int64_t K) {
     const int64_t nk = K / BK;
-    if (pl.ks != 1 || !(pl.bn == 256 || pl.bn == 128 || pl.bn == 32) || nk % 8 != 0 || nk < 24) return 0;
-    const int64_t sms = num_sms(), ctas = mt * cols;
-    if (ctas <= sms || ctas % sms == 0) return 0;
+    if (pl.ks != 1 || !(pl.bn == 256 || pl.bn == 128 || pl.bn == 32) || nk % 8 != 0 || nk < 24) return {0, 0};
+    const int64_t sms = num_sms(), cols = (T + pl.bn - 1) / pl.bn * jobs, ctas = mt * cols;
+    if (ctas <= sms || ctas % sms == 0) return {0, 0};
     int64_t r = (ctas % sms + cols - 1) / cols;   // row tiles of the partial last wave
     if (pair) r = (r + 1) & ~(int64_t)1;          // CTA pairs take neighbouring row tiles
-    if (r >= mt || 2 * r * cols > sms) return 0;  // the split tiles must fit in one wave
-    return r;
+    if (r >= mt) return {0, 0};
+    for (int bn : {32, 128, 256}) {
+        if (bn > pl.bn) break;
+        if (2 * r * ((T + bn - 1) / bn) * jobs <= sms) return {r, bn};
+    }
+    return {0, 0};
 }
 
 Params make_params(const TcArgs& a) {
@@ -977,15 +986,17 @@ cudaError_t launch_q4_tmem_one(const TcArgs& a, const Params& p, const Plan& pl,
 template <int GU>
 cudaError_t launch_q4_tmem(const TcArgs& a, const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
     const bool pair = (pl.bn >= 128 || pl.bn == 32) && pl.pair_ok;
-    const int64_t r = tail_row_tiles(pl, pair, grid.x, grid.y, a.K);
-    if (r == 0) return launch_q4_tmem_one<GU>(a, p, pl, grid, s);
-    cudaError_t e = launch_q4_tmem_one<GU>(a, p, pl, dim3(grid.x - (unsigned)r, grid.y, 1), s);
+    const Tail tl = tail_plan(pl, pair, grid.x, a.T, a.jobs(), a.K);
+    if (tl.r == 0) return launch_q4_tmem_one<GU>(a, p, pl, grid, s);
+    cudaError_t e = launch_q4_tmem_one<GU>(a, p, pl, dim3(grid.x - (unsigned)tl.r, grid.y, 1), s);
     if (e != cudaSuccess) return e;
     Params pt = p;
-    pt.mt0 = (int)(grid.x - r);
-    const Plan plt = {pl.bn, 2, pl.pair_ok};
-    trace_plan("tail", 0, a, plt, pair, dim3((unsigned)r, grid.y, 2));
-    return launch_q4_tmem_one<GU>(a, pt, plt, dim3((unsigned)r, grid.y, 2), s);
+    pt.mt0 = (int)(grid.x - tl.r);
+    pt.tiles_y = (int)((a.T + tl.bn - 1) / tl.bn);
+    const Plan plt = {tl.bn, 2, pl.pair_ok};
+    const dim3 gt((unsigned)tl.r, (unsigned)(pt.tiles_y * a.jobs()), 2);
+    trace_plan("tail", 0, a, plt, pair, gt);
+    return launch_q4_tmem_one<GU>(a, pt, plt, gt, s);
 }
 
 }  // namespace
