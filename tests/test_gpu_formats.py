@@ -47,11 +47,12 @@ def test_q8b(path, T, K, N, out, xdt):
     check(y_host(Y), yref, S, out, f"q8/32 path={path} T={T} K={K} N={N} {xdt}->{out}")
 
 
-@pytest.mark.parametrize("path,T", [(1, 8), (1, 32), (2, 40), (2, 300)])
+@pytest.mark.parametrize("path,T,kern", [(1, 8, 1), (1, 32, 1), (1, 8, 2), (1, 16, 2), (2, 40, 0), (2, 300, 0)])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
-def test_q8b_decoders_bit_exact_identity(path, T, xdt):
-    """X[t] = e_{k_t}.  Streaming: Y = RNE_f32(q * s), the oracle's dequantised
-    weight.  tcgen05: Y = RNE_fp16(q * RNE_fp16(s)) (numpy's roundings)."""
+def test_q8b_decoders_bit_exact_identity(path, T, kern, xdt):
+    """X[t] = e_{k_t}.  Streaming (kern 1 K-split, 2 row-partitioned): Y =
+    RNE_f32(q * s), the oracle's dequantised weight.  tcgen05: Y =
+    RNE_fp16(q * RNE_fp16(s)) (numpy's roundings)."""
     K, N = 512, 136
     _, q, s = _q8b_case(9950 + T, 1, K, N, xdt)
     s[0, :] = 0.0
@@ -62,7 +63,7 @@ def test_q8b_decoders_bit_exact_identity(path, T, xdt):
     x = synth.to_storage(xv, xdt)
     Y = torch.empty(T, N, dtype=torch.float32, device=DEV)
     ws = torch.empty(cq.cq_gemm_q8b_workspace_bytes(T, K), dtype=torch.uint8, device=DEV)
-    with ForcePath(path):
+    with ForcePath(path), Opt(cq.CQ_OPT_STREAM_KERNEL, kern):
         cq.cq_gemm_q8b(to_dev_x(x, xdt), to_dev(q), to_dev(s), Y, ws)
     assert cq.cq_get_device_error() == 0
     if path == 1:

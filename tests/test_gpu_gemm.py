@@ -444,7 +444,9 @@ def _assert_values_equal(Y, E, what):
 
 @pytest.mark.parametrize("T", [1, 8, 16, 32])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
-def test_q4_streaming_decoder_bit_exact_identity(T, xdt):
+@pytest.mark.parametrize("kern", [1, 2])
+def test_q4_streaming_decoder_bit_exact_identity(T, xdt, kern):
+    """Both weight-streaming kernels (1 K-split, 2 row-partitioned)."""
     N, K = 300, 1024
     codes, scales = _decoder_case(8100 + T, N, K, big_scales=True)
     wq = pack.pack_q4(codes)
@@ -452,11 +454,11 @@ def test_q4_streaming_decoder_bit_exact_identity(T, xdt):
     for shift in (0, 7):
         x, kt = _unit_rows(T, K, xdt, shift)
         Y = torch.empty(T, N, dtype=torch.float32, device=DEV)
-        with ForcePath(1):
+        with ForcePath(1), _Opt(cq.CQ_OPT_STREAM_KERNEL, kern):
             cq.cq_gemm_q4(to_dev_x(x, xdt), to_dev(wq), to_dev(scales), Y,
                           torch.empty(cq.cq_gemm_q4_workspace_bytes(T, K), dtype=torch.uint8, device=DEV))
         assert cq.cq_get_device_error() == 0
-        _assert_values_equal(Y, W[:, kt].T, f"q4 streaming decode T={T} {xdt} shift={shift}")
+        _assert_values_equal(Y, W[:, kt].T, f"q4 streaming decode kernel={kern} T={T} {xdt} shift={shift}")
 
 
 @pytest.mark.parametrize("T,bn,ks", [(40, 0, 0), (64, 64, 1), (150, 128, 2), (300, 256, 1), (300, 256, 2),
@@ -476,8 +478,8 @@ def test_q4_tcgen05_decoder_bit_exact_identity(T, bn, ks, xdt):
     _assert_values_equal(Y, W16[:, kt].T, f"q4 tcgen05 decode T={T} bn={bn} ks={ks} {xdt}")
 
 
-@pytest.mark.parametrize("path,T,bn,ks", [(1, 8, 0, 0), (1, 32, 0, 0), (2, 64, 64, 1), (2, 300, 256, 2),
-                                          (2, 200, 128, 1)])
+@pytest.mark.parametrize("path,T,bn,ks", [(1, 8, 0, 0), (1, 32, 0, 0), (3, 8, 0, 0), (3, 32, 0, 0),
+                                          (2, 64, 64, 1), (2, 300, 256, 2), (2, 200, 128, 1)])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
 def test_q8_decoders_bit_exact_identity(path, T, bn, ks, xdt):
     """Q8-row: int8 -> the activation type exactly, the row scale on the f32
@@ -491,7 +493,9 @@ def test_q8_decoders_bit_exact_identity(path, T, bn, ks, xdt):
     W = oracle.dequant_q8row(q, rs)
     x, kt = _unit_rows(T, K, xdt, 11)
     Y = torch.empty(T, N, dtype=torch.float32, device=DEV)
-    with ForcePath(path), _Opt(cq.CQ_OPT_TC_BN, bn), _Opt(cq.CQ_OPT_TC_KSPLIT, ks):
+    # path 1: the K-split streaming kernel, 3: the row-partitioned one, 2: tcgen05
+    with ForcePath(min(path, 2) if path != 3 else 1), _Opt(cq.CQ_OPT_STREAM_KERNEL, 2 if path == 3 else 1), \
+            _Opt(cq.CQ_OPT_TC_BN, bn), _Opt(cq.CQ_OPT_TC_KSPLIT, ks):
         cq.cq_gemm_q8row(to_dev_x(x, xdt), to_dev(q), to_dev(rs), Y)
     assert cq.cq_get_device_error() == 0
     _assert_values_equal(Y, W[:, kt].T, f"q8 decode path={path} T={T} bn={bn} ks={ks} {xdt}")
