@@ -883,14 +883,18 @@ Plan plan_tiles(const TcArgs& a, int64_t mt, bool tmem_only) {
     for (const Cand& c : cands) {
         if (bn != 0 && c.bn != bn) continue;
         if (ks != 0 && c.ks != ks) continue;
-        if (bn == 0 && 2 * a.T <= c.bn && c.bn > 32) continue;   // at least half of every tile's columns unused
+        // at least half of every tile's columns unused: skipped for the wide tiles, whose stages cost
+        // more; narrow tiles cost about the same per stage whatever their width (measured), so the
+        // cost model decides among them
+        if (bn == 0 && 2 * a.T <= c.bn && c.bn >= 192) continue;
         if (c.bn == 32 && amode == 1) continue;
         // split only to fill the GPU: when the unsplit tiles leave a quarter of the SMs idle
         if (c.ks == 2 && (!ks2_ok || (ks == 0 && mt * ((a.T + c.bn - 1) / c.bn) * a.jobs() * 4 > 3 * num_sms()))) continue;
         if (c.bn == 192 && c.ks != 1) continue;
         if (c.bn == 192 && !pair_ok) continue;   // 192-column tiles only in CTA pairs
+        // measured cycles per 64-k stage (N = K = 8192; 32-column pairs about 550, T = 32-64)
         const double stage = c.bn == 256 ? (pair_ok ? 690.0 : 800.0) : c.bn == 192 ? 680.0
-                           : c.bn == 128 ? (pair_ok ? 515.0 : 570.0) : c.bn == 64 ? 520.0 : (pair_ok ? 300.0 : 520.0);
+                           : c.bn == 128 ? (pair_ok ? 515.0 : 570.0) : c.bn == 64 ? 520.0 : (pair_ok ? 560.0 : 530.0);
         const int64_t ctas = mt * ((a.T + c.bn - 1) / c.bn) * c.ks * a.jobs();
         const int64_t waves = (ctas + num_sms() - 1) / num_sms();
         const double cost = (double)waves * ((double)(nk / c.ks) * stage + (c.ks > 1 ? 6000.0 : 0.0));
