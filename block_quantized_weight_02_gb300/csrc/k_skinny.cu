@@ -295,7 +295,8 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
     // dense: recv [ks][slice] f32, the partial sums the cluster's ranks push to this rank
     // (a region of its own, so ranks still streaming are never written into)
     constexpr int RECV_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
-    constexpr int RECV_BYTES = (MODE == DENSE) ? PART_BYTES : 0;
+    // MoE: the group's per-column epilogue scales [2][NCOL] (guard inverse, routing weight)
+    constexpr int RECV_BYTES = (MODE == DENSE) ? PART_BYTES : 2 * NCOL * 4;
     constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
     float* part = reinterpret_cast<float*>(smem + PART_OFF);
     float* recv = reinterpret_cast<float*>(smem + RECV_OFF);
@@ -378,8 +379,10 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
             // walk every stage in order; this lane issues the ones that land in slot s
             int gi = 0, slot = 0;
             uint32_t phase = 0;
+            Item nxt = get_item(first);
             for (int idx = first; idx < nitems && ok; idx += stride) {
-                const Item it = get_item(idx);
+                const Item it = nxt;
+                if (MODE != DENSE && idx + stride < nitems) nxt = get_item(idx + stride);
                 for (int grp = 0; grp < it.ngroups && ok; ++grp) {
                     for (int i = 0; i < nst; ++i, ++gi) {
                         const int my = slot == s && !(pre && gi == s);
@@ -429,12 +432,28 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
                                           (((((uint32_t)c >> 1)) ^ (4u * (uint32_t)(g & 1)) ^ (4u * kqv)) << 4)
                                     : (uint32_t)(512 * g) | ((((uint32_t)c) ^ (4u * (uint32_t)(g & 1)) ^ (4u * kqv)) << 4);
         uint32_t slot = 0, phase = 0;             // ring position of the next stage (same walk as the producers)
+        // MoE: the next item's expert and columns are read while this one streams, and the
+        // group's per-column epilogue scales (thread t < NCOL: column t) before its stages, so
+        // their loads' latency hides behind the MMAs; they reach the epilogue through shared memory
+        float* escol = reinterpret_cast<float*>(smem + RECV_OFF);
+        Item nxt = get_item(first);
         for (int idx = first; idx < nitems; idx += stride) {
-          const Item it = get_item(idx);
+          const Item it = nxt;
+          if (MODE != DENSE && idx + stride < nitems) nxt = get_item(idx + stride);
           const int64_t col0 = it.col0, ncols_total = it.ncols;
           const int rb = it.rb;
           for (int grp = 0; grp < it.ngroups; ++grp) {
             const int64_t cbase = (int64_t)grp * NCOL;
+            float eca = 0.f, ecw = 0.f;   // DOWN: guard inverse and routing weight; GATEUP: guard inverse
+            if (MODE != DENSE && threadIdx.x < NCOL && cbase + (int)threadIdx.x < ncols_total) {
+                const int64_t pos = col0 + cbase + threadIdx.x;
+                if (MODE == DOWN) {
+                    eca = p.rsa[pos];
+                    ecw = p.w[p.perm[pos]];
+                } else {
+                    eca = p.rsx[pos];
+                }
+            }
             float acc[MT][NT][4];
 #pragma unroll
             for (int a = 0; a < MT; ++a)
@@ -639,6 +658,10 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
             // (dense: part aliases the ring, so every warp must be done with it; the k
             // halves of KW == 2 are added in a fixed order)
             if (MODE == DENSE) asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
+            if (MODE != DENSE && threadIdx.x < NCOL) {   // read after the barrier below
+                escol[threadIdx.x] = eca;
+                escol[NCOL + threadIdx.x] = ecw;
+            }
 #pragma unroll
             for (int h = 0; h < KW; ++h) {
                 if (kq == h) {
@@ -673,7 +696,7 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
                         const int64_t q = cbase + col;
                         if (q >= ncols_total) continue;
                         const int64_t pos = col0 + q;
-                        const float sc = p.rsx[pos];
+                        const float sc = escol[col];
                         const float gv = part[i * NCOL + col] * sc;
                         const float uv = part[(RB / 2 + i) * NCOL + col] * sc;
                         p.out[pos * p.I + (int64_t)rb * (RB / 2) + i] = gv / (1.0f + expf(-gv)) * uv;
@@ -684,7 +707,7 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
                         const int64_t q = cbase + col;
                         if (q >= ncols_total) continue;
                         const int64_t pos = col0 + q;
-                        const float v = part[r * NCOL + col] * p.rsa[pos] * p.w[p.perm[pos]];
+                        const float v = part[r * NCOL + col] * escol[col] * escol[NCOL + col];
                         p.out[pos * p.H + (int64_t)rb * RB + r] = v;
                     }
                 }
@@ -835,7 +858,7 @@ constexpr size_t smem_bytes() {
     constexpr int RING = NSLOT * G::BYTES;
     constexpr int PART_BYTES = RB * NCOL * 4;
     constexpr int RECV_OFF = (MODE == DENSE) ? (RING > PART_BYTES ? RING : PART_BYTES) : RING + PART_BYTES;
-    constexpr int BAR_OFF = RECV_OFF + ((MODE == DENSE) ? PART_BYTES : 0);
+    constexpr int BAR_OFF = RECV_OFF + ((MODE == DENSE) ? PART_BYTES : 2 * NCOL * 4);
     return (size_t)BAR_OFF + 2 * NSLOT * 8 + 16 + 1024;   // + abort, never and last flags
 }
 
