@@ -260,6 +260,13 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
     for (int pass = 0; pass < npass; ++pass) {
         const int ub = u0 + pass * upp, nu = min(upp, u1 - ub);
         const bool lo_ok = 2 * tile < nu, hi_ok = 2 * tile + 1 < nu;
+        // Q8-row: the epilogue's row scales (rows g, g + 8 of the tile), loaded before the stages
+        float rsc[2] = {1.f, 1.f};
+        if (FMT == 1 && part == 0 && lo_ok) {
+            const int64_t n0 = (int64_t)(ub + 2 * tile) * UNIT + g;
+            if (n0 < p.N) rsc[0] = p.rs[n0];
+            if (hi_ok && n0 + 8 < p.N) rsc[1] = p.rs[n0 + 8];
+        }
         float acc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -374,7 +381,7 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
             for (int hr = 0; hr < 2; ++hr) {
                 const int64_t n = n0 + 8 * hr;
                 if ((hr == 1 && !hi_ok) || n >= p.N) continue;
-                const float sc = FMT == 1 ? p.rs[n] : 1.f;
+                const float sc = rsc[hr];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll

@@ -237,6 +237,14 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
     const CUtensorMap* tmS = &maps.s[jz];
     const CUtensorMap* tmX = &maps.x[jz];
     pdl_launch_dependents();   // the next kernel in the stream may be scheduled now
+    // dense Q8: the epilogue's row scale of this thread's row (tid % RB; weights-side data,
+    // never written by this library, so read before waiting for the previous kernel)
+    float rs_pre = 1.f;
+    if (MODE == DENSE && FMT == 1 && warp < CONSUMERS) {
+        const float* const RSj = jz == 0 ? p.rsj[0] : jz == 1 ? p.rsj[1] : jz == 2 ? p.rsj[2] : p.rsj[3];
+        const int64_t n = (int64_t)blockIdx.y * RB + (threadIdx.x & (RB - 1));
+        if (n < p.N) rs_pre = RSj[n];
+    }
     // ---- work items: (expert, row block) pairs; each may hold several column groups ----
     // dense: one item per CTA (row block blockIdx.y, k range blockIdx.x of the cluster);
     // MoE: a static round-robin share of (active expert x row block), so the
@@ -829,7 +837,8 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
                     for (int q = 0; q < p.ks; ++q) s += recv[q * per + (e - lo)];
                     const int64_t n = (int64_t)rb * RB + r, t = col;
                     if (n < p.N && t < p.T) {
-                        float v = s * (FMT == 1 ? RSj[n] * (p.rsx ? p.rsx[t] : 1.f) : (RAW ? 1.f : p.rsx[t]));
+                        const float rsn = r == (int)(threadIdx.x & (RB - 1)) ? rs_pre : RSj[n];
+                        float v = s * (FMT == 1 ? rsn * (p.rsx ? p.rsx[t] : 1.f) : (RAW ? 1.f : p.rsx[t]));
                         if (p.add) v += p.add[t * p.N + n];
                         if (p.yt == CQ_F32) reinterpret_cast<float*>(Yj)[t * p.ldy + n] = v;
                         else reinterpret_cast<__nv_bfloat16*>(Yj)[t * p.ldy + n] = __float2bfloat16_rn(v);
@@ -841,7 +850,8 @@ k_skinny(const __grid_constant__ SMaps maps, const Params p) {
                 const int r = e & (RB - 1), col = e / RB;
                 const int64_t n = (int64_t)rb * RB + r, t = col;
                 if (n < p.N && t < p.T) {
-                    float v = part[r * NCOL + col] * (FMT == 1 ? RSj[n] * (p.rsx ? p.rsx[t] : 1.f) : (RAW ? 1.f : p.rsx[t]));
+                    const float rsn = r == (int)(threadIdx.x & (RB - 1)) ? rs_pre : RSj[n];
+                    float v = part[r * NCOL + col] * (FMT == 1 ? rsn * (p.rsx ? p.rsx[t] : 1.f) : (RAW ? 1.f : p.rsx[t]));
                     if (p.add) v += p.add[t * p.N + n];
                     if (p.yt == CQ_F32) reinterpret_cast<float*>(Yj)[t * p.ldy + n] = v;
                     else reinterpret_cast<__nv_bfloat16*>(Yj)[t * p.ldy + n] = __float2bfloat16_rn(v);
