@@ -65,3 +65,30 @@ def test_batched_four_jobs_two_activation_slices_gapped_output(T):
     tensor-core path); the outputs leave gaps in Y that must stay untouched."""
     K, N = 512, 136
     _run(9500 + T, T, K, N, [0, K, 0, K], [8, 152, 296, 440], 2 * K, 600, "bf16", "f32")
+
+
+def test_batched_tail_launch(capfd):
+    """z = 2 jobs of T = 256, K = 1536, N = 10240 in 256-token tiles: 80 row tiles
+    x 2 jobs leave a partial last wave, so the last row tiles of both jobs go to
+    a K-split tail launch (trace line "tail"); outputs sampled over every row and
+    densely over the last 1024 rows of each job."""
+    from cqtest import Opt, sample_positions, traced_kernels
+    T, K, N = 256, 1536, 10240
+    rng = np.random.default_rng(9600)
+    xv = synth.draw_x(rng, T, K, 1.0, "bf16")
+    packed = [(pack.pack_q4(c), s) for c, s in (synth.draw_q4(rng, N, K, signed=True) for _ in range(2))]
+    X = torch.from_numpy(xv.view(np.int16)).view(TORCH_DT["bf16"]).to(DEV)
+    Y = torch.full((T, 2 * N), float("nan"), dtype=torch.float32, device=DEV)
+    jobs = [(to_dev(q), to_dev(s), 0, j * N) for j, (q, s) in enumerate(packed)]
+    ws = torch.empty(cq.cq_gemm_q4_batched_workspace_bytes(T, K, 2), dtype=torch.uint8, device=DEV)
+    with Opt(cq.CQ_OPT_TC_BN, 256):
+        trace = traced_kernels(capfd, lambda: cq.cq_gemm_q4_batched(X, K, jobs, N, Y, ws))
+    assert any(l.startswith("cq: tcgen05 tail") for l in trace), trace
+    assert cq.cq_get_device_error() == 0
+    y = y_host(Y)
+    Xf = oracle.x_to_f64(xv, "bf16")
+    for j, (q, s) in enumerate(packed):
+        tn = np.concatenate([sample_positions(T, N, 1500, 9601 + j),
+                             np.stack([rng.integers(0, T, 2000), rng.integers(N - 1024, N, 2000)], 1)]).astype(np.int64)
+        yref, S = oracle.gemm_q4_sampled(q, s, N, K, Xf, tn)
+        check(y[:, j * N:(j + 1) * N][tn[:, 0], tn[:, 1]], yref, S, "f32", f"batched job {j} with a tail launch")
