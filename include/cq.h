@@ -327,9 +327,10 @@ typedef enum {
     CQ_OPT_TC_BN = 5,        /* tcgen05 token tile: 0 auto (default), or 32, 64, 128, 192 (CTA pairs only, no K split), 256 */
     CQ_OPT_TC_KSPLIT = 6,    /* tcgen05 K split over a 2-CTA cluster (partials exchanged in shared memory): 0 auto, 1, 2 */
     CQ_OPT_TC_AMODE = 7,     /* decoded weight operand of the tcgen05 MMA: 0 auto (tensor memory), 1 shared, 2 tensor memory */
-    CQ_OPT_TC_PAIR = 8,      /* tcgen05, 256-column tiles with decoded weights in tensor memory: 0 auto / 2 on
-                                (neighbouring weight-row tiles share one 256-row MMA on a CTA pair, each CTA
-                                loading half of the activation tile; needs an even number of row tiles), 1 off */
+    CQ_OPT_TC_PAIR = 8,      /* tcgen05 CTA pairs (neighbouring weight-row tiles share one 256-row MMA, each
+                                CTA loading half of the activation tile; decoded weights in tensor memory, an
+                                even number of row tiles): 2 on, 1 off, 0 auto (on, except Q4 256-column
+                                tiles, which measured faster unpaired) */
     CQ_OPT_STREAM_KERNEL = 9 /* weight-streaming kernel: 2 the row-partitioned kernel (one CTA per SM, each
                                 streaming the whole K of an equal share of the weight rows) wherever it serves
                                 (one job, K % 512 == 0, T <= 32; Q8/32: T <= 16), 1 the K-split cluster
