@@ -980,7 +980,7 @@ cudaError_t launch_q4_tmem_one(const TcArgs& a, const Params& p, const Plan& pl,
     }
     if (pair && bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 4, 4, 12, 1, 2, 2, GU>(a, p, grid, s) : launch_bn<0, 128, 0, 4, 4, 12, 1, 1, 2, GU>(a, p, grid, s);
     if (pair) return ks == 2 ? launch_bn<0, 256, 0, 2, 5, 8, 1, 2, 2, GU>(a, p, grid, s) : launch_bn<0, 256, 0, 2, 5, 8, 1, 1, 2, GU>(a, p, grid, s);
-    if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 1, 6, 8, 1, 2, 1, GU>(a, p, grid, s) : launch_bn<0, 256, 0, 1, 6, 8, 1, 1, 1, GU>(a, p, grid, s);
+    if (bn == 256) return ks == 2 ? launch_bn<0, 256, 0, 2, 3, 8, 1, 2, 1, GU>(a, p, grid, s) : launch_bn<0, 256, 0, 2, 3, 8, 1, 1, 1, GU>(a, p, grid, s);
     if (bn == 128) return ks == 2 ? launch_bn<0, 128, 0, 2, 5, 12, 1, 2, 1, GU>(a, p, grid, s) : launch_bn<0, 128, 0, 2, 5, 12, 1, 1, 1, GU>(a, p, grid, s);
     return launch_bn<0, 64, 0, 4, 4, 12, 1, 1, 1, GU>(a, p, grid, s);
 }
