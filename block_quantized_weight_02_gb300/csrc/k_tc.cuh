@@ -973,7 +973,7 @@ template <int GU>
 cudaError_t launch_q4_tmem_one(const TcArgs& a, const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
     const int bn = pl.bn, ks = pl.ks;
     const bool pair = (bn >= 128 || bn == 32) && pl.pair_ok;
-    if (bn == 192) return launch_bn<0, 192, 0, 2, 6, 8, 1, 1, 2, GU>(a, p, grid, s);
+    if (bn == 192) return launch_bn<0, 192, 0, 4, 3, 8, 1, 1, 2, GU>(a, p, grid, s);
     if (bn == 32) {
         if (pair) return ks == 2 ? launch_bn<0, 32, 0, 4, 8, 12, 1, 2, 2, GU>(a, p, grid, s) : launch_bn<0, 32, 0, 4, 8, 12, 1, 1, 2, GU>(a, p, grid, s);
         return ks == 2 ? launch_bn<0, 32, 0, 4, 6, 12, 1, 2, 1, GU>(a, p, grid, s) : launch_bn<0, 32, 0, 4, 6, 12, 1, 1, 1, GU>(a, p, grid, s);
