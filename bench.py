@@ -202,6 +202,84 @@ def _moe_routed_calls(cq, m, dev):
                  h2d=[X, lg], d2h=[Y], counter=counter)], touched
 
 
+_HOST_CACHE = {}
+
+
+def _host_arrays(key, fn):
+    """Seeded host inputs built once per process (the rotating sets copy them to the device)."""
+    if key not in _HOST_CACHE:
+        _HOST_CACHE[key] = fn()
+    return _HOST_CACHE[key]
+
+
+def _batched_calls(cq, dev):
+    """z-batched Q4: three weights of one shape sharing one X (a qkv projection),
+    T=512, K=N=4096 each, outputs side by side in Y[512][3*4096] bf16."""
+    import torch
+    from block_quantized_weight_02_gb300 import pack, synth
+    T, K, N, z = 512, 4096, 4096, 3
+
+    def draw():
+        rng = np.random.default_rng(11)
+        x = synth.draw_x(rng, T, K, 1.0, "bf16")
+        ws = [synth.draw_q4(rng, N, K) for _ in range(z)]
+        return x, [(pack.pack_q4(c), np.ascontiguousarray(sc).view(np.uint16)) for c, sc in ws]
+    x, packed = _host_arrays("batched", draw)
+    X = _dev_x(x, "bf16", dev)
+    jobs = [(torch.from_numpy(q).to(dev), _u16(sc, dev), 0, j * N) for j, (q, sc) in enumerate(packed)]
+    Y = torch.empty(T, z * N, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(cq.cq_gemm_q4_batched_workspace_bytes(T, K, z), dtype=torch.uint8, device=dev)
+    wbytes = z * (N * K // 2 + N * K // 32 * 2)
+    return [Call("qkv z=3 q4->bf16", lambda: cq.cq_gemm_q4_batched(X, K, jobs, N, Y, ws), 2.0 * T * z * N * K, wbytes,
+                 X.numel() * 2 + Y.numel() * 2, h2d=[X], d2h=[Y])]
+
+
+def _format_calls(cq, dev):
+    """The format variants at K=N=4096, bf16 out, each at T=8 (weight streaming) and
+    T=512 (tcgen05): Q8 per 32-k block, affine Q4 (one bf16 offset per 2 blocks) and
+    q8_2f (int8 times a column field, f32 row scale)."""
+    import torch
+    from block_quantized_weight_02_gb300 import pack, synth
+    K, N, gk = 4096, 4096, 2
+
+    def draw():
+        rng = np.random.default_rng(12)
+        q8 = rng.integers(-127, 128, (N, K)).astype(np.int8)
+        s8b = (rng.uniform(1e-3, 1e-2, (N, K // 32)) * np.where(rng.random((N, K // 32)) < 0.5, -1, 1)).astype(np.float32)
+        codes, sc = synth.draw_q4(rng, N, K, signed=True)
+        off = synth.f32_to_bf16_bits(rng.uniform(-0.15, 0.15, (N, K // 32 // gk)).astype(np.float32))
+        rs = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+        col = rng.uniform(0.25, 4.0, K).astype(np.float16).astype(np.float32)
+        xs = {T: synth.draw_x(rng, T, K, 1.0, "bf16") for T in (8, 512)}
+        return q8, s8b, pack.pack_q4(codes), np.ascontiguousarray(sc).view(np.uint16), off, rs, col, xs
+    q8, s8b, q4p, sc, off, rs, col, xs = _host_arrays("formats", draw)
+    Q8 = torch.from_numpy(q8).to(dev)
+    S8B = torch.from_numpy(s8b).to(dev)
+    Q4 = torch.from_numpy(q4p).to(dev)
+    SC = _u16(sc, dev)
+    OFF = _u16(off, dev)
+    RS = torch.from_numpy(rs).to(dev)
+    COL = torch.from_numpy(col).to(dev)
+    calls = []
+    for T in (8, 512):
+        X = _dev_x(xs[T], "bf16", dev)
+        fl = 2.0 * T * N * K
+        xb = X.numel() * 2 + T * N * 2
+        Yb = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+        wsb = torch.empty(cq.cq_gemm_q8b_workspace_bytes(T, K), dtype=torch.uint8, device=dev)
+        calls.append(Call(f"T{T} q8b->bf16", (lambda X=X, Y=Yb, ws=wsb: cq.cq_gemm_q8b(X, Q8, S8B, Y, ws)), fl,
+                          N * K + N * K // 32 * 4, xb, h2d=[X], d2h=[Yb]))
+        Ya = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+        wsa = torch.empty(cq.cq_gemm_q4a_workspace_bytes(T, K, N, gk), dtype=torch.uint8, device=dev)
+        calls.append(Call(f"T{T} q4a->bf16", (lambda X=X, Y=Ya, ws=wsa: cq.cq_gemm_q4a(X, Q4, SC, OFF, gk, Y, ws)), fl,
+                          N * K // 2 + N * K // 32 * 2 + N * K // 32 // gk * 2, xb, h2d=[X], d2h=[Ya]))
+        Yf = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+        wsf = torch.empty(cq.cq_gemm_q8_2f_workspace_bytes(T, K), dtype=torch.uint8, device=dev)
+        calls.append(Call(f"T{T} q8_2f->bf16", (lambda X=X, Y=Yf, ws=wsf: cq.cq_gemm_q8_2f(X, Q8, RS, COL, Y, ws)), fl,
+                          N * K + 4 * N + 4 * K, xb, h2d=[X], d2h=[Yf]))
+    return calls
+
+
 def _dtype_of(name, info):
     """The arithmetic each call of the workload runs in: the tcgen05 path (T > 32)
     multiplies guarded fp16 activations by fp16 weights; the weight-streaming path
@@ -212,10 +290,14 @@ def _dtype_of(name, info):
         return "q4:fp16xfp16->f32"
     if name == "smallest_q4":
         return "q4:fp16xfp16->f32"
+    if name == "formats_4096":
+        return ("T8: q8b/q4a bf16xbf16->f32, q8_2f fp16xfp16->f32; "
+                "T512: q8b/q8_2f/q4a fp16xfp16->f32")
     T = info.get("T", 0)
     q4 = "q4:bf16xbf16->f32" if T <= 32 else "q4:fp16xfp16->f32"
     if name == "prefill_projection_4096":
         return q4 + ", q8row:bf16xbf16->f32"
+
     if name.startswith("sweep_q8"):
         return "q8row:bf16xbf16->f32"
     return q4
@@ -253,6 +335,12 @@ def build_workload(name, dev, max_sets=16):
         calls, touched = _moe_calls(cq, m, dev)
         info = {"T": 32, "H": 2048, "I": 768, "E": 128, "topk": 8, "touched_experts": touched, "outputs": ["f32"]}
         return (lambda: [calls]), info, 1
+    elif name == "batched_qkv_4096":
+        make = lambda: _batched_calls(cq, dev)
+        info = {"T": 512, "K": 4096, "N": 4096, "z": 3, "shared_x": True, "formats": ["q4"], "outputs": ["bf16"]}
+    elif name == "formats_4096":
+        make = lambda: _format_calls(cq, dev)
+        info = {"T": [8, 512], "K": 4096, "N": 4096, "formats": ["q8b", "q4a", "q8_2f"], "outputs": ["bf16"]}
     elif name.startswith("sweep_q4_T") or name.startswith("sweep_q8_T"):
         T = int(name.split("_T")[1])
         if "q4" in name:
@@ -338,7 +426,8 @@ def whole_job_rate(units_per_step: float, world: int, ms_per_step_max: float) ->
     return units_per_step * world / (ms_per_step_max * 1e-3)
 
 
-PER_CONFIG = (["smallest_q4", "prefill_projection_4096", "denoiser_ffn_chain", "moe_panels", "moe_routed_from_logits"]
+PER_CONFIG = (["smallest_q4", "prefill_projection_4096", "denoiser_ffn_chain", "moe_panels", "moe_routed_from_logits",
+               "batched_qkv_4096", "formats_4096"]
               + [f"sweep_{f}_T{t}" for f in ("q4", "q8") for t in (1, 8, 32, 128, 512, 2048)])
 
 TRAFFIC_MD = os.path.join(ROOT, "profiles", "traffic_per_call.md")

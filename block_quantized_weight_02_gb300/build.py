@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcq.so")
-SOURCES = ["cq_api.cu", "k_aux.cu", "k_skinny.cu", "k_tc.cu", "k_tc_ffn.cu", "k_tc_q8b.cu", "k_rows.cu", "cq_noalloc.cu"]
+SOURCES = ["cq_api.cu", "k_aux.cu", "k_skinny.cu", "k_tc.cu", "k_tc_ffn.cu", "k_tc_q4a.cu", "k_tc_q8b.cu", "k_rows.cu", "cq_noalloc.cu"]
 HEADERS = ["cq_internal.h", "cq_ptx.cuh", "k_tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

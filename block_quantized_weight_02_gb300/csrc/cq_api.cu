@@ -599,18 +599,21 @@ cq_status cq_gemm_q4a(const void* X, int xt, int64_t T, int64_t K, const uint8_t
     const Q4Ws w = q4_ws(ws, T, K);
     float* xs = reinterpret_cast<float*>(b + q4_ws_bytes(T, K));
     float* add = reinterpret_cast<float*>(b + q4_ws_bytes(T, K) + up((size_t)T * (size_t)(K / 32 / gk) * 4));
-    // the offsets' term sum_g off[n][g] * (sum of X over group g), added by the GEMM's epilogue
-    if ((st = launched(launch_offset_term(X, xt, T, K, Wo, (int)gk, N, xs, add, s), "affine Q4 offset term"))) return st;
     if (use_skinny(T)) {
         if (T > 32) return fail(CQ_ERR_ARG, "cq_gemm_q4a: the weight-streaming path serves T <= 32");
+        // the offsets' term sum_g off[n][g] * (sum of X over group g), added by the GEMM's epilogue
+        if ((st = launched(launch_offset_term(X, xt, T, K, Wo, (int)gk, N, xs, add, s), "affine Q4 offset term")))
+            return st;
         SkinnyDense a = {X, xt == CQ_BF16 ? 1 : 0, nullptr, nullptr, Wq, Ws, T, K, N, Y, yt, err};
         a.add = add;
         return launched(launch_skinny_q4(a, s), "weight-streaming affine Q4 GEMM");
     }
+    // tcgen05: the offsets join the weight decode, fp16((nibble - 8) * scale + offset) in one rounding
     if ((st = launched(launch_x_half(X, xt, T, K, w.xh, w.rsx, s), "activation guard pass"))) return st;
     TcArgs a = {w.xh, 0, w.rsx, nullptr, Wq, Ws, T, K, N, Y, yt, err};
-    a.add = add;
-    return launched(launch_tc_q4(a, s), "tcgen05 affine Q4 GEMM");
+    a.off = Wo;
+    a.gk = (int)gk;
+    return launched(launch_tc_q4a(a, s), "tcgen05 affine Q4 GEMM");
 }
 
 size_t cq_ffn_q4_workspace_bytes(int64_t T, int64_t H, int64_t I) {

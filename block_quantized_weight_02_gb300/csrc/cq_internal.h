@@ -183,10 +183,13 @@ struct TcArgs {
     int64_t ldy;         // output row pitch in elements (0: N)
     const float* wsf;    // single job: Q8/32 block scales
     const float* add;    // single job: addend
+    const uint16_t* off; // affine Q4 (single job): offsets bf16 [N][K/32/gk], joined to the decode
+    int gk;              // blocks per offset group
     TcJob job(int j) const { return nz > 1 ? more[j] : TcJob{x, rsx, rs, wq, ws, y, wsf, add}; }
     int jobs() const { return nz > 1 ? nz : 1; }
 };
 cudaError_t launch_tc_q4(const TcArgs& a, cudaStream_t s);
+cudaError_t launch_tc_q4a(const TcArgs& a, cudaStream_t s);   // affine Q4: off, gk set, one job
 cudaError_t launch_tc_q8(const TcArgs& a, cudaStream_t s);   // x fp16 or bf16; rsx nullable (q8_2f: the guard)
 // Q8 per 32-k block: x guarded fp16 in k order, rsx its scales, wsf the f32 block scales.
 cudaError_t launch_tc_q8b(const TcArgs& a, cudaStream_t s);

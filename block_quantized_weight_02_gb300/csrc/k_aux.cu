@@ -464,26 +464,59 @@ __global__ void __launch_bounds__(256) k_group_sums(const T* __restrict__ x, int
     if (lane == 0) xs[wid] = s;
 }
 
-// add[t][n] = sum_g m[n][g] * xs[t][g]: a CTA of 128 threads takes 128 rows n
-// and 8 tokens; xs of those tokens is staged in shared memory (G <= 512).
-__global__ void __launch_bounds__(128) k_offset_term(const uint16_t* __restrict__ off, const float* __restrict__ xs,
+// add[t][n] = sum_g m[n][g] * xs[t][g] (g in order, one fused multiply-add each): a
+// CTA of 256 threads takes 128 rows n and 32 tokens t, the offsets and group sums
+// staged through shared memory 32 groups at a time with coalesced loads; thread
+// (tx, ty) computes rows tx + 32 i and tokens ty + 8 j (i, j < 4).
+__global__ void __launch_bounds__(256) k_offset_term(const uint16_t* __restrict__ off, const float* __restrict__ xs,
                                                      int64_t Tn, int64_t N, int G, float* __restrict__ add) {
     pdl_launch_dependents();
     pdl_wait();
-    __shared__ float sx[8 * 512];
-    const int64_t t0 = (int64_t)blockIdx.y * 8;
-    const int nt = Tn - t0 < 8 ? (int)(Tn - t0) : 8;
-    for (int i = threadIdx.x; i < nt * G; i += 128) sx[i] = xs[t0 * G + i];
-    __syncthreads();
-    const int64_t n = (int64_t)blockIdx.x * 128 + threadIdx.x;
-    if (n >= N) return;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int g = 0; g < G; ++g) {
-        const float m = __uint_as_float((uint32_t)off[n * G + g] << 16);
+    __shared__ float sm[32][129];   // [g][row]
+    __shared__ float sx[32][33];    // [token][g]
+    const int64_t n0 = (int64_t)blockIdx.x * 128, t0 = (int64_t)blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    float acc[4][4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] = fmaf(m, sx[u * G + g], acc[u]);
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+        const int ng = G - g0 < 32 ? G - g0 : 32;
+        // offsets: row r = e / 32, group e % 32 (a warp reads 32 consecutive groups of one row)
+        for (int e = threadIdx.x; e < 128 * 32; e += 256) {
+            const int r = e >> 5, gg = e & 31;
+            const int64_t n = n0 + r;
+            sm[gg][r] = (gg < ng && n < N) ? __uint_as_float((uint32_t)off[n * G + g0 + gg] << 16) : 0.f;
+        }
+        for (int e = threadIdx.x; e < 32 * 32; e += 256) {
+            const int t = e >> 5, gg = e & 31;
+            sx[t][gg] = (gg < ng && t0 + t < Tn) ? xs[(t0 + t) * G + g0 + gg] : 0.f;
+        }
+        __syncthreads();
+        for (int gg = 0; gg < ng; ++gg) {
+            float m[4], x[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m[i] = sm[gg][tx + 32 * i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = sx[ty + 8 * j][gg];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(m[i], x[j], acc[i][j]);
+        }
+        __syncthreads();
     }
-    for (int u = 0; u < nt; ++u) add[(t0 + u) * N + n] = acc[u];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t t = t0 + ty + 8 * j;
+        if (t >= Tn) continue;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t n = n0 + tx + 32 * i;
+            if (n < N) add[t * N + n] = acc[i][j];
+        }
+    }
 }
 
 cudaError_t launch_offset_term(const void* x, int xt, int64_t T, int64_t K, const uint16_t* off, int gk, int64_t N,
@@ -495,7 +528,7 @@ cudaError_t launch_offset_term(const void* x, int xt, int64_t T, int64_t K, cons
                      T, K, gk, xs)
         : launch_pdl(k_group_sums<__half>, dim3(gs), dim3(256), 0, s, reinterpret_cast<const __half*>(x), T, K, gk, xs);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k_offset_term, dim3((unsigned)((N + 127) / 128), (unsigned)((T + 7) / 8)), dim3(128), 0, s, off,
+    return launch_pdl(k_offset_term, dim3((unsigned)((N + 127) / 128), (unsigned)((T + 31) / 32)), dim3(256), 0, s, off,
                       (const float*)xs, T, N, (int)G, add);
 }
 

@@ -35,7 +35,10 @@
 // int8 -> the activation type exactly; the row scale is applied to the f32
 // accumulator in the epilogue ("cortiq-engine 0.8.3 src/gpu_metal/qi21.rs",
 // module header on q8_row).
-// Gate/up mode (GU): the CTA's 128 weight rows are 64 gate rows i0 .. i0 + 63
+// Affine mode (GU = 2, Q4): a bf16 offset per group of gk blocks joins the
+// decode, fp16((n - 8) * scale + fp16(offset)) in one rounding ("oxinfer 0.0.5
+// src/metal.rs", Dequantizers, struct Q4A).
+// Gate/up mode (GU = 1): the CTA's 128 weight rows are 64 gate rows i0 .. i0 + 63
 // and the matching 64 up rows I + i0 .. (one 3-D TMA box over the two
 // halves of the [2I][K] matrix), and the epilogue applies SwiGLU,
 // a = g / (1 + exp(-g)) * u, writing a[T][I] in f32: the gate/up GEMM of the
@@ -45,8 +48,9 @@
 // flight land, frees its tensor memory and reports CQ_ERR_TIMEOUT in the
 // calling stream's device error word.
 //
-// Included by k_tc.cu (dense GEMMs) and k_tc_ffn.cu (gate/up mode), so that
-// the two sets of instantiations compile in parallel.
+// Included by k_tc.cu (dense GEMMs), k_tc_ffn.cu (gate/up mode), k_tc_q4a.cu
+// (affine mode) and k_tc_q8b.cu (Q8/32), so that the sets of instantiations
+// compile in parallel.
 #pragma once
 #include <algorithm>
 #include <cstring>
@@ -81,6 +85,8 @@ struct Maps {
 
 struct Params {
     Job job[ZMAX];
+    const uint16_t* off;  // affine mode (single job): offsets bf16 [N][K/32/gk]
+    int gk;               // blocks per offset group
     int mt0;              // first weight-row tile of this launch (a call may split its tiles over two)
     int tiles_y;          // token tiles per job
     int64_t ldy;          // output row pitch (elements)
@@ -117,6 +123,15 @@ __device__ __forceinline__ void decode_q4_word_scaled(uint32_t w, uint32_t sc, u
     o[1] = mul_f16x2(fma_f16x2(and_or<0x00F000F0u>(w, c6400), k16th, km72), sc);
     o[2] = mul_f16x2(sub_f16x2(and_or<0x000F000Fu>(w8, c6400), k1032), sc);
     o[3] = mul_f16x2(fma_f16x2(and_or<0x00F000F0u>(w8, c6400), k16th, km72), sc);
+}
+// The same with an affine offset m in both halves: (n - 8) * scale + m, rounded once.
+__device__ __forceinline__ void decode_q4_word_scaled_off(uint32_t w, uint32_t sc, uint32_t m, uint32_t* o) {
+    const uint32_t c6400 = 0x64006400u, k1032 = 0x64086408u, k16th = 0x2C002C00u, km72 = 0xD480D480u;
+    const uint32_t w8 = w >> 8;
+    o[0] = fma_f16x2(sub_f16x2(and_or<0x000F000Fu>(w, c6400), k1032), sc, m);
+    o[1] = fma_f16x2(fma_f16x2(and_or<0x00F000F0u>(w, c6400), k16th, km72), sc, m);
+    o[2] = fma_f16x2(sub_f16x2(and_or<0x000F000Fu>(w8, c6400), k1032), sc, m);
+    o[3] = fma_f16x2(fma_f16x2(and_or<0x00F000F0u>(w8, c6400), k16th, km72), sc, m);
 }
 
 template <int FMT>
@@ -221,7 +236,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // first weight row (gate/up mode: first gate row i0; the tile is i0 .. i0 + 63 and I + i0 ..)
-    const int m0 = (p.mt0 + (int)blockIdx.x) * (GU ? BM / 2 : BM);
+    const int m0 = (p.mt0 + (int)blockIdx.x) * (GU == 1 ? BM / 2 : BM);
     const int jz = (int)blockIdx.y / p.tiles_y;                 // job of a z-batched launch
     const int t0 = ((int)blockIdx.y - jz * p.tiles_y) * BN;    // first activation row
     const Job J = jz == 0 ? p.job[0] : jz == 1 ? p.job[1] : jz == 2 ? p.job[2] : p.job[3];
@@ -324,7 +339,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             auto issue = [&](int j) {
                 if (wl) {
                     mbar_arrive_expect_tx(full_bar(s), (uint32_t)(L::X_BYTES + L::W_BYTES));
-                    if (GU) tma_load_3d(base + L::X_BYTES, tmW, full_bar(s), (j0 + j) * L::WROW, m0, 0);
+                    if (GU == 1) tma_load_3d(base + L::X_BYTES, tmW, full_bar(s), (j0 + j) * L::WROW, m0, 0);
                     else tma_load_2d(base + L::X_BYTES, tmW, full_bar(s), (j0 + j) * L::WROW, m0);
                 } else {
                     tma_load_3d(base, tmX, full_bar(s), 0, t0 + cx * (BN / CG), (j0 + j) * G);
@@ -457,8 +472,8 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
         const int q4w = warp & 3, grp = warp >> 2;
         const int r = 32 * q4w + lane;             // weight row within the tile
         // its row of the weight matrix (gate/up mode: gate row m0 + r, or up row I + m0 + r - 64)
-        const int64_t n = GU ? (r < BM / 2 ? (int64_t)m0 + r : p.N + m0 + (r - BM / 2)) : (int64_t)m0 + r;
-        const bool row_ok = GU ? (int64_t)m0 + (r & (BM / 2 - 1)) < p.N : n < p.N;
+        const int64_t n = GU == 1 ? (r < BM / 2 ? (int64_t)m0 + r : p.N + m0 + (r - BM / 2)) : (int64_t)m0 + r;
+        const bool row_ok = GU == 1 ? (int64_t)m0 + (r & (BM / 2 - 1)) < p.N : n < p.N;
         const uint32_t xr = (uint32_t)(r & 7);
         const uint32_t t_lane = (uint32_t)(32 * q4w) << 16;
         // weight rows of G * ROW bytes: 128-byte swizzle (chunk c at c ^ (r % 8)), 64-byte
@@ -481,6 +496,25 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             if (grp < nk) sc0 = scale_pair(grp);
             if (grp + 4 < nk) sc1 = scale_pair(grp + 4);
         }
+        // Affine Q4: the offsets of stage kb's two blocks (2 kb, 2 kb + 1: groups of gk blocks,
+        // a shift where gk is a power of two) as an fp16 pair, prefetched like the scales
+        constexpr bool aff = GU == 2;
+        const uint16_t* orow = aff ? p.off + n * (p.K / 32 / p.gk) : nullptr;
+        const uint32_t gsh = (p.gk & (p.gk - 1)) == 0 ? (uint32_t)(__ffs(p.gk) - 1) : 32u;
+        auto offset_pair = [&](int kbi) -> uint32_t {
+            const uint32_t b0 = 2u * (uint32_t)(k0 + kbi);
+            const uint32_t g0 = gsh < 32u ? b0 >> gsh : b0 / (uint32_t)p.gk;
+            const uint32_t g1 = gsh < 32u ? (b0 + 1u) >> gsh : (b0 + 1u) / (uint32_t)p.gk;
+            const uint32_t ua = __ldg(orow + g0);
+            const uint32_t ub = g1 == g0 ? ua : (uint32_t)__ldg(orow + g1);
+            const __half2 h = __floats2half2_rn(__uint_as_float(ua << 16), __uint_as_float(ub << 16));
+            return *reinterpret_cast<const uint32_t*>(&h);
+        };
+        uint32_t mo0 = 0, mo1 = 0;
+        if (aff && row_ok) {
+            if (grp < nk) mo0 = offset_pair(grp);
+            if (grp + 4 < nk) mo1 = offset_pair(grp + 4);
+        }
         // Every group waits for every super-stage in order (decoding only its own stages
         // in it), so each round of each super-slot is waited for in order and a parity
         // wait never mistakes round r for round r - 2, whatever LSS is.
@@ -499,8 +533,9 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             const int a = kb % AS;                             // decoded slot
             const int rb = (kb / RS) % NRB;                    // its round's barriers
             const uint32_t rph = (uint32_t)((kb / AS) & 1);    // and their phase
-            uint32_t sc_next = 0;
+            uint32_t sc_next = 0, mo_next = 0;
             if (FMT != 1 && row_ok && kb + 8 < nk) sc_next = scale_pair(kb + 8);
+            if (aff && row_ok && kb + 8 < nk) mo_next = offset_pair(kb + 8);
             // the slot's previous round (NRB back) must have been consumed
             const int rp = kb / RS - NRB;
             const bool freed = MERGE ? (rp < 0 || mbar_wait_spin(empty_bar(rp % LSS), (uint32_t)((rp / LSS) & 1), p.wait_ns, abort_flag))
@@ -522,14 +557,26 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                 const uint4 v1 = ld_shared_v4(wrow + (((uint32_t)(2 * u + 1) ^ wsw) << 4));
                 // the block scales, each in both halves of a register
                 const uint32_t s0 = prmt(sc0, sc0, 0x1010u), s1 = prmt(sc0, sc0, 0x3232u);
-                decode_q4_word_scaled(v0.x, s0, o);
-                decode_q4_word_scaled(v0.y, s0, o + 4);
-                decode_q4_word_scaled(v0.z, s0, o + 8);
-                decode_q4_word_scaled(v0.w, s0, o + 12);
-                decode_q4_word_scaled(v1.x, s1, o + 16);
-                decode_q4_word_scaled(v1.y, s1, o + 20);
-                decode_q4_word_scaled(v1.z, s1, o + 24);
-                decode_q4_word_scaled(v1.w, s1, o + 28);
+                if (aff) {   // and the two offsets
+                    const uint32_t ma = prmt(mo0, mo0, 0x1010u), mb = prmt(mo0, mo0, 0x3232u);
+                    decode_q4_word_scaled_off(v0.x, s0, ma, o);
+                    decode_q4_word_scaled_off(v0.y, s0, ma, o + 4);
+                    decode_q4_word_scaled_off(v0.z, s0, ma, o + 8);
+                    decode_q4_word_scaled_off(v0.w, s0, ma, o + 12);
+                    decode_q4_word_scaled_off(v1.x, s1, mb, o + 16);
+                    decode_q4_word_scaled_off(v1.y, s1, mb, o + 20);
+                    decode_q4_word_scaled_off(v1.z, s1, mb, o + 24);
+                    decode_q4_word_scaled_off(v1.w, s1, mb, o + 28);
+                } else {
+                    decode_q4_word_scaled(v0.x, s0, o);
+                    decode_q4_word_scaled(v0.y, s0, o + 4);
+                    decode_q4_word_scaled(v0.z, s0, o + 8);
+                    decode_q4_word_scaled(v0.w, s0, o + 12);
+                    decode_q4_word_scaled(v1.x, s1, o + 16);
+                    decode_q4_word_scaled(v1.y, s1, o + 20);
+                    decode_q4_word_scaled(v1.z, s1, o + 24);
+                    decode_q4_word_scaled(v1.w, s1, o + 28);
+                }
             } else {
                 // stage u = chunks 4u .. 4u + 3 of the row, in k order; Q8/32: chunks 0, 1 are
                 // block 2 kb, chunks 2, 3 block 2 kb + 1, each pair times its fp16 block scale
@@ -571,6 +618,8 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             if (lane == 0) mbar_arrive(afull_bar(rb));
             sc0 = sc1;
             sc1 = sc_next;
+            mo0 = mo1;
+            mo1 = mo_next;
           }
           if (++s == LSS) {
               s = 0;
@@ -673,7 +722,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             const int esz = f32 ? 4 : 2;
             // the addend (affine offset term) only where a format uses it: its loads stay out of
             // the loop that stages the outputs
-            const float* addp = (FMT != 1 && !GU && row_ok) ? J.add : nullptr;
+            const float* addp = (FMT != 1 && GU != 1 && row_ok) ? J.add : nullptr;
 #pragma unroll 1
             for (int ci = 0; ci < CW / CH; ++ci) {
                 const int cc = grp * CW + ci * CH;
@@ -703,7 +752,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                 for (int jj = 0; jj < CH; ++jj) {
                     const int64_t t = tb + jj;
                     const float val = vals[jj];
-                    if (GU) {
+                    if (GU == 1) {
                         reinterpret_cast<float*>(smem + YST_OFF)[(cc + jj) * 128 + r] = val;
                     } else if (p.y_tma) {
                         if (f32) reinterpret_cast<float*>(smem + YST_OFF)[(cc + jj) * 128 + r] = val;
@@ -713,7 +762,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                         else reinterpret_cast<__nv_bfloat16*>(J.y)[t * p.ldy + n] = __float2bfloat16_rn(val);
                     }
                 }
-                if (GU) {
+                if (GU == 1) {
                     // SwiGLU over the staged chunk: gate rows in staged rows 0..63, up rows in
                     // 64..127; thread (q4w, lane) takes gate row i = lane + 32 (q4w % 2) and the
                     // chunk's columns q4w / 2, q4w / 2 + 2, ...  a[t][m0 + i] in f32, coalesced
@@ -772,7 +821,7 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
     // round barrier is waited for by fixed groups, every one of its rounds in order.
     static_assert(AS % L::RS == 0 && (L::RS == 4 || L::NRB % 2 == 0) && (G == 1 || G == 2 || G == 4),
                   "decoded slots owned by fixed decoder groups");
-    static_assert(GU == 0 || FMT == 0, "gate/up mode: Q4 weights");
+    static_assert(GU == 0 || FMT == 0, "gate/up and affine modes: Q4 weights");
     // weights: rows of G stages (G * ROW bytes) per box
     // one set of tensor maps per job (a z-batched launch holds up to ZMAX jobs of one shape)
     Maps maps;
@@ -783,7 +832,7 @@ cudaError_t launch_bn(const TcArgs& a, const Params& p, dim3 grid, cudaStream_t 
     const int64_t ldy = a.ldy > 0 ? a.ldy : a.N;
     for (int j = 0; j < a.jobs(); ++j) {
         const TcJob jb = a.job(j);
-        if (GU) {
+        if (GU == 1) {
             // [2][I][K bytes]: gate half, up half; one box = 64 gate rows then the 64 matching up rows
             uint64_t d[3] = {kbytes, (uint64_t)a.N, 2};
             uint64_t st[2] = {kbytes, kbytes * (uint64_t)a.N};
@@ -942,6 +991,8 @@ Params make_params(const TcArgs& a) {
         const TcJob jb = a.job(j);
         p.job[j] = {jb.rsx, jb.rs, jb.ws, jb.wsf, jb.add, jb.y};
     }
+    p.off = a.jobs() == 1 ? a.off : nullptr;
+    p.gk = a.gk > 0 ? a.gk : 1;
     p.mt0 = 0;
     p.tiles_y = 1;
     p.ldy = a.ldy > 0 ? a.ldy : a.N;
@@ -967,7 +1018,7 @@ void trace_plan(const char* what, int fmt, const TcArgs& a, const Plan& pl, bool
 }
 
 // Q4 with the decoded weights in tensor memory, every tile shape; GU selects the
-// gate/up (SwiGLU) mode.  <FMT, BN, XBF, G, LSS, AS, AM, KS, CG, GU>: super-stages
+// gate/up (SwiGLU, 1) or the affine (2) mode.  <FMT, BN, XBF, G, LSS, AS, AM, KS, CG, GU>: super-stages
 // of G stages, as many super-slots as fit next to the decoded slots.
 template <int GU>
 cudaError_t launch_q4_tmem_one(const TcArgs& a, const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {

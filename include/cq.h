@@ -163,10 +163,13 @@ cq_status cq_gemm_q4_batched(const void* X, int xt, int64_t T, int64_t K, int64_
  * Affine Q4 ("oxinfer 0.0.5 src/metal.rs", Dequantizers, struct Q4A and
  * load(Q4A ...)): the Q4 split plane Wq, Ws plus Wo bf16 [N][K/32/gk], one
  * offset per group of gk blocks of 32;  W[n][k] = (nibble - 8) * scale +
- * Wo[n][(k/32)/gk].  Computed as the Q4 GEMM plus the offsets' term
- * sum_g Wo[n][g] * (sum of X[t] over group g) (f32), added before the
- * output's rounding.  Shape rules: as cq_gemm_q4, gk >= 1 dividing K/32,
- * K/32/gk <= 512.
+ * Wo[n][(k/32)/gk].  Weight streaming (T <= 32): the Q4 GEMM plus the
+ * offsets' term sum_g Wo[n][g] * (sum of X[t] over group g) (f32), added
+ * before the output's rounding.  tcgen05 (T > 32): the offset joins the
+ * decode, each weight fp16((nibble - 8) * scale + fp16(Wo)) with one
+ * rounding (the bf16 offset reaches fp16 exactly in fp16's normal range), so
+ * the decoded weights must lie in fp16's range, as for cq_gemm_q4.
+ * Shape rules: as cq_gemm_q4, gk >= 1 dividing K/32, K/32/gk <= 512.
  *
  * q8_2f ("cortiq-engine 0.8.3 src/gpu_metal/qi21.rs", module header: int8
  * weights staged times the column field, the row scale in the epilogue; the
@@ -326,7 +329,8 @@ typedef enum {
     CQ_OPT_TRACE = 4,        /* 1 prints the chosen path and grid of each call to stderr */
     CQ_OPT_TC_BN = 5,        /* tcgen05 token tile: 0 auto (default), or 32, 64, 128, 192 (CTA pairs only, no K split), 256 */
     CQ_OPT_TC_KSPLIT = 6,    /* tcgen05 K split over a 2-CTA cluster (partials exchanged in shared memory): 0 auto, 1, 2 */
-    CQ_OPT_TC_AMODE = 7,     /* decoded weight operand of the tcgen05 MMA: 0 auto (tensor memory), 1 shared, 2 tensor memory */
+    CQ_OPT_TC_AMODE = 7,     /* decoded weight operand of the tcgen05 MMA: 0 auto (tensor memory), 1 shared, 2 tensor memory
+                                (affine Q4 and the gate/up GEMM: tensor memory always) */
     CQ_OPT_TC_PAIR = 8,      /* tcgen05 CTA pairs (neighbouring weight-row tiles share one 256-row MMA, each
                                 CTA loading half of the activation tile; decoded weights in tensor memory, an
                                 even number of row tiles): 2 on, 1 off, 0 auto (on, except Q4 256-column

@@ -94,6 +94,44 @@ def test_q4a(path, T, K, N, gk, out):
     check(y_host(Y), yref, S, out, f"affine q4 path={path} T={T} K={K} N={N} gk={gk} {out}")
 
 
+@pytest.mark.parametrize("T,bn,ks", [(40, 0, 0), (64, 64, 1), (150, 128, 2), (300, 256, 1), (256, 192, 1)])
+@pytest.mark.parametrize("gk", [1, 4])
+def test_q4a_tcgen05_decoder_bit_exact_identity(T, bn, ks, gk):
+    """X[t] = e_{k_t}.  The tcgen05 decoder takes the bf16 offset to fp16
+    (RNE) and forms (nibble - 8) * scale + offset in one fp16 rounding; the
+    guard scales the unit row to 2^13 and back exactly, so Y[t][n] =
+    RNE_fp16(W4[n][k_t] + RNE_fp16(off)), W4 the oracle's plain Q4 weight
+    (exact), the sum taken exactly in f64."""
+    K, N = 512, 264
+    rng = np.random.default_rng(9600 + T + bn + gk)
+    codes = rng.integers(0, 16, (N, K), dtype=np.uint8)
+    codes[:, ::7] = 8
+    sc = (rng.uniform(0.005, 0.02, (N, K // 32)) * np.where(rng.random((N, K // 32)) < 0.5, -1, 1))
+    sc = sc.astype(np.float16).view(np.uint16)
+    sc[0, :4] = [0x0000, 0x8000, 0x0001, 0x83FF]   # +-0 and fp16 subnormal scales
+    ov = rng.uniform(0.01, 0.15, (N, K // 32 // gk)) * np.where(rng.random((N, K // 32 // gk)) < 0.5, -1, 1)
+    ov[1, :3] = [0.0, -0.0, 3.0e-6]                # zeros, and an offset below the fp16 normal range
+    off = synth.f32_to_bf16_bits(ov.astype(np.float32))
+    wq = pack.pack_q4(codes)
+    m16 = synth.bf16_bits_to_f32(off).astype(np.float16).astype(np.float64)
+    W = oracle.dequant_q4(wq, sc, N, K).astype(np.float64) + np.repeat(m16, 32 * gk, axis=1)
+    E = W.astype(np.float16).astype(np.float32)
+    kt = 32 * ((5 * np.arange(T) + 3) % (K // 32)) + (13 * np.arange(T) + 3) % 32
+    xv = np.zeros((T, K))
+    xv[np.arange(T), kt] = 1.0
+    x = synth.to_storage(xv, "bf16")
+    Y = torch.empty(T, N, dtype=torch.float32, device=DEV)
+    ws = torch.empty(cq.cq_gemm_q4a_workspace_bytes(T, K, N, gk), dtype=torch.uint8, device=DEV)
+    with ForcePath(2), Opt(cq.CQ_OPT_TC_BN, bn), Opt(cq.CQ_OPT_TC_KSPLIT, ks):
+        cq.cq_gemm_q4a(to_dev_x(x, "bf16"), to_dev(wq), to_dev(sc), to_dev(off), gk, Y, ws)
+    assert cq.cq_get_device_error() == 0
+    y = Y.cpu().numpy()
+    e = E[:, kt].T
+    assert np.array_equal(y == e, np.ones_like(y, bool)), f"{int((y != e).sum())} outputs differ"
+    nz = e != 0
+    assert np.array_equal(y[nz].view(np.uint32), e[nz].view(np.uint32))
+
+
 @pytest.mark.parametrize("path,T,K,N", [(1, *c) for c in STREAM] + [(2, *c) for c in TC])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
