@@ -260,10 +260,15 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mas
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
                  ::"r"(bar), "h"(cta_mask) : "memory");
 }
-// Arrival (release at cluster scope) on an mbarrier of another CTA of the cluster
-// (address from mapa_shared).
+// Arrival on an mbarrier of another CTA of the cluster (address from mapa_shared),
+// with the instruction's default semantics (release at CTA scope).  Used where the
+// data being announced never leaves the arriving SM: a CTA pair's decoded weights,
+// written to the odd CTA's own tensor memory (tcgen05.wait::st has completed the
+// stores and tcgen05.fence::before_thread_sync orders them before the arrival) and
+// read there by the pair's MMA.  Release at cluster scope measured about a
+// thousand cycles per arrival on GB300.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;

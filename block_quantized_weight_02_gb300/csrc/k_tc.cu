@@ -55,10 +55,7 @@ cudaError_t launch_one(int fmt, int xbf, int am, const Plan& pl, const TcArgs& a
 cudaError_t launch(int fmt, const TcArgs& a, cudaStream_t s) {
     const int xbf = fmt == 0 ? 0 : a.x_bf16;
     const int64_t mt = (a.N + BM - 1) / BM;
-    Plan pl = plan_tiles(a, mt, false);
-    // Q4 256-token tiles run unpaired unless pairs are forced: measured 2-5 % faster on
-    // GB300 for every configured shape that takes them (Q8-row: pairs faster)
-    if (fmt == 0 && pl.bn == 256 && options().tc_pair != 2) pl.pair_ok = false;
+    const Plan pl = plan_tiles(a, mt, false);
     Params p = make_params(a);
     p.tiles_y = (int)((a.T + pl.bn - 1) / pl.bn);
     dim3 grid((unsigned)mt, (unsigned)(p.tiles_y * a.jobs()), (unsigned)pl.ks);

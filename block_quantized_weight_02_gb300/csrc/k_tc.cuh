@@ -222,8 +222,9 @@ __device__ __forceinline__ uint32_t i8x2_to_bf2(uint32_t w, uint32_t sel) {
 // CG: CTA pairs along x (1 or 2).  With 2, two neighbouring weight-row tiles share
 // one 256-row MMA (cta_group::2): each CTA decodes its 128 rows into its own tensor
 // memory and loads half of the activation rows; the even CTA's MMA thread issues
-// for both once both CTAs' decoders have arrived on its barrier, and every release
-// it commits reaches both CTAs.  Each CTA's accumulator holds its rows x all BN
+// for both once both CTAs' decoders have arrived on its barrier (the odd CTA's
+// decoder warps arrive there directly, each after its tensor-memory stores have
+// completed), and every release it commits reaches both CTAs.  Each CTA's accumulator holds its rows x all BN
 // columns, so the epilogue is unchanged.  Cluster ranks run x fastest: the pair
 // peer is rank ^ 1, the K-split partner rank ^ CG.
 template <int FMT, int BN, int XBF, int G, int LSS, int AS, int AM, int KS, int CG, int GU>
@@ -279,8 +280,8 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
         }
         for (int rb = 0; rb < NRB; ++rb) {
             // one arrival per warp of each of the round's RS stages; in a pair the even CTA's
-            // barrier also takes the odd CTA's relayed arrival
-            mbar_init(afull_bar(rb), 4 * RS + (CG > 1 && leader ? 1 : 0));
+            // barrier takes both CTAs' (the odd CTA's barriers stay unused)
+            mbar_init(afull_bar(rb), (CG > 1 && leader ? 8 : 4) * RS);
             mbar_init(aempty_bar(rb), 1);       // the MMA's commit of the round
         }
         mbar_init(accf_bar, 1);
@@ -447,19 +448,6 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             // also lets teardown know every MMA has finished
             if (CG > 1) tc_commit_pair_mc(accf_bar, pair_mask);
             else tc_commit(accf_bar);
-        } else if (CG > 1 && lane == 0) {
-            // The odd CTA of a pair relays each round: once its own decoders have arrived,
-            // one arrival (release at cluster scope) on the even CTA's barrier.
-            const int nr = (nk + RS - 1) / RS;
-            const uint32_t peer_afull = mapa_shared(afull_bar(0), crank ^ 1u);
-            for (int r = 0; r < nr; ++r) {
-                const int rb = r % NRB;
-                if (!mbar_wait_spin(afull_bar(rb), (uint32_t)((r / NRB) & 1), p.wait_ns, abort_flag)) {
-                    give_up();
-                    break;
-                }
-                mbar_arrive_remote(peer_afull + 8u * (uint32_t)rb);
-            }
         }
         __syncwarp();
     } else {
@@ -476,6 +464,12 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
         const bool row_ok = GU == 1 ? (int64_t)m0 + (r & (BM / 2 - 1)) < p.N : n < p.N;
         const uint32_t xr = (uint32_t)(r & 7);
         const uint32_t t_lane = (uint32_t)(32 * q4w) << 16;
+        // a decoded round is announced on the pair's even CTA (its own barrier there)
+        const uint32_t afull0 = (CG > 1 && !leader) ? mapa_shared(afull_bar(0), crank ^ 1u) : afull_bar(0);
+        auto announce = [&](int rb) {
+            if (CG > 1 && !leader) mbar_arrive_remote(afull0 + 8u * (uint32_t)rb);
+            else mbar_arrive(afull0 + 8u * (uint32_t)rb);
+        };
         // weight rows of G * ROW bytes: 128-byte swizzle (chunk c at c ^ (r % 8)), 64-byte
         // swizzle (chunk c at c ^ ((r / 2) % 4)) or 32-byte swizzle (chunk c at c ^ ((r / 4) % 2))
         const uint32_t wsw = L::WROW == 128 ? (uint32_t)(r & 7)
@@ -536,16 +530,6 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             uint32_t sc_next = 0, mo_next = 0;
             if (FMT != 1 && row_ok && kb + 8 < nk) sc_next = scale_pair(kb + 8);
             if (aff && row_ok && kb + 8 < nk) mo_next = offset_pair(kb + 8);
-            // the slot's previous round (NRB back) must have been consumed
-            const int rp = kb / RS - NRB;
-            const bool freed = MERGE ? (rp < 0 || mbar_wait_spin(empty_bar(rp % LSS), (uint32_t)((rp / LSS) & 1), p.wait_ns, abort_flag))
-                                     : mbar_wait_spin(aempty_bar(rb), rph ^ 1u, p.wait_ns, abort_flag);
-            if (!freed) {
-                give_up();
-                stop = true;
-                break;
-            }
-            tc_fence_after();   // the slot's earlier MMAs (committed by this or the pair's CTA) are done
             const uint32_t wrow = slot_base(s) + (uint32_t)(L::X_BYTES + r * L::WROW);
             // this thread's 64 decoded values (the whole stage for row r), two per word
             uint32_t o[32];
@@ -601,6 +585,18 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                     }
                 }
             }
+            // Only the store waits for the decoded slot: the slot's previous round (NRB back)
+            // must have been consumed.  The loads and the decode above read the super-slot,
+            // which stays full until this stage's MMAs are done, so they run ahead of it.
+            const int rp = kb / RS - NRB;
+            const bool freed = MERGE ? (rp < 0 || mbar_wait_spin(empty_bar(rp % LSS), (uint32_t)((rp / LSS) & 1), p.wait_ns, abort_flag))
+                                     : mbar_wait_spin(aempty_bar(rb), rph ^ 1u, p.wait_ns, abort_flag);
+            if (!freed) {
+                give_up();
+                stop = true;
+                break;
+            }
+            tc_fence_after();   // the slot's earlier MMAs (committed by this or the pair's CTA) are done
             if (AM == 0) {
                 // shared-memory A tile, 128-byte swizzled K-major: the 8 chunks of row r
                 const uint32_t adst = sb + L::A_OFF + a * A_BYTES + (uint32_t)(r * 128);
@@ -615,7 +611,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                 tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(rb));
+            if (lane == 0) announce(rb);
             sc0 = sc1;
             sc1 = sc_next;
             mo0 = mo1;
@@ -639,7 +635,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                 break;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(rb));
+            if (lane == 0) announce(rb);
         }
 
         // Output scales of the epilogue (Q4: the guard inverse of each token this thread's

@@ -9,8 +9,7 @@ namespace cq {
 cudaError_t launch_tc_q4_gateup(const TcArgs& a, cudaStream_t s) {
     // a.N is I (gate rows); a row tile is 64 gate rows and their 64 up rows
     const int64_t mt = (a.N + BM / 2 - 1) / (BM / 2);
-    Plan pl = plan_tiles(a, mt, true);
-    if (pl.bn == 256 && options().tc_pair != 2) pl.pair_ok = false;   // as for the dense Q4 GEMM
+    const Plan pl = plan_tiles(a, mt, true);
     Params p = make_params(a);
     p.y_tma = 0;    // a[T][I] f32 leaves by direct stores after the SwiGLU
     p.tiles_y = (int)((a.T + pl.bn - 1) / pl.bn);

@@ -12,8 +12,7 @@ namespace cq {
 cudaError_t launch_tc_q4a(const TcArgs& a, cudaStream_t s) {
     if (!a.off || a.gk < 1 || a.jobs() != 1) return cudaErrorInvalidValue;
     const int64_t mt = (a.N + BM - 1) / BM;
-    Plan pl = plan_tiles(a, mt, false);
-    if (pl.bn == 256 && options().tc_pair != 2) pl.pair_ok = false;   // as for the plain Q4 GEMM
+    const Plan pl = plan_tiles(a, mt, false);
     Params p = make_params(a);
     p.tiles_y = (int)((a.T + pl.bn - 1) / pl.bn);
     dim3 grid((unsigned)mt, (unsigned)p.tiles_y, (unsigned)pl.ks);

@@ -333,8 +333,8 @@ typedef enum {
                                 (affine Q4 and the gate/up GEMM: tensor memory always) */
     CQ_OPT_TC_PAIR = 8,      /* tcgen05 CTA pairs (neighbouring weight-row tiles share one 256-row MMA, each
                                 CTA loading half of the activation tile; decoded weights in tensor memory, an
-                                even number of row tiles): 2 on, 1 off, 0 auto (on, except Q4 256-column
-                                tiles, which measured faster unpaired) */
+                                even number of row tiles): 2 on, 1 off, 0 auto (on wherever the row tiles
+                                pair up) */
     CQ_OPT_STREAM_KERNEL = 9 /* weight-streaming kernel: 2 the row-partitioned kernel (one CTA per SM, each
                                 streaming the whole K of an equal share of the weight rows) wherever it serves
                                 (one job, K % 512 == 0, T <= 32; Q8/32: T <= 16), 1 the K-split cluster
