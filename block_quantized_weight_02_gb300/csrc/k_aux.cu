@@ -465,26 +465,28 @@ __global__ void __launch_bounds__(256) k_group_sums(const T* __restrict__ x, int
 }
 
 // add[t][n] = sum_g m[n][g] * xs[t][g] (g in order, one fused multiply-add each): a
-// CTA of 256 threads takes 128 rows n and 32 tokens t, the offsets and group sums
+// CTA of 256 threads takes 32 RI rows n and 32 tokens t, the offsets and group sums
 // staged through shared memory 32 groups at a time with coalesced loads; thread
-// (tx, ty) computes rows tx + 32 i and tokens ty + 8 j (i, j < 4).
+// (tx, ty) computes rows tx + 32 i (i < RI) and tokens ty + 8 j (j < 4).  RI = 1
+// where there are few tokens, so that the rows alone spread over enough CTAs.
+template <int RI>
 __global__ void __launch_bounds__(256) k_offset_term(const uint16_t* __restrict__ off, const float* __restrict__ xs,
                                                      int64_t Tn, int64_t N, int G, float* __restrict__ add) {
     pdl_launch_dependents();
     pdl_wait();
     __shared__ float sm[32][129];   // [g][row]
     __shared__ float sx[32][33];    // [token][g]
-    const int64_t n0 = (int64_t)blockIdx.x * 128, t0 = (int64_t)blockIdx.y * 32;
+    const int64_t n0 = (int64_t)blockIdx.x * (32 * RI), t0 = (int64_t)blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    float acc[4][4];
+    float acc[RI][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < RI; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     for (int g0 = 0; g0 < G; g0 += 32) {
         const int ng = G - g0 < 32 ? G - g0 : 32;
         // offsets: row r = e / 32, group e % 32 (a warp reads 32 consecutive groups of one row)
-        for (int e = threadIdx.x; e < 128 * 32; e += 256) {
+        for (int e = threadIdx.x; e < 32 * RI * 32; e += 256) {
             const int r = e >> 5, gg = e & 31;
             const int64_t n = n0 + r;
             sm[gg][r] = (gg < ng && n < N) ? __uint_as_float((uint32_t)off[n * G + g0 + gg] << 16) : 0.f;
@@ -495,13 +497,13 @@ __global__ void __launch_bounds__(256) k_offset_term(const uint16_t* __restrict_
         }
         __syncthreads();
         for (int gg = 0; gg < ng; ++gg) {
-            float m[4], x[4];
+            float m[RI], x[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) m[i] = sm[gg][tx + 32 * i];
+            for (int i = 0; i < RI; ++i) m[i] = sm[gg][tx + 32 * i];
 #pragma unroll
             for (int j = 0; j < 4; ++j) x[j] = sx[ty + 8 * j][gg];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < RI; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(m[i], x[j], acc[i][j]);
         }
@@ -512,7 +514,7 @@ __global__ void __launch_bounds__(256) k_offset_term(const uint16_t* __restrict_
         const int64_t t = t0 + ty + 8 * j;
         if (t >= Tn) continue;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < RI; ++i) {
             const int64_t n = n0 + tx + 32 * i;
             if (n < N) add[t * N + n] = acc[i][j];
         }
@@ -528,7 +530,10 @@ cudaError_t launch_offset_term(const void* x, int xt, int64_t T, int64_t K, cons
                      T, K, gk, xs)
         : launch_pdl(k_group_sums<__half>, dim3(gs), dim3(256), 0, s, reinterpret_cast<const __half*>(x), T, K, gk, xs);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k_offset_term, dim3((unsigned)((N + 127) / 128), (unsigned)((T + 31) / 32)), dim3(256), 0, s, off,
+    if (T <= 32)
+        return launch_pdl(k_offset_term<1>, dim3((unsigned)((N + 31) / 32), 1u), dim3(256), 0, s, off, (const float*)xs, T,
+                          N, (int)G, add);
+    return launch_pdl(k_offset_term<4>, dim3((unsigned)((N + 127) / 128), (unsigned)((T + 31) / 32)), dim3(256), 0, s, off,
                       (const float*)xs, T, N, (int)G, add);
 }
 
