@@ -709,7 +709,9 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             }
             cluster_arrive_release();
         } else if (CG > 1) {
-            cluster_arrive_release();   // neither CTA of a pair leaves while the other may still use it
+            // neither CTA of a pair leaves before the other is done; every MMA of the pair has
+            // finished (the accumulator barrier), so nothing of one is read by the other any more
+            cluster_arrive_relaxed();
         }
         if (dec && grp < NG) {
             const int64_t n = (int64_t)m0 + r;
@@ -720,12 +722,17 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
             // the addend (affine offset term) only where a format uses it: its loads stay out of
             // the loop that stages the outputs
             const float* addp = (FMT != 1 && GU != 1 && row_ok) ? J.add : nullptr;
-#pragma unroll 1
+            // every column of the group out of tensor memory at once, one wait
+            uint32_t vall[CW];
+#pragma unroll
+            for (int ci = 0; ci < CW / CH; ++ci)
+                tmem_ld_cols<CH>(tmem + t_lane + (uint32_t)(cbase + grp * CW + ci * CH),
+                                 *reinterpret_cast<uint32_t(*)[CH]>(&vall[ci * CH]));
+            tmem_ld_wait();
+#pragma unroll
             for (int ci = 0; ci < CW / CH; ++ci) {
                 const int cc = grp * CW + ci * CH;
-                uint32_t v[CH];
-                tmem_ld_cols<CH>(tmem + t_lane + (uint32_t)(cbase + cc), v);
-                tmem_ld_wait();
+                const uint32_t* v = &vall[ci * CH];
                 const int64_t tb = (int64_t)t0 + cbase + cc;
                 const bool skip = *abort_flag != 0;
                 float vals[CH];
