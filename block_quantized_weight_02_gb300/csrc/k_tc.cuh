@@ -302,7 +302,12 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
     }
     tc_fence_before();
     __syncthreads();
-    if (CG > 1) cluster_sync_all();   // the peer's barriers and tensor memory exist before any use
+    // the peer's barriers and tensor memory exist before any use (the barriers' initialisation
+    // was released at cluster scope by its own fence, so the arrival itself need not release)
+    if (CG > 1) {
+        cluster_arrive_relaxed();
+        cluster_wait_acquire();
+    }
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
