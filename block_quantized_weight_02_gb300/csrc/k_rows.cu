@@ -256,6 +256,19 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
     pdl_wait();   // outputs (and the previous kernel's readers of them) only after the previous kernel
     constexpr int NT = TP / 8;                             // n8 tiles of activation rows
     const int tile = warp % TILES, part = warp / TILES;    // m16 tile of the pass, quarter of the blocks
+    // This thread's offsets from a ring slot's base, the same in every stage (Q4): the weight word
+    // of each of its blocks (row g; row g + 8 is 1024 bytes on) and the two 8-byte activation runs
+    // of token g of the first n8 tile (the others 1024 bytes apart)
+    uint32_t woff[G::BPW], xoff[G::BPW][2];
+#pragma unroll
+    for (int jh = 0; jh < G::BPW; ++jh) {
+        const int jb = part * G::BPW + jh;
+        woff[jh] = (uint32_t)((16 * tile + g) * 128 + 4 * c + (jb >> 3) * G::WBOX) + ((((uint32_t)(jb & 7)) ^ (uint32_t)g) << 4);
+        const uint32_t clo = (uint32_t)(4 * (jb & 1) + (c >> 1));
+        const uint32_t xr = (uint32_t)L::X_OFF + ((uint32_t)(jb >> 1) * TP + (uint32_t)g) * 128u + 8u * (uint32_t)(c & 1);
+        xoff[jh][0] = xr + ((clo ^ (uint32_t)g) << 4);
+        xoff[jh][1] = xr + (((clo + 2u) ^ (uint32_t)g) << 4);
+    }
     int gi = 0;
     for (int pass = 0; pass < npass; ++pass) {
         const int ub = u0 + pass * upp, nu = min(upp, u1 - ub);
@@ -273,7 +286,7 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
         bool ok = !*abort_flag;
         for (int i = 0; i < nst; ++i, ++gi) {
             const int slot = gi % NSLOT;
-            if (ok && !mbar_wait(full_bar(slot), (uint32_t)((gi / NSLOT) & 1), p.wait_ns, abort_flag)) {
+            if (ok && !mbar_wait_spin(full_bar(slot), (uint32_t)((gi / NSLOT) & 1), p.wait_ns, abort_flag)) {
                 ok = false;
                 *abort_flag = 1;
                 atomicCAS(p.err, 0, DEV_TIMEOUT);
@@ -312,7 +325,7 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
                     const uint32_t xr = sX + (slab * TP + (uint32_t)g) * 128u + off8;
                     uint32_t a1[4], a2[4];
                     if (FMT == 0) {
-                        const uint32_t wa = wrow + (uint32_t)((jb >> 3) * G::WBOX) + ((((uint32_t)(jb & 7)) ^ (uint32_t)g) << 4);
+                        const uint32_t wa = sW + woff[jh];
                         uint32_t dl[4], dh[4];
                         q4_adjacent<XBF>(r_lds32(wa), dl);
                         q4_adjacent<XBF>(r_lds32(wa + 1024u), dh);
@@ -331,8 +344,8 @@ k_rows(const __grid_constant__ RMaps maps, const RParams p) {
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {   // tokens 8 nt + g
-                        const uint2 xlo = r_lds64(xr + 1024u * nt + ((clo ^ (uint32_t)g) << 4));
-                        const uint2 xhi = r_lds64(xr + 1024u * nt + (((clo + 2u) ^ (uint32_t)g) << 4));
+                        const uint2 xlo = r_lds64(FMT == 0 ? sW + xoff[jh][0] + 1024u * nt : xr + 1024u * nt + ((clo ^ (uint32_t)g) << 4));
+                        const uint2 xhi = r_lds64(FMT == 0 ? sW + xoff[jh][1] + 1024u * nt : xr + 1024u * nt + (((clo + 2u) ^ (uint32_t)g) << 4));
                         if (FMT == 1) {
                             mma_f<XBF>(acc[nt], a1, xlo.x, xlo.y);
                             mma_f<XBF>(acc[nt], a2, xhi.x, xhi.y);
