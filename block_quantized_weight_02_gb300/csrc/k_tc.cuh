@@ -690,7 +690,10 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
         const int gbar = 2 + grp;                    // the group's named barrier (1 is all decoders)
         if (KS > 1) {
             const uint32_t partner = crank ^ (uint32_t)CG;
-            cluster_sync_all();
+            // both CTAs past their last MMAs (each waited for its accumulator barrier), so their
+            // rings are idle: arrivals without release, the exchange itself completes on mbarriers
+            cluster_arrive_relaxed();
+            cluster_wait_acquire();
             // each group receives the partner's values of its own CW columns
             if (dec && grp < NG && lead) mbar_arrive_expect_tx(xchg_bar(grp), (uint32_t)(CW * 128 * 4));
             if (dec && grp < NG) {
@@ -712,7 +715,7 @@ k_tc(const __grid_constant__ Maps maps, const Params p) {
                 }
                 if (!*abort_flag && !mbar_wait(xchg_bar(grp), 0, p.wait_ns, abort_flag)) give_up();
             }
-            cluster_arrive_release();
+            cluster_arrive_relaxed();
         } else if (CG > 1) {
             // neither CTA of a pair leaves before the other is done; every MMA of the pair has
             // finished (the accumulator barrier), so nothing of one is read by the other any more
